@@ -1,0 +1,173 @@
+"""fp64 CPU parity oracle for the speculative-decoding verification step.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / reference leg are the only callers.  The
+product library never imports this package, and this package imports
+nothing from the product.
+
+The arithmetic lives in ``spec_oracle.c`` (plain C, fp64, optional OpenMP
+over independent units); this module compiles it with gcc on first use and
+wraps it for numpy arrays.  Every function cites the page passage it
+follows in the C source.
+
+Parity status of each function (what pins it, in tests/test_oracle_*.py):
+  verify_attention  brute force vs torch's fp64 scaled-dot-product attention
+                    with a materialised mask; D=0 equals decode attention;
+                    row i equals D=0 over the prefix L-D+i; paged equals
+                    contiguous; one-hot and constant-key closed forms.
+  gemm              numpy fp64 matmul (library routine).
+  accept_greedy     brute force over all drafts of a toy target model:
+                    emitted tokens equal plain greedy decoding.
+  accept_sample     exact enumeration on a toy model (emitted sequence law
+                    equals the target's), tau closed form, chi-square.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force=False):
+    """Compile liboracle.so with gcc (OpenMP when available)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-lm", "-o", _LIB + ".tmp"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.oracle_verify_attention.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                                    i32, f64, i64, i32, P, P, P, i32]
+            lib.oracle_gemm.argtypes = [P, P, i32, i32, i32, i32, P, P, i32]
+            lib.oracle_accept_greedy.argtypes = [P, P, i32, i32, i32, P, P, i32]
+            lib.oracle_accept_sample.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, P, P, i32]
+            for f in ("oracle_verify_attention", "oracle_gemm", "oracle_accept_greedy",
+                      "oracle_accept_sample", "oracle_max_threads"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def max_threads():
+    return _load().oracle_max_threads()
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def verify_attention(q, k_pages, v_pages, block_table, kv_len, D, Hkv, G, head_dim,
+                     page_size, softmax_scale=None, rows=None, threads=0):
+    """fp64 verify attention.
+
+    q: uint16 bf16 bits [B, 1+D, Hkv*G, d]; k_pages/v_pages: uint16
+    [P, page, Hkv, d]; block_table int32 [B, max_pages]; kv_len int32 [B].
+    rows: optional int array [n, 4] of (b, i, h, g).  Returns (out, lse):
+    full shapes [B, 1+D, Hq, d] / [B, 1+D, Hq], or [n, d] / [n].
+    """
+    lib = _load()
+    q, k_pages, v_pages = (_c(a, np.uint16) for a in (q, k_pages, v_pages))
+    block_table = _c(block_table, np.int32)
+    kv_len = _c(kv_len, np.int32)
+    B = kv_len.shape[0]
+    Hq = Hkv * G
+    if softmax_scale is None:
+        softmax_scale = 1.0 / np.sqrt(head_dim)
+    P = k_pages.shape[0]
+    if rows is not None:
+        rows = _c(rows, np.int32).reshape(-1, 4)
+        n = rows.shape[0]
+        out = np.empty((n, head_dim), dtype=np.float64)
+        lse = np.empty((n,), dtype=np.float64)
+    else:
+        n = 0
+        out = np.empty((B, 1 + D, Hq, head_dim), dtype=np.float64)
+        lse = np.empty((B, 1 + D, Hq), dtype=np.float64)
+    rc = lib.oracle_verify_attention(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                     block_table.shape[1], _ptr(kv_len), B, D, Hkv, G, head_dim,
+                                     page_size, float(softmax_scale), P, n, _ptr(rows), _ptr(out),
+                                     _ptr(lse), int(threads))
+    if rc:
+        raise ValueError(f"oracle_verify_attention failed: {rc}")
+    return out, lse
+
+
+def gemm(x, w, samples=None, threads=0):
+    """fp64 y = x @ w.T for bf16 bits x [M, K], w [N, K]; samples [n, 2]."""
+    lib = _load()
+    x, w = _c(x, np.uint16), _c(w, np.uint16)
+    M, K = x.shape
+    N = w.shape[0]
+    if samples is not None:
+        samples = _c(samples, np.int32).reshape(-1, 2)
+        y = np.empty((samples.shape[0],), dtype=np.float64)
+        n = samples.shape[0]
+    else:
+        y = np.empty((M, N), dtype=np.float64)
+        n = 0
+    rc = lib.oracle_gemm(_ptr(x), _ptr(w), M, N, K, n, _ptr(samples), _ptr(y), int(threads))
+    if rc:
+        raise ValueError(f"oracle_gemm failed: {rc}")
+    return y
+
+
+def accept_greedy(p, draft, threads=0):
+    """Greedy prefix acceptance: returns (n_accepted [B], token [B]) int32."""
+    lib = _load()
+    p = _c(p, np.float32)
+    draft = _c(draft, np.int32)
+    B, D1, V = p.shape
+    D = D1 - 1
+    n_acc = np.empty((B,), np.int32)
+    tok = np.empty((B,), np.int32)
+    rc = lib.oracle_accept_greedy(_ptr(p), _ptr(draft), B, D, V, _ptr(n_acc), _ptr(tok),
+                                  int(threads))
+    if rc:
+        raise ValueError(f"oracle_accept_greedy failed: {rc}")
+    return n_acc, tok
+
+
+def accept_sample(p, q, draft, u_acc, u_res, threads=0):
+    """Stochastic acceptance: returns (n_accepted, token, margin, fallback)."""
+    lib = _load()
+    p, q = _c(p, np.float32), _c(q, np.float32)
+    draft = _c(draft, np.int32)
+    u_acc, u_res = _c(u_acc, np.float32), _c(u_res, np.float32)
+    B, D1, V = p.shape
+    D = D1 - 1
+    n_acc = np.empty((B,), np.int32)
+    tok = np.empty((B,), np.int32)
+    margin = np.empty((B,), np.float64)
+    fb = np.empty((B,), np.int32)
+    rc = lib.oracle_accept_sample(_ptr(p), _ptr(q), _ptr(draft), _ptr(u_acc), _ptr(u_res),
+                                  B, D, V, _ptr(n_acc), _ptr(tok), _ptr(margin), _ptr(fb),
+                                  int(threads))
+    if rc:
+        raise ValueError(f"oracle_accept_sample failed: {rc}")
+    return n_acc, tok, margin, fb

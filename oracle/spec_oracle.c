@@ -1,0 +1,315 @@
+/*
+ * Parity oracle for the speculative-decoding verification step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is a plain, slow, fp64 CPU statement of
+ * what the verification step computes.  It shares no code with the CUDA
+ * library; only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg may load it.  The product path never calls it.
+ *
+ * Sources (web pages on speculative decoding):
+ *  - "Co-Designing AI Models Using Speculative Decoding for Faster LLM
+ *    Inference" (NVIDIA Technical Blog; Chinese translation), sections
+ *    "What is speculative decoding" (AL in [1, 1+D]), "Draft length and
+ *    performance of linear layers" (GEMM-M grows from M to M(1+D)) and
+ *    "Draft length and attention performance" (drafts reuse the KV cache,
+ *    attention GEMM-M = G(1+D)).
+ *  - "How does speculative decoding speed up LLM inference?" (llm-digest),
+ *    sections "Mechanism" and "Math intuition": accept x with probability
+ *    min(1, p(x)/q(x)); at the first rejection resample from
+ *    max(0, p - q) renormalised.
+ *  - LLM inference handbook, "Speculative decoding", section "How
+ *    speculative decoding works": accept the longest agreeing prefix, then
+ *    emit one more token from the target.
+ *
+ * Readings where the pages are silent (each restated where it is used):
+ *  R1 kv_len[b] counts the 1+D verify tokens; query row i sees keys
+ *     j < kv_len[b] - D + i (drafts see the prefix, earlier drafts and
+ *     themselves).  D = 0 is plain decode over kv_len[b] keys.
+ *  R2 softmax scale is a caller argument (1/sqrt(head_dim) by default).
+ *  R3 accept test is strict u * q(x) < p(x), evaluated exactly.
+ *  R4 residual/bonus draw: smallest v (ascending id) with C(v) > u * Z where
+ *     C is the running sum and Z the total.
+ *  R5 if Z <= 0 after a rejection, draw from p of that row instead.
+ *  R6 greedy ties resolve to the lowest index.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double bf16_to_f64(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static void set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------
+ * Verify attention, one query row.
+ *
+ * Row (b, i, h, g): query head hq = h*G + g, draft position i in [0, D].
+ * Visible keys j in [0, kv_len[b] - D + i) (reading R1).  With fp64 scores
+ * s_j = scale * sum_c q_c K_jc, m = max_j s_j, w_j = exp(s_j - m):
+ *   o = sum_j w_j V_j / sum_j w_j,   lse = m + ln(sum_j w_j).
+ * Key j of sequence b lives in page block_table[b][j / page_size] at slot
+ * j % page_size.  Returns 0, or -1 if a page id is outside [0, num_pages).
+ * ---------------------------------------------------------------------- */
+static int attention_row(const uint16_t *q, const uint16_t *kp, const uint16_t *vp,
+                         const int32_t *block_table, int max_pages, const int32_t *kv_len,
+                         int D, int Hkv, int G, int d, int page_size, double scale,
+                         int64_t num_pages, int b, int i, int h, int g,
+                         double *out, double *lse, double *scratch)
+{
+    const int Hq = Hkv * G;
+    const uint16_t *qrow = q + (((int64_t)b * (1 + D) + i) * Hq + (int64_t)h * G + g) * d;
+    const int64_t n_keys = (int64_t)kv_len[b] - D + i;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n_keys; ++j) {
+        int32_t page = block_table[(int64_t)b * max_pages + j / page_size];
+        if (page < 0 || page >= num_pages) return -1;
+        const uint16_t *krow = kp + (((int64_t)page * page_size + j % page_size) * Hkv + h) * d;
+        double s = 0.0;
+        for (int c = 0; c < d; ++c) s += bf16_to_f64(qrow[c]) * bf16_to_f64(krow[c]);
+        s *= scale;
+        scratch[j] = s;
+        if (s > m) m = s;
+    }
+    double l = 0.0;
+    for (int c = 0; c < d; ++c) out[c] = 0.0;
+    for (int64_t j = 0; j < n_keys; ++j) {
+        int32_t page = block_table[(int64_t)b * max_pages + j / page_size];
+        const uint16_t *vrow = vp + (((int64_t)page * page_size + j % page_size) * Hkv + h) * d;
+        double w = exp(scratch[j] - m);
+        l += w;
+        for (int c = 0; c < d; ++c) out[c] += w * bf16_to_f64(vrow[c]);
+    }
+    for (int c = 0; c < d; ++c) out[c] /= l;
+    if (lse) *lse = m + log(l);
+    return 0;
+}
+
+/* rows == NULL: every row, out laid out [B][1+D][Hq][d], lse [B][1+D][Hq].
+ * rows != NULL: n_rows entries (b, i, h, g); out [n_rows][d], lse [n_rows]. */
+int oracle_verify_attention(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                            const int32_t *block_table, int max_pages_per_seq,
+                            const int32_t *kv_len, int B, int D, int Hkv, int G,
+                            int head_dim, int page_size, double softmax_scale,
+                            int64_t num_pages, int n_rows, const int32_t *rows,
+                            double *out, double *lse, int num_threads)
+{
+    if (B < 0 || D < 0 || Hkv < 1 || G < 1 || head_dim < 1 || page_size < 1) return -2;
+    for (int b = 0; b < B; ++b)
+        if (kv_len[b] < 1 + D || (int64_t)kv_len[b] > (int64_t)max_pages_per_seq * page_size)
+            return -3;
+    const int Hq = Hkv * G;
+    const int64_t total = rows ? (int64_t)n_rows : (int64_t)B * (1 + D) * Hq;
+    int64_t max_len = 1;
+    for (int b = 0; b < B; ++b) if (kv_len[b] > max_len) max_len = kv_len[b];
+    int err = 0;
+    set_threads(num_threads);
+#pragma omp parallel
+    {
+        double *scratch = (double *)malloc(sizeof(double) * (size_t)max_len);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < total; ++r) {
+            int b, i, h, g;
+            if (rows) {
+                b = rows[4 * r]; i = rows[4 * r + 1]; h = rows[4 * r + 2]; g = rows[4 * r + 3];
+            } else {
+                int64_t t = r;
+                g = (int)(t % G); t /= G;
+                h = (int)(t % Hkv); t /= Hkv;
+                i = (int)(t % (1 + D)); t /= (1 + D);
+                b = (int)t;
+            }
+            int rc = attention_row(q, k_pages, v_pages, block_table, max_pages_per_seq, kv_len,
+                                   D, Hkv, G, head_dim, page_size, softmax_scale, num_pages,
+                                   b, i, h, g, out + r * head_dim, lse ? lse + r : NULL, scratch);
+            if (rc) {
+#pragma omp atomic write
+                err = rc;
+            }
+        }
+        free(scratch);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------
+ * Verify GEMM: y[m][n] = sum_k x[m][k] * w[n][k] in fp64, x [M][K] and
+ * w [N][K] bf16 (both K-contiguous).  GEMM-M = B(1+D) is the batch of
+ * verified tokens.  samples == NULL: full y [M][N]; else y[s] for the n
+ * pairs (m, n) in samples.
+ * ---------------------------------------------------------------------- */
+int oracle_gemm(const uint16_t *x, const uint16_t *w, int M, int N, int K,
+                int n_samples, const int32_t *samples, double *y, int num_threads)
+{
+    if (M < 0 || N < 0 || K < 0) return -2;
+    const int64_t total = samples ? (int64_t)n_samples : (int64_t)M * N;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(static)
+    for (int64_t s = 0; s < total; ++s) {
+        int m, n;
+        if (samples) { m = samples[2 * s]; n = samples[2 * s + 1]; }
+        else { m = (int)(s / N); n = (int)(s % N); }
+        const uint16_t *xr = x + (int64_t)m * K;
+        const uint16_t *wr = w + (int64_t)n * K;
+        double acc = 0.0;
+        for (int k = 0; k < K; ++k) acc += bf16_to_f64(xr[k]) * bf16_to_f64(wr[k]);
+        y[s] = acc;
+    }
+    return 0;
+}
+
+/* Lowest index of the maximum of row[0..V) (reading R6). */
+static int argmax_row(const float *row, int V)
+{
+    int best = 0;
+    double bv = (double)row[0];
+    for (int v = 1; v < V; ++v) {
+        double x = (double)row[v];
+        if (x > bv) { bv = x; best = v; }
+    }
+    return best;
+}
+
+/* ------------------------------------------------------------------------
+ * Greedy acceptance.  Target token t_i = argmax_v p[b][i][v].  Drafts are
+ * accepted in order until the first i with draft[b][i] != t_i; n_acc = that
+ * i (or D if all match); the emitted extra token is t_{n_acc}.  Accepted
+ * length AL = n_acc + 1 lies in [1, 1+D].
+ * ---------------------------------------------------------------------- */
+int oracle_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,
+                         int32_t *n_accepted, int32_t *token, int num_threads)
+{
+    if (B < 0 || D < 0 || V < 1) return -2;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const float *pb = p + (int64_t)b * (1 + D) * V;
+        int n = D;
+        for (int i = 0; i < D; ++i) {
+            if (draft[(int64_t)b * D + i] != argmax_row(pb + (int64_t)i * V, V)) { n = i; break; }
+        }
+        n_accepted[b] = n;
+        token[b] = argmax_row(pb + (int64_t)n * V, V);
+    }
+    return 0;
+}
+
+/* Draw from weights r (computed on the fly): smallest v with C(v) > u * Z,
+ * C the ascending running sum, Z = C(V-1) (reading R4).  Also returns the
+ * boundary margin min_v |u*Z - C(v)| / Z.  kind 0: r = p; kind 1:
+ * r = max(0, p - q).  Returns -1 if Z <= 0. */
+static int draw_residual(const float *p, const float *q, int V, int kind, double u,
+                         double *margin)
+{
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v) {
+        double r = kind ? fmax(0.0, (double)p[v] - (double)q[v]) : (double)p[v];
+        Z += r;
+    }
+    if (!(Z > 0.0)) return -1;
+    const double T = u * Z;
+    double C = 0.0, mg = INFINITY;
+    int pick = -1;
+    for (int v = 0; v < V; ++v) {
+        double r = kind ? fmax(0.0, (double)p[v] - (double)q[v]) : (double)p[v];
+        C += r;
+        double gap = fabs(T - C);
+        if (gap < mg) mg = gap;
+        if (pick < 0 && C > T) pick = v;
+    }
+    if (pick < 0) { /* rounding left T >= Z: take the last token with mass */
+        for (int v = V - 1; v >= 0; --v) {
+            double r = kind ? fmax(0.0, (double)p[v] - (double)q[v]) : (double)p[v];
+            if (r > 0.0) { pick = v; break; }
+        }
+    }
+    if (margin) *margin = mg / Z;
+    return pick;
+}
+
+/* ------------------------------------------------------------------------
+ * Stochastic acceptance (modified rejection sampling).  For i = 0..D-1 with
+ * x = draft[b][i]: accept iff u_acc[b][i] * q[b][i][x] < p[b][i][x] (reading
+ * R3; the fp32 inputs make the fp64 product exact).  At the first
+ * rejection j, emit a draw from max(0, p[b][j] - q[b][j]) renormalised with
+ * uniform u_res[b]; if none is rejected, emit a draw from p[b][D] (the bonus
+ * token).  n_acc = j (or D).  Outputs per sequence: n_accepted, token, the
+ * boundary margin (min over the accept tests of |u - p/q| and over the draw
+ * of the CDF gap / Z) and a flag set when reading R5's fallback was taken.
+ * ---------------------------------------------------------------------- */
+int oracle_accept_sample(const float *p, const float *q, const int32_t *draft,
+                         const float *u_acc, const float *u_res, int B, int D, int V,
+                         int32_t *n_accepted, int32_t *token, double *margin,
+                         int32_t *fallback, int num_threads)
+{
+    if (B < 0 || D < 0 || V < 1) return -2;
+    int err = 0;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const float *pb = p + (int64_t)b * (1 + D) * V;
+        const float *qb = q + (int64_t)b * D * V;
+        double mg = INFINITY;
+        int j = D;
+        for (int i = 0; i < D; ++i) {
+            int x = draft[(int64_t)b * D + i];
+            if (x < 0 || x >= V) {
+#pragma omp atomic write
+                err = -4;
+                x = 0;
+            }
+            double px = (double)pb[(int64_t)i * V + x];
+            double qx = (double)qb[(int64_t)i * V + x];
+            double u = (double)u_acc[(int64_t)b * D + i];
+            if (qx > 0.0) {
+                double gap = fabs(u - px / qx);
+                if (gap < mg) mg = gap;
+            }
+            if (!(u * qx < px)) { j = i; break; }
+        }
+        int fb = 0, tok;
+        double dm = INFINITY;
+        if (j < D) {
+            tok = draw_residual(pb + (int64_t)j * V, qb + (int64_t)j * V, V, 1,
+                                (double)u_res[b], &dm);
+            if (tok < 0) {
+                fb = 1;
+                tok = draw_residual(pb + (int64_t)j * V, NULL, V, 0, (double)u_res[b], &dm);
+            }
+        } else {
+            tok = draw_residual(pb + (int64_t)D * V, NULL, V, 0, (double)u_res[b], &dm);
+        }
+        if (tok < 0) { tok = 0; }
+        if (dm < mg) mg = dm;
+        n_accepted[b] = j;
+        token[b] = tok;
+        if (margin) margin[b] = mg;
+        if (fallback) fallback[b] = fb;
+    }
+    return err;
+}
