@@ -1,0 +1,214 @@
+/*
+ * spec_verify.h -- C ABI of the speculative-decoding verification step on
+ * one GB300 (sm_103a) GPU.
+ *
+ * The verification step runs the target model once over B x (1 + D)
+ * tokens: for every sequence, the last accepted token plus D draft tokens
+ * ("What is speculative decoding", co-design blog).  This library provides
+ * the three data-parallel parts of that step:
+ *
+ *   spec_verify_attention  GQA attention of the B(1+D) query tokens over a
+ *                          paged bf16 KV cache, causal among the drafts.
+ *   spec_verify_gemm       a linear layer of the verify pass, GEMM-M = B(1+D).
+ *   spec_accept_greedy     greedy longest-prefix acceptance.
+ *   spec_accept_sample     stochastic min(1, p/q) acceptance with residual
+ *                          resampling.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *    the library never frees or retains them and allocates no device memory.
+ *    Scratch space is the caller's `workspace` (size from the matching
+ *    *_workspace_size call).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously; the call returns once it is enqueued.
+ *  - Arguments are validated on the host before anything is enqueued; an
+ *    invalid call returns an error status and launches nothing.
+ *  - Conditions only the device can see (a page id outside the pool, a
+ *    kv_len outside its range, a token id outside [0, V), a uniform outside
+ *    [0, 1), a bounded wait that expired) are OR-ed into *dev_status when
+ *    dev_status is non-NULL (a device uint32_t the caller zeroes and reads
+ *    after synchronising).  Kernels never trap.
+ *  - All entry points are thread-safe; calls on one stream execute in order.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1,   /* NULL/misaligned pointer, negative size, ... */
+    SPEC_ERR_UNSUPPORTED = 2,   /* valid but outside the supported set        */
+    SPEC_ERR_WORKSPACE = 3,     /* workspace missing or too small             */
+    SPEC_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed          */
+    SPEC_ERR_TIMEOUT = 5        /* reserved: bounded device wait expired      */
+} spec_status_t;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define SPEC_DEV_ERR_PAGE_ID     0x00000001u /* block_table entry outside [0, num_pages) */
+#define SPEC_DEV_ERR_KV_LEN      0x00000002u /* kv_len[b] < 1+D or > max_pages*page_size */
+#define SPEC_DEV_ERR_TIMEOUT     0x00000004u /* a bounded mbarrier wait expired          */
+#define SPEC_DEV_ERR_TOKEN_ID    0x00000008u /* draft token outside [0, V)               */
+#define SPEC_DEV_ERR_UNIFORM     0x00000010u /* uniform outside [0, 1)                   */
+#define SPEC_DEV_ERR_ZERO_MASS   0x00000020u /* a row to sample from has zero total mass */
+#define SPEC_DEV_INFO_ZERO_RESIDUAL 0x00010000u /* informational: max(0,p-q) summed to 0
+                                                   after a rejection; drew from p instead */
+
+/* Human-readable name of a status code (static storage). */
+const char *spec_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int spec_version(void);
+
+/* ------------------------------------------------------------------------
+ * Verify attention.
+ *
+ * Defined by "Draft length and attention performance" (co-design blog): the
+ * D draft tokens reuse the same KV cache, so each KV head serves G(1+D)
+ * query rows and the attention GEMM-M is G(1+D).  For sequence b, KV head
+ * h, draft position i in [0, D] and group member g in [0, G):
+ *
+ *     o = softmax(softmax_scale * q K^T) V over keys j < kv_len[b] - D + i
+ *
+ * i.e. kv_len[b] counts the 1 + D verify tokens, whose K/V the preceding
+ * projection has already written into the cache; row i sees the prefix,
+ * the earlier drafts and itself.  D = 0 is ordinary decode attention.
+ *
+ * Layouts (all row-major, innermost last):
+ *   q_bf16        device, bf16 [B][1+D][Hkv*G][head_dim]; query head h*G+g
+ *                 belongs to KV head h.  16-byte aligned.
+ *   k_pages_bf16,
+ *   v_pages_bf16  device, bf16 [num_pages][page_size][Hkv][head_dim].
+ *                 16-byte aligned.  V entries must be finite and within
+ *                 +-65504 (they are staged in fp16 for the P.V product).
+ *   block_table   device, int32 [B][max_pages_per_seq]; key j of sequence b
+ *                 is slot j % page_size of page block_table[b][j/page_size].
+ *                 Entries past a sequence's last page are never read.
+ *   kv_len        device, int32 [B]; 1 + D <= kv_len[b] <=
+ *                 max_pages_per_seq * page_size.
+ *   out_f32       device, fp32 [B][1+D][Hkv*G][head_dim]; 16-byte aligned.
+ *   lse_f32       device, fp32 [B][1+D][Hkv*G] or NULL: natural-log
+ *                 partition function log(sum_j exp(softmax_scale q.k_j)).
+ * Contiguous caches are passed as pages with an identity block table.
+ *
+ * Supported set: head_dim in {64, 128}; page_size a multiple of 16;
+ * 0 <= D <= 63; G >= 1 with G*(1+D) <= 1024.  Other values return
+ * SPEC_ERR_UNSUPPORTED.  workspace must hold
+ * spec_verify_attention_workspace_size(...) bytes (device, 256-byte
+ * aligned); its contents need no initialisation and are scratch only.
+ * Rows of a sequence whose kv_len is out of range are not written and set
+ * SPEC_DEV_ERR_KV_LEN.
+ * ---------------------------------------------------------------------- */
+size_t spec_verify_attention_workspace_size(int B, int D, int Hkv, int G, int head_dim,
+                                            int max_kv_len);
+
+spec_status_t spec_verify_attention(const void *q_bf16, const void *k_pages_bf16,
+                                    const void *v_pages_bf16, int num_pages,
+                                    const int32_t *block_table, int max_pages_per_seq,
+                                    const int32_t *kv_len, int B, int D, int Hkv, int G,
+                                    int head_dim, int page_size, float softmax_scale,
+                                    float *out_f32, float *lse_f32, void *workspace,
+                                    size_t workspace_bytes, uint32_t *dev_status,
+                                    void *stream);
+
+/* ------------------------------------------------------------------------
+ * Verify GEMM.
+ *
+ * Defined by "Draft length and performance of linear layers" (co-design
+ * blog): with speculation every linear layer of the target runs with
+ * GEMM-M = M(1+D) instead of M; the representative expert GEMM is
+ * N = K = 6144.
+ *
+ *     y[m][n] = sum_k x[m][k] * w[n][k]     (fp32 accumulate, bf16 out)
+ *
+ *   x_bf16   device, bf16 [M][K] row-major, 16-byte aligned.
+ *   w_bf16   device, bf16 [N][K] row-major (nn.Linear weight layout),
+ *            16-byte aligned.
+ *   y_bf16   device, bf16 [M][N] row-major, 16-byte aligned.
+ * Supported set: 1 <= M <= 65536, N a multiple of 128, K a multiple of 64.
+ * workspace: spec_verify_gemm_workspace_size(M, N, K) bytes (may be 0;
+ * device, 256-byte aligned; scratch only).
+ * ---------------------------------------------------------------------- */
+size_t spec_verify_gemm_workspace_size(int M, int N, int K);
+
+spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_bf16, int M,
+                               int N, int K, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/* ------------------------------------------------------------------------
+ * Greedy acceptance.
+ *
+ * "Accept the longest prefix the target agrees with, then emit one more
+ * target token" (LLM inference handbook, "How speculative decoding works";
+ * co-design blog, "What is speculative decoding").  With
+ * t_i = argmax_v p[b][i][v] (lowest index on ties):
+ *     n_accepted[b] = first i < D with draft[b][i] != t_i, else D
+ *     token[b]      = t_{n_accepted[b]}
+ * so the accepted length AL = n_accepted + 1 lies in [1, 1 + D].  Only the
+ * rows 0..n_accepted[b] of p are read.
+ *
+ *   p        device, fp32 [B][1+D][V] target probabilities (or logits: only
+ *            their order matters).  NaN-free.
+ *   draft    device, int32 [B][D].
+ *   n_accepted, token   device, int32 [B].
+ * Supported set: B >= 0, 0 <= D <= 63, 1 <= V <= 2^26.
+ * ---------------------------------------------------------------------- */
+spec_status_t spec_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,
+                                 int32_t *n_accepted, int32_t *token, uint32_t *dev_status,
+                                 void *stream);
+
+/* ------------------------------------------------------------------------
+ * Stochastic acceptance (modified rejection sampling).
+ *
+ * From "How does speculative decoding speed up LLM inference?" (llm-digest,
+ * sections "Mechanism" and "Math intuition"): walk the drafts left to
+ * right, accept draft x with probability min(1, p(x)/q(x)); at the first
+ * rejection discard the rest and resample that position from
+ * max(0, p - q) renormalised; the emitted tokens then follow p exactly.
+ * With explicit uniforms:
+ *     accept draft i  iff  u_acc[b][i] * q[b][i][x] < p[b][i][x]   (exact)
+ *     j = first rejected i, else D;  n_accepted[b] = j
+ *     r(v) = max(0, p[b][j][v] - q[b][j][v])  if j < D,  else p[b][D][v]
+ *     token[b] = smallest v with sum_{w<=v} r(w) > u_res[b] * sum_w r(w)
+ * If r sums to zero after a rejection, r = p[b][j] is used instead and
+ * SPEC_DEV_INFO_ZERO_RESIDUAL is set.  The sums are carried out exactly
+ * (fixed point with 2^-61 resolution), so the result does not depend on
+ * summation order.
+ *
+ *   p        device, fp32 [B][1+D][V], entries in [0, 1], row sums < 8.
+ *   q        device, fp32 [B][D][V], same constraints (may be NULL if D=0).
+ *   draft    device, int32 [B][D].
+ *   u_acc    device, fp32 [B][D] in [0, 1).
+ *   u_res    device, fp32 [B] in [0, 1).
+ *   n_accepted, token   device, int32 [B].
+ * Supported set: B >= 0, 0 <= D <= 63, 1 <= V <= 2^26.
+ * ---------------------------------------------------------------------- */
+spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *draft,
+                                 const float *u_acc, const float *u_res, int B, int D, int V,
+                                 int32_t *n_accepted, int32_t *token, uint32_t *dev_status,
+                                 void *stream);
+
+/* ------------------------------------------------------------------------
+ * Host-side planning helper (no GPU work).
+ *
+ * Reports how spec_verify_attention splits the KV stream across CTAs for
+ * the given host copy of kv_len and CTA-group count: segment s covers key
+ * tiles [tile_begin, tile_end) (64 keys per tile) of unit (b, h), processed
+ * by group `group` and written to partial slot `slot` (-1 when the segment
+ * covers the whole unit and is written straight to the output).  Writes up
+ * to max_segments records of 6 int32 (group, b, h, tile_begin, tile_end,
+ * slot) and returns the number of segments, or -1 on invalid arguments.
+ * ---------------------------------------------------------------------- */
+int spec_verify_attention_plan(int B, const int32_t *kv_len_host, int D, int Hkv,
+                               int num_groups, int32_t *segments, int max_segments);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

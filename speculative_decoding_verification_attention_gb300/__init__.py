@@ -1,0 +1,228 @@
+"""Speculative-decoding verification step on one GB300 GPU.
+
+Thin Python binding over the C ABI in ``include/spec_verify.h`` (library
+``libspec_verify.so`` built in-tree from ``csrc/``).  The functions below
+only marshal arguments -- tensors become device pointers, the current torch
+stream becomes the launch stream -- and every step runs in the library's
+sm_103a kernels.  PyTorch supplies device memory and streams.
+
+There is no fallback: if the library is missing or a call fails, an
+exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "SpecError", "library", "library_path", "verify_attention", "verify_gemm",
+    "accept_greedy", "accept_sample", "attention_workspace_size",
+    "gemm_workspace_size", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libspec_verify.so")
+
+EXPORTED_SYMBOLS = (
+    "spec_status_string", "spec_version", "spec_verify_attention_workspace_size",
+    "spec_verify_attention", "spec_verify_gemm_workspace_size", "spec_verify_gemm",
+    "spec_accept_greedy", "spec_accept_sample", "spec_verify_attention_plan",
+)
+
+DEV_STATUS_BITS = {
+    "PAGE_ID": 0x1, "KV_LEN": 0x2, "TIMEOUT": 0x4, "TOKEN_ID": 0x8, "UNIFORM": 0x10,
+    "ZERO_MASS": 0x20, "INFO_ZERO_RESIDUAL": 0x10000,
+}
+
+_STATUS = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_UNSUPPORTED",
+           3: "SPEC_ERR_WORKSPACE", 4: "SPEC_ERR_CUDA", 5: "SPEC_ERR_TIMEOUT"}
+
+
+class SpecError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library():
+    """Load libspec_verify.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(library_path):
+                raise RuntimeError(
+                    f"{library_path} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(library_path)
+            P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            lib.spec_status_string.argtypes = [I]
+            lib.spec_status_string.restype = ctypes.c_char_p
+            lib.spec_version.restype = I
+            lib.spec_verify_attention_workspace_size.argtypes = [I, I, I, I, I, I]
+            lib.spec_verify_attention_workspace_size.restype = S
+            lib.spec_verify_attention.argtypes = [P, P, P, I, P, I, P, I, I, I, I, I, I, F, P, P,
+                                                  P, S, P, P]
+            lib.spec_verify_attention.restype = I
+            lib.spec_verify_gemm_workspace_size.argtypes = [I, I, I]
+            lib.spec_verify_gemm_workspace_size.restype = S
+            lib.spec_verify_gemm.argtypes = [P, P, P, I, I, I, P, S, P]
+            lib.spec_verify_gemm.restype = I
+            lib.spec_accept_greedy.argtypes = [P, P, I, I, I, P, P, P, P]
+            lib.spec_accept_greedy.restype = I
+            lib.spec_accept_sample.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P]
+            lib.spec_accept_sample.restype = I
+            lib.spec_verify_attention_plan.argtypes = [I, P, I, I, I, P, I]
+            lib.spec_verify_attention_plan.restype = I
+            _lib = lib
+    return _lib
+
+
+def _check(status, where):
+    if status != 0:
+        raise SpecError(status, where)
+
+
+def _dev(t, name, dtype=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------ attention
+def attention_workspace_size(B, D, Hkv, G, head_dim, max_kv_len):
+    return int(library().spec_verify_attention_workspace_size(B, D, Hkv, G, head_dim, max_kv_len))
+
+
+def verify_attention(q, k_pages, v_pages, block_table, kv_len, D, Hkv, G, softmax_scale=None,
+                     out=None, lse=None, workspace=None, dev_status=None, stream=None):
+    """GQA verify attention over a paged bf16 KV cache.
+
+    q [B, 1+D, Hkv*G, d] bf16; k_pages/v_pages [P, page, Hkv, d] bf16;
+    block_table [B, max_pages] int32; kv_len [B] int32 (counts the 1+D
+    verify tokens).  Returns out [B, 1+D, Hkv*G, d] fp32 (and fills ``lse``
+    [B, 1+D, Hkv*G] fp32 when given).
+    """
+    import torch
+    B, D1, Hq, d = q.shape
+    if D1 != D + 1 or Hq != Hkv * G:
+        raise ValueError("q shape does not match D/Hkv/G")
+    P, page, hk, dk = k_pages.shape
+    if hk != Hkv or dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages/v_pages shape mismatch")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, D + 1, Hq, d), dtype=torch.float32, device=q.device)
+    max_pages = block_table.shape[1]
+    need = attention_workspace_size(B, D, Hkv, G, d, max_pages * page)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = library().spec_verify_attention(
+        _dev(q, "q", torch.bfloat16), _dev(k_pages, "k_pages", torch.bfloat16),
+        _dev(v_pages, "v_pages", torch.bfloat16), P, _dev(block_table, "block_table", torch.int32),
+        max_pages, _dev(kv_len, "kv_len", torch.int32), B, D, Hkv, G, d, page,
+        float(softmax_scale), _dev(out, "out", torch.float32),
+        _dev(lse, "lse", torch.float32, allow_none=True),
+        _dev(workspace, "workspace", allow_none=True),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
+    _check(st, "spec_verify_attention")
+    return out
+
+
+def attention_plan(kv_len_host, D, Hkv, num_groups, max_segments=None):
+    """Segments (group, b, h, tile_begin, tile_end, slot) of the KV split."""
+    import numpy as np
+    kv = np.ascontiguousarray(kv_len_host, dtype=np.int32)
+    if max_segments is None:
+        tiles = int(np.sum((kv.astype(np.int64) + 63) // 64)) * Hkv
+        max_segments = tiles + 2 * num_groups + 8
+    seg = np.zeros((max_segments, 6), np.int32)
+    n = library().spec_verify_attention_plan(len(kv), kv.ctypes.data_as(ctypes.c_void_p), D,
+                                             Hkv, num_groups,
+                                             seg.ctypes.data_as(ctypes.c_void_p), max_segments)
+    if n < 0:
+        raise ValueError("spec_verify_attention_plan rejected its arguments")
+    return seg[:n]
+
+
+# ----------------------------------------------------------------------- GEMM
+def gemm_workspace_size(M, N, K):
+    return int(library().spec_verify_gemm_workspace_size(M, N, K))
+
+
+def verify_gemm(x, w, y=None, workspace=None, stream=None):
+    """y[M, N] (bf16) = x[M, K] @ w[N, K]^T with fp32 accumulation."""
+    import torch
+    M, K = x.shape
+    N, K2 = w.shape
+    if K2 != K:
+        raise ValueError("x/w inner dimensions differ")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    need = gemm_workspace_size(M, N, K)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    st = library().spec_verify_gemm(
+        _dev(x, "x", torch.bfloat16), _dev(w, "w", torch.bfloat16), _dev(y, "y", torch.bfloat16),
+        M, N, K, _dev(workspace, "workspace", allow_none=True),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "spec_verify_gemm")
+    return y
+
+
+# ----------------------------------------------------------------- acceptance
+def accept_greedy(p, draft, n_accepted=None, token=None, dev_status=None, stream=None):
+    """Greedy prefix acceptance; p [B, 1+D, V] fp32, draft [B, D] int32."""
+    import torch
+    B, D1, V = p.shape
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=p.device)
+    if token is None:
+        token = torch.empty(B, dtype=torch.int32, device=p.device)
+    st = library().spec_accept_greedy(
+        _dev(p, "p", torch.float32), _dev(draft, "draft", torch.int32, allow_none=True), B, D1 - 1,
+        V, _dev(n_accepted, "n_accepted", torch.int32), _dev(token, "token", torch.int32),
+        _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
+    _check(st, "spec_accept_greedy")
+    return n_accepted, token
+
+
+def accept_sample(p, q, draft, u_acc, u_res, n_accepted=None, token=None, dev_status=None,
+                  stream=None):
+    """Stochastic acceptance with residual resampling (explicit uniforms)."""
+    import torch
+    B, D1, V = p.shape
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=p.device)
+    if token is None:
+        token = torch.empty(B, dtype=torch.int32, device=p.device)
+    st = library().spec_accept_sample(
+        _dev(p, "p", torch.float32), _dev(q, "q", torch.float32, allow_none=True),
+        _dev(draft, "draft", torch.int32, allow_none=True),
+        _dev(u_acc, "u_acc", torch.float32, allow_none=True), _dev(u_res, "u_res", torch.float32),
+        B, D1 - 1, V, _dev(n_accepted, "n_accepted", torch.int32),
+        _dev(token, "token", torch.int32), _dev(dev_status, "dev_status", allow_none=True),
+        _stream(stream))
+    _check(st, "spec_accept_sample")
+    return n_accepted, token

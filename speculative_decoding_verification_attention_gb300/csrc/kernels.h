@@ -1,0 +1,19 @@
+// Launch functions implemented by the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace spec {
+
+constexpr int kMaxDraft = 63;
+
+cudaError_t launch_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,
+                                 int32_t *n_acc, int32_t *token, cudaStream_t st);
+
+cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *draft,
+                                 const float *u_acc, const float *u_res, int B, int D, int V,
+                                 int32_t *n_acc, int32_t *token, uint32_t *dev_status,
+                                 cudaStream_t st);
+
+}  // namespace spec

@@ -205,31 +205,43 @@ def tune_sigma_for_alpha(alpha, V, seed=1234, rows=64, target_std=3.0, tol=0.005
 
 
 def accept_inputs(seed, B, D, V, target_std=2.0, draft_noise=0.5, mode="sample",
-                  b_offset=0):
+                  b_offset=0, chunk=32):
     """p [B, 1+D, V], q [B, D, V] (fp32 softmax of fp64 logits), drafts
     [B, D] int32, u_acc [B, D], u_res [B] fp32.
 
-    mode="sample": draft i is drawn from q[b, i] with Philox stream 2;
-    mode="greedy": draft i = argmax q[b, i] (lowest index on ties).
+    Target logits ~ N(0, target_std^2); draft logits = target logits (first D
+    positions) + N(0, draft_noise^2).  mode="sample": draft i is drawn from
+    q[b, i] with Philox stream 2; mode="greedy": draft i = argmax q[b, i]
+    (lowest index on ties); mode="both" returns both as draft_sample /
+    draft_greedy (and draft = draft_sample).  Generated in chunks of
+    sequences to bound host memory.
     """
     rng = np.random.default_rng(seed)
-    t = rng.standard_normal((B, 1 + D, V)) * target_std
-    dl = t[:, :D, :] + rng.standard_normal((B, D, V)) * draft_noise
-    p = _softmax64(t).astype(np.float32)
-    q = _softmax64(dl).astype(np.float32)
-    if mode == "sample":
-        b = np.arange(b_offset, b_offset + B, dtype=np.uint64)
-        i = np.arange(max(D, 1), dtype=np.uint64)
+    p = np.empty((B, 1 + D, V), np.float32)
+    q = np.empty((B, D, V), np.float32)
+    for s0 in range(0, B, chunk):
+        s1 = min(B, s0 + chunk)
+        t = rng.standard_normal((s1 - s0, 1 + D, V)) * target_std
+        p[s0:s1] = _softmax64(t)
+        if D:
+            q[s0:s1] = _softmax64(t[:, :D, :] + rng.standard_normal((s1 - s0, D, V)) * draft_noise)
+        del t
+    out = dict(p=p, q=q, B=B, D=D, V=V)
+    b = np.arange(b_offset, b_offset + B, dtype=np.uint64)
+    i = np.arange(max(D, 1), dtype=np.uint64)
+    if mode in ("sample", "both"):
         ud = philox_uniform(seed, b[:, None], i[None, :], STREAM_DRAFT)[:, :D]
-        drafts = draw_from_rows(q, ud)
-    elif mode == "greedy":
-        drafts = np.argmax(q, axis=-1).astype(np.int32)
-    else:
+        ds = np.empty((B, D), np.int32)
+        for s0 in range(0, B, chunk):
+            ds[s0:s0 + chunk] = draw_from_rows(q[s0:s0 + chunk], ud[s0:s0 + chunk])
+        out["draft_sample"] = ds
+    if mode in ("greedy", "both"):
+        out["draft_greedy"] = np.argmax(q, axis=-1).astype(np.int32) if D else np.zeros((B, 0), np.int32)
+    if mode not in ("sample", "greedy", "both"):
         raise ValueError(mode)
-    u_acc, u_res = acceptance_uniforms(seed, B, D, b_offset)
-    return dict(p=np.ascontiguousarray(p), q=np.ascontiguousarray(q),
-                draft=np.ascontiguousarray(drafts, dtype=np.int32),
-                u_acc=u_acc, u_res=u_res, B=B, D=D, V=V)
+    out["draft"] = out["draft_greedy"] if mode == "greedy" else out["draft_sample"]
+    out["u_acc"], out["u_res"] = acceptance_uniforms(seed, B, D, b_offset)
+    return out
 
 
 def gemm_inputs(seed, M, N, K, w_std=0.02):

@@ -1,0 +1,70 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry
+point the header declares, and rejects invalid arguments on the host before
+anything is enqueued (so none of these calls touches a device)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import speculative_decoding_verification_attention_gb300 as sv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_attention_gb300 import _build
+    _build.build()
+    return sv.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    assert set(names) == set(sv.EXPORTED_SYMBOLS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert lib.spec_status_string(0) == b"SPEC_OK"
+    assert lib.spec_status_string(3) == b"SPEC_ERR_WORKSPACE"
+    assert lib.spec_status_string(99) == b"SPEC_ERR_UNKNOWN"
+    assert lib.spec_version() >= 100
+
+
+P = ctypes.c_void_p
+FAKE = P(0x7F0000001000)   # never dereferenced: validation fails first
+
+
+def test_accept_greedy_rejects_bad_arguments(lib):
+    f = lib.spec_accept_greedy
+    assert f(FAKE, FAKE, -1, 3, 10, FAKE, FAKE, None, None) == INVALID
+    assert f(FAKE, FAKE, 1, -1, 10, FAKE, FAKE, None, None) == INVALID
+    assert f(FAKE, FAKE, 1, 3, 0, FAKE, FAKE, None, None) == INVALID
+    assert f(FAKE, FAKE, 1, 64, 10, FAKE, FAKE, None, None) == UNSUPPORTED
+    assert f(None, FAKE, 1, 3, 10, FAKE, FAKE, None, None) == INVALID
+    assert f(FAKE, None, 1, 3, 10, FAKE, FAKE, None, None) == INVALID
+    assert f(P(0x7F0000001002), FAKE, 1, 3, 10, FAKE, FAKE, None, None) == INVALID
+    assert f(None, None, 0, 3, 10, None, None, None, None) == 0   # empty batch: no-op
+
+
+def test_accept_sample_rejects_bad_arguments(lib):
+    f = lib.spec_accept_sample
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 3, 0, FAKE, FAKE, None, None) == INVALID
+    assert f(FAKE, None, FAKE, FAKE, FAKE, 1, 3, 10, FAKE, FAKE, None, None) == INVALID
+    assert f(FAKE, FAKE, FAKE, None, FAKE, 1, 3, 10, FAKE, FAKE, None, None) == INVALID
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 3, 10, FAKE, FAKE, None, None) == INVALID
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 70, 10, FAKE, FAKE, None, None) == UNSUPPORTED
+    assert f(None, None, None, None, None, 0, 3, 10, None, None, None, None) == 0
