@@ -3,7 +3,9 @@
 #include <cstdio>
 
 #include "common.cuh"
+#include "gemm.h"
 #include "kernels.h"
+#include "tmap.h"
 
 using namespace spec;
 
@@ -84,12 +86,38 @@ spec_status_t spec_verify_attention(const void *, const void *, const void *, in
 
 int spec_verify_attention_plan(int, const int32_t *, int, int, int, int32_t *, int) { return -1; }
 
+
+}  // extern "C"
+
+extern "C" {
+
 size_t spec_verify_gemm_workspace_size(int, int, int) { return 0; }
 
-spec_status_t spec_verify_gemm(const void *, const void *, void *, int, int, int, void *, size_t,
-                               void *)
+spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_bf16, int M, int N,
+                               int K, void *workspace, size_t workspace_bytes, void *stream)
 {
-    return SPEC_ERR_UNSUPPORTED;
+    (void)workspace;
+    (void)workspace_bytes;
+    if (M < 0 || N < 0 || K < 0) return SPEC_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return SPEC_OK;
+    if (M > 65536 || N % 128 != 0 || K % 64 != 0 || K == 0 || N > (1 << 20) || K > (1 << 20))
+        return SPEC_ERR_UNSUPPORTED;
+    if (!x_bf16 || !w_bf16 || !y_bf16) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(w_bf16, 16) || !aligned(y_bf16, 16))
+        return SPEC_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return SPEC_ERR_CUDA;
+    const GemmPlan plan = plan_gemm(M, N, K, sms);
+    CUtensorMap tx, tw;
+    const uint64_t dx[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+    const uint64_t dw[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
+    const uint64_t st[1] = {static_cast<uint64_t>(K) * 2};
+    const uint32_t bx[2] = {64, static_cast<uint32_t>(plan.swap ? plan.mpad : 128)};
+    const uint32_t bw[2] = {64, static_cast<uint32_t>(plan.swap ? 128 : plan.bn)};
+    if (!encode_bf16_tmap(&tx, x_bf16, 2, dx, st, bx) || !encode_bf16_tmap(&tw, w_bf16, 2, dw, st, bw))
+        return SPEC_ERR_CUDA;
+    return from_cuda(launch_gemm(plan, tx, tw, y_bf16, M, N, K, sms, nullptr,
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

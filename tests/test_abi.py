@@ -68,3 +68,14 @@ def test_accept_sample_rejects_bad_arguments(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 3, 10, FAKE, FAKE, None, None) == INVALID
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 70, 10, FAKE, FAKE, None, None) == UNSUPPORTED
     assert f(None, None, None, None, None, 0, 3, 10, None, None, None, None) == 0
+
+
+def test_gemm_rejects_bad_arguments(lib):
+    f = lib.spec_verify_gemm
+    assert f(FAKE, FAKE, FAKE, -1, 128, 64, None, 0, None) == INVALID
+    assert f(FAKE, FAKE, FAKE, 8, 100, 64, None, 0, None) == UNSUPPORTED   # N % 128
+    assert f(FAKE, FAKE, FAKE, 8, 128, 60, None, 0, None) == UNSUPPORTED   # K % 64
+    assert f(None, FAKE, FAKE, 8, 128, 64, None, 0, None) == INVALID
+    assert f(P(0x7F0000001008), FAKE, FAKE, 8, 128, 64, None, 0, None) == INVALID
+    assert f(None, None, None, 0, 128, 64, None, 0, None) == 0   # empty: no-op
+    assert lib.spec_verify_gemm_workspace_size(512, 6144, 6144) == 0

@@ -1,0 +1,94 @@
+"""GPU parity of spec_verify_gemm against the fp64 oracle.
+
+Bar: relative L2 error <= 5e-3 over the compared entries (bf16 output
+rounding alone gives ~1e-3), plus an elementwise bound of 2^-7 |y| + 1e-3.
+Small shapes are compared in full; the verify shapes (N = K = 6144,
+M = B(1+D) from 8 to 4096) on a seeded sample of entries that covers every
+128-row / 128-column tile edge, plus a full-tensor comparison with torch's
+fp32-accumulating matmul as a secondary property check.
+"""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 5e-3
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from speculative_decoding_verification_attention_gb300 import _build
+    _build.build()
+    import speculative_decoding_verification_attention_gb300 as m
+    m.library()
+    return m
+
+
+def bits_to_dev(bits):
+    import torch
+    return torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def run(sv, x, w):
+    import torch
+    y = sv.verify_gemm(bits_to_dev(x), bits_to_dev(w))
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy().astype(np.float64), y
+
+
+def check(y, ref):
+    err = y - ref
+    rel = np.linalg.norm(err) / max(np.linalg.norm(ref), 1e-30)
+    assert rel <= REL_L2, rel
+    assert (np.abs(err) <= 2 ** -7 * np.abs(ref) + 1e-3).all(), np.abs(err).max()
+    return rel
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (8, 256, 512), (31, 384, 640), (64, 128, 1024),
+                                   (100, 256, 256), (128, 512, 128), (200, 128, 192),
+                                   (256, 256, 512), (257, 256, 256), (300, 512, 320),
+                                   (512, 384, 256)])
+def test_full_compare_small(sv, oracle_lib, M, N, K):
+    x, w = synth.gemm_inputs(M + N + K, M, N, K)
+    y, _ = run(sv, x, w)
+    check(y, oracle_lib.gemm(x, w))
+
+
+def sample_entries(rng, M, N, n=3000):
+    m = rng.integers(0, M, n)
+    c = rng.integers(0, N, n)
+    edges_m = np.unique(np.clip(np.concatenate([[0, M - 1], np.arange(127, M, 128),
+                                                np.arange(128, M, 128)]), 0, M - 1))
+    edges_n = np.unique(np.clip(np.concatenate([[0, N - 1], np.arange(127, N, 128),
+                                                np.arange(128, N, 128)]), 0, N - 1))
+    em, en = np.meshgrid(edges_m[:64], edges_n[:64])
+    m = np.concatenate([m, em.ravel()])
+    c = np.concatenate([c, en.ravel()])
+    return np.stack([m, c], axis=1).astype(np.int32)
+
+
+@pytest.mark.parametrize("M", [8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096, 56, 120, 504])
+def test_verify_shapes_sampled(sv, oracle_lib, M):
+    import torch
+    N = K = 6144
+    x, w = synth.gemm_inputs(1000 + M, M, N, K)
+    y, ydev = run(sv, x, w)
+    rng = np.random.default_rng(M)
+    s = sample_entries(rng, M, N)
+    ref = oracle_lib.gemm(x, w, samples=s)
+    check(y[s[:, 0], s[:, 1]], ref)
+    # whole-tensor property: agrees with an fp32-accumulating library matmul
+    yt = (bits_to_dev(x).float() @ bits_to_dev(w).float().T)
+    rel = (ydev.float() - yt).norm() / yt.norm()
+    assert float(rel) < REL_L2
+
+
+def test_two_calls_in_a_row_agree(sv):
+    x, w = synth.gemm_inputs(5, 64, 768, 6144)
+    a, _ = run(sv, x, w)
+    b, _ = run(sv, x, w)
+    assert np.array_equal(a, b)
