@@ -2,6 +2,8 @@
 // stream.  Nothing here allocates device memory.
 #include <cstdio>
 
+#include "attention.h"
+#include "attn_schedule.h"
 #include "common.cuh"
 #include "gemm.h"
 #include "kernels.h"
@@ -71,21 +73,121 @@ spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *
 
 }  // extern "C"
 
-// Entry points whose kernels are not built yet.
-extern "C" {
+namespace {
 
-size_t spec_verify_attention_workspace_size(int, int, int, int, int, int) { return 0; }
+constexpr int kMaxRows = 1024;      // G * (1 + D)
+constexpr int kSmFallback = 256;    // upper bound when no device is current
 
-spec_status_t spec_verify_attention(const void *, const void *, const void *, int,
-                                    const int32_t *, int, const int32_t *, int, int, int, int,
-                                    int, int, float, float *, float *, void *, size_t,
-                                    uint32_t *, void *)
+bool attention_shape_supported(int D, int Hkv, int G, int head_dim)
 {
-    return SPEC_ERR_UNSUPPORTED;
+    return D >= 0 && D <= kMaxDraft && Hkv >= 1 && G >= 1 &&
+           static_cast<long long>(G) * (1 + D) <= kMaxRows && (head_dim == 64 || head_dim == 128);
 }
 
-int spec_verify_attention_plan(int, const int32_t *, int, int, int, int32_t *, int) { return -1; }
+}  // namespace
 
+extern "C" {
+
+size_t spec_verify_attention_workspace_size(int B, int D, int Hkv, int G, int head_dim,
+                                            int max_kv_len)
+{
+    if (B < 0 || max_kv_len < 0 || !attention_shape_supported(D, Hkv, G, head_dim)) return 0;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = kSmFallback;
+    const int nt = (G * (1 + D) + 127) / 128;
+    return attention_workspace_bytes(nt, head_dim, sms);
+}
+
+spec_status_t spec_verify_attention(const void *q_bf16, const void *k_pages_bf16,
+                                    const void *v_pages_bf16, int num_pages,
+                                    const int32_t *block_table, int max_pages_per_seq,
+                                    const int32_t *kv_len, int B, int D, int Hkv, int G,
+                                    int head_dim, int page_size, float softmax_scale,
+                                    float *out_f32, float *lse_f32, void *workspace,
+                                    size_t workspace_bytes, uint32_t *dev_status, void *stream)
+{
+    if (B < 0 || D < 0 || Hkv < 1 || G < 1 || head_dim < 1 || page_size < 1 || num_pages < 1 ||
+        max_pages_per_seq < 1)
+        return SPEC_ERR_INVALID_ARG;
+    if (!attention_shape_supported(D, Hkv, G, head_dim) || page_size % 16 != 0)
+        return SPEC_ERR_UNSUPPORTED;
+    if (static_cast<long long>(num_pages) * page_size > 0x7fffffffLL ||
+        static_cast<long long>(max_pages_per_seq) * page_size > 0x7fffffffLL)
+        return SPEC_ERR_UNSUPPORTED;
+    if (!(softmax_scale > 0.0f) || softmax_scale > 1e30f) return SPEC_ERR_INVALID_ARG;
+    if (B == 0) return SPEC_OK;
+    if (!q_bf16 || !k_pages_bf16 || !v_pages_bf16 || !block_table || !kv_len || !out_f32)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned(q_bf16, 16) || !aligned(k_pages_bf16, 16) || !aligned(v_pages_bf16, 16) ||
+        !aligned(out_f32, 16) || !aligned(block_table, 4) || !aligned(kv_len, 4) ||
+        (lse_f32 && !aligned(lse_f32, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return SPEC_ERR_CUDA;
+    const int nt = (G * (1 + D) + 127) / 128;
+    const size_t need = attention_workspace_bytes(nt, head_dim, sms);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SPEC_ERR_WORKSPACE;
+
+    CUtensorMap tk, tv;
+    const int box_rows = page_size % 64 == 0 ? 64 : page_size % 32 == 0 ? 32 : 16;
+    const uint64_t dims[3] = {static_cast<uint64_t>(head_dim), static_cast<uint64_t>(Hkv),
+                              static_cast<uint64_t>(num_pages) * page_size};
+    const uint64_t strides[2] = {static_cast<uint64_t>(head_dim) * 2,
+                                 static_cast<uint64_t>(Hkv) * head_dim * 2};
+    const uint32_t box[3] = {64, 1, static_cast<uint32_t>(box_rows)};
+    if (!encode_bf16_tmap(&tk, k_pages_bf16, 3, dims, strides, box) ||
+        !encode_bf16_tmap(&tv, v_pages_bf16, 3, dims, strides, box))
+        return SPEC_ERR_CUDA;
+
+    AttnArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(q_bf16);
+    a.block_table = block_table;
+    a.kv_len = kv_len;
+    a.out = out_f32;
+    a.lse = lse_f32;
+    a.part_o = static_cast<float *>(workspace);
+    a.nt = nt;
+    a.groups = attention_groups(nt, sms);
+    const size_t o_bytes = static_cast<size_t>(2) * a.groups * nt * 128 * head_dim * sizeof(float);
+    a.part_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + ((o_bytes + 255) & ~size_t(255)));
+    a.dev_status = dev_status;
+    a.B = B; a.D = D; a.Hkv = Hkv; a.G = G; a.R = G * (1 + D);
+    a.page_size = page_size; a.box_rows = box_rows; a.max_pages = max_pages_per_seq;
+    a.num_pages = num_pages;
+    a.max_len = static_cast<int64_t>(max_pages_per_seq) * page_size;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    return from_cuda(launch_verify_attention(tk, tv, a, head_dim, static_cast<cudaStream_t>(stream)));
+}
+
+int spec_verify_attention_plan(int B, const int32_t *kv_len_host, int D, int Hkv, int num_groups,
+                               int32_t *segments, int max_segments)
+{
+    if (B < 0 || D < 0 || Hkv < 1 || num_groups < 1 || (B > 0 && !kv_len_host) ||
+        max_segments < 0 || (max_segments > 0 && !segments))
+        return -1;
+    const int64_t max_len = INT64_MAX;
+    const int64_t total = total_tiles_serial(kv_len_host, B, D, Hkv, max_len);
+    const int ge = effective_groups(total, num_groups);
+    int n = 0;
+    for (int g = 0; g < ge; ++g) {
+        const int64_t gb = group_begin(total, ge, g), gn = group_begin(total, ge, g + 1);
+        if (gb >= gn) continue;
+        int b0, h0;
+        int64_t ub0;
+        locate_serial(kv_len_host, B, D, Hkv, max_len, gb, b0, h0, ub0);
+        SegmentWalker w;
+        w.init(kv_len_host, B, D, Hkv, max_len, g, gb, gn, b0, h0, ub0);
+        Segment s;
+        while (w.next(s)) {
+            if (n < max_segments) {
+                int32_t *o = segments + 6 * static_cast<int64_t>(n);
+                o[0] = g; o[1] = s.b; o[2] = s.h; o[3] = s.tile_begin; o[4] = s.tile_end; o[5] = s.slot;
+            }
+            ++n;
+        }
+    }
+    return n;
+}
 
 }  // extern "C"
 

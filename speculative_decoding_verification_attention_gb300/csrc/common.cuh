@@ -93,6 +93,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// mbar_wait for warps that go on to execute warp-collective (.sync.aligned)
+// tcgen05 instructions: the result is made uniform across the warp, so no
+// lane can proceed to a collective op that another lane has abandoned.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                               uint32_t *dev_status)
+{
+    const bool ok = mbar_wait(bar, parity, abort, dev_status);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Bounded wait used while unwinding after an abort (never sets abort).
 __device__ __forceinline__ void mbar_wait_drain(uint64_t *bar, uint32_t parity,
                                                 unsigned long long limit_ns)

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t lt = 0;
         for (int t = blockIdx.x; t < tiles && !*abort; t += gridDim.x, ++lt) {
             const uint32_t ab = lt & 1;
-            if (!mbar_wait(&acc_full[ab], (lt >> 1) & 1, abort, dev_status)) break;
+            if (!mbar_wait_warp(&acc_full[ab], (lt >> 1) & 1, abort, dev_status)) break;
             tc_fence_after();
             const int mt = t % tiles_m, nt = t / tiles_m;
             const int m = mt * kBM + row;
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool epi = warp >= 2;
     bool ok = true;
     if (epi) {
-        ok = mbar_wait(&acc_full[0], 0, abort, dev_status);
+        ok = mbar_wait_warp(&acc_full[0], 0, abort, dev_status);
         tc_fence_after();
     }
     if (splits > 1) {
