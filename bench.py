@@ -1,0 +1,583 @@
+#!/usr/bin/env python3
+"""Benchmark of the speculative-decoding verification step on GB300.
+
+One step = one pass of the whole verification path over one batch of
+synthetic inputs resident in HBM:
+  1. verify attention  B=64 sequences, L_b ~ U{4096..131072}, 64-token pages
+                       in a random permutation, Hkv=8, G=8, head_dim=128, D=7
+  2. verify GEMM       M = B(1+D) = 512, N = K = 6144 (bf16, fp32 accumulate)
+  3. greedy accept     B=64, D=7, V=131072 fp32 target probabilities
+  4. stochastic accept same shapes, draft probabilities at acceptance ~0.6
+Headline metric: verified query tokens per second, B(1+D) / step time.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch one process per GPU (torchrun); every rank runs the same
+step on its own GPU (independent replicas, weak scaling) and rank 0 prints
+one JSON line with the aggregate over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "verified query-tokens/s (verify attention + verify GEMM + greedy and stochastic accept)"
+UNIT = "tokens/s"
+WORKLOAD = dict(B=64, D=7, Hkv=8, G=8, head_dim=128, page_size=64, L_lo=4096, L_hi=131072,
+                V=131072, alpha=0.6, N=6144, K=6144, seed=2026)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return dict(hbm_gbs=float(m["hbm_gbs"]), bf16_tflops=float(m["bf16_tflops"]),
+                    bf16_tflops_sustained=float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------- workload
+class Workload:
+    """Device-resident inputs of one verification step."""
+
+    def __init__(self, device, seed=WORKLOAD["seed"]):
+        import torch
+        w = WORKLOAD
+        self.B, self.D, self.V = w["B"], w["D"], w["V"]
+        self.kv_len_host = synth.full_step_kv_lengths(seed, w["B"], w["L_lo"], w["L_hi"])
+        self.attn = synth.attention_inputs_device(seed + 1, w["B"], w["Hkv"], w["G"],
+                                                  w["head_dim"], w["D"], self.kv_len_host,
+                                                  page_size=w["page_size"], device=device)
+        g = torch.Generator(device=device)
+        g.manual_seed(seed + 2)
+        M = w["B"] * (1 + w["D"])
+        self.M = M
+        self.x = torch.randn((M, w["K"]), generator=g, device=device).to(torch.bfloat16)
+        self.w = (torch.randn((w["N"], w["K"]), generator=g, device=device) * 0.02).to(torch.bfloat16)
+        # acceptance inputs: fp32 softmax of N(0, 3^2) target logits; draft
+        # logits = target + N(0, sigma^2) with sigma tuned for alpha
+        sigma, _ = synth.tune_sigma_for_alpha(w["alpha"], w["V"], rows=8, target_std=3.0)
+        self.sigma = sigma
+        t = torch.randn((w["B"], w["D"] + 1, w["V"]), generator=g, device=device) * 3.0
+        dl = t[:, :w["D"], :] + torch.randn((w["B"], w["D"], w["V"]), generator=g, device=device) * sigma
+        self.p = torch.softmax(t.double(), dim=-1).float()
+        self.q = torch.softmax(dl.double(), dim=-1).float()
+        del t, dl
+        u_acc, u_res = synth.acceptance_uniforms(seed + 3, w["B"], w["D"])
+        b = np.arange(w["B"], dtype=np.uint64)
+        i = np.arange(w["D"], dtype=np.uint64)
+        ud = synth.philox_uniform(seed + 3, b[:, None], i[None, :], synth.STREAM_DRAFT)
+        q_host = self.q.cpu().numpy()
+        self.draft_sample = torch.from_numpy(synth.draw_from_rows(q_host, ud)).to(device)
+        self.draft_greedy = torch.from_numpy(np.argmax(q_host, axis=-1).astype(np.int32)).to(device)
+        del q_host
+        self.u_acc = torch.from_numpy(u_acc).to(device)
+        self.u_res = torch.from_numpy(u_res).to(device)
+        self.sum_L = int(self.kv_len_host.astype(np.int64).sum())
+
+    # algorithmic bytes / flops per launch
+    def attention_bytes(self):
+        w = WORKLOAD
+        kv = 2 * self.sum_L * w["Hkv"] * w["head_dim"] * 2
+        q = self.B * (1 + self.D) * w["Hkv"] * w["G"] * w["head_dim"] * 2
+        o = self.B * (1 + self.D) * w["Hkv"] * w["G"] * (w["head_dim"] + 1) * 4
+        return kv + q + o
+
+    def attention_flops(self):
+        w = WORKLOAD
+        rows = (1 + self.D) * w["G"]
+        return 4 * self.sum_L * w["Hkv"] * rows * w["head_dim"]
+
+    def gemm_flops(self):
+        return 2 * self.M * WORKLOAD["N"] * WORKLOAD["K"]
+
+    def gemm_bytes(self):
+        return 2 * (self.M * WORKLOAD["K"] + WORKLOAD["N"] * WORKLOAD["K"] + self.M * WORKLOAD["N"])
+
+
+def accept_bytes(n_acc_greedy, n_acc_sample, B, D, V):
+    greedy = int((np.asarray(n_acc_greedy) + 1).sum()) * V * 4
+    rows = np.where(np.asarray(n_acc_sample) < D, 2, 1)
+    sample = int(rows.sum()) * V * 4 + B * D * 16
+    return greedy, sample
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, out_path):
+        self.path = out_path
+        self.proc = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, device_index=0):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9 or parts[0] != str(device_index):
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_step(sv, wl, ws, outs, ev=None):
+    """Enqueue one verification step; ev: optional list of 5 event pairs."""
+    a = wl.attn
+    if ev: ev[0].record()
+    sv.verify_attention(a.q, a.k_pages, a.v_pages, a.block_table, a.kv_len, wl.D, WORKLOAD["Hkv"],
+                        WORKLOAD["G"], out=outs["o"], lse=outs["lse"], workspace=ws["attn"])
+    if ev: ev[1].record()
+    sv.verify_gemm(wl.x, wl.w, y=outs["y"], workspace=ws["gemm"])
+    if ev: ev[2].record()
+    sv.accept_greedy(wl.p, wl.draft_greedy, n_accepted=outs["ng"], token=outs["tg"])
+    if ev: ev[3].record()
+    sv.accept_sample(wl.p, wl.q, wl.draft_sample, wl.u_acc, wl.u_res, n_accepted=outs["ns"],
+                     token=outs["ts"])
+    if ev: ev[4].record()
+
+
+def gpu_arm(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    from speculative_decoding_verification_attention_gb300 import _build
+    import speculative_decoding_verification_attention_gb300 as sv
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    sv.library()
+    wl = Workload(dev)
+    w = WORKLOAD
+    Hq = w["Hkv"] * w["G"]
+    outs = dict(o=torch.empty((wl.B, wl.D + 1, Hq, w["head_dim"]), device=dev),
+                lse=torch.empty((wl.B, wl.D + 1, Hq), device=dev),
+                y=torch.empty((wl.M, w["N"]), dtype=torch.bfloat16, device=dev),
+                ng=torch.empty(wl.B, dtype=torch.int32, device=dev),
+                tg=torch.empty(wl.B, dtype=torch.int32, device=dev),
+                ns=torch.empty(wl.B, dtype=torch.int32, device=dev),
+                ts=torch.empty(wl.B, dtype=torch.int32, device=dev))
+    max_len = wl.attn.block_table.shape[1] * w["page_size"]
+    ws = dict(attn=torch.empty(max(256, sv.attention_workspace_size(wl.B, wl.D, w["Hkv"], w["G"],
+                                                                        w["head_dim"], max_len)),
+                               dtype=torch.uint8, device=dev),
+              gemm=None)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        run_step(sv, wl, ws, outs)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    clock_path = os.path.join(tempfile.gettempdir(), f"spec_clocks_{os.getpid()}.csv")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    with ClockSampler(clock_path) as clk:
+        for i in range(K):
+            flush.fill_((i + 7) & 0xFF)          # evict L2 between steps (not timed)
+            run_step(sv, wl, ws, outs, evs[i])
+        torch.cuda.synchronize()
+        # stretch the sampled window so a short run still yields samples
+        time.sleep(max(0.0, 0.45 - (time.perf_counter() - t_wall)))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    per = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(4)] for i in range(K)])
+    step_ms = per.sum(axis=1)
+    ms_step = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    ng, ns = outs["ng"].cpu().numpy(), outs["ns"].cpu().numpy()
+    g_bytes, s_bytes = accept_bytes(ng, ns, wl.B, wl.D, wl.V)
+
+    # ------------------------------------------------------------- e2e
+    e2e = e2e_arm(sv, wl, ws, outs, dev, args.e2e_steps) if args.e2e_steps > 0 else None
+
+    pk = peaks()
+    attn_ms = float(per[:, 0].mean())
+    gemm_ms = float(per[:, 1].mean())
+    greedy_ms = float(per[:, 2].mean())
+    sample_ms = float(per[:, 3].mean())
+    attn_gbs = wl.attention_bytes() / (attn_ms * 1e-3) / 1e9
+    gemm_tf = wl.gemm_flops() / (gemm_ms * 1e-3) / 1e12
+    tokens = wl.B * (1 + wl.D) * world
+    line = {
+        "metric": METRIC, "value": tokens / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random bf16 KV/Q/W, softmax probabilities of random logits)",
+        "config": {"workload": "full verify step: paged GQA attention B=64 L~U[4096,131072] "
+                               "page=64 Hkv=8 G=8 d=128 D=7 + GEMM M=512 N=K=6144 + "
+                               "greedy/stochastic accept B=64 D=7 V=131072 alpha~0.6",
+                   "global_batch_sequences": wl.B * world, "draft_len": wl.D,
+                   "tokens_per_step_per_gpu": wl.B * (1 + wl.D), "sum_kv_len": wl.sum_L,
+                   "kv_cache_gb": 2 * wl.sum_L * w["Hkv"] * w["head_dim"] * 2 / 1e9,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between steps (512 MB write, untimed)",
+                   "precision": "bf16 inputs, fp32 accumulate, fp16 P in P.V, fp32 attention "
+                                "output; acceptance exact (fp64 products, fixed-point sums)"},
+        "kernels": {
+            "attention": {"ms": attn_ms, "GB_per_s": attn_gbs,
+                          "frac_hbm": attn_gbs / pk["hbm_gbs"],
+                          "algorithmic_bytes": wl.attention_bytes(),
+                          "tflops": wl.attention_flops() / (attn_ms * 1e-3) / 1e12},
+            "gemm_M512": {"ms": gemm_ms, "TFLOP_per_s": gemm_tf,
+                          "frac_tensor": gemm_tf / pk["bf16_tflops_sustained"],
+                          "GB_per_s": wl.gemm_bytes() / (gemm_ms * 1e-3) / 1e9},
+            "accept_greedy": {"ms": greedy_ms, "algorithmic_bytes": g_bytes,
+                              "GB_per_s": g_bytes / (greedy_ms * 1e-3) / 1e9,
+                              "accepted_tokens_per_s": float((ng + 1).sum()) / (greedy_ms * 1e-3)},
+            "accept_sample": {"ms": sample_ms, "algorithmic_bytes": s_bytes,
+                              "GB_per_s": s_bytes / (sample_ms * 1e-3) / 1e9,
+                              "accepted_tokens_per_s": float((ns + 1).sum()) / (sample_ms * 1e-3),
+                              "mean_AL": float((ns + 1).mean())},
+        },
+        "roofline": {"kernel": "verify_attention (main + partial merge)", "bound": "hbm",
+                     "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": attn_gbs / pk["hbm_gbs"], "traffic": None,
+                     "peak_source": pk["source"] + " (copy bandwidth, of measured)"},
+        "gpu_launches": 5 * K,
+        "wall_s_timed_region": wall,
+        "clocks": clk.summary(dev.index or 0),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    return line
+
+
+def e2e_arm(sv, wl, ws, outs, dev, steps):
+    """Same step through the public API with per-step inputs in pinned host
+    memory: H2D of queries, page table, lengths, GEMM input, target/draft
+    probabilities, drafts and uniforms; D2H of the accepted counts and
+    tokens.  The KV cache and the weights stay resident (model state)."""
+    import torch
+    a = wl.attn
+    host = {}
+    for name, t in [("q", a.q), ("bt", a.block_table), ("kv", a.kv_len), ("x", wl.x),
+                    ("p", wl.p), ("qd", wl.q), ("ds", wl.draft_sample), ("dg", wl.draft_greedy),
+                    ("ua", wl.u_acc), ("ur", wl.u_res)]:
+        host[name] = t.cpu().pin_memory()
+    dst = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    res = torch.empty((4, wl.B), dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = res.numel() * res.element_size()
+    Hkv, G = WORKLOAD["Hkv"], WORKLOAD["G"]
+
+    def one():
+        for k in host:
+            dst[k].copy_(host[k], non_blocking=True)
+        sv.verify_attention(dst["q"], a.k_pages, a.v_pages, dst["bt"], dst["kv"], wl.D, Hkv, G,
+                            out=outs["o"], lse=outs["lse"], workspace=ws["attn"])
+        sv.verify_gemm(dst["x"], wl.w, y=outs["y"])
+        sv.accept_greedy(dst["p"], dst["dg"], n_accepted=outs["ng"], token=outs["tg"])
+        sv.accept_sample(dst["p"], dst["qd"], dst["ds"], dst["ua"], dst["ur"],
+                         n_accepted=outs["ns"], token=outs["ts"])
+        res[0].copy_(outs["ng"], non_blocking=True)
+        res[1].copy_(outs["tg"], non_blocking=True)
+        res[2].copy_(outs["ns"], non_blocking=True)
+        res[3].copy_(outs["ts"], non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": wl.B * (1 + wl.D) / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "note": "KV cache and GEMM weights resident; per-step inputs copied from pinned host"}
+
+
+# ---------------------------------------------------------------- CPU arm
+def cpu_sample_time(threads=0, budget_s=12.0):
+    """Time the fp64 oracle on a bounded sample of one step and scale to the
+    whole step.  Returns (seconds per step, description, threads).
+
+    The sample: whole (b, h) attention units of a 16384-key sequence (all 64
+    query rows) until about 70% of the budget is spent, 4 of the 512 GEMM
+    rows, and 16 of the 64 sequences of acceptance (both modes); each part is
+    scaled linearly (keys x heads, rows, sequences) to the full step.
+    """
+    import oracle
+    w = WORKLOAD
+    kv = synth.full_step_kv_lengths(WORKLOAD["seed"], w["B"], w["L_lo"], w["L_hi"])
+    sum_L = int(kv.astype(np.int64).sum())
+    nthreads = oracle.max_threads() if threads <= 0 else threads
+    L = 16384
+    inp = synth.attention_inputs(1, 1, 1, w["G"], w["head_dim"], w["D"], [L], page_size=64)
+    n_units = 0
+    t0 = time.perf_counter()
+    while n_units < 1 or (time.perf_counter() - t0 < 0.7 * budget_s and n_units < 64):
+        oracle.verify_attention(inp.q, inp.k_pages, inp.v_pages, inp.block_table, inp.kv_len,
+                                w["D"], 1, w["G"], w["head_dim"], 64, threads=threads)
+        n_units += 1
+    t_attn = (time.perf_counter() - t0) / (n_units * L) * sum_L * w["Hkv"]
+    M = w["B"] * (1 + w["D"])
+    x, wt = synth.gemm_inputs(2, 4, w["N"], w["K"])
+    t0 = time.perf_counter()
+    oracle.gemm(x, wt, threads=threads)
+    t_gemm = (time.perf_counter() - t0) / 4 * M
+    acc = synth.accept_inputs(3, 16, w["D"], w["V"], target_std=3.0, draft_noise=1.0, mode="both")
+    t0 = time.perf_counter()
+    oracle.accept_greedy(acc["p"], acc["draft_greedy"], threads=threads)
+    oracle.accept_sample(acc["p"], acc["q"], acc["draft_sample"], acc["u_acc"], acc["u_res"],
+                         threads=threads)
+    t_acc = (time.perf_counter() - t0) / 16 * w["B"]
+    total = t_attn + t_gemm + t_acc
+    desc = (f"fp64 oracle on {n_units} attention unit(s) of {L} keys x 64 rows (scaled by keys "
+            f"to sum L={sum_L} over {w['Hkv']} KV heads), 4 of {M} GEMM rows, 16 of {w['B']} "
+            f"sequences of greedy+stochastic acceptance; each scaled linearly to one step")
+    return total, desc, nthreads
+
+
+def reference_arm(args, rank, world):
+    line = {"impl": "reference", "metric": METRIC, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "full verify step (same as the GPU arm), evaluated by the "
+                                   "fp64 CPU oracle on a bounded sample per step"}}
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    times = []
+    desc, nthreads = "", 0
+    for i in range(args.warmup + args.steps):
+        t, desc, nthreads = cpu_sample_time(budget_s=3.0)
+        if i >= args.warmup:
+            times.append(t)
+    ms = 1e3 * float(np.mean(times))
+    tokens = WORKLOAD["B"] * (1 + WORKLOAD["D"])
+    v = tokens / (ms * 1e-3)
+    line.update({"value": v, "ms_per_step": ms,
+                 "cpu_baseline": {"value": v, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                                  "sample": desc},
+                 "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
+    return line
+
+
+# ------------------------------------------------------ single-kernel cases
+def time_launches(fn, warmup, steps, flush=None):
+    """Mean device time (ms) of fn() over `steps` launches after `warmup`,
+    flushing L2 between launches when a flush buffer is given."""
+    import torch
+    for i in range(warmup):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_((i + 3) & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in ts]))
+
+
+def case_lines(args):
+    """Secondary measurements, one JSON line each (not the headline)."""
+    import torch
+    from speculative_decoding_verification_attention_gb300 import _build
+    import speculative_decoding_verification_attention_gb300 as sv
+    _build.build()
+    sv.library()
+    dev = torch.device("cuda", 0)
+    pk = peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    lines = []
+
+    def attention_case(name, B, Hkv, G, D, L, seed):
+        inp = synth.attention_inputs_device(seed, B, Hkv, G, 128, D, L, page_size=64, device=dev)
+        out = torch.empty((B, D + 1, Hkv * G, 128), device=dev)
+        lse = torch.empty((B, D + 1, Hkv * G), device=dev)
+        ws = torch.empty(sv.attention_workspace_size(B, D, Hkv, G, 128, inp.block_table.shape[1] * 64),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: sv.verify_attention(inp.q, inp.k_pages, inp.v_pages, inp.block_table,
+                                         inp.kv_len, D, Hkv, G, out=out, lse=lse, workspace=ws)
+        ms = time_launches(fn, args.warmup, args.steps)   # KV >> L2: no flush needed
+        sumL = int(np.sum(inp.kv_len_host.astype(np.int64)))
+        by = 2 * sumL * Hkv * 128 * 2 + B * (D + 1) * Hkv * G * (128 * 2 + 129 * 4)
+        fl = 4 * sumL * Hkv * G * (1 + D) * 128
+        fl_pad = 4 * sumL * Hkv * 128 * 128 * ((G * (1 + D) + 127) // 128)
+        gbs = by / (ms * 1e-3) / 1e9
+        lines.append({"case": name, "kernel": "verify_attention", "B": B, "Hkv": Hkv, "G": G, "D": D,
+                      "L": L if np.isscalar(L) else "ragged", "ms": ms,
+                      "query_tokens_per_s": B * (D + 1) / (ms * 1e-3), "GB_per_s": gbs,
+                      "frac_hbm": gbs / pk["hbm_gbs"], "TFLOP_per_s": fl / (ms * 1e-3) / 1e12,
+                      "padded_TFLOP_per_s": fl_pad / (ms * 1e-3) / 1e12,
+                      "frac_tensor_padded": fl_pad / (ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"],
+                      "G(1+D)": G * (1 + D)})
+        del inp
+        torch.cuda.empty_cache()
+
+    if args.workload in ("attention", "all"):
+        attention_case("throughput B16 L32768 D15", 16, 8, 8, 15, 32768, 11)
+    if args.workload in ("dsweep", "all"):
+        for D in (0, 1, 3, 4, 7, 15):
+            attention_case(f"large-group B8 G32 L131072 D{D}", 8, 4, 32, D, 131072, 20 + D)
+    if args.workload == "attention-small":
+        attention_case("small B4 L32768 D7 (profiling)", 4, 8, 8, 7, 32768, 5)
+    if args.workload in ("gemm", "all"):
+        N = K = 6144
+        w = (torch.randn((N, K), device=dev) * 0.02).to(torch.bfloat16)
+        for M in (8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096):
+            x = torch.randn((M, K), device=dev).to(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ms = time_launches(lambda: sv.verify_gemm(x, w, y=y), args.warmup, args.steps, flush)
+            tf = 2 * M * N * K / (ms * 1e-3) / 1e12
+            by = 2 * (M * K + N * K + M * N)
+            lines.append({"case": f"gemm M{M} N{N} K{K}", "kernel": "verify_gemm", "M": M, "ms": ms,
+                          "TFLOP_per_s": tf, "frac_tensor": tf / pk["bf16_tflops_sustained"],
+                          "GB_per_s": by / (ms * 1e-3) / 1e9,
+                          "frac_hbm": by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]})
+    if args.workload in ("accept", "all"):
+        B, D, V = 256, 7, 131072
+        for alpha in (0.4, 0.6, 0.8):
+            sigma, _ = synth.tune_sigma_for_alpha(alpha, V, rows=8, target_std=3.0)
+            g = torch.Generator(device=dev)
+            g.manual_seed(int(alpha * 100))
+            t = torch.randn((B, D + 1, V), generator=g, device=dev) * 3.0
+            p = torch.softmax(t.double(), -1).float()
+            q = torch.softmax((t[:, :D] + torch.randn((B, D, V), generator=g, device=dev) * sigma).double(), -1).float()
+            del t
+            qh = q.cpu().numpy()
+            u_acc, u_res = synth.acceptance_uniforms(7, B, D)
+            ud = synth.philox_uniform(7, np.arange(B, dtype=np.uint64)[:, None],
+                                      np.arange(D, dtype=np.uint64)[None, :], synth.STREAM_DRAFT)
+            ds = torch.from_numpy(synth.draw_from_rows(qh, ud)).to(dev)
+            dg = torch.from_numpy(np.argmax(qh, -1).astype(np.int32)).to(dev)
+            ua, ur = torch.from_numpy(u_acc).to(dev), torch.from_numpy(u_res).to(dev)
+            na, tk = torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev)
+            ms_g = time_launches(lambda: sv.accept_greedy(p, dg, na, tk), args.warmup, args.steps, flush)
+            ng = na.cpu().numpy()
+            ms_s = time_launches(lambda: sv.accept_sample(p, q, ds, ua, ur, na, tk), args.warmup, args.steps, flush)
+            ns = na.cpu().numpy()
+            gb, sb = accept_bytes(ng, ns, B, D, V)
+            for mode, ms, n, by in (("greedy", ms_g, ng, gb), ("sample", ms_s, ns, sb)):
+                lines.append({"case": f"accept {mode} B{B} D{D} V{V} alpha{alpha}", "kernel": f"accept_{mode}",
+                              "ms": ms, "accepted_tokens_per_s": float((n + 1).sum()) / (ms * 1e-3),
+                              "sequences_per_s": B / (ms * 1e-3), "mean_AL": float((n + 1).mean()),
+                              "algorithmic_bytes": by, "GB_per_s": by / (ms * 1e-3) / 1e9,
+                              "frac_hbm": by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]})
+            del p, q
+            torch.cuda.empty_cache()
+    for ln in lines:
+        ln["peak_source"] = pk["source"]
+        print(json.dumps(ln), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="step",
+                    choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small"],
+                    help="step: the headline line; others print one secondary JSON line per case")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group(backend=backend)
+    if args.workload != "step":
+        case_lines(args)
+        return
+    try:
+        if args.impl == "reference":
+            line = reference_arm(args, rank, world)
+        else:
+            line = gpu_arm(args, rank, world)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                t, desc, nthreads = cpu_sample_time()
+                v = WORKLOAD["B"] * (1 + WORKLOAD["D"]) / t
+                line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": nthreads,
+                                        "kind": "oracle", "sample": desc}
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
