@@ -117,6 +117,40 @@ spec_status_t spec_verify_attention(const void *q_bf16, const void *k_pages_bf16
                                     void *stream);
 
 /* ------------------------------------------------------------------------
+ * Verify attention without a caller workspace: allocates nothing.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot hand the library a device buffer -- for example a plugin in
+ * an inference engine whose own memory pool owns all device memory and
+ * forbids other allocations, or a latency-critical loop in which
+ * cudaMalloc / cudaFree would synchronise the device.  It computes exactly
+ * what spec_verify_attention computes, with the same arguments minus the
+ * workspace pair, but takes its scratch from a fixed device array of
+ * SPEC_NOALLOC_SCRATCH_BYTES built into the library (every GPU that loads
+ * the library holds that array until the process exits) and calls no
+ * allocator of any kind.
+ *  - A problem whose spec_verify_attention_workspace_size(...) exceeds
+ *    SPEC_NOALLOC_SCRATCH_BYTES is rejected with SPEC_ERR_WORKSPACE before
+ *    anything is launched.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array, whose contents persist between calls
+ *    but need no clearing.  Calls that can overlap on the GPU (two streams,
+ *    or host threads without ordering between them) race on the array and
+ *    must be serialised by the caller.
+ * ---------------------------------------------------------------------- */
+#define SPEC_NOALLOC_SCRATCH_BYTES (24u << 20)
+
+spec_status_t spec_verify_attention_noalloc(const void *q_bf16, const void *k_pages_bf16,
+                                            const void *v_pages_bf16, int num_pages,
+                                            const int32_t *block_table, int max_pages_per_seq,
+                                            const int32_t *kv_len, int B, int D, int Hkv, int G,
+                                            int head_dim, int page_size, float softmax_scale,
+                                            float *out_f32, float *lse_f32, uint32_t *dev_status,
+                                            void *stream);
+
+/* ------------------------------------------------------------------------
  * Verify GEMM.
  *
  * Defined by "Draft length and performance of linear layers" (co-design

@@ -29,6 +29,7 @@ EXPORTED_SYMBOLS = (
     "spec_status_string", "spec_version", "spec_verify_attention_workspace_size",
     "spec_verify_attention", "spec_verify_gemm_workspace_size", "spec_verify_gemm",
     "spec_accept_greedy", "spec_accept_sample", "spec_verify_attention_plan",
+    "spec_verify_attention_noalloc",
 )
 
 DEV_STATUS_BITS = {
@@ -77,6 +78,9 @@ def library():
             lib.spec_accept_greedy.restype = I
             lib.spec_accept_sample.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P]
             lib.spec_accept_sample.restype = I
+            lib.spec_verify_attention_noalloc.argtypes = [P, P, P, I, P, I, P, I, I, I, I, I, I, F,
+                                                          P, P, P, P]
+            lib.spec_verify_attention_noalloc.restype = I
             lib.spec_verify_attention_plan.argtypes = [I, P, I, I, I, P, I]
             lib.spec_verify_attention_plan.restype = I
             _lib = lib
