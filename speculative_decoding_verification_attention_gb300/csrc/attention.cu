@@ -306,13 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int i = r / a.G, gg = r % a.G;
                     const uint4 *src = reinterpret_cast<const uint4 *>(
                         a.q + ((static_cast<int64_t>(seg.b) * (a.D + 1) + i) * Hq + seg.h * a.G + gg) * HD);
-#pragma unroll
+#pragma unroll 4
                     for (int c = 0; c < HD / 8; ++c) {
                         const uint4 v = __ldg(src + c);
                         *reinterpret_cast<uint4 *>(sQ + (c >> 3) * (kBM * 128) + sw128_offset(rl, c & 7)) = v;
                     }
                 } else {
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < HD / 8; ++c)
                         *reinterpret_cast<uint4 *>(sQ + (c >> 3) * (kBM * 128) + sw128_offset(rl, c & 7)) = make_uint4(0, 0, 0, 0);
                 }
@@ -377,16 +377,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[sb]);
+                // Raw scores; keys at or past this row's limit become -inf.  Only
+                // the tail tiles of a sequence need the mask.
                 const int key0 = (seg.tile_begin + k) * kBN;
-                const int nvis = max(0, min(kBN, limit - key0));
                 float x[kBN];
-                float mx = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    x[c] = c < nvis ? __uint_as_float(s0[c]) * a.scale_log2 : -INFINITY;
-                    x[c + 32] = c + 32 < nvis ? __uint_as_float(s1[c]) * a.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, fmaxf(x[c], x[c + 32]));
+                    x[c] = __uint_as_float(s0[c]);
+                    x[c + 32] = __uint_as_float(s1[c]);
                 }
+                if (key0 + kBN > limit) {
+                    const int nvis = limit - key0;       // may be <= 0
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c)
+                        if (c >= nvis) x[c] = -INFINITY;
+                }
+                float m0 = fmaxf(x[0], x[1]), m1 = fmaxf(x[2], x[3]);
+#pragma unroll
+                for (int c = 4; c < kBN; c += 4) {
+                    m0 = fmaxf(m0, fmaxf(x[c], x[c + 1]));
+                    m1 = fmaxf(m1, fmaxf(x[c + 2], x[c + 3]));
+                }
+                // max commutes with the positive scale: scale once
+                const float mx = fmaxf(m0, m1) * a.scale_log2;
                 // Lazy rescaling: a row moves its reference max only when the
                 // tile max exceeds it by more than 2^8.  The decision is per
                 // row, but the TMEM access below is warp-collective, so the
@@ -418,18 +431,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (j >= 2 && !mbar_wait_warp(&p_empty[pb], ((j >> 1) & 1) ^ 1, abort, a.dev_status)) { ok = false; break; }
+                // p = 2^(s * scale_log2 - m_ref): one FFMA and one MUFU per key;
+                // masked keys (-inf) give 0.  A row with no visible key yet
+                // (m_ref = -inf) writes zeros.
                 uint32_t ph[kBN / 2];
-                float lsum = 0.f;
+                const float neg_m = -m_ref;
+                const float sc = a.scale_log2;
+                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+                if (m_ref != -INFINITY) {
 #pragma unroll
-                for (int c = 0; c < kBN; c += 2) {
-                    const float p0 = x[c] == -INFINITY ? 0.f : ex2(x[c] - m_ref);
-                    const float p1 = x[c + 1] == -INFINITY ? 0.f : ex2(x[c + 1] - m_ref);
-                    const __half2 h2 = __floats2half2_rn(p0, p1);
-                    const float2 back = __half22float2(h2);
-                    lsum += back.x + back.y;
-                    ph[c / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+                    for (int c = 0; c < kBN; c += 4) {
+                        const float p0 = ex2(fmaf(x[c], sc, neg_m));
+                        const float p1 = ex2(fmaf(x[c + 1], sc, neg_m));
+                        const float p2 = ex2(fmaf(x[c + 2], sc, neg_m));
+                        const float p3 = ex2(fmaf(x[c + 3], sc, neg_m));
+                        l0 += p0; l1 += p1; l2 += p2; l3 += p3;
+                        const __half2 h01 = __floats2half2_rn(p0, p1);
+                        const __half2 h23 = __floats2half2_rn(p2, p3);
+                        ph[c / 2] = *reinterpret_cast<const uint32_t *>(&h01);
+                        ph[c / 2 + 1] = *reinterpret_cast<const uint32_t *>(&h23);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kBN / 2; ++c) ph[c] = 0u;
                 }
-                l += lsum;
+                l += (l0 + l1) + (l2 + l3);
                 uint8_t *prow = sP + pb * L::kP;
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
