@@ -232,12 +232,15 @@ spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *
  *
  * Reports how spec_verify_attention splits the KV stream across CTAs for
  * the given host copy of kv_len and CTA-group count: segment s covers key
- * tiles [tile_begin, tile_end) (64 keys per tile) of unit (b, h), processed
+ * tiles [tile_begin, tile_end) (SPEC_ATTENTION_KEY_TILE keys per tile) of
+ * unit (b, h), processed
  * by group `group` and written to partial slot `slot` (-1 when the segment
  * covers the whole unit and is written straight to the output).  Writes up
  * to max_segments records of 6 int32 (group, b, h, tile_begin, tile_end,
  * slot) and returns the number of segments, or -1 on invalid arguments.
  * ---------------------------------------------------------------------- */
+#define SPEC_ATTENTION_KEY_TILE 128
+
 int spec_verify_attention_plan(int B, const int32_t *kv_len_host, int D, int Hkv,
                                int num_groups, int32_t *segments, int max_segments);
 

@@ -37,6 +37,8 @@ DEV_STATUS_BITS = {
     "ZERO_MASS": 0x20, "INFO_ZERO_RESIDUAL": 0x10000,
 }
 
+ATTENTION_KEY_TILE = 128   # SPEC_ATTENTION_KEY_TILE: keys per tile of the KV split
+
 _STATUS = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_UNSUPPORTED",
            3: "SPEC_ERR_WORKSPACE", 4: "SPEC_ERR_CUDA", 5: "SPEC_ERR_TIMEOUT"}
 
@@ -159,7 +161,8 @@ def attention_plan(kv_len_host, D, Hkv, num_groups, max_segments=None):
     import numpy as np
     kv = np.ascontiguousarray(kv_len_host, dtype=np.int32)
     if max_segments is None:
-        tiles = int(np.sum((kv.astype(np.int64) + 63) // 64)) * Hkv
+        kt = ATTENTION_KEY_TILE
+        tiles = int(np.sum((kv.astype(np.int64) + kt - 1) // kt)) * Hkv
         max_segments = tiles + 2 * num_groups + 8
     seg = np.zeros((max_segments, 6), np.int32)
     n = library().spec_verify_attention_plan(len(kv), kv.ctypes.data_as(ctypes.c_void_p), D,

@@ -8,28 +8,34 @@
 // j < kv_len - D + i.
 //
 // Kernel structure (one CTA per SM, 8 warps):
-//   warp 0      TMA producer: K and V tiles of 64 keys, page by page, into a
+//   warp 0      TMA producer: K and V tiles of 128 keys, page by page, into a
 //               ring of shared-memory stages (128-byte swizzle).
-//   warp 1      tcgen05 issuer: S = Q K^T (bf16, fp32 in TMEM, two S
-//               buffers) and O += P V (fp16, fp32 accumulator in TMEM).
+//   warp 1      tcgen05 issuer: S = Q K^T (bf16, M = 128 rows x N = 128 keys,
+//               fp32 in TMEM) and O += P V (P read from TMEM, fp32
+//               accumulator in TMEM), issued as soon as their inputs are
+//               ready.
 //   warps 2-3   load the 128 query rows of each segment into shared memory;
-//               convert each V tile bf16 -> fp16 in place (zeroing keys past
-//               the end of the sequence).
-//   warps 4-7   softmax: one thread per query row reads its S row from TMEM,
-//               masks, keeps an online max / sum with lazy rescaling of O
-//               (only when the max grows by more than 2^8), writes P as fp16
-//               to shared memory; at the end of a segment reads O from TMEM
-//               and writes the normalised output or a partial result.
+//               zero the V rows of keys past the end of a sequence.
+//   warps 4-11  softmax, as two streams that take alternate key tiles (each
+//               with its own S buffers and O accumulator in TMEM): one thread
+//               per query row reads its S row from TMEM, masks, keeps an
+//               online max / sum with lazy rescaling of O (only when the max
+//               grows by more than 2^8), and writes P back into its S buffer
+//               as a bf16 pair hi + lo; at the end of a segment the two
+//               streams are merged and the normalised output or a partial
+//               result is written.
 // The KV stream of all (b, h) units is split evenly across CTA groups (see
 // attn_schedule.h); units cut by a group boundary are merged by
 // attention_combine.  G(1+D) > 128 uses several 128-row m-tiles, each its
 // own CTA of the same group, so the same K/V tiles are read concurrently
 // and served from L2.
 //
-// P is kept in fp16 rather than bf16: rounding P to bf16 alone gives about
-// 2e-3 relative error in O; fp16 (11-bit significand) keeps it near 3e-4.
+// P is split as P = hi + lo with hi = bf16(P) and lo = bf16(P - hi) (about
+// 16 significant bits), and O += hi V + lo V takes two bf16 MMAs that read
+// the A operand straight from tensor memory.  Rounding P to a single bf16
+// would cost about 2e-3 relative error in O; the pair keeps it near 1e-5
+// and leaves V in bf16 as stored.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
 #include "attention.h"
 #include "attn_schedule.h"
@@ -40,7 +46,8 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBN = kKeyTile;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;                 // 12 warps
+constexpr int kCombineThreads = 128;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -48,15 +55,15 @@ template <int HD>
 struct AttnSmem {
     static constexpr int kSub = HD / 64;                   // 64-column chunks
     static constexpr uint32_t kQ = kBM * HD * 2;
-    static constexpr uint32_t kKV = kBN * HD * 2;          // one K or V tile
-    static constexpr int kStages = HD == 128 ? 4 : 6;
-    static constexpr uint32_t kP = kBM * kBN * 2;          // one fp16 P buffer
+    static constexpr uint32_t kSubBytes = kBN * 128;       // one 64-column chunk of a K/V tile
+    static constexpr uint32_t kKV = kSub * kSubBytes;      // one K or V tile
+    static constexpr int kStages = HD == 128 ? 3 : 6;
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffK = kOffQ + kQ;
     static constexpr uint32_t kOffV = kOffK + kStages * kKV;
-    static constexpr uint32_t kOffP = kOffV + kStages * kKV;
-    static constexpr uint32_t kOffBar = kOffP + 2 * kP;
-    static constexpr uint32_t kBytes = kOffBar + 256 + 1024;
+    static constexpr uint32_t kOffML = kOffV + kStages * kKV;   // float2 per row: stream merge
+    static constexpr uint32_t kOffBar = kOffML + kBM * 8;
+    static constexpr uint32_t kBytes = kOffBar + 512 + 1024;
 };
 
 struct PlanShared {
@@ -90,7 +97,7 @@ __device__ int64_t block_incl_scan64(int64_t x, PlanShared *ps, int64_t *total)
     if (lane == 31) ps->warp_tot[warp] = incl;
     __syncthreads();
     int64_t before = 0, all = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
         if (w < warp) before += ps->warp_tot[w];
         all += ps->warp_tot[w];
     }
@@ -103,7 +110,7 @@ __device__ int64_t block_incl_scan64(int64_t x, PlanShared *ps, int64_t *total)
 __device__ void plan_group(const AttnArgs &a, int g, PlanShared *ps)
 {
     int64_t local = 0;
-    for (int b = threadIdx.x; b < a.B; b += kThreads) {
+    for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
         const int nk = seq_tiles(a.kv_len[b], a.D, a.max_len);
         if (nk == 0 && blockIdx.x == 0) report(a.dev_status, SPEC_DEV_ERR_KV_LEN);
         local += static_cast<int64_t>(a.Hkv) * nk;
@@ -120,7 +127,7 @@ __device__ void plan_group(const AttnArgs &a, int g, PlanShared *ps)
     __syncthreads();
     if (gb >= gn) return;
     int64_t base = 0;
-    for (int c0 = 0; c0 < a.B; c0 += kThreads) {
+    for (int c0 = 0; c0 < a.B; c0 += blockDim.x) {
         const int b = c0 + threadIdx.x;
         const int nk = b < a.B ? seq_tiles(a.kv_len[b], a.D, a.max_len) : 0;
         const int64_t span = static_cast<int64_t>(a.Hkv) * nk;
@@ -150,39 +157,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sQ = smem + L::kOffQ;
     uint8_t *sK = smem + L::kOffK;
     uint8_t *sV = smem + L::kOffV;
-    uint8_t *sP = smem + L::kOffP;
+    float2 *sML = reinterpret_cast<float2 *>(smem + L::kOffML);
     uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
     uint64_t *kv_empty = kv_full + S;
     uint64_t *v_ready = kv_empty + S;
-    uint64_t *s_full = v_ready + S;
-    uint64_t *s_empty = s_full + 2;
-    uint64_t *p_full = s_empty + 2;
-    uint64_t *p_empty = p_full + 2;
+    uint64_t *s_full = v_ready + S;       // [stream]: S of the stream's current tile is in TMEM
+    uint64_t *s_empty = s_full + 2;       // [stream]: its P.V has run, the S/P columns are free
+    uint64_t *p_full = s_empty + 2;       // [stream]: P written
+    uint64_t *p_empty = p_full + 2;       // [stream]: P.V done (O updated)
     uint64_t *q_full = p_empty + 2;
     uint64_t *q_empty = q_full + 1;
-    uint64_t *drain = q_empty + 1;
+    uint64_t *ml_ready = q_empty + 1;     // stream 1 published (m, l) and its O is final
+    uint64_t *o_taken = ml_ready + 1;     // stream 0 has read stream 1's O
+    uint64_t *drain = o_taken + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.x / a.nt, mt = blockIdx.x % a.nt;
-    constexpr uint32_t kCols = 256;        // O: HD columns, S: 2 x 64 columns
-    constexpr uint32_t kColS = HD;
+    // TMEM: O of stream s at column s*HD; the S/P buffer of stream s at
+    // 2*HD + s*128.  After the softmax has read S it writes P over it: for
+    // keys [16c, 16c + 16), hi in columns 16c..16c+7 and lo in 16c+8..16c+15
+    // (two bf16 per column), i.e. exactly over those keys' own S columns.
+    constexpr uint32_t kCols = 512;
+    constexpr uint32_t kColS = 2 * HD;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
-            mbar_init(&v_ready[s], 64);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&v_ready[i], 64);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&s_full[s], 1);
-            mbar_init(&s_empty[s], 4);
-            mbar_init(&p_full[s], 4);
-            mbar_init(&p_empty[s], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 1);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&p_empty[i], 1);
         }
         mbar_init(q_full, 64);
         mbar_init(q_empty, 1);
+        mbar_init(ml_ready, 4);
+        mbar_init(o_taken, 4);
         mbar_init(drain, 1);
         *abort = 0;
         fence_mbar_init();
@@ -210,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t *bt = a.block_table + static_cast<int64_t>(seg.b) * a.max_pages;
                 for (int t = seg.tile_begin; t < seg.tile_end; ++t, ++kg) {
                     const int st = kg % S;
-                    if (kg >= S && !mbar_wait(&kv_empty[st], ((kg / S) & 1) ^ 1, abort, a.dev_status)) { ok = false; break; }
+                    // page ids are looked up before waiting for the stage, so the
+                    // block-table loads overlap the wait
                     const int key0 = t * kBN;
                     const int nvalid = min(kBN, Lb - key0);
                     int rows[kBN / 16];
@@ -225,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         rows[nbox] = page * a.page_size + key % a.page_size;
                         bytes += 2u * L::kSub * a.box_rows * 128u;
                     }
+                    if (kg >= S && !mbar_wait(&kv_empty[st], ((kg / S) & 1) ^ 1, abort, a.dev_status)) { ok = false; break; }
                     mbar_arrive_expect_tx(&kv_full[st], bytes);
                     uint8_t *dk = sK + st * L::kKV;
                     uint8_t *dv = sV + st * L::kKV;
@@ -233,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int r0 = i * a.box_rows;
 #pragma unroll
                         for (int sub = 0; sub < L::kSub; ++sub) {
-                            tma_load_3d(dk + sub * (kBN * 128) + r0 * 128, &tm_k, &kv_full[st], sub * 64, seg.h, rows[i]);
-                            tma_load_3d(dv + sub * (kBN * 128) + r0 * 128, &tm_v, &kv_full[st], sub * 64, seg.h, rows[i]);
+                            tma_load_3d(dk + sub * L::kSubBytes + r0 * 128, &tm_k, &kv_full[st], sub * 64, seg.h, rows[i]);
+                            tma_load_3d(dv + sub * L::kSubBytes + r0 * 128, &tm_v, &kv_full[st], sub * 64, seg.h, rows[i]);
                         }
                     }
                 }
@@ -246,54 +263,115 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // --------------------------------------------- tcgen05 issuer
+        // Tile k of a segment belongs to stream k & 1.  The issuer keeps one
+        // cursor for S = QK^T (all tiles in order) and one per stream for
+        // O += PV, and issues whichever operation's inputs are ready.
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_f16(kBM, kBN, 1, 0, 0);
-            constexpr uint32_t idesc_pv = idesc_f16(kBM, HD, 0, 0, 1);
-            const uint32_t q_base = smem_u32(sQ), k_base = smem_u32(sK), v_base = smem_u32(sV),
-                           p_base = smem_u32(sP);
-            uint32_t kg = 0, si = 0;
-            bool ok = true;
-            auto issue_pv = [&](uint32_t j, bool first) -> bool {
-                const uint32_t pb = j & 1, st = j % S;
-                if (!mbar_wait(&p_full[pb], (j >> 1) & 1, abort, a.dev_status)) return false;
-                if (!mbar_wait(&v_ready[st], (j / S) & 1, abort, a.dev_status)) return false;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t ad = sdesc(p_base + pb * L::kP + kk * 32, 16, 1024);
-                    const uint64_t bd = sdesc(v_base + st * L::kKV + kk * 2048, kBN * 128, 1024);
-                    umma_f16_ss(tmem, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
+            constexpr uint32_t idesc_pv = idesc_f16(kBM, HD, 1, 0, 1);
+            // descriptors of the tile bases; a K step or a stage only moves
+            // the start-address field
+            const uint64_t dq0 = sdesc(smem_u32(sQ), 16, 1024);
+            const uint64_t dk0 = sdesc(smem_u32(sK), 16, 1024);
+            const uint64_t dv0 = sdesc(smem_u32(sV), L::kSubBytes, 1024);
+            struct Cursor {
+                SegmentWalker w;
+                Segment seg;
+                bool valid;
+                int k, step;
+                uint32_t j, base, si;   // global tile, segment's first global tile, segment index
+                __device__ void start(const SegmentWalker &w0, int k0, int st)
+                {
+                    w = w0; k = k0; step = st; j = 0; base = 0; si = 0;
+                    valid = w.next(seg);
+                    settle(k0);
                 }
-                umma_commit(&p_empty[pb]);
-                umma_commit(&kv_empty[st]);
-                return true;
-            };
-            while (ok && walk.next(seg)) {
-                const int n = seg.tile_end - seg.tile_begin;
-                if (!mbar_wait(q_full, si & 1, abort, a.dev_status)) break;
-                for (int k = 0; k < n && ok; ++k) {
-                    const uint32_t j = kg + k, st = j % S, sb = j & 1;
-                    if (!mbar_wait(&kv_full[st], (j / S) & 1, abort, a.dev_status)) { ok = false; break; }
-                    if (j >= 2 && !mbar_wait(&s_empty[sb], ((j >> 1) & 1) ^ 1, abort, a.dev_status)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint64_t ad = sdesc(q_base + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = sdesc(k_base + st * L::kKV + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
-                        umma_f16_ss(tmem + kColS + sb * kBN, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                // move on while the current segment has no tile for this cursor
+                __device__ void settle(int k_restart)
+                {
+                    while (valid && k >= seg.tile_end - seg.tile_begin) {
+                        base += seg.tile_end - seg.tile_begin;
+                        ++si;
+                        k = k_restart;
+                        valid = w.next(seg);
                     }
-                    umma_commit(&s_full[sb]);
-                    if (k == n - 1) umma_commit(q_empty);
-                    if (k >= 1 && !issue_pv(j - 1, k - 1 == 0)) { ok = false; break; }
+                    j = base + k;
                 }
-                if (!ok) break;
-                if (!issue_pv(kg + n - 1, n == 1)) break;
-                kg += n;
-                ++si;
+                __device__ void advance(int k_restart)
+                {
+                    k += step;
+                    settle(k_restart);
+                }
+            };
+            Cursor cq, cp[2];
+            cq.start(walk, 0, 1);
+            cp[0].start(walk, 0, 2);
+            cp[1].start(walk, 1, 2);
+            uint32_t nqk[2] = {0, 0}, npv[2] = {0, 0};
+            unsigned long long t_idle = 0;
+            uint32_t spins = 0;
+            while (cq.valid || cp[0].valid || cp[1].valid) {
+                bool progress = false;
+                if (cq.valid) {
+                    const int n = cq.seg.tile_end - cq.seg.tile_begin;
+                    const uint32_t j = cq.j, st = j % S, sm = cq.k & 1, jq = nqk[sm];
+                    if ((cq.k != 0 || mbar_test(q_full, cq.si & 1)) && mbar_test(&kv_full[st], (j / S) & 1) &&
+                        (jq == 0 || mbar_test(&s_empty[sm], (jq - 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t d = tmem + kColS + sm * kBN;
+#pragma unroll
+                        for (int kk = 0; kk < HD / 16; ++kk) {
+                            const uint64_t ad = dq0 + ((static_cast<uint32_t>(kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+                            const uint64_t bd = dk0 + ((st * L::kKV + static_cast<uint32_t>(kk >> 2) * L::kSubBytes + (kk & 3) * 32) >> 4);
+                            umma_f16_ss(d, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&s_full[sm]);
+                        if (cq.k == n - 1) umma_commit(q_empty);
+                        ++nqk[sm];
+                        cq.advance(0);
+                        progress = true;
+                    }
+                }
+#pragma unroll
+                for (int sm = 0; sm < 2; ++sm) {
+                    Cursor &c = cp[sm];
+                    if (!c.valid) continue;
+                    const uint32_t j = c.j, st = j % S, jp = npv[sm];
+                    if (mbar_test(&p_full[sm], jp & 1) && mbar_test(&v_ready[st], (j / S) & 1)) {
+                        tc_fence_after();
+                        const bool first = c.k < 2;     // first tile of this stream in the segment
+                        const uint32_t p_tm = tmem + kColS + sm * kBN;
+                        const uint32_t d = tmem + sm * HD;
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk) {
+                            const uint64_t bd = dv0 + ((st * L::kKV + kk * 2048) >> 4);
+                            umma_f16_ts(d, p_tm + kk * 16, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
+                            umma_f16_ts(d, p_tm + kk * 16 + 8, bd, idesc_pv, 1u);
+                        }
+                        umma_commit(&p_empty[sm]);
+                        umma_commit(&kv_empty[st]);
+                        umma_commit(&s_empty[sm]);   // S/P columns reusable
+                        ++npv[sm];
+                        c.advance(sm);
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    spins = 0;
+                } else if ((++spins & 255u) == 0) {
+                    if (*abort) break;
+                    const unsigned long long now = globaltimer_ns();
+                    if (spins == 256) t_idle = now;
+                    else if (now - t_idle > kWaitTimeoutNs) {
+                        *abort = 1;
+                        report(a.dev_status, SPEC_DEV_ERR_TIMEOUT);
+                        break;
+                    }
+                }
             }
         }
     } else if (warp < 4) {
-        // ------------------------------- Q loader + V bf16 -> fp16 converter
+        // ---------------------------- Q loader + V tail clearing (warps 2-3)
         const int ct = threadIdx.x - 64;       // 0..63
         uint32_t kg = 0, si = 0;
         bool ok = true;
@@ -323,27 +401,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = seg.tile_begin; t < seg.tile_end; ++t, ++kg) {
                 const int st = kg % S;
                 if (!mbar_wait(&kv_full[st], (kg / S) & 1, abort, a.dev_status)) { ok = false; break; }
+                // Keys past the end of the sequence get P = 0, but 0 * NaN would
+                // still poison O: clear those V rows (they hold whatever the
+                // page or the stage held before).
                 const int nvalid = min(kBN, Lb - t * kBN);
-                uint8_t *vt = sV + st * L::kKV;
-#pragma unroll 4
-                for (int idx = ct; idx < L::kSub * kBN * 8; idx += 64) {
-                    const int row = (idx & (kBN * 8 - 1)) >> 3;
-                    uint4 *pch = reinterpret_cast<uint4 *>(vt + idx * 16);
-                    uint4 w = make_uint4(0, 0, 0, 0);
-                    if (row < nvalid) {
-                        const uint4 in = *pch;
-                        const uint32_t iw[4] = {in.x, in.y, in.z, in.w};
-                        uint32_t ow[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float lo = __uint_as_float(iw[e] << 16);
-                            const float hi = __uint_as_float(iw[e] & 0xFFFF0000u);
-                            const __half2 h2 = __floats2half2_rn(lo, hi);
-                            ow[e] = *reinterpret_cast<const uint32_t *>(&h2);
-                        }
-                        w = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                if (nvalid < kBN) {
+                    uint8_t *vt = sV + st * L::kKV;
+                    for (int idx = ct; idx < L::kSub * kBN * 8; idx += 64) {
+                        const int row = (idx & (kBN * 8 - 1)) >> 3;
+                        if (row >= nvalid) *reinterpret_cast<uint4 *>(vt + idx * 16) = make_uint4(0, 0, 0, 0);
                     }
-                    *pch = w;
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&v_ready[st]);
@@ -351,7 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++si;
         }
     } else {
-        // --------------------------------------------- softmax / epilogue
+        // --------------------------------- softmax / epilogue, two streams
+        // Warps 4-7 are stream 0, warps 8-11 stream 1; both streams own the
+        // same 128 query rows (TMEM lanes) and take alternate key tiles.
+        const int sm = (warp - 4) >> 2;
         const int quad = warp & 3;
         const int rl = quad * 32 + lane;
         const int r = mt * kBM + rl;
@@ -359,69 +429,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i_row = row_ok ? r / a.G : 0;
         const int g_row = row_ok ? r % a.G : 0;
         const uint32_t t_lane = tmem + ((quad * 32) << 16);
-        uint32_t kg = 0;
+        const uint32_t t_o = t_lane + sm * HD;
+        const uint32_t t_s = t_lane + kColS + sm * kBN;
+        const float sc = a.scale_log2;
+        uint32_t ns = 0, si = 0;     // tiles of this stream so far; segments
         bool ok = true;
         while (ok && walk.next(seg)) {
             const int n = seg.tile_end - seg.tile_begin;
             const int Lb = a.kv_len[seg.b];
             const int limit = row_ok ? Lb - a.D + i_row : 0;    // keys j < limit are visible
             float m_ref = -INFINITY, l = 0.f;
-            for (int k = 0; k < n; ++k) {
-                const uint32_t j = kg + k, sb = j & 1, pb = j & 1;
-                if (!mbar_wait_warp(&s_full[sb], (j >> 1) & 1, abort, a.dev_status)) { ok = false; break; }
+            int ks = 0;
+            for (int k = sm; k < n; k += 2, ++ks, ++ns) {
+                if (!mbar_wait_warp(&s_full[sm], ns & 1, abort, a.dev_status)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t s0[32], s1[32];
-                tmem_ld_32x32b_x32(t_lane + kColS + sb * kBN, s0);
-                tmem_ld_32x32b_x32(t_lane + kColS + sb * kBN + 32, s1);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[sb]);
-                // Raw scores; keys at or past this row's limit become -inf.  Only
-                // the tail tiles of a sequence need the mask.
+                // S(ns) exists only after the stream's previous P.V finished
+                // (the issuer waits for that before S = QK^T), so this confirms
+                // that phase at once and keeps the p_empty waits in step.
+                if (ns >= 1 && !mbar_wait_warp(&p_empty[sm], (ns - 1) & 1, abort, a.dev_status)) { ok = false; break; }
                 const int key0 = (seg.tile_begin + k) * kBN;
-                float x[kBN];
+                const int nvis = limit - key0;            // keys [0, nvis) of the tile are visible
+                // pass 1: row max of the raw scores
+                float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll 1
+                for (int q = 0; q < kBN / 32; q += 2) {
+                    uint32_t x0[32], x1[32];
+                    tmem_ld_32x32b_x32(t_s + 32 * q, x0);
+                    tmem_ld_32x32b_x32(t_s + 32 * q + 32, x1);
+                    tmem_ld_wait();
+                    if (key0 + kBN <= limit) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    x[c] = __uint_as_float(s0[c]);
-                    x[c + 32] = __uint_as_float(s1[c]);
-                }
-                if (key0 + kBN > limit) {
-                    const int nvis = limit - key0;       // may be <= 0
+                        for (int c = 0; c < 32; c += 2) {
+                            m0 = fmaxf(m0, fmaxf(__uint_as_float(x0[c]), __uint_as_float(x0[c + 1])));
+                            m1 = fmaxf(m1, fmaxf(__uint_as_float(x1[c]), __uint_as_float(x1[c + 1])));
+                        }
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c)
-                        if (c >= nvis) x[c] = -INFINITY;
-                }
-                float m0 = fmaxf(x[0], x[1]), m1 = fmaxf(x[2], x[3]);
-#pragma unroll
-                for (int c = 4; c < kBN; c += 4) {
-                    m0 = fmaxf(m0, fmaxf(x[c], x[c + 1]));
-                    m1 = fmaxf(m1, fmaxf(x[c + 2], x[c + 3]));
+                        for (int c = 0; c < 32; ++c) {
+                            if (32 * q + c < nvis) m0 = fmaxf(m0, __uint_as_float(x0[c]));
+                            if (32 * q + 32 + c < nvis) m1 = fmaxf(m1, __uint_as_float(x1[c]));
+                        }
+                    }
                 }
                 // max commutes with the positive scale: scale once
-                const float mx = fmaxf(m0, m1) * a.scale_log2;
+                const float mx = fmaxf(m0, m1) * sc;
                 // Lazy rescaling: a row moves its reference max only when the
                 // tile max exceeds it by more than 2^8.  The decision is per
                 // row, but the TMEM access below is warp-collective, so the
                 // whole warp takes the branch when any row needs it (rows that
-                // do not keep alpha = 1).
+                // do not keep alpha = 1).  The previous P.V of this stream is
+                // already complete (confirmed above).
                 const bool mine = mx > m_ref + kRescaleLog2;
                 if (__any_sync(0xffffffffu, mine)) {
                     const float alpha = mine ? ex2(m_ref - mx) : 1.0f;   // 0 when m_ref = -inf
-                    if (k > 0) {
-                        // O holds the P.V sums of this segment so far: wait for the
-                        // last of them, then scale the rows in tensor memory.
-                        const uint32_t jp = j - 1;
-                        if (!mbar_wait_warp(&p_empty[jp & 1], (jp >> 1) & 1, abort, a.dev_status)) { ok = false; break; }
-                        tc_fence_after();
+                    if (ks > 0) {
 #pragma unroll 1
                         for (int c = 0; c < HD / 32; ++c) {
                             uint32_t o[32];
-                            tmem_ld_32x32b_x32(t_lane + c * 32, o);
+                            tmem_ld_32x32b_x32(t_o + c * 32, o);
                             tmem_ld_wait();
 #pragma unroll
                             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                            tmem_st_32x32b_x32(t_lane + c * 32, o);
+                            tmem_st_32x32b_x32(t_o + c * 32, o);
                         }
                         tmem_st_wait();
                     }
@@ -430,78 +499,111 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m_ref = mx;
                     }
                 }
-                if (j >= 2 && !mbar_wait_warp(&p_empty[pb], ((j >> 1) & 1) ^ 1, abort, a.dev_status)) { ok = false; break; }
-                // p = 2^(s * scale_log2 - m_ref): one FFMA and one MUFU per key;
-                // masked keys (-inf) give 0.  A row with no visible key yet
-                // (m_ref = -inf) writes zeros.
-                uint32_t ph[kBN / 2];
+                // pass 2: p = 2^(s * scale_log2 - m_ref) (one FFMA and one MUFU
+                // per key; masked keys give 0; a row with no visible key yet,
+                // m_ref = -inf, writes zeros), split into hi = bf16(p) and
+                // lo = bf16(p - hi) and written over the same keys' S columns.
                 const float neg_m = -m_ref;
-                const float sc = a.scale_log2;
-                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-                if (m_ref != -INFINITY) {
+                const bool live = m_ref != -INFINITY;
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll 1
+                for (int q = 0; q < kBN / 32; ++q) {
+                    uint32_t x[32], pw[32];
+                    tmem_ld_32x32b_x32(t_s + 32 * q, x);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < kBN; c += 4) {
-                        const float p0 = ex2(fmaf(x[c], sc, neg_m));
-                        const float p1 = ex2(fmaf(x[c + 1], sc, neg_m));
-                        const float p2 = ex2(fmaf(x[c + 2], sc, neg_m));
-                        const float p3 = ex2(fmaf(x[c + 3], sc, neg_m));
-                        l0 += p0; l1 += p1; l2 += p2; l3 += p3;
-                        const __half2 h01 = __floats2half2_rn(p0, p1);
-                        const __half2 h23 = __floats2half2_rn(p2, p3);
-                        ph[c / 2] = *reinterpret_cast<const uint32_t *>(&h01);
-                        ph[c / 2 + 1] = *reinterpret_cast<const uint32_t *>(&h23);
+                    for (int c = 0; c < 32; c += 2) {
+                        const bool v0 = live && 32 * q + c < nvis;
+                        const bool v1 = live && 32 * q + c + 1 < nvis;
+                        const float p0 = v0 ? ex2(fmaf(__uint_as_float(x[c]), sc, neg_m)) : 0.f;
+                        const float p1 = v1 ? ex2(fmaf(__uint_as_float(x[c + 1]), sc, neg_m)) : 0.f;
+                        l0 += p0;
+                        l1 += p1;
+                        const __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
+                        const uint32_t hw = *reinterpret_cast<const uint32_t *>(&hb);
+                        const __nv_bfloat162 lb = __floats2bfloat162_rn(p0 - __uint_as_float(hw << 16),
+                                                                        p1 - __uint_as_float(hw & 0xFFFF0000u));
+                        // 16-key group gi = c / 16 of this chunk: hi words first, then lo
+                        const int gi = c >> 4, wi = (c & 15) >> 1;
+                        pw[gi * 16 + wi] = hw;
+                        pw[gi * 16 + 8 + wi] = *reinterpret_cast<const uint32_t *>(&lb);
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kBN / 2; ++c) ph[c] = 0u;
+                    tmem_st_32x32b_x32(t_s + 32 * q, pw);
                 }
-                l += (l0 + l1) + (l2 + l3);
-                uint8_t *prow = sP + pb * L::kP;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4 *>(prow + sw128_offset(rl, c)) =
-                        make_uint4(ph[4 * c], ph[4 * c + 1], ph[4 * c + 2], ph[4 * c + 3]);
-                fence_proxy_async_smem();
+                l += l0 + l1;
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[pb]);
+                if (lane == 0) mbar_arrive(&p_full[sm]);
             }
             if (!ok) break;
-            // segment end: O is complete once the last P.V has finished
-            const uint32_t jl = kg + n - 1;
-            if (!mbar_wait_warp(&p_empty[jl & 1], (jl >> 1) & 1, abort, a.dev_status)) break;
-            tc_fence_after();
-            float *dst;
-            if (seg.slot < 0) {
-                dst = a.out + ((static_cast<int64_t>(seg.b) * (a.D + 1) + i_row) * Hq + seg.h * a.G + g_row) * HD;
-            } else {
-                dst = a.part_o + ((static_cast<int64_t>(seg.slot) * a.nt + mt) * kBM + rl) * HD;
-            }
-            const float inv = (seg.slot < 0 && l > 0.f) ? 1.0f / l : 1.0f;
-#pragma unroll 1
-            for (int c = 0; c < HD / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld_32x32b_x32(t_lane + c * 32, o);
-                tmem_ld_wait();
-                if (row_ok) {
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        d4[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
-                                            __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
-                }
-            }
-            if (row_ok) {
-                if (seg.slot < 0) {
-                    if (a.lse)
-                        a.lse[(static_cast<int64_t>(seg.b) * (a.D + 1) + i_row) * Hq + seg.h * a.G + g_row] =
-                            (m_ref + __log2f(l)) * kLn2;
-                } else {
-                    a.part_ml[(static_cast<int64_t>(seg.slot) * a.nt + mt) * kBM + rl] = make_float2(m_ref, l);
-                }
-            }
+            // Segment end: each stream's O is final once its last P.V is done.
+            if (ks > 0 && !mbar_wait_warp(&p_empty[sm], (ns - 1) & 1, abort, a.dev_status)) break;
             tc_fence_before();
-            kg += n;
+            if (sm == 1) {
+                sML[rl] = make_float2(m_ref, l);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ml_ready);
+                // stream 0 reads this stream's O before it may be overwritten
+                if (!mbar_wait_warp(o_taken, si & 1, abort, a.dev_status)) break;
+                tc_fence_after();
+            } else {
+                if (!mbar_wait_warp(ml_ready, si & 1, abort, a.dev_status)) break;
+                tc_fence_after();
+                const bool has1 = n >= 2;
+                const float2 ml1 = sML[rl];
+                const float m1v = has1 ? ml1.x : -INFINITY;
+                const float M = fmaxf(m_ref, m1v);
+                const float w0 = m_ref == -INFINITY ? 0.f : ex2(m_ref - M);
+                const float w1 = m1v == -INFINITY ? 0.f : ex2(m1v - M);
+                const float lsum = w0 * l + (has1 ? w1 * ml1.y : 0.f);
+                float *dst;
+                if (seg.slot < 0) {
+                    dst = a.out + ((static_cast<int64_t>(seg.b) * (a.D + 1) + i_row) * Hq + seg.h * a.G + g_row) * HD;
+                } else {
+                    dst = a.part_o + ((static_cast<int64_t>(seg.slot) * a.nt + mt) * kBM + rl) * HD;
+                }
+                const float inv = (seg.slot < 0 && lsum > 0.f) ? 1.0f / lsum : 1.0f;
+                const float c0w = w0 * inv, c1w = w1 * inv;
+#pragma unroll 1
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o0[32], o1[32];
+                    tmem_ld_32x32b_x32(t_lane + c * 32, o0);
+                    if (has1) tmem_ld_32x32b_x32(t_lane + HD + c * 32, o1);
+                    tmem_ld_wait();
+                    if (row_ok) {
+                        float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            float4 v;
+                            v.x = __uint_as_float(o0[4 * e]) * c0w;
+                            v.y = __uint_as_float(o0[4 * e + 1]) * c0w;
+                            v.z = __uint_as_float(o0[4 * e + 2]) * c0w;
+                            v.w = __uint_as_float(o0[4 * e + 3]) * c0w;
+                            if (has1) {
+                                v.x += __uint_as_float(o1[4 * e]) * c1w;
+                                v.y += __uint_as_float(o1[4 * e + 1]) * c1w;
+                                v.z += __uint_as_float(o1[4 * e + 2]) * c1w;
+                                v.w += __uint_as_float(o1[4 * e + 3]) * c1w;
+                            }
+                            d4[e] = v;
+                        }
+                    }
+                }
+                if (row_ok) {
+                    if (seg.slot < 0) {
+                        if (a.lse)
+                            a.lse[(static_cast<int64_t>(seg.b) * (a.D + 1) + i_row) * Hq + seg.h * a.G + g_row] =
+                                (M + __log2f(lsum)) * kLn2;
+                    } else {
+                        a.part_ml[(static_cast<int64_t>(seg.slot) * a.nt + mt) * kBM + rl] = make_float2(M, lsum);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_taken);
+            }
+            ++si;
         }
     }
 
@@ -519,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // if group g's range begins inside a unit that started in an earlier group
 // and ends within g, g is that unit's last group and merges it.
 template <int HD>
-__global__ void __launch_bounds__(kThreads) attention_combine_kernel(const AttnArgs a)
+__global__ void __launch_bounds__(kCombineThreads) attention_combine_kernel(const AttnArgs a)
 {
     __shared__ PlanShared ps;
     const int g = blockIdx.x, mt = blockIdx.y;
@@ -533,7 +635,7 @@ __global__ void __launch_bounds__(kThreads) attention_combine_kernel(const AttnA
     const int64_t total = ps.total;
     const int g_first = group_of(ub, total, ge);
     const int Hq = a.Hkv * a.G;
-    for (int rl = threadIdx.x; rl < kBM; rl += kThreads) {
+    for (int rl = threadIdx.x; rl < kBM; rl += kCombineThreads) {
         const int r = mt * kBM + rl;
         if (r >= a.R) continue;
         const int i = r / a.G, gg = r % a.G;
@@ -584,7 +686,7 @@ cudaError_t run(const CUtensorMap &tk, const CUtensorMap &tv, const AttnArgs &a,
     k<<<a.groups * a.nt, kThreads, L::kBytes, st>>>(tk, tv, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attention_combine_kernel<HD><<<dim3(a.groups, a.nt), kThreads, 0, st>>>(a);
+    attention_combine_kernel<HD><<<dim3(a.groups, a.nt), kCombineThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 

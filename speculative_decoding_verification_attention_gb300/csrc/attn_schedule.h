@@ -1,7 +1,7 @@
 // Split of the verify-attention KV stream across CTA groups (host and
 // device share this code).
 //
-// Unit = (sequence b, KV head h).  Unit (b, h) owns nk(b) = ceil(L_b / 64)
+// Unit = (sequence b, KV head h).  Unit (b, h) owns nk(b) = ceil(L_b / 128)
 // key tiles; units are concatenated in (b, h) order into one stream of T
 // tiles.  Group g processes the contiguous range [T*g/n, T*(g+1)/n) of that
 // stream, so every group does the same number of tile steps whatever the
@@ -22,7 +22,7 @@
 
 namespace spec {
 
-constexpr int kKeyTile = 64;        // keys per tile
+constexpr int kKeyTile = 128;       // keys per tile
 constexpr int kMinTilesPerGroup = 4;
 
 // Tiles of sequence b, or 0 when kv_len is outside [1 + D, max_len].

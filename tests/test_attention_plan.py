@@ -29,7 +29,8 @@ CASES = [
 def test_plan_covers_each_tile_once(lens, D, Hkv, groups):
     kv = np.array(lens, np.int32)
     seg = sv.attention_plan(kv, D, Hkv, groups)
-    nk = np.where(kv >= 1 + D, (kv.astype(np.int64) + 63) // 64, 0)
+    kt = sv.ATTENTION_KEY_TILE
+    nk = np.where(kv >= 1 + D, (kv.astype(np.int64) + kt - 1) // kt, 0)
     covered = {}
     per_group = {}
     slots = set()
