@@ -10,12 +10,12 @@
 // Kernel structure (one CTA per SM, 8 warps):
 //   warp 0      TMA producer: K and V tiles of 128 keys, page by page, into a
 //               ring of shared-memory stages (128-byte swizzle).
-//   warp 1      tcgen05 issuer: S = Q K^T (bf16, M = 128 rows x N = 128 keys,
-//               fp32 in TMEM) and O += P V (P read from TMEM, fp32
-//               accumulator in TMEM), issued as soon as their inputs are
-//               ready.
-//   warps 2-3   load the 128 query rows of each segment into shared memory;
-//               zero the V rows of keys past the end of a sequence.
+//   warp 1      tcgen05 issuer of S = Q K^T (bf16, M = 128 rows x N = 128
+//               keys, fp32 in TMEM).
+//   warp 2      loads the 128 query rows of each segment into shared memory
+//               and zeroes the V rows of keys past the end of a sequence.
+//   warp 3      tcgen05 issuer of O += P V (P read from TMEM, fp32
+//               accumulator in TMEM), as soon as a stream's P is ready.
 //   warps 4-11  softmax, as two streams that take alternate key tiles (each
 //               with its own S buffers and O accumulator in TMEM): one thread
 //               per query row reads its S row from TMEM, masks, keeps an
@@ -30,8 +30,8 @@
 // own CTA of the same group, so the same K/V tiles are read concurrently
 // and served from L2.
 //
-// P is split as P = hi + lo with hi = bf16(P) and lo = bf16(P - hi) (about
-// 16 significant bits), and O += hi V + lo V takes two bf16 MMAs that read
+// P is split as P = hi + lo with hi = P truncated to bf16 and
+// lo = bf16(P - hi) (about 16 significant bits), and O += hi V + lo V takes two bf16 MMAs that read
 // the A operand straight from tensor memory.  Rounding P to a single bf16
 // would cost about 2e-3 relative error in O; the pair keeps it near 1e-5
 // and leaves V in bf16 as stored.
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < S; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
-            mbar_init(&v_ready[i], 64);
+            mbar_init(&v_ready[i], 32);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&p_full[i], 4);
             mbar_init(&p_empty[i], 1);
         }
-        mbar_init(q_full, 64);
+        mbar_init(q_full, 32);
         mbar_init(q_empty, 1);
         mbar_init(ml_ready, 4);
         mbar_init(o_taken, 4);
@@ -261,11 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (uint32_t i = first; i < kg; ++i) mbar_wait_drain(&kv_full[i % S], (i / S) & 1, 100000000ull);
             }
         }
-    } else if (warp == 1) {
-        // --------------------------------------------- tcgen05 issuer
-        // Tile k of a segment belongs to stream k & 1.  The issuer keeps one
-        // cursor for S = QK^T (all tiles in order) and one per stream for
-        // O += PV, and issues whichever operation's inputs are ready.
+    } else if (warp == 1 || warp == 3) {
+        // -------------------------------------------- tcgen05 issuers
+        // Tile k of a segment belongs to stream k & 1.  Warp 1 issues
+        // S = QK^T for all tiles in order; warp 3 issues O += PV with one
+        // cursor per stream, whichever stream's P is ready first.  Two
+        // issuing threads keep a ready P.V from queueing behind a QK issue.
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_f16(kBM, kBN, 1, 0, 0);
             constexpr uint32_t idesc_pv = idesc_f16(kBM, HD, 1, 0, 1);
@@ -303,10 +304,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     settle(k_restart);
                 }
             };
+            const bool qk_role = warp == 1;
             Cursor cq, cp[2];
-            cq.start(walk, 0, 1);
-            cp[0].start(walk, 0, 2);
-            cp[1].start(walk, 1, 2);
+            if (qk_role) {
+                cq.start(walk, 0, 1);
+                cp[0].valid = cp[1].valid = false;
+            } else {
+                cq.valid = false;
+                cp[0].start(walk, 0, 2);
+                cp[1].start(walk, 1, 2);
+            }
             uint32_t nqk[2] = {0, 0}, npv[2] = {0, 0};
             unsigned long long t_idle = 0;
             uint32_t spins = 0;
@@ -370,15 +377,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp < 4) {
-        // ---------------------------- Q loader + V tail clearing (warps 2-3)
-        const int ct = threadIdx.x - 64;       // 0..63
+    } else if (warp == 2) {
+        // ------------------------------- Q loader + V tail clearing (warp 2)
+        const int ct = lane;
         uint32_t kg = 0, si = 0;
         bool ok = true;
         while (ok && walk.next(seg)) {
             if (si >= 1 && !mbar_wait(q_empty, (si - 1) & 1, abort, a.dev_status)) break;
-            for (int rr = 0; rr < 2; ++rr) {
-                const int rl = ct + rr * 64;
+            for (int rr = 0; rr < 4; ++rr) {
+                const int rl = ct + rr * 32;
                 const int r = mt * kBM + rl;
                 if (r < a.R) {
                     const int i = r / a.G, gg = r % a.G;
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nvalid = min(kBN, Lb - t * kBN);
                 if (nvalid < kBN) {
                     uint8_t *vt = sV + st * L::kKV;
-                    for (int idx = ct; idx < L::kSub * kBN * 8; idx += 64) {
+                    for (int idx = ct; idx < L::kSub * kBN * 8; idx += 32) {
                         const int row = (idx & (kBN * 8 - 1)) >> 3;
                         if (row >= nvalid) *reinterpret_cast<uint4 *>(vt + idx * 16) = make_uint4(0, 0, 0, 0);
                     }
@@ -426,6 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rl = quad * 32 + lane;
         const int r = mt * kBM + rl;
         const bool row_ok = r < a.R;
+        // a warp whose 32 rows are all padding (G(1+D) not a multiple of
+        // 128) only has to write P = 0
+        const bool pad_warp = mt * kBM + quad * 32 >= a.R;
         const int i_row = row_ok ? r / a.G : 0;
         const int g_row = row_ok ? r % a.G : 0;
         const uint32_t t_lane = tmem + ((quad * 32) << 16);
@@ -447,6 +457,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (the issuer waits for that before S = QK^T), so this confirms
                 // that phase at once and keeps the p_empty waits in step.
                 if (ns >= 1 && !mbar_wait_warp(&p_empty[sm], (ns - 1) & 1, abort, a.dev_status)) { ok = false; break; }
+                if (pad_warp) {
+                    uint32_t z[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) z[c] = 0u;
+#pragma unroll
+                    for (int q = 0; q < kBN / 32; ++q) tmem_st_32x32b_x32(t_s + 32 * q, z);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[sm]);
+                    continue;
+                }
                 const int key0 = (seg.tile_begin + k) * kBN;
                 const int nvis = limit - key0;            // keys [0, nvis) of the tile are visible
                 // pass 1: row max of the raw scores
@@ -501,28 +523,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // pass 2: p = 2^(s * scale_log2 - m_ref) (one FFMA and one MUFU
                 // per key; masked keys give 0; a row with no visible key yet,
-                // m_ref = -inf, writes zeros), split into hi = bf16(p) and
-                // lo = bf16(p - hi) and written over the same keys' S columns.
+                // m_ref = -inf, writes zeros), split into hi + lo bf16 and
+                // written over the same keys' S columns.
                 const float neg_m = -m_ref;
                 const bool live = m_ref != -INFINITY;
+                const bool full = live && nvis >= kBN;   // no key of this tile is masked
                 float l0 = 0.f, l1 = 0.f;
 #pragma unroll 1
                 for (int q = 0; q < kBN / 32; ++q) {
                     uint32_t x[32], pw[32];
                     tmem_ld_32x32b_x32(t_s + 32 * q, x);
                     tmem_ld_wait();
+                    if (!full) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (!live || 32 * q + c >= nvis) x[c] = __float_as_uint(-INFINITY);
+                    }
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
-                        const bool v0 = live && 32 * q + c < nvis;
-                        const bool v1 = live && 32 * q + c + 1 < nvis;
-                        const float p0 = v0 ? ex2(fmaf(__uint_as_float(x[c]), sc, neg_m)) : 0.f;
-                        const float p1 = v1 ? ex2(fmaf(__uint_as_float(x[c + 1]), sc, neg_m)) : 0.f;
+                        // masked keys: fma(-inf, sc, -m) = -inf and 2^-inf = 0;
+                        // rows with m_ref = -inf have every key masked
+                        const float p0 = ex2(fmaf(__uint_as_float(x[c]), sc, live ? neg_m : 0.f));
+                        const float p1 = ex2(fmaf(__uint_as_float(x[c + 1]), sc, live ? neg_m : 0.f));
                         l0 += p0;
                         l1 += p1;
-                        const __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
-                        const uint32_t hw = *reinterpret_cast<const uint32_t *>(&hb);
-                        const __nv_bfloat162 lb = __floats2bfloat162_rn(p0 - __uint_as_float(hw << 16),
-                                                                        p1 - __uint_as_float(hw & 0xFFFF0000u));
+                        // hi = p truncated to bf16 (exact: the top half of p),
+                        // lo = bf16(p - hi): hi + lo carries ~16 bits of p
+                        const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+                        const uint32_t hw = __byte_perm(b0, b1, 0x7632);
+                        const __nv_bfloat162 lb = __floats2bfloat162_rn(p0 - __uint_as_float(b0 & 0xFFFF0000u),
+                                                                        p1 - __uint_as_float(b1 & 0xFFFF0000u));
                         // 16-key group gi = c / 16 of this chunk: hi words first, then lo
                         const int gi = c >> 4, wi = (c & 15) >> 1;
                         pw[gi * 16 + wi] = hw;
@@ -612,6 +642,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (*abort && threadIdx.x == 32) {
         umma_commit(drain);
         mbar_wait_drain(drain, 0, 100000000ull);
+    }
+    __syncthreads();
+    if (*abort && threadIdx.x == 96) {
+        umma_commit(drain);
+        mbar_wait_drain(drain, 1, 100000000ull);
     }
     __syncthreads();
     if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, kCols); }
