@@ -52,6 +52,23 @@ def peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def attention_traffic_ratio():
+    """DRAM bytes / algorithmic bytes of the attention kernel from the last
+    ncu capture (profiles/verify_attention_traffic.json), or None if the
+    kernel sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "verify_attention_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_attention_gb300", "csrc")
+    src = "".join(open(os.path.join(csrc, n)).read() for n in ("attention.cu", "attn_schedule.h", "common.cuh"))
+    if hashlib.sha256(src.encode()).hexdigest() != rec.get("source_sha256"):
+        return None
+    return float(rec["ratio"])
+
+
 # ---------------------------------------------------------------- workload
 class Workload:
     """Device-resident inputs of one verification step."""
@@ -254,6 +271,7 @@ def gpu_arm(args, rank, world):
     e2e = e2e_arm(sv, wl, ws, outs, dev, args.e2e_steps) if args.e2e_steps > 0 else None
 
     pk = peaks()
+    traffic_ratio = attention_traffic_ratio()
     attn_ms = float(per[:, 0].mean())
     gemm_ms = float(per[:, 1].mean())
     greedy_ms = float(per[:, 2].mean())
@@ -274,7 +292,7 @@ def gpu_arm(args, rank, world):
                    "kv_cache_gb": 2 * wl.sum_L * w["Hkv"] * w["head_dim"] * 2 / 1e9,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (512 MB write, untimed)",
-                   "precision": "bf16 inputs, fp32 accumulate, fp16 P in P.V, fp32 attention "
+                   "precision": "bf16 inputs, fp32 accumulate, P as bf16 hi+lo in P.V, fp32 attention "
                                 "output; acceptance exact (fp64 products, fixed-point sums)"},
         "kernels": {
             "attention": {"ms": attn_ms, "GB_per_s": attn_gbs,
@@ -294,7 +312,10 @@ def gpu_arm(args, rank, world):
         },
         "roofline": {"kernel": "verify_attention (main + partial merge)", "bound": "hbm",
                      "achieved": attn_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": attn_gbs / pk["hbm_gbs"], "traffic": None,
+                     "frac": attn_gbs / pk["hbm_gbs"],
+                     "traffic": (None if traffic_ratio is None else traffic_ratio * wl.attention_bytes()),
+                     "traffic_note": "DRAM read+write bytes per launch, from an ncu capture of a smaller "
+                                     "case scaled by algorithmic bytes (profiles/verify_attention_small_B4_L32768_D7.md)",
                      "peak_source": pk["source"] + " (copy bandwidth, of measured)"},
         "gpu_launches": 5 * K,
         "wall_s_timed_region": wall,
@@ -489,7 +510,7 @@ def case_lines(args):
     if args.workload in ("gemm", "all"):
         N = K = 6144
         w = (torch.randn((N, K), device=dev) * 0.02).to(torch.bfloat16)
-        for M in (8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096):
+        for M in ((args.gemm_m,) if args.gemm_m else (8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096)):
             x = torch.randn((M, K), device=dev).to(torch.bfloat16)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ms = time_launches(lambda: sv.verify_gemm(x, w, y=y), args.warmup, args.steps, flush)
@@ -543,6 +564,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-m", type=int, default=0, help="gemm workload: only this M")
     ap.add_argument("--workload", default="step",
                     choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small"],
                     help="step: the headline line; others print one secondary JSON line per case")
