@@ -186,6 +186,24 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# ------------------------------------------------------------ multi-rank
+def max_over_ranks(x, world, device=None):
+    """Max of a per-rank scalar over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(tokens_per_rank, ms_per_step_max, world):
+    """Whole-job tokens/s: every rank processes its own batch (replicas), the
+    job's step time is the slowest rank's."""
+    return tokens_per_rank * world / (ms_per_step_max * 1e-3)
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_step(sv, wl, ws, outs, ev=None):
     """Enqueue one verification step; ev: optional list of 5 event pairs."""
@@ -259,11 +277,7 @@ def gpu_arm(args, rank, world):
         dist.barrier()
     per = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(4)] for i in range(K)])
     step_ms = per.sum(axis=1)
-    ms_step = float(step_ms.mean())
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(float(step_ms.mean()), world, dev)
     ng, ns = outs["ng"].cpu().numpy(), outs["ns"].cpu().numpy()
     g_bytes, s_bytes = accept_bytes(ng, ns, wl.B, wl.D, wl.V)
 
@@ -278,9 +292,9 @@ def gpu_arm(args, rank, world):
     sample_ms = float(per[:, 3].mean())
     attn_gbs = wl.attention_bytes() / (attn_ms * 1e-3) / 1e9
     gemm_tf = wl.gemm_flops() / (gemm_ms * 1e-3) / 1e12
-    tokens = wl.B * (1 + wl.D) * world
     line = {
-        "metric": METRIC, "value": tokens / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": aggregate_throughput(wl.B * (1 + wl.D), ms_step, world),
+        "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random bf16 KV/Q/W, softmax probabilities of random logits)",
@@ -428,7 +442,7 @@ def reference_arm(args, rank, world):
     times = []
     desc, nthreads = "", 0
     for i in range(args.warmup + args.steps):
-        t, desc, nthreads = cpu_sample_time(budget_s=3.0)
+        t, desc, nthreads = cpu_sample_time(budget_s=args.cpu_budget_s)
         if i >= args.warmup:
             times.append(t)
     ms = 1e3 * float(np.mean(times))
@@ -565,6 +579,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--gemm-m", type=int, default=0, help="gemm workload: only this M")
+    ap.add_argument("--cpu-budget-s", type=float, default=3.0,
+                    help="reference arm: seconds of oracle attention work sampled per step")
     ap.add_argument("--workload", default="step",
                     choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small"],
                     help="step: the headline line; others print one secondary JSON line per case")
