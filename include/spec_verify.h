@@ -220,12 +220,16 @@ spec_status_t spec_accept_greedy(const float *p, const int32_t *draft, int B, in
  *   u_acc    device, fp32 [B][D] in [0, 1).
  *   u_res    device, fp32 [B] in [0, 1).
  *   n_accepted, token   device, int32 [B].
+ *   workspace  device, spec_accept_sample_workspace_size(B, V) bytes,
+ *              256-byte aligned; scratch only, needs no initialisation.
  * Supported set: B >= 0, 0 <= D <= 63, 1 <= V <= 2^26.
  * ---------------------------------------------------------------------- */
+size_t spec_accept_sample_workspace_size(int B, int V);
+
 spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *draft,
                                  const float *u_acc, const float *u_res, int B, int D, int V,
-                                 int32_t *n_accepted, int32_t *token, uint32_t *dev_status,
-                                 void *stream);
+                                 int32_t *n_accepted, int32_t *token, void *workspace,
+                                 size_t workspace_bytes, uint32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
  * Host-side planning helper (no GPU work).

@@ -18,7 +18,7 @@ import threading
 
 __all__ = [
     "SpecError", "library", "library_path", "verify_attention", "verify_gemm",
-    "accept_greedy", "accept_sample", "attention_workspace_size",
+    "accept_greedy", "accept_sample", "accept_sample_workspace_size", "attention_workspace_size",
     "gemm_workspace_size", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
 ]
 
@@ -29,7 +29,7 @@ EXPORTED_SYMBOLS = (
     "spec_status_string", "spec_version", "spec_verify_attention_workspace_size",
     "spec_verify_attention", "spec_verify_gemm_workspace_size", "spec_verify_gemm",
     "spec_accept_greedy", "spec_accept_sample", "spec_verify_attention_plan",
-    "spec_verify_attention_noalloc",
+    "spec_verify_attention_noalloc", "spec_accept_sample_workspace_size",
 )
 
 DEV_STATUS_BITS = {
@@ -78,7 +78,9 @@ def library():
             lib.spec_verify_gemm.restype = I
             lib.spec_accept_greedy.argtypes = [P, P, I, I, I, P, P, P, P]
             lib.spec_accept_greedy.restype = I
-            lib.spec_accept_sample.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P]
+            lib.spec_accept_sample_workspace_size.argtypes = [I, I]
+            lib.spec_accept_sample_workspace_size.restype = S
+            lib.spec_accept_sample.argtypes = [P, P, P, P, P, I, I, I, P, P, P, S, P, P]
             lib.spec_accept_sample.restype = I
             lib.spec_verify_attention_noalloc.argtypes = [P, P, P, I, P, I, P, I, I, I, I, I, I, F,
                                                           P, P, P, P]
@@ -215,8 +217,12 @@ def accept_greedy(p, draft, n_accepted=None, token=None, dev_status=None, stream
     return n_accepted, token
 
 
-def accept_sample(p, q, draft, u_acc, u_res, n_accepted=None, token=None, dev_status=None,
-                  stream=None):
+def accept_sample_workspace_size(B, V):
+    return int(library().spec_accept_sample_workspace_size(B, V))
+
+
+def accept_sample(p, q, draft, u_acc, u_res, n_accepted=None, token=None, workspace=None,
+                  dev_status=None, stream=None):
     """Stochastic acceptance with residual resampling (explicit uniforms)."""
     import torch
     B, D1, V = p.shape
@@ -224,12 +230,16 @@ def accept_sample(p, q, draft, u_acc, u_res, n_accepted=None, token=None, dev_st
         n_accepted = torch.empty(B, dtype=torch.int32, device=p.device)
     if token is None:
         token = torch.empty(B, dtype=torch.int32, device=p.device)
+    need = accept_sample_workspace_size(B, V)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=p.device)
     st = library().spec_accept_sample(
         _dev(p, "p", torch.float32), _dev(q, "q", torch.float32, allow_none=True),
         _dev(draft, "draft", torch.int32, allow_none=True),
         _dev(u_acc, "u_acc", torch.float32, allow_none=True), _dev(u_res, "u_res", torch.float32),
         B, D1 - 1, V, _dev(n_accepted, "n_accepted", torch.int32),
-        _dev(token, "token", torch.int32), _dev(dev_status, "dev_status", allow_none=True),
-        _stream(stream))
+        _dev(token, "token", torch.int32), _dev(workspace, "workspace", allow_none=True),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
     _check(st, "spec_accept_sample")
     return n_accepted, token

@@ -54,10 +54,16 @@ spec_status_t spec_accept_greedy(const float *p, const int32_t *draft, int B, in
                                           static_cast<cudaStream_t>(stream)));
 }
 
+size_t spec_accept_sample_workspace_size(int B, int V)
+{
+    if (B < 0 || V < 1 || V > (1 << 26)) return 0;
+    return accept_sample_workspace_bytes(B, V);
+}
+
 spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *draft,
                                  const float *u_acc, const float *u_res, int B, int D, int V,
-                                 int32_t *n_accepted, int32_t *token, uint32_t *dev_status,
-                                 void *stream)
+                                 int32_t *n_accepted, int32_t *token, void *workspace,
+                                 size_t workspace_bytes, uint32_t *dev_status, void *stream)
 {
     if (B < 0 || D < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
     if (D > kMaxDraft || V > (1 << 26)) return SPEC_ERR_UNSUPPORTED;
@@ -66,9 +72,11 @@ spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *
     if (D > 0 && (!q || !draft || !u_acc)) return SPEC_ERR_INVALID_ARG;
     if (!aligned(p, 4) || (q && !aligned(q, 4)) || !aligned(n_accepted, 4) || !aligned(token, 4))
         return SPEC_ERR_INVALID_ARG;
-    if (static_cast<long long>(B) * 8 > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * 8 > 0x7fffffffLL || B > 65535) return SPEC_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < accept_sample_workspace_bytes(B, V) || !aligned(workspace, 256))
+        return SPEC_ERR_WORKSPACE;
     return from_cuda(launch_accept_sample(p, q, draft, u_acc, u_res, B, D, V, n_accepted, token,
-                                          dev_status, static_cast<cudaStream_t>(stream)));
+                                          workspace, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

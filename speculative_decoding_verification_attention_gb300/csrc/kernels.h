@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace spec {
@@ -11,9 +12,11 @@ constexpr int kMaxDraft = 63;
 cudaError_t launch_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,
                                  int32_t *n_acc, int32_t *token, cudaStream_t st);
 
+size_t accept_sample_workspace_bytes(int B, int V);
+
 cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *draft,
                                  const float *u_acc, const float *u_res, int B, int D, int V,
-                                 int32_t *n_acc, int32_t *token, uint32_t *dev_status,
-                                 cudaStream_t st);
+                                 int32_t *n_acc, int32_t *token, void *workspace,
+                                 uint32_t *dev_status, cudaStream_t st);
 
 }  // namespace spec

@@ -62,12 +62,17 @@ def test_accept_greedy_rejects_bad_arguments(lib):
 
 def test_accept_sample_rejects_bad_arguments(lib):
     f = lib.spec_accept_sample
-    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 3, 0, FAKE, FAKE, None, None) == INVALID
-    assert f(FAKE, None, FAKE, FAKE, FAKE, 1, 3, 10, FAKE, FAKE, None, None) == INVALID
-    assert f(FAKE, FAKE, FAKE, None, FAKE, 1, 3, 10, FAKE, FAKE, None, None) == INVALID
-    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 3, 10, FAKE, FAKE, None, None) == INVALID
-    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 70, 10, FAKE, FAKE, None, None) == UNSUPPORTED
-    assert f(None, None, None, None, None, 0, 3, 10, None, None, None, None) == 0
+    W = 1 << 20
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 3, 0, FAKE, FAKE, FAKE, W, None, None) == INVALID
+    assert f(FAKE, None, FAKE, FAKE, FAKE, 1, 3, 10, FAKE, FAKE, FAKE, W, None, None) == INVALID
+    assert f(FAKE, FAKE, FAKE, None, FAKE, 1, 3, 10, FAKE, FAKE, FAKE, W, None, None) == INVALID
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 3, 10, FAKE, FAKE, FAKE, W, None, None) == INVALID
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 70, 10, FAKE, FAKE, FAKE, W, None, None) == UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 3, 10, FAKE, FAKE, None, W, None, None) == WORKSPACE
+    need = lib.spec_accept_sample_workspace_size(4, 1000)
+    assert need > 0
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 3, 1000, FAKE, FAKE, FAKE, need - 1, None, None) == WORKSPACE
+    assert f(None, None, None, None, None, 0, 3, 10, None, None, None, 0, None, None) == 0
 
 
 def test_gemm_rejects_bad_arguments(lib):
