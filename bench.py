@@ -248,14 +248,16 @@ def gpu_arm(args, rank, world):
     ws = dict(attn=torch.empty(max(256, sv.attention_workspace_size(wl.B, wl.D, w["Hkv"], w["G"],
                                                                         w["head_dim"], max_len)),
                                dtype=torch.uint8, device=dev),
-              gemm=None,
+              gemm=torch.zeros(max(256, sv.gemm_workspace_size(wl.x.shape[0], wl.w.shape[0],
+                                                               wl.x.shape[1])),
+                               dtype=torch.uint8, device=dev),
               accept=torch.empty(sv.accept_sample_workspace_size(wl.B, wl.V), dtype=torch.uint8,
                                  device=dev))
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     for i in range(args.warmup):
-        flush.fill_(i & 0xFF)
+        flush(i)
         run_step(sv, wl, ws, outs)
     torch.cuda.synchronize()
 
@@ -268,7 +270,7 @@ def gpu_arm(args, rank, world):
     t_wall = time.perf_counter()
     with ClockSampler(clock_path) as clk:
         for i in range(K):
-            flush.fill_((i + 7) & 0xFF)          # evict L2 between steps (not timed)
+            flush(i + 7)                         # evict L2 between steps (not timed)
             run_step(sv, wl, ws, outs, evs[i])
         torch.cuda.synchronize()
         # stretch the sampled window so a short run still yields samples
@@ -307,7 +309,7 @@ def gpu_arm(args, rank, world):
                    "tokens_per_step_per_gpu": wl.B * (1 + wl.D), "sum_kv_len": wl.sum_L,
                    "kv_cache_gb": 2 * wl.sum_L * w["Hkv"] * w["head_dim"] * 2 / 1e9,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between steps (512 MB write, untimed)",
+                   "l2": "flushed between steps (512 MB write + 256 MB read, untimed)",
                    "precision": "bf16 inputs, fp32 accumulate, P as bf16 hi+lo in P.V, fp32 attention "
                                 "output; acceptance exact (fp64 products, fixed-point sums)"},
         "kernels": {
@@ -365,7 +367,7 @@ def e2e_arm(sv, wl, ws, outs, dev, steps):
             dst[k].copy_(host[k], non_blocking=True)
         sv.verify_attention(dst["q"], a.k_pages, a.v_pages, dst["bt"], dst["kv"], wl.D, Hkv, G,
                             out=outs["o"], lse=outs["lse"], workspace=ws["attn"])
-        sv.verify_gemm(dst["x"], wl.w, y=outs["y"])
+        sv.verify_gemm(dst["x"], wl.w, y=outs["y"], workspace=ws["gemm"])
         sv.accept_greedy(dst["p"], dst["dg"], n_accepted=outs["ng"], token=outs["tg"])
         sv.accept_sample(dst["p"], dst["qd"], dst["ds"], dst["ua"], dst["ur"],
                          n_accepted=outs["ns"], token=outs["ts"], workspace=ws["accept"])
@@ -458,19 +460,35 @@ def reference_arm(args, rank, world):
 
 
 # ------------------------------------------------------ single-kernel cases
+class L2Flush:
+    """Evicts L2 between timed launches (untimed): writes a 512 MB buffer
+    (> the 129 MB L2), then reads a 256 MB one so that the lines left in L2
+    are clean -- otherwise the next kernel would pay for writing back the
+    flush's own dirty lines."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+
+    def __call__(self, i):
+        self.w.fill_(i & 0xFF)
+        self.r.sum()
+
+
 def time_launches(fn, warmup, steps, flush=None):
     """Mean device time (ms) of fn() over `steps` launches after `warmup`,
     flushing L2 between launches when a flush buffer is given."""
     import torch
     for i in range(warmup):
         if flush is not None:
-            flush.fill_(i & 0xFF)
+            flush(i)
         fn()
     torch.cuda.synchronize()
     ts = []
     for i in range(steps):
         if flush is not None:
-            flush.fill_((i + 3) & 0xFF)
+            flush(i + 3)
         # keep the GPU busy (~0.5 ms, outside the timed events) while the host
         # enqueues the launch, so the events measure device time only
         torch.cuda._sleep(1_000_000)
@@ -492,7 +510,7 @@ def case_lines(args):
     sv.library()
     dev = torch.device("cuda", 0)
     pk = peaks()
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     lines = []
 
     def attention_case(name, B, Hkv, G, D, L, seed):
@@ -532,11 +550,14 @@ def case_lines(args):
         for M in ((args.gemm_m,) if args.gemm_m else (8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096)):
             x = torch.randn((M, K), device=dev).to(torch.bfloat16)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            ms = time_launches(lambda: sv.verify_gemm(x, w, y=y), args.warmup, args.steps, flush)
+            wsg = torch.zeros(max(256, sv.gemm_workspace_size(M, N, K)), dtype=torch.uint8, device=dev)
+            ms = time_launches(lambda: sv.verify_gemm(x, w, y=y, workspace=wsg), args.warmup,
+                               args.steps, flush)
             tf = 2 * M * N * K / (ms * 1e-3) / 1e12
             by = 2 * (M * K + N * K + M * N)
             lines.append({"case": f"gemm M{M} N{N} K{K}", "kernel": "verify_gemm", "M": M, "ms": ms,
                           "TFLOP_per_s": tf, "frac_tensor": tf / pk["bf16_tflops_sustained"],
+                          "frac_tensor_burst": tf / pk["bf16_tflops"],
                           "GB_per_s": by / (ms * 1e-3) / 1e9,
                           "frac_hbm": by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]})
     if args.workload in ("accept", "all", "accept-one"):

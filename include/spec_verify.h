@@ -165,8 +165,15 @@ spec_status_t spec_verify_attention_noalloc(const void *q_bf16, const void *k_pa
  *            16-byte aligned.
  *   y_bf16   device, bf16 [M][N] row-major, 16-byte aligned.
  * Supported set: 1 <= M <= 65536, N a multiple of 128, K a multiple of 64.
- * workspace: spec_verify_gemm_workspace_size(M, N, K) bytes (may be 0;
- * device, 256-byte aligned; scratch only).
+ * workspace: spec_verify_gemm_workspace_size(M, N, K) bytes of device
+ * memory, 256-byte aligned, owned by the caller.  It holds one ready flag
+ * per CTA (the first 1024 bytes) and the fp32 partial tiles of the
+ * stream-K split: zero it once before its first use (cudaMemset); every
+ * call that completes leaves the flags zero again, also under CUDA-graph
+ * replay.  Calls that share a
+ * workspace must not overlap in time.  A smaller workspace returns
+ * SPEC_ERR_WORKSPACE.  The size depends on the current device's SM count
+ * (without a device it is sized for 256 SMs).
  * ---------------------------------------------------------------------- */
 size_t spec_verify_gemm_workspace_size(int M, int N, int K);
 
@@ -247,6 +254,29 @@ spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *
 
 int spec_verify_attention_plan(int B, const int32_t *kv_len_host, int D, int Hkv,
                                int num_groups, int32_t *segments, int max_segments);
+
+/* ------------------------------------------------------------------------
+ * Host-side view of how spec_verify_gemm splits the work (no counterpart
+ * on the pages; launches nothing, needs no device).
+ *
+ * The work is split into units over at most num_sms SMs, one CTA per SM.
+ *  - M > 256: a unit is a pair of CTAs (a thread-block cluster of 2); pair
+ *    tile t covers output rows (t % tiles_mp) * 256 and columns
+ *    (t / tiles_mp) * BN, tiles_mp = ceil(ceil(M / 128) / 2), 128 rows per
+ *    CTA, both CTAs sharing each w tile.
+ *  - M <= 256: a unit is one CTA; tile t covers the 128 w rows (output
+ *    columns) t * 128 .. t * 128 + 127 for all M rows, which are padded to
+ *    BN in {32, 64, 128, 256} on the MMA side.
+ * Each unit walks a list of segments (a tile and a range [kb0, kb1) of its
+ * 64-wide k-blocks).  Writes, for each segment in unit order, the row
+ * (unit, tile, kb0, kb1, last, BN) into segments[6 * i ..] (int32, host
+ * memory), where last is, for a segment with kb0 == 0, the last unit
+ * holding a later piece of the same tile (the unit itself when the tile is
+ * whole), and -1 otherwise.  Returns the number of segments (rows beyond
+ * max_segments are counted, not written), or -1 for invalid arguments.
+ * ---------------------------------------------------------------------- */
+int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments,
+                          int max_segments);
 
 #ifdef __cplusplus
 }

@@ -19,7 +19,7 @@ import threading
 __all__ = [
     "SpecError", "library", "library_path", "verify_attention", "verify_gemm",
     "accept_greedy", "accept_sample", "accept_sample_workspace_size", "attention_workspace_size",
-    "gemm_workspace_size", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
+    "gemm_workspace_size", "gemm_plan", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -29,7 +29,7 @@ EXPORTED_SYMBOLS = (
     "spec_status_string", "spec_version", "spec_verify_attention_workspace_size",
     "spec_verify_attention", "spec_verify_gemm_workspace_size", "spec_verify_gemm",
     "spec_accept_greedy", "spec_accept_sample", "spec_verify_attention_plan",
-    "spec_verify_attention_noalloc", "spec_accept_sample_workspace_size",
+    "spec_verify_attention_noalloc", "spec_accept_sample_workspace_size", "spec_verify_gemm_plan",
 )
 
 DEV_STATUS_BITS = {
@@ -87,6 +87,8 @@ def library():
             lib.spec_verify_attention_noalloc.restype = I
             lib.spec_verify_attention_plan.argtypes = [I, P, I, I, I, P, I]
             lib.spec_verify_attention_plan.restype = I
+            lib.spec_verify_gemm_plan.argtypes = [I, I, I, I, P, I]
+            lib.spec_verify_gemm_plan.restype = I
             _lib = lib
     return _lib
 
@@ -180,8 +182,25 @@ def gemm_workspace_size(M, N, K):
     return int(library().spec_verify_gemm_workspace_size(M, N, K))
 
 
+def gemm_plan(M, N, K, num_sms):
+    """Segments (cta, tile, kb0, kb1, last, BN) of the stream-K split."""
+    import numpy as np
+    lib = library()
+    n = lib.spec_verify_gemm_plan(M, N, K, num_sms, None, 0)
+    if n < 0:
+        raise ValueError("spec_verify_gemm_plan rejected its arguments")
+    seg = np.zeros((max(n, 1), 6), np.int32)
+    lib.spec_verify_gemm_plan(M, N, K, num_sms, seg.ctypes.data_as(ctypes.c_void_p), n)
+    return seg[:n]
+
+
 def verify_gemm(x, w, y=None, workspace=None, stream=None):
-    """y[M, N] (bf16) = x[M, K] @ w[N, K]^T with fp32 accumulation."""
+    """y[M, N] (bf16) = x[M, K] @ w[N, K]^T with fp32 accumulation.
+
+    ``workspace`` (uint8, ``gemm_workspace_size(M, N, K)`` bytes) must be
+    zero-filled before its first use; every call leaves it ready for the
+    next.  Without one, a zeroed workspace is allocated for this call.
+    """
     import torch
     M, K = x.shape
     N, K2 = w.shape
@@ -191,7 +210,7 @@ def verify_gemm(x, w, y=None, workspace=None, stream=None):
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     need = gemm_workspace_size(M, N, K)
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=x.device)
     st = library().spec_verify_gemm(
         _dev(x, "x", torch.bfloat16), _dev(w, "w", torch.bfloat16), _dev(y, "y", torch.bfloat16),
         M, N, K, _dev(workspace, "workspace", allow_none=True),

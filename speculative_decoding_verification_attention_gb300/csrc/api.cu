@@ -201,13 +201,43 @@ int spec_verify_attention_plan(int B, const int32_t *kv_len_host, int D, int Hkv
 
 extern "C" {
 
-size_t spec_verify_gemm_workspace_size(int, int, int) { return 0; }
+size_t spec_verify_gemm_workspace_size(int M, int N, int K)
+{
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = kSmFallback;
+    return plan_gemm(M, N, K, sms, sms / 2).workspace_bytes;   // an upper bound
+}
+
+int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments, int max_segments)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 64 != 0 || num_sms <= 0 ||
+        max_segments < 0 || (max_segments > 0 && !segments))
+        return -1;
+    const GemmPlan plan = plan_gemm(M, N, K, num_sms, num_sms / 2);
+    int n = 0;
+    for (int c = 0; c < plan.sk.G; ++c) {
+        SegWalker wk(plan.sk, c);
+        Seg s;
+        while (wk.next(s)) {
+            if (n < max_segments) {
+                int32_t *r = segments + 6 * static_cast<size_t>(n);
+                r[0] = c;
+                r[1] = s.t;
+                r[2] = s.kb0;
+                r[3] = s.kb1;
+                r[4] = s.kb0 == 0 ? sk_last_contributor(plan.sk, c, s) : -1;
+                r[5] = plan.bn;
+            }
+            ++n;
+        }
+    }
+    return n;
+}
 
 spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_bf16, int M, int N,
                                int K, void *workspace, size_t workspace_bytes, void *stream)
 {
-    (void)workspace;
-    (void)workspace_bytes;
     if (M < 0 || N < 0 || K < 0) return SPEC_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return SPEC_OK;
     if (M > 65536 || N % 128 != 0 || K % 64 != 0 || K == 0 || N > (1 << 20) || K > (1 << 20))
@@ -217,16 +247,25 @@ spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_b
         return SPEC_ERR_INVALID_ARG;
     const int sms = device_sm_count();
     if (sms <= 0) return SPEC_ERR_CUDA;
-    const GemmPlan plan = plan_gemm(M, N, K, sms);
+    // only the variant this call runs is asked for its residency
+    const GemmPlan probe = plan_gemm(M, N, K, sms, sms / 2);
+    const int units = gemm_max_units(probe.bn, probe.swap);
+    if (units <= 0) return SPEC_ERR_CUDA;
+    const GemmPlan plan = plan_gemm(M, N, K, probe.swap ? units : sms,
+                                    probe.swap ? sms / 2 : units);
+    if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 256))
+        return SPEC_ERR_WORKSPACE;
     CUtensorMap tx, tw;
     const uint64_t dx[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
     const uint64_t dw[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
     const uint64_t st[1] = {static_cast<uint64_t>(K) * 2};
-    const uint32_t bx[2] = {64, static_cast<uint32_t>(plan.swap ? plan.mpad : 128)};
-    const uint32_t bw[2] = {64, static_cast<uint32_t>(plan.swap ? 128 : plan.bn)};
+    // swap: x padded to bn rows, 128-row w tiles; tiled: 128-row x tiles,
+    // each CTA of a pair loading half of the w tile (multicast to both)
+    const uint32_t bx[2] = {64, static_cast<uint32_t>(plan.swap ? plan.bn : 128)};
+    const uint32_t bw[2] = {64, static_cast<uint32_t>(plan.swap ? 128 : plan.bn / 2)};
     if (!encode_bf16_tmap(&tx, x_bf16, 2, dx, st, bx) || !encode_bf16_tmap(&tw, w_bf16, 2, dw, st, bw))
         return SPEC_ERR_CUDA;
-    return from_cuda(launch_gemm(plan, tx, tw, y_bf16, M, N, K, sms, nullptr,
+    return from_cuda(launch_gemm(plan, tx, tw, y_bf16, M, N, workspace, nullptr,
                                  static_cast<cudaStream_t>(stream)));
 }
 

@@ -149,6 +149,19 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// Tiled 2-D load written to the same shared offset of every CTA in cta_mask
+// (this cluster); each destination's mbarrier at bar's offset receives the
+// byte count.
+__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const void *tmap, uint64_t *bar,
+                                                      int x, int y, uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int x,
                                             int y, int z)
 {
@@ -157,6 +170,23 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+// Untiled bulk copy global -> shared.  dst, src 16-byte aligned; bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Orders this thread's earlier (generic-proxy) observations of global memory
+// before its later async-proxy accesses (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_all()
+{
+    asm volatile("fence.proxy.async;" ::: "memory");
 }
 
 // ----------------------------------------------------------- tcgen05 / TMEM
@@ -223,6 +253,16 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// Arrive on the mbarrier at the same shared offset in every CTA of cta_mask
+// (this cluster) once the MMAs issued so far have completed.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)), "h"(cta_mask)
         : "memory");
 }
 

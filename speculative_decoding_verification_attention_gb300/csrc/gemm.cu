@@ -6,21 +6,29 @@
 // representative expert GEMM is N = K = 6144.  Small M streams the weights
 // (HBM-bound); large M is a dense contraction on the tensor cores.
 //
-// Two kernels, both warp-specialised (warp 0: TMA producer, warp 1: MMA
-// issuer, warps 2-5: epilogue), operands staged by TMA with the 128-byte
-// swizzle, tcgen05.mma kind::f16 (M = 128) accumulating in TMEM:
-//  * gemm_tiled: persistent over 128 x BN output tiles, two TMEM
-//    accumulators so one tile's epilogue overlaps the next tile's
-//    main loop.  A = x, B = w.
-//  * gemm_swap: for small M the weight rows take the MMA M side (A = w,
-//    128 rows per tile) and the M rows of x the N side (B = x, padded to
-//    MPAD).  K is split across a thread-block cluster; the partial sums are
-//    reduced in fixed order through distributed shared memory.
+// One warp-specialised kernel (warp 0: TMA producer, warp 1: MMA issuer,
+// warps 2-5: epilogue), operands staged by TMA with the 128-byte swizzle,
+// tcgen05.mma kind::f16 (M = 128) accumulating in TMEM, two accumulators so
+// one piece's epilogue overlaps the next piece's main loop.  Two operand
+// orientations:
+//  * tiled (M > 256): A = x rows, B = w rows.  CTAs run in pairs (clusters
+//    of 2) on 256 x BN tiles, 128 rows each; each CTA loads half of the w
+//    tile and multicasts it to both, halving the L2 -> SM traffic of w.
+//  * swap (M <= 256): A = w rows (128 per tile), B = the M rows of x padded
+//    to MPAD, so the MMA is not mostly padding; the output is written
+//    transposed.
+// Both split the k-block iterations of all tiles evenly over the CTAs
+// (stream-K, see gemm_schedule.h); a tile cut between CTAs is summed by the
+// CTA holding its first k-block from the fp32 partials the others leave in
+// the workspace, in a fixed order, so results are deterministic.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "gemm.h"
+#include "gemm_schedule.h"
 
 namespace cg = cooperative_groups;
 
@@ -69,18 +77,79 @@ __device__ __forceinline__ void mma_kblock(uint32_t d_tmem, uint32_t a_smem, uin
     }
 }
 
-// ------------------------------------------------------------------ tiled
+constexpr uint32_t kPartialReady = 0x5A17C0DEu;   // flag value of a published partial
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait for a later CTA's partial.  All CTAs of the launch are
+// co-resident (cooperative launch), a CTA only waits on CTAs after it, and
+// each publishes its partial before it waits on anyone, so the wait ends;
+// the limit only guards against a fault elsewhere.
+__device__ bool wait_partial(const uint32_t *flag, volatile int *abort, uint32_t *dev_status)
+{
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (ld_acquire(flag) == kPartialReady) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            *abort = 1;
+            report(dev_status, SPEC_DEV_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
+__device__ __forceinline__ void store_bf16_row32(__nv_bfloat16 *dst_row, const float (&a)[32])
+{
+    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        uint4 o;
+        o.x = pack_bf16x2(a[8 * v + 0], a[8 * v + 1]);
+        o.y = pack_bf16x2(a[8 * v + 2], a[8 * v + 3]);
+        o.z = pack_bf16x2(a[8 * v + 4], a[8 * v + 5]);
+        o.w = pack_bf16x2(a[8 * v + 6], a[8 * v + 7]);
+        dst[v] = o;
+    }
+}
+
+// Partial tiles (128 rows x BN fp32) are laid out in 32-column units of
+// 16 KB, each [8 column quads][128 rows][4]: a warp's float4 accesses to one
+// quad are contiguous, and a unit is one bulk copy.
+__device__ __forceinline__ uint32_t partial_index(int cc, int quad, int row)
+{
+    return static_cast<uint32_t>(((cc * 8 + quad) * kBM + row) * 4);
+}
+
 template <int BN, int STAGES>
 struct TiledSmem {
     static constexpr uint32_t kTileB = BN * kBK * 2;
     static constexpr uint32_t kStage = kTileA + kTileB;
     static constexpr uint32_t kBytes = STAGES * kStage + 1024 /*align*/ + 256 /*barriers*/;
+    static_assert(STAGES * kStage >= kBM * BN * 4, "a partial tile must fit in the stage ring");
 };
 
-template <int BN, int STAGES>
+constexpr int stages_for(int bn) { return bn >= 256 ? 4 : bn >= 128 ? 6 : 8; }
+
+// SWAP = false: 256 x BN tiles on CTA pairs, A = x, B = w (shared half by
+// half through multicast).  SWAP = true: 128-row w tiles, A = w, B = x
+// padded to BN rows, single CTAs.
+template <int BN, int STAGES, bool SWAP>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tiled(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-               __nv_bfloat16 *__restrict__ y, int M, int N, int K, uint32_t *dev_status)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                __nv_bfloat16 *__restrict__ y, int M, int N, SkGrid grid, float *__restrict__ part,
+                uint32_t *__restrict__ flags, uint32_t *dev_status)
 {
     using L = TiledSmem<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
@@ -90,232 +159,223 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *acc_full = empty + STAGES;
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *pub_bar = drain + 1;      // 4 epilogue warps stored a partial
+    uint64_t *red_full = pub_bar + 1;   // a later piece's partial landed in the ring
+    uint64_t *red_empty = red_full + 1; // 4 epilogue warps finished reading it
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(red_empty + 1);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_m = (M + kBM - 1) / kBM, tiles_n = N / BN;
-    const int tiles = tiles_m * tiles_n;
-    const int kblocks = K / kBK;
+    // tiled: CTA within its pair, and the pair index (the unit of the split)
+    const int rank = SWAP ? 0 : static_cast<int>(blockIdx.x & 1);
+    const int c = SWAP ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x >> 1);
+    constexpr int kUnit = SWAP ? 1 : 2;   // CTAs per unit of the split
+    constexpr uint16_t kPair = 0x3;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        // tiled: a stage is free once the MMAs of both CTAs of the pair read it
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kUnit); }
         for (int a = 0; a < 2; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 4); }
         mbar_init(drain, 1);
+        mbar_init(pub_bar, 4);
+        mbar_init(red_full, 1);
+        mbar_init(red_empty, 4);
         *abort = 0;
         fence_mbar_init();
     }
     if (warp == 1) { tmem_alloc(tmem_slot, 2 * BN); tmem_relinquish(); }
-    __syncthreads();
+    if constexpr (SWAP) __syncthreads();
+    else cg::this_cluster().sync();   // the peer's barriers exist before anything targets them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_w);
+        SegWalker wk(grid, c);
+        Seg s;
         uint32_t it = 0;
-        for (int t = blockIdx.x; t < tiles && !*abort; t += gridDim.x) {
-            const int mt = t % tiles_m, nt = t / tiles_m;
-            for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                const int s = it % STAGES;
-                if (it >= STAGES && !mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, abort, dev_status)) break;
-                uint8_t *sa = smem + s * L::kStage;
-                mbar_arrive_expect_tx(&full[s], L::kStage);
-                tma_load_2d(sa, &tm_x, &full[s], kb * kBK, mt * kBM);
-                tma_load_2d(sa + kTileA, &tm_w, &full[s], kb * kBK, nt * BN);
+        while (!*abort && wk.next(s)) {
+            const int mt = 2 * (s.t % grid.tiles_m) + rank, nt = s.t / grid.tiles_m;
+            for (int kb = s.kb0; kb < s.kb1; ++kb, ++it) {
+                const int st = it % STAGES;
+                if (it >= STAGES && !mbar_wait(&empty[st], ((it / STAGES) & 1) ^ 1, abort, dev_status)) break;
+                uint8_t *sa = smem + st * L::kStage;
+                mbar_arrive_expect_tx(&full[st], L::kStage);
+                if constexpr (SWAP) {
+                    tma_load_2d(sa, &tm_w, &full[st], kb * kBK, s.t * kBM);
+                    tma_load_2d(sa + kTileA, &tm_x, &full[st], kb * kBK, 0);
+                } else {
+                    // this CTA's rows of x, plus its half of the shared w
+                    // tile, which lands in both CTAs of the pair
+                    tma_load_2d(sa, &tm_x, &full[st], kb * kBK, mt * kBM);
+                    tma_load_2d_multicast(sa + kTileA + rank * (L::kTileB / 2), &tm_w, &full[st],
+                                          kb * kBK, nt * BN + rank * (BN / 2), kPair);
+                }
             }
         }
-        if (*abort) drain_copies(full, it, STAGES);
+        if (*abort) {
+            drain_copies(full, it, STAGES);
+        } else if (!SWAP) {
+            // the peer's MMAs signal this CTA's empty barriers: wait for their
+            // last arrivals before this CTA may exit
+            for (uint32_t i = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0; i < it; ++i)
+                if (!mbar_wait(&empty[i % STAGES], (i / STAGES) & 1, abort, dev_status)) break;
+        }
     } else if (warp == 1 && lane == 0) {
+        SegWalker wk(grid, c);
+        Seg s;
         uint32_t it = 0, lt = 0;
-        for (int t = blockIdx.x; t < tiles && !*abort; t += gridDim.x, ++lt) {
+        while (!*abort && wk.next(s)) {
             const uint32_t ab = lt & 1;
             if (lt >= 2 && !mbar_wait(&acc_empty[ab], ((lt >> 1) & 1) ^ 1, abort, dev_status)) break;
             tc_fence_after();
             const uint32_t d = tmem + ab * BN;
             bool ok = true;
-            for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                const int s = it % STAGES;
-                if (!mbar_wait(&full[s], (it / STAGES) & 1, abort, dev_status)) { ok = false; break; }
+            for (int kb = s.kb0; kb < s.kb1; ++kb, ++it) {
+                const int st = it % STAGES;
+                if (!mbar_wait(&full[st], (it / STAGES) & 1, abort, dev_status)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem + s * L::kStage);
-                mma_kblock<BN>(d, sa, sa + kTileA, kb > 0);
-                umma_commit(&empty[s]);
+                const uint32_t sa = smem_u32(smem + st * L::kStage);
+                mma_kblock<BN>(d, sa, sa + kTileA, kb > s.kb0);
+                if constexpr (SWAP) umma_commit(&empty[st]);
+                else umma_commit_multicast(&empty[st], kPair);
             }
             if (!ok) break;
             umma_commit(&acc_full[ab]);
+            ++lt;
         }
     } else if (warp >= 2) {
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
-        uint32_t lt = 0;
-        for (int t = blockIdx.x; t < tiles && !*abort; t += gridDim.x, ++lt) {
+        // swap: only the 32-column chunks that hold rows of x are needed
+        const int nchunks = SWAP ? (M + 31) / 32 < BN / 32 ? (M + 31) / 32 : BN / 32 : BN / 32;
+        SegWalker wk(grid, c);
+        Seg s;
+        uint32_t lt = 0, npub = 0, nred = 0;
+        while (!*abort && wk.next(s)) {
             const uint32_t ab = lt & 1;
             if (!mbar_wait_warp(&acc_full[ab], (lt >> 1) & 1, abort, dev_status)) break;
             tc_fence_after();
-            const int mt = t % tiles_m, nt = t / tiles_m;
-            const int m = mt * kBM + row;
-            __nv_bfloat16 *yrow = y + static_cast<int64_t>(m) * N + nt * BN;
+            const uint32_t tbase = tmem + ((quad * 32) << 16) + ab * BN;
+            if (s.kb0 > 0) {
+                // A later piece of a cut tile: publish the fp32 partial.
+                float *slot = part + static_cast<size_t>(blockIdx.x) * kBM * BN;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + ((quad * 32) << 16) + ab * BN + c * 32, r);
-                tmem_ld_wait();
-                if (m < M) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + c * 32);
+                for (int cc = 0; cc < nchunks; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + cc * 32, r);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 o;
-                        o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-                        o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-                        o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-                        o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                        dst[v] = o;
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        __stcg(reinterpret_cast<float4 *>(slot + partial_index(cc, q4, row)),
+                               make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
+                                           __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3])));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&acc_empty[ab]);
+                    mbar_arrive(pub_bar);
+                }
+                if (threadIdx.x == 64 && mbar_wait(pub_bar, npub & 1, abort, dev_status)) {
+                    __threadfence();
+                    st_release(&flags[blockIdx.x], kPartialReady);
+                }
+                __syncwarp();
+                ++npub;
+            } else {
+                // A whole tile, or the first piece of a cut tile, which this
+                // CTA owns.  The later pieces' partials are fetched one at a
+                // time by bulk copies into the stage ring -- idle by now, as
+                // an owned cut piece is always the CTA's last segment -- and
+                // added; a running sum between passes stays in tensor memory.
+                // The partials are taken last piece first: a piece at the
+                // start of its CTA's range was published long ago, while the
+                // piece right after this one ends when this one does.  The
+                // order is fixed, so results are deterministic.
+                const int last = sk_last_contributor(grid, c, s);
+                const int npass = last > c ? last - c : 1;
+                const float *ring = reinterpret_cast<const float *>(smem);
+                bool ok = true;
+                for (int q = 0; q < npass && ok; ++q) {
+                    if (last > c) {
+                        if (threadIdx.x == 64) {
+                            const int p = kUnit * (last - q) + rank;   // same rank in a later unit
+                            bool go = nred == 0 || mbar_wait(red_empty, (nred - 1) & 1, abort, dev_status);
+                            go = go && wait_partial(&flags[p], abort, dev_status);
+                            if (go) {
+                                flags[p] = 0;   // zero again for the next call
+                                fence_proxy_async_all();
+                                mbar_arrive_expect_tx(red_full, nchunks * 32 * kBM * 4);
+                                const float *slot = part + static_cast<size_t>(p) * kBM * BN;
+                                for (int u = 0; u < nchunks; ++u)
+                                    bulk_load(smem + u * 32 * kBM * 4, slot + u * 32 * kBM, 32 * kBM * 4,
+                                              red_full);
+                            }
+                        }
+                        ok = mbar_wait_warp(red_full, nred & 1, abort, dev_status);
+                        if (!ok) break;
+                    }
+                    const bool final_pass = q + 1 == npass;
+#pragma unroll 1
+                    for (int cc = 0; cc < nchunks; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tbase + cc * 32, r);
+                        tmem_ld_wait();
+                        float a[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(r[j]);
+                        if (last > c) {
+#pragma unroll
+                            for (int q4 = 0; q4 < 8; ++q4) {
+                                const float4 v = *reinterpret_cast<const float4 *>(ring + partial_index(cc, q4, row));
+                                a[4 * q4] += v.x;
+                                a[4 * q4 + 1] += v.y;
+                                a[4 * q4 + 2] += v.z;
+                                a[4 * q4 + 3] += v.w;
+                            }
+                        }
+                        if (!final_pass) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(a[j]);
+                            tmem_st_32x32b_x32(tbase + cc * 32, r);
+                        } else if constexpr (SWAP) {
+                            // rows of the tile are w rows n; columns are x rows m
+                            const int n = s.t * kBM + row;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                const int m = cc * 32 + j;
+                                if (m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(a[j]);
+                            }
+                        } else {
+                            const int mt = 2 * (s.t % grid.tiles_m) + rank, nt = s.t / grid.tiles_m;
+                            const int m = mt * kBM + row;
+                            if (m < M)
+                                store_bf16_row32(y + static_cast<int64_t>(m) * N + nt * BN + cc * 32, a);
+                        }
+                    }
+                    if (!final_pass) tmem_st_wait();
+                    if (last > c) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(red_empty);
+                        ++nred;
                     }
                 }
+                if (!ok) break;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[ab]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[ab]);
+            ++lt;
         }
     }
     __syncwarp();
     __syncthreads();
     if (*abort && threadIdx.x == 32) drain_mmas(drain);
-    __syncthreads();
+    if constexpr (SWAP) __syncthreads();
+    else cg::this_cluster().sync();   // neither CTA of a pair exits while the other may signal it
     if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, 2 * BN); }
-}
-
-// ------------------------------------------------------------------- swap
-template <int MPAD, int STAGES>
-struct SwapSmem {
-    static constexpr uint32_t kTileB = MPAD * kBK * 2;
-    static constexpr uint32_t kStage = kTileA + kTileB;
-    static constexpr uint32_t kPipe = STAGES * kStage;
-    static constexpr uint32_t kRed = kBM * MPAD * 4;    // fp32 partial of one CTA
-    static constexpr uint32_t kMain = kPipe > kRed ? kPipe : kRed;
-    static constexpr uint32_t kBytes = kMain + 1024 + 256;
-};
-
-template <int MPAD, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_swap(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-              __nv_bfloat16 *__restrict__ y, int M, int N, int K, int splits, uint32_t *dev_status)
-{
-    using L = SwapSmem<MPAD, STAGES>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kMain);
-    uint64_t *empty = full + STAGES;
-    uint64_t *acc_full = empty + STAGES;
-    uint64_t *drain = acc_full + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *red = reinterpret_cast<float *>(smem);   // reused after the main loop
-
-    static_assert(MPAD >= 32 && MPAD % 32 == 0, "epilogue reads 32 columns at a time");
-    constexpr int kTmemCols = MPAD;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = blockIdx.x % splits;
-    const int nt = blockIdx.x / splits;
-    const int kblocks = K / kBK;
-    const int per = (kblocks + splits - 1) / splits;
-    const int kb0 = min(kblocks, rank * per), kb1 = min(kblocks, kb0 + per);
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        mbar_init(&acc_full[0], 1);
-        mbar_init(drain, 1);
-        *abort = 0;
-        fence_mbar_init();
-    }
-    if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tm_w);
-        tma_prefetch_desc(&tm_x);
-        uint32_t it = 0;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-            const int s = it % STAGES;
-            if (it >= STAGES && !mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, abort, dev_status)) break;
-            uint8_t *sa = smem + s * L::kStage;
-            mbar_arrive_expect_tx(&full[s], L::kStage);
-            tma_load_2d(sa, &tm_w, &full[s], kb * kBK, nt * kBM);
-            tma_load_2d(sa + kTileA, &tm_x, &full[s], kb * kBK, 0);
-        }
-        if (*abort) drain_copies(full, it, STAGES);
-    } else if (warp == 1 && lane == 0) {
-        bool ok = true;
-        for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
-            const int s = it % STAGES;
-            if (!mbar_wait(&full[s], (it / STAGES) & 1, abort, dev_status)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t sa = smem_u32(smem + s * L::kStage);
-            mma_kblock<MPAD>(tmem, sa, sa + kTileA, it > 0);
-            umma_commit(&empty[s]);
-        }
-        // completes once every MMA above has finished (also with none issued)
-        if (ok) umma_commit(&acc_full[0]);
-    }
-
-    __syncwarp();   // reconverge the producer / MMA warps before cluster barriers
-
-    // Epilogue warps: fetch this CTA's partial (rows = weight rows n, columns
-    // = x rows m); split 0 reduces the others' partials in rank order.
-    const bool has_k = kb1 > kb0;
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;                 // weight row within the tile
-    const bool epi = warp >= 2;
-    bool ok = true;
-    if (epi) {
-        ok = mbar_wait_warp(&acc_full[0], 0, abort, dev_status);
-        tc_fence_after();
-    }
-    if (splits > 1) {
-        if (epi && rank != 0 && ok) {
-            for (int c = 0; c < MPAD / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + ((quad * 32) << 16) + c * 32, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    red[(c * 32 + j) * kBM + row] = has_k ? __uint_as_float(r[j]) : 0.0f;
-            }
-        }
-        cg::this_cluster().sync();
-    }
-    if (epi && rank == 0 && ok) {
-        const int n = nt * kBM + row;
-        for (int c = 0; c < MPAD / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem + ((quad * 32) << 16) + c * 32, r);
-            tmem_ld_wait();
-            float acc[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = has_k ? __uint_as_float(r[j]) : 0.0f;
-            if (splits > 1) {
-                cg::cluster_group cluster = cg::this_cluster();
-                for (int s = 1; s < splits; ++s) {
-                    const float *rr = cluster.map_shared_rank(red, s);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] += rr[(c * 32 + j) * kBM + row];
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int m = c * 32 + j;
-                if (m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(acc[j]);
-            }
-        }
-    }
-    if (splits > 1) cg::this_cluster().sync();
-    __syncthreads();
-    if (*abort && threadIdx.x == 32) drain_mmas(drain);
-    __syncthreads();
-    if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, kTmemCols); }
 }
 
 template <typename Kern>
@@ -324,93 +384,166 @@ cudaError_t set_smem(Kern k, uint32_t bytes)
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
-template <int MPAD>
-cudaError_t run_swap(const CUtensorMap &tw, const CUtensorMap &tx, __nv_bfloat16 *y, int M, int N,
-                     int K, int splits, uint32_t *dev_status, cudaStream_t st)
+template <int BN, bool SWAP>
+cudaLaunchConfig_t kernel_config(int grid, cudaStream_t st, cudaLaunchAttribute (&attr)[2])
 {
-    constexpr int STAGES = MPAD >= 256 ? 4 : 6;
-    using L = SwapSmem<MPAD, STAGES>;
-    auto k = gemm_swap<MPAD, STAGES>;
-    cudaError_t e = set_smem(k, L::kBytes);
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N / kBM) * splits);
+    cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = L::kBytes;
+    cfg.dynamicSmemBytes = TiledSmem<BN, stages_for(BN)>::kBytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    int n = 0;
+    if (!SWAP) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;   // CTA pairs share the w tile
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    attr[n].id = cudaLaunchAttributeCooperative;   // owners wait on later CTAs' partials
+    attr[n].val.cooperative = 1;
+    ++n;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, tw, tx, y, M, N, K, splits, dev_status);
+    cfg.numAttrs = n;
+    return cfg;
 }
 
-template <int BN>
-cudaError_t run_tiled(const CUtensorMap &tx, const CUtensorMap &tw, __nv_bfloat16 *y, int M, int N,
-                      int K, int num_sms, uint32_t *dev_status, cudaStream_t st)
+template <int BN, bool SWAP>
+cudaError_t run(const GemmPlan &p, const CUtensorMap &tx, const CUtensorMap &tw, __nv_bfloat16 *y,
+                int M, int N, void *workspace, uint32_t *dev_status, cudaStream_t st)
 {
-    constexpr int STAGES = BN >= 256 ? 4 : 6;
-    using L = TiledSmem<BN, STAGES>;
-    auto k = gemm_tiled<BN, STAGES>;
-    cudaError_t e = set_smem(k, L::kBytes);
+    constexpr int STAGES = stages_for(BN);
+    auto k = gemm_kernel<BN, STAGES, SWAP>;
+    cudaError_t e = set_smem(k, TiledSmem<BN, STAGES>::kBytes);
     if (e != cudaSuccess) return e;
-    const int tiles = ((M + kBM - 1) / kBM) * (N / BN);
-    const int grid = tiles < num_sms ? tiles : num_sms;
-    k<<<grid, kThreads, L::kBytes, st>>>(tx, tw, y, M, N, K, dev_status);
-    return cudaGetLastError();
+    uint32_t *flags = static_cast<uint32_t *>(workspace);
+    float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kFlagBytes);
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg = kernel_config<BN, SWAP>(p.grid, st, attr);
+    return cudaLaunchKernelEx(&cfg, k, tx, tw, y, M, N, p.sk, part, flags, dev_status);
+}
+
+// Units (CTA pairs, or single CTAs for the swap orientation) that can be
+// resident at once, from the occupancy calculator; 0 if the query fails.
+template <int BN, bool SWAP>
+int max_units_for()
+{
+    constexpr int STAGES = stages_for(BN);
+    auto k = gemm_kernel<BN, STAGES, SWAP>;
+    if (set_smem(k, TiledSmem<BN, STAGES>::kBytes) != cudaSuccess) return 0;
+    int n = 0;
+    if (SWAP) {
+        int dev = 0, sms = 0, per_sm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads,
+                                                          TiledSmem<BN, STAGES>::kBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        n = per_sm > 0 ? sms : 0;   // one CTA per SM
+    } else {
+        cudaLaunchAttribute attr[2];
+        cudaLaunchConfig_t cfg = kernel_config<BN, SWAP>(2, nullptr, attr);
+        cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+    }
+    return n;
+}
+
+int query_max_units(int bn, bool swap)
+{
+    if (swap) {
+        switch (bn) {
+        case 32: return max_units_for<32, true>();
+        case 64: return max_units_for<64, true>();
+        case 128: return max_units_for<128, true>();
+        default: return max_units_for<256, true>();
+        }
+    }
+    return bn == 256 ? max_units_for<256, false>() : max_units_for<128, false>();
 }
 
 }  // namespace
 
-GemmPlan plan_gemm(int M, int N, int K, int num_sms)
+int gemm_max_units(int bn, bool swap)
+{
+    // per device and kernel variant; the answer never changes for a process
+    static std::atomic<int> cache[64][6];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    const int v_idx = swap ? (bn == 32 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : 3) : (bn == 256 ? 5 : 4);
+    std::atomic<int> &slot = cache[dev][v_idx];
+    int v = slot.load(std::memory_order_relaxed);
+    if (v <= 0) {
+        v = query_max_units(bn, swap);
+        slot.store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_tiled)
 {
     GemmPlan p{};
-    (void)K;
+    const int kblocks = K / kBK;
+    int tiles, min_iters, cap;
     if (M <= 256) {
+        // Weight streaming: 128-row w tiles; a tile may be cut into up to
+        // five pieces (min_iters = ceil(kblocks / 4)), so every SM streams.
         p.swap = true;
-        p.mpad = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-        const int tiles = N / kBM;
-        int s = num_sms / (tiles > 0 ? tiles : 1);
-        s = s < 1 ? 1 : s > 4 ? 4 : s;
-        const int kblocks = K / kBK;
-        while (s > 1 && kblocks < s * 2) --s;
-        p.splits = s;
-        p.bn = 0;
+        p.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+        tiles = N / kBM;
+        p.sk.tiles_m = 1;
+        min_iters = (kblocks + 3) / 4 > 8 ? (kblocks + 3) / 4 : 8;
+        cap = max_units_swap;
     } else {
+        // 256 x BN tiles on CTA pairs; a tile is cut into at most three
+        // pieces (min_iters = ceil(kblocks / 2)).
         p.swap = false;
-        p.splits = 1;
-        // pick the tile width that wastes the least of the last wave
-        const int tiles_m = (M + kBM - 1) / kBM;
-        double best = 1e30;
-        for (int bn : {256, 128}) {
-            if (N % bn) continue;
-            const int tiles = tiles_m * (N / bn);
-            const int waves = (tiles + num_sms - 1) / num_sms;
-            const double cost = static_cast<double>(waves) * bn * (bn == 256 ? 0.92 : 1.0);
-            if (cost < best) { best = cost; p.bn = bn; }
-        }
+        p.bn = N % 256 == 0 ? 256 : 128;
+        p.sk.tiles_m = ((M + kBM - 1) / kBM + 1) / 2;
+        tiles = p.sk.tiles_m * (N / p.bn);
+        min_iters = (kblocks + 1) / 2 > 16 ? (kblocks + 1) / 2 : 16;
+        cap = max_units_tiled;
     }
+    // Stream-K: whole-tile waves while more than two waves remain, the rest
+    // cut into equal k-block ranges, one per unit.
+    const long long iters = static_cast<long long>(tiles) * kblocks;
+    const int unit_ctas = p.swap ? 1 : 2;
+    cap = cap < kMaxCtas / unit_ctas ? cap : kMaxCtas / unit_ctas;
+    cap = cap < 1 ? 1 : cap;
+    long long u = iters / min_iters;
+    u = u < 1 ? 1 : u > cap ? cap : u;
+    const int units = static_cast<int>(u);
+    const int waves = tiles / units;
+    p.grid = unit_ctas * units;
+    p.sk.tiles = tiles;
+    p.sk.kblocks = kblocks;
+    p.sk.G = units;
+    p.sk.dp_tiles = waves >= 2 ? (waves - 1) * units : 0;
+    p.sk.sk_iters = static_cast<long long>(tiles - p.sk.dp_tiles) * kblocks;
+    p.workspace_bytes = kFlagBytes + static_cast<size_t>(p.grid) * kBM * p.bn * 4;
     return p;
 }
 
 cudaError_t launch_gemm(const GemmPlan &p, const CUtensorMap &t_x, const CUtensorMap &t_w,
-                        void *y, int M, int N, int K, int num_sms, uint32_t *dev_status,
+                        void *y, int M, int N, void *workspace, uint32_t *dev_status,
                         cudaStream_t st)
 {
     __nv_bfloat16 *yy = static_cast<__nv_bfloat16 *>(y);
     if (p.swap) {
-        switch (p.mpad) {
-        case 32: return run_swap<32>(t_w, t_x, yy, M, N, K, p.splits, dev_status, st);
-        case 64: return run_swap<64>(t_w, t_x, yy, M, N, K, p.splits, dev_status, st);
-        case 128: return run_swap<128>(t_w, t_x, yy, M, N, K, p.splits, dev_status, st);
-        default: return run_swap<256>(t_w, t_x, yy, M, N, K, p.splits, dev_status, st);
+        switch (p.bn) {
+        case 32: return run<32, true>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
+        case 64: return run<64, true>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
+        case 128: return run<128, true>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
+        default: return run<256, true>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
         }
     }
-    if (p.bn == 256) return run_tiled<256>(t_x, t_w, yy, M, N, K, num_sms, dev_status, st);
-    return run_tiled<128>(t_x, t_w, yy, M, N, K, num_sms, dev_status, st);
+    if (p.bn == 256) return run<256, false>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
+    return run<128, false>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
 }
 
 }  // namespace spec

@@ -3,21 +3,36 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
+
+#include "gemm_schedule.h"
 
 namespace spec {
 
+// Workspace of the GEMM: one ready flag per CTA (at most kMaxCtas CTAs) in
+// the first kFlagBytes, then one fp32 128 x BN partial tile per CTA.
+constexpr int kMaxCtas = 256;
+constexpr size_t kFlagBytes = 1024;
+
 struct GemmPlan {
-    bool swap;     // weights on the MMA M side (small M)
-    int mpad;      // swap: x rows padded to the MMA N size
-    int splits;    // swap: K split across a cluster of this many CTAs
-    int bn;        // tiled: output tile width
+    bool swap;     // w rows on the MMA M side (M <= 256), x rows padded to bn
+    int bn;        // MMA N: output tile width, or (swap) padded rows of x
+    int grid;      // CTAs (tiled: in pairs), all co-resident
+    SkGrid sk;     // stream-K decomposition; units are CTA pairs (tiled) or CTAs (swap)
+    size_t workspace_bytes;  // ready flags + fp32 partial slots
 };
 
-GemmPlan plan_gemm(int M, int N, int K, int num_sms);
+// max_units_*: units (single CTAs for the swap orientation, CTA pairs for
+// the tiled one) that can be resident at once.
+GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_tiled);
+
+// Resident units of the kernel variant on the current device (0 if the
+// query fails).
+int gemm_max_units(int bn, bool swap);
 
 cudaError_t launch_gemm(const GemmPlan &p, const CUtensorMap &t_x, const CUtensorMap &t_w,
-                        void *y, int M, int N, int K, int num_sms, uint32_t *dev_status,
+                        void *y, int M, int N, void *workspace, uint32_t *dev_status,
                         cudaStream_t st);
 
 }  // namespace spec

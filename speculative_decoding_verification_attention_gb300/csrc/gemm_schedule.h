@@ -1,0 +1,74 @@
+// Stream-K work decomposition of the tiled verify GEMM, shared by the
+// kernel's three roles (TMA producer, MMA issuer, epilogue) and by the host
+// planner that the CPU tests enumerate.
+//
+// Output tile t covers rows (t % tiles_m) * 128 and columns
+// (t / tiles_m) * BN.  The first dp_tiles tiles are whole-tile work (CTA c
+// takes c, c + G, c + 2G, ...); the k-block iterations of the remaining
+// tiles are cut into G equal contiguous ranges, one per CTA (stream-K), so
+// every SM gets the same number of MMAs whatever the tile count.  A tile
+// cut between CTAs is finished by the CTA holding its first k-block (its
+// owner), which adds, in CTA order, the fp32 partial sums that the later
+// CTAs holding the rest of the tile left in the workspace.
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define SPEC_HD __host__ __device__ __forceinline__
+#else
+#define SPEC_HD inline
+#endif
+
+namespace spec {
+
+struct SkGrid {
+    int tiles_m, tiles, kblocks, G, dp_tiles;
+    long long sk_iters;   // (tiles - dp_tiles) * kblocks
+    SPEC_HD long long begin(int c) const { return sk_iters * c / G; }
+};
+
+struct Seg {
+    int t, kb0, kb1;
+};
+
+struct SegWalker {
+    SkGrid g;
+    int c, w;
+    long long it, end;
+    SPEC_HD SegWalker(const SkGrid &g_, int c_)
+        : g(g_), c(c_), w(0), it(g_.begin(c_)), end(g_.begin(c_ + 1)) {}
+    SPEC_HD bool next(Seg &s)
+    {
+        if (w * g.G < g.dp_tiles) {
+            s.t = c + w * g.G;
+            s.kb0 = 0;
+            s.kb1 = g.kblocks;
+            ++w;
+            return true;
+        }
+        if (it >= end) return false;
+        const long long t = it / g.kblocks;
+        s.t = g.dp_tiles + static_cast<int>(t);
+        s.kb0 = static_cast<int>(it - t * g.kblocks);
+        const long long left = end - it;
+        s.kb1 = left < g.kblocks - s.kb0 ? s.kb0 + static_cast<int>(left) : g.kblocks;
+        it += s.kb1 - s.kb0;
+        return true;
+    }
+};
+
+// For a segment that starts its tile (kb0 == 0) on CTA c: the last CTA
+// holding a later piece of the same tile (c itself when the tile is whole).
+// The pieces' holders are exactly CTAs c+1 .. last.
+SPEC_HD int sk_last_contributor(const SkGrid &g, int c, const Seg &s)
+{
+    int last = c;
+    if (s.kb1 < g.kblocks) {
+        const long long tile_end = static_cast<long long>(s.t - g.dp_tiles + 1) * g.kblocks;
+        while (last + 1 < g.G && g.begin(last + 1) < tile_end) ++last;
+    }
+    return last;
+}
+
+}  // namespace spec

@@ -83,4 +83,10 @@ def test_gemm_rejects_bad_arguments(lib):
     assert f(None, FAKE, FAKE, 8, 128, 64, None, 0, None) == INVALID
     assert f(P(0x7F0000001008), FAKE, FAKE, 8, 128, 64, None, 0, None) == INVALID
     assert f(None, None, None, 0, 128, 64, None, 0, None) == 0   # empty: no-op
-    assert lib.spec_verify_gemm_workspace_size(512, 6144, 6144) == 0
+    # stream-K: 1 KB of ready flags, then one fp32 partial tile per CTA
+    ws = lib.spec_verify_gemm_workspace_size(512, 6144, 6144)
+    assert ws >= 1024 + 128 * 256 * 4 and ws % 256 == 0
+    assert lib.spec_verify_gemm_workspace_size(512, 6144 + 128, 6144) < ws   # 128-wide tiles
+    # small M: partials as wide as the padded x rows
+    assert lib.spec_verify_gemm_workspace_size(8, 6144, 6144) < lib.spec_verify_gemm_workspace_size(
+        256, 6144, 6144)

@@ -92,3 +92,59 @@ def test_two_calls_in_a_row_agree(sv):
     a, _ = run(sv, x, w)
     b, _ = run(sv, x, w)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("M,N,K", [(384, 128, 6144), (640, 256, 4096), (2000, 6272, 640)])
+def test_stream_k_many_pieces(sv, oracle_lib, M, N, K):
+    """Few tiles and long K: tiles are cut into several pieces whose fp32
+    partials the owning CTA adds (checked in full against the oracle)."""
+    x, w = synth.gemm_inputs(7 * M + K, M, N, K)
+    segs = sv.gemm_plan(M, N, K, 152)
+    assert (segs[:, 2] > 0).any()          # the split really cuts tiles
+    if M * N <= 640 * 256:
+        y, _ = run(sv, x, w)
+        check(y, oracle_lib.gemm(x, w))
+    else:
+        y, _ = run(sv, x, w)
+        rng = np.random.default_rng(3)
+        s = sample_entries(rng, M, N)
+        check(y[s[:, 0], s[:, 1]], oracle_lib.gemm(x, w, samples=s))
+
+
+def test_workspace_reused_and_left_zero(sv):
+    """One zeroed workspace serves many calls: each call leaves the ready
+    flags zero again, and results are bit-identical (fixed summation order)."""
+    import torch
+    M, N, K = 512, 6144, 6144
+    x, w = synth.gemm_inputs(11, M, N, K)
+    xd, wd = bits_to_dev(x), bits_to_dev(w)
+    ws = torch.zeros(sv.gemm_workspace_size(M, N, K), dtype=torch.uint8, device="cuda")
+    outs = [sv.verify_gemm(xd, wd, workspace=ws).clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    flags = ws[:1024]                      # one ready flag per CTA
+    assert int(flags.count_nonzero()) == 0
+
+
+def test_graph_replay(sv, oracle_lib):
+    """Captured once in a CUDA graph and replayed: every replay is right."""
+    import torch
+    M, N, K = 1024, 768, 6144
+    x, w = synth.gemm_inputs(13, M, N, K)
+    xd, wd = bits_to_dev(x), bits_to_dev(w)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(max(256, sv.gemm_workspace_size(M, N, K)), dtype=torch.uint8, device="cuda")
+    sv.verify_gemm(xd, wd, y=y, workspace=ws)      # warm-up outside capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            sv.verify_gemm(xd, wd, y=y, workspace=ws)
+    ref = oracle_lib.gemm(x, w)
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        check(y.float().cpu().numpy().astype(np.float64), ref)
