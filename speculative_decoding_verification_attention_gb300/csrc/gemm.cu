@@ -99,14 +99,14 @@ __device__ bool wait_partial(const uint32_t *flag, volatile int *abort, uint32_t
 {
     const unsigned long long t0 = globaltimer_ns();
     for (;;) {
-        if (ld_acquire(flag) == kPartialReady) return true;
+        for (int i = 0; i < 32; ++i)
+            if (ld_acquire(flag) == kPartialReady) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
             *abort = 1;
             report(dev_status, SPEC_DEV_ERR_TIMEOUT);
             return false;
         }
-        __nanosleep(64);
     }
 }
 
@@ -278,10 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&acc_empty[ab]);
                     mbar_arrive(pub_bar);
                 }
-                if (threadIdx.x == 64 && mbar_wait(pub_bar, npub & 1, abort, dev_status)) {
-                    __threadfence();
+                // the release store is cumulative: it also orders the other
+                // epilogue threads' partial stores, which this thread observed
+                // through pub_bar
+                if (threadIdx.x == 64 && mbar_wait(pub_bar, npub & 1, abort, dev_status))
                     st_release(&flags[blockIdx.x], kPartialReady);
-                }
                 __syncwarp();
                 ++npub;
             } else {
@@ -295,25 +296,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // piece right after this one ends when this one does.  The
                 // order is fixed, so results are deterministic.
                 const int last = sk_last_contributor(grid, c, s);
-                const int npass = last > c ? last - c : 1;
+                const int ncontrib = last - c;
+                // partials per pass: as many as fit in the stage ring at once
+                const int unit_bytes = nchunks * 32 * kBM * 4;
+                const int per_pass = (STAGES * static_cast<int>(L::kStage)) / unit_bytes;
+                const int npass = ncontrib > 0 ? (ncontrib + per_pass - 1) / per_pass : 1;
                 const float *ring = reinterpret_cast<const float *>(smem);
                 bool ok = true;
                 for (int q = 0; q < npass && ok; ++q) {
-                    if (last > c) {
+                    const int k0 = q * per_pass;   // contributors k0 .. k1-1 of this pass,
+                    const int k1 = ncontrib < k0 + per_pass ? ncontrib : k0 + per_pass;
+                    if (ncontrib > 0) {            // counted from the last one
                         if (threadIdx.x == 64) {
-                            const int p = kUnit * (last - q) + rank;   // same rank in a later unit
                             bool go = nred == 0 || mbar_wait(red_empty, (nred - 1) & 1, abort, dev_status);
-                            go = go && wait_partial(&flags[p], abort, dev_status);
-                            if (go) {
+                            if (go) mbar_arrive_expect_tx(red_full, (k1 - k0) * unit_bytes);
+                            for (int k = k0; k < k1 && go; ++k) {
+                                const int p = kUnit * (last - k) + rank;   // same rank in a later unit
+                                go = wait_partial(&flags[p], abort, dev_status);
+                                if (!go) break;
                                 flags[p] = 0;   // zero again for the next call
                                 fence_proxy_async_all();
-                                mbar_arrive_expect_tx(red_full, nchunks * 32 * kBM * 4);
                                 const float *slot = part + static_cast<size_t>(p) * kBM * BN;
+                                uint8_t *dst = smem + (k - k0) * unit_bytes;
                                 for (int u = 0; u < nchunks; ++u)
-                                    bulk_load(smem + u * 32 * kBM * 4, slot + u * 32 * kBM, 32 * kBM * 4,
+                                    bulk_load(dst + u * 32 * kBM * 4, slot + u * 32 * kBM, 32 * kBM * 4,
                                               red_full);
                             }
                         }
+                        // the rest of warp 2 waits here rather than polling the
+                        // barrier, which would stall lane 0's divergent path
+                        __syncwarp();
                         ok = mbar_wait_warp(red_full, nred & 1, abort, dev_status);
                         if (!ok) break;
                     }
@@ -326,10 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float a[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(r[j]);
-                        if (last > c) {
+                        for (int k = k0; k < k1; ++k) {
+                            const float *src = ring + (k - k0) * (unit_bytes / 4);
 #pragma unroll
                             for (int q4 = 0; q4 < 8; ++q4) {
-                                const float4 v = *reinterpret_cast<const float4 *>(ring + partial_index(cc, q4, row));
+                                const float4 v = *reinterpret_cast<const float4 *>(src + partial_index(cc, q4, row));
                                 a[4 * q4] += v.x;
                                 a[4 * q4 + 1] += v.y;
                                 a[4 * q4 + 2] += v.z;
@@ -356,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     if (!final_pass) tmem_st_wait();
-                    if (last > c) {
+                    if (ncontrib > 0) {
                         __syncwarp();
                         if (lane == 0) mbar_arrive(red_empty);
                         ++nred;
@@ -491,13 +504,16 @@ GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_tiled)
     const int kblocks = K / kBK;
     int tiles, min_iters, cap;
     if (M <= 256) {
-        // Weight streaming: 128-row w tiles; a tile may be cut into up to
-        // five pieces (min_iters = ceil(kblocks / 4)), so every SM streams.
+        // Weight streaming: 128-row w tiles cut so that every SM streams.
+        // Narrow partials are cheap to add, so a tile may be cut into up to
+        // five pieces (min_iters = ceil(kblocks / 4)); with 128 or more
+        // columns into at most three (ceil(kblocks / 2)).
         p.swap = true;
         p.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
         tiles = N / kBM;
         p.sk.tiles_m = 1;
-        min_iters = (kblocks + 3) / 4 > 8 ? (kblocks + 3) / 4 : 8;
+        const int div = p.bn <= 64 ? 4 : 2;
+        min_iters = (kblocks + div - 1) / div > 8 ? (kblocks + div - 1) / div : 8;
         cap = max_units_swap;
     } else {
         // 256 x BN tiles on CTA pairs; a tile is cut into at most three

@@ -26,7 +26,7 @@ def test_stream_k_split(M, N, K, sms):
     if swap:        # 128-row w tiles; x rows padded to the MMA N
         bn = 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
         tiles = N // 128
-        max_units, max_contrib = sms, 4
+        max_units, max_contrib = sms, 4 if bn <= 64 else 2
     else:           # 256-row pair tiles
         bn = 256 if N % 256 == 0 else 128
         tiles = -(-(-(-M // 128)) // 2) * (N // bn)
