@@ -251,7 +251,7 @@ def gpu_arm(args, rank, world):
               gemm=torch.zeros(max(256, sv.gemm_workspace_size(wl.x.shape[0], wl.w.shape[0],
                                                                wl.x.shape[1])),
                                dtype=torch.uint8, device=dev),
-              accept=torch.empty(sv.accept_sample_workspace_size(wl.B, wl.V), dtype=torch.uint8,
+              accept=torch.zeros(sv.accept_sample_workspace_size(wl.B, wl.V), dtype=torch.uint8,
                                  device=dev))
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
@@ -580,7 +580,7 @@ def case_lines(args):
             na, tk = torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev)
             ms_g = time_launches(lambda: sv.accept_greedy(p, dg, na, tk), args.warmup, args.steps, flush)
             ng = na.cpu().numpy()
-            wsa = torch.empty(sv.accept_sample_workspace_size(B, V), dtype=torch.uint8, device=dev)
+            wsa = torch.zeros(sv.accept_sample_workspace_size(B, V), dtype=torch.uint8, device=dev)
             ms_s = time_launches(lambda: sv.accept_sample(p, q, ds, ua, ur, na, tk, workspace=wsa), args.warmup, args.steps, flush)
             ns = na.cpu().numpy()
             gb, sb = accept_bytes(ng, ns, B, D, V)

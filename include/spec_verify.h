@@ -228,7 +228,11 @@ spec_status_t spec_accept_greedy(const float *p, const int32_t *draft, int B, in
  *   u_res    device, fp32 [B] in [0, 1).
  *   n_accepted, token   device, int32 [B].
  *   workspace  device, spec_accept_sample_workspace_size(B, V) bytes,
- *              256-byte aligned; scratch only, needs no initialisation.
+ *              256-byte aligned, owned by the caller; scratch only (the
+ *              first rejected draft and the exact masses of every 1024- and
+ *              128-element slice of the needed rows), needs no
+ *              initialisation.  Calls sharing a workspace must not overlap
+ *              in time.
  * Supported set: B >= 0, 0 <= D <= 63, 1 <= V <= 2^26.
  * ---------------------------------------------------------------------- */
 size_t spec_accept_sample_workspace_size(int B, int V);

@@ -242,7 +242,11 @@ def accept_sample_workspace_size(B, V):
 
 def accept_sample(p, q, draft, u_acc, u_res, n_accepted=None, token=None, workspace=None,
                   dev_status=None, stream=None):
-    """Stochastic acceptance with residual resampling (explicit uniforms)."""
+    """Stochastic acceptance with residual resampling (explicit uniforms).
+
+    ``workspace`` (uint8, ``accept_sample_workspace_size(B, V)`` bytes) is
+    scratch; without one it is allocated for this call.
+    """
     import torch
     B, D1, V = p.shape
     if n_accepted is None:

@@ -6,18 +6,24 @@
 // rejection resample from max(0, p - q) renormalised (llm-digest,
 // "Mechanism" and "Math intuition").
 //
-// Layout of the work: one thread-block cluster of CS CTAs per sequence;
-// CTA `rank` owns a contiguous slice of the vocabulary and each of its 8
-// warps a contiguous sub-slice, streamed in 128-element steps (one float4
-// per lane, coalesced).  Cluster-wide reductions go through distributed
-// shared memory.
+// Greedy: one thread-block cluster of CS CTAs per sequence; CTA `rank`
+// owns a contiguous slice of the vocabulary and each of its 8 warps a
+// contiguous sub-slice, streamed in 128-element steps (one float4 per lane,
+// coalesced).  Cluster-wide reductions go through distributed shared
+// memory.  Stochastic: three kernels chained by programmatic dependent
+// launch (first rejection per sequence; a persistent streaming kernel that
+// stages the needed rows by bulk copies and writes exact slice masses; a
+// warp per sequence that draws the token).
 //
 // Exactness: the accept test u*q < p is evaluated in fp64, where the
-// product of two fp32 values is exact.  Residual / bonus mass is summed in
-// 64-bit fixed point (2^-61 resolution, truncation of each element), so
-// every partial sum is exact and independent of the summation order; the
-// draw compares running sums against floor(u * Z) computed exactly from
-// the 24-bit mantissa of u.
+// product of two fp32 values is exact.  The residual of an element is
+// max(0, p - q) with the difference rounded to fp32; residual / bonus masses
+// are summed in 64-bit fixed point (2^-61 resolution, truncation of each
+// element), so every partial sum is exact and independent of the summation
+// order; the draw compares running sums against floor(u * Z) computed
+// exactly from the 24-bit mantissa of u.  Against the exact real-number
+// residual, each element is off by at most 2^-24 of its value, so a draw
+// can differ from the exact one only within 2^-23 Z of a CDF boundary.
 #include <cooperative_groups.h>
 #include <float.h>
 
@@ -166,36 +172,34 @@ __global__ void __launch_bounds__(kThreads, 4) accept_greedy_kernel(
 }
 
 // --------------------------------------------------------------- stochastic
-// Fixed point with 2^-61 resolution: floor(x * 2^61) for 0 <= x < 8 (row
-// sums below 8 fit in 64 bits).  x * 2^61 = m * 2^sh with m the 24-bit
-// significand and sh = exponent - 89; the result is (m << max(sh, 0)) >>
-// max(-sh, 0).  PTX clamps shift counts, so zero, denormals (sh = -89),
-// negatives (the sign bit makes sh >= 167), infinities and NaN all give 0
-// without special cases.  Integer shifts only: the float-to-64-bit-integer
-// conversion instruction runs on the small fp64 pipe of this GPU.
+// Fixed point with 2^-61 resolution: floor(x * 2^61) for 0 <= x < 2 (row
+// sums of probabilities fit in 64 bits).  With x = m * 2^(E - 150), m the
+// 24-bit significand and E the biased exponent, x * 2^61 = (m << 38) >>
+// (127 - E).  m << 38 has a zero low word, so this is one 32-bit shift and
+// one 64-bit right shift.  PTX clamps shift counts, so zero and denormals
+// (E = 0), negatives (the sign bit makes E >= 256), x >= 2, infinities and
+// NaN all give 0 without special cases.  Integer work only: the
+// float-to-64-bit-integer conversion runs on the small fp64 pipe.
 __device__ __forceinline__ unsigned long long fix61(float x)
 {
-    const uint32_t b = __float_as_uint(x);
-    const unsigned long long m = (b & 0x7FFFFFu) | 0x800000u;
-    const int sh = static_cast<int>(b >> 23) - 89;
+    const uint32_t bits = __float_as_uint(x);
+    const uint32_t m = (bits & 0x7FFFFFu) | 0x800000u;
+    const uint32_t sh = 127u - (bits >> 23);
     unsigned long long r;
-    asm("{\n\t.reg .u32 l, rr;\n\t"
-        "max.s32 l, %1, 0;\n\t"
-        "neg.s32 rr, %1;\n\t"
-        "max.s32 rr, rr, 0;\n\t"
-        "shl.b64 %0, %2, l;\n\t"
-        "shr.b64 %0, %0, rr;\n\t}"
+    asm("{\n\t.reg .b64 t;\n\t"
+        "mov.b64 t, {%2, %3};\n\t"
+        "shr.b64 %0, t, %1;\n\t}"
         : "=l"(r)
-        : "r"(sh), "l"(m));
+        : "r"(sh), "r"(0u), "r"(m << 6));
     return r;
 }
 
+// Mass of one element: p, or the residual max(0, p - q) with the difference
+// rounded to fp32 (round to nearest).  Each element's mass is then exact in
+// the fixed point, so every sum of masses is exact and order-independent.
 __device__ __forceinline__ unsigned long long mass(float pv, float qv, int residual)
 {
-    unsigned long long a = fix61(pv);
-    if (!residual) return a;
-    unsigned long long c = fix61(qv);
-    return a > c ? a - c : 0ull;
+    return fix61(residual ? fmaxf(__fsub_rn(pv, qv), 0.0f) : pv);
 }
 
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x)
@@ -229,30 +233,48 @@ __device__ __forceinline__ unsigned long long scaled_threshold(float u, unsigned
     return (hi << (64 - s)) | (lo >> s);
 }
 
-// ----------------------------------------------------- stochastic, staged
-// Scratch layout in the caller's workspace (see spec_accept_sample):
-//   js    int32  [B]                 first rejected draft (or D)
-//   cnt   uint32 [B]                 chunks of the sequence finished
-//   steps uint64 [B][ceil(V / 128)]  exact residual / bonus mass of every
-//                                    128-element step of the needed row
+// Scratch in the caller's workspace (see spec_accept_sample):
+//   js    int32  [B]            first rejected draft (or D) of each sequence
+//   gtot  uint64 [B][ngroups]   exact residual / bonus mass of every group
+//                               of 4 steps (512 elements)
+//   steps uint64 [B][nsteps]    ... and of every 128-element step
 struct SampleScratch {
     int32_t *js;
-    uint32_t *cnt;
+    unsigned long long *gtot;
     unsigned long long *steps;
-    int nsteps;
+    int nsteps, ngroups;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-constexpr int kChunk = kThreads * 32;      // elements of one streaming CTA
-constexpr int kWarpElems = kChunk / kWarps;   // 1024: 8 steps of 128
+constexpr int kChunk = 8192;                   // elements of one work item
+constexpr int kConsumers = 16;                 // consumer warps of the streaming kernel
+constexpr int kGroupSteps = kChunk / kStep / kConsumers;   // 4
+constexpr int kGroup = kGroupSteps * kStep;    // 512: one consumer warp's share of an item
+constexpr int kRing = 3;                       // items staged at once per CTA
+constexpr int kStreamThreads = (kConsumers + 1) * 32;   // + 1 producer warp
+constexpr uint32_t kItemBytes = 2 * kChunk * 4;   // p and q slices of one item
+constexpr uint32_t kStreamSmem = kRing * kItemBytes + 1024;
+
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled now / wait until the previous one's results are visible.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // Stage 1: first rejected draft of every sequence (one warp per sequence);
-// the accept test u * q(x) < p(x) is evaluated in fp64, where it is exact.
+// the accept test u * q(x) < p(x) is evaluated in fp64, where the product
+// is exact.
 __global__ void __launch_bounds__(kThreads) accept_prep_kernel(
     const float *__restrict__ p, const float *__restrict__ q, const int32_t *__restrict__ draft,
     const float *__restrict__ u_acc, int B, int D, int V, SampleScratch sc, uint32_t *dev_status)
 {
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * kWarps + warp;
     if (b >= B) return;
@@ -279,177 +301,226 @@ __global__ void __launch_bounds__(kThreads) accept_prep_kernel(
             break;
         }
     }
-    if (lane == 0) {
-        sc.js[b] = j;
-        sc.cnt[b] = 0u;
-    }
+    if (lane == 0) sc.js[b] = j;
 }
 
-// Exact masses of the 8 steps of 128 elements starting at element e0 of a
-// row (one warp; lane k of the result holds step k's total, k < 8).
-__device__ __forceinline__ unsigned long long warp_step_masses(const float *prow, const float *qrow,
-                                                               int residual, int64_t e0, int64_t V,
-                                                               bool vec4, int lane)
+// Exact masses of the kGroupSteps steps of 128 elements starting at element
+// w0 of the n-element slice (sp, sq): staged in shared memory (SMEM,
+// n % 4 == 0) or read from global memory.  Lane k of the result holds step
+// k's total (k < kGroupSteps).
+template <bool SMEM>
+__device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, const float *sq,
+                                                               int residual, int w0, int n, bool vec4,
+                                                               int lane)
 {
-    float4 xp[8], xq[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int64_t e = e0 + k * kStep + lane * 4;
-        xp[k] = e < V ? load4(prow, e, V, vec4, 0.f) : make_float4(0, 0, 0, 0);
-        xq[k] = (residual && e < V) ? load4(qrow, e, V, vec4, 0.f) : make_float4(0, 0, 0, 0);
-    }
     unsigned long long mine = 0;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const unsigned long long m = mass(xp[k].x, xq[k].x, residual) + mass(xp[k].y, xq[k].y, residual) +
-                                     mass(xp[k].z, xq[k].z, residual) + mass(xp[k].w, xq[k].w, residual);
+    for (int k = 0; k < kGroupSteps; ++k) {
+        const int e = w0 + k * kStep + lane * 4;
+        unsigned long long m = 0;
+        if (e < n) {
+            float4 xp, xq = make_float4(0, 0, 0, 0);
+            if (SMEM) {
+                xp = *reinterpret_cast<const float4 *>(sp + e);
+                if (residual) xq = *reinterpret_cast<const float4 *>(sq + e);
+            } else {
+                xp = load4(sp, e, n, vec4, 0.f);
+                if (residual) xq = load4(sq, e, n, vec4, 0.f);
+            }
+            m = mass(xp.x, xq.x, residual) + mass(xp.y, xq.y, residual) + mass(xp.z, xq.z, residual) +
+                mass(xp.w, xq.w, residual);
+        }
         const unsigned long long t = warp_sum_u64(m);
         if (lane == k) mine = t;
     }
     return mine;
 }
 
-// Stage 2: every CTA streams one 8192-element chunk of the row its
-// sequence needs (the residual row j, or the bonus row D) and writes the
-// exact mass of each 128-element step.  The last CTA of a sequence to
-// finish finds the crossing of u * Z in the running sum from the step
-// masses and re-reads only the 128 elements of that step.
-__global__ void __launch_bounds__(kThreads, 2) accept_stream_kernel(
+// Stage 2, persistent: each CTA takes work items (sequence b, 8192-element
+// chunk of the one row b needs -- the residual row j, or the bonus row D)
+// round robin.  The producer warp stages up to kRing items ahead in shared
+// memory with bulk copies; each of the 16 consumer warps turns 512 elements
+// of an item into 4 exact step masses and their group total.
+__global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
+    const float *__restrict__ p, const float *__restrict__ q, int D, int V, int nchunks, int items,
+    SampleScratch sc, uint32_t *dev_status, bool bulk)
+{
+    extern __shared__ uint8_t s_raw[];
+    float *ring = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_raw) + 127) & ~uintptr_t(127));
+    __shared__ uint64_t full[kRing], empty[kRing];
+    __shared__ int s_j[kRing];
+    __shared__ int s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRing; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kConsumers); }
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+    pdl_wait();   // js comes from the previous kernel
+
+    if (warp == kConsumers) {
+        if (lane == 0) {
+            for (int k = 0;; ++k) {
+                const int item = blockIdx.x + k * gridDim.x;
+                if (item >= items) break;
+                const int slot = k % kRing;
+                if (k >= kRing && !mbar_wait(&empty[slot], ((k / kRing) - 1) & 1, abort, dev_status)) break;
+                const int b = item / nchunks, chunk = item % nchunks;
+                const int j = __ldcg(sc.js + b);
+                s_j[slot] = j;
+                if (bulk) {
+                    const int64_t e0 = static_cast<int64_t>(chunk) * kChunk;
+                    const uint32_t bytes = static_cast<uint32_t>(imin64(kChunk, V - e0)) * 4;  // % 16 == 0
+                    float *dst = ring + slot * (2 * kChunk);
+                    mbar_arrive_expect_tx(&full[slot], j < D ? 2 * bytes : bytes);
+                    bulk_load(dst, p + (static_cast<int64_t>(b) * (D + 1) + j) * V + e0, bytes, &full[slot]);
+                    if (j < D)
+                        bulk_load(dst + kChunk, q + (static_cast<int64_t>(b) * D + j) * V + e0, bytes,
+                                  &full[slot]);
+                } else {
+                    mbar_arrive(&full[slot]);   // consumers read global memory directly
+                }
+            }
+        }
+        return;
+    }
+
+    for (int k = 0;; ++k) {
+        const int item = blockIdx.x + k * gridDim.x;
+        if (item >= items) break;
+        const int slot = k % kRing;
+        if (!mbar_wait_warp(&full[slot], (k / kRing) & 1, abort, dev_status)) break;
+        const int b = item / nchunks, chunk = item % nchunks;
+        const int j = s_j[slot];
+        const int residual = j < D;
+        const int64_t e0 = static_cast<int64_t>(chunk) * kChunk;
+        const int n = static_cast<int>(imin64(kChunk, V - e0));
+        const float *sp, *sq;
+        if (bulk) {
+            sp = ring + slot * (2 * kChunk);
+            sq = sp + kChunk;
+        } else {
+            sp = p + (static_cast<int64_t>(b) * (D + 1) + j) * V + e0;
+            sq = residual ? q + (static_cast<int64_t>(b) * D + j) * V + e0 : nullptr;
+        }
+        const unsigned long long t = bulk ? warp_step_masses<true>(sp, sq, residual, warp * kGroup, n, true, lane)
+                                          : warp_step_masses<false>(sp, sq, residual, warp * kGroup, n, false, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
+        const int s0 = chunk * (kChunk / kStep) + warp * kGroupSteps;
+        if (lane < kGroupSteps && s0 + lane < sc.nsteps)
+            sc.steps[static_cast<int64_t>(b) * sc.nsteps + s0 + lane] = t;
+        const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull);
+        const int gi = chunk * kConsumers + warp;
+        if (lane == 0 && gi < sc.ngroups) sc.gtot[static_cast<int64_t>(b) * sc.ngroups + gi] = gt;
+    }
+}
+
+// Stage 3: one warp per sequence draws the token: Z = sum of the group
+// masses, then the group, the step and finally the element whose running
+// sum first exceeds floor(u * Z) (re-reading only the 128 elements of one
+// step).
+__global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
     const float *__restrict__ p, const float *__restrict__ q, const float *__restrict__ u_res,
-    int D, int V, int nchunks, SampleScratch sc, int32_t *__restrict__ n_accepted,
+    int B, int D, int V, SampleScratch sc, int32_t *__restrict__ n_accepted,
     int32_t *__restrict__ token, uint32_t *dev_status, bool vec4)
 {
-    __shared__ unsigned long long s_wsum[kWarps];
-    __shared__ unsigned long long s_run;
-    __shared__ int s_step, s_last;
-    const int b = blockIdx.y, chunk = blockIdx.x;
+    pdl_wait();   // step and group masses come from the previous kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x * kWarps + warp;
+    if (b >= B) return;
     const int j = sc.js[b];
-    const float *prow = p + (static_cast<int64_t>(b) * (D + 1) + j) * V;
-    const float *qrow = j < D ? q + (static_cast<int64_t>(b) * D + j) * V : nullptr;
     int residual = j < D;
+    const float *prow = p + (static_cast<int64_t>(b) * (D + 1) + j) * V;
+    const float *qrow = residual ? q + (static_cast<int64_t>(b) * D + j) * V : nullptr;
     unsigned long long *steps = sc.steps + static_cast<int64_t>(b) * sc.nsteps;
-
-    {
-        const int64_t e0 = static_cast<int64_t>(chunk) * kChunk + warp * kWarpElems;
-        const unsigned long long t = warp_step_masses(prow, qrow, residual, e0, V, vec4, lane);
-        const int s0 = static_cast<int>(e0 / kStep);
-        if (lane < 8 && s0 + lane < sc.nsteps) steps[s0 + lane] = t;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        s_last = atomicAdd(&sc.cnt[b], 1u) == static_cast<unsigned>(nchunks - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+    unsigned long long *gtot = sc.gtot + static_cast<int64_t>(b) * sc.ngroups;
 
     float u = u_res[b];
     if (!(u >= 0.0f && u < 1.0f)) {
-        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
+        if (lane == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
         u = (u >= 1.0f) ? 0x1.fffffep-1f : 0.0f;
     }
+    unsigned long long Z = 0;
     for (int attempt = 0; attempt < 2; ++attempt) {
-        // Block-wide exclusive scan of the step masses, 4 consecutive steps per
-        // thread per pass.
-        const int per_pass = kThreads * 4;
-        unsigned long long Z = 0;
-        for (int s0 = 0; s0 < sc.nsteps; s0 += per_pass) {
-            unsigned long long t = 0;
-            for (int k = 0; k < 4; ++k) {
-                const int st = s0 + threadIdx.x * 4 + k;
-                if (st < sc.nsteps) t += __ldcg(steps + st);
-            }
-            t = warp_sum_u64(t);
-            if (lane == 0) s_wsum[warp] = t;
-            __syncthreads();
-            for (int w = 0; w < kWarps; ++w) Z += s_wsum[w];
-            __syncthreads();
+        unsigned long long z = 0;
+        for (int g = lane; g < sc.ngroups; g += 32) z += gtot[g];
+        Z = warp_sum_u64(z);
+        if (Z != 0 || !residual) break;
+        // reading: max(0, p - q) has no mass -> draw from the target row
+        // itself; this warp recomputes the step and group masses of p
+        residual = 0;
+        if (lane == 0) report(dev_status, SPEC_DEV_INFO_ZERO_RESIDUAL);
+        for (int g = 0; g < sc.ngroups; ++g) {
+            const int64_t g0 = static_cast<int64_t>(g) * kGroup;
+            const int n = static_cast<int>(imin64(kGroup, V - g0));
+            const unsigned long long t = warp_step_masses<false>(prow + g0, nullptr, 0, 0, n, false, lane);
+            if (lane < kGroupSteps && g * kGroupSteps + lane < sc.nsteps) steps[g * kGroupSteps + lane] = t;
+            const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull);
+            if (lane == 0) gtot[g] = gt;
         }
-        if (Z == 0) {
-            if (residual) {
-                // reading: max(0, p - q) has no mass -> draw from the target row
-                // itself; this CTA recomputes the step masses of p alone
-                residual = 0;
-                if (threadIdx.x == 0) report(dev_status, SPEC_DEV_INFO_ZERO_RESIDUAL);
-                for (int64_t e0 = warp * kWarpElems; e0 < V; e0 += kChunk) {
-                    const unsigned long long t = warp_step_masses(prow, nullptr, 0, e0, V, vec4, lane);
-                    const int s0 = static_cast<int>(e0 / kStep);
-                    if (lane < 8 && s0 + lane < sc.nsteps) steps[s0 + lane] = t;
-                }
-                __threadfence_block();
-                __syncthreads();
-                continue;
-            }
-            if (threadIdx.x == 0) {
-                report(dev_status, SPEC_DEV_ERR_ZERO_MASS);
-                n_accepted[b] = j;
-                token[b] = 0;
-                sc.cnt[b] = 0u;
-            }
-            return;
-        }
-        const unsigned long long T = scaled_threshold(u, Z);
-        // Locate the step holding the crossing: smallest step s with
-        // prefix(s) <= T < prefix(s) + mass(s).
-        if (threadIdx.x == 0) s_step = -1;
-        unsigned long long base = 0;
-        for (int s0 = 0; s0 < sc.nsteps; s0 += per_pass) {
-            unsigned long long v[4], t = 0;
-            for (int k = 0; k < 4; ++k) {
-                const int st = s0 + threadIdx.x * 4 + k;
-                v[k] = st < sc.nsteps ? __ldcg(steps + st) : 0ull;
-                t += v[k];
-            }
-            const unsigned long long incl = warp_incl_scan_u64(t, lane);
-            if (lane == 31) s_wsum[warp] = incl;
-            __syncthreads();
-            unsigned long long wpre = base, all = 0;
-            for (int w = 0; w < kWarps; ++w) {
-                if (w < warp) wpre += s_wsum[w];
-                all += s_wsum[w];
-            }
-            unsigned long long run = wpre + incl - t;
-            if (run <= T && T < run + t) {
-                for (int k = 0; k < 4; ++k) {
-                    if (T < run + v[k]) {
-                        s_step = s0 + threadIdx.x * 4 + k;
-                        s_run = run;
-                        break;
-                    }
-                    run += v[k];
-                }
-            }
-            base += all;
-            __syncthreads();
-        }
-        if (warp == 0 && s_step >= 0) {
-            const int64_t e = static_cast<int64_t>(s_step) * kStep + lane * 4;
-            const float4 xp = e < V ? load4(prow, e, V, vec4, 0.f) : make_float4(0, 0, 0, 0);
-            const float4 xq = (residual && e < V) ? load4(qrow, e, V, vec4, 0.f) : make_float4(0, 0, 0, 0);
-            const unsigned long long m[4] = {mass(xp.x, xq.x, residual), mass(xp.y, xq.y, residual),
-                                             mass(xp.z, xq.z, residual), mass(xp.w, xq.w, residual)};
-            const unsigned long long lane_sum = m[0] + m[1] + m[2] + m[3];
-            const unsigned long long incl = warp_incl_scan_u64(lane_sum, lane);
-            const unsigned long long run = s_run;
-            const unsigned hit = __ballot_sync(0xffffffffu, run + incl > T);
-            const int Lh = hit ? __ffs(hit) - 1 : 31;
-            if (lane == Lh) {
-                unsigned long long c = run + incl - lane_sum;
-                int v = static_cast<int>(e);
-                for (int k = 0; k < 4; ++k) {
-                    c += m[k];
-                    if (c > T) { v = static_cast<int>(e) + k; break; }
-                }
-                token[b] = v;
-            }
-        }
-        break;
+        __syncwarp();
     }
-    if (threadIdx.x == 0) {
+    if (Z == 0) {
+        if (lane == 0) {
+            report(dev_status, SPEC_DEV_ERR_ZERO_MASS);
+            n_accepted[b] = j;
+            token[b] = 0;
+        }
+        return;
+    }
+    const unsigned long long T = scaled_threshold(u, Z);
+    // the group holding the crossing: smallest g with prefix(g) <= T < prefix(g) + mass(g)
+    int found = -1;
+    unsigned long long run_g = 0, base = 0;
+    for (int g0 = 0; g0 < sc.ngroups && found < 0; g0 += 32) {
+        const int g = g0 + lane;
+        const unsigned long long v = g < sc.ngroups ? gtot[g] : 0ull;
+        const unsigned long long incl = warp_incl_scan_u64(v, lane);
+        const unsigned long long run = base + incl - v;
+        const unsigned hit = __ballot_sync(0xffffffffu, g < sc.ngroups && run <= T && T < run + v);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            found = g0 + l;
+            run_g = __shfl_sync(0xffffffffu, run, l);
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    int tok = 0;
+    if (found >= 0) {
+        // the step within the group
+        const int st = found * kGroupSteps + (lane % kGroupSteps);
+        const unsigned long long v = (lane < kGroupSteps && st < sc.nsteps) ? steps[st] : 0ull;
+        const unsigned long long incl = warp_incl_scan_u64(v, lane);
+        const unsigned long long run = run_g + incl - v;
+        const unsigned hit = __ballot_sync(0xffffffffu, lane < kGroupSteps && run <= T && T < run + v);
+        const int l = hit ? __ffs(hit) - 1 : 0;
+        const int step = found * kGroupSteps + l;
+        const unsigned long long run_s = __shfl_sync(0xffffffffu, run, l);
+        // the element within the step
+        const int64_t e = static_cast<int64_t>(step) * kStep + lane * 4;
+        const float4 xp = e < V ? load4(prow, e, V, vec4, 0.f) : make_float4(0, 0, 0, 0);
+        const float4 xq = (residual && e < V) ? load4(qrow, e, V, vec4, 0.f) : make_float4(0, 0, 0, 0);
+        const unsigned long long m[4] = {mass(xp.x, xq.x, residual), mass(xp.y, xq.y, residual),
+                                         mass(xp.z, xq.z, residual), mass(xp.w, xq.w, residual)};
+        const unsigned long long lane_sum = m[0] + m[1] + m[2] + m[3];
+        const unsigned long long lincl = warp_incl_scan_u64(lane_sum, lane);
+        const unsigned ehit = __ballot_sync(0xffffffffu, run_s + lincl > T);
+        const int Lh = ehit ? __ffs(ehit) - 1 : 31;
+        unsigned long long c = run_s + lincl - lane_sum;
+        int v_tok = static_cast<int>(e);
+        for (int k = 0; k < 4; ++k) {
+            c += m[k];
+            if (c > T) { v_tok = static_cast<int>(e) + k; break; }
+        }
+        tok = __shfl_sync(0xffffffffu, v_tok, Lh);
+    }
+    if (lane == 0) {
         n_accepted[b] = j;
-        sc.cnt[b] = 0u;     // ready for the next call
+        token[b] = tok;
     }
 }
 
@@ -495,8 +566,26 @@ cudaError_t launch_accept_greedy(const float *p, const int32_t *draft, int B, in
 size_t accept_sample_workspace_bytes(int B, int V)
 {
     const size_t nsteps = (static_cast<size_t>(V) + kStep - 1) / kStep;
-    return 2 * align256(sizeof(int32_t) * static_cast<size_t>(B)) +
+    const size_t ngroups = (static_cast<size_t>(V) + kGroup - 1) / kGroup;
+    return align256(sizeof(int32_t) * static_cast<size_t>(B)) +
+           align256(sizeof(unsigned long long) * ngroups * static_cast<size_t>(B)) +
            align256(sizeof(unsigned long long) * nsteps * static_cast<size_t>(B));
+}
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, uint32_t smem, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
 cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *draft,
@@ -504,21 +593,39 @@ cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *
                                  int32_t *n_acc, int32_t *token, void *workspace,
                                  uint32_t *dev_status, cudaStream_t st)
 {
-    const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
+    // bulk copies need 16-byte aligned rows: V % 4 == 0 and aligned bases
+    const bool bulk = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
                       (q == nullptr || reinterpret_cast<uintptr_t>(q) % 16 == 0);
     char *w = static_cast<char *>(workspace);
     SampleScratch sc;
-    sc.js = reinterpret_cast<int32_t *>(w);
-    sc.cnt = reinterpret_cast<uint32_t *>(w + align256(sizeof(int32_t) * B));
-    sc.steps = reinterpret_cast<unsigned long long *>(w + 2 * align256(sizeof(int32_t) * B));
     sc.nsteps = (V + kStep - 1) / kStep;
-    accept_prep_kernel<<<(B + kWarps - 1) / kWarps, kThreads, 0, st>>>(p, q, draft, u_acc, B, D, V, sc, dev_status);
-    cudaError_t e = cudaGetLastError();
+    sc.ngroups = (V + kGroup - 1) / kGroup;
+    sc.js = reinterpret_cast<int32_t *>(w);
+    w += align256(sizeof(int32_t) * B);
+    sc.gtot = reinterpret_cast<unsigned long long *>(w);
+    w += align256(sizeof(unsigned long long) * static_cast<size_t>(sc.ngroups) * B);
+    sc.steps = reinterpret_cast<unsigned long long *>(w);
+
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(accept_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kStreamSmem));
+    if (e != cudaSuccess) return e;
+
+    const unsigned sgrid = static_cast<unsigned>((B + kWarps - 1) / kWarps);
+    accept_prep_kernel<<<sgrid, kThreads, 0, st>>>(p, q, draft, u_acc, B, D, V, sc, dev_status);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int nchunks = (V + kChunk - 1) / kChunk;
-    accept_stream_kernel<<<dim3(nchunks, B), kThreads, 0, st>>>(p, q, u_res, D, V, nchunks, sc, n_acc, token,
-                                                               dev_status, vec4);
-    return cudaGetLastError();
+    const long long items = static_cast<long long>(B) * nchunks;
+    const int grid = static_cast<int>(items < sms ? items : sms);
+    e = launch_pdl(accept_stream_kernel, dim3(grid), dim3(kStreamThreads), kStreamSmem, st, p, q, D, V,
+                   nchunks, static_cast<int>(items), sc, dev_status, bulk);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(accept_finalize_kernel, dim3(sgrid), dim3(kThreads), 0u, st, p, q, u_res, B, D, V,
+                      sc, n_acc, token, dev_status, bulk);
 }
 
 }  // namespace spec

@@ -154,3 +154,21 @@ def test_repeat_calls_are_identical(sv, oracle_lib):
     a = run_sample(sv, inp["p"], inp["q"], inp["draft"], inp["u_acc"], inp["u_res"])
     b = run_sample(sv, inp["p"], inp["q"], inp["draft"], inp["u_acc"], inp["u_res"])
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_one_workspace_serves_many_calls(sv, oracle_lib):
+    """One workspace is reused by calls with different draft lengths (so
+    different rows are streamed): every result is exact."""
+    import torch
+    B, V = 48, 20000
+    ws = torch.empty(sv.accept_sample_workspace_size(B, V), dtype=torch.uint8, device="cuda")
+    for seed, D in ((21, 3), (22, 0), (23, 6)):
+        inp = synth.accept_inputs(seed, B, D, V, mode="sample")
+        n, t = sv.accept_sample(to_dev(inp["p"]), to_dev(inp["q"]) if D else None,
+                                to_dev(inp["draft"]) if D else None,
+                                to_dev(inp["u_acc"]) if D else None, to_dev(inp["u_res"]), workspace=ws)
+        torch.cuda.synchronize()
+        n_ref, t_ref, margin, _ = oracle_lib.accept_sample(inp["p"], inp["q"], inp["draft"], inp["u_acc"],
+                                                           inp["u_res"])
+        bad = (n.cpu().numpy() != n_ref) | (t.cpu().numpy() != t_ref)
+        assert not (bad & (margin >= MARGIN)).any()
