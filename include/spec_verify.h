@@ -197,6 +197,7 @@ spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_b
  *            their order matters).  NaN-free.
  *   draft    device, int32 [B][D].
  *   n_accepted, token   device, int32 [B].
+ *   dev_status  device uint32 or NULL (SPEC_DEV_ERR_TIMEOUT).
  * Supported set: B >= 0, 0 <= D <= 63, 1 <= V <= 2^26.
  * ---------------------------------------------------------------------- */
 spec_status_t spec_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,

@@ -71,6 +71,17 @@ __device__ __forceinline__ float4 load4(const float *row, int64_t e, int64_t end
     return r;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled now / wait until the previous one's results are visible.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ greedy
 struct ArgMax {
     float v;
@@ -93,38 +104,88 @@ __device__ __forceinline__ ArgMax warp_argmax(ArgMax a)
     return a;
 }
 
+__device__ __forceinline__ unsigned long long pack_argmax(ArgMax a)
+{
+    const uint32_t lo = a.i == INT_MAX ? 0xFFFFFFFFu : static_cast<uint32_t>(a.i);
+    return (static_cast<unsigned long long>(__float_as_uint(a.v)) << 32) | lo;
+}
+
+__device__ __forceinline__ ArgMax unpack_argmax(unsigned long long w)
+{
+    const uint32_t lo = static_cast<uint32_t>(w);
+    return {__uint_as_float(static_cast<uint32_t>(w >> 32)), lo == 0xFFFFFFFFu ? INT_MAX : static_cast<int>(lo)};
+}
+
+// Address of the same shared variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t peer_smem(const void *local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+
+// 8-byte store into a peer CTA's shared memory that completes on the peer's
+// mbarrier (both addresses in the cluster window).
+__device__ __forceinline__ void st_async_peer(uint32_t addr, unsigned long long v, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(addr),
+                 "l"(v), "r"(bar)
+                 : "memory");
+}
+
+constexpr int kGUnroll = 8;    // greedy: 128-element steps whose loads are in flight together
+
+// Greedy acceptance: one thread-block cluster of CS CTAs per sequence, CTA
+// `rank` owning a contiguous slice of the vocabulary.  Row by row, each CTA
+// reduces its slice to an argmax (all loads of a lane issued at once) and
+// sends the result to every CTA of the cluster with an asynchronous
+// distributed-shared-memory store that completes on the receiver's
+// mbarrier; every CTA then reduces the CS results itself and takes the same
+// decision, so no cluster-wide barrier sits on the per-row path.  Only rows
+// 0..n_accepted are read.
 template <int CS>
 __global__ void __launch_bounds__(kThreads, 4) accept_greedy_kernel(
     const float *__restrict__ p, const int32_t *__restrict__ draft, int D, int V,
-    int32_t *__restrict__ n_accepted, int32_t *__restrict__ token, bool vec4)
+    int32_t *__restrict__ n_accepted, int32_t *__restrict__ token, uint32_t *dev_status, bool vec4)
 {
     __shared__ ArgMax s_warp[kWarps];
-    __shared__ ArgMax s_cta[2];  // per row parity, read by the whole cluster
-    __shared__ ArgMax s_g[2];    // cluster-wide result, per row parity
+    __shared__ __align__(8) unsigned long long s_res[2][CS];   // per row parity, one per CTA
+    __shared__ uint64_t s_bar[2];
+    __shared__ int32_t s_draft[kMaxDraft];
+    __shared__ int s_abort;
     const int rank = CS > 1 ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
     const int b = blockIdx.x / CS;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Slice sl = warp_slice(V, CS, rank, warp);
-    // the drafts are read up front, off the per-row critical path
-    __shared__ int32_t s_draft[kMaxDraft];
+    volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
     for (int i = threadIdx.x; i < D; i += kThreads) s_draft[i] = draft[static_cast<int64_t>(b) * D + i];
-    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_init(&s_bar[0], 1);
+        mbar_init(&s_bar[1], 1);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    if constexpr (CS > 1) cg::this_cluster().sync();   // peers' barriers exist before any send
+    else __syncthreads();
 
     for (int i = 0; i <= D; ++i) {
+        const int par = i & 1;
+        if (CS > 1 && threadIdx.x == 0) mbar_arrive_expect_tx(&s_bar[par], CS * 8);
         const float *row = p + (static_cast<int64_t>(b) * (D + 1) + i) * V;
         // Per lane, elements are visited in increasing index order; only a
         // strictly larger value replaces the best, so ties keep the lowest
         // index.  The index is located only when a float4's max wins.
         ArgMax best{-FLT_MAX, INT_MAX};
-        for (int64_t base = sl.begin; base < sl.end; base += kStep * kUnroll) {
-            float4 x[kUnroll];
+        for (int64_t base = sl.begin; base < sl.end; base += kStep * kGUnroll) {
+            float4 x[kGUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                int64_t e = base + u * kStep + lane * 4;
-                x[u] = e < sl.end ? load4(row, e, sl.end, vec4, -INFINITY) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            for (int u = 0; u < kGUnroll; ++u) {
+                const int64_t e = base + u * kStep + lane * 4;
+                x[u] = e < sl.end ? load4(row, e, sl.end, vec4, -INFINITY)
+                                  : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < kGUnroll; ++u) {
                 const int e = static_cast<int>(base) + u * kStep + lane * 4;
                 const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
                 if (e < sl.end && (m4 > best.v || (best.i == INT_MAX && m4 == m4))) {
@@ -136,38 +197,35 @@ __global__ void __launch_bounds__(kThreads, 4) accept_greedy_kernel(
         best = warp_argmax(best);
         if (lane == 0) s_warp[warp] = best;
         __syncthreads();
-        if (threadIdx.x == 0) {
-            ArgMax c = s_warp[0];
-            for (int w = 1; w < kWarps; ++w) c = better(c, s_warp[w]);
-            s_cta[i & 1] = c;
-        }
-        ArgMax g;
-        if constexpr (CS > 1) {
-            // every peer's result is read at once, one lane per rank
-            cg::cluster_group cluster = cg::this_cluster();
-            cluster.sync();
-            if (warp == 0) {
-                ArgMax c{-FLT_MAX, INT_MAX};
-                if (lane < CS) c = *cluster.map_shared_rank(&s_cta[i & 1], lane);
-                c = warp_argmax(c);
-                if (lane == 0) s_g[i & 1] = c;
+        if (warp == 0) {
+            ArgMax c = lane < kWarps ? s_warp[lane] : ArgMax{-FLT_MAX, INT_MAX};
+            c = warp_argmax(c);
+            // this CTA's result, to every CTA of the cluster (itself included)
+            if (lane < CS) {
+                const unsigned long long w = pack_argmax(c);
+                if constexpr (CS > 1)
+                    st_async_peer(peer_smem(&s_res[par][rank], lane), w, peer_smem(&s_bar[par], lane));
+                else
+                    s_res[par][0] = w;   // a lone CTA: its own result is the row's
             }
-            __syncthreads();
-            g = s_g[i & 1];
-        } else {
-            __syncthreads();
-            g = s_cta[i & 1];
         }
-        const bool stop = (i == D) || (s_draft[i] != g.i);
+        bool ok = true;
+        if constexpr (CS > 1) ok = mbar_wait_warp(&s_bar[par], (i >> 1) & 1, abort, dev_status);
+        else __syncthreads();
+        ArgMax g{-FLT_MAX, INT_MAX};
+#pragma unroll
+        for (int r = 0; r < CS; ++r) g = better(g, unpack_argmax(s_res[par][r]));
+        const bool stop = !ok || i == D || s_draft[i] != g.i;
         if (stop) {
-            if (rank == 0 && threadIdx.x == 0) {
+            if (ok && rank == 0 && threadIdx.x == 0) {
                 n_accepted[b] = i;
                 token[b] = g.i;
             }
             break;
         }
+        __syncthreads();   // s_warp is rewritten by the next row
     }
-    // keep this CTA's shared memory alive until every peer has read it
+    // keep this CTA's shared memory alive until every peer is done with it
     if constexpr (CS > 1) cg::this_cluster().sync();
 }
 
@@ -256,16 +314,6 @@ constexpr int kStreamThreads = (kConsumers + 1) * 32;   // + 1 producer warp
 constexpr uint32_t kItemBytes = 2 * kChunk * 4;   // p and q slices of one item
 constexpr uint32_t kStreamSmem = kRing * kItemBytes + 1024;
 
-// Programmatic dependent launch: let the next kernel on the stream be
-// scheduled now / wait until the previous one's results are visible.
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
 
 // Stage 1: first rejected draft of every sequence (one warp per sequence);
 // the accept test u * q(x) < p(x) is evaluated in fp64, where the product
@@ -524,53 +572,7 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
     }
 }
 
-int pick_cluster(int V)
-{
-    if (V >= 32768) return 8;
-    if (V >= 8192) return 4;
-    if (V >= 2048) return 2;
-    return 1;
-}
-
-template <typename Kernel, typename... Args>
-cudaError_t launch_clustered(Kernel k, int B, int cs, cudaStream_t st, Args... args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(B) * cs);
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, args...);
-}
-
 }  // namespace
-
-cudaError_t launch_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,
-                                 int32_t *n_acc, int32_t *token, cudaStream_t st)
-{
-    const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0);
-    switch (pick_cluster(V)) {
-    case 8: return launch_clustered(accept_greedy_kernel<8>, B, 8, st, p, draft, D, V, n_acc, token, vec4);
-    case 4: return launch_clustered(accept_greedy_kernel<4>, B, 4, st, p, draft, D, V, n_acc, token, vec4);
-    case 2: return launch_clustered(accept_greedy_kernel<2>, B, 2, st, p, draft, D, V, n_acc, token, vec4);
-    default: return launch_clustered(accept_greedy_kernel<1>, B, 1, st, p, draft, D, V, n_acc, token, vec4);
-    }
-}
-
-size_t accept_sample_workspace_bytes(int B, int V)
-{
-    const size_t nsteps = (static_cast<size_t>(V) + kStep - 1) / kStep;
-    const size_t ngroups = (static_cast<size_t>(V) + kGroup - 1) / kGroup;
-    return align256(sizeof(int32_t) * static_cast<size_t>(B)) +
-           align256(sizeof(unsigned long long) * ngroups * static_cast<size_t>(B)) +
-           align256(sizeof(unsigned long long) * nsteps * static_cast<size_t>(B));
-}
 
 template <typename Kernel, typename... Args>
 cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, uint32_t smem, cudaStream_t st, Args... args)
@@ -586,6 +588,53 @@ cudaError_t launch_pdl(Kernel k, dim3 grid, dim3 block, uint32_t smem, cudaStrea
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
+int pick_cluster(int V)
+{
+    if (V >= 32768) return 8;
+    if (V >= 8192) return 4;
+    if (V >= 2048) return 2;
+    return 1;
+}
+
+template <int CS>
+cudaError_t launch_greedy_cs(const float *p, const int32_t *draft, int B, int D, int V, int32_t *n_acc,
+                             int32_t *token, uint32_t *dev_status, bool vec4, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B) * CS);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, accept_greedy_kernel<CS>, p, draft, D, V, n_acc, token, dev_status, vec4);
+}
+
+cudaError_t launch_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,
+                                 int32_t *n_acc, int32_t *token, uint32_t *dev_status, cudaStream_t st)
+{
+    const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0);
+    switch (pick_cluster(V)) {
+    case 8: return launch_greedy_cs<8>(p, draft, B, D, V, n_acc, token, dev_status, vec4, st);
+    case 4: return launch_greedy_cs<4>(p, draft, B, D, V, n_acc, token, dev_status, vec4, st);
+    case 2: return launch_greedy_cs<2>(p, draft, B, D, V, n_acc, token, dev_status, vec4, st);
+    default: return launch_greedy_cs<1>(p, draft, B, D, V, n_acc, token, dev_status, vec4, st);
+    }
+}
+
+size_t accept_sample_workspace_bytes(int B, int V)
+{
+    const size_t nsteps = (static_cast<size_t>(V) + kStep - 1) / kStep;
+    const size_t ngroups = (static_cast<size_t>(V) + kGroup - 1) / kGroup;
+    return align256(sizeof(int32_t) * static_cast<size_t>(B)) +
+           align256(sizeof(unsigned long long) * ngroups * static_cast<size_t>(B)) +
+           align256(sizeof(unsigned long long) * nsteps * static_cast<size_t>(B));
 }
 
 cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *draft,

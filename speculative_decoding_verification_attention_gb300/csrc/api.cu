@@ -43,14 +43,13 @@ spec_status_t spec_accept_greedy(const float *p, const int32_t *draft, int B, in
                                  int32_t *n_accepted, int32_t *token, uint32_t *dev_status,
                                  void *stream)
 {
-    (void)dev_status;
     if (B < 0 || D < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
     if (D > kMaxDraft || V > (1 << 26)) return SPEC_ERR_UNSUPPORTED;
     if (B == 0) return SPEC_OK;
     if (!p || !n_accepted || !token || (D > 0 && !draft)) return SPEC_ERR_INVALID_ARG;
     if (!aligned(p, 4) || !aligned(n_accepted, 4) || !aligned(token, 4)) return SPEC_ERR_INVALID_ARG;
     if (static_cast<long long>(B) * 8 > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
-    return from_cuda(launch_accept_greedy(p, draft, B, D, V, n_accepted, token,
+    return from_cuda(launch_accept_greedy(p, draft, B, D, V, n_accepted, token, dev_status,
                                           static_cast<cudaStream_t>(stream)));
 }
 

@@ -10,7 +10,7 @@ namespace spec {
 constexpr int kMaxDraft = 63;
 
 cudaError_t launch_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,
-                                 int32_t *n_acc, int32_t *token, cudaStream_t st);
+                                 int32_t *n_acc, int32_t *token, uint32_t *dev_status, cudaStream_t st);
 
 size_t accept_sample_workspace_bytes(int B, int V);
 

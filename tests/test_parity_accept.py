@@ -172,3 +172,26 @@ def test_one_workspace_serves_many_calls(sv, oracle_lib):
                                                            inp["u_res"])
         bad = (n.cpu().numpy() != n_ref) | (t.cpu().numpy() != t_ref)
         assert not (bad & (margin >= MARGIN)).any()
+
+
+def test_greedy_calls_with_changing_shapes(sv, oracle_lib):
+    """Back-to-back calls with different draft lengths on one stream: every
+    result is exact (the per-row exchange state starts fresh each call)."""
+    B, V = 40, 30000
+    for seed, D in ((31, 7), (32, 0), (33, 3), (34, 7)):
+        inp = synth.accept_inputs(seed, B, D, V, mode="greedy")
+        check_greedy(sv, oracle_lib, inp["p"], inp["draft"])
+
+
+def test_greedy_deep_rows_many_sequences(sv, oracle_lib):
+    """Drafts equal to the target argmax for most positions: sequences run
+    through many rows, so later rows wait on earlier decisions."""
+    B, D, V = 300, 7, 9000
+    inp = synth.accept_inputs(41, B, D, V, mode="greedy")
+    p = inp["p"]
+    draft = np.argmax(p[:, :D, :], axis=2).astype(np.int32)
+    rng = np.random.default_rng(5)
+    flip = rng.random((B, D)) < 0.1
+    draft[flip] = (draft[flip] + 1) % V
+    n = check_greedy(sv, oracle_lib, p, draft)
+    assert (n == D).sum() > 10
