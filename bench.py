@@ -335,7 +335,9 @@ def gpu_arm(args, rank, world):
                      "traffic_note": "DRAM read+write bytes per launch, from an ncu capture of a smaller "
                                      "case scaled by algorithmic bytes (profiles/verify_attention_small_B4_L32768_D7.md)",
                      "peak_source": pk["source"] + " (copy bandwidth, of measured)"},
-        "gpu_launches": 5 * K,
+        # per step: attention main + merge, GEMM, greedy accept, and the
+        # three stochastic-accept kernels (first rejection, stream, draw)
+        "gpu_launches": 7 * K,
         "wall_s_timed_region": wall,
         "clocks": clk.summary(dev.index or 0),
     }

@@ -56,6 +56,8 @@ typedef enum {
 #define SPEC_DEV_ERR_TOKEN_ID    0x00000008u /* draft token outside [0, V)               */
 #define SPEC_DEV_ERR_UNIFORM     0x00000010u /* uniform outside [0, 1)                   */
 #define SPEC_DEV_ERR_ZERO_MASS   0x00000020u /* a row to sample from has zero total mass */
+#define SPEC_DEV_ERR_LAUNCH      0x00000040u /* launched without the cluster shape it
+                                                needs (e.g. replayed by a tool): did nothing */
 #define SPEC_DEV_INFO_ZERO_RESIDUAL 0x00010000u /* informational: max(0,p-q) summed to 0
                                                    after a rejection; drew from p instead */
 
@@ -166,11 +168,11 @@ spec_status_t spec_verify_attention_noalloc(const void *q_bf16, const void *k_pa
  *   y_bf16   device, bf16 [M][N] row-major, 16-byte aligned.
  * Supported set: 1 <= M <= 65536, N a multiple of 128, K a multiple of 64.
  * workspace: spec_verify_gemm_workspace_size(M, N, K) bytes of device
- * memory, 256-byte aligned, owned by the caller.  It holds one ready flag
- * per CTA (the first 1024 bytes) and the fp32 partial tiles of the
- * stream-K split: zero it once before its first use (cudaMemset); every
- * call that completes leaves the flags zero again, also under CUDA-graph
- * replay.  Calls that share a
+ * memory, 256-byte aligned, owned by the caller.  It holds the arrival
+ * counters of the tiles cut between CTAs (the first 4096 bytes) and the
+ * fp32 partial tiles of the stream-K split: zero it once before its first
+ * use (cudaMemset); every call that completes leaves the counters zero
+ * again, also under CUDA-graph replay.  Calls that share a
  * workspace must not overlap in time.  A smaller workspace returns
  * SPEC_ERR_WORKSPACE.  The size depends on the current device's SM count
  * (without a device it is sized for 256 SMs).

@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = (
 
 DEV_STATUS_BITS = {
     "PAGE_ID": 0x1, "KV_LEN": 0x2, "TIMEOUT": 0x4, "TOKEN_ID": 0x8, "UNIFORM": 0x10,
-    "ZERO_MASS": 0x20, "INFO_ZERO_RESIDUAL": 0x10000,
+    "ZERO_MASS": 0x20, "LAUNCH": 0x40, "INFO_ZERO_RESIDUAL": 0x10000,
 }
 
 ATTENTION_KEY_TILE = 128   # SPEC_ATTENTION_KEY_TILE: keys per tile of the KV split

@@ -153,6 +153,10 @@ __global__ void __launch_bounds__(kThreads, 4) accept_greedy_kernel(
     __shared__ uint64_t s_bar[2];
     __shared__ int32_t s_draft[kMaxDraft];
     __shared__ int s_abort;
+    if (cluster_ctas() != static_cast<uint32_t>(CS)) {   // uniform over the grid
+        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
+        return;
+    }
     const int rank = CS > 1 ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
     const int b = blockIdx.x / CS;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

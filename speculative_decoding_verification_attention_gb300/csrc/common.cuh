@@ -32,6 +32,16 @@ __device__ __forceinline__ void report(uint32_t *dev_status, uint32_t bits)
     if (dev_status) atomicOr(dev_status, bits);
 }
 
+// CTAs in this CTA's cluster (1 without a cluster launch).  Kernels that use
+// cluster instructions check it first and do nothing when launched without
+// the shape they were built for.
+__device__ __forceinline__ uint32_t cluster_ctas()
+{
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {

@@ -18,9 +18,10 @@
 //    to MPAD, so the MMA is not mostly padding; the output is written
 //    transposed.
 // Both split the k-block iterations of all tiles evenly over the CTAs
-// (stream-K, see gemm_schedule.h); a tile cut between CTAs is summed by the
-// CTA holding its first k-block from the fp32 partials the others leave in
-// the workspace, in a fixed order, so results are deterministic.
+// (stream-K, see gemm_schedule.h).  Every piece of a tile cut between CTAs
+// leaves its fp32 partial in the workspace and counts itself in; the last
+// piece to arrive adds them all in k order (so results are deterministic)
+// and writes the tile.  No CTA waits for another.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
@@ -77,37 +78,13 @@ __device__ __forceinline__ void mma_kblock(uint32_t d_tmem, uint32_t a_smem, uin
     }
 }
 
-constexpr uint32_t kPartialReady = 0x5A17C0DEu;   // flag value of a published partial
+__device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
 {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-
-__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Bounded wait for a later CTA's partial.  All CTAs of the launch are
-// co-resident (cooperative launch), a CTA only waits on CTAs after it, and
-// each publishes its partial before it waits on anyone, so the wait ends;
-// the limit only guards against a fault elsewhere.
-__device__ bool wait_partial(const uint32_t *flag, volatile int *abort, uint32_t *dev_status)
-{
-    const unsigned long long t0 = globaltimer_ns();
-    for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (ld_acquire(flag) == kPartialReady) return true;
-        if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-            *abort = 1;
-            report(dev_status, SPEC_DEV_ERR_TIMEOUT);
-            return false;
-        }
-    }
 }
 
 __device__ __forceinline__ void store_bf16_row32(__nv_bfloat16 *dst_row, const float (&a)[32])
@@ -127,9 +104,46 @@ __device__ __forceinline__ void store_bf16_row32(__nv_bfloat16 *dst_row, const f
 // Partial tiles (128 rows x BN fp32) are laid out in 32-column units of
 // 16 KB, each [8 column quads][128 rows][4]: a warp's float4 accesses to one
 // quad are contiguous, and a unit is one bulk copy.
+__device__ __forceinline__ uint32_t unit_index(int quad, int row)
+{
+    return static_cast<uint32_t>((quad * kBM + row) * 4);
+}
 __device__ __forceinline__ uint32_t partial_index(int cc, int quad, int row)
 {
-    return static_cast<uint32_t>(((cc * 8 + quad) * kBM + row) * 4);
+    return static_cast<uint32_t>(cc * 32 * kBM) + unit_index(quad, row);
+}
+
+// Partial slot of the piece that unit v's CTA `rank` holds: two per CTA,
+// for the first and the last segment of its stream-K range.
+__device__ __forceinline__ int piece_slot(int v, int rank, bool first_segment, int unit_ctas)
+{
+    return (v * unit_ctas + rank) * 2 + (first_segment ? 0 : 1);
+}
+
+// Whether unit f's stream-K range starts exactly at tile t's first k-block
+// (then f's piece of t is its first segment).
+__device__ __forceinline__ bool other_first(const SkGrid &g, int f, int t)
+{
+    return g.begin(f) == static_cast<long long>(t - g.dp_tiles) * g.kblocks;
+}
+
+// Write 32 columns (chunk cc) of a finished output tile row as bf16.
+template <bool SWAP>
+__device__ __forceinline__ void store_out(__nv_bfloat16 *__restrict__ y, int M, int N, int t, int mt, int nt,
+                                          int BN, int row, int cc, const float (&a)[32])
+{
+    if (SWAP) {
+        // rows of the tile are w rows n; columns are x rows m
+        const int n = t * kBM + row;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int m = cc * 32 + j;
+            if (m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(a[j]);
+        }
+    } else {
+        const int m = mt * kBM + row;
+        if (m < M) store_bf16_row32(y + static_cast<int64_t>(m) * N + nt * BN + cc * 32, a);
+    }
 }
 
 template <int BN, int STAGES>
@@ -160,10 +174,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *acc_empty = acc_full + 2;
     uint64_t *drain = acc_empty + 2;
     uint64_t *pub_bar = drain + 1;      // 4 epilogue warps stored a partial
-    uint64_t *red_full = pub_bar + 1;   // a later piece's partial landed in the ring
-    uint64_t *red_empty = red_full + 1; // 4 epilogue warps finished reading it
+    uint64_t *dec_bar = pub_bar + 1;    // whether this piece arrived last is known
+    uint64_t *red_full = dec_bar + 1;   // other pieces' partials landed in the ring
+    uint64_t *red_empty = red_full + 1; // 4 epilogue warps finished reading them
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(red_empty + 1);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *s_last = abort + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // tiled: CTA within its pair, and the pair index (the unit of the split)
@@ -171,6 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c = SWAP ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x >> 1);
     constexpr int kUnit = SWAP ? 1 : 2;   // CTAs per unit of the split
     constexpr uint16_t kPair = 0x3;
+    if (cluster_ctas() != static_cast<uint32_t>(kUnit)) {   // uniform over the grid
+        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         // tiled: a stage is free once the MMAs of both CTAs of the pair read it
@@ -178,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < 2; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 4); }
         mbar_init(drain, 1);
         mbar_init(pub_bar, 4);
+        mbar_init(dec_bar, 1);
         mbar_init(red_full, 1);
         mbar_init(red_empty, 4);
         *abort = 0;
@@ -250,19 +271,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;
         // swap: only the 32-column chunks that hold rows of x are needed
         const int nchunks = SWAP ? (M + 31) / 32 < BN / 32 ? (M + 31) / 32 : BN / 32 : BN / 32;
+        const int unit_bytes = nchunks * 32 * kBM * 4;   // one piece's partial
         SegWalker wk(grid, c);
         Seg s;
-        uint32_t lt = 0, npub = 0, nred = 0;
+        uint32_t lt = 0, npub = 0, nred = 0, ndec = 0;
         while (!*abort && wk.next(s)) {
             const uint32_t ab = lt & 1;
             if (!mbar_wait_warp(&acc_full[ab], (lt >> 1) & 1, abort, dev_status)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((quad * 32) << 16) + ab * BN;
-            if (s.kb0 > 0) {
-                // A later piece of a cut tile: publish the fp32 partial.
-                float *slot = part + static_cast<size_t>(blockIdx.x) * kBM * BN;
+            const int mt = 2 * (s.t % grid.tiles_m) + rank, nt = s.t / grid.tiles_m;
+            bool ok = true;
+            if (s.kb0 == 0 && s.kb1 == grid.kblocks) {
+                // a whole tile
 #pragma unroll 1
                 for (int cc = 0; cc < nchunks; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + cc * 32, r);
+                    tmem_ld_wait();
+                    float a[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(r[j]);
+                    store_out<SWAP>(y, M, N, s.t, mt, nt, BN, row, cc, a);
+                }
+            } else {
+                // A piece of a cut tile: publish the fp32 partial, then count
+                // the tile's published pieces; the last piece to arrive adds
+                // all of them in k order and writes the tile.  No CTA ever
+                // waits for another, so residency is never assumed.
+                int f, l;
+                sk_tile_units(grid, s.t, f, l);
+                const int me = c;
+                const int my_slot = piece_slot(me, rank, sk_first_segment(grid, me, s), kUnit);
+                float *slot = part + static_cast<size_t>(my_slot) * kBM * BN;
+                uint32_t *cnt = flags + (s.t - grid.dp_tiles) * kUnit + rank;
+                // A piece that ends its unit's range usually finishes with or
+                // after the others: if all of them have arrived already it is
+                // the last for sure and need not publish its own partial.
+                bool sure_last = false;
+                if (!wk.has_more()) {
+                    uint32_t seen = 0;
+                    if (lane == 0) seen = ld_acquire(cnt);
+                    sure_last = __shfl_sync(0xffffffffu, seen, 0) == static_cast<uint32_t>(l - f);
+                }
+#pragma unroll 1
+                for (int cc = 0; cc < nchunks && !sure_last; ++cc) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + cc * 32, r);
                     tmem_ld_wait();
@@ -272,114 +325,118 @@ __global__ void __launch_bounds__(kThreads, 1)
                                make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
                                            __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3])));
                 }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&acc_empty[ab]);
-                    mbar_arrive(pub_bar);
+                if (lane == 0) mbar_arrive(pub_bar);
+                if (threadIdx.x == 64) {
+                    bool last = false;
+                    if (mbar_wait(pub_bar, npub & 1, abort, dev_status)) {
+                        if (sure_last) {
+                            last = true;
+                        } else {
+                            __threadfence();
+                            last = atomicAdd(cnt, 1u) == static_cast<uint32_t>(l - f);
+                        }
+                        if (last) {
+                            __threadfence();
+                            *cnt = 0u;   // zero again for the next call
+                        }
+                    }
+                    *s_last = last ? 1 : 0;
+                    mbar_arrive(dec_bar);
                 }
-                // the release store is cumulative: it also orders the other
-                // epilogue threads' partial stores, which this thread observed
-                // through pub_bar
-                if (threadIdx.x == 64 && mbar_wait(pub_bar, npub & 1, abort, dev_status))
-                    st_release(&flags[blockIdx.x], kPartialReady);
                 __syncwarp();
                 ++npub;
-            } else {
-                // A whole tile, or the first piece of a cut tile, which this
-                // CTA owns.  The later pieces' partials are fetched one at a
-                // time by bulk copies into the stage ring -- idle by now, as
-                // an owned cut piece is always the CTA's last segment -- and
-                // added; a running sum between passes stays in tensor memory.
-                // The partials are taken last piece first: a piece at the
-                // start of its CTA's range was published long ago, while the
-                // piece right after this one ends when this one does.  The
-                // order is fixed, so results are deterministic.
-                const int last = sk_last_contributor(grid, c, s);
-                const int ncontrib = last - c;
-                // partials per pass: as many as fit in the stage ring at once
-                const int unit_bytes = nchunks * 32 * kBM * 4;
-                const int per_pass = (STAGES * static_cast<int>(L::kStage)) / unit_bytes;
-                const int npass = ncontrib > 0 ? (ncontrib + per_pass - 1) / per_pass : 1;
-                const float *ring = reinterpret_cast<const float *>(smem);
-                bool ok = true;
-                for (int q = 0; q < npass && ok; ++q) {
-                    const int k0 = q * per_pass;   // contributors k0 .. k1-1 of this pass,
-                    const int k1 = ncontrib < k0 + per_pass ? ncontrib : k0 + per_pass;
-                    if (ncontrib > 0) {            // counted from the last one
-                        if (threadIdx.x == 64) {
-                            bool go = nred == 0 || mbar_wait(red_empty, (nred - 1) & 1, abort, dev_status);
-                            if (go) mbar_arrive_expect_tx(red_full, (k1 - k0) * unit_bytes);
-                            for (int k = k0; k < k1 && go; ++k) {
-                                const int p = kUnit * (last - k) + rank;   // same rank in a later unit
-                                go = wait_partial(&flags[p], abort, dev_status);
-                                if (!go) break;
-                                flags[p] = 0;   // zero again for the next call
-                                fence_proxy_async_all();
-                                const float *slot = part + static_cast<size_t>(p) * kBM * BN;
-                                uint8_t *dst = smem + (k - k0) * unit_bytes;
-                                for (int u = 0; u < nchunks; ++u)
-                                    bulk_load(dst + u * 32 * kBM * 4, slot + u * 32 * kBM, 32 * kBM * 4,
-                                              red_full);
+                ok = mbar_wait_warp(dec_bar, ndec & 1, abort, dev_status);
+                ++ndec;
+                if (ok && *s_last) {
+                    // other pieces' partials: through the stage ring with bulk
+                    // copies when this is the unit's last segment (the ring is
+                    // idle then), else straight from L2
+                    const bool ring_ok = !wk.has_more();
+                    const float *ring = reinterpret_cast<const float *>(smem);
+                    const int others = l - f;
+                    const int per_pass_chunks =
+                        ring_ok ? imin((STAGES * static_cast<int>(L::kStage)) / (others * 32 * kBM * 4), nchunks)
+                                : 1;
+                    for (int c0 = 0; c0 < nchunks && ok; c0 += per_pass_chunks) {
+                        const int c1 = imin(nchunks, c0 + per_pass_chunks);
+                        if (ring_ok) {
+                            if (threadIdx.x == 64) {
+                                bool go = nred == 0 || mbar_wait(red_empty, (nred - 1) & 1, abort, dev_status);
+                                if (go) {
+                                    fence_proxy_async_all();
+                                    mbar_arrive_expect_tx(red_full, (c1 - c0) * others * 32 * kBM * 4);
+                                    int k = 0;
+                                    for (int v = f; v <= l; ++v) {
+                                        if (v == me) continue;
+                                        const float *src = part + static_cast<size_t>(
+                                            piece_slot(v, rank, v != f || other_first(grid, f, s.t), kUnit)) * kBM * BN;
+                                        for (int cc = c0; cc < c1; ++cc)
+                                            bulk_load(smem + ((cc - c0) * others + k) * 32 * kBM * 4,
+                                                      src + cc * 32 * kBM, 32 * kBM * 4, red_full);
+                                        ++k;
+                                    }
+                                }
                             }
+                            __syncwarp();
+                            ok = mbar_wait_warp(red_full, nred & 1, abort, dev_status);
+                            if (!ok) break;
                         }
-                        // the rest of warp 2 waits here rather than polling the
-                        // barrier, which would stall lane 0's divergent path
-                        __syncwarp();
-                        ok = mbar_wait_warp(red_full, nred & 1, abort, dev_status);
-                        if (!ok) break;
-                    }
-                    const bool final_pass = q + 1 == npass;
 #pragma unroll 1
-                    for (int cc = 0; cc < nchunks; ++cc) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(tbase + cc * 32, r);
-                        tmem_ld_wait();
-                        float a[32];
+                        for (int cc = c0; cc < c1; ++cc) {
+                            uint32_t r[32];
+                            tmem_ld_32x32b_x32(tbase + cc * 32, r);
+                            tmem_ld_wait();
+                            float a[32];
+                            int k = 0;
+                            for (int v = f; v <= l; ++v) {
+                                float4 pv[8];
+                                if (v == me) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(r[j]);
-                        for (int k = k0; k < k1; ++k) {
-                            const float *src = ring + (k - k0) * (unit_bytes / 4);
+                                    for (int q4 = 0; q4 < 8; ++q4)
+                                        pv[q4] = make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
+                                                             __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
+                                } else {
+                                    if (ring_ok) {
+                                        const float *u = ring + ((cc - c0) * others + k) * 32 * kBM;
 #pragma unroll
-                            for (int q4 = 0; q4 < 8; ++q4) {
-                                const float4 v = *reinterpret_cast<const float4 *>(src + partial_index(cc, q4, row));
-                                a[4 * q4] += v.x;
-                                a[4 * q4 + 1] += v.y;
-                                a[4 * q4 + 2] += v.z;
-                                a[4 * q4 + 3] += v.w;
+                                        for (int q4 = 0; q4 < 8; ++q4)
+                                            pv[q4] = *reinterpret_cast<const float4 *>(u + unit_index(q4, row));
+                                    } else {
+                                        const float *src = part + static_cast<size_t>(piece_slot(
+                                            v, rank, v != f || other_first(grid, f, s.t), kUnit)) * kBM * BN;
+#pragma unroll
+                                        for (int q4 = 0; q4 < 8; ++q4)
+                                            pv[q4] = __ldcg(reinterpret_cast<const float4 *>(src + partial_index(cc, q4, row)));
+                                    }
+                                    ++k;
+                                }
+                                // k order, the same whichever piece arrived last
+#pragma unroll
+                                for (int q4 = 0; q4 < 8; ++q4) {
+                                    if (v == f) {
+                                        a[4 * q4] = pv[q4].x; a[4 * q4 + 1] = pv[q4].y;
+                                        a[4 * q4 + 2] = pv[q4].z; a[4 * q4 + 3] = pv[q4].w;
+                                    } else {
+                                        a[4 * q4] += pv[q4].x; a[4 * q4 + 1] += pv[q4].y;
+                                        a[4 * q4 + 2] += pv[q4].z; a[4 * q4 + 3] += pv[q4].w;
+                                    }
+                                }
                             }
+                            store_out<SWAP>(y, M, N, s.t, mt, nt, BN, row, cc, a);
                         }
-                        if (!final_pass) {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(a[j]);
-                            tmem_st_32x32b_x32(tbase + cc * 32, r);
-                        } else if constexpr (SWAP) {
-                            // rows of the tile are w rows n; columns are x rows m
-                            const int n = s.t * kBM + row;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const int m = cc * 32 + j;
-                                if (m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(a[j]);
-                            }
-                        } else {
-                            const int mt = 2 * (s.t % grid.tiles_m) + rank, nt = s.t / grid.tiles_m;
-                            const int m = mt * kBM + row;
-                            if (m < M)
-                                store_bf16_row32(y + static_cast<int64_t>(m) * N + nt * BN + cc * 32, a);
+                        if (ring_ok) {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(red_empty);
+                            ++nred;
                         }
-                    }
-                    if (!final_pass) tmem_st_wait();
-                    if (ncontrib > 0) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(red_empty);
-                        ++nred;
                     }
                 }
-                if (!ok) break;
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[ab]);
             }
+            if (!ok) break;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[ab]);
             ++lt;
         }
     }
@@ -413,9 +470,6 @@ cudaLaunchConfig_t kernel_config(int grid, cudaStream_t st, cudaLaunchAttribute 
         attr[n].val.clusterDim.z = 1;
         ++n;
     }
-    attr[n].id = cudaLaunchAttributeCooperative;   // owners wait on later CTAs' partials
-    attr[n].val.cooperative = 1;
-    ++n;
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cfg;
@@ -541,7 +595,7 @@ GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_tiled)
     p.sk.G = units;
     p.sk.dp_tiles = waves >= 2 ? (waves - 1) * units : 0;
     p.sk.sk_iters = static_cast<long long>(tiles - p.sk.dp_tiles) * kblocks;
-    p.workspace_bytes = kFlagBytes + static_cast<size_t>(p.grid) * kBM * p.bn * 4;
+    p.workspace_bytes = kFlagBytes + 2 * static_cast<size_t>(p.grid) * kBM * p.bn * 4;
     return p;
 }
 

@@ -10,10 +10,11 @@
 
 namespace spec {
 
-// Workspace of the GEMM: one ready flag per CTA (at most kMaxCtas CTAs) in
-// the first kFlagBytes, then one fp32 128 x BN partial tile per CTA.
+// Workspace of the GEMM: an arrival counter per stream-K tile and CTA rank
+// (fewer than 2 * kMaxCtas of them) in the first kFlagBytes, then two fp32
+// 128 x BN partial tiles per CTA (its first and last stream-K segment).
 constexpr int kMaxCtas = 256;
-constexpr size_t kFlagBytes = 1024;
+constexpr size_t kFlagBytes = 4096;
 
 struct GemmPlan {
     bool swap;     // w rows on the MMA M side (M <= 256), x rows padded to bn

@@ -6,10 +6,9 @@
 // (t / tiles_m) * BN.  The first dp_tiles tiles are whole-tile work (CTA c
 // takes c, c + G, c + 2G, ...); the k-block iterations of the remaining
 // tiles are cut into G equal contiguous ranges, one per CTA (stream-K), so
-// every SM gets the same number of MMAs whatever the tile count.  A tile
-// cut between CTAs is finished by the CTA holding its first k-block (its
-// owner), which adds, in CTA order, the fp32 partial sums that the later
-// CTAs holding the rest of the tile left in the workspace.
+// every SM gets the same number of MMAs whatever the tile count.  The
+// pieces of a tile cut between CTAs are added, in k order, by whichever
+// piece is finished last.
 #pragma once
 
 #include <stdint.h>
@@ -56,11 +55,13 @@ struct SegWalker {
         it += s.kb1 - s.kb0;
         return true;
     }
+    // whether a segment follows the one next() returned last
+    SPEC_HD bool has_more() const { return w * g.G < g.dp_tiles || it < end; }
 };
 
-// For a segment that starts its tile (kb0 == 0) on CTA c: the last CTA
+// For a segment that starts its tile (kb0 == 0) on unit c: the last unit
 // holding a later piece of the same tile (c itself when the tile is whole).
-// The pieces' holders are exactly CTAs c+1 .. last.
+// The pieces' holders are exactly units c+1 .. last.
 SPEC_HD int sk_last_contributor(const SkGrid &g, int c, const Seg &s)
 {
     int last = c;
@@ -69,6 +70,32 @@ SPEC_HD int sk_last_contributor(const SkGrid &g, int c, const Seg &s)
         while (last + 1 < g.G && g.begin(last + 1) < tile_end) ++last;
     }
     return last;
+}
+
+// The unit whose stream-K range holds iteration x (0 <= x < sk_iters).
+SPEC_HD int sk_unit_of(const SkGrid &g, long long x)
+{
+    int u = static_cast<int>(x * g.G / g.sk_iters);
+    while (u + 1 < g.G && g.begin(u + 1) <= x) ++u;
+    while (u > 0 && g.begin(u) > x) --u;
+    return u;
+}
+
+// The units holding pieces of stream-K tile t (t >= dp_tiles): f .. l, in
+// k order; f holds the first k-block.
+SPEC_HD void sk_tile_units(const SkGrid &g, int t, int &f, int &l)
+{
+    const long long x0 = static_cast<long long>(t - g.dp_tiles) * g.kblocks;
+    f = sk_unit_of(g, x0);
+    l = sk_unit_of(g, x0 + g.kblocks - 1);
+}
+
+// Whether segment s of unit u is the first segment of u's stream-K range
+// (a unit has at most two cut pieces: its first and its last segment).
+SPEC_HD bool sk_first_segment(const SkGrid &g, int u, const Seg &s)
+{
+    return s.t >= g.dp_tiles &&
+           static_cast<long long>(s.t - g.dp_tiles) * g.kblocks + s.kb0 == g.begin(u);
 }
 
 }  // namespace spec
