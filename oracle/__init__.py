@@ -20,6 +20,15 @@ Parity status of each function (what pins it, in tests/test_oracle_*.py):
                     emitted tokens equal plain greedy decoding.
   accept_sample     exact enumeration on a toy model (emitted sequence law
                     equals the target's), tau closed form, chi-square.
+  tree_attention    a chain tree equals verify_attention bit for bit; every
+                    node's row equals decode attention over the prefix
+                    followed by its root-to-node path (gathered cache);
+                    brute force vs torch's fp64 attention with a
+                    materialised tree mask.
+  accept_tree_greedy  a chain tree equals accept_greedy; brute force over
+                    the accepted-node set on trees with distinct sibling
+                    tokens; emitted tokens equal plain greedy decoding of a
+                    toy target model.
 """
 from __future__ import annotations
 
@@ -63,8 +72,12 @@ def _load():
             lib.oracle_gemm.argtypes = [P, P, i32, i32, i32, i32, P, P, i32]
             lib.oracle_accept_greedy.argtypes = [P, P, i32, i32, i32, P, P, i32]
             lib.oracle_accept_sample.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, P, P, i32]
+            lib.oracle_tree_attention.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
+                                                  i32, f64, i64, i32, P, P, P, i32]
+            lib.oracle_accept_tree_greedy.argtypes = [P, P, P, i32, i32, i32, P, P, P, i32]
             for f in ("oracle_verify_attention", "oracle_gemm", "oracle_accept_greedy",
-                      "oracle_accept_sample", "oracle_max_threads"):
+                      "oracle_accept_sample", "oracle_max_threads", "oracle_tree_attention",
+                      "oracle_accept_tree_greedy"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -171,3 +184,54 @@ def accept_sample(p, q, draft, u_acc, u_res, threads=0):
     if rc:
         raise ValueError(f"oracle_accept_sample failed: {rc}")
     return n_acc, tok, margin, fb
+
+
+def tree_attention(q, k_pages, v_pages, block_table, kv_len, parent, D, Hkv, G, head_dim,
+                   page_size, softmax_scale=None, rows=None, threads=0):
+    """fp64 tree verify attention (reading R7).  As verify_attention, plus
+    parent int32 [B, 1+D] (parent[:, 0] = -1, 0 <= parent[b, k] < k)."""
+    lib = _load()
+    q, k_pages, v_pages = (_c(a, np.uint16) for a in (q, k_pages, v_pages))
+    block_table = _c(block_table, np.int32)
+    kv_len = _c(kv_len, np.int32)
+    parent = _c(parent, np.int32)
+    B = kv_len.shape[0]
+    Hq = Hkv * G
+    if softmax_scale is None:
+        softmax_scale = 1.0 / np.sqrt(head_dim)
+    P = k_pages.shape[0]
+    if rows is not None:
+        rows = _c(rows, np.int32).reshape(-1, 4)
+        n = rows.shape[0]
+        out = np.empty((n, head_dim), dtype=np.float64)
+        lse = np.empty((n,), dtype=np.float64)
+    else:
+        n = 0
+        out = np.empty((B, 1 + D, Hq, head_dim), dtype=np.float64)
+        lse = np.empty((B, 1 + D, Hq), dtype=np.float64)
+    rc = lib.oracle_tree_attention(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                   block_table.shape[1], _ptr(kv_len), _ptr(parent), B, D, Hkv, G,
+                                   head_dim, page_size, float(softmax_scale), P, n, _ptr(rows),
+                                   _ptr(out), _ptr(lse), int(threads))
+    if rc:
+        raise ValueError(f"oracle_tree_attention failed: {rc}")
+    return out, lse
+
+
+def accept_tree_greedy(p, tokens, parent, threads=0):
+    """Greedy tree acceptance (reading R8): p float32 [B, 1+D, V], tokens and
+    parent int32 [B, 1+D].  Returns (n_accepted, token, path [B, D])."""
+    lib = _load()
+    p = _c(p, np.float32)
+    tokens = _c(tokens, np.int32)
+    parent = _c(parent, np.int32)
+    B, T, V = p.shape
+    D = T - 1
+    n = np.empty(B, np.int32)
+    t = np.empty(B, np.int32)
+    path = np.empty((B, max(D, 1)), np.int32)
+    rc = lib.oracle_accept_tree_greedy(_ptr(p), _ptr(tokens), _ptr(parent), B, D, V, _ptr(n), _ptr(t),
+                                       _ptr(path), int(threads))
+    if rc:
+        raise ValueError(f"oracle_accept_tree_greedy failed: {rc}")
+    return n, t, path[:, :D]

@@ -313,3 +313,169 @@ int oracle_accept_sample(const float *p, const float *q, const int32_t *draft,
     }
     return err;
 }
+
+/* ------------------------------------------------------------------------
+ * Tree verification (Medusa / EAGLE-2 style draft trees).
+ *
+ * "The candidates ... are combined into a tree of possible continuations;
+ * the target model evaluates the whole tree in one forward pass with tree
+ * attention, whose attention mask keeps causality inside each candidate
+ * branch; the longest accepted candidate prefix moves on to the next
+ * decoding step" (LLM inference handbook, "Speculative decoding", section
+ * on Medusa; EAGLE-2's dynamic draft tree in the same section).
+ *
+ * The tree of sequence b has T = 1 + D nodes in topological order:
+ * parent[b][0] = -1 (node 0 is the last accepted token, the root) and
+ * 0 <= parent[b][k] < k for k >= 1.  Node k's K/V occupy cache position
+ * kv_len[b] - T + k.
+ *  R7 node k's query attends to the prefix keys j < kv_len[b] - T and to
+ *     the tree keys of the nodes on its root-to-k path (its ancestors and
+ *     itself).  A chain (parent[k] = k - 1) is reading R1.
+ *  R8 greedy tree acceptance: from the root, repeatedly move to the child
+ *     whose token equals the target argmax at the current node (the lowest
+ *     node index if several siblings carry it); stop when no child matches.
+ *     n_acc = the depth reached, the emitted token is the argmax at the
+ *     last node, and the path lists the accepted nodes in order.  A chain
+ *     whose node k carries draft k-1 is the greedy acceptance above.
+ * ---------------------------------------------------------------------- */
+
+/* Whether parent[0..T) is a valid tree in topological order. */
+static int tree_valid(const int32_t *parent, int T)
+{
+    if (T < 1 || parent[0] != -1) return 0;
+    for (int k = 1; k < T; ++k)
+        if (parent[k] < 0 || parent[k] >= k) return 0;
+    return 1;
+}
+
+static int tree_attention_row(const uint16_t *q, const uint16_t *kp, const uint16_t *vp,
+                              const int32_t *block_table, int max_pages, const int32_t *kv_len,
+                              const int32_t *parent, int D, int Hkv, int G, int d, int page_size,
+                              double scale, int64_t num_pages, int b, int k, int h, int g,
+                              double *out, double *lse, double *scratch, int64_t *keys)
+{
+    const int T = 1 + D, Hq = Hkv * G;
+    const int32_t *par = parent + (int64_t)b * T;
+    const int64_t P = (int64_t)kv_len[b] - T;   /* prefix keys */
+    /* visible keys, ascending: the prefix, then the tree path root..k */
+    int onpath[64];
+    for (int a = 0; a < T; ++a) onpath[a] = 0;
+    for (int a = k; a >= 0; a = par[a]) onpath[a] = 1;
+    int64_t n = 0;
+    for (int64_t j = 0; j < P; ++j) keys[n++] = j;
+    for (int a = 0; a < T; ++a) if (onpath[a]) keys[n++] = P + a;
+    const uint16_t *qrow = q + (((int64_t)b * T + k) * Hq + (int64_t)h * G + g) * d;
+    double m = -INFINITY;
+    for (int64_t x = 0; x < n; ++x) {
+        const int64_t j = keys[x];
+        int32_t page = block_table[(int64_t)b * max_pages + j / page_size];
+        if (page < 0 || page >= num_pages) return -1;
+        const uint16_t *krow = kp + (((int64_t)page * page_size + j % page_size) * Hkv + h) * d;
+        double s = 0.0;
+        for (int c = 0; c < d; ++c) s += bf16_to_f64(qrow[c]) * bf16_to_f64(krow[c]);
+        s *= scale;
+        scratch[x] = s;
+        if (s > m) m = s;
+    }
+    double l = 0.0;
+    for (int c = 0; c < d; ++c) out[c] = 0.0;
+    for (int64_t x = 0; x < n; ++x) {
+        const int64_t j = keys[x];
+        int32_t page = block_table[(int64_t)b * max_pages + j / page_size];
+        const uint16_t *vrow = vp + (((int64_t)page * page_size + j % page_size) * Hkv + h) * d;
+        double w = exp(scratch[x] - m);
+        l += w;
+        for (int c = 0; c < d; ++c) out[c] += w * bf16_to_f64(vrow[c]);
+    }
+    for (int c = 0; c < d; ++c) out[c] /= l;
+    if (lse) *lse = m + log(l);
+    return 0;
+}
+
+/* Tree verify attention; arguments as oracle_verify_attention plus
+ * parent [B][1+D] (1 + D <= 64).  Returns -4 for an invalid tree. */
+int oracle_tree_attention(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                          const int32_t *block_table, int max_pages_per_seq,
+                          const int32_t *kv_len, const int32_t *parent, int B, int D, int Hkv,
+                          int G, int head_dim, int page_size, double softmax_scale,
+                          int64_t num_pages, int n_rows, const int32_t *rows, double *out,
+                          double *lse, int num_threads)
+{
+    if (B < 0 || D < 0 || D > 63 || Hkv < 1 || G < 1 || head_dim < 1 || page_size < 1) return -2;
+    for (int b = 0; b < B; ++b) {
+        if (kv_len[b] < 1 + D || (int64_t)kv_len[b] > (int64_t)max_pages_per_seq * page_size)
+            return -3;
+        if (!tree_valid(parent + (int64_t)b * (1 + D), 1 + D)) return -4;
+    }
+    const int Hq = Hkv * G;
+    const int64_t total = rows ? (int64_t)n_rows : (int64_t)B * (1 + D) * Hq;
+    int64_t max_len = 1;
+    for (int b = 0; b < B; ++b) if (kv_len[b] > max_len) max_len = kv_len[b];
+    int err = 0;
+    set_threads(num_threads);
+#pragma omp parallel
+    {
+        double *scratch = (double *)malloc(sizeof(double) * (size_t)max_len);
+        int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * (size_t)max_len);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < total; ++r) {
+            int b, k, h, g;
+            if (rows) {
+                b = rows[4 * r]; k = rows[4 * r + 1]; h = rows[4 * r + 2]; g = rows[4 * r + 3];
+            } else {
+                int64_t t = r;
+                g = (int)(t % G); t /= G;
+                h = (int)(t % Hkv); t /= Hkv;
+                k = (int)(t % (1 + D)); t /= (1 + D);
+                b = (int)t;
+            }
+            int rc = tree_attention_row(q, k_pages, v_pages, block_table, max_pages_per_seq,
+                                        kv_len, parent, D, Hkv, G, head_dim, page_size,
+                                        softmax_scale, num_pages, b, k, h, g,
+                                        out + r * head_dim, lse ? lse + r : NULL, scratch, keys);
+            if (rc) {
+#pragma omp atomic write
+                err = rc;
+            }
+        }
+        free(scratch);
+        free(keys);
+    }
+    return err;
+}
+
+/* Greedy tree acceptance (reading R8).  p [B][1+D][V] target probabilities
+ * at every node, tokens [B][1+D] the node tokens (node 0's is unused),
+ * parent [B][1+D].  Outputs n_accepted [B], token [B] and path [B][D]
+ * (accepted node ids in order, -1 after the last).  Returns -4 for an
+ * invalid tree. */
+int oracle_accept_tree_greedy(const float *p, const int32_t *tokens, const int32_t *parent, int B,
+                              int D, int V, int32_t *n_accepted, int32_t *token, int32_t *path,
+                              int num_threads)
+{
+    if (B < 0 || D < 0 || D > 63 || V < 1) return -2;
+    for (int b = 0; b < B; ++b)
+        if (!tree_valid(parent + (int64_t)b * (1 + D), 1 + D)) return -4;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const int T = 1 + D;
+        const float *pb = p + (int64_t)b * T * V;
+        const int32_t *par = parent + (int64_t)b * T, *tok = tokens + (int64_t)b * T;
+        for (int x = 0; x < D; ++x) path[(int64_t)b * D + x] = -1;
+        int cur = 0, depth = 0, t;
+        for (;;) {
+            t = argmax_row(pb + (int64_t)cur * V, V);
+            int next = -1;
+            for (int c = cur + 1; c < T; ++c)
+                if (par[c] == cur && tok[c] == t) { next = c; break; }
+            if (next < 0) break;
+            path[(int64_t)b * D + depth] = next;
+            ++depth;
+            cur = next;
+        }
+        n_accepted[b] = depth;
+        token[b] = t;
+    }
+    return 0;
+}

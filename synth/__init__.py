@@ -306,3 +306,59 @@ def softmax_rows_fp32(logits):
 
 def log2_ceil(x):
     return int(math.ceil(math.log2(max(1, x))))
+
+
+# ---------------------------------------------------------------------------
+# Draft trees.
+# ---------------------------------------------------------------------------
+def tree_parents(seed, B, T, kind="random"):
+    """Parent arrays int32 [B, T] of draft trees in topological order
+    (parent[:, 0] = -1, 0 <= parent[b, k] < k).
+
+    kind: "chain" (k - 1), "star" (every node a child of the root),
+    "random" (uniform earlier node, a fresh tree per sequence), or "wide"
+    (a fixed tree shaped like the static trees of multi-head drafters:
+    several candidates at the first level, fewer below).
+    """
+    par = np.empty((B, T), np.int32)
+    par[:, 0] = -1
+    if kind == "chain":
+        par[:, 1:] = np.arange(T - 1)
+    elif kind == "star":
+        par[:, 1:] = 0
+    elif kind == "random":
+        rng = np.random.default_rng(seed)
+        for k in range(1, T):
+            par[:, k] = rng.integers(0, k, size=B)
+    elif kind == "wide":
+        # level sizes 4, 3, 2, 1, ... : node k's parent is the first node of
+        # the previous level that still has room (at most 3 children each)
+        shape = [0]
+        levels = [[0]]
+        k = 1
+        width = 4
+        while k < T:
+            prev = levels[-1]
+            cur = []
+            for c in range(width):
+                if k >= T:
+                    break
+                shape.append(prev[min(c // 3, len(prev) - 1)] if c >= 1 else prev[0])
+                cur.append(k)
+                k += 1
+            levels.append(cur)
+            width = max(1, width - 1)
+        par[:, :] = np.asarray(shape[:T], np.int32)[None, :]
+        par[:, 0] = -1
+    else:
+        raise ValueError(kind)
+    return par
+
+
+def tree_depths(parent):
+    """Depth of every node (root 0) of int32 parent arrays [B, T]."""
+    B, T = parent.shape
+    dep = np.zeros((B, T), np.int32)
+    for k in range(1, T):
+        dep[:, k] = dep[np.arange(B), parent[:, k]] + 1
+    return dep
