@@ -562,6 +562,62 @@ def case_lines(args):
                           "frac_tensor_burst": tf / pk["bf16_tflops"],
                           "GB_per_s": by / (ms * 1e-3) / 1e9,
                           "frac_hbm": by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]})
+    if args.workload in ("tree", "all"):
+        # tree verification at the full-step attention shape (B=64 paged
+        # sequences of 4096..131072 tokens, Hkv=8, G=8, d=128) with an
+        # 8-node draft tree, and greedy tree acceptance at V=131072
+        lens = synth.full_step_kv_lengths(50)
+        B, Hkv, G, D = 64, 8, 8, 7
+        inp = synth.attention_inputs_device(51, B, Hkv, G, 128, D, lens, page_size=64, device=dev)
+        parent = torch.from_numpy(synth.tree_parents(3, B, D + 1, "wide")).to(dev)
+        out = torch.empty((B, D + 1, Hkv * G, 128), device=dev)
+        lse = torch.empty((B, D + 1, Hkv * G), device=dev)
+        wst = torch.empty(sv.tree_attention_workspace_size(B, D, Hkv, G, 128, inp.block_table.shape[1] * 64),
+                          dtype=torch.uint8, device=dev)
+        fn = lambda: sv.verify_tree_attention(inp.q, inp.k_pages, inp.v_pages, inp.block_table, inp.kv_len,
+                                              parent, D, Hkv, G, out=out, lse=lse, workspace=wst)
+        ms = time_launches(fn, args.warmup, args.steps)
+        sumL = int(np.sum(inp.kv_len_host.astype(np.int64)))
+        by = 2 * sumL * Hkv * 128 * 2 + B * (D + 1) * Hkv * G * (128 * 2 + 129 * 4)
+        gbs = by / (ms * 1e-3) / 1e9
+        lines.append({"case": "tree attention B64 L~U[4096,131072] D7 wide tree", "kernel": "verify_tree_attention",
+                      "ms": ms, "query_tokens_per_s": B * (D + 1) / (ms * 1e-3), "GB_per_s": gbs,
+                      "frac_hbm": gbs / pk["hbm_gbs"]})
+        # the chain on the same inputs, for comparison
+        wsc = torch.empty(sv.attention_workspace_size(B, D, Hkv, G, 128, inp.block_table.shape[1] * 64),
+                          dtype=torch.uint8, device=dev)
+        ms_c = time_launches(lambda: sv.verify_attention(inp.q, inp.k_pages, inp.v_pages, inp.block_table,
+                                                         inp.kv_len, D, Hkv, G, out=out, lse=lse, workspace=wsc),
+                             args.warmup, args.steps)
+        lines.append({"case": "chain attention, same inputs", "kernel": "verify_attention", "ms": ms_c,
+                      "GB_per_s": by / (ms_c * 1e-3) / 1e9, "frac_hbm": by / (ms_c * 1e-3) / 1e9 / pk["hbm_gbs"]})
+        del wsc
+        del inp, out, lse, wst
+        torch.cuda.empty_cache()
+        Bt, Vt = 256, 131072
+        acc = synth.accept_inputs(77, Bt, D, Vt, target_std=3.0, mode="greedy", chunk=32)
+        pt = torch.from_numpy(acc["p"]).to(dev)
+        par_h = synth.tree_parents(4, Bt, D + 1, "wide")
+        am = np.argmax(acc["p"], axis=2)
+        rng = np.random.default_rng(5)
+        tok_h = rng.integers(0, Vt, size=(Bt, D + 1)).astype(np.int32)
+        for k in range(1, D + 1):
+            hit = rng.random(Bt) < 0.6
+            tok_h[hit, k] = am[hit, par_h[hit, k]]
+        tok, par = torch.from_numpy(tok_h).to(dev), torch.from_numpy(par_h).to(dev)
+        na = torch.empty(Bt, dtype=torch.int32, device=dev)
+        tk = torch.empty(Bt, dtype=torch.int32, device=dev)
+        path = torch.empty((Bt, D), dtype=torch.int32, device=dev)
+        ms_t = time_launches(lambda: sv.accept_tree_greedy(pt, tok, par, na, tk, path), args.warmup,
+                             args.steps, flush)
+        nacc = na.cpu().numpy().astype(np.int64)
+        by_t = int(np.sum(nacc + 1)) * Vt * 4
+        lines.append({"case": f"tree accept greedy B{Bt} D{D} V{Vt} wide tree", "kernel": "accept_tree_greedy",
+                      "ms": ms_t, "mean_AL": float(np.mean(nacc + 1)), "algorithmic_bytes": by_t,
+                      "GB_per_s": by_t / (ms_t * 1e-3) / 1e9,
+                      "frac_hbm": by_t / (ms_t * 1e-3) / 1e9 / pk["hbm_gbs"]})
+        del pt
+        torch.cuda.empty_cache()
     if args.workload in ("accept", "all", "accept-one"):
         B, D, V = 256, 7, 131072
         for alpha in ((0.6,) if args.workload == "accept-one" else (0.4, 0.6, 0.8)):
@@ -611,7 +667,7 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=3.0,
                     help="reference arm: seconds of oracle attention work sampled per step")
     ap.add_argument("--workload", default="step",
-                    choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small",
+                    choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small", "tree",
                              "accept-one"],
                     help="step: the headline line; others print one secondary JSON line per case")
     args = ap.parse_args()

@@ -58,6 +58,7 @@ typedef enum {
 #define SPEC_DEV_ERR_ZERO_MASS   0x00000020u /* a row to sample from has zero total mass */
 #define SPEC_DEV_ERR_LAUNCH      0x00000040u /* launched without the cluster shape it
                                                 needs (e.g. replayed by a tool): did nothing */
+#define SPEC_DEV_ERR_TREE        0x00000080u /* draft tree not in topological order */
 #define SPEC_DEV_INFO_ZERO_RESIDUAL 0x00010000u /* informational: max(0,p-q) summed to 0
                                                    after a rejection; drew from p instead */
 
@@ -205,6 +206,59 @@ spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_b
 spec_status_t spec_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,
                                  int32_t *n_accepted, int32_t *token, uint32_t *dev_status,
                                  void *stream);
+
+/* ------------------------------------------------------------------------
+ * Tree verification.
+ *
+ * "The candidates are combined into a tree of possible continuations; the
+ * target evaluates the whole tree in one forward pass with tree attention,
+ * whose mask keeps causality inside each candidate branch; the longest
+ * accepted candidate prefix moves on" (LLM inference handbook, "Speculative
+ * decoding", Medusa; EAGLE-2's dynamic draft tree in the same section).
+ *
+ * A draft tree of sequence b has 1 + D nodes in topological order:
+ *   tree_parent  device, int32 [B][1+D]; tree_parent[b][0] = -1 (the root:
+ *                the last accepted token), 0 <= tree_parent[b][k] < k.
+ * Node k's K/V sit at cache position kv_len[b] - (1+D) + k, and its query
+ * is q[b][k].  Malformed trees set SPEC_DEV_ERR_TREE (their nodes then see
+ * the prefix and themselves only).
+ *
+ * spec_verify_tree_attention: as spec_verify_attention, except that node k
+ * attends to keys j < kv_len[b] - (1+D) and to the tree keys of the nodes
+ * on its root-to-k path (its ancestors and itself).  The chain
+ * tree_parent[b][k] = k - 1 gives exactly spec_verify_attention.  workspace:
+ * spec_verify_tree_attention_workspace_size(...) bytes (the chain workspace
+ * plus 8 bytes per node), scratch only.
+ * ---------------------------------------------------------------------- */
+size_t spec_verify_tree_attention_workspace_size(int B, int D, int Hkv, int G, int head_dim,
+                                                 int max_kv_len);
+
+spec_status_t spec_verify_tree_attention(const void *q_bf16, const void *k_pages_bf16,
+                                         const void *v_pages_bf16, int num_pages,
+                                         const int32_t *block_table, int max_pages_per_seq,
+                                         const int32_t *kv_len, const int32_t *tree_parent, int B,
+                                         int D, int Hkv, int G, int head_dim, int page_size,
+                                         float softmax_scale, float *out_f32, float *lse_f32,
+                                         void *workspace, size_t workspace_bytes,
+                                         uint32_t *dev_status, void *stream);
+
+/* spec_accept_tree_greedy: with t_k = argmax_v p[b][k][v] (lowest index on
+ * ties), start at the root and repeatedly move to the child of the current
+ * node whose token equals t_(current) -- the lowest node index if several
+ * siblings carry it -- until no child does.
+ *   p          device, fp32 [B][1+D][V] target probabilities at every node.
+ *   tokens     device, int32 [B][1+D]; tokens[b][k] is node k's draft token
+ *              (tokens[b][0] is not read).
+ *   n_accepted device, int32 [B]: the depth reached (accepted drafts).
+ *   token      device, int32 [B]: t at the last node reached.
+ *   path       device, int32 [B][D] or NULL: the accepted node ids in order,
+ *              then -1.
+ * Only the rows of the nodes on the accepted path are read.  The chain with
+ * node k carrying draft k - 1 gives exactly spec_accept_greedy.
+ * ---------------------------------------------------------------------- */
+spec_status_t spec_accept_tree_greedy(const float *p, const int32_t *tokens, const int32_t *parent,
+                                      int B, int D, int V, int32_t *n_accepted, int32_t *token,
+                                      int32_t *path, uint32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
  * Stochastic acceptance (modified rejection sampling).

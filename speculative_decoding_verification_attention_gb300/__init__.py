@@ -20,6 +20,7 @@ __all__ = [
     "SpecError", "library", "library_path", "verify_attention", "verify_gemm",
     "accept_greedy", "accept_sample", "accept_sample_workspace_size", "attention_workspace_size",
     "gemm_workspace_size", "gemm_plan", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
+    "verify_tree_attention", "tree_attention_workspace_size", "accept_tree_greedy",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -30,11 +31,13 @@ EXPORTED_SYMBOLS = (
     "spec_verify_attention", "spec_verify_gemm_workspace_size", "spec_verify_gemm",
     "spec_accept_greedy", "spec_accept_sample", "spec_verify_attention_plan",
     "spec_verify_attention_noalloc", "spec_accept_sample_workspace_size", "spec_verify_gemm_plan",
+    "spec_verify_tree_attention_workspace_size", "spec_verify_tree_attention",
+    "spec_accept_tree_greedy",
 )
 
 DEV_STATUS_BITS = {
     "PAGE_ID": 0x1, "KV_LEN": 0x2, "TIMEOUT": 0x4, "TOKEN_ID": 0x8, "UNIFORM": 0x10,
-    "ZERO_MASS": 0x20, "LAUNCH": 0x40, "INFO_ZERO_RESIDUAL": 0x10000,
+    "ZERO_MASS": 0x20, "LAUNCH": 0x40, "TREE": 0x80, "INFO_ZERO_RESIDUAL": 0x10000,
 }
 
 ATTENTION_KEY_TILE = 128   # SPEC_ATTENTION_KEY_TILE: keys per tile of the KV split
@@ -87,6 +90,13 @@ def library():
             lib.spec_verify_attention_noalloc.restype = I
             lib.spec_verify_attention_plan.argtypes = [I, P, I, I, I, P, I]
             lib.spec_verify_attention_plan.restype = I
+            lib.spec_verify_tree_attention_workspace_size.argtypes = [I, I, I, I, I, I]
+            lib.spec_verify_tree_attention_workspace_size.restype = S
+            lib.spec_verify_tree_attention.argtypes = [P, P, P, I, P, I, P, P, I, I, I, I, I, I, F,
+                                                       P, P, P, S, P, P]
+            lib.spec_verify_tree_attention.restype = I
+            lib.spec_accept_tree_greedy.argtypes = [P, P, P, I, I, I, P, P, P, P, P]
+            lib.spec_accept_tree_greedy.restype = I
             lib.spec_verify_gemm_plan.argtypes = [I, I, I, I, P, I]
             lib.spec_verify_gemm_plan.restype = I
             _lib = lib
@@ -157,6 +167,47 @@ def verify_attention(q, k_pages, v_pages, block_table, kv_len, D, Hkv, G, softma
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
     _check(st, "spec_verify_attention")
+    return out
+
+
+def tree_attention_workspace_size(B, D, Hkv, G, head_dim, max_kv_len):
+    return int(library().spec_verify_tree_attention_workspace_size(B, D, Hkv, G, head_dim,
+                                                                    max_kv_len))
+
+
+def verify_tree_attention(q, k_pages, v_pages, block_table, kv_len, tree_parent, D, Hkv, G,
+                          softmax_scale=None, out=None, lse=None, workspace=None, dev_status=None,
+                          stream=None):
+    """Tree verify attention: node k of sequence b attends to the prefix and
+    to its root-to-node path.  tree_parent int32 [B, 1+D]; other arguments
+    as verify_attention."""
+    import torch
+    B, D1, Hq, d = q.shape
+    if D1 != D + 1 or Hq != Hkv * G:
+        raise ValueError("q shape does not match D/Hkv/G")
+    P, page, hk, dk = k_pages.shape
+    if hk != Hkv or dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("k_pages/v_pages shape mismatch")
+    if tuple(tree_parent.shape) != (B, D + 1):
+        raise ValueError("tree_parent must be [B, 1+D]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, D + 1, Hq, d), dtype=torch.float32, device=q.device)
+    max_pages = block_table.shape[1]
+    need = tree_attention_workspace_size(B, D, Hkv, G, d, max_pages * page)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = library().spec_verify_tree_attention(
+        _dev(q, "q", torch.bfloat16), _dev(k_pages, "k_pages", torch.bfloat16),
+        _dev(v_pages, "v_pages", torch.bfloat16), P, _dev(block_table, "block_table", torch.int32),
+        max_pages, _dev(kv_len, "kv_len", torch.int32), _dev(tree_parent, "tree_parent", torch.int32),
+        B, D, Hkv, G, d, page, float(softmax_scale), _dev(out, "out", torch.float32),
+        _dev(lse, "lse", torch.float32, allow_none=True),
+        _dev(workspace, "workspace", allow_none=True),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
+    _check(st, "spec_verify_tree_attention")
     return out
 
 
@@ -234,6 +285,27 @@ def accept_greedy(p, draft, n_accepted=None, token=None, dev_status=None, stream
         _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
     _check(st, "spec_accept_greedy")
     return n_accepted, token
+
+
+def accept_tree_greedy(p, tokens, tree_parent, n_accepted=None, token=None, path=None,
+                       dev_status=None, stream=None):
+    """Greedy tree acceptance; p [B, 1+D, V] fp32, tokens / tree_parent int32
+    [B, 1+D].  Returns (n_accepted, token, path [B, D])."""
+    import torch
+    B, D1, V = p.shape
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=p.device)
+    if token is None:
+        token = torch.empty(B, dtype=torch.int32, device=p.device)
+    if path is None:
+        path = torch.empty((B, max(D1 - 1, 1)), dtype=torch.int32, device=p.device)
+    st = library().spec_accept_tree_greedy(
+        _dev(p, "p", torch.float32), _dev(tokens, "tokens", torch.int32),
+        _dev(tree_parent, "tree_parent", torch.int32), B, D1 - 1, V,
+        _dev(n_accepted, "n_accepted", torch.int32), _dev(token, "token", torch.int32),
+        _dev(path, "path", torch.int32), _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
+    _check(st, "spec_accept_tree_greedy")
+    return n_accepted, token, path[:, :D1 - 1]
 
 
 def accept_sample_workspace_size(B, V):

@@ -143,16 +143,23 @@ constexpr int kGUnroll = 8;    // greedy: 128-element steps whose loads are in f
 // mbarrier; every CTA then reduces the CS results itself and takes the same
 // decision, so no cluster-wide barrier sits on the per-row path.  Only rows
 // 0..n_accepted are read.
-template <int CS>
+// TREE: the 1 + D rows are the nodes of a draft tree (parent[b][k] < k,
+// node tokens tokens[b][k]); from the root the walk moves to the child whose
+// token equals the row's argmax (lowest node index among such siblings) and
+// stops when none does.  The chain is the tree parent[k] = k - 1 whose node
+// k carries draft k - 1.
+template <int CS, bool TREE>
 __global__ void __launch_bounds__(kThreads, 4) accept_greedy_kernel(
-    const float *__restrict__ p, const int32_t *__restrict__ draft, int D, int V,
-    int32_t *__restrict__ n_accepted, int32_t *__restrict__ token, uint32_t *dev_status, bool vec4)
+    const float *__restrict__ p, const int32_t *__restrict__ draft, const int32_t *__restrict__ parent,
+    int D, int V, int32_t *__restrict__ n_accepted, int32_t *__restrict__ token,
+    int32_t *__restrict__ path, uint32_t *dev_status, bool vec4)
 {
     __shared__ ArgMax s_warp[kWarps];
     __shared__ __align__(8) unsigned long long s_res[2][CS];   // per row parity, one per CTA
     __shared__ uint64_t s_bar[2];
-    __shared__ int32_t s_draft[kMaxDraft];
-    __shared__ int s_abort;
+    __shared__ int32_t s_draft[kMaxDraft + 1];   // chain: drafts; tree: node tokens
+    __shared__ int32_t s_par[TREE ? kMaxDraft + 1 : 1];
+    __shared__ int s_abort, s_bad;
     if (cluster_ctas() != static_cast<uint32_t>(CS)) {   // uniform over the grid
         if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
         return;
@@ -162,7 +169,18 @@ __global__ void __launch_bounds__(kThreads, 4) accept_greedy_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Slice sl = warp_slice(V, CS, rank, warp);
     volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
-    for (int i = threadIdx.x; i < D; i += kThreads) s_draft[i] = draft[static_cast<int64_t>(b) * D + i];
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    if constexpr (TREE) {
+        for (int k = threadIdx.x; k <= D; k += kThreads) {
+            s_draft[k] = draft[static_cast<int64_t>(b) * (D + 1) + k];
+            const int pa = parent[static_cast<int64_t>(b) * (D + 1) + k];
+            s_par[k] = pa;
+            if (k == 0 ? pa != -1 : (pa < 0 || pa >= k)) s_bad = 1;
+        }
+    } else {
+        for (int i = threadIdx.x; i < D; i += kThreads) s_draft[i] = draft[static_cast<int64_t>(b) * D + i];
+    }
     if (threadIdx.x == 0) {
         mbar_init(&s_bar[0], 1);
         mbar_init(&s_bar[1], 1);
@@ -172,10 +190,13 @@ __global__ void __launch_bounds__(kThreads, 4) accept_greedy_kernel(
     if constexpr (CS > 1) cg::this_cluster().sync();   // peers' barriers exist before any send
     else __syncthreads();
 
+    // a malformed tree is reported and walked as a lone root
+    if (TREE && s_bad && rank == 0 && threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_TREE);
+    int node = 0;   // tree: the node whose row this iteration reads
     for (int i = 0; i <= D; ++i) {
         const int par = i & 1;
         if (CS > 1 && threadIdx.x == 0) mbar_arrive_expect_tx(&s_bar[par], CS * 8);
-        const float *row = p + (static_cast<int64_t>(b) * (D + 1) + i) * V;
+        const float *row = p + (static_cast<int64_t>(b) * (D + 1) + (TREE ? node : i)) * V;
         // Per lane, elements are visited in increasing index order; only a
         // strictly larger value replaces the best, so ties keep the lowest
         // index.  The index is located only when a float4's max wins.
@@ -219,13 +240,30 @@ __global__ void __launch_bounds__(kThreads, 4) accept_greedy_kernel(
         ArgMax g{-FLT_MAX, INT_MAX};
 #pragma unroll
         for (int r = 0; r < CS; ++r) g = better(g, unpack_argmax(s_res[par][r]));
-        const bool stop = !ok || i == D || s_draft[i] != g.i;
+        bool stop;
+        int next = -1;
+        if constexpr (TREE) {
+            // the lowest-index child of `node` carrying the argmax (every
+            // thread scans the same small tree, so all agree)
+            if (ok && !s_bad)
+                for (int k = node + 1; k <= D; ++k)
+                    if (s_par[k] == node && s_draft[k] == g.i) { next = k; break; }
+            stop = !ok || next < 0;
+        } else {
+            stop = !ok || i == D || s_draft[i] != g.i;
+        }
         if (stop) {
             if (ok && rank == 0 && threadIdx.x == 0) {
                 n_accepted[b] = i;
                 token[b] = g.i;
             }
+            if (TREE && path && rank == 0)
+                for (int x = i + threadIdx.x; x < D; x += kThreads) path[static_cast<int64_t>(b) * D + x] = -1;
             break;
+        }
+        if constexpr (TREE) {
+            if (path && rank == 0 && threadIdx.x == 0) path[static_cast<int64_t>(b) * D + i] = next;
+            node = next;
         }
         __syncthreads();   // s_warp is rewritten by the next row
     }
@@ -602,9 +640,10 @@ int pick_cluster(int V)
     return 1;
 }
 
-template <int CS>
-cudaError_t launch_greedy_cs(const float *p, const int32_t *draft, int B, int D, int V, int32_t *n_acc,
-                             int32_t *token, uint32_t *dev_status, bool vec4, cudaStream_t st)
+template <int CS, bool TREE>
+cudaError_t launch_greedy_cs(const float *p, const int32_t *draft, const int32_t *parent, int B, int D,
+                             int V, int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
+                             bool vec4, cudaStream_t st)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(B) * CS);
@@ -617,19 +656,35 @@ cudaError_t launch_greedy_cs(const float *p, const int32_t *draft, int B, int D,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, accept_greedy_kernel<CS>, p, draft, D, V, n_acc, token, dev_status, vec4);
+    return cudaLaunchKernelEx(&cfg, accept_greedy_kernel<CS, TREE>, p, draft, parent, D, V, n_acc, token,
+                              path, dev_status, vec4);
+}
+
+template <bool TREE>
+cudaError_t launch_greedy(const float *p, const int32_t *draft, const int32_t *parent, int B, int D,
+                          int V, int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
+                          cudaStream_t st)
+{
+    const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0);
+    switch (pick_cluster(V)) {
+    case 8: return launch_greedy_cs<8, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
+    case 4: return launch_greedy_cs<4, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
+    case 2: return launch_greedy_cs<2, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
+    default: return launch_greedy_cs<1, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
+    }
 }
 
 cudaError_t launch_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,
                                  int32_t *n_acc, int32_t *token, uint32_t *dev_status, cudaStream_t st)
 {
-    const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0);
-    switch (pick_cluster(V)) {
-    case 8: return launch_greedy_cs<8>(p, draft, B, D, V, n_acc, token, dev_status, vec4, st);
-    case 4: return launch_greedy_cs<4>(p, draft, B, D, V, n_acc, token, dev_status, vec4, st);
-    case 2: return launch_greedy_cs<2>(p, draft, B, D, V, n_acc, token, dev_status, vec4, st);
-    default: return launch_greedy_cs<1>(p, draft, B, D, V, n_acc, token, dev_status, vec4, st);
-    }
+    return launch_greedy<false>(p, draft, nullptr, B, D, V, n_acc, token, nullptr, dev_status, st);
+}
+
+cudaError_t launch_accept_tree_greedy(const float *p, const int32_t *tokens, const int32_t *parent, int B,
+                                      int D, int V, int32_t *n_acc, int32_t *token, int32_t *path,
+                                      uint32_t *dev_status, cudaStream_t st)
+{
+    return launch_greedy<true>(p, tokens, parent, B, D, V, n_acc, token, path, dev_status, st);
 }
 
 size_t accept_sample_workspace_bytes(int B, int V)

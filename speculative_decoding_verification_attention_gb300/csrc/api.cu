@@ -15,6 +15,11 @@ namespace {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+size_t tree_mask_bytes(int B, int D)
+{
+    return (static_cast<size_t>(B) * (D + 1) * 8 + 255) & ~size_t(255);
+}
+
 spec_status_t from_cuda(cudaError_t e)
 {
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
@@ -51,6 +56,22 @@ spec_status_t spec_accept_greedy(const float *p, const int32_t *draft, int B, in
     if (static_cast<long long>(B) * 8 > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
     return from_cuda(launch_accept_greedy(p, draft, B, D, V, n_accepted, token, dev_status,
                                           static_cast<cudaStream_t>(stream)));
+}
+
+spec_status_t spec_accept_tree_greedy(const float *p, const int32_t *tokens, const int32_t *parent,
+                                      int B, int D, int V, int32_t *n_accepted, int32_t *token,
+                                      int32_t *path, uint32_t *dev_status, void *stream)
+{
+    if (B < 0 || D < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+    if (D > kMaxDraft || V > (1 << 26)) return SPEC_ERR_UNSUPPORTED;
+    if (B == 0) return SPEC_OK;
+    if (!p || !tokens || !parent || !n_accepted || !token) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(p, 4) || !aligned(tokens, 4) || !aligned(parent, 4) || !aligned(n_accepted, 4) ||
+        !aligned(token, 4) || (path && !aligned(path, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * 8 > 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
+    return from_cuda(launch_accept_tree_greedy(p, tokens, parent, B, D, V, n_accepted, token, path,
+                                               dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 size_t spec_accept_sample_workspace_size(int B, int V)
@@ -105,13 +126,20 @@ size_t spec_verify_attention_workspace_size(int B, int D, int Hkv, int G, int he
     return attention_workspace_bytes(nt, head_dim, sms);
 }
 
-spec_status_t spec_verify_attention(const void *q_bf16, const void *k_pages_bf16,
+}  // extern "C"
+
+namespace {
+
+// Chain (tree_parent == NULL) or tree verify attention.  The tree's node
+// masks go after the chain workspace.
+spec_status_t verify_attention_impl(const void *q_bf16, const void *k_pages_bf16,
                                     const void *v_pages_bf16, int num_pages,
                                     const int32_t *block_table, int max_pages_per_seq,
-                                    const int32_t *kv_len, int B, int D, int Hkv, int G,
-                                    int head_dim, int page_size, float softmax_scale,
-                                    float *out_f32, float *lse_f32, void *workspace,
-                                    size_t workspace_bytes, uint32_t *dev_status, void *stream)
+                                    const int32_t *kv_len, const int32_t *tree_parent, int B, int D,
+                                    int Hkv, int G, int head_dim, int page_size,
+                                    float softmax_scale, float *out_f32, float *lse_f32,
+                                    void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                                    void *stream)
 {
     if (B < 0 || D < 0 || Hkv < 1 || G < 1 || head_dim < 1 || page_size < 1 || num_pages < 1 ||
         max_pages_per_seq < 1)
@@ -127,12 +155,13 @@ spec_status_t spec_verify_attention(const void *q_bf16, const void *k_pages_bf16
         return SPEC_ERR_INVALID_ARG;
     if (!aligned(q_bf16, 16) || !aligned(k_pages_bf16, 16) || !aligned(v_pages_bf16, 16) ||
         !aligned(out_f32, 16) || !aligned(block_table, 4) || !aligned(kv_len, 4) ||
-        (lse_f32 && !aligned(lse_f32, 4)))
+        (lse_f32 && !aligned(lse_f32, 4)) || (tree_parent && !aligned(tree_parent, 4)))
         return SPEC_ERR_INVALID_ARG;
     const int sms = device_sm_count();
     if (sms <= 0) return SPEC_ERR_CUDA;
     const int nt = (G * (1 + D) + 127) / 128;
-    const size_t need = attention_workspace_bytes(nt, head_dim, sms);
+    const size_t chain_need = attention_workspace_bytes(nt, head_dim, sms);
+    const size_t need = chain_need + (tree_parent ? tree_mask_bytes(B, D) : 0);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SPEC_ERR_WORKSPACE;
 
     CUtensorMap tk, tv;
@@ -163,8 +192,59 @@ spec_status_t spec_verify_attention(const void *q_bf16, const void *k_pages_bf16
     a.num_pages = num_pages;
     a.max_len = static_cast<int64_t>(max_pages_per_seq) * page_size;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.tree_mask = nullptr;
+    if (tree_parent) {
+        unsigned long long *masks =
+            reinterpret_cast<unsigned long long *>(static_cast<char *>(workspace) + chain_need);
+        const cudaError_t e = launch_tree_masks(tree_parent, B, D + 1, masks, dev_status,
+                                                static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return from_cuda(e);
+        a.tree_mask = masks;
+    }
     return from_cuda(launch_verify_attention(tk, tv, a, head_dim, static_cast<cudaStream_t>(stream)));
 }
+
+}  // namespace
+
+extern "C" {
+
+spec_status_t spec_verify_attention(const void *q_bf16, const void *k_pages_bf16,
+                                    const void *v_pages_bf16, int num_pages,
+                                    const int32_t *block_table, int max_pages_per_seq,
+                                    const int32_t *kv_len, int B, int D, int Hkv, int G,
+                                    int head_dim, int page_size, float softmax_scale,
+                                    float *out_f32, float *lse_f32, void *workspace,
+                                    size_t workspace_bytes, uint32_t *dev_status, void *stream)
+{
+    return verify_attention_impl(q_bf16, k_pages_bf16, v_pages_bf16, num_pages, block_table,
+                                 max_pages_per_seq, kv_len, nullptr, B, D, Hkv, G, head_dim, page_size,
+                                 softmax_scale, out_f32, lse_f32, workspace, workspace_bytes,
+                                 dev_status, stream);
+}
+
+size_t spec_verify_tree_attention_workspace_size(int B, int D, int Hkv, int G, int head_dim,
+                                                 int max_kv_len)
+{
+    const size_t chain = spec_verify_attention_workspace_size(B, D, Hkv, G, head_dim, max_kv_len);
+    return B > 0 && D >= 0 ? chain + tree_mask_bytes(B, D) : chain;
+}
+
+spec_status_t spec_verify_tree_attention(const void *q_bf16, const void *k_pages_bf16,
+                                         const void *v_pages_bf16, int num_pages,
+                                         const int32_t *block_table, int max_pages_per_seq,
+                                         const int32_t *kv_len, const int32_t *tree_parent, int B,
+                                         int D, int Hkv, int G, int head_dim, int page_size,
+                                         float softmax_scale, float *out_f32, float *lse_f32,
+                                         void *workspace, size_t workspace_bytes,
+                                         uint32_t *dev_status, void *stream)
+{
+    if (B > 0 && !tree_parent) return SPEC_ERR_INVALID_ARG;
+    return verify_attention_impl(q_bf16, k_pages_bf16, v_pages_bf16, num_pages, block_table,
+                                 max_pages_per_seq, kv_len, tree_parent, B, D, Hkv, G, head_dim,
+                                 page_size, softmax_scale, out_f32, lse_f32, workspace,
+                                 workspace_bytes, dev_status, stream);
+}
+
 
 int spec_verify_attention_plan(int B, const int32_t *kv_len_host, int D, int Hkv, int num_groups,
                                int32_t *segments, int max_segments)

@@ -144,7 +144,9 @@ __device__ void plan_group(const AttnArgs &a, int g, PlanShared *ps)
     }
 }
 
-template <int HD>
+// TREE: rows see the prefix plus their root-to-node path (a.tree_mask);
+// otherwise the chain mask, compiled without the tree's per-key bit tests.
+template <int HD, bool TREE>
 __global__ void __launch_bounds__(kThreads, 1)
     verify_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const AttnArgs a)
@@ -447,7 +449,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (ok && walk.next(seg)) {
             const int n = seg.tile_end - seg.tile_begin;
             const int Lb = a.kv_len[seg.b];
-            const int limit = row_ok ? Lb - a.D + i_row : 0;    // keys j < limit are visible
+            // Visible keys of this row: j < vis_end, plus key vis_end + x
+            // for every bit x of vis_bits.  Chain: the prefix and drafts
+            // 0..i (vis_bits = 0).  Tree: the prefix before the 1+D tree
+            // keys, plus the tree keys on the root-to-node path.
+            int vis_end;
+            unsigned long long vis_bits;
+            if (TREE) {
+                vis_end = row_ok ? Lb - a.D - 1 : 0;
+                vis_bits = row_ok ? a.tree_mask[static_cast<int64_t>(seg.b) * (a.D + 1) + i_row] : 0ull;
+            } else {
+                vis_end = row_ok ? Lb - a.D + i_row : 0;
+                vis_bits = 0ull;
+            }
+            const int limit = vis_end;   // keys j < limit are visible for sure
             float m_ref = -INFINITY, l = 0.f;
             int ks = 0;
             for (int k = sm; k < n; k += 2, ++ks, ++ns) {
@@ -471,6 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int key0 = (seg.tile_begin + k) * kBN;
                 const int nvis = limit - key0;            // keys [0, nvis) of the tile are visible
+                // whether key c of the tile is visible (the slow path only)
+                auto visible = [&](int c) {
+                    if (!TREE) return c < nvis;
+                    const unsigned x = static_cast<unsigned>(c - nvis);
+                    return c < nvis || (x < 64u && ((vis_bits >> x) & 1ull));
+                };
                 // pass 1: row max of the raw scores
                 float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll 1
@@ -488,8 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
-                            if (32 * q + c < nvis) m0 = fmaxf(m0, __uint_as_float(x0[c]));
-                            if (32 * q + 32 + c < nvis) m1 = fmaxf(m1, __uint_as_float(x1[c]));
+                            if (visible(32 * q + c)) m0 = fmaxf(m0, __uint_as_float(x0[c]));
+                            if (visible(32 * q + 32 + c)) m1 = fmaxf(m1, __uint_as_float(x1[c]));
                         }
                     }
                 }
@@ -537,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!full) {
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            if (!live || 32 * q + c >= nvis) x[c] = __float_as_uint(-INFINITY);
+                            if (!live || !visible(32 * q + c)) x[c] = __float_as_uint(-INFINITY);
                     }
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
@@ -715,7 +736,7 @@ template <int HD>
 cudaError_t run(const CUtensorMap &tk, const CUtensorMap &tv, const AttnArgs &a, cudaStream_t st)
 {
     using L = AttnSmem<HD>;
-    auto k = verify_attention_kernel<HD>;
+    auto k = a.tree_mask ? verify_attention_kernel<HD, true> : verify_attention_kernel<HD, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kBytes));
     if (e != cudaSuccess) return e;
     k<<<a.groups * a.nt, kThreads, L::kBytes, st>>>(tk, tv, a);
@@ -745,6 +766,50 @@ cudaError_t launch_verify_attention(const CUtensorMap &tk, const CUtensorMap &tv
                                     int head_dim, cudaStream_t st)
 {
     return head_dim == 128 ? run<128>(tk, tv, a, st) : run<64>(tk, tv, a, st);
+}
+
+namespace {
+
+// One thread per (sequence, node): walk up to the root, collecting the
+// path's bits.  Nodes are in topological order (parent < node), so a walk
+// ends within T steps; anything else is reported and the node keeps its own
+// bit only.
+__global__ void tree_mask_kernel(const int32_t *__restrict__ parent, int B, int T,
+                                 unsigned long long *__restrict__ mask, uint32_t *dev_status)
+{
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<int64_t>(B) * T) return;
+    const int k = static_cast<int>(idx % T);
+    const int32_t *par = parent + (idx - k);
+    bool ok = k == 0 ? par[0] == -1 : true;
+    unsigned long long m = 1ull << k;
+    int a = k;
+    for (int steps = 0; ok && a > 0 && steps < T; ++steps) {
+        const int pa = par[a];
+        if (pa < 0 || pa >= a) {
+            ok = false;
+            break;
+        }
+        m |= 1ull << pa;
+        a = pa;
+    }
+    if (ok && par[0] != -1) ok = false;
+    if (!ok) {
+        report(dev_status, SPEC_DEV_ERR_TREE);
+        m = 1ull << k;
+    }
+    mask[idx] = m;
+}
+
+}  // namespace
+
+cudaError_t launch_tree_masks(const int32_t *parent, int B, int T, unsigned long long *mask,
+                              uint32_t *dev_status, cudaStream_t st)
+{
+    const int64_t n = static_cast<int64_t>(B) * T;
+    if (n == 0) return cudaSuccess;
+    tree_mask_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(parent, B, T, mask, dev_status);
+    return cudaGetLastError();
 }
 
 }  // namespace spec

@@ -90,3 +90,22 @@ def test_gemm_rejects_bad_arguments(lib):
     # small M: partials as wide as the padded x rows
     assert lib.spec_verify_gemm_workspace_size(8, 6144, 6144) < lib.spec_verify_gemm_workspace_size(
         256, 6144, 6144)
+
+
+def test_tree_entry_points_reject_bad_arguments(lib):
+    f = lib.spec_verify_tree_attention
+    W = 1 << 30
+    args = lambda parent, D=3: (FAKE, FAKE, FAKE, 10, FAKE, 4, FAKE, parent, 2, D, 1, 4, 64, 16, 0.125,
+                                FAKE, None, FAKE, W, None, None)
+    assert f(*args(None)) == INVALID                       # a tree needs its parents
+    assert f(*args(P(0x7F0000001002))) == INVALID          # misaligned parents
+    assert f(*args(FAKE, D=64)) == UNSUPPORTED             # at most 64 nodes
+    chain = lib.spec_verify_attention_workspace_size(2, 3, 1, 4, 64, 64)
+    tree = lib.spec_verify_tree_attention_workspace_size(2, 3, 1, 4, 64, 64)
+    assert tree >= chain + 2 * 4 * 8
+    g = lib.spec_accept_tree_greedy
+    assert g(FAKE, FAKE, None, 2, 3, 10, FAKE, FAKE, None, None, None) == INVALID
+    assert g(FAKE, None, FAKE, 2, 3, 10, FAKE, FAKE, None, None, None) == INVALID
+    assert g(FAKE, FAKE, FAKE, 2, 64, 10, FAKE, FAKE, None, None, None) == UNSUPPORTED
+    assert g(FAKE, FAKE, FAKE, 2, 3, 0, FAKE, FAKE, None, None, None) == INVALID
+    assert g(None, None, None, 0, 3, 10, None, None, None, None, None) == 0
