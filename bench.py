@@ -562,6 +562,84 @@ def case_lines(args):
                           "frac_tensor_burst": tf / pk["bf16_tflops"],
                           "GB_per_s": by / (ms * 1e-3) / 1e9,
                           "frac_hbm": by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]})
+    if args.workload in ("adaptive", "all"):
+        # one CUDA graph per draft-length tier of a verification step (verify
+        # attention B=8 L=4096 Hkv=8 G=8 d=128, the N=K=6144 linear layer at
+        # M=8(1+D), stochastic acceptance V=32768); host wall time per round,
+        # eager launches vs graph replay
+        import time
+        from speculative_decoding_verification_attention_gb300.graphs import TierGraphs
+        B, Hkv, G, L, V, N = 8, 8, 8, 4096, 32768, 6144
+        tiers = (1, 3, 7)
+        bufs = {}
+        for D in tiers:
+            a = synth.attention_inputs_device(90 + D, B, Hkv, G, 128, D, L, page_size=64, device=dev)
+            acc = synth.accept_inputs(95 + D, B, D, V, mode="sample")
+            M = B * (D + 1)
+            bufs[D] = dict(
+                a=a, out=torch.empty((B, D + 1, Hkv * G, 128), device=dev),
+                wsa=torch.empty(sv.attention_workspace_size(B, D, Hkv, G, 128, L), dtype=torch.uint8, device=dev),
+                x=torch.randn((M, N), device=dev).to(torch.bfloat16),
+                w=(torch.randn((N, N), device=dev) * 0.02).to(torch.bfloat16),
+                y=torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                wsg=torch.zeros(max(256, sv.gemm_workspace_size(M, N, N)), dtype=torch.uint8, device=dev),
+                acc={k: torch.from_numpy(np.ascontiguousarray(acc[k])).to(dev)
+                     for k in ("p", "q", "draft", "u_acc", "u_res")},
+                na=torch.empty(B, dtype=torch.int32, device=dev), tk=torch.empty(B, dtype=torch.int32, device=dev),
+                wss=torch.empty(sv.accept_sample_workspace_size(B, V), dtype=torch.uint8, device=dev))
+
+        def step(D):
+            s = bufs[D]
+            a, c = s["a"], s["acc"]
+            sv.verify_attention(a.q, a.k_pages, a.v_pages, a.block_table, a.kv_len, D, Hkv, G, out=s["out"],
+                                workspace=s["wsa"])
+            sv.verify_gemm(s["x"], s["w"], y=s["y"], workspace=s["wsg"])
+            sv.accept_sample(c["p"], c["q"], c["draft"], c["u_acc"], c["u_res"], s["na"], s["tk"],
+                             workspace=s["wss"])
+
+        graphs = TierGraphs(step, tiers)
+
+        def wall(fn, n):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(n):
+                fn()
+                torch.cuda.synchronize()   # a round ends when its acceptance is known
+            return (time.perf_counter() - t0) / n * 1e3
+
+        for D in tiers:
+            n = max(10, args.steps * 5)
+            ms_e = wall(lambda: step(D), n)
+            ms_g = wall(lambda: graphs.replay(D), n)
+            lines.append({"case": f"adaptive tier D={D}: round B{B} L{L} V{V} (attention + GEMM + sample accept)",
+                          "kernel": "tier graph", "D": D, "ms_eager_wall": ms_e, "ms_graph_wall": ms_g,
+                          "ms": ms_g, "verified_tokens_per_s_graph": B * (D + 1) / (ms_g * 1e-3),
+                          "frac_hbm": None})
+        # a controller-driven run: acceptance drifts from low to high and back
+        ctl = sv.AdaptiveDraftLength(tiers, beta=0.7)
+        rng = np.random.default_rng(0)
+        alphas = np.concatenate([np.full(40, 0.2), np.full(40, 0.9), np.full(40, 0.4)])
+        used, acc_tok = [], 0
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for al in alphas:
+            D = ctl.draft_len
+            used.append(D)
+            graphs.replay(D)
+            torch.cuda.synchronize()
+            n_acc = np.minimum(rng.geometric(1.0 - al, size=B) - 1, D)   # synthetic acceptance
+            acc_tok += int(np.sum(n_acc + 1))
+            ctl.update(n_acc.astype(np.int32))
+        dt = time.perf_counter() - t0
+        lines.append({"case": "adaptive controller over 120 rounds (acceptance 0.2 -> 0.9 -> 0.4)",
+                      "kernel": "tier graphs + controller", "ms": dt / len(alphas) * 1e3,
+                      "rounds_per_tier": {str(D): int(np.sum(np.asarray(used) == D)) for D in tiers},
+                      "accepted_tokens_per_s": acc_tok / dt, "frac_hbm": None})
+        del bufs, graphs
+        torch.cuda.empty_cache()
+
     if args.workload in ("tree", "all"):
         # tree verification at the full-step attention shape (B=64 paged
         # sequences of 4096..131072 tokens, Hkv=8, G=8, d=128) with an
@@ -668,6 +746,7 @@ def main():
                     help="reference arm: seconds of oracle attention work sampled per step")
     ap.add_argument("--workload", default="step",
                     choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small", "tree",
+                             "adaptive",
                              "accept-one"],
                     help="step: the headline line; others print one secondary JSON line per case")
     args = ap.parse_args()

@@ -339,6 +339,41 @@ int spec_verify_attention_plan(int B, const int32_t *kv_len_host, int D, int Hkv
 int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments,
                           int max_segments);
 
+/* ------------------------------------------------------------------------
+ * Adaptive draft length (host only; no counterpart kernels).
+ *
+ * "After each verification round, keep an exponential moving average of
+ * the accept length and switch between a small set of predefined
+ * speculation lengths (default [1, 3, 7]), each with its own pre-captured
+ * CUDA graph" (LLM inference handbook, "Adaptive speculative decoding",
+ * SGLang).  Rule (the pages leave it open): the next round uses the
+ * smallest tier D >= EMA(AL), AL = n_accepted + 1, else the largest tier;
+ * EMA_1 = mean AL of the first round, EMA_r = beta * EMA_(r-1) +
+ * (1 - beta) * mean AL.
+ *
+ * spec_adaptive_init: tiers strictly increasing draft lengths in [0, 63]
+ *   (host array, n_tiers <= SPEC_ADAPTIVE_MAX_TIERS), 0 <= beta < 1.  The
+ *   controller starts at the largest tier.
+ * spec_adaptive_update: n_accepted host int32 [B] of the round just
+ *   verified; returns the draft length for the next round (-1 on bad
+ *   arguments).  B = 0 re-evaluates the tier without a new sample.
+ * spec_adaptive_draft_len: the current tier's draft length.
+ * ---------------------------------------------------------------------- */
+#define SPEC_ADAPTIVE_MAX_TIERS 8
+
+typedef struct {
+    float ema;       /* moving average of the accept length */
+    float beta;      /* weight of the previous average */
+    int rounds;      /* rounds seen */
+    int n_tiers;
+    int current;     /* index of the tier in use */
+    int tiers[SPEC_ADAPTIVE_MAX_TIERS];
+} spec_adaptive_t;
+
+spec_status_t spec_adaptive_init(spec_adaptive_t *s, const int32_t *tiers, int n_tiers, float beta);
+int spec_adaptive_update(spec_adaptive_t *s, const int32_t *n_accepted, int B);
+int spec_adaptive_draft_len(const spec_adaptive_t *s);
+
 #ifdef __cplusplus
 }
 #endif

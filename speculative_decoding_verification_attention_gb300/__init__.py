@@ -21,6 +21,7 @@ __all__ = [
     "accept_greedy", "accept_sample", "accept_sample_workspace_size", "attention_workspace_size",
     "gemm_workspace_size", "gemm_plan", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
     "verify_tree_attention", "tree_attention_workspace_size", "accept_tree_greedy",
+    "AdaptiveDraftLength",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -32,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "spec_accept_greedy", "spec_accept_sample", "spec_verify_attention_plan",
     "spec_verify_attention_noalloc", "spec_accept_sample_workspace_size", "spec_verify_gemm_plan",
     "spec_verify_tree_attention_workspace_size", "spec_verify_tree_attention",
-    "spec_accept_tree_greedy",
+    "spec_accept_tree_greedy", "spec_adaptive_init", "spec_adaptive_update", "spec_adaptive_draft_len",
 )
 
 DEV_STATUS_BITS = {
@@ -97,6 +98,12 @@ def library():
             lib.spec_verify_tree_attention.restype = I
             lib.spec_accept_tree_greedy.argtypes = [P, P, P, I, I, I, P, P, P, P, P]
             lib.spec_accept_tree_greedy.restype = I
+            lib.spec_adaptive_init.argtypes = [P, P, I, F]
+            lib.spec_adaptive_init.restype = I
+            lib.spec_adaptive_update.argtypes = [P, P, I]
+            lib.spec_adaptive_update.restype = I
+            lib.spec_adaptive_draft_len.argtypes = [P]
+            lib.spec_adaptive_draft_len.restype = I
             lib.spec_verify_gemm_plan.argtypes = [I, I, I, I, P, I]
             lib.spec_verify_gemm_plan.restype = I
             _lib = lib
@@ -338,3 +345,39 @@ def accept_sample(p, q, draft, u_acc, u_res, n_accepted=None, token=None, worksp
         _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
     _check(st, "spec_accept_sample")
     return n_accepted, token
+
+
+# ------------------------------------------------------------ adaptive draft length
+class _AdaptiveState(ctypes.Structure):
+    _fields_ = [("ema", ctypes.c_float), ("beta", ctypes.c_float), ("rounds", ctypes.c_int),
+                ("n_tiers", ctypes.c_int), ("current", ctypes.c_int), ("tiers", ctypes.c_int * 8)]
+
+
+class AdaptiveDraftLength:
+    """Host controller of the draft length (spec_adaptive_*): an EMA of the
+    accept length picks one of a few draft-length tiers per round."""
+
+    def __init__(self, tiers=(1, 3, 7), beta=0.9):
+        import numpy as np
+        self._s = _AdaptiveState()
+        t = np.ascontiguousarray(tiers, dtype=np.int32)
+        _check(library().spec_adaptive_init(ctypes.byref(self._s), t.ctypes.data_as(ctypes.c_void_p),
+                                            len(t), float(beta)), "spec_adaptive_init")
+
+    @property
+    def draft_len(self):
+        return int(library().spec_adaptive_draft_len(ctypes.byref(self._s)))
+
+    @property
+    def ema(self):
+        return float(self._s.ema)
+
+    def update(self, n_accepted):
+        """n_accepted: host int32 array of the round just verified; returns
+        the draft length for the next round."""
+        import numpy as np
+        a = np.ascontiguousarray(n_accepted, dtype=np.int32)
+        d = library().spec_adaptive_update(ctypes.byref(self._s), a.ctypes.data_as(ctypes.c_void_p), a.size)
+        if d < 0:
+            raise ValueError("spec_adaptive_update rejected its arguments")
+        return int(d)
