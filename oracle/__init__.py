@@ -29,6 +29,11 @@ Parity status of each function (what pins it, in tests/test_oracle_*.py):
                     the accepted-node set on trees with distinct sibling
                     tokens; emitted tokens equal plain greedy decoding of a
                     toy target model.
+  logits_to_probs   exp_f32 within 2 ulp of the exact exponential; the fp32
+                    softmax within its rounding bound of the fp64 softmax; its
+                    Philox equals the independent implementation of the
+                    published definition in synth bit for bit; temperature
+                    scaling and invariance to a constant shift of the logits.
 """
 from __future__ import annotations
 
@@ -50,7 +55,9 @@ def build(force=False):
     """Compile liboracle.so with gcc (OpenMP when available)."""
     if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
         return _LIB
-    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-lm", "-o", _LIB + ".tmp"]
+    # -ffp-contract=off: every fp32 step of the logits softmax rounds on its own
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-lm", "-o",
+            _LIB + ".tmp"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
     except subprocess.CalledProcessError:
@@ -75,9 +82,13 @@ def _load():
             lib.oracle_tree_attention.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
                                                   i32, f64, i64, i32, P, P, P, i32]
             lib.oracle_accept_tree_greedy.argtypes = [P, P, P, i32, i32, i32, P, P, P, i32]
+            lib.oracle_logits_to_probs.argtypes = [P, P, ctypes.c_float, ctypes.c_uint64, i32, i32, i32,
+                                                   P, P, P, P, i32]
+            lib.oracle_exp_f32.argtypes = [P, P, i64]
+            lib.oracle_exp_f32.restype = None
             for f in ("oracle_verify_attention", "oracle_gemm", "oracle_accept_greedy",
                       "oracle_accept_sample", "oracle_max_threads", "oracle_tree_attention",
-                      "oracle_accept_tree_greedy"):
+                      "oracle_accept_tree_greedy", "oracle_logits_to_probs"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -235,3 +246,36 @@ def accept_tree_greedy(p, tokens, parent, threads=0):
     if rc:
         raise ValueError(f"oracle_accept_tree_greedy failed: {rc}")
     return n, t, path[:, :D]
+
+
+def logits_to_probs(zp, zq, temperature, seed, threads=0):
+    """p, q (fp32 softmax of logits / temperature, reading R10) and the
+    Philox uniforms u_acc, u_res (reading R11)."""
+    lib = _load()
+    zp = _c(zp, np.float32)
+    zq = _c(zq, np.float32)
+    B, T, V = zp.shape
+    D = T - 1
+    p = np.empty_like(zp)
+    q = np.empty((B, D, V), np.float32)
+    u_acc = np.empty((B, max(D, 1)), np.float32)
+    u_res = np.empty(B, np.float32)
+    rc = lib.oracle_logits_to_probs(_ptr(zp), _ptr(zq), float(temperature), int(seed), B, D, V, _ptr(p),
+                                    _ptr(q), _ptr(u_acc), _ptr(u_res), int(threads))
+    if rc:
+        raise ValueError(f"oracle_logits_to_probs failed: {rc}")
+    return p, q, np.ascontiguousarray(u_acc[:, :D]), u_res
+
+
+def accept_sample_logits(zp, zq, draft, temperature, seed, threads=0):
+    """Stochastic acceptance from logits: logits_to_probs, then accept_sample."""
+    p, q, u_acc, u_res = logits_to_probs(zp, zq, temperature, seed, threads)
+    return accept_sample(p, q, draft, u_acc, u_res, threads)
+
+
+def exp_f32(y):
+    lib = _load()
+    y = _c(y, np.float32)
+    out = np.empty_like(y)
+    lib.oracle_exp_f32(_ptr(y), _ptr(out), y.size)
+    return out

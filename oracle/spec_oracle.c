@@ -479,3 +479,162 @@ int oracle_accept_tree_greedy(const float *p, const int32_t *tokens, const int32
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Acceptance from logits (the fused form of the stochastic acceptance).
+ *
+ * "Accept x with probability min(1, p(x)/q(x)) ..." (llm-digest,
+ * "Mechanism") with p = softmax(target logits / T), q = softmax(draft
+ * logits / T), and the uniforms drawn by Philox4x32-10 from a seed.
+ *  R9  one temperature T > 0 for both models.
+ *  R10 the softmax is taken in fp32 by a fully specified procedure, so that
+ *      every device computes the same probabilities (the accept/reject
+ *      decisions hinge on them):
+ *        m = max_v z_v;  y_v = (z_v - m) * fl32(1/T);
+ *        e_v = exp_f32(y_v) (below);  Z = sum_v floor(e_v * 2^55) exactly;
+ *        p_v = e_v / fl32(Z * 2^-55)  (fp32 division).
+ *      exp_f32(y), y <= 0: log2 e = hi + lo (fp32 parts); t = y * hi,
+ *      n = rint(t), tl = fma(y, lo, fma(y, hi, -t)), f = (t - n) + tl;
+ *      P(f) = the degree-7 Taylor polynomial of 2^f = e^(f ln 2) with fp32
+ *      coefficients (ln 2)^k / k!, Horner with fused multiply-adds, and
+ *      e = P(f) * 2^n; e = 0 when n < -125.  Every step rounds to nearest.
+ *      fl32(Z * 2^-55) rounds the exact sum to nearest-even.
+ *  R11 u_acc[b][i] = Philox4x32-10(key = seed, counter (b, i, 0, 0)) and
+ *      u_res[b] = Philox4x32-10(key = seed, counter (b, 0, 1, 0)): word 0's
+ *      top 24 bits times 2^-24 (Salmon et al., "Parallel random numbers: as
+ *      easy as 1, 2, 3", SC'11: the Philox S-box, 10 rounds, Weyl key
+ *      schedule).
+ * Then the acceptance is oracle_accept_sample on these p, q, u.
+ * ---------------------------------------------------------------------- */
+static void philox4x32_10(uint32_t c[4], uint64_t key)
+{
+    uint32_t k0 = (uint32_t)key, k1 = (uint32_t)(key >> 32);
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c[0] = n0; c[1] = n1; c[2] = n2; c[3] = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+}
+
+static float philox_u(uint64_t seed, uint32_t c0, uint32_t c1, uint32_t stream)
+{
+    uint32_t c[4] = {c0, c1, stream, 0u};
+    philox4x32_10(c, seed);
+    return (float)((double)(c[0] >> 8) * 0x1p-24);
+}
+
+static float exp_f32(float y)
+{
+    /* log2 e = hi + lo, both fp32; y * log2 e = t + tl with the rounding
+     * error of y * hi recovered exactly by a fused multiply-add */
+    const float log2e_hi = 0x1.715476p+0f, log2e_lo = 0x1.4ae0c0p-26f;
+    const float c0 = 1.0f, c1 = 0x1.62e430p-1f, c2 = 0x1.ebfbe0p-3f, c3 = 0x1.c6b08ep-5f,
+                c4 = 0x1.3b2ab6p-7f, c5 = 0x1.5d87fep-10f, c6 = 0x1.430912p-13f,
+                c7 = 0x1.ffcbfcp-17f;
+    const float t = y * log2e_hi;
+    const float n = rintf(t);
+    if (!(n >= -125.0f)) return 0.0f;          /* also y = -inf */
+    const float tl = fmaf(y, log2e_lo, fmaf(y, log2e_hi, -t));
+    const float f = (t - n) + tl;
+    float p = c7;
+    p = fmaf(p, f, c6);
+    p = fmaf(p, f, c5);
+    p = fmaf(p, f, c4);
+    p = fmaf(p, f, c3);
+    p = fmaf(p, f, c2);
+    p = fmaf(p, f, c1);
+    p = fmaf(p, f, c0);
+    const uint32_t sb = (uint32_t)((int)n + 127) << 23;
+    float scale;
+    memcpy(&scale, &sb, sizeof scale);
+    return p * scale;
+}
+
+/* floor(x * 2^55) for 0 <= x < 2 (0 for anything else), from the bits. */
+static uint64_t fix55(float x)
+{
+    uint32_t b;
+    memcpy(&b, &x, sizeof b);
+    const uint32_t e = b >> 23;                 /* sign bit set: e >= 256 */
+    if (e > 127u || e == 0u) return 0;
+    const uint64_t m = (uint64_t)((b & 0x7FFFFFu) | 0x800000u) << 32;
+    const uint32_t sh = 127u - e;
+    return sh >= 64u ? 0 : m >> sh;
+}
+
+/* Z * 2^-55 rounded to the nearest fp32 (ties to even); Z > 0. */
+static float fix55_to_f32(unsigned __int128 Z)
+{
+    int top = 127;
+    while (!((Z >> top) & 1)) --top;
+    /* keep 24 bits: bits top..top-23 */
+    uint64_t mant;
+    int exp2 = top - 55;                        /* value = 1.xxx * 2^exp2 */
+    if (top >= 23) {
+        const int drop = top - 23;
+        mant = (uint64_t)(Z >> drop);
+        if (drop > 0) {
+            const unsigned __int128 rem = Z & ((((unsigned __int128)1) << drop) - 1);
+            const unsigned __int128 half = ((unsigned __int128)1) << (drop - 1);
+            if (rem > half || (rem == half && (mant & 1))) ++mant;
+            if (mant >> 24) { mant >>= 1; ++exp2; }
+        }
+    } else {
+        mant = (uint64_t)Z << (23 - top);
+    }
+    const uint32_t bits = ((uint32_t)(exp2 + 127) << 23) | ((uint32_t)mant & 0x7FFFFFu);
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return f;
+}
+
+static void softmax_f32(const float *z, int V, float invT, float *p)
+{
+    float m = z[0];
+    for (int v = 1; v < V; ++v) if (z[v] > m) m = z[v];
+    unsigned __int128 Z = 0;
+    for (int v = 0; v < V; ++v) {
+        const float e = exp_f32((z[v] - m) * invT);
+        p[v] = e;
+        Z += fix55(e);
+    }
+    const float zf = fix55_to_f32(Z);
+    for (int v = 0; v < V; ++v) p[v] = p[v] / zf;
+}
+
+/* Probabilities and uniforms of the logits form (readings R9-R11), for the
+ * acceptance oracle and for the tests: p [B][1+D][V], q [B][D][V],
+ * u_acc [B][D], u_res [B]. */
+int oracle_logits_to_probs(const float *zp, const float *zq, float temperature, uint64_t seed,
+                           int B, int D, int V, float *p, float *q, float *u_acc, float *u_res,
+                           int num_threads)
+{
+    if (B < 0 || D < 0 || V < 1 || !(temperature > 0.0f)) return -2;
+    const float invT = 1.0f / temperature;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < (int64_t)B * (2 * D + 1); ++r) {
+        const int64_t b = r / (2 * D + 1), k = r % (2 * D + 1);
+        if (k <= D)
+            softmax_f32(zp + (b * (1 + D) + k) * V, V, invT, p + (b * (1 + D) + k) * V);
+        else
+            softmax_f32(zq + (b * D + (k - D - 1)) * V, V, invT, q + (b * D + (k - D - 1)) * V);
+    }
+    for (int b = 0; b < B; ++b) {
+        for (int i = 0; i < D; ++i) u_acc[(int64_t)b * D + i] = philox_u(seed, (uint32_t)b, (uint32_t)i, 0u);
+        u_res[b] = philox_u(seed, (uint32_t)b, 0u, 1u);
+    }
+    return 0;
+}
+
+/* The exp_f32 of reading R10 on an array (for its pins). */
+void oracle_exp_f32(const float *y, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = exp_f32(y[i]);
+}
