@@ -728,6 +728,47 @@ def case_lines(args):
                               "frac_hbm": by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]})
             del p, q
             torch.cuda.empty_cache()
+    if args.workload in ("logits", "all"):
+        # acceptance from logits: B=256, D=7, V=131072, target logits N(0, 3^2),
+        # draft logits the target's plus N(0, sigma^2) with sigma tuned to alpha = 0.6
+        B, D, V, T = 256, 7, 131072, 1.0
+        sigma, _ = synth.tune_sigma_for_alpha(0.6, V, rows=8, target_std=3.0)
+        g = torch.Generator(device=dev)
+        g.manual_seed(60)
+        zp = torch.randn((B, D + 1, V), generator=g, device=dev) * 3.0
+        zq = (zp[:, :D] + torch.randn((B, D, V), generator=g, device=dev) * sigma).contiguous()
+        qh = torch.softmax(zq.double() / T, -1).float().cpu().numpy()
+        ud = synth.philox_uniform(7, np.arange(B, dtype=np.uint64)[:, None],
+                                  np.arange(D, dtype=np.uint64)[None, :], synth.STREAM_DRAFT)
+        ds = torch.from_numpy(synth.draw_from_rows(qh, ud)).to(dev)
+        del qh
+        na, tk = torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev)
+        wsl = torch.empty(sv.accept_sample_logits_workspace_size(B, D, V), dtype=torch.uint8, device=dev)
+        ms_f = time_launches(lambda: sv.accept_sample_logits(zp, zq, ds, T, 7, na, tk, workspace=wsl),
+                             args.warmup, args.steps, flush)
+        nf = na.cpu().numpy()
+        rows_bytes = B * (2 * D + 1) * V * 4
+        _, sb = accept_bytes(nf, nf, B, D, V)
+        by = rows_bytes + sb
+        lines.append({"case": f"accept from logits B{B} D{D} V{V} T{T} alpha0.6", "kernel": "accept_sample_logits",
+                      "ms": ms_f, "mean_AL": float((nf + 1).mean()),
+                      "accepted_tokens_per_s": float((nf + 1).sum()) / (ms_f * 1e-3),
+                      "algorithmic_bytes": by, "logit_bytes": rows_bytes, "GB_per_s": by / (ms_f * 1e-3) / 1e9,
+                      "frac_hbm": by / (ms_f * 1e-3) / 1e9 / pk["hbm_gbs"]})
+        # the same decisions taken the unfused way: library fp32 softmax of both
+        # tensors (written to HBM), then the probability-form kernels
+        u_acc, u_res = synth.acceptance_uniforms(7, B, D)
+        ua, ur = torch.from_numpy(u_acc).to(dev), torch.from_numpy(u_res).to(dev)
+        wsa = torch.empty(sv.accept_sample_workspace_size(B, V), dtype=torch.uint8, device=dev)
+
+        def unfused():
+            sv.accept_sample(torch.softmax(zp, -1), torch.softmax(zq, -1), ds, ua, ur, na, tk, workspace=wsa)
+        ms_u = time_launches(unfused, args.warmup, args.steps, flush)
+        lines.append({"case": f"accept from logits, unfused (library softmax + accept_sample) B{B} D{D} V{V}",
+                      "kernel": "torch.softmax x2 + accept_sample", "ms": ms_u,
+                      "speedup_of_fused": ms_u / ms_f})
+        del zp, zq
+        torch.cuda.empty_cache()
     for ln in lines:
         ln["peak_source"] = pk["source"]
         print(json.dumps(ln), flush=True)
@@ -746,7 +787,7 @@ def main():
                     help="reference arm: seconds of oracle attention work sampled per step")
     ap.add_argument("--workload", default="step",
                     choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small", "tree",
-                             "adaptive",
+                             "adaptive", "logits",
                              "accept-one"],
                     help="step: the headline line; others print one secondary JSON line per case")
     args = ap.parse_args()

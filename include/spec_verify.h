@@ -13,6 +13,7 @@
  *   spec_accept_greedy     greedy longest-prefix acceptance.
  *   spec_accept_sample     stochastic min(1, p/q) acceptance with residual
  *                          resampling.
+ *   spec_accept_sample_logits   the same from logits, temperature and seed.
  *
  * Conventions shared by every entry point:
  *  - Pointers marked "device" are CUDA device pointers owned by the caller;
@@ -59,6 +60,8 @@ typedef enum {
 #define SPEC_DEV_ERR_LAUNCH      0x00000040u /* launched without the cluster shape it
                                                 needs (e.g. replayed by a tool): did nothing */
 #define SPEC_DEV_ERR_TREE        0x00000080u /* draft tree not in topological order */
+#define SPEC_DEV_ERR_LOGITS      0x00000100u /* a logits row holding NaN or +inf, or no
+                                                finite entry: all its probabilities 0 */
 #define SPEC_DEV_INFO_ZERO_RESIDUAL 0x00010000u /* informational: max(0,p-q) summed to 0
                                                    after a rejection; drew from p instead */
 
@@ -286,7 +289,7 @@ spec_status_t spec_accept_tree_greedy(const float *p, const int32_t *tokens, con
  *   n_accepted, token   device, int32 [B].
  *   workspace  device, spec_accept_sample_workspace_size(B, V) bytes,
  *              256-byte aligned, owned by the caller; scratch only (the
- *              first rejected draft and the exact masses of every 1024- and
+ *              first rejected draft and the exact masses of every 512- and
  *              128-element slice of the needed rows), needs no
  *              initialisation.  Calls sharing a workspace must not overlap
  *              in time.
@@ -298,6 +301,47 @@ spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *
                                  const float *u_acc, const float *u_res, int B, int D, int V,
                                  int32_t *n_accepted, int32_t *token, void *workspace,
                                  size_t workspace_bytes, uint32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Stochastic acceptance from logits.
+ *
+ * The acceptance above with p = softmax(target_logits / T) and
+ * q = softmax(draft_logits / T) taken inside the library, and the uniforms
+ * drawn from `seed` by Philox4x32-10 (Salmon, Moraes, Dror and Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC'11; key = seed, word 0
+ * of the output, u = (word >> 8) * 2^-24):
+ *     u_acc[b][i] from counter (b, i, 0, 0),  u_res[b] from (b, 0, 1, 0).
+ * The softmax is one fully specified fp32 procedure, so the decisions are
+ * the same on every device: per row, m = max_v z_v, y_v = (z_v - m) *
+ * fl32(1/T), e_v = exp_f32(y_v), Z = sum_v floor(e_v 2^55) (exact),
+ * p_v = e_v / fl32(Z 2^-55) (IEEE division).  exp_f32(y): with log2 e =
+ * hi + lo split into two fp32 values, t = y hi, n = rint(t),
+ * f = (t - n) + fma(y, lo, fma(y, hi, -t)), e = P7(f) 2^n where P7 is the
+ * degree-7 Taylor polynomial of 2^f (fp32 coefficients (ln 2)^k / k!,
+ * Horner with fused multiply-adds), and e = 0 when n < -125.  Every step
+ * rounds to nearest-even.
+ * Every logit is read from HBM once for the row statistics; afterwards
+ * only the gathered draft entries and the one row each sequence samples
+ * from are read again.
+ *
+ *   target_logits  device, fp32 [B][1+D][V]; finite or -inf.
+ *   draft_logits   device, fp32 [B][D][V] (may be NULL if D = 0).
+ *   temperature    T, finite and > 0.
+ *   draft, n_accepted, token   as in spec_accept_sample.
+ *   workspace  device, spec_accept_sample_logits_workspace_size(B, D, V)
+ *              bytes, 256-byte aligned; scratch only (the row statistics
+ *              (m, fl32(Z 2^-55)) of the B (2D + 1) rows, then the scratch
+ *              of spec_accept_sample), needs no initialisation.
+ * A row holding NaN or +inf, or only -inf, sets SPEC_DEV_ERR_LOGITS and
+ * reads as all-zero probabilities.
+ * Supported set: B <= 65535, 0 <= D <= 63, 1 <= V <= 2^26.
+ * ---------------------------------------------------------------------- */
+size_t spec_accept_sample_logits_workspace_size(int B, int D, int V);
+
+spec_status_t spec_accept_sample_logits(const float *target_logits, const float *draft_logits,
+                                        const int32_t *draft, float temperature, uint64_t seed, int B, int D,
+                                        int V, int32_t *n_accepted, int32_t *token, void *workspace,
+                                        size_t workspace_bytes, uint32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
  * Host-side planning helper (no GPU work).

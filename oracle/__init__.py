@@ -84,11 +84,12 @@ def _load():
             lib.oracle_accept_tree_greedy.argtypes = [P, P, P, i32, i32, i32, P, P, P, i32]
             lib.oracle_logits_to_probs.argtypes = [P, P, ctypes.c_float, ctypes.c_uint64, i32, i32, i32,
                                                    P, P, P, P, i32]
+            lib.oracle_logits_row_stats.argtypes = [P, P, ctypes.c_float, i32, i32, i32, P, P, i32]
             lib.oracle_exp_f32.argtypes = [P, P, i64]
             lib.oracle_exp_f32.restype = None
             for f in ("oracle_verify_attention", "oracle_gemm", "oracle_accept_greedy",
                       "oracle_accept_sample", "oracle_max_threads", "oracle_tree_attention",
-                      "oracle_accept_tree_greedy", "oracle_logits_to_probs"):
+                      "oracle_accept_tree_greedy", "oracle_logits_to_probs", "oracle_logits_row_stats"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -265,6 +266,24 @@ def logits_to_probs(zp, zq, temperature, seed, threads=0):
     if rc:
         raise ValueError(f"oracle_logits_to_probs failed: {rc}")
     return p, q, np.ascontiguousarray(u_acc[:, :D]), u_res
+
+
+def logits_row_stats(zp, zq, temperature, threads=0):
+    """(m, zf) of reading R10 for every row: [B, 2D + 1] each, row k <= D
+    being target row k and row k > D draft row k - D - 1; rows without a
+    softmax (NaN, +inf or no finite entry) give (0, +inf)."""
+    lib = _load()
+    zp = _c(zp, np.float32)
+    zq = _c(zq, np.float32)
+    B, T, V = zp.shape
+    D = T - 1
+    m = np.empty((B, 2 * D + 1), np.float32)
+    zf = np.empty((B, 2 * D + 1), np.float32)
+    rc = lib.oracle_logits_row_stats(_ptr(zp), _ptr(zq), float(temperature), B, D, V, _ptr(m), _ptr(zf),
+                                     int(threads))
+    if rc < 0:
+        raise ValueError(f"oracle_logits_row_stats failed: {rc}")
+    return m, zf
 
 
 def accept_sample_logits(zp, zq, draft, temperature, seed, threads=0):

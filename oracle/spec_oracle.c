@@ -594,18 +594,35 @@ static float fix55_to_f32(unsigned __int128 Z)
     return f;
 }
 
-static void softmax_f32(const float *z, int V, float invT, float *p)
+/* Row statistics of reading R10: m = max_v z_v and zf = fl32(Z * 2^-55).
+ * A row holding NaN or +inf, or no finite entry, has no softmax: it reads
+ * as all-zero probabilities (m = 0, zf = +inf) and the call returns 1. */
+static int softmax_row_stats(const float *z, int V, float invT, float *m_out, float *zf_out)
 {
-    float m = z[0];
-    for (int v = 1; v < V; ++v) if (z[v] > m) m = z[v];
-    unsigned __int128 Z = 0;
+    int bad = 0;
+    float m = -INFINITY;
     for (int v = 0; v < V; ++v) {
-        const float e = exp_f32((z[v] - m) * invT);
-        p[v] = e;
-        Z += fix55(e);
+        if (isnan(z[v]) || z[v] == INFINITY) bad = 1;
+        else if (z[v] > m) m = z[v];
     }
-    const float zf = fix55_to_f32(Z);
-    for (int v = 0; v < V; ++v) p[v] = p[v] / zf;
+    if (bad || m == -INFINITY) {
+        *m_out = 0.0f;
+        *zf_out = INFINITY;
+        return 1;
+    }
+    unsigned __int128 Z = 0;
+    for (int v = 0; v < V; ++v) Z += fix55(exp_f32((z[v] - m) * invT));
+    *m_out = m;
+    *zf_out = fix55_to_f32(Z);   /* Z >= 2^55: the maximum contributes exp_f32(0) = 1 */
+    return 0;
+}
+
+static int softmax_f32(const float *z, int V, float invT, float *p)
+{
+    float m, zf;
+    const int bad = softmax_row_stats(z, V, invT, &m, &zf);
+    for (int v = 0; v < V; ++v) p[v] = bad ? 0.0f : exp_f32((z[v] - m) * invT) / zf;
+    return bad;
 }
 
 /* Probabilities and uniforms of the logits form (readings R9-R11), for the
@@ -631,6 +648,25 @@ int oracle_logits_to_probs(const float *zp, const float *zq, float temperature, 
         u_res[b] = philox_u(seed, (uint32_t)b, 0u, 1u);
     }
     return 0;
+}
+
+/* The row statistics (m, zf) of reading R10 for the B (2D + 1) rows, row
+ * b (2D + 1) + k being target row k for k <= D and draft row k - D - 1
+ * otherwise.  Returns the number of rows without a softmax. */
+int oracle_logits_row_stats(const float *zp, const float *zq, float temperature, int B, int D, int V,
+                            float *m, float *zf, int num_threads)
+{
+    if (B < 0 || D < 0 || V < 1 || !(temperature > 0.0f)) return -2;
+    const float invT = 1.0f / temperature;
+    int nbad = 0;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : nbad)
+    for (int64_t r = 0; r < (int64_t)B * (2 * D + 1); ++r) {
+        const int64_t b = r / (2 * D + 1), k = r % (2 * D + 1);
+        const float *z = k <= D ? zp + (b * (1 + D) + k) * V : zq + (b * D + (k - D - 1)) * V;
+        nbad += softmax_row_stats(z, V, invT, m + r, zf + r);
+    }
+    return nbad;
 }
 
 /* The exp_f32 of reading R10 on an array (for its pins). */

@@ -21,7 +21,7 @@ __all__ = [
     "accept_greedy", "accept_sample", "accept_sample_workspace_size", "attention_workspace_size",
     "gemm_workspace_size", "gemm_plan", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
     "verify_tree_attention", "tree_attention_workspace_size", "accept_tree_greedy",
-    "AdaptiveDraftLength",
+    "AdaptiveDraftLength", "accept_sample_logits", "accept_sample_logits_workspace_size",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -34,11 +34,13 @@ EXPORTED_SYMBOLS = (
     "spec_verify_attention_noalloc", "spec_accept_sample_workspace_size", "spec_verify_gemm_plan",
     "spec_verify_tree_attention_workspace_size", "spec_verify_tree_attention",
     "spec_accept_tree_greedy", "spec_adaptive_init", "spec_adaptive_update", "spec_adaptive_draft_len",
+    "spec_accept_sample_logits_workspace_size", "spec_accept_sample_logits",
 )
 
 DEV_STATUS_BITS = {
     "PAGE_ID": 0x1, "KV_LEN": 0x2, "TIMEOUT": 0x4, "TOKEN_ID": 0x8, "UNIFORM": 0x10,
-    "ZERO_MASS": 0x20, "LAUNCH": 0x40, "TREE": 0x80, "INFO_ZERO_RESIDUAL": 0x10000,
+    "ZERO_MASS": 0x20, "LAUNCH": 0x40, "TREE": 0x80, "LOGITS": 0x100,
+    "INFO_ZERO_RESIDUAL": 0x10000,
 }
 
 ATTENTION_KEY_TILE = 128   # SPEC_ATTENTION_KEY_TILE: keys per tile of the KV split
@@ -106,6 +108,11 @@ def library():
             lib.spec_adaptive_draft_len.restype = I
             lib.spec_verify_gemm_plan.argtypes = [I, I, I, I, P, I]
             lib.spec_verify_gemm_plan.restype = I
+            lib.spec_accept_sample_logits_workspace_size.argtypes = [I, I, I]
+            lib.spec_accept_sample_logits_workspace_size.restype = S
+            lib.spec_accept_sample_logits.argtypes = [P, P, P, F, ctypes.c_uint64, I, I, I, P, P, P, S,
+                                                      P, P]
+            lib.spec_accept_sample_logits.restype = I
             _lib = lib
     return _lib
 
@@ -344,6 +351,41 @@ def accept_sample(p, q, draft, u_acc, u_res, n_accepted=None, token=None, worksp
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
     _check(st, "spec_accept_sample")
+    return n_accepted, token
+
+
+def accept_sample_logits_workspace_size(B, D, V):
+    return int(library().spec_accept_sample_logits_workspace_size(B, D, V))
+
+
+def accept_sample_logits(target_logits, draft_logits, draft, temperature, seed, n_accepted=None,
+                         token=None, workspace=None, dev_status=None, stream=None):
+    """Stochastic acceptance from logits: p = softmax(target_logits / T),
+    q = softmax(draft_logits / T), uniforms from Philox4x32-10 keyed by
+    ``seed`` (spec_accept_sample_logits).
+
+    ``workspace`` (uint8, ``accept_sample_logits_workspace_size(B, D, V)``
+    bytes) is scratch; without one it is allocated for this call.
+    """
+    import torch
+    B, D1, V = target_logits.shape
+    D = D1 - 1
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=target_logits.device)
+    if token is None:
+        token = torch.empty(B, dtype=torch.int32, device=target_logits.device)
+    need = accept_sample_logits_workspace_size(B, D, V)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=target_logits.device)
+    st = library().spec_accept_sample_logits(
+        _dev(target_logits, "target_logits", torch.float32),
+        _dev(draft_logits, "draft_logits", torch.float32, allow_none=True),
+        _dev(draft, "draft", torch.int32, allow_none=True), float(temperature),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, B, D, V, _dev(n_accepted, "n_accepted", torch.int32),
+        _dev(token, "token", torch.int32), _dev(workspace, "workspace", allow_none=True),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
+    _check(st, "spec_accept_sample_logits")
     return n_accepted, token
 
 

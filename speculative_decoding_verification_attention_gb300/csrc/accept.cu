@@ -333,6 +333,177 @@ __device__ __forceinline__ unsigned long long scaled_threshold(float u, unsigned
     return (hi << (64 - s)) | (lo >> s);
 }
 
+// ------------------------------------------------------- from logits
+// The logits form of the stochastic acceptance takes p = softmax(zp / T)
+// and q = softmax(zq / T) through one fully specified fp32 procedure, so
+// that the accept/reject decisions do not depend on the device's own
+// exponential or summation order:
+//   m = max_v z_v;  y_v = (z_v - m) * fl32(1/T);  e_v = exp_f32(y_v);
+//   Z = sum_v floor(e_v * 2^55) (exact, 128-bit);  p_v = e_v / fl32(Z 2^-55).
+// exp_f32(y), y <= 0, is written here from the mathematics: log2 e = hi +
+// lo (fp32 parts), t = y hi, n = rint(t), f = (t - n) + fma(y, lo, fma(y,
+// hi, -t)), 2^f by its degree-7 Taylor polynomial (coefficients (ln 2)^k /
+// k! rounded to fp32, Horner with fused multiply-adds), times 2^n; 0 when
+// n < -125.  Every operation below rounds to nearest on its own (explicit
+// _rn intrinsics: no contraction).
+__device__ __forceinline__ float exp_f32(float y)
+{
+    const float log2e_hi = 0x1.715476p+0f, log2e_lo = 0x1.4ae0c0p-26f;
+    const float t = __fmul_rn(y, log2e_hi);
+    const float n = rintf(t);
+    if (!(n >= -125.0f)) return 0.0f;   // also y = -inf
+    const float tl = __fmaf_rn(y, log2e_lo, __fmaf_rn(y, log2e_hi, -t));
+    const float f = __fadd_rn(__fsub_rn(t, n), tl);
+    float p = 0x1.ffcbfcp-17f;
+    p = __fmaf_rn(p, f, 0x1.430912p-13f);
+    p = __fmaf_rn(p, f, 0x1.5d87fep-10f);
+    p = __fmaf_rn(p, f, 0x1.3b2ab6p-7f);
+    p = __fmaf_rn(p, f, 0x1.c6b08ep-5f);
+    p = __fmaf_rn(p, f, 0x1.ebfbe0p-3f);
+    p = __fmaf_rn(p, f, 0x1.62e430p-1f);
+    p = __fmaf_rn(p, f, 1.0f);
+    return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(static_cast<int>(n) + 127) << 23));
+}
+
+// floor(x * 2^55) for 0 <= x < 2, 0 for anything else (zero, denormals,
+// negatives, x >= 2, NaN): x = m * 2^(E - 150) with m the 24-bit
+// significand, so x * 2^55 = (m << 32) >> (127 - E).
+__device__ __forceinline__ unsigned long long fix55(float x)
+{
+    const uint32_t bits = __float_as_uint(x);
+    const uint32_t e = bits >> 23;   // the sign bit makes negatives >= 256
+    if (e > 127u || e == 0u) return 0ull;
+    const unsigned long long m = static_cast<unsigned long long>((bits & 0x7FFFFFu) | 0x800000u) << 32;
+    const uint32_t sh = 127u - e;
+    return sh >= 64u ? 0ull : m >> sh;
+}
+
+// A 128-bit unsigned sum as (hi, lo).
+struct U128 {
+    unsigned long long lo, hi;
+};
+
+__device__ __forceinline__ void add128(U128 &a, unsigned long long x)
+{
+    a.lo += x;
+    a.hi += a.lo < x ? 1ull : 0ull;
+}
+
+__device__ __forceinline__ void add128(U128 &a, const U128 &x)
+{
+    a.lo += x.lo;
+    a.hi += x.hi + (a.lo < x.lo ? 1ull : 0ull);
+}
+
+__device__ __forceinline__ U128 warp_sum128(U128 a)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        U128 x;
+        x.lo = __shfl_xor_sync(0xffffffffu, a.lo, o);
+        x.hi = __shfl_xor_sync(0xffffffffu, a.hi, o);
+        add128(a, x);
+    }
+    return a;
+}
+
+// Z * 2^-55 rounded to the nearest fp32, ties to even; Z > 0.  Z is shifted
+// left until its top bit is bit 127; the top 24 bits are the significand,
+// bit 103 the rounding bit and bits 0..102 the sticky bits.
+__device__ __forceinline__ float fix55_to_f32(U128 z)
+{
+    const int top = z.hi ? 127 - __clzll(static_cast<long long>(z.hi)) : 63 - __clzll(static_cast<long long>(z.lo));
+    const int s = 127 - top;
+    unsigned long long h = z.hi, l = z.lo;
+    if (s >= 64) {
+        h = l << (s - 64);
+        l = 0ull;
+    } else if (s > 0) {
+        h = (h << s) | (l >> (64 - s));
+        l <<= s;
+    }
+    unsigned long long mant = h >> 40;                       // 24 bits
+    const bool round_bit = (h >> 39) & 1ull;
+    const bool sticky = (h & ((1ull << 39) - 1)) != 0ull || l != 0ull;
+    int exp2 = top - 55;
+    if (round_bit && (sticky || (mant & 1ull))) {
+        ++mant;
+        if (mant >> 24) {
+            mant >>= 1;
+            ++exp2;
+        }
+    }
+    return __uint_as_float((static_cast<uint32_t>(exp2 + 127) << 23) | (static_cast<uint32_t>(mant) & 0x7FFFFFu));
+}
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): word 0 for counter (c0, c1, stream, 0) and key
+// = seed; the uniform is its top 24 bits times 2^-24.
+__device__ __forceinline__ float philox_u(unsigned long long seed, uint32_t c0, uint32_t c1, uint32_t stream)
+{
+    uint32_t x0 = c0, x1 = c1, x2 = stream, x3 = 0u;
+    uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, x0), lo0 = 0xD2511F53u * x0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, x2), lo1 = 0xCD9E8D57u * x2;
+        const uint32_t n0 = hi1 ^ x1 ^ k0, n2 = hi0 ^ x3 ^ k1;
+        x0 = n0; x1 = lo1; x2 = n2; x3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return __fmul_rn(__uint2float_rn(x0 >> 8), 0x1p-24f);
+}
+
+// A row of logits' softmax parameters: p_v = exp_f32((z_v - m) / T) / zf.
+struct SoftmaxRow {
+    float m, zf, inv_t;
+};
+
+__device__ __forceinline__ float softmax_prob(float z, const SoftmaxRow &r)
+{
+    return __fdiv_rn(exp_f32(__fmul_rn(__fsub_rn(z, r.m), r.inv_t)), r.zf);
+}
+
+// Inputs of the stochastic acceptance.  Probability form: p, q and the
+// uniforms u_acc, u_res.  Logits form: p, q hold the target / draft logits,
+// stats the softmax parameters (m, zf) of every row -- row b (2D + 1) + k
+// is target row k for k <= D and draft row k - D - 1 otherwise -- and the
+// uniforms come from Philox with key `seed`: u_acc[b][i] from counter
+// (b, i, 0, 0), u_res[b] from (b, 0, 1, 0).
+struct SampleIn {
+    const float *p, *q;
+    const float *u_acc, *u_res;
+    const float2 *stats;
+    float inv_t;
+    unsigned long long seed;
+};
+
+template <bool LOGITS>
+__device__ __forceinline__ SoftmaxRow row_params(const SampleIn &in, int b, int D, int k)
+{
+    SoftmaxRow r{0.0f, 1.0f, 1.0f};
+    if (LOGITS) {
+        const float2 s = __ldcg(in.stats + static_cast<int64_t>(b) * (2 * D + 1) + k);
+        r = {s.x, s.y, in.inv_t};
+    }
+    return r;
+}
+
+template <bool LOGITS>
+__device__ __forceinline__ float4 to_prob4(float4 z, const SoftmaxRow &r)
+{
+    if (!LOGITS) return z;
+    return make_float4(softmax_prob(z.x, r), softmax_prob(z.y, r), softmax_prob(z.z, r), softmax_prob(z.w, r));
+}
+
+// Value read for an element past the end of a row: no mass either way.
+template <bool LOGITS>
+__device__ __forceinline__ float pad_value()
+{
+    return LOGITS ? -INFINITY : 0.0f;
+}
+
 // Scratch in the caller's workspace (see spec_accept_sample):
 //   js    int32  [B]            first rejected draft (or D) of each sequence
 //   gtot  uint64 [B][ngroups]   exact residual / bonus mass of every group
@@ -360,11 +531,13 @@ constexpr uint32_t kStreamSmem = kRing * kItemBytes + 1024;
 // Stage 1: first rejected draft of every sequence (one warp per sequence);
 // the accept test u * q(x) < p(x) is evaluated in fp64, where the product
 // is exact.
-__global__ void __launch_bounds__(kThreads) accept_prep_kernel(
-    const float *__restrict__ p, const float *__restrict__ q, const int32_t *__restrict__ draft,
-    const float *__restrict__ u_acc, int B, int D, int V, SampleScratch sc, uint32_t *dev_status)
+template <bool LOGITS>
+__global__ void __launch_bounds__(kThreads) accept_prep_kernel(SampleIn in, const int32_t *__restrict__ draft,
+                                                                int B, int D, int V, SampleScratch sc,
+                                                                uint32_t *dev_status)
 {
     pdl_launch_dependents();
+    if (LOGITS) pdl_wait();   // the row softmax parameters come from the previous kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * kWarps + warp;
     if (b >= B) return;
@@ -378,11 +551,19 @@ __global__ void __launch_bounds__(kThreads) accept_prep_kernel(
                 report(dev_status, SPEC_DEV_ERR_TOKEN_ID);
                 rej = true;
             } else {
-                const double pv = p[(static_cast<int64_t>(b) * (D + 1) + i) * V + x];
-                const double qv = q[(static_cast<int64_t>(b) * D + i) * V + x];
-                const float uf = u_acc[static_cast<int64_t>(b) * D + i];
-                if (!(uf >= 0.0f && uf < 1.0f)) report(dev_status, SPEC_DEV_ERR_UNIFORM);
-                rej = !(static_cast<double>(uf) * qv < pv);   // exact product
+                float pv = in.p[(static_cast<int64_t>(b) * (D + 1) + i) * V + x];
+                float qv = in.q[(static_cast<int64_t>(b) * D + i) * V + x];
+                float uf;
+                if (LOGITS) {
+                    pv = softmax_prob(pv, row_params<true>(in, b, D, i));
+                    qv = softmax_prob(qv, row_params<true>(in, b, D, D + 1 + i));
+                    uf = philox_u(in.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
+                } else {
+                    uf = in.u_acc[static_cast<int64_t>(b) * D + i];
+                    if (!(uf >= 0.0f && uf < 1.0f)) report(dev_status, SPEC_DEV_ERR_UNIFORM);
+                }
+                // the product of two fp32 values is exact in fp64
+                rej = !(static_cast<double>(uf) * static_cast<double>(qv) < static_cast<double>(pv));
             }
         }
         const unsigned m = __ballot_sync(0xffffffffu, rej);
@@ -398,10 +579,11 @@ __global__ void __launch_bounds__(kThreads) accept_prep_kernel(
 // w0 of the n-element slice (sp, sq): staged in shared memory (SMEM,
 // n % 4 == 0) or read from global memory.  Lane k of the result holds step
 // k's total (k < kGroupSteps).
-template <bool SMEM>
+template <bool SMEM, bool LOGITS>
 __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, const float *sq,
                                                                int residual, int w0, int n, bool vec4,
-                                                               int lane)
+                                                               int lane, const SoftmaxRow &rp,
+                                                               const SoftmaxRow &rq)
 {
     unsigned long long mine = 0;
 #pragma unroll
@@ -414,9 +596,11 @@ __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, 
                 xp = *reinterpret_cast<const float4 *>(sp + e);
                 if (residual) xq = *reinterpret_cast<const float4 *>(sq + e);
             } else {
-                xp = load4(sp, e, n, vec4, 0.f);
-                if (residual) xq = load4(sq, e, n, vec4, 0.f);
+                xp = load4(sp, e, n, vec4, pad_value<LOGITS>());
+                if (residual) xq = load4(sq, e, n, vec4, pad_value<LOGITS>());
             }
+            xp = to_prob4<LOGITS>(xp, rp);
+            if (residual) xq = to_prob4<LOGITS>(xq, rq);
             m = mass(xp.x, xq.x, residual) + mass(xp.y, xq.y, residual) + mass(xp.z, xq.z, residual) +
                 mass(xp.w, xq.w, residual);
         }
@@ -431,14 +615,19 @@ __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, 
 // round robin.  The producer warp stages up to kRing items ahead in shared
 // memory with bulk copies; each of the 16 consumer warps turns 512 elements
 // of an item into 4 exact step masses and their group total.
+// LOGITS: the staged slices are logits, turned into probabilities with the
+// softmax parameters of their rows as they are consumed.
+template <bool LOGITS>
 __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
-    const float *__restrict__ p, const float *__restrict__ q, int D, int V, int nchunks, int items,
-    SampleScratch sc, uint32_t *dev_status, bool bulk)
+    SampleIn in, int D, int V, int nchunks, int items, SampleScratch sc, uint32_t *dev_status, bool bulk)
 {
+    const float *__restrict__ p = in.p;
+    const float *__restrict__ q = in.q;
     extern __shared__ uint8_t s_raw[];
     float *ring = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_raw) + 127) & ~uintptr_t(127));
     __shared__ uint64_t full[kRing], empty[kRing];
     __shared__ int s_j[kRing];
+    __shared__ float4 s_rows[kRing];   // LOGITS: (m, zf) of the target row, then of the draft row
     __shared__ int s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
@@ -461,6 +650,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
                 const int b = item / nchunks, chunk = item % nchunks;
                 const int j = __ldcg(sc.js + b);
                 s_j[slot] = j;
+                if (LOGITS) {
+                    const SoftmaxRow rp = row_params<true>(in, b, D, j);
+                    const SoftmaxRow rq = j < D ? row_params<true>(in, b, D, D + 1 + j) : rp;
+                    s_rows[slot] = make_float4(rp.m, rp.zf, rq.m, rq.zf);
+                }
                 if (bulk) {
                     const int64_t e0 = static_cast<int64_t>(chunk) * kChunk;
                     const uint32_t bytes = static_cast<uint32_t>(imin64(kChunk, V - e0)) * 4;  // % 16 == 0
@@ -486,6 +680,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
         const int b = item / nchunks, chunk = item % nchunks;
         const int j = s_j[slot];
         const int residual = j < D;
+        SoftmaxRow rp{0.0f, 1.0f, 1.0f}, rq{0.0f, 1.0f, 1.0f};
+        if (LOGITS) {
+            const float4 r = s_rows[slot];
+            rp = {r.x, r.y, in.inv_t};
+            rq = {r.z, r.w, in.inv_t};
+        }
         const int64_t e0 = static_cast<int64_t>(chunk) * kChunk;
         const int n = static_cast<int>(imin64(kChunk, V - e0));
         const float *sp, *sq;
@@ -496,8 +696,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
             sp = p + (static_cast<int64_t>(b) * (D + 1) + j) * V + e0;
             sq = residual ? q + (static_cast<int64_t>(b) * D + j) * V + e0 : nullptr;
         }
-        const unsigned long long t = bulk ? warp_step_masses<true>(sp, sq, residual, warp * kGroup, n, true, lane)
-                                          : warp_step_masses<false>(sp, sq, residual, warp * kGroup, n, false, lane);
+        const unsigned long long t =
+            bulk ? warp_step_masses<true, LOGITS>(sp, sq, residual, warp * kGroup, n, true, lane, rp, rq)
+                 : warp_step_masses<false, LOGITS>(sp, sq, residual, warp * kGroup, n, false, lane, rp, rq);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
         const int s0 = chunk * (kChunk / kStep) + warp * kGroupSteps;
@@ -513,11 +714,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
 // masses, then the group, the step and finally the element whose running
 // sum first exceeds floor(u * Z) (re-reading only the 128 elements of one
 // step).
+template <bool LOGITS>
 __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
-    const float *__restrict__ p, const float *__restrict__ q, const float *__restrict__ u_res,
-    int B, int D, int V, SampleScratch sc, int32_t *__restrict__ n_accepted,
+    SampleIn in, int B, int D, int V, SampleScratch sc, int32_t *__restrict__ n_accepted,
     int32_t *__restrict__ token, uint32_t *dev_status, bool vec4)
 {
+    const float *__restrict__ p = in.p;
+    const float *__restrict__ q = in.q;
     pdl_wait();   // step and group masses come from the previous kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * kWarps + warp;
@@ -528,8 +731,10 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
     const float *qrow = residual ? q + (static_cast<int64_t>(b) * D + j) * V : nullptr;
     unsigned long long *steps = sc.steps + static_cast<int64_t>(b) * sc.nsteps;
     unsigned long long *gtot = sc.gtot + static_cast<int64_t>(b) * sc.ngroups;
+    const SoftmaxRow rp = row_params<LOGITS>(in, b, D, j);
+    const SoftmaxRow rq = residual ? row_params<LOGITS>(in, b, D, D + 1 + j) : rp;
 
-    float u = u_res[b];
+    float u = LOGITS ? philox_u(in.seed, static_cast<uint32_t>(b), 0u, 1u) : in.u_res[b];
     if (!(u >= 0.0f && u < 1.0f)) {
         if (lane == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
         u = (u >= 1.0f) ? 0x1.fffffep-1f : 0.0f;
@@ -547,7 +752,8 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
         for (int g = 0; g < sc.ngroups; ++g) {
             const int64_t g0 = static_cast<int64_t>(g) * kGroup;
             const int n = static_cast<int>(imin64(kGroup, V - g0));
-            const unsigned long long t = warp_step_masses<false>(prow + g0, nullptr, 0, 0, n, false, lane);
+            const unsigned long long t =
+                warp_step_masses<false, LOGITS>(prow + g0, nullptr, 0, 0, n, false, lane, rp, rq);
             if (lane < kGroupSteps && g * kGroupSteps + lane < sc.nsteps) steps[g * kGroupSteps + lane] = t;
             const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull);
             if (lane == 0) gtot[g] = gt;
@@ -592,8 +798,10 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
         const unsigned long long run_s = __shfl_sync(0xffffffffu, run, l);
         // the element within the step
         const int64_t e = static_cast<int64_t>(step) * kStep + lane * 4;
-        const float4 xp = e < V ? load4(prow, e, V, vec4, 0.f) : make_float4(0, 0, 0, 0);
-        const float4 xq = (residual && e < V) ? load4(qrow, e, V, vec4, 0.f) : make_float4(0, 0, 0, 0);
+        const float pad = pad_value<LOGITS>();
+        const float4 xp = to_prob4<LOGITS>(e < V ? load4(prow, e, V, vec4, pad) : make_float4(pad, pad, pad, pad), rp);
+        const float4 xq = (residual && e < V) ? to_prob4<LOGITS>(load4(qrow, e, V, vec4, pad), rq)
+                                              : make_float4(0, 0, 0, 0);
         const unsigned long long m[4] = {mass(xp.x, xq.x, residual), mass(xp.y, xq.y, residual),
                                          mass(xp.z, xq.z, residual), mass(xp.w, xq.w, residual)};
         const unsigned long long lane_sum = m[0] + m[1] + m[2] + m[3];
@@ -611,6 +819,182 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
     if (lane == 0) {
         n_accepted[b] = j;
         token[b] = tok;
+    }
+}
+
+// Logits row statistics: for every row of the target and draft logits,
+// m = max_v z_v and zf = fl32(2^-55 sum_v floor(exp_f32((z_v - m) / T) 2^55)).
+// One thread-block cluster of CS CTAs per row at a time, CTA `rank` owning
+// the elements [rank * slice, (rank + 1) * slice); clusters walk the rows
+// round robin.  BULK: each CTA stages its slice of the next row in shared
+// memory with a bulk copy while it works on the current one, so every
+// logit is read from HBM once; the max and the exact sum are exchanged
+// through distributed shared memory.  Otherwise both passes read global
+// memory (the second from L2).  Rows whose maximum is not finite, or that
+// hold NaN or +inf, get zf = +inf (every probability 0) and set
+// SPEC_DEV_ERR_LOGITS.
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v)
+{
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+constexpr int kStatsAcc = 64 * 4 * kThreads;   // elements per 64-bit partial sum: 256 per thread
+
+template <int CS, bool BULK>
+__global__ void __launch_bounds__(kThreads, 1) logits_rowstats_kernel(
+    const float *__restrict__ zp, const float *__restrict__ zq, int B, int D, int V, float inv_t, int slice,
+    bool vec4, float2 *__restrict__ stats, uint32_t *dev_status)
+{
+    extern __shared__ uint8_t s_raw[];
+    float *buf = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_raw) + 127) & ~uintptr_t(127));
+    __shared__ uint64_t full[2];
+    __shared__ unsigned long long s_max[CS];      // (bad << 32) | bits of CTA `i`'s max
+    __shared__ unsigned long long s_sum[CS][2];   // CTA `i`'s exact sum (lo, hi)
+    __shared__ float s_wmax[kWarps];
+    __shared__ int s_wbad[kWarps];
+    __shared__ U128 s_wsum[kWarps];
+    __shared__ int s_abort;
+    volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (CS > 1 && cluster_ctas() != static_cast<uint32_t>(CS)) {
+        if (tid == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
+        return;
+    }
+    uint32_t rank = 0;
+    if (CS > 1) asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int cluster = blockIdx.x / CS, nclusters = gridDim.x / CS;
+    const int rows_per_b = 2 * D + 1;
+    const int R = B * rows_per_b;
+    const int64_t e0 = static_cast<int64_t>(rank) * slice;
+    const int len = static_cast<int>(imin64(slice, imin64(V, e0 + slice) - imin64(V, e0)));
+    auto row_src = [&](int r) -> const float * {
+        const int b = r / rows_per_b, k = r % rows_per_b;
+        const float *base = k <= D ? zp + (static_cast<int64_t>(b) * (D + 1) + k) * V
+                                   : zq + (static_cast<int64_t>(b) * D + (k - D - 1)) * V;
+        return base + e0;
+    };
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    // producer state (thread 0): loads issued into each slot, loads waited
+    uint32_t issued0 = 0u, issued1 = 0u;
+    auto issue = [&](int r, int slot) {
+        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(len) * 4u);
+        bulk_load(buf + slot * slice, row_src(r), static_cast<uint32_t>(len) * 4u, &full[slot]);
+        if (slot) ++issued1;
+        else ++issued0;
+    };
+    if (BULK && tid == 0 && cluster < R && len > 0) issue(cluster, 0);
+
+    int k = 0;
+    for (int r = cluster; r < R; r += nclusters, ++k) {
+        const int slot = k & 1;
+        const float *src;
+        if (BULK) {
+            if (tid == 0 && len > 0 && r + nclusters < R && !*abort) issue(r + nclusters, slot ^ 1);
+            if (len > 0) mbar_wait(&full[slot], (k >> 1) & 1, abort, dev_status);
+            src = buf + slot * slice;
+        } else {
+            src = row_src(r);
+        }
+        // pass 1: the maximum (and whether the row holds NaN or +inf)
+        float mx = -INFINITY;
+        bool bad = false;
+        for (int i = tid * 4; i < len; i += kThreads * 4) {
+            const float4 v = BULK ? *reinterpret_cast<const float4 *>(src + i) : load4(src, i, len, vec4, -INFINITY);
+            mx = fmaxf(fmaxf(mx, v.x), fmaxf(v.y, fmaxf(v.z, v.w)));
+            bad |= !(v.x < INFINITY) | !(v.y < INFINITY) | !(v.z < INFINITY) | !(v.w < INFINITY);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const int wbad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            s_wmax[warp] = mx;
+            s_wbad[warp] = wbad;
+        }
+        __syncthreads();
+        if (tid < CS) {
+            float cm = s_wmax[0];
+            int cb = s_wbad[0];
+            for (int w = 1; w < kWarps; ++w) {
+                cm = fmaxf(cm, s_wmax[w]);
+                cb |= s_wbad[w];
+            }
+            const unsigned long long word = (static_cast<unsigned long long>(cb ? 1u : 0u) << 32) | __float_as_uint(cm);
+            if (CS > 1) st_cluster_u64(peer_smem(&s_max[rank], static_cast<uint32_t>(tid)), word);
+            else s_max[0] = word;
+        }
+        if (CS > 1) cluster_sync_all();
+        else __syncthreads();
+        float m = -INFINITY;
+        int rbad = 0;
+#pragma unroll
+        for (int c = 0; c < CS; ++c) {
+            m = fmaxf(m, __uint_as_float(static_cast<uint32_t>(s_max[c])));
+            rbad |= static_cast<int>(s_max[c] >> 32);
+        }
+        rbad |= !(m > -INFINITY);
+        // pass 2: the exact fixed-point sum of the exponentials
+        U128 acc{0ull, 0ull};
+        if (!rbad) {
+            for (int base = 0; base < len; base += kStatsAcc) {
+                const int end = static_cast<int>(imin64(len, static_cast<int64_t>(base) + kStatsAcc));
+                unsigned long long a = 0ull;   // at most 256 terms of at most 2^55
+                for (int i = base + tid * 4; i < end; i += kThreads * 4) {
+                    const float4 v =
+                        BULK ? *reinterpret_cast<const float4 *>(src + i) : load4(src, i, end, vec4, -INFINITY);
+                    a += fix55(exp_f32(__fmul_rn(__fsub_rn(v.x, m), inv_t)));
+                    a += fix55(exp_f32(__fmul_rn(__fsub_rn(v.y, m), inv_t)));
+                    a += fix55(exp_f32(__fmul_rn(__fsub_rn(v.z, m), inv_t)));
+                    a += fix55(exp_f32(__fmul_rn(__fsub_rn(v.w, m), inv_t)));
+                }
+                add128(acc, a);
+            }
+        }
+        acc = warp_sum128(acc);
+        if (lane == 0) s_wsum[warp] = acc;
+        __syncthreads();
+        if (tid < CS) {
+            U128 t = s_wsum[0];
+            for (int w = 1; w < kWarps; ++w) add128(t, s_wsum[w]);
+            if (CS > 1) {
+                st_cluster_u64(peer_smem(&s_sum[rank][0], static_cast<uint32_t>(tid)), t.lo);
+                st_cluster_u64(peer_smem(&s_sum[rank][1], static_cast<uint32_t>(tid)), t.hi);
+            } else {
+                s_sum[0][0] = t.lo;
+                s_sum[0][1] = t.hi;
+            }
+        }
+        if (CS > 1) cluster_sync_all();
+        else __syncthreads();
+        if (rank == 0 && tid == 0) {
+            U128 z{0ull, 0ull};
+            for (int c = 0; c < CS; ++c) add128(z, U128{s_sum[c][0], s_sum[c][1]});
+            float2 st;
+            if (rbad || (z.lo == 0ull && z.hi == 0ull)) {
+                report(dev_status, SPEC_DEV_ERR_LOGITS);
+                st = make_float2(0.0f, INFINITY);
+            } else {
+                st = make_float2(m, fix55_to_f32(z));
+            }
+            stats[r] = st;
+        }
+    }
+    if (BULK && tid == 0 && *abort) {
+        // unwind after a timed-out wait: let the copies still in flight land
+        if (issued0) mbar_wait_drain(&full[0], (issued0 - 1u) & 1u, kWaitTimeoutNs);
+        if (issued1) mbar_wait_drain(&full[1], (issued1 - 1u) & 1u, kWaitTimeoutNs);
     }
 }
 
@@ -687,23 +1071,18 @@ cudaError_t launch_accept_tree_greedy(const float *p, const int32_t *tokens, con
     return launch_greedy<true>(p, tokens, parent, B, D, V, n_acc, token, path, dev_status, st);
 }
 
-size_t accept_sample_workspace_bytes(int B, int V)
-{
-    const size_t nsteps = (static_cast<size_t>(V) + kStep - 1) / kStep;
-    const size_t ngroups = (static_cast<size_t>(V) + kGroup - 1) / kGroup;
-    return align256(sizeof(int32_t) * static_cast<size_t>(B)) +
-           align256(sizeof(unsigned long long) * ngroups * static_cast<size_t>(B)) +
-           align256(sizeof(unsigned long long) * nsteps * static_cast<size_t>(B));
-}
+namespace {
 
-cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *draft,
-                                 const float *u_acc, const float *u_res, int B, int D, int V,
-                                 int32_t *n_acc, int32_t *token, void *workspace,
-                                 uint32_t *dev_status, cudaStream_t st)
+// Stages 1-3 of the stochastic acceptance (prep, stream, finalize) on the
+// scratch that starts at `workspace`.  LOGITS: the first stage waits for the
+// row statistics of the kernel before it (programmatic dependent launch).
+template <bool LOGITS>
+cudaError_t launch_sample_stages(const SampleIn &in, const int32_t *draft, int B, int D, int V, int32_t *n_acc,
+                                 int32_t *token, void *workspace, uint32_t *dev_status, cudaStream_t st)
 {
     // bulk copies need 16-byte aligned rows: V % 4 == 0 and aligned bases
-    const bool bulk = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
-                      (q == nullptr || reinterpret_cast<uintptr_t>(q) % 16 == 0);
+    const bool bulk = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(in.p) % 16 == 0) &&
+                      (in.q == nullptr || reinterpret_cast<uintptr_t>(in.q) % 16 == 0);
     char *w = static_cast<char *>(workspace);
     SampleScratch sc;
     sc.nsteps = (V + kStep - 1) / kStep;
@@ -718,22 +1097,123 @@ cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(accept_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(accept_stream_kernel<LOGITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kStreamSmem));
     if (e != cudaSuccess) return e;
 
     const unsigned sgrid = static_cast<unsigned>((B + kWarps - 1) / kWarps);
-    accept_prep_kernel<<<sgrid, kThreads, 0, st>>>(p, q, draft, u_acc, B, D, V, sc, dev_status);
-    e = cudaGetLastError();
+    if (LOGITS) {
+        e = launch_pdl(accept_prep_kernel<LOGITS>, dim3(sgrid), dim3(kThreads), 0u, st, in, draft, B, D, V, sc,
+                       dev_status);
+    } else {
+        accept_prep_kernel<LOGITS><<<sgrid, kThreads, 0, st>>>(in, draft, B, D, V, sc, dev_status);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     const int nchunks = (V + kChunk - 1) / kChunk;
     const long long items = static_cast<long long>(B) * nchunks;
     const int grid = static_cast<int>(items < sms ? items : sms);
-    e = launch_pdl(accept_stream_kernel, dim3(grid), dim3(kStreamThreads), kStreamSmem, st, p, q, D, V,
+    e = launch_pdl(accept_stream_kernel<LOGITS>, dim3(grid), dim3(kStreamThreads), kStreamSmem, st, in, D, V,
                    nchunks, static_cast<int>(items), sc, dev_status, bulk);
     if (e != cudaSuccess) return e;
-    return launch_pdl(accept_finalize_kernel, dim3(sgrid), dim3(kThreads), 0u, st, p, q, u_res, B, D, V,
-                      sc, n_acc, token, dev_status, bulk);
+    return launch_pdl(accept_finalize_kernel<LOGITS>, dim3(sgrid), dim3(kThreads), 0u, st, in, B, D, V, sc,
+                      n_acc, token, dev_status, bulk);
+}
+
+constexpr uint32_t kStatsStaticSmem = 1024;   // bound on the row-statistics kernel's static shared memory
+
+template <int CS, bool BULK>
+cudaError_t launch_rowstats_cs(const float *zp, const float *zq, int B, int D, int V, float inv_t, int slice,
+                               bool vec4, float2 *stats, uint32_t *dev_status, cudaStream_t st)
+{
+    auto kernel = logits_rowstats_kernel<CS, BULK>;
+    const uint32_t smem = BULK ? static_cast<uint32_t>(2 * slice) * 4u + 128u : 0u;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many clusters as fit on the device at once, at most one per row
+    const long long rows = static_cast<long long>(B) * (2 * D + 1);
+    int clusters = 0;
+    cfg.gridDim = dim3(CS);
+    e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    if (clusters > rows) clusters = static_cast<int>(rows);
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CS));
+    return cudaLaunchKernelEx(&cfg, kernel, zp, zq, B, D, V, inv_t, slice, vec4, stats, dev_status);
+}
+
+template <int CS>
+cudaError_t launch_rowstats(const float *zp, const float *zq, int B, int D, int V, float inv_t, float2 *stats,
+                            uint32_t *dev_status, cudaStream_t st)
+{
+    const int slice = ((V + CS - 1) / CS + 3) & ~3;
+    const bool aligned = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(zp) % 16 == 0) &&
+                         (zq == nullptr || reinterpret_cast<uintptr_t>(zq) % 16 == 0);
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    const bool fits = static_cast<long long>(2 * slice) * 4 + 128 + kStatsStaticSmem <= optin;
+    if (aligned && fits)
+        return launch_rowstats_cs<CS, true>(zp, zq, B, D, V, inv_t, slice, true, stats, dev_status, st);
+    return launch_rowstats_cs<CS, false>(zp, zq, B, D, V, inv_t, slice, aligned, stats, dev_status, st);
+}
+
+}  // namespace
+
+size_t accept_sample_workspace_bytes(int B, int V)
+{
+    const size_t nsteps = (static_cast<size_t>(V) + kStep - 1) / kStep;
+    const size_t ngroups = (static_cast<size_t>(V) + kGroup - 1) / kGroup;
+    return align256(sizeof(int32_t) * static_cast<size_t>(B)) +
+           align256(sizeof(unsigned long long) * ngroups * static_cast<size_t>(B)) +
+           align256(sizeof(unsigned long long) * nsteps * static_cast<size_t>(B));
+}
+
+cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *draft,
+                                 const float *u_acc, const float *u_res, int B, int D, int V,
+                                 int32_t *n_acc, int32_t *token, void *workspace,
+                                 uint32_t *dev_status, cudaStream_t st)
+{
+    const SampleIn in{p, q, u_acc, u_res, nullptr, 1.0f, 0ull};
+    return launch_sample_stages<false>(in, draft, B, D, V, n_acc, token, workspace, dev_status, st);
+}
+
+size_t accept_sample_logits_workspace_bytes(int B, int D, int V)
+{
+    return align256(sizeof(float2) * static_cast<size_t>(B) * (2 * static_cast<size_t>(D) + 1)) +
+           accept_sample_workspace_bytes(B, V);
+}
+
+cudaError_t launch_accept_sample_logits(const float *zp, const float *zq, const int32_t *draft, float temperature,
+                                        unsigned long long seed, int B, int D, int V, int32_t *n_acc,
+                                        int32_t *token, void *workspace, uint32_t *dev_status, cudaStream_t st)
+{
+    float2 *stats = static_cast<float2 *>(workspace);
+    void *rest = static_cast<char *>(workspace) +
+                 align256(sizeof(float2) * static_cast<size_t>(B) * (2 * static_cast<size_t>(D) + 1));
+    const float inv_t = 1.0f / temperature;   // IEEE single-precision division
+    cudaError_t e;
+    switch (pick_cluster(V)) {
+    case 8: e = launch_rowstats<8>(zp, zq, B, D, V, inv_t, stats, dev_status, st); break;
+    case 4: e = launch_rowstats<4>(zp, zq, B, D, V, inv_t, stats, dev_status, st); break;
+    case 2: e = launch_rowstats<2>(zp, zq, B, D, V, inv_t, stats, dev_status, st); break;
+    default: e = launch_rowstats<1>(zp, zq, B, D, V, inv_t, stats, dev_status, st); break;
+    }
+    if (e != cudaSuccess) return e;
+    const SampleIn in{zp, zq, nullptr, nullptr, stats, inv_t, seed};
+    return launch_sample_stages<true>(in, draft, B, D, V, n_acc, token, rest, dev_status, st);
 }
 
 }  // namespace spec

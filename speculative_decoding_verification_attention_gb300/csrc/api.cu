@@ -1,5 +1,6 @@
 // C-ABI entry points: host-side validation, then launches on the caller's
 // stream.  Nothing here allocates device memory.
+#include <cmath>
 #include <cstdio>
 
 #include "attention.h"
@@ -97,6 +98,34 @@ spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *
         return SPEC_ERR_WORKSPACE;
     return from_cuda(launch_accept_sample(p, q, draft, u_acc, u_res, B, D, V, n_accepted, token,
                                           workspace, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+size_t spec_accept_sample_logits_workspace_size(int B, int D, int V)
+{
+    if (B < 0 || D < 0 || D > kMaxDraft || V < 1 || V > (1 << 26)) return 0;
+    return accept_sample_logits_workspace_bytes(B, D, V);
+}
+
+spec_status_t spec_accept_sample_logits(const float *target_logits, const float *draft_logits,
+                                        const int32_t *draft, float temperature, uint64_t seed, int B, int D,
+                                        int V, int32_t *n_accepted, int32_t *token, void *workspace,
+                                        size_t workspace_bytes, uint32_t *dev_status, void *stream)
+{
+    if (B < 0 || D < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+    if (!(temperature > 0.0f) || !(temperature < INFINITY)) return SPEC_ERR_INVALID_ARG;
+    if (D > kMaxDraft || V > (1 << 26)) return SPEC_ERR_UNSUPPORTED;
+    if (B == 0) return SPEC_OK;
+    if (!target_logits || !n_accepted || !token) return SPEC_ERR_INVALID_ARG;
+    if (D > 0 && (!draft_logits || !draft)) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(target_logits, 4) || (draft_logits && !aligned(draft_logits, 4)) || !aligned(n_accepted, 4) ||
+        !aligned(token, 4) || (draft && !aligned(draft, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if (B > 65535) return SPEC_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < accept_sample_logits_workspace_bytes(B, D, V) || !aligned(workspace, 256))
+        return SPEC_ERR_WORKSPACE;
+    return from_cuda(launch_accept_sample_logits(target_logits, D > 0 ? draft_logits : nullptr, draft, temperature,
+                                                 seed, B, D, V, n_accepted, token, workspace, dev_status,
+                                                 static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

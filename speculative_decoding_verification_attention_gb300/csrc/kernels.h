@@ -23,4 +23,10 @@ cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *
                                  int32_t *n_acc, int32_t *token, void *workspace,
                                  uint32_t *dev_status, cudaStream_t st);
 
+size_t accept_sample_logits_workspace_bytes(int B, int D, int V);
+
+cudaError_t launch_accept_sample_logits(const float *zp, const float *zq, const int32_t *draft, float temperature,
+                                        unsigned long long seed, int B, int D, int V, int32_t *n_acc,
+                                        int32_t *token, void *workspace, uint32_t *dev_status, cudaStream_t st);
+
 }  // namespace spec

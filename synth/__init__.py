@@ -244,6 +244,44 @@ def accept_inputs(seed, B, D, V, target_std=2.0, draft_noise=0.5, mode="sample",
     return out
 
 
+def logits_inputs(seed, B, D, V, target_std=3.0, draft_noise=0.5, temperature=1.0, masked=0,
+                  b_offset=0, chunk=16):
+    """Target logits zp [B, 1+D, V] and draft logits zq [B, D, V] (fp32),
+    drafts [B, D] int32.
+
+    zp ~ N(0, target_std^2); zq = zp (first D positions) + N(0, draft_noise^2).
+    ``masked`` vocabulary entries per sequence (the same positions in every
+    row of it) are -inf in both.  Draft i is drawn from the fp64 softmax of
+    zq[b, i] / temperature with Philox stream 2 (the drafter's own sampling).
+    Generated in chunks of sequences to bound host memory.
+    """
+    rng = np.random.default_rng(seed)
+    zp = np.empty((B, 1 + D, V), np.float32)
+    zq = np.empty((B, D, V), np.float32)
+    draft = np.empty((B, D), np.int32)
+    b = np.arange(b_offset, b_offset + B, dtype=np.uint64)
+    i = np.arange(max(D, 1), dtype=np.uint64)
+    ud = philox_uniform(seed, b[:, None], i[None, :], STREAM_DRAFT)[:, :D]
+    for s0 in range(0, B, chunk):
+        s1 = min(B, s0 + chunk)
+        t = (rng.standard_normal((s1 - s0, 1 + D, V), dtype=np.float32) * np.float32(target_std))
+        zp[s0:s1] = t
+        if D:
+            zq[s0:s1] = t[:, :D, :] + rng.standard_normal((s1 - s0, D, V), dtype=np.float32) * np.float32(
+                draft_noise)
+        if masked:
+            for s in range(s0, s1):
+                cols = rng.choice(V, size=min(masked, V - 1), replace=False)
+                zp[s][:, cols] = -np.inf
+                zq[s][:, cols] = -np.inf
+        if D:
+            probs = _softmax64(zq[s0:s1].astype(np.float64) / temperature)
+            draft[s0:s1] = draw_from_rows(probs, ud[s0:s1])
+            del probs
+        del t
+    return dict(zp=zp, zq=zq, draft=draft, B=B, D=D, V=V, temperature=temperature, seed=seed)
+
+
 def gemm_inputs(seed, M, N, K, w_std=0.02):
     rng = np.random.default_rng(seed)
     x = f32_to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))

@@ -109,3 +109,26 @@ def test_tree_entry_points_reject_bad_arguments(lib):
     assert g(FAKE, FAKE, FAKE, 2, 64, 10, FAKE, FAKE, None, None, None) == UNSUPPORTED
     assert g(FAKE, FAKE, FAKE, 2, 3, 0, FAKE, FAKE, None, None, None) == INVALID
     assert g(None, None, None, 0, 3, 10, None, None, None, None, None) == 0
+
+
+def test_logits_acceptance_rejects_bad_arguments(lib):
+    f = lib.spec_accept_sample_logits
+    W = 1 << 30
+    args = lambda T=1.0, zp=FAKE, zq=FAKE, dr=FAKE, B=2, D=3, V=10, ws=FAKE, wb=W: (
+        zp, zq, dr, T, 7, B, D, V, FAKE, FAKE, ws, wb, None, None)
+    assert f(*args(T=0.0)) == INVALID
+    assert f(*args(T=-1.0)) == INVALID
+    assert f(*args(T=float("nan"))) == INVALID
+    assert f(*args(T=float("inf"))) == INVALID
+    assert f(*args(zp=None)) == INVALID
+    assert f(*args(zq=None)) == INVALID
+    assert f(*args(dr=None)) == INVALID
+    assert f(*args(zp=P(0x7F0000001002))) == INVALID
+    assert f(*args(V=0)) == INVALID
+    assert f(*args(D=64)) == UNSUPPORTED
+    assert f(*args(ws=None)) == WORKSPACE
+    need = lib.spec_accept_sample_logits_workspace_size(2, 3, 10)
+    assert need >= lib.spec_accept_sample_workspace_size(2, 10) + 2 * 7 * 8
+    assert f(*args(wb=need - 1)) == WORKSPACE
+    assert f(*args(zq=None, dr=None, D=0, B=0)) == 0   # empty batch: no-op
+    assert lib.spec_accept_sample_logits_workspace_size(2, 64, 10) == 0

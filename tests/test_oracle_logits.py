@@ -99,3 +99,47 @@ def test_first_token_follows_the_target(oracle_lib):
     counts = np.bincount(first, minlength=V)
     expect = fp64_softmax(zt, T) * B
     assert stats.chisquare(counts, expect).pvalue > 1e-3
+
+
+def test_row_stats_max_and_exact_sum(oracle_lib):
+    """m is the row maximum (numpy's); zf is the sum of the fp32
+    exponentials truncated to 2^-55, within the exponential's 2 ulp of the
+    fp64 sum of exp((z - m) / T) (the truncation adds at most V 2^-55)."""
+    rng = np.random.default_rng(11)
+    B, D, V, T = 4, 3, 6000, 0.8
+    zp = (rng.standard_normal((B, D + 1, V)) * 3).astype(np.float32)
+    zq = (rng.standard_normal((B, D, V)) * 3).astype(np.float32)
+    m, zf = oracle_lib.logits_row_stats(zp, zq, T)
+    rows = np.concatenate([zp, zq], axis=1)
+    assert np.array_equal(m, rows.max(axis=-1))
+    invT = np.float32(1.0) / np.float32(T)
+    y = (rows - rows.max(axis=-1, keepdims=True)) * invT          # fp32, as specified
+    ref = np.exp(y.astype(np.float64)).sum(axis=-1)
+    assert (np.abs(zf / ref - 1) <= 2 * 2.0 ** -24 + 2.0 ** -24 + V * 2.0 ** -55).all()
+    # the maximum contributes exactly 1, so zf >= 1
+    assert (zf >= 1.0).all()
+
+
+def test_row_stats_truncation_is_exact_on_dyadic_rows(oracle_lib):
+    """Rows whose exponentials are exactly 1 or 0 (k equal maxima, the rest
+    -inf) sum without rounding: zf = k exactly and p = fl32(1 / k)."""
+    V = 100
+    for k in (1, 2, 3, 7, 64, 100):
+        z = np.full((1, 1, V), -np.inf, np.float32)
+        z[0, 0, :k] = 5.0
+        m, zf = oracle_lib.logits_row_stats(z, np.zeros((1, 0, V), np.float32), 1.0)
+        assert m[0, 0] == 5.0 and zf[0, 0] == np.float32(k)
+        p, _, _, _ = oracle_lib.logits_to_probs(z, np.zeros((1, 0, V), np.float32), 1.0, 0)
+        assert (p[0, 0, :k] == np.float32(1.0) / np.float32(k)).all() and (p[0, 0, k:] == 0).all()
+
+
+def test_rows_without_a_softmax(oracle_lib):
+    V = 50
+    zp = np.zeros((3, 1, V), np.float32)
+    zp[0, 0, 3] = np.nan
+    zp[1, 0, :] = -np.inf
+    zp[2, 0, 7] = np.inf
+    m, zf = oracle_lib.logits_row_stats(zp, np.zeros((3, 0, V), np.float32), 1.0)
+    assert (m == 0).all() and np.isinf(zf).all()
+    p, _, _, _ = oracle_lib.logits_to_probs(zp, np.zeros((3, 0, V), np.float32), 1.0, 0)
+    assert (p == 0).all()
