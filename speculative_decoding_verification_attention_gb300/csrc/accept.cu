@@ -38,7 +38,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kStep = 128;   // elements per warp step
-constexpr int kUnroll = 8;   // greedy: steps whose loads are in flight together
 
 __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 
@@ -363,19 +362,6 @@ __device__ __forceinline__ float exp_f32(float y)
     p = __fmaf_rn(p, f, 0x1.62e430p-1f);
     p = __fmaf_rn(p, f, 1.0f);
     return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(static_cast<int>(n) + 127) << 23));
-}
-
-// floor(x * 2^55) for 0 <= x < 2, 0 for anything else (zero, denormals,
-// negatives, x >= 2, NaN): x = m * 2^(E - 150) with m the 24-bit
-// significand, so x * 2^55 = (m << 32) >> (127 - E).
-__device__ __forceinline__ unsigned long long fix55(float x)
-{
-    const uint32_t bits = __float_as_uint(x);
-    const uint32_t e = bits >> 23;   // the sign bit makes negatives >= 256
-    if (e > 127u || e == 0u) return 0ull;
-    const unsigned long long m = static_cast<unsigned long long>((bits & 0x7FFFFFu) | 0x800000u) << 32;
-    const uint32_t sh = 127u - e;
-    return sh >= 64u ? 0ull : m >> sh;
 }
 
 // A 128-bit unsigned sum as (hi, lo).
@@ -824,18 +810,140 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
 
 // Logits row statistics: for every row of the target and draft logits,
 // m = max_v z_v and zf = fl32(2^-55 sum_v floor(exp_f32((z_v - m) / T) 2^55)).
-// One thread-block cluster of CS CTAs per row at a time, CTA `rank` owning
-// the elements [rank * slice, (rank + 1) * slice); clusters walk the rows
-// round robin.  BULK: each CTA stages its slice of the next row in shared
-// memory with a bulk copy while it works on the current one, so every
-// logit is read from HBM once; the max and the exact sum are exchanged
-// through distributed shared memory.  Otherwise both passes read global
-// memory (the second from L2).  Rows whose maximum is not finite, or that
-// hold NaN or +inf, get zf = +inf (every probability 0) and set
-// SPEC_DEV_ERR_LOGITS.
-__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v)
+//
+// One thread-block cluster of CS CTAs works on one row at a time, CTA
+// `rank` owning the elements [rank * slice, (rank + 1) * slice); clusters
+// walk the rows round robin, several clusters' CTAs sharing an SM so that
+// one CTA's copy or exchange overlaps another's arithmetic.  BULK: the
+// slice is staged in shared memory by one bulk copy, so every logit is read
+// from HBM once; otherwise both passes read global memory (the second from
+// L2).  Pass 1 takes the slice maximum; the CTAs exchange their maxima
+// through distributed shared memory (asynchronous stores that complete on
+// the receiver's mbarrier; no cluster-wide barrier per row).  Pass 2 sums
+// the fixed-point exponentials; the partial sums go to the row's owner
+// (rank = row iteration mod CS), which writes (m, zf).  Rows whose maximum
+// is not finite, or that hold NaN or +inf, get zf = +inf (every
+// probability 0) and set SPEC_DEV_ERR_LOGITS.
+//
+// Pass 2 evaluates exp_f32 on pairs of elements with packed fp32x2
+// instructions, each step rounding exactly like the scalar definition
+// (add/sub/mul/fma .rn on both halves).  Two rewrites keep it bit-identical:
+//  - it carries the negations t' = -t = y * (-hi) and F = -f, so that no
+//    operand needs negating: fma(y, hi, t') is fma(y, hi, -t), and the
+//    Taylor polynomial in F with coefficients (-1)^k c_k yields exactly the
+//    same Horner values as the polynomial in f (round to nearest is
+//    symmetric);
+//  - rint(t) is (t + 1.5 * 2^23) - 1.5 * 2^23, exact with ties to even for
+//    |t| < 2^22 (guaranteed by clamping y at -80, which changes no term:
+//    every y <= -80 contributes floor(e 2^55) = 0).
+// The fixed-point term floor(P 2^n 2^55), P = mp 2^(ep - 150) the
+// polynomial value, is mp 2^s with s = ep + n - 95 <= 32: for s >= 1 it is
+// 2 * (mp * 2^(s - 1)) (one 32 x 32 -> 64-bit multiply-add), for s <= 0 it
+// is mp >> -s; both shifts clamp at 32, so the other case contributes 0 and
+// no branch is needed.
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi)
 {
-    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+    return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo_of(unsigned long long v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_of(unsigned long long v)
+{
+    return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c)
+{
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t shl_clamp(uint32_t x, uint32_t s)
+{
+    uint32_t d;
+    asm("shl.b32 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(s));
+    return d;
+}
+__device__ __forceinline__ uint32_t shr_clamp(uint32_t x, uint32_t s)
+{
+    uint32_t d;
+    asm("shr.b32 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(s));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Row constants of pass 2, packed for both halves of a pair.
+struct ExpConsts {
+    unsigned long long neg_m, inv_t, neg_hi, hi, lo, magic, c[8];
+};
+
+__device__ __forceinline__ ExpConsts exp_consts(float m, float inv_t)
+{
+    ExpConsts k;
+    k.neg_m = pack2(-m, -m);
+    k.inv_t = pack2(inv_t, inv_t);
+    k.neg_hi = pack2(-0x1.715476p+0f, -0x1.715476p+0f);
+    k.hi = pack2(0x1.715476p+0f, 0x1.715476p+0f);
+    k.lo = pack2(0x1.4ae0c0p-26f, 0x1.4ae0c0p-26f);
+    k.magic = pack2(0x1.8p+23f, 0x1.8p+23f);
+    const float c[8] = {1.0f, 0x1.62e430p-1f, 0x1.ebfbe0p-3f, 0x1.c6b08ep-5f,
+                        0x1.3b2ab6p-7f, 0x1.5d87fep-10f, 0x1.430912p-13f, 0x1.ffcbfcp-17f};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) k.c[i] = (i & 1) ? pack2(-c[i], -c[i]) : pack2(c[i], c[i]);
+    return k;
+}
+
+// One element's fixed-point term from the polynomial value P (bits pb) and
+// r = t + 1.5 * 2^23 (bits rb): adds to big (terms / 2 for s >= 1) or small.
+__device__ __forceinline__ void fix_term(uint32_t pb, uint32_t rb, unsigned long long &big, uint32_t &small)
+{
+    const uint32_t mp = (pb & 0x7FFFFFu) | 0x800000u;
+    const uint32_t ep = pb >> 23;
+    // s - 1 = ep + (rb - 0x4B400000) - 96, -s = 0x4B400000 + 95 - ep - rb (mod 2^32)
+    const uint32_t s1 = ep + rb - (0x4B400000u + 96u);
+    const uint32_t ns = (0x4B400000u + 95u) - ep - rb;
+    big += static_cast<unsigned long long>(mp) * shl_clamp(1u, s1);
+    small += shr_clamp(mp, ns);
+}
+
+// floor(exp_f32((z - m) / T) 2^55) of the two elements of a pair, added to
+// big / small.
+__device__ __forceinline__ void pair_terms(unsigned long long z2, const ExpConsts &k, unsigned long long &big,
+                                           uint32_t &small)
+{
+    unsigned long long y = mul2(add2(z2, k.neg_m), k.inv_t);
+    y = pack2(fmaxf(lo_of(y), -80.0f), fmaxf(hi_of(y), -80.0f));
+    const unsigned long long tn = mul2(y, k.neg_hi);            // -t
+    const unsigned long long tl = fma2(y, k.lo, fma2(y, k.hi, tn));
+    const unsigned long long r = sub2(k.magic, tn);             // t + 1.5 * 2^23
+    const unsigned long long n = sub2(r, k.magic);              // rint(t)
+    const unsigned long long F = sub2(add2(tn, n), tl);         // -f
+    unsigned long long P = k.c[7];
+#pragma unroll
+    for (int i = 6; i >= 0; --i) P = fma2(P, F, k.c[i]);
+    fix_term(static_cast<uint32_t>(P), static_cast<uint32_t>(r), big, small);
+    fix_term(static_cast<uint32_t>(P >> 32), static_cast<uint32_t>(r >> 32), big, small);
 }
 
 __device__ __forceinline__ void cluster_sync_all()
@@ -843,25 +951,33 @@ __device__ __forceinline__ void cluster_sync_all()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-constexpr int kStatsAcc = 64 * 4 * kThreads;   // elements per 64-bit partial sum: 256 per thread
+__device__ __forceinline__ void st_async_peer_v2(uint32_t addr, unsigned long long a, unsigned long long b,
+                                                 uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b64 [%0], {%1, %2}, [%3];" ::"r"(addr),
+                 "l"(a), "l"(b), "r"(bar)
+                 : "memory");
+}
+
+constexpr int kStatsChunk = 256 * kThreads;   // elements per partial sum: 256 per thread
 
 template <int CS, bool BULK>
-__global__ void __launch_bounds__(kThreads, 1) logits_rowstats_kernel(
+__global__ void __launch_bounds__(kThreads, 3) logits_rowstats_kernel(
     const float *__restrict__ zp, const float *__restrict__ zq, int B, int D, int V, float inv_t, int slice,
     bool vec4, float2 *__restrict__ stats, uint32_t *dev_status)
 {
     extern __shared__ uint8_t s_raw[];
     float *buf = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_raw) + 127) & ~uintptr_t(127));
-    __shared__ uint64_t full[2];
-    __shared__ unsigned long long s_max[CS];      // (bad << 32) | bits of CTA `i`'s max
-    __shared__ unsigned long long s_sum[CS][2];   // CTA `i`'s exact sum (lo, hi)
+    __shared__ uint64_t full, bar_max[2], bar_sum[2];
+    __shared__ unsigned long long s_xmax[2][CS];   // (bad << 32) | bits of CTA c's max, by row parity
+    __shared__ ulonglong2 s_xsum[2][CS];           // CTA c's exact partial sum (lo, hi), owned rows
     __shared__ float s_wmax[kWarps];
     __shared__ int s_wbad[kWarps];
     __shared__ U128 s_wsum[kWarps];
     __shared__ int s_abort;
     volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (CS > 1 && cluster_ctas() != static_cast<uint32_t>(CS)) {
+    if (cluster_ctas() != static_cast<uint32_t>(CS)) {   // uniform over the grid
         if (tid == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
         return;
     }
@@ -879,43 +995,71 @@ __global__ void __launch_bounds__(kThreads, 1) logits_rowstats_kernel(
         return base + e0;
     };
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
+        mbar_init(&full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar_max[i], 1);
+            mbar_init(&bar_sum[i], 1);
+        }
         s_abort = 0;
         fence_mbar_init();
     }
-    __syncthreads();
+    if (CS > 1) cluster_sync_all();   // every peer's barriers exist before the first send
+    else __syncthreads();
     pdl_launch_dependents();
 
-    // producer state (thread 0): loads issued into each slot, loads waited
-    uint32_t issued0 = 0u, issued1 = 0u;
-    auto issue = [&](int r, int slot) {
-        mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(len) * 4u);
-        bulk_load(buf + slot * slice, row_src(r), static_cast<uint32_t>(len) * 4u, &full[slot]);
-        if (slot) ++issued1;
-        else ++issued0;
+    // the owner of row iteration k (k % CS == rank) collects the partial sums
+    auto finish_row = [&](int k, int r, float m, int rbad) {
+        const int slot = (k / CS) & 1;
+        if (CS > 1 && !mbar_wait(&bar_sum[slot], ((k / CS) >> 1) & 1, abort, dev_status)) return;
+        U128 z{0ull, 0ull};
+        for (int c = 0; c < CS; ++c) add128(z, U128{s_xsum[slot][c].x, s_xsum[slot][c].y});
+        float2 st;
+        if (rbad || (z.lo == 0ull && z.hi == 0ull)) {
+            report(dev_status, SPEC_DEV_ERR_LOGITS);
+            st = make_float2(0.0f, INFINITY);
+        } else {
+            st = make_float2(m, fix55_to_f32(z));
+        }
+        stats[r] = st;
     };
-    if (BULK && tid == 0 && cluster < R && len > 0) issue(cluster, 0);
+    int pend_k = -1, pend_r = 0, pend_bad = 0;   // thread 0: an owned row whose sums are still due
+    float pend_m = 0.0f;
+    uint32_t loads = 0;   // thread 0: copies issued
 
     int k = 0;
     for (int r = cluster; r < R; r += nclusters, ++k) {
-        const int slot = k & 1;
-        const float *src;
-        if (BULK) {
-            if (tid == 0 && len > 0 && r + nclusters < R && !*abort) issue(r + nclusters, slot ^ 1);
-            if (len > 0) mbar_wait(&full[slot], (k >> 1) & 1, abort, dev_status);
-            src = buf + slot * slice;
-        } else {
-            src = row_src(r);
+        const int owner = k % CS;
+        if (tid == 0) {
+            if (BULK && len > 0 && !*abort) {
+                mbar_arrive_expect_tx(&full, static_cast<uint32_t>(len) * 4u);
+                bulk_load(buf, row_src(r), static_cast<uint32_t>(len) * 4u, &full);
+                ++loads;
+            }
+            if (CS > 1) {
+                mbar_arrive_expect_tx(&bar_max[k & 1], CS * 8u);
+                if (owner == static_cast<int>(rank)) mbar_arrive_expect_tx(&bar_sum[(k / CS) & 1], CS * 16u);
+            }
+            // while this row's slice lands: the sums of the previous owned row
+            if (pend_k >= 0) {
+                finish_row(pend_k, pend_r, pend_m, pend_bad);
+                pend_k = -1;
+            }
         }
-        // pass 1: the maximum (and whether the row holds NaN or +inf)
+        const float *src = row_src(r);
+        if (BULK) {
+            // row iteration k's copy completes phase k of `full`
+            if (len > 0) mbar_wait(&full, static_cast<uint32_t>(k) & 1u, abort, dev_status);
+            src = buf;
+        }
+        // pass 1: the maximum; a NaN anywhere makes the running sum NaN
         float mx = -INFINITY;
-        bool bad = false;
+        unsigned long long acc2 = 0ull;
         for (int i = tid * 4; i < len; i += kThreads * 4) {
             const float4 v = BULK ? *reinterpret_cast<const float4 *>(src + i) : load4(src, i, len, vec4, -INFINITY);
-            mx = fmaxf(fmaxf(mx, v.x), fmaxf(v.y, fmaxf(v.z, v.w)));
-            bad |= !(v.x < INFINITY) | !(v.y < INFINITY) | !(v.z < INFINITY) | !(v.w < INFINITY);
+            mx = max3(mx, max3(v.x, v.y, v.z), v.w);
+            acc2 = add2(acc2, add2(pack2(v.x, v.y), pack2(v.z, v.w)));
         }
+        const bool bad = lo_of(acc2) != lo_of(acc2) || hi_of(acc2) != hi_of(acc2);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         const int wbad = __any_sync(0xffffffffu, bad);
@@ -932,70 +1076,67 @@ __global__ void __launch_bounds__(kThreads, 1) logits_rowstats_kernel(
                 cb |= s_wbad[w];
             }
             const unsigned long long word = (static_cast<unsigned long long>(cb ? 1u : 0u) << 32) | __float_as_uint(cm);
-            if (CS > 1) st_cluster_u64(peer_smem(&s_max[rank], static_cast<uint32_t>(tid)), word);
-            else s_max[0] = word;
+            if (CS > 1)
+                st_async_peer(peer_smem(&s_xmax[k & 1][rank], static_cast<uint32_t>(tid)), word,
+                              peer_smem(&bar_max[k & 1], static_cast<uint32_t>(tid)));
+            else
+                s_xmax[k & 1][0] = word;
         }
-        if (CS > 1) cluster_sync_all();
+        if (CS > 1) mbar_wait(&bar_max[k & 1], (k >> 1) & 1, abort, dev_status);
         else __syncthreads();
         float m = -INFINITY;
         int rbad = 0;
 #pragma unroll
         for (int c = 0; c < CS; ++c) {
-            m = fmaxf(m, __uint_as_float(static_cast<uint32_t>(s_max[c])));
-            rbad |= static_cast<int>(s_max[c] >> 32);
+            const unsigned long long w = s_xmax[k & 1][c];
+            m = fmaxf(m, __uint_as_float(static_cast<uint32_t>(w)));
+            rbad |= static_cast<int>(w >> 32);
         }
-        rbad |= !(m > -INFINITY);
+        rbad |= !(m > -INFINITY) | !(m < INFINITY);
         // pass 2: the exact fixed-point sum of the exponentials
         U128 acc{0ull, 0ull};
         if (!rbad) {
-            for (int base = 0; base < len; base += kStatsAcc) {
-                const int end = static_cast<int>(imin64(len, static_cast<int64_t>(base) + kStatsAcc));
-                unsigned long long a = 0ull;   // at most 256 terms of at most 2^55
+            const ExpConsts kc = exp_consts(m, inv_t);
+            for (int base = 0; base < len; base += kStatsChunk) {
+                const int end = static_cast<int>(imin64(len, static_cast<int64_t>(base) + kStatsChunk));
+                unsigned long long big = 0ull;   // at most 256 terms of at most 2^54
+                uint32_t small = 0u;             // at most 256 terms below 2^24
                 for (int i = base + tid * 4; i < end; i += kThreads * 4) {
                     const float4 v =
                         BULK ? *reinterpret_cast<const float4 *>(src + i) : load4(src, i, end, vec4, -INFINITY);
-                    a += fix55(exp_f32(__fmul_rn(__fsub_rn(v.x, m), inv_t)));
-                    a += fix55(exp_f32(__fmul_rn(__fsub_rn(v.y, m), inv_t)));
-                    a += fix55(exp_f32(__fmul_rn(__fsub_rn(v.z, m), inv_t)));
-                    a += fix55(exp_f32(__fmul_rn(__fsub_rn(v.w, m), inv_t)));
+                    pair_terms(pack2(v.x, v.y), kc, big, small);
+                    pair_terms(pack2(v.z, v.w), kc, big, small);
                 }
-                add128(acc, a);
+                add128(acc, (big << 1) + small);
             }
         }
         acc = warp_sum128(acc);
         if (lane == 0) s_wsum[warp] = acc;
-        __syncthreads();
-        if (tid < CS) {
+        __syncthreads();   // also: every thread is done with this slice
+        if (tid == 0) {
             U128 t = s_wsum[0];
             for (int w = 1; w < kWarps; ++w) add128(t, s_wsum[w]);
-            if (CS > 1) {
-                st_cluster_u64(peer_smem(&s_sum[rank][0], static_cast<uint32_t>(tid)), t.lo);
-                st_cluster_u64(peer_smem(&s_sum[rank][1], static_cast<uint32_t>(tid)), t.hi);
-            } else {
-                s_sum[0][0] = t.lo;
-                s_sum[0][1] = t.hi;
+            const int slot = (k / CS) & 1;
+            if (CS > 1)
+                st_async_peer_v2(peer_smem(&s_xsum[slot][rank], static_cast<uint32_t>(owner)), t.lo, t.hi,
+                                 peer_smem(&bar_sum[slot], static_cast<uint32_t>(owner)));
+            else
+                s_xsum[slot][0] = make_ulonglong2(t.lo, t.hi);
+            if (owner == static_cast<int>(rank)) {
+                pend_k = k;
+                pend_r = r;
+                pend_m = m;
+                pend_bad = rbad;
             }
         }
-        if (CS > 1) cluster_sync_all();
-        else __syncthreads();
-        if (rank == 0 && tid == 0) {
-            U128 z{0ull, 0ull};
-            for (int c = 0; c < CS; ++c) add128(z, U128{s_sum[c][0], s_sum[c][1]});
-            float2 st;
-            if (rbad || (z.lo == 0ull && z.hi == 0ull)) {
-                report(dev_status, SPEC_DEV_ERR_LOGITS);
-                st = make_float2(0.0f, INFINITY);
-            } else {
-                st = make_float2(m, fix55_to_f32(z));
-            }
-            stats[r] = st;
-        }
     }
-    if (BULK && tid == 0 && *abort) {
-        // unwind after a timed-out wait: let the copies still in flight land
-        if (issued0) mbar_wait_drain(&full[0], (issued0 - 1u) & 1u, kWaitTimeoutNs);
-        if (issued1) mbar_wait_drain(&full[1], (issued1 - 1u) & 1u, kWaitTimeoutNs);
+    if (tid == 0) {
+        if (pend_k >= 0) finish_row(pend_k, pend_r, pend_m, pend_bad);
+        // unwind after a timed-out wait: let a copy still in flight land
+        if (BULK && *abort && loads) mbar_wait_drain(&full, (loads - 1u) & 1u, kWaitTimeoutNs);
     }
+    // keep this CTA's shared memory alive until every peer is done with it
+    if (CS > 1) cluster_sync_all();
 }
 
 }  // namespace
@@ -1127,7 +1268,7 @@ cudaError_t launch_rowstats_cs(const float *zp, const float *zq, int B, int D, i
                                bool vec4, float2 *stats, uint32_t *dev_status, cudaStream_t st)
 {
     auto kernel = logits_rowstats_kernel<CS, BULK>;
-    const uint32_t smem = BULK ? static_cast<uint32_t>(2 * slice) * 4u + 128u : 0u;
+    const uint32_t smem = BULK ? static_cast<uint32_t>(slice) * 4u + 128u : 0u;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -1164,7 +1305,7 @@ cudaError_t launch_rowstats(const float *zp, const float *zq, int B, int D, int 
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    const bool fits = static_cast<long long>(2 * slice) * 4 + 128 + kStatsStaticSmem <= optin;
+    const bool fits = static_cast<long long>(slice) * 4 + 128 + kStatsStaticSmem <= optin;
     if (aligned && fits)
         return launch_rowstats_cs<CS, true>(zp, zq, B, D, V, inv_t, slice, true, stats, dev_status, st);
     return launch_rowstats_cs<CS, false>(zp, zq, B, D, V, inv_t, slice, aligned, stats, dev_status, st);
