@@ -833,14 +833,17 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
 //    Taylor polynomial in F with coefficients (-1)^k c_k yields exactly the
 //    same Horner values as the polynomial in f (round to nearest is
 //    symmetric);
-//  - rint(t) is (t + 1.5 * 2^23) - 1.5 * 2^23, exact with ties to even for
-//    |t| < 2^22 (guaranteed by clamping y at -80, which changes no term:
-//    every y <= -80 contributes floor(e 2^55) = 0).
+//  - rint(t) is r - 1.5 * 2^23 with r = t + 1.5 * 2^23, exact with ties to
+//    even for |t| < 2^22, and then the bits of r are 0x4B400000 + n.
 // The fixed-point term floor(P 2^n 2^55), P = mp 2^(ep - 150) the
 // polynomial value, is mp 2^s with s = ep + n - 95 <= 32: for s >= 1 it is
 // 2 * (mp * 2^(s - 1)) (one 32 x 32 -> 64-bit multiply-add), for s <= 0 it
 // is mp >> -s; both shifts clamp at 32, so the other case contributes 0 and
-// no branch is needed.
+// no branch is needed.  Far below the maximum (|t| >= 2^22, y = -inf) the
+// bits of r leave 0x4B000000..0x4B400000 and both shift counts exceed 31,
+// so such elements add 0, as the definition's do: no clamp is needed.
+// (Checked on the host against the scalar definition for every negative
+// fp32 value and -inf.)
 __device__ __forceinline__ unsigned long long pack2(float lo, float hi)
 {
     return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
@@ -874,16 +877,19 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
-__device__ __forceinline__ uint32_t shl_clamp(uint32_t x, uint32_t s)
+// 2^s for s < 32, 0 for s >= 32 (s as unsigned: negatives are huge):
+// (1:0) << s, upper word, shift count clamped at 32.
+__device__ __forceinline__ uint32_t pow2_clamp(uint32_t s)
 {
     uint32_t d;
-    asm("shl.b32 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(s));
+    asm("shf.l.clamp.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(0u), "r"(1u), "r"(s));
     return d;
 }
+// x >> s, 0 for s >= 32: (0:x) >> s, lower word, shift count clamped at 32.
 __device__ __forceinline__ uint32_t shr_clamp(uint32_t x, uint32_t s)
 {
     uint32_t d;
-    asm("shr.b32 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(s));
+    asm("shf.r.clamp.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(0u), "r"(s));
     return d;
 }
 __device__ __forceinline__ float max3(float a, float b, float c)
@@ -923,7 +929,7 @@ __device__ __forceinline__ void fix_term(uint32_t pb, uint32_t rb, unsigned long
     // s - 1 = ep + (rb - 0x4B400000) - 96, -s = 0x4B400000 + 95 - ep - rb (mod 2^32)
     const uint32_t s1 = ep + rb - (0x4B400000u + 96u);
     const uint32_t ns = (0x4B400000u + 95u) - ep - rb;
-    big += static_cast<unsigned long long>(mp) * shl_clamp(1u, s1);
+    big += static_cast<unsigned long long>(mp) * pow2_clamp(s1);
     small += shr_clamp(mp, ns);
 }
 
@@ -932,8 +938,7 @@ __device__ __forceinline__ void fix_term(uint32_t pb, uint32_t rb, unsigned long
 __device__ __forceinline__ void pair_terms(unsigned long long z2, const ExpConsts &k, unsigned long long &big,
                                            uint32_t &small)
 {
-    unsigned long long y = mul2(add2(z2, k.neg_m), k.inv_t);
-    y = pack2(fmaxf(lo_of(y), -80.0f), fmaxf(hi_of(y), -80.0f));
+    const unsigned long long y = mul2(add2(z2, k.neg_m), k.inv_t);
     const unsigned long long tn = mul2(y, k.neg_hi);            // -t
     const unsigned long long tl = fma2(y, k.lo, fma2(y, k.hi, tn));
     const unsigned long long r = sub2(k.magic, tn);             // t + 1.5 * 2^23
@@ -944,6 +949,11 @@ __device__ __forceinline__ void pair_terms(unsigned long long z2, const ExpConst
     for (int i = 6; i >= 0; --i) P = fma2(P, F, k.c[i]);
     fix_term(static_cast<uint32_t>(P), static_cast<uint32_t>(r), big, small);
     fix_term(static_cast<uint32_t>(P >> 32), static_cast<uint32_t>(r >> 32), big, small);
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all()
@@ -959,10 +969,13 @@ __device__ __forceinline__ void st_async_peer_v2(uint32_t addr, unsigned long lo
                  : "memory");
 }
 
-constexpr int kStatsChunk = 256 * kThreads;   // elements per partial sum: 256 per thread
+constexpr int kStatsThreads = 256;
+constexpr int kStatsWarps = kStatsThreads / 32;
+constexpr int kStatsMinBlocks = 3;                 // CTAs per SM (shared memory allows 3 slices of 64 KB)
+constexpr int kStatsChunk = 256 * kStatsThreads;   // elements per partial sum: 256 per thread
 
 template <int CS, bool BULK>
-__global__ void __launch_bounds__(kThreads, 3) logits_rowstats_kernel(
+__global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) logits_rowstats_kernel(
     const float *__restrict__ zp, const float *__restrict__ zq, int B, int D, int V, float inv_t, int slice,
     bool vec4, float2 *__restrict__ stats, uint32_t *dev_status)
 {
@@ -971,9 +984,9 @@ __global__ void __launch_bounds__(kThreads, 3) logits_rowstats_kernel(
     __shared__ uint64_t full, bar_max[2], bar_sum[2];
     __shared__ unsigned long long s_xmax[2][CS];   // (bad << 32) | bits of CTA c's max, by row parity
     __shared__ ulonglong2 s_xsum[2][CS];           // CTA c's exact partial sum (lo, hi), owned rows
-    __shared__ float s_wmax[kWarps];
-    __shared__ int s_wbad[kWarps];
-    __shared__ U128 s_wsum[kWarps];
+    __shared__ float s_wmax[kStatsWarps];
+    __shared__ int s_wbad[kStatsWarps];
+    __shared__ U128 s_wsum[kStatsWarps];
     __shared__ int s_abort;
     volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1034,6 +1047,8 @@ __global__ void __launch_bounds__(kThreads, 3) logits_rowstats_kernel(
                 mbar_arrive_expect_tx(&full, static_cast<uint32_t>(len) * 4u);
                 bulk_load(buf, row_src(r), static_cast<uint32_t>(len) * 4u, &full);
                 ++loads;
+                // the next row's slice travels to L2 while this one is worked on
+                if (r + nclusters < R) prefetch_l2(row_src(r + nclusters), static_cast<uint32_t>(len) * 4u);
             }
             if (CS > 1) {
                 mbar_arrive_expect_tx(&bar_max[k & 1], CS * 8u);
@@ -1054,7 +1069,7 @@ __global__ void __launch_bounds__(kThreads, 3) logits_rowstats_kernel(
         // pass 1: the maximum; a NaN anywhere makes the running sum NaN
         float mx = -INFINITY;
         unsigned long long acc2 = 0ull;
-        for (int i = tid * 4; i < len; i += kThreads * 4) {
+        for (int i = tid * 4; i < len; i += kStatsThreads * 4) {
             const float4 v = BULK ? *reinterpret_cast<const float4 *>(src + i) : load4(src, i, len, vec4, -INFINITY);
             mx = max3(mx, max3(v.x, v.y, v.z), v.w);
             acc2 = add2(acc2, add2(pack2(v.x, v.y), pack2(v.z, v.w)));
@@ -1071,7 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 3) logits_rowstats_kernel(
         if (tid < CS) {
             float cm = s_wmax[0];
             int cb = s_wbad[0];
-            for (int w = 1; w < kWarps; ++w) {
+            for (int w = 1; w < kStatsWarps; ++w) {
                 cm = fmaxf(cm, s_wmax[w]);
                 cb |= s_wbad[w];
             }
@@ -1101,7 +1116,7 @@ __global__ void __launch_bounds__(kThreads, 3) logits_rowstats_kernel(
                 const int end = static_cast<int>(imin64(len, static_cast<int64_t>(base) + kStatsChunk));
                 unsigned long long big = 0ull;   // at most 256 terms of at most 2^54
                 uint32_t small = 0u;             // at most 256 terms below 2^24
-                for (int i = base + tid * 4; i < end; i += kThreads * 4) {
+                for (int i = base + tid * 4; i < end; i += kStatsThreads * 4) {
                     const float4 v =
                         BULK ? *reinterpret_cast<const float4 *>(src + i) : load4(src, i, end, vec4, -INFINITY);
                     pair_terms(pack2(v.x, v.y), kc, big, small);
@@ -1115,7 +1130,7 @@ __global__ void __launch_bounds__(kThreads, 3) logits_rowstats_kernel(
         __syncthreads();   // also: every thread is done with this slice
         if (tid == 0) {
             U128 t = s_wsum[0];
-            for (int w = 1; w < kWarps; ++w) add128(t, s_wsum[w]);
+            for (int w = 1; w < kStatsWarps; ++w) add128(t, s_wsum[w]);
             const int slot = (k / CS) & 1;
             if (CS > 1)
                 st_async_peer_v2(peer_smem(&s_xsum[slot][rank], static_cast<uint32_t>(owner)), t.lo, t.hi,
@@ -1272,7 +1287,7 @@ cudaError_t launch_rowstats_cs(const float *zp, const float *zq, int B, int D, i
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kStatsThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
