@@ -29,6 +29,12 @@ Parity status of each function (what pins it, in tests/test_oracle_*.py):
                     the accepted-node set on trees with distinct sibling
                     tokens; emitted tokens equal plain greedy decoding of a
                     toy target model.
+  adasd_stats       scipy's entropy and Jensen-Shannon distance; uniform,
+                    one-hot, identical and disjoint rows in closed form.
+  accept_adasd      reduces to accept_sample when nothing is relaxed and
+                    nothing stops; d_eff from rows of known entropy; the
+                    first emitted token follows the draft distribution where
+                    JS <= tau (chi-square) and the target elsewhere.
   logits_to_probs   exp_f32 within 2 ulp of the exact exponential; the fp32
                     softmax within its rounding bound of the fp64 softmax; its
                     Philox equals the independent implementation of the
@@ -85,11 +91,15 @@ def _load():
             lib.oracle_logits_to_probs.argtypes = [P, P, ctypes.c_float, ctypes.c_uint64, i32, i32, i32,
                                                    P, P, P, P, i32]
             lib.oracle_logits_row_stats.argtypes = [P, P, ctypes.c_float, i32, i32, i32, P, P, i32]
+            lib.oracle_adasd_stats.argtypes = [P, P, i32, i32, i32, P, P, i32]
+            lib.oracle_accept_adasd.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, i32, i32, i32,
+                                                P, P, P, P, P, P, i32]
             lib.oracle_exp_f32.argtypes = [P, P, i64]
             lib.oracle_exp_f32.restype = None
             for f in ("oracle_verify_attention", "oracle_gemm", "oracle_accept_greedy",
                       "oracle_accept_sample", "oracle_max_threads", "oracle_tree_attention",
-                      "oracle_accept_tree_greedy", "oracle_logits_to_probs", "oracle_logits_row_stats"):
+                      "oracle_accept_tree_greedy", "oracle_logits_to_probs", "oracle_logits_row_stats",
+                      "oracle_adasd_stats", "oracle_accept_adasd"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -290,6 +300,47 @@ def accept_sample_logits(zp, zq, draft, temperature, seed, threads=0):
     """Stochastic acceptance from logits: logits_to_probs, then accept_sample."""
     p, q, u_acc, u_res = logits_to_probs(zp, zq, temperature, seed, threads)
     return accept_sample(p, q, draft, u_acc, u_res, threads)
+
+
+def adasd_stats(p, q, threads=0):
+    """Entropy H(q_i) and JS distance JS(p_i, q_i) of every draft position
+    (readings R12, R13): two [B, D] fp64 arrays."""
+    lib = _load()
+    p = _c(p, np.float32)
+    q = _c(q, np.float32)
+    B, T, V = p.shape
+    D = T - 1
+    H = np.empty((B, D), np.float64)
+    JS = np.empty((B, D), np.float64)
+    rc = lib.oracle_adasd_stats(_ptr(p), _ptr(q), B, D, V, _ptr(H), _ptr(JS), int(threads))
+    if rc:
+        raise ValueError(f"oracle_adasd_stats failed: {rc}")
+    return H, JS
+
+
+def accept_adasd(p, q, draft, u_acc, u_res, tau_h, tau_js, threads=0):
+    """AdaSD relaxed acceptance (readings R12-R14): n_accepted, token, d_eff,
+    margin_u, margin_stat, fallback."""
+    lib = _load()
+    p = _c(p, np.float32)
+    q = _c(q, np.float32)
+    B, T, V = p.shape
+    D = T - 1
+    draft = _c(draft if D else np.zeros((B, 1), np.int32), np.int32)
+    u_acc = _c(u_acc if D else np.zeros((B, 1), np.float32), np.float32)
+    u_res = _c(u_res, np.float32)
+    n = np.empty(B, np.int32)
+    t = np.empty(B, np.int32)
+    de = np.empty(B, np.int32)
+    mu = np.empty(B, np.float64)
+    ms = np.empty(B, np.float64)
+    fb = np.empty(B, np.int32)
+    rc = lib.oracle_accept_adasd(_ptr(p), _ptr(q), _ptr(draft), _ptr(u_acc), _ptr(u_res), float(tau_h),
+                                 float(tau_js), B, D, V, _ptr(n), _ptr(t), _ptr(de), _ptr(mu), _ptr(ms),
+                                 _ptr(fb), int(threads))
+    if rc:
+        raise ValueError(f"oracle_accept_adasd failed: {rc}")
+    return n, t, de, mu, ms, fb
 
 
 def exp_f32(y):

@@ -674,3 +674,123 @@ void oracle_exp_f32(const float *y, float *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = exp_f32(y[i]);
 }
+
+/* ------------------------------------------------------------------------
+ * AdaSD relaxed acceptance ("Adaptive speculative decoding" article,
+ * section AdaSD): two thresholds taken from runtime statistics -- the
+ * entropy of the draft distribution decides where the drafter stops, and
+ * the Jensen-Shannon distance between the draft and target distributions
+ * decides whether a draft token is close enough to be accepted even where
+ * the min(1, p/q) rule would reject it (so the method is lossy); both act
+ * on the token distributions of a shared vocabulary.  Readings:
+ *  R12 entropy H(q) = -sum_v q(v) ln q(v) (natural log, 0 ln 0 = 0); the
+ *      drafter stops at the first position whose draft distribution is too
+ *      uncertain: D_eff = min{ i : H(q_i) > tau_H }, else D; drafts from
+ *      D_eff on are not proposed.
+ *  R13 JS distance = sqrt(JSD), JSD(p, q) = (KL(p || m) + KL(q || m)) / 2,
+ *      m = (p + q) / 2, natural log: a value in [0, sqrt(ln 2)].
+ *  R14 draft i < D_eff is accepted iff u_acc * q(x) < p(x) (the exact rule of
+ *      the stochastic acceptance) or JS(p_i, q_i) <= tau_JS.  At the first
+ *      failure j the token is drawn from max(0, p_j - q_j) renormalised (R5's
+ *      fallback to p_j when that is zero); if all D_eff are accepted, from
+ *      p_{D_eff}.  n_accepted = j or D_eff.
+ *  R15 the thresholds are inputs of the call; the per-row statistics H and
+ *      JS are outputs, from which the caller adapts the thresholds.
+ * ---------------------------------------------------------------------- */
+static double xlnx(double x) { return x > 0.0 ? x * log(x) : 0.0; }
+
+static void adasd_row_stats(const float *p, const float *q, int V, double *H, double *JS)
+{
+    double h = 0.0, jsd = 0.0;
+    for (int v = 0; v < V; ++v) {
+        const double pv = (double)p[v], qv = (double)q[v];
+        const double m = 0.5 * (pv + qv);
+        h -= xlnx(qv);
+        /* p ln(p/m) + q ln(q/m), each term 0 where its weight is 0 */
+        if (pv > 0.0) jsd += pv * log(pv / m);
+        if (qv > 0.0) jsd += qv * log(qv / m);
+    }
+    *H = h;
+    *JS = sqrt(fmax(0.0, 0.5 * jsd));
+}
+
+/* H [B][D] and JS [B][D] of every draft position's (p_i, q_i). */
+int oracle_adasd_stats(const float *p, const float *q, int B, int D, int V, double *H, double *JS,
+                       int num_threads)
+{
+    if (B < 0 || D < 0 || V < 1) return -2;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < (int64_t)B * D; ++r) {
+        const int64_t b = r / D, i = r % D;
+        adasd_row_stats(p + (b * (1 + D) + i) * V, q + (b * D + i) * V, V, H + r, JS + r);
+    }
+    return 0;
+}
+
+/* Readings R12-R14 with the statistics above.  Outputs per sequence:
+ * n_accepted, token, d_eff, margin_u (as oracle_accept_sample's margin, over
+ * the uniform-based decisions and the draw), margin_stat (min over the
+ * decisive threshold comparisons of |H - tau_H| and |JS - tau_JS|) and the
+ * R5 fallback flag. */
+int oracle_accept_adasd(const float *p, const float *q, const int32_t *draft, const float *u_acc,
+                        const float *u_res, float tau_h, float tau_js, int B, int D, int V,
+                        int32_t *n_accepted, int32_t *token, int32_t *d_eff, double *margin_u,
+                        double *margin_stat, int32_t *fallback, int num_threads)
+{
+    if (B < 0 || D < 0 || V < 1) return -2;
+    int err = 0;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const float *pb = p + (int64_t)b * (1 + D) * V;
+        const float *qb = q + (int64_t)b * D * V;
+        double mu = INFINITY, ms = INFINITY;
+        int de = D;
+        for (int i = 0; i < D; ++i) {
+            double H, JS;
+            adasd_row_stats(pb + (int64_t)i * V, qb + (int64_t)i * V, V, &H, &JS);
+            if (fabs(H - (double)tau_h) < ms) ms = fabs(H - (double)tau_h);
+            if (H > (double)tau_h) { de = i; break; }
+        }
+        int j = de;
+        for (int i = 0; i < de; ++i) {
+            int x = draft[(int64_t)b * D + i];
+            if (x < 0 || x >= V) {
+#pragma omp atomic write
+                err = -4;
+                x = 0;
+            }
+            const double px = (double)pb[(int64_t)i * V + x], qx = (double)qb[(int64_t)i * V + x];
+            const double u = (double)u_acc[(int64_t)b * D + i];
+            if (qx > 0.0 && fabs(u - px / qx) < mu) mu = fabs(u - px / qx);
+            if (u * qx < px) continue;                 /* the exact rule accepts */
+            double H, JS;
+            adasd_row_stats(pb + (int64_t)i * V, qb + (int64_t)i * V, V, &H, &JS);
+            if (fabs(JS - (double)tau_js) < ms) ms = fabs(JS - (double)tau_js);
+            if (JS <= (double)tau_js) continue;        /* close enough: accepted anyway */
+            j = i;
+            break;
+        }
+        int fb = 0, tok;
+        double dm = INFINITY;
+        if (j < de) {
+            tok = draw_residual(pb + (int64_t)j * V, qb + (int64_t)j * V, V, 1, (double)u_res[b], &dm);
+            if (tok < 0) {
+                fb = 1;
+                tok = draw_residual(pb + (int64_t)j * V, NULL, V, 0, (double)u_res[b], &dm);
+            }
+        } else {
+            tok = draw_residual(pb + (int64_t)de * V, NULL, V, 0, (double)u_res[b], &dm);
+        }
+        if (tok < 0) tok = 0;
+        if (dm < mu) mu = dm;
+        n_accepted[b] = j;
+        token[b] = tok;
+        if (d_eff) d_eff[b] = de;
+        if (margin_u) margin_u[b] = mu;
+        if (margin_stat) margin_stat[b] = ms;
+        if (fallback) fallback[b] = fb;
+    }
+    return err;
+}
