@@ -14,6 +14,8 @@
  *   spec_accept_sample     stochastic min(1, p/q) acceptance with residual
  *                          resampling.
  *   spec_accept_sample_logits   the same from logits, temperature and seed.
+ *   spec_accept_adasd      AdaSD relaxed acceptance (draft-entropy stop,
+ *                          Jensen-Shannon distance threshold).
  *
  * Conventions shared by every entry point:
  *  - Pointers marked "device" are CUDA device pointers owned by the caller;
@@ -301,6 +303,49 @@ spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *
                                  const float *u_acc, const float *u_res, int B, int D, int V,
                                  int32_t *n_accepted, int32_t *token, void *workspace,
                                  size_t workspace_bytes, uint32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * AdaSD relaxed acceptance (lossy).
+ *
+ * From "Adaptive speculative decoding" (section AdaSD): two thresholds act
+ * on the token distributions of the shared vocabulary -- the entropy of the
+ * draft distribution decides where the drafter stops, and the
+ * Jensen-Shannon distance between draft and target distributions decides
+ * whether a draft token is close enough to be accepted even where the
+ * min(1, p/q) rule would reject it.  Per sequence b and position i < D:
+ *     H[b][i]  = -sum_v q ln q                   (natural log, 0 ln 0 = 0)
+ *     JS[b][i] = sqrt((KL(p || m) + KL(q || m)) / 2),  m = (p + q) / 2
+ *     d_eff    = first i with H[b][i] > tau_entropy, else D
+ *     draft i < d_eff accepted iff u_acc * q(x) < p(x) (exact, as in
+ *         spec_accept_sample) or JS[b][i] <= tau_js
+ *     at the first failure j: n_accepted = j and the token is drawn from
+ *     max(0, p[j] - q[j]) renormalised (p[j] if that is zero); if all d_eff
+ *     drafts pass: n_accepted = d_eff and the token is drawn from p[d_eff].
+ * tau_entropy = +inf and tau_js < 0 give exactly spec_accept_sample.  The
+ * thresholds are the caller's (it adapts them from the statistics this call
+ * returns).  H and JS are computed in fp32 with the hardware logarithm
+ * (absolute error about 1e-5 against exact arithmetic at V = 131072), so a
+ * decision can differ from the exact one only for a statistic that close
+ * to its threshold.  Every p_i and q_i row with i < D is read once for the
+ * statistics, then the gathered draft entries and the one row each sequence
+ * draws from.
+ *
+ *   p, q, draft, u_acc, u_res, n_accepted, token   as in spec_accept_sample.
+ *   tau_entropy, tau_js   thresholds (not NaN).
+ *   draft_len    device int32 [B] or NULL: d_eff.
+ *   entropy, js_distance  device fp32 [B][D] or NULL: H and JS of every
+ *                position (all D, also past d_eff).
+ *   workspace  device, spec_accept_adasd_workspace_size(B, D, V) bytes,
+ *              256-byte aligned, scratch only, needs no initialisation.
+ * Supported set: B <= 65535, 0 <= D <= 63, 1 <= V <= 2^26.
+ * ---------------------------------------------------------------------- */
+size_t spec_accept_adasd_workspace_size(int B, int D, int V);
+
+spec_status_t spec_accept_adasd(const float *p, const float *q, const int32_t *draft, const float *u_acc,
+                                const float *u_res, float tau_entropy, float tau_js, int B, int D, int V,
+                                int32_t *n_accepted, int32_t *token, int32_t *draft_len, float *entropy,
+                                float *js_distance, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                                void *stream);
 
 /* ------------------------------------------------------------------------
  * Stochastic acceptance from logits.

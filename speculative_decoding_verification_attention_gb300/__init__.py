@@ -22,6 +22,7 @@ __all__ = [
     "gemm_workspace_size", "gemm_plan", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
     "verify_tree_attention", "tree_attention_workspace_size", "accept_tree_greedy",
     "AdaptiveDraftLength", "accept_sample_logits", "accept_sample_logits_workspace_size",
+    "accept_adasd", "accept_adasd_workspace_size",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -35,6 +36,7 @@ EXPORTED_SYMBOLS = (
     "spec_verify_tree_attention_workspace_size", "spec_verify_tree_attention",
     "spec_accept_tree_greedy", "spec_adaptive_init", "spec_adaptive_update", "spec_adaptive_draft_len",
     "spec_accept_sample_logits_workspace_size", "spec_accept_sample_logits",
+    "spec_accept_adasd_workspace_size", "spec_accept_adasd",
 )
 
 DEV_STATUS_BITS = {
@@ -113,6 +115,10 @@ def library():
             lib.spec_accept_sample_logits.argtypes = [P, P, P, F, ctypes.c_uint64, I, I, I, P, P, P, S,
                                                       P, P]
             lib.spec_accept_sample_logits.restype = I
+            lib.spec_accept_adasd_workspace_size.argtypes = [I, I, I]
+            lib.spec_accept_adasd_workspace_size.restype = S
+            lib.spec_accept_adasd.argtypes = [P, P, P, P, P, F, F, I, I, I, P, P, P, P, P, P, S, P, P]
+            lib.spec_accept_adasd.restype = I
             _lib = lib
     return _lib
 
@@ -387,6 +393,47 @@ def accept_sample_logits(target_logits, draft_logits, draft, temperature, seed, 
         _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
     _check(st, "spec_accept_sample_logits")
     return n_accepted, token
+
+
+def accept_adasd_workspace_size(B, D, V):
+    return int(library().spec_accept_adasd_workspace_size(B, D, V))
+
+
+def accept_adasd(p, q, draft, u_acc, u_res, tau_entropy, tau_js, n_accepted=None, token=None,
+                 draft_len=None, entropy=None, js_distance=None, workspace=None, dev_status=None,
+                 stream=None):
+    """AdaSD relaxed acceptance (spec_accept_adasd): returns n_accepted,
+    token, draft_len (d_eff), entropy [B, D], js_distance [B, D]."""
+    import torch
+    B, D1, V = p.shape
+    D = D1 - 1
+    dev = p.device
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if token is None:
+        token = torch.empty(B, dtype=torch.int32, device=dev)
+    if draft_len is None:
+        draft_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if entropy is None:
+        entropy = torch.empty((B, D), dtype=torch.float32, device=dev)
+    if js_distance is None:
+        js_distance = torch.empty((B, D), dtype=torch.float32, device=dev)
+    need = accept_adasd_workspace_size(B, D, V)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    st = library().spec_accept_adasd(
+        _dev(p, "p", torch.float32), _dev(q, "q", torch.float32, allow_none=True),
+        _dev(draft, "draft", torch.int32, allow_none=True),
+        _dev(u_acc, "u_acc", torch.float32, allow_none=True), _dev(u_res, "u_res", torch.float32),
+        float(tau_entropy), float(tau_js), B, D, V, _dev(n_accepted, "n_accepted", torch.int32),
+        _dev(token, "token", torch.int32), _dev(draft_len, "draft_len", torch.int32),
+        _dev(entropy, "entropy", torch.float32) if D else None,
+        _dev(js_distance, "js_distance", torch.float32) if D else None,
+        _dev(workspace, "workspace", allow_none=True),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
+    _check(st, "spec_accept_adasd")
+    return n_accepted, token, draft_len, entropy, js_distance
 
 
 # ------------------------------------------------------------ adaptive draft length

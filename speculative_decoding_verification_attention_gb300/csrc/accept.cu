@@ -491,7 +491,11 @@ __device__ __forceinline__ float pad_value()
 }
 
 // Scratch in the caller's workspace (see spec_accept_sample):
-//   js    int32  [B]            first rejected draft (or D) of each sequence
+//   js    int32  [B]            the row j the token is drawn from, which is
+//                               also n_accepted; kBonusFlag set when it is a
+//                               bonus draw from p[j] (all proposed drafts
+//                               accepted), clear for a residual draw from
+//                               max(0, p[j] - q[j]) after a rejection
 //   gtot  uint64 [B][ngroups]   exact residual / bonus mass of every group
 //                               of 4 steps (512 elements)
 //   steps uint64 [B][nsteps]    ... and of every 128-element step
@@ -503,6 +507,18 @@ struct SampleScratch {
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+constexpr int32_t kBonusFlag = 1 << 30;
+
+struct DrawRow {
+    int j;          // row of the draw (= n_accepted)
+    int residual;   // 1: max(0, p[j] - q[j]); 0: p[j]
+};
+
+__device__ __forceinline__ DrawRow decode_draw(int32_t v)
+{
+    return {v & ~kBonusFlag, (v & kBonusFlag) ? 0 : 1};
+}
 
 constexpr int kChunk = 8192;                   // elements of one work item
 constexpr int kConsumers = 16;                 // consumer warps of the streaming kernel
@@ -558,7 +574,7 @@ __global__ void __launch_bounds__(kThreads) accept_prep_kernel(SampleIn in, cons
             break;
         }
     }
-    if (lane == 0) sc.js[b] = j;
+    if (lane == 0) sc.js[b] = j == D ? (j | kBonusFlag) : j;
 }
 
 // Exact masses of the kGroupSteps steps of 128 elements starting at element
@@ -634,20 +650,22 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
                 const int slot = k % kRing;
                 if (k >= kRing && !mbar_wait(&empty[slot], ((k / kRing) - 1) & 1, abort, dev_status)) break;
                 const int b = item / nchunks, chunk = item % nchunks;
-                const int j = __ldcg(sc.js + b);
-                s_j[slot] = j;
+                const int32_t code = __ldcg(sc.js + b);
+                s_j[slot] = code;
+                const DrawRow dr = decode_draw(code);
+                const int j = dr.j;
                 if (LOGITS) {
                     const SoftmaxRow rp = row_params<true>(in, b, D, j);
-                    const SoftmaxRow rq = j < D ? row_params<true>(in, b, D, D + 1 + j) : rp;
+                    const SoftmaxRow rq = dr.residual ? row_params<true>(in, b, D, D + 1 + j) : rp;
                     s_rows[slot] = make_float4(rp.m, rp.zf, rq.m, rq.zf);
                 }
                 if (bulk) {
                     const int64_t e0 = static_cast<int64_t>(chunk) * kChunk;
                     const uint32_t bytes = static_cast<uint32_t>(imin64(kChunk, V - e0)) * 4;  // % 16 == 0
                     float *dst = ring + slot * (2 * kChunk);
-                    mbar_arrive_expect_tx(&full[slot], j < D ? 2 * bytes : bytes);
+                    mbar_arrive_expect_tx(&full[slot], dr.residual ? 2 * bytes : bytes);
                     bulk_load(dst, p + (static_cast<int64_t>(b) * (D + 1) + j) * V + e0, bytes, &full[slot]);
-                    if (j < D)
+                    if (dr.residual)
                         bulk_load(dst + kChunk, q + (static_cast<int64_t>(b) * D + j) * V + e0, bytes,
                                   &full[slot]);
                 } else {
@@ -664,8 +682,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
         const int slot = k % kRing;
         if (!mbar_wait_warp(&full[slot], (k / kRing) & 1, abort, dev_status)) break;
         const int b = item / nchunks, chunk = item % nchunks;
-        const int j = s_j[slot];
-        const int residual = j < D;
+        const DrawRow dr = decode_draw(s_j[slot]);
+        const int j = dr.j;
+        const int residual = dr.residual;
         SoftmaxRow rp{0.0f, 1.0f, 1.0f}, rq{0.0f, 1.0f, 1.0f};
         if (LOGITS) {
             const float4 r = s_rows[slot];
@@ -711,8 +730,9 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * kWarps + warp;
     if (b >= B) return;
-    const int j = sc.js[b];
-    int residual = j < D;
+    const DrawRow dr = decode_draw(sc.js[b]);
+    const int j = dr.j;
+    int residual = dr.residual;
     const float *prow = p + (static_cast<int64_t>(b) * (D + 1) + j) * V;
     const float *qrow = residual ? q + (static_cast<int64_t>(b) * D + j) * V : nullptr;
     unsigned long long *steps = sc.steps + static_cast<int64_t>(b) * sc.nsteps;
@@ -805,6 +825,144 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
     if (lane == 0) {
         n_accepted[b] = j;
         token[b] = tok;
+    }
+}
+
+// ------------------------------------------------------------------ AdaSD
+// AdaSD relaxed acceptance ("Adaptive speculative decoding", section AdaSD):
+// the entropy of the draft distribution decides where the drafter stops and
+// the Jensen-Shannon distance between draft and target distributions lets a
+// draft token be accepted where min(1, p/q) would reject it.
+//   H(q_i)   = -sum_v q ln q                       (natural log, 0 ln 0 = 0)
+//   JSD_i    = (sum_v p ln p + q ln q - s ln s) / 2 + ln 2 * sum_v s / 2,
+//              s = p + q  (= (KL(p||m) + KL(q||m)) / 2 with m = s / 2)
+//   JS_i     = sqrt(max(0, JSD_i))
+//   d_eff    = first i with H(q_i) > tau_H, else D
+//   draft i < d_eff accepted iff u_acc q(x) < p(x) (exact) or JS_i <= tau_JS;
+//   the token is drawn as in the stochastic acceptance from row j (residual
+//   after a rejection at j, else the bonus row d_eff).
+// Stage A streams the D (p_i, q_i) row pairs of every sequence once, one
+// 8192-element chunk per CTA, and writes each chunk's two partial sums;
+// stage B (a warp per sequence) adds the partials in a fixed order, takes
+// the decisions and hands the draw row to the streaming and finalising
+// kernels of the stochastic acceptance.  The sums are fp32 (the logarithms
+// from the hardware approximation), so H and JS are close to, not equal
+// to, the exact values; decisions can differ from exact ones only for a
+// statistic within that error of its threshold.
+constexpr int kAdaChunk = 8192;
+constexpr int kAdaVec = kAdaChunk / (4 * kThreads);   // float4 loads per thread and row: 8
+
+__device__ __forceinline__ float xlogx(float x) { return x > 0.0f ? x * __logf(x) : 0.0f; }
+
+__global__ void __launch_bounds__(kThreads) adasd_stats_kernel(const float *__restrict__ p,
+                                                                const float *__restrict__ q, int D, int V,
+                                                                int nchunks, bool vec4, float2 *__restrict__ parts)
+{
+    __shared__ float2 s_w[kWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int item = blockIdx.x;
+    const int r = item / nchunks, c = item % nchunks;
+    const int b = r / D, i = r % D;
+    const int64_t e0 = static_cast<int64_t>(c) * kAdaChunk;
+    const int n = static_cast<int>(imin64(kAdaChunk, V - e0));
+    const float *pr = p + (static_cast<int64_t>(b) * (D + 1) + i) * V + e0;
+    const float *qr = q + (static_cast<int64_t>(b) * D + i) * V + e0;
+    float4 xp[kAdaVec], xq[kAdaVec];
+#pragma unroll
+    for (int u = 0; u < kAdaVec; ++u) {   // every load of the thread in flight at once
+        const int e = (u * kThreads + threadIdx.x) * 4;
+        xp[u] = e < n ? load4(pr, e, n, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        xq[u] = e < n ? load4(qr, e, n, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_launch_dependents();
+    float h = 0.0f, js = 0.0f, sum = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kAdaVec; ++u) {
+        const float pv[4] = {xp[u].x, xp[u].y, xp[u].z, xp[u].w};
+        const float qv[4] = {xq[u].x, xq[u].y, xq[u].z, xq[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float qlq = xlogx(qv[k]);
+            const float s = pv[k] + qv[k];
+            h += qlq;
+            js += xlogx(pv[k]) + qlq - xlogx(s);
+            sum += s;
+        }
+    }
+    js += 0.69314718f * sum;   // + ln 2 * sum of s
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        h += __shfl_xor_sync(0xffffffffu, h, o);
+        js += __shfl_xor_sync(0xffffffffu, js, o);
+    }
+    if (lane == 0) s_w[warp] = make_float2(h, js);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float2 t = s_w[0];
+        for (int w = 1; w < kWarps; ++w) {
+            t.x += s_w[w].x;
+            t.y += s_w[w].y;
+        }
+        parts[static_cast<int64_t>(r) * nchunks + c] = t;
+    }
+}
+
+// Stage B: one warp per sequence.
+__global__ void __launch_bounds__(kThreads) adasd_prep_kernel(
+    const float *__restrict__ p, const float *__restrict__ q, const int32_t *__restrict__ draft,
+    const float *__restrict__ u_acc, const float2 *__restrict__ parts, int nchunks, float tau_h, float tau_js,
+    int B, int D, int V, float *__restrict__ entropy, float *__restrict__ js_dist, int32_t *__restrict__ d_eff,
+    SampleScratch sc, uint32_t *dev_status)
+{
+    pdl_launch_dependents();
+    pdl_wait();   // the partial sums come from the previous kernel
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x * kWarps + warp;
+    if (b >= B) return;
+    int de = D;          // first position whose draft entropy exceeds tau_H
+    int j = -1;          // first position that fails both tests
+    for (int i = 0; i < D; ++i) {
+        const int64_t r = static_cast<int64_t>(b) * D + i;
+        float h = 0.0f, s = 0.0f;
+        for (int c = lane; c < nchunks; c += 32) {
+            const float2 v = __ldcg(parts + r * nchunks + c);
+            h += v.x;
+            s += v.y;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {   // the same order on every lane
+            h += __shfl_xor_sync(0xffffffffu, h, o);
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+        }
+        const float H = -h, JS = sqrtf(fmaxf(0.5f * s, 0.0f));
+        if (lane == 0) {
+            if (entropy) entropy[r] = H;
+            if (js_dist) js_dist[r] = JS;
+        }
+        if (de < D) continue;   // past the stop: statistics only
+        if (H > tau_h) {
+            de = i;
+            continue;
+        }
+        if (j >= 0) continue;   // already decided
+        const int x = draft[r];
+        bool ok;
+        if (x < 0 || x >= V) {
+            if (lane == 0) report(dev_status, SPEC_DEV_ERR_TOKEN_ID);
+            ok = false;
+        } else {
+            const double pv = p[(static_cast<int64_t>(b) * (D + 1) + i) * V + x];
+            const double qv = q[r * V + x];
+            const float uf = u_acc[r];
+            if (!(uf >= 0.0f && uf < 1.0f) && lane == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
+            // the product of two fp32 values is exact in fp64
+            ok = static_cast<double>(uf) * qv < pv || JS <= tau_js;
+        }
+        if (!ok) j = i;
+    }
+    if (lane == 0) {
+        sc.js[b] = j >= 0 ? j : (de | kBonusFlag);
+        if (d_eff) d_eff[b] = de;
     }
 }
 
@@ -1229,12 +1387,23 @@ cudaError_t launch_accept_tree_greedy(const float *p, const int32_t *tokens, con
 
 namespace {
 
+// The AdaSD decision stage's inputs and outputs.
+struct AdaArgs {
+    const float2 *parts;
+    int nchunks;
+    float tau_h, tau_js;
+    float *entropy, *js_dist;
+    int32_t *d_eff;
+};
+
 // Stages 1-3 of the stochastic acceptance (prep, stream, finalize) on the
 // scratch that starts at `workspace`.  LOGITS: the first stage waits for the
 // row statistics of the kernel before it (programmatic dependent launch).
+// ada: the AdaSD decision stage replaces the first stage.
 template <bool LOGITS>
 cudaError_t launch_sample_stages(const SampleIn &in, const int32_t *draft, int B, int D, int V, int32_t *n_acc,
-                                 int32_t *token, void *workspace, uint32_t *dev_status, cudaStream_t st)
+                                 int32_t *token, void *workspace, uint32_t *dev_status, cudaStream_t st,
+                                 const AdaArgs *ada = nullptr)
 {
     // bulk copies need 16-byte aligned rows: V % 4 == 0 and aligned bases
     const bool bulk = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(in.p) % 16 == 0) &&
@@ -1258,7 +1427,12 @@ cudaError_t launch_sample_stages(const SampleIn &in, const int32_t *draft, int B
     if (e != cudaSuccess) return e;
 
     const unsigned sgrid = static_cast<unsigned>((B + kWarps - 1) / kWarps);
-    if (LOGITS) {
+    if (ada) {
+        // AdaSD: the decisions come from the row statistics of the kernel before
+        e = launch_pdl(adasd_prep_kernel, dim3(sgrid), dim3(kThreads), 0u, st, in.p, in.q, draft, in.u_acc,
+                       ada->parts, ada->nchunks, ada->tau_h, ada->tau_js, B, D, V, ada->entropy, ada->js_dist,
+                       ada->d_eff, sc, dev_status);
+    } else if (LOGITS) {
         e = launch_pdl(accept_prep_kernel<LOGITS>, dim3(sgrid), dim3(kThreads), 0u, st, in, draft, B, D, V, sc,
                        dev_status);
     } else {
@@ -1344,6 +1518,53 @@ cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *
 {
     const SampleIn in{p, q, u_acc, u_res, nullptr, 1.0f, 0ull};
     return launch_sample_stages<false>(in, draft, B, D, V, n_acc, token, workspace, dev_status, st);
+}
+
+namespace {
+
+size_t adasd_parts_bytes(int B, int D, int V)
+{
+    const size_t nchunks = (static_cast<size_t>(V) + kAdaChunk - 1) / kAdaChunk;
+    return align256(sizeof(float2) * static_cast<size_t>(B) * D * nchunks);
+}
+
+size_t adasd_stats_bytes(int B, int D) { return align256(sizeof(float) * static_cast<size_t>(B) * D); }
+
+}  // namespace
+
+size_t accept_adasd_workspace_bytes(int B, int D, int V)
+{
+    return adasd_parts_bytes(B, D, V) + 2 * adasd_stats_bytes(B, D) + accept_sample_workspace_bytes(B, V);
+}
+
+cudaError_t launch_accept_adasd(const float *p, const float *q, const int32_t *draft, const float *u_acc,
+                                const float *u_res, float tau_h, float tau_js, int B, int D, int V, int32_t *n_acc,
+                                int32_t *token, int32_t *d_eff, float *entropy, float *js_dist, void *workspace,
+                                uint32_t *dev_status, cudaStream_t st)
+{
+    char *w = static_cast<char *>(workspace);
+    AdaArgs ada;
+    ada.parts = reinterpret_cast<const float2 *>(w);
+    ada.nchunks = (V + kAdaChunk - 1) / kAdaChunk;
+    w += adasd_parts_bytes(B, D, V);
+    ada.entropy = entropy ? entropy : reinterpret_cast<float *>(w);
+    w += adasd_stats_bytes(B, D);
+    ada.js_dist = js_dist ? js_dist : reinterpret_cast<float *>(w);
+    w += adasd_stats_bytes(B, D);
+    ada.tau_h = tau_h;
+    ada.tau_js = tau_js;
+    ada.d_eff = d_eff;
+    if (D > 0) {
+        const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
+                          (reinterpret_cast<uintptr_t>(q) % 16 == 0);
+        const long long items = static_cast<long long>(B) * D * ada.nchunks;
+        adasd_stats_kernel<<<static_cast<unsigned>(items), kThreads, 0, st>>>(
+            p, q, D, V, ada.nchunks, vec4, const_cast<float2 *>(ada.parts));
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const SampleIn in{p, q, u_acc, u_res, nullptr, 1.0f, 0ull};
+    return launch_sample_stages<false>(in, draft, B, D, V, n_acc, token, w, dev_status, st, &ada);
 }
 
 size_t accept_sample_logits_workspace_bytes(int B, int D, int V)

@@ -100,6 +100,36 @@ spec_status_t spec_accept_sample(const float *p, const float *q, const int32_t *
                                           workspace, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+size_t spec_accept_adasd_workspace_size(int B, int D, int V)
+{
+    if (B < 0 || D < 0 || D > kMaxDraft || V < 1 || V > (1 << 26)) return 0;
+    return accept_adasd_workspace_bytes(B, D, V);
+}
+
+spec_status_t spec_accept_adasd(const float *p, const float *q, const int32_t *draft, const float *u_acc,
+                                const float *u_res, float tau_entropy, float tau_js, int B, int D, int V,
+                                int32_t *n_accepted, int32_t *token, int32_t *draft_len, float *entropy,
+                                float *js_distance, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                                void *stream)
+{
+    if (B < 0 || D < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+    if (tau_entropy != tau_entropy || tau_js != tau_js) return SPEC_ERR_INVALID_ARG;   // NaN thresholds
+    if (D > kMaxDraft || V > (1 << 26)) return SPEC_ERR_UNSUPPORTED;
+    if (B == 0) return SPEC_OK;
+    if (!p || !u_res || !n_accepted || !token) return SPEC_ERR_INVALID_ARG;
+    if (D > 0 && (!q || !draft || !u_acc)) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(p, 4) || (q && !aligned(q, 4)) || !aligned(n_accepted, 4) || !aligned(token, 4) ||
+        (draft_len && !aligned(draft_len, 4)) || (entropy && !aligned(entropy, 4)) ||
+        (js_distance && !aligned(js_distance, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if (B > 65535) return SPEC_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < accept_adasd_workspace_bytes(B, D, V) || !aligned(workspace, 256))
+        return SPEC_ERR_WORKSPACE;
+    return from_cuda(launch_accept_adasd(p, D > 0 ? q : nullptr, draft, u_acc, u_res, tau_entropy, tau_js, B, D, V,
+                                         n_accepted, token, draft_len, entropy, js_distance, workspace, dev_status,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 size_t spec_accept_sample_logits_workspace_size(int B, int D, int V)
 {
     if (B < 0 || D < 0 || D > kMaxDraft || V < 1 || V > (1 << 26)) return 0;

@@ -29,4 +29,11 @@ cudaError_t launch_accept_sample_logits(const float *zp, const float *zq, const 
                                         unsigned long long seed, int B, int D, int V, int32_t *n_acc,
                                         int32_t *token, void *workspace, uint32_t *dev_status, cudaStream_t st);
 
+size_t accept_adasd_workspace_bytes(int B, int D, int V);
+
+cudaError_t launch_accept_adasd(const float *p, const float *q, const int32_t *draft, const float *u_acc,
+                                const float *u_res, float tau_h, float tau_js, int B, int D, int V, int32_t *n_acc,
+                                int32_t *token, int32_t *d_eff, float *entropy, float *js_dist, void *workspace,
+                                uint32_t *dev_status, cudaStream_t st);
+
 }  // namespace spec

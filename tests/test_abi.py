@@ -132,3 +132,24 @@ def test_logits_acceptance_rejects_bad_arguments(lib):
     assert f(*args(wb=need - 1)) == WORKSPACE
     assert f(*args(zq=None, dr=None, D=0, B=0)) == 0   # empty batch: no-op
     assert lib.spec_accept_sample_logits_workspace_size(2, 64, 10) == 0
+
+
+def test_adasd_rejects_bad_arguments(lib):
+    f = lib.spec_accept_adasd
+    W = 1 << 30
+    args = lambda th=1.0, tj=0.2, p=FAKE, q=FAKE, dr=FAKE, ua=FAKE, B=2, D=3, V=10, ws=FAKE, wb=W: (
+        p, q, dr, ua, FAKE, th, tj, B, D, V, FAKE, FAKE, None, None, None, ws, wb, None, None)
+    assert f(*args(th=float("nan"))) == INVALID
+    assert f(*args(tj=float("nan"))) == INVALID
+    assert f(*args(p=None)) == INVALID
+    assert f(*args(q=None)) == INVALID
+    assert f(*args(dr=None)) == INVALID
+    assert f(*args(ua=None)) == INVALID
+    assert f(*args(p=P(0x7F0000001002))) == INVALID
+    assert f(*args(D=64)) == UNSUPPORTED
+    assert f(*args(ws=None)) == WORKSPACE
+    need = lib.spec_accept_adasd_workspace_size(2, 3, 10)
+    assert need >= lib.spec_accept_sample_workspace_size(2, 10) + 2 * 3 * 8
+    assert f(*args(wb=need - 1)) == WORKSPACE
+    assert f(*args(q=None, dr=None, ua=None, D=0, B=0)) == 0   # empty batch: no-op
+    assert f(*args(th=float("inf"), tj=float("-inf"), B=0)) == 0

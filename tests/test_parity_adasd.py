@@ -1,0 +1,140 @@
+"""GPU parity of spec_accept_adasd against the oracle.
+
+The statistics are fp32 sums with the hardware logarithm, compared with the
+oracle's fp64 values: |H - H_ref| <= 1e-5 (1 + H_ref) and
+|JS^2 - JS_ref^2| <= 2e-6 + 1e-5 JS_ref^2 (JS itself loses accuracy near 0
+through the square root).  Decisions (d_eff, n_accepted, token) are compared
+element by element; a difference is allowed only for a sequence whose oracle
+margin is below the bar -- a uniform within 1e-6 of its decision boundary,
+or a statistic within 5e-4 of its threshold -- and such differences must
+stay rare.
+"""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+MARGIN_U = 1e-6
+MARGIN_STAT = 5e-4
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from speculative_decoding_verification_attention_gb300 import _build
+    _build.build()
+    import speculative_decoding_verification_attention_gb300 as m
+    m.library()
+    return m
+
+
+def to_dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run(sv, inp, tau_h, tau_js, dev_status=None):
+    import torch
+    D = inp["p"].shape[1] - 1
+    out = sv.accept_adasd(to_dev(inp["p"]), to_dev(inp["q"]) if D else None, to_dev(inp["draft"]) if D else None,
+                          to_dev(inp["u_acc"]) if D else None, to_dev(inp["u_res"]), tau_h, tau_js,
+                          dev_status=dev_status)
+    torch.cuda.synchronize()
+    return [o.cpu().numpy() for o in out]
+
+
+def check(sv, oracle_lib, inp, tau_h, tau_js, max_close=0.02):
+    n, t, de, H, JS = run(sv, inp, tau_h, tau_js)
+    p, q = inp["p"], inp["q"]
+    D = p.shape[1] - 1
+    if D:
+        H_ref, JS_ref = oracle_lib.adasd_stats(p, q)
+        assert (np.abs(H - H_ref) <= 1e-5 * (1 + H_ref)).all(), np.abs(H - H_ref).max()
+        jsd, jsd_ref = JS.astype(np.float64) ** 2, JS_ref ** 2
+        assert (np.abs(jsd - jsd_ref) <= 2e-6 + 1e-5 * jsd_ref).all(), np.abs(jsd - jsd_ref).max()
+    n_ref, t_ref, de_ref, mu, ms, _ = oracle_lib.accept_adasd(p, q, inp["draft"], inp["u_acc"], inp["u_res"],
+                                                             tau_h, tau_js)
+    close = (mu < MARGIN_U) | (ms < MARGIN_STAT)
+    bad = (n != n_ref) | (t != t_ref) | (de != de_ref)
+    assert not (bad & ~close).any(), np.nonzero(bad & ~close)
+    assert bad.sum() <= max(1, int(max_close * len(n)))
+    assert (n <= de).all() and (de <= D).all()
+    return n, de
+
+
+@pytest.mark.parametrize("V", [1000, 4099, 32768, 131072])
+@pytest.mark.parametrize("D", [0, 1, 7])
+def test_shapes_and_thresholds(sv, oracle_lib, V, D):
+    inp = synth.accept_inputs(V + D, 16, D, V, target_std=2.5, draft_noise=1.0, mode="sample")
+    if D:
+        H_ref, JS_ref = oracle_lib.adasd_stats(inp["p"], inp["q"])
+        tau_h = float(np.quantile(H_ref, 0.8)) + 1e-3
+        tau_js = float(np.quantile(JS_ref, 0.5)) + 1e-3
+    else:
+        tau_h, tau_js = 1.0, 0.1
+    check(sv, oracle_lib, inp, tau_h, tau_js)
+
+
+def test_no_stop_no_relaxation_equals_the_stochastic_acceptance(sv, oracle_lib):
+    import torch
+    inp = synth.accept_inputs(5, 64, 5, 20000, target_std=2.0, draft_noise=0.8, mode="sample")
+    n, t, de, _, _ = run(sv, inp, float("inf"), -1.0)
+    ns, ts = sv.accept_sample(to_dev(inp["p"]), to_dev(inp["q"]), to_dev(inp["draft"]), to_dev(inp["u_acc"]),
+                              to_dev(inp["u_res"]))
+    torch.cuda.synchronize()
+    assert np.array_equal(n, ns.cpu().numpy()) and np.array_equal(t, ts.cpu().numpy())
+    assert (de == 5).all()
+    n_ref, t_ref, _, _ = oracle_lib.accept_sample(inp["p"], inp["q"], inp["draft"], inp["u_acc"], inp["u_res"])
+    assert np.array_equal(n, n_ref) and np.array_equal(t, t_ref)
+
+
+def test_entropy_stop_positions(sv, oracle_lib):
+    """Draft rows uniform over k tokens (entropy ln k): d_eff is the first
+    position with ln k > tau_H, and all proposed drafts are accepted."""
+    V, D = 4096, 5
+    ks = [[2, 4, 8, 100, 3], [50, 2, 2, 2, 2], [2, 2, 2, 2, 2], [1, 1, 1, 1, 11]]
+    B = len(ks)
+    p = np.full((B, D + 1, V), 1.0 / V, np.float32)
+    q = np.zeros((B, D, V), np.float32)
+    for b in range(B):
+        for i in range(D):
+            q[b, i, :ks[b][i]] = 1.0 / ks[b][i]
+    inp = dict(p=p, q=q, draft=np.zeros((B, D), np.int32), u_acc=np.zeros((B, D), np.float32),
+               u_res=np.full(B, 0.5, np.float32))
+    n, t, de, H, _ = run(sv, inp, float(np.log(10.0)), -1.0)
+    assert list(de) == [3, 0, 5, 4]
+    assert list(n) == [3, 0, 5, 4]
+    assert np.allclose(H, np.log(np.array(ks, np.float64)), atol=1e-5)
+    check(sv, oracle_lib, inp, float(np.log(10.0)), -1.0)
+
+
+def test_full_relaxation_accepts_every_proposed_draft(sv, oracle_lib):
+    inp = synth.accept_inputs(7, 32, 6, 8192, draft_noise=3.0, mode="sample")
+    n, _, de, _, _ = run(sv, inp, float("inf"), 1.0)
+    assert (n == 6).all() and (de == 6).all()
+    check(sv, oracle_lib, inp, float("inf"), 1.0)
+
+
+def test_invalid_draft_is_flagged(sv):
+    import torch
+    inp = synth.accept_inputs(8, 4, 3, 1000, mode="sample")
+    inp["draft"] = inp["draft"].copy()
+    inp["draft"][2, 0] = 5000
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n, _, _, _, _ = run(sv, inp, float("inf"), -1.0, dev_status=st)
+    assert int(st.item()) & sv.DEV_STATUS_BITS["TOKEN_ID"]
+    assert n[2] == 0
+
+
+def test_batched_full_size(sv, oracle_lib):
+    """B = 256, D = 7, V = 131072, target logits N(0, 3^2); tau_H at the 90th
+    percentile of the draft entropies and tau_JS at the median distance."""
+    inp = synth.accept_inputs(90, 256, 7, 131072, target_std=3.0, draft_noise=1.2, mode="sample")
+    H_ref, JS_ref = oracle_lib.adasd_stats(inp["p"], inp["q"])
+    tau_h = float(np.quantile(H_ref, 0.9))
+    tau_js = float(np.quantile(JS_ref, 0.5))
+    n, de = check(sv, oracle_lib, inp, tau_h, tau_js)
+    assert (de < 7).any() and (n > 0).any()
