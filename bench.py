@@ -728,6 +728,52 @@ def case_lines(args):
                               "frac_hbm": by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]})
             del p, q
             torch.cuda.empty_cache()
+    if args.workload in ("adasd", "all"):
+        # AdaSD relaxed acceptance: B=256, D=7, V=131072, target logits N(0, 3^2),
+        # draft logits the target's plus N(0, sigma^2) (alpha = 0.6); tau_H at the
+        # 90th percentile of the draft entropies, tau_JS at the median distance
+        B, D, V = 256, 7, 131072
+        sigma, _ = synth.tune_sigma_for_alpha(0.6, V, rows=8, target_std=3.0)
+        g = torch.Generator(device=dev)
+        g.manual_seed(61)
+        t = torch.randn((B, D + 1, V), generator=g, device=dev) * 3.0
+        p = torch.softmax(t.double(), -1).float()
+        q = torch.softmax((t[:, :D] + torch.randn((B, D, V), generator=g, device=dev) * sigma).double(), -1).float()
+        del t
+        qh = q.cpu().numpy()
+        u_acc, u_res = synth.acceptance_uniforms(8, B, D)
+        ud = synth.philox_uniform(8, np.arange(B, dtype=np.uint64)[:, None],
+                                  np.arange(D, dtype=np.uint64)[None, :], synth.STREAM_DRAFT)
+        ds = torch.from_numpy(synth.draw_from_rows(qh, ud)).to(dev)
+        del qh
+        ua, ur = torch.from_numpy(u_acc).to(dev), torch.from_numpy(u_res).to(dev)
+        na, tk = torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev)
+        dl = torch.empty(B, dtype=torch.int32, device=dev)
+        H = torch.empty((B, D), device=dev)
+        JS = torch.empty((B, D), device=dev)
+        wsd = torch.empty(sv.accept_adasd_workspace_size(B, D, V), dtype=torch.uint8, device=dev)
+        sv.accept_adasd(p, q, ds, ua, ur, float("inf"), -1.0, na, tk, dl, H, JS, workspace=wsd)
+        torch.cuda.synchronize()
+        tau_h = float(torch.quantile(H.flatten(), 0.9))
+        tau_js = float(torch.quantile(JS.flatten(), 0.5))
+        run = lambda: sv.accept_adasd(p, q, ds, ua, ur, tau_h, tau_js, na, tk, dl, H, JS, workspace=wsd)
+        ms_a = time_launches(run, args.warmup, args.steps, flush)
+        n_a, d_a = na.cpu().numpy(), dl.cpu().numpy()
+        _, sb = accept_bytes(n_a, np.where(n_a < d_a, 0, D), B, D, V)
+        by = B * D * 2 * V * 4 + sb
+        # the lossless rule on the same inputs, for the accepted-length gain
+        wsa = torch.empty(sv.accept_sample_workspace_size(B, V), dtype=torch.uint8, device=dev)
+        ms_s = time_launches(lambda: sv.accept_sample(p, q, ds, ua, ur, na, tk, workspace=wsa),
+                             args.warmup, args.steps, flush)
+        n_s = na.cpu().numpy()
+        lines.append({"case": f"accept AdaSD B{B} D{D} V{V} alpha0.6 tauH=p90 tauJS=p50", "kernel": "accept_adasd",
+                      "ms": ms_a, "mean_AL": float((n_a + 1).mean()), "mean_d_eff": float(d_a.mean()),
+                      "mean_AL_lossless": float((n_s + 1).mean()), "ms_lossless": ms_s,
+                      "accepted_tokens_per_s": float((n_a + 1).sum()) / (ms_a * 1e-3),
+                      "algorithmic_bytes": by, "GB_per_s": by / (ms_a * 1e-3) / 1e9,
+                      "frac_hbm": by / (ms_a * 1e-3) / 1e9 / pk["hbm_gbs"]})
+        del p, q
+        torch.cuda.empty_cache()
     if args.workload in ("logits", "all"):
         # acceptance from logits: B=256, D=7, V=131072, target logits N(0, 3^2),
         # draft logits the target's plus N(0, sigma^2) with sigma tuned to alpha = 0.6
@@ -787,7 +833,7 @@ def main():
                     help="reference arm: seconds of oracle attention work sampled per step")
     ap.add_argument("--workload", default="step",
                     choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small", "tree",
-                             "adaptive", "logits",
+                             "adaptive", "logits", "adasd",
                              "accept-one"],
                     help="step: the headline line; others print one secondary JSON line per case")
     args = ap.parse_args()
