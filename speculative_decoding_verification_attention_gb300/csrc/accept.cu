@@ -134,8 +134,10 @@ __device__ __forceinline__ void st_async_peer(uint32_t addr, unsigned long long 
 
 constexpr int kGUnroll = 8;    // greedy: 128-element steps whose loads are in flight together
 
-// Greedy acceptance: one thread-block cluster of CS CTAs per sequence, CTA
-// `rank` owning a contiguous slice of the vocabulary.  Row by row, each CTA
+// Greedy acceptance with register loads (rows that are not 16-byte aligned;
+// aligned rows take accept_greedy_bulk_kernel below): one thread-block
+// cluster of CS CTAs per sequence, CTA `rank` owning a contiguous slice of
+// the vocabulary.  Row by row, each CTA
 // reduces its slice to an argmax (all loads of a lane issued at once) and
 // sends the result to every CTA of the cluster with an asynchronous
 // distributed-shared-memory store that completes on the receiver's
@@ -266,6 +268,205 @@ __global__ void __launch_bounds__(kThreads, 4) accept_greedy_kernel(
         }
         __syncthreads();   // s_warp is rewritten by the next row
     }
+    // keep this CTA's shared memory alive until every peer is done with it
+    if constexpr (CS > 1) cg::this_cluster().sync();
+}
+
+// Greedy acceptance with the CTA's vocabulary slice staged in shared memory
+// by bulk copies (rows whose elements are 16-byte aligned).  The same walk
+// as accept_greedy_kernel, but each row's slice arrives in chunks of kGChunk
+// elements, kGSlots of them in flight at once, issued by one thread: no
+// loads held in registers, and the arithmetic on a chunk starts as soon as
+// it lands; a slice longer than the ring (64 KB at V = 131072 against a
+// 48 KB ring, which keeps 4 CTAs on an SM) streams through it.  Thread 0
+// issues the next row's copies as soon as it has the row's decision.  The
+// cluster barrier that orders the peers' mbarrier initialisation before
+// the first exchange is split: arrived at before row 0 is read, waited for
+// only before row 0's result is sent.
+constexpr int kGChunk = 4096;                                    // elements per bulk copy (16 KB)
+constexpr int kGSlots = 3;                                       // copies in flight per CTA
+constexpr uint32_t kGSmem = kGSlots * kGChunk * 4 + 128;         // ring + alignment slack
+constexpr int kGMinBlocks = 4;                                   // CTAs per SM (4 rings of 48 KB)
+
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int CS, bool TREE>
+__global__ void __launch_bounds__(kThreads, kGMinBlocks) accept_greedy_bulk_kernel(
+    const float *__restrict__ p, const int32_t *__restrict__ draft, const int32_t *__restrict__ parent,
+    int D, int V, int32_t *__restrict__ n_accepted, int32_t *__restrict__ token, int32_t *__restrict__ path,
+    uint32_t *dev_status)
+{
+    extern __shared__ uint8_t s_graw[];
+    float *ring = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_graw) + 127) & ~uintptr_t(127));
+    __shared__ ArgMax s_warp[kWarps];
+    __shared__ __align__(8) unsigned long long s_res[2][CS];   // per row parity, one per CTA
+    __shared__ uint64_t s_bar[2];
+    __shared__ uint64_t s_full[kGSlots];
+    __shared__ int32_t s_draft[kMaxDraft + 1];   // chain: drafts; tree: node tokens
+    __shared__ int32_t s_par[TREE ? kMaxDraft + 1 : 1];
+    __shared__ int s_abort, s_bad;
+    if (cluster_ctas() != static_cast<uint32_t>(CS)) {   // uniform over the grid
+        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
+        return;
+    }
+    const int rank = CS > 1 ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
+    const int b = blockIdx.x / CS;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // this CTA's slice [c0, c0 + n) (a multiple of 4 elements: V % 4 == 0)
+    const int64_t cta_len = ((static_cast<int64_t>(V) + CS - 1) / CS + 3) & ~int64_t(3);
+    const int64_t c0 = imin64(V, cta_len * rank);
+    const int n = static_cast<int>(imin64(V, c0 + cta_len) - c0);
+    const int nchunks = (n + kGChunk - 1) / kGChunk;
+    volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
+    if (tid == 0) {
+        s_bad = 0;
+        mbar_init(&s_bar[0], 1);
+        mbar_init(&s_bar[1], 1);
+        for (int k = 0; k < kGSlots; ++k) mbar_init(&s_full[k], 1);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if constexpr (CS > 1) cluster_arrive_release();   // waited for before the first send
+    if constexpr (TREE) {
+        for (int k = tid; k <= D; k += kThreads) {
+            s_draft[k] = draft[static_cast<int64_t>(b) * (D + 1) + k];
+            const int pa = parent[static_cast<int64_t>(b) * (D + 1) + k];
+            s_par[k] = pa;
+            if (k == 0 ? pa != -1 : (pa < 0 || pa >= k)) s_bad = 1;
+        }
+    } else {
+        for (int i = tid; i < D; i += kThreads) s_draft[i] = draft[static_cast<int64_t>(b) * D + i];
+    }
+    __syncthreads();
+
+    // a malformed tree is reported and walked as a lone root
+    if (TREE && s_bad && rank == 0 && tid == 0) report(dev_status, SPEC_DEV_ERR_TREE);
+    uint32_t issued[kGSlots] = {};   // thread 0: copies issued per slot (its phase count)
+    uint32_t used = 0;               // every thread: chunks consumed so far (slot c % kGSlots)
+    // thread 0: arm row i's exchange barrier and copy the first chunks of
+    // its slice (row index r of sequence b) into the ring
+    auto issue_row = [&](int i, int r) {
+        if (CS > 1) mbar_arrive_expect_tx(&s_bar[i & 1], CS * 8);
+        const float *src = p + (static_cast<int64_t>(b) * (D + 1) + r) * V + c0;
+        for (int c = 0; c < nchunks && c < kGSlots; ++c) {
+            const uint32_t bytes = static_cast<uint32_t>(imin64(kGChunk, n - c * kGChunk)) * 4u;
+            const int slot = static_cast<int>((used + c) % kGSlots);
+            mbar_arrive_expect_tx(&s_full[slot], bytes);
+            bulk_load(ring + slot * kGChunk, src + c * kGChunk, bytes, &s_full[slot]);
+            ++issued[slot];
+        }
+    };
+    if (tid == 0) issue_row(0, 0);
+    int node = 0;                    // tree: the node whose row this iteration reads
+    for (int i = 0; i <= D; ++i) {
+        const int par = i & 1;
+        const float *row = p + (static_cast<int64_t>(b) * (D + 1) + (TREE ? node : i)) * V + c0;
+        // Per lane, elements are visited in increasing index order; only a
+        // strictly larger value replaces the best, so ties keep the lowest
+        // index.  The index is located only when a float4's max wins.
+        ArgMax best{-FLT_MAX, INT_MAX};
+        bool ok = true;
+        // every thread runs every chunk iteration (a failed wait only skips
+        // the arithmetic), so the refill barriers below always pair up
+        for (int c = 0; c < nchunks; ++c, ++used) {
+            const int slot = static_cast<int>(used % kGSlots);
+            if (ok) ok = mbar_wait(&s_full[slot], (used / kGSlots) & 1u, abort, dev_status);
+            if (ok) {
+                const float *src = ring + slot * kGChunk;
+                const int len = static_cast<int>(imin64(kGChunk, n - c * kGChunk));
+                const int gbase = static_cast<int>(c0) + c * kGChunk;
+#pragma unroll 4
+                for (int e = tid * 4; e < len; e += kThreads * 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src + e);
+                    const float m4 = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+                    if (m4 > best.v || (best.i == INT_MAX && m4 == m4)) {
+                        const int k = x.x == m4 ? 0 : x.y == m4 ? 1 : x.z == m4 ? 2 : 3;
+                        best = {m4, gbase + e + k};
+                    }
+                }
+            }
+            if (c + kGSlots < nchunks) {   // a slice longer than the ring: refill this slot
+                __syncthreads();
+                if (tid == 0 && !*abort) {
+                    const uint32_t bytes =
+                        static_cast<uint32_t>(imin64(kGChunk, n - (c + kGSlots) * kGChunk)) * 4u;
+                    mbar_arrive_expect_tx(&s_full[slot], bytes);
+                    bulk_load(ring + slot * kGChunk, row + (c + kGSlots) * kGChunk, bytes, &s_full[slot]);
+                    ++issued[slot];
+                }
+            }
+        }
+        ok = __syncthreads_and(ok);
+        best = warp_argmax(best);
+        if (lane == 0) s_warp[warp] = best;
+        if constexpr (CS > 1) {
+            if (i == 0) cluster_wait_acquire();   // every peer's barriers are initialised
+        }
+        __syncthreads();
+        if (warp == 0 && ok) {
+            ArgMax c = lane < kWarps ? s_warp[lane] : ArgMax{-FLT_MAX, INT_MAX};
+            c = warp_argmax(c);
+            // this CTA's result, to every CTA of the cluster (itself included)
+            if (lane < CS) {
+                const unsigned long long w = pack_argmax(c);
+                if constexpr (CS > 1)
+                    st_async_peer(peer_smem(&s_res[par][rank], lane), w, peer_smem(&s_bar[par], lane));
+                else
+                    s_res[par][0] = w;   // a lone CTA: its own result is the row's
+            }
+        }
+        if constexpr (CS > 1) {
+            if (ok) ok = mbar_wait_warp(&s_bar[par], (i >> 1) & 1, abort, dev_status);
+        } else {
+            __syncthreads();
+        }
+        ArgMax g{-FLT_MAX, INT_MAX};
+#pragma unroll
+        for (int r = 0; r < CS; ++r) g = better(g, unpack_argmax(s_res[par][r]));
+        bool stop;
+        int next = -1;
+        if constexpr (TREE) {
+            // the lowest-index child of `node` carrying the argmax (every
+            // thread scans the same small tree, so all agree)
+            if (ok && !s_bad)
+                for (int k = node + 1; k <= D; ++k)
+                    if (s_par[k] == node && s_draft[k] == g.i) { next = k; break; }
+            stop = !ok || next < 0;
+        } else {
+            stop = !ok || i == D || s_draft[i] != g.i;
+        }
+        if (stop) {
+            if (ok && rank == 0 && tid == 0) {
+                n_accepted[b] = i;
+                token[b] = g.i;
+            }
+            if (TREE && path && rank == 0)
+                for (int x = i + tid; x < D; x += kThreads) path[static_cast<int64_t>(b) * D + x] = -1;
+            break;
+        }
+        if constexpr (TREE) {
+            if (path && rank == 0 && tid == 0) path[static_cast<int64_t>(b) * D + i] = next;
+            node = next;
+        }
+        // The next row's copies go out as soon as thread 0 knows the
+        // decision: every thread of this CTA finished reading the ring before
+        // the barrier that precedes this row's send, and no thread rewrites
+        // s_warp or s_res[par] before every CTA has sent its next result.
+        if (tid == 0) issue_row(i + 1, TREE ? node : i + 1);
+    }
+    // unwind after a timed-out wait: let the copies in flight land
+    if (tid == 0 && *abort)
+        for (int k = 0; k < kGSlots; ++k)
+            if (issued[k]) mbar_wait_drain(&s_full[k], (issued[k] - 1u) & 1u, kWaitTimeoutNs);
     // keep this CTA's shared memory alive until every peer is done with it
     if constexpr (CS > 1) cg::this_cluster().sync();
 }
@@ -1358,12 +1559,44 @@ cudaError_t launch_greedy_cs(const float *p, const int32_t *draft, const int32_t
                               path, dev_status, vec4);
 }
 
+template <int CS, bool TREE>
+cudaError_t launch_greedy_bulk_cs(const float *p, const int32_t *draft, const int32_t *parent, int B, int D,
+                                  int V, int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
+                                  cudaStream_t st)
+{
+    cudaError_t e = cudaFuncSetAttribute(accept_greedy_bulk_kernel<CS, TREE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kGSmem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B) * CS);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kGSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, accept_greedy_bulk_kernel<CS, TREE>, p, draft, parent, D, V, n_acc, token,
+                              path, dev_status);
+}
+
 template <bool TREE>
 cudaError_t launch_greedy(const float *p, const int32_t *draft, const int32_t *parent, int B, int D,
                           int V, int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
                           cudaStream_t st)
 {
     const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0);
+    if (vec4) {   // rows staged by bulk copies
+        switch (pick_cluster(V)) {
+        case 8: return launch_greedy_bulk_cs<8, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, st);
+        case 4: return launch_greedy_bulk_cs<4, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, st);
+        case 2: return launch_greedy_bulk_cs<2, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, st);
+        default: return launch_greedy_bulk_cs<1, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, st);
+        }
+    }
     switch (pick_cluster(V)) {
     case 8: return launch_greedy_cs<8, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
     case 4: return launch_greedy_cs<4, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);

@@ -77,12 +77,30 @@ def test_tiny_step_both_modes(sv, oracle_lib, seed):
     check_sample(sv, oracle_lib, inp)
 
 
-@pytest.mark.parametrize("V", [1, 3, 7, 1001, 2048, 4099, 8192, 32768, 50257])
+@pytest.mark.parametrize("V", [1, 3, 7, 1001, 2048, 4099, 8192, 32768, 40000, 50257, 200000])
 @pytest.mark.parametrize("D", [0, 1, 5])
 def test_vocab_shapes_and_cluster_paths(sv, oracle_lib, V, D):
     inp = synth.accept_inputs(V + D, 24, D, V, target_std=2.0, draft_noise=0.7, mode="both")
     check_greedy(sv, oracle_lib, inp["p"], inp["draft_greedy"])
     check_sample(sv, oracle_lib, inp)
+
+
+def test_greedy_rows_without_16_byte_alignment(sv, oracle_lib):
+    """p starting 4 bytes past a 16-byte boundary (V % 4 == 0): rows cannot
+    be staged by bulk copies and take the register-load kernel; the results
+    must not change."""
+    import torch
+    B, D, V = 24, 5, 32768
+    inp = synth.accept_inputs(77, B, D, V, target_std=2.0, draft_noise=0.7, mode="both")
+    p, draft = inp["p"], inp["draft_greedy"]
+    flat = torch.empty(p.size + 1, dtype=torch.float32, device="cuda")
+    flat[1:] = to_dev(p.reshape(-1))
+    pd = flat[1:].view(B, D + 1, V)
+    assert pd.data_ptr() % 16 == 4
+    n, t = sv.accept_greedy(pd, to_dev(draft))
+    torch.cuda.synchronize()
+    n_ref, t_ref = oracle_lib.accept_greedy(p, draft)
+    assert (n.cpu().numpy() == n_ref).all() and (t.cpu().numpy() == t_ref).all()
 
 
 @pytest.fixture(scope="module")
