@@ -401,9 +401,15 @@ spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_b
     // each CTA of a pair loading half of the w tile (multicast to both)
     const uint32_t bx[2] = {64, static_cast<uint32_t>(plan.swap ? plan.bn : 128)};
     const uint32_t bw[2] = {64, static_cast<uint32_t>(plan.swap ? 128 : plan.bn / 2)};
-    if (!encode_bf16_tmap(&tx, x_bf16, 2, dx, st, bx) || !encode_bf16_tmap(&tw, w_bf16, 2, dw, st, bw))
+    // y: 32 x 32 output blocks staged in shared memory, written by TMA stores
+    CUtensorMap ty;
+    const uint64_t dy[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+    const uint64_t sy[1] = {static_cast<uint64_t>(N) * 2};
+    const uint32_t by[2] = {32, 32};
+    if (!encode_bf16_tmap(&tx, x_bf16, 2, dx, st, bx) || !encode_bf16_tmap(&tw, w_bf16, 2, dw, st, bw) ||
+        !encode_bf16_tmap_plain(&ty, y_bf16, 2, dy, sy, by))
         return SPEC_ERR_CUDA;
-    return from_cuda(launch_gemm(plan, tx, tw, y_bf16, M, N, workspace, nullptr,
+    return from_cuda(launch_gemm(plan, tx, tw, ty, y_bf16, M, N, workspace, nullptr,
                                  static_cast<cudaStream_t>(stream)));
 }
 

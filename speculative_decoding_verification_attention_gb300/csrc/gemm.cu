@@ -21,7 +21,9 @@
 // (stream-K, see gemm_schedule.h).  Every piece of a tile cut between CTAs
 // leaves its fp32 partial in the workspace and counts itself in; the last
 // piece to arrive adds them all in k order (so results are deterministic)
-// and writes the tile.  No CTA waits for another.
+// and writes the tile.  No CTA waits for another.  Output blocks of 32 x 32
+// are staged in shared memory by each epilogue warp and written by TMA
+// tensor stores (coalesced, asynchronous; rows past M are clipped).
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
@@ -87,20 +89,6 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
     return v;
 }
 
-__device__ __forceinline__ void store_bf16_row32(__nv_bfloat16 *dst_row, const float (&a)[32])
-{
-    uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-        uint4 o;
-        o.x = pack_bf16x2(a[8 * v + 0], a[8 * v + 1]);
-        o.y = pack_bf16x2(a[8 * v + 2], a[8 * v + 3]);
-        o.z = pack_bf16x2(a[8 * v + 4], a[8 * v + 5]);
-        o.w = pack_bf16x2(a[8 * v + 6], a[8 * v + 7]);
-        dst[v] = o;
-    }
-}
-
 // Partial tiles (128 rows x BN fp32) are laid out in 32-column units of
 // 16 KB, each [8 column quads][128 rows][4]: a warp's float4 accesses to one
 // quad are contiguous, and a unit is one bulk copy.
@@ -127,30 +115,66 @@ __device__ __forceinline__ bool other_first(const SkGrid &g, int f, int t)
     return g.begin(f) == static_cast<long long>(t - g.dp_tiles) * g.kblocks;
 }
 
-// Write 32 columns (chunk cc) of a finished output tile row as bf16.
-template <bool SWAP>
-__device__ __forceinline__ void store_out(__nv_bfloat16 *__restrict__ y, int M, int N, int t, int mt, int nt,
-                                          int BN, int row, int cc, const float (&a)[32])
+// Output staging: each epilogue warp owns two 32 x 32 bf16 blocks (2 KB).
+constexpr uint32_t kOutBlock = 32 * 32 * 2;
+constexpr uint32_t kOutStaging = 4 * 2 * kOutBlock;
+
+__device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, int x, int y)
 {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most one bulk group of this thread still reading its shared source
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// every bulk group of this thread complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Write 32 columns (chunk cc) of this warp's 32 tile rows as one bf16 block:
+// staged in the warp's next buffer, then one TMA store by lane 0.  Tiled:
+// tile row = y row, block at (x = nt BN + 32 cc, y = 128 mt + 32 quad).
+// Swap: tile row = w row n = y column, tile column = x row m, so the block
+// is transposed while staged, at (x = 128 t + 32 quad, y = 32 cc).
+template <bool SWAP>
+__device__ __forceinline__ void store_out(const CUtensorMap *tm_y, uint8_t *obuf, uint32_t &nst, int lane,
+                                          int t, int mt, int nt, int BN, int quad, int cc, const float (&a)[32])
+{
+    uint8_t *buf = obuf + (nst & 1u) * kOutBlock;
+    if (lane == 0) bulk_wait_read_1();   // the store issued from this buffer two blocks ago has read it
+    __syncwarp();
     if (SWAP) {
-        // rows of the tile are w rows n; columns are x rows m
-        const int n = t * kBM + row;
+        __nv_bfloat16 *b = reinterpret_cast<__nv_bfloat16 *>(buf);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int m = cc * 32 + j;
-            if (m < M) y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(a[j]);
-        }
+        for (int j = 0; j < 32; ++j) b[j * 32 + lane] = __float2bfloat16_rn(a[j]);
     } else {
-        const int m = mt * kBM + row;
-        if (m < M) store_bf16_row32(y + static_cast<int64_t>(m) * N + nt * BN + cc * 32, a);
+        uint4 *b = reinterpret_cast<uint4 *>(buf + lane * 64);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            uint4 o;
+            o.x = pack_bf16x2(a[8 * v + 0], a[8 * v + 1]);
+            o.y = pack_bf16x2(a[8 * v + 2], a[8 * v + 3]);
+            o.z = pack_bf16x2(a[8 * v + 4], a[8 * v + 5]);
+            o.w = pack_bf16x2(a[8 * v + 6], a[8 * v + 7]);
+            b[v] = o;
+        }
     }
+    fence_proxy_async_smem();   // the staged block is visible to the TMA unit
+    __syncwarp();
+    if (lane == 0) {
+        if (SWAP) tma_store_2d(tm_y, buf, t * kBM + quad * 32, cc * 32);
+        else tma_store_2d(tm_y, buf, nt * BN + cc * 32, mt * kBM + quad * 32);
+        bulk_commit();
+    }
+    ++nst;
 }
 
 template <int BN, int STAGES>
 struct TiledSmem {
     static constexpr uint32_t kTileB = BN * kBK * 2;
     static constexpr uint32_t kStage = kTileA + kTileB;
-    static constexpr uint32_t kBytes = STAGES * kStage + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t kBytes = STAGES * kStage + kOutStaging + 1024 /*align*/ + 256 /*barriers*/;
     static_assert(STAGES * kStage >= kBM * BN * 4, "a partial tile must fit in the stage ring");
 };
 
@@ -162,13 +186,14 @@ constexpr int stages_for(int bn) { return bn >= 256 ? 4 : bn >= 128 ? 6 : 8; }
 template <int BN, int STAGES, bool SWAP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                __nv_bfloat16 *__restrict__ y, int M, int N, SkGrid grid, float *__restrict__ part,
+                const __grid_constant__ CUtensorMap tm_y, int M, int N, SkGrid grid, float *__restrict__ part,
                 uint32_t *__restrict__ flags, uint32_t *dev_status)
 {
     using L = TiledSmem<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * L::kStage);
+    uint8_t *out_stage = smem + STAGES * L::kStage;   // 4 warps x 2 output blocks
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_stage + kOutStaging);
     uint64_t *empty = full + STAGES;
     uint64_t *acc_full = empty + STAGES;
     uint64_t *acc_empty = acc_full + 2;
@@ -213,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tm_x);
         tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_y);
         SegWalker wk(grid, c);
         Seg s;
         uint32_t it = 0;
@@ -271,10 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;
         // swap: only the 32-column chunks that hold rows of x are needed
         const int nchunks = SWAP ? (M + 31) / 32 < BN / 32 ? (M + 31) / 32 : BN / 32 : BN / 32;
-        const int unit_bytes = nchunks * 32 * kBM * 4;   // one piece's partial
         SegWalker wk(grid, c);
         Seg s;
         uint32_t lt = 0, npub = 0, nred = 0, ndec = 0;
+        uint8_t *obuf = out_stage + (warp - 2) * 2 * kOutBlock;
+        uint32_t nst = 0;   // output blocks this warp has stored
         while (!*abort && wk.next(s)) {
             const uint32_t ab = lt & 1;
             if (!mbar_wait_warp(&acc_full[ab], (lt >> 1) & 1, abort, dev_status)) break;
@@ -292,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float a[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(r[j]);
-                    store_out<SWAP>(y, M, N, s.t, mt, nt, BN, row, cc, a);
+                    store_out<SWAP>(&tm_y, obuf, nst, lane, s.t, mt, nt, BN, quad, cc, a);
                 }
             } else {
                 // A piece of a cut tile: publish the fp32 partial, then count
@@ -423,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     }
                                 }
                             }
-                            store_out<SWAP>(y, M, N, s.t, mt, nt, BN, row, cc, a);
+                            store_out<SWAP>(&tm_y, obuf, nst, lane, s.t, mt, nt, BN, quad, cc, a);
                         }
                         if (ring_ok) {
                             __syncwarp();
@@ -439,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&acc_empty[ab]);
             ++lt;
         }
+        if (lane == 0) bulk_wait_all();   // output stores done before the CTA may exit
     }
     __syncwarp();
     __syncthreads();
@@ -476,7 +504,7 @@ cudaLaunchConfig_t kernel_config(int grid, cudaStream_t st, cudaLaunchAttribute 
 }
 
 template <int BN, bool SWAP>
-cudaError_t run(const GemmPlan &p, const CUtensorMap &tx, const CUtensorMap &tw, __nv_bfloat16 *y,
+cudaError_t run(const GemmPlan &p, const CUtensorMap &tx, const CUtensorMap &tw, const CUtensorMap &ty,
                 int M, int N, void *workspace, uint32_t *dev_status, cudaStream_t st)
 {
     constexpr int STAGES = stages_for(BN);
@@ -487,7 +515,7 @@ cudaError_t run(const GemmPlan &p, const CUtensorMap &tx, const CUtensorMap &tw,
     float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kFlagBytes);
     cudaLaunchAttribute attr[2];
     const cudaLaunchConfig_t cfg = kernel_config<BN, SWAP>(p.grid, st, attr);
-    return cudaLaunchKernelEx(&cfg, k, tx, tw, y, M, N, p.sk, part, flags, dev_status);
+    return cudaLaunchKernelEx(&cfg, k, tx, tw, ty, M, N, p.sk, part, flags, dev_status);
 }
 
 // Units (CTA pairs, or single CTAs for the swap orientation) that can be
@@ -600,20 +628,20 @@ GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_tiled)
 }
 
 cudaError_t launch_gemm(const GemmPlan &p, const CUtensorMap &t_x, const CUtensorMap &t_w,
-                        void *y, int M, int N, void *workspace, uint32_t *dev_status,
-                        cudaStream_t st)
+                        const CUtensorMap &t_y, void *y, int M, int N, void *workspace,
+                        uint32_t *dev_status, cudaStream_t st)
 {
-    __nv_bfloat16 *yy = static_cast<__nv_bfloat16 *>(y);
+    (void)y;   // written through t_y
     if (p.swap) {
         switch (p.bn) {
-        case 32: return run<32, true>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
-        case 64: return run<64, true>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
-        case 128: return run<128, true>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
-        default: return run<256, true>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
+        case 32: return run<32, true>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
+        case 64: return run<64, true>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
+        case 128: return run<128, true>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
+        default: return run<256, true>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
         }
     }
-    if (p.bn == 256) return run<256, false>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
-    return run<128, false>(p, t_x, t_w, yy, M, N, workspace, dev_status, st);
+    if (p.bn == 256) return run<256, false>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
+    return run<128, false>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
 }
 
 }  // namespace spec

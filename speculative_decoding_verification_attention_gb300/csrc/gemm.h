@@ -32,8 +32,9 @@ GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_tiled)
 // query fails).
 int gemm_max_units(int bn, bool swap);
 
+// t_y: y as bf16 [M][N] with 32 x 32 boxes and no swizzle (output stores).
 cudaError_t launch_gemm(const GemmPlan &p, const CUtensorMap &t_x, const CUtensorMap &t_w,
-                        void *y, int M, int N, void *workspace, uint32_t *dev_status,
-                        cudaStream_t st);
+                        const CUtensorMap &t_y, void *y, int M, int N, void *workspace,
+                        uint32_t *dev_status, cudaStream_t st);
 
 }  // namespace spec

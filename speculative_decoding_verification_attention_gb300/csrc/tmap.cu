@@ -27,10 +27,8 @@ EncodeFn encode_fn()
     return fn;
 }
 
-}  // namespace
-
-bool encode_bf16_tmap(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                      const uint64_t *strides_bytes, const uint32_t *box)
+bool encode_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle)
 {
     EncodeFn fn = encode_fn();
     if (!fn) return false;
@@ -44,9 +42,22 @@ bool encode_bf16_tmap(CUtensorMap *map, const void *base, int rank, const uint64
     }
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
                     const_cast<void *>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool encode_bf16_tmap(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                      const uint64_t *strides_bytes, const uint32_t *box)
+{
+    return encode_bf16(map, base, rank, dims, strides_bytes, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool encode_bf16_tmap_plain(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                            const uint64_t *strides_bytes, const uint32_t *box)
+{
+    return encode_bf16(map, base, rank, dims, strides_bytes, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 int device_sm_count()

@@ -14,6 +14,11 @@ namespace spec {
 bool encode_bf16_tmap(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                       const uint64_t *strides_bytes, const uint32_t *box);
 
+// Tiled bf16 tensor map without swizzle (row-major boxes in shared memory),
+// e.g. for TMA stores of output blocks.  Same argument convention.
+bool encode_bf16_tmap_plain(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                            const uint64_t *strides_bytes, const uint32_t *box);
+
 // SM count of the current device (cached per device), or -1.
 int device_sm_count();
 
