@@ -728,11 +728,12 @@ def case_lines(args):
                               "frac_hbm": by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]})
             del p, q
             torch.cuda.empty_cache()
-    if args.workload in ("adasd", "all"):
+    if args.workload in ("adasd", "all", "adasd-small"):
         # AdaSD relaxed acceptance: B=256, D=7, V=131072, target logits N(0, 3^2),
         # draft logits the target's plus N(0, sigma^2) (alpha = 0.6); tau_H at the
         # 90th percentile of the draft entropies, tau_JS at the median distance
-        B, D, V = 256, 7, 131072
+        # (adasd-small: B=32, 0.25 GB of probabilities, for profiler captures)
+        B, D, V = (32 if args.workload == "adasd-small" else 256), 7, 131072
         sigma, _ = synth.tune_sigma_for_alpha(0.6, V, rows=8, target_std=3.0)
         g = torch.Generator(device=dev)
         g.manual_seed(61)
@@ -774,10 +775,11 @@ def case_lines(args):
                       "frac_hbm": by / (ms_a * 1e-3) / 1e9 / pk["hbm_gbs"]})
         del p, q
         torch.cuda.empty_cache()
-    if args.workload in ("logits", "all"):
+    if args.workload in ("logits", "all", "logits-small"):
         # acceptance from logits: B=256, D=7, V=131072, target logits N(0, 3^2),
         # draft logits the target's plus N(0, sigma^2) with sigma tuned to alpha = 0.6
-        B, D, V, T = 256, 7, 131072, 1.0
+        # (logits-small: B=32, 0.25 GB of logits, for profiler captures)
+        B, D, V, T = (32 if args.workload == "logits-small" else 256), 7, 131072, 1.0
         sigma, _ = synth.tune_sigma_for_alpha(0.6, V, rows=8, target_std=3.0)
         g = torch.Generator(device=dev)
         g.manual_seed(60)
@@ -833,7 +835,7 @@ def main():
                     help="reference arm: seconds of oracle attention work sampled per step")
     ap.add_argument("--workload", default="step",
                     choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small", "tree",
-                             "adaptive", "logits", "adasd",
+                             "adaptive", "logits", "adasd", "logits-small", "adasd-small",
                              "accept-one"],
                     help="step: the headline line; others print one secondary JSON line per case")
     args = ap.parse_args()
