@@ -575,6 +575,10 @@ def case_lines(args):
             attention_case(f"large-group B8 G32 L131072 D{D}", 8, 4, 32, D, 131072, 20 + D)
     if args.workload == "attention-small":
         attention_case("small B4 L32768 D7 (profiling)", 4, 8, 8, 7, 32768, 5)
+    if args.workload == "attention-largeg-small":
+        # the large-group case at B=1: 4 KV heads x G=32, L=131072, D=15 (G(1+D) = 512,
+        # four 128-row tiles per KV head), 268 MB of K/V, for profiler captures
+        attention_case("large-group small B1 G32 L131072 D15 (profiling)", 1, 4, 32, 15, 131072, 35)
     if args.workload in ("gemm", "all"):
         N = K = 6144
         w = (torch.randn((N, K), device=dev) * 0.02).to(torch.bfloat16)
@@ -864,6 +868,7 @@ def main():
                     help="reference arm: seconds of oracle attention work sampled per step")
     ap.add_argument("--workload", default="step",
                     choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small", "tree",
+                             "attention-largeg-small",
                              "adaptive", "logits", "adasd", "logits-small", "adasd-small",
                              "accept-one"],
                     help="step: the headline line; others print one secondary JSON line per case")
