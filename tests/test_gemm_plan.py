@@ -91,3 +91,24 @@ def test_rejects_bad_arguments():
     assert lib.spec_verify_gemm_plan(512, 128, 60, 152, None, 0) == -1
     assert lib.spec_verify_gemm_plan(512, 128, 64, 0, None, 0) == -1
     assert lib.spec_verify_gemm_plan(512, 128, 64, 152, None, 4) == -1
+
+
+@pytest.mark.parametrize("M", [384, 512, 640, 768])
+def test_half_to_full_wave_takes_whole_tiles(M):
+    """N = K = 6144 with 76 resident CTA pairs: 48 or 72 pair tiles fill at
+    least half of the pairs, so every pair takes one whole tile and no tile
+    is cut (nothing to add up through the workspace)."""
+    N = K = 6144
+    seg = sv.gemm_plan(M, N, K, 152)
+    tiles = -(-(-(-M // 128)) // 2) * (N // 256)
+    assert len(seg) == tiles
+    assert sorted(seg[:, 1].tolist()) == list(range(tiles))
+    assert (seg[:, 2] == 0).all() and (seg[:, 3] == K // 64).all()
+    assert int(seg[:, 0].max()) + 1 == tiles
+
+
+def test_less_than_half_a_wave_is_cut():
+    """16 pair tiles for 76 pairs: the k-blocks are split so every pair works."""
+    seg = sv.gemm_plan(512, 2048, 6144, 152)
+    assert int(seg[:, 0].max()) + 1 > 16
+    assert ((seg[:, 2] > 0) | (seg[:, 3] < 96)).any()
