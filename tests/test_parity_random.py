@@ -1,4 +1,6 @@
-"""Seeded random shapes for every entry point of the step, against the oracle.
+"""Seeded random shapes for every entry point of the step (chain and tree
+attention, GEMM, greedy, stochastic and tree acceptance, acceptance from
+logits), against the oracle.
 
 Each case draws its shape from a fixed seed inside the supported set --
 group size, draft length (1 + D <= 64, G(1+D) up to 512 rows), head_dim,
@@ -112,3 +114,68 @@ def test_random_acceptance(sv, oracle_lib, seed):
     n_ref, t_ref, margin, _ = oracle_lib.accept_sample(p, inp["q"], inp["draft"], inp["u_acc"], inp["u_res"])
     bad = (n.cpu().numpy() != n_ref) | (t.cpu().numpy() != t_ref)
     assert not (bad & (margin >= MARGIN)).any(), (B, D, V)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_tree_attention(sv, oracle_lib, seed):
+    import torch
+    rng = np.random.default_rng(7000 + seed)
+    B, Hkv, G, d, D, lens, page = attention_shape(rng)
+    kind = str(rng.choice(["random", "star", "wide", "chain"]))
+    inp = synth.attention_inputs(8000 + seed, B, Hkv, G, d, D, lens, page_size=page)
+    parent = synth.tree_parents(9000 + seed, B, 1 + D, kind)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = sv.verify_tree_attention(bits_dev(inp.q), bits_dev(inp.k_pages), bits_dev(inp.v_pages),
+                                   to_dev(inp.block_table), to_dev(inp.kv_len), to_dev(parent), D, Hkv, G,
+                                   dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref, _ = oracle_lib.tree_attention(inp.q, inp.k_pages, inp.v_pages, inp.block_table, inp.kv_len, parent,
+                                       D, Hkv, G, d, page)
+    err = out.cpu().numpy().astype(np.float64) - ref
+    assert np.abs(err).max() <= 2e-2, (B, Hkv, G, d, D, page, kind)
+    assert np.linalg.norm(err) <= 1e-3 * np.linalg.norm(ref), (B, Hkv, G, d, D, page, kind)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_tree_greedy(sv, oracle_lib, seed):
+    import torch
+    rng = np.random.default_rng(10000 + seed)
+    B = int(rng.integers(1, 40))
+    D = int(rng.integers(1, 16))
+    V = int(rng.choice([7, 1000, 4099, 32768, 65536]))
+    kind = str(rng.choice(["random", "star", "wide", "chain"]))
+    p = synth.accept_inputs(11000 + seed, B, D, V, mode="greedy")["p"]
+    parent = synth.tree_parents(12000 + seed, B, 1 + D, kind)
+    am = np.argmax(p, axis=2)
+    tokens = rng.integers(0, V, size=(B, 1 + D)).astype(np.int32)
+    hit = rng.random((B, 1 + D)) < 0.7
+    for b in range(B):
+        for k in range(1, 1 + D):
+            if hit[b, k]:
+                tokens[b, k] = am[b, parent[b, k]]
+    n, t, path = sv.accept_tree_greedy(to_dev(p), to_dev(tokens), to_dev(parent))
+    torch.cuda.synchronize()
+    n_ref, t_ref, path_ref = oracle_lib.accept_tree_greedy(p, tokens, parent)
+    assert np.array_equal(n.cpu().numpy(), n_ref), (B, D, V, kind)
+    assert np.array_equal(t.cpu().numpy(), t_ref) and np.array_equal(path.cpu().numpy(), path_ref)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_acceptance_from_logits(sv, oracle_lib, seed):
+    import torch
+    rng = np.random.default_rng(13000 + seed)
+    B = int(rng.integers(1, 24))
+    D = int(rng.integers(0, 10))
+    V = int(rng.choice([3, 300, 4096, 9001, 32768, 65536]))
+    T = float(rng.choice([0.5, 1.0, 1.7]))
+    inp = synth.logits_inputs(14000 + seed, B, D, V, target_std=float(rng.uniform(1.0, 4.0)),
+                              draft_noise=float(rng.uniform(0.2, 1.5)), temperature=T,
+                              masked=int(rng.integers(0, 3)) * (V // 4))
+    zp, zq, draft = inp["zp"], inp["zq"], inp["draft"]
+    n, t = sv.accept_sample_logits(to_dev(zp), to_dev(zq) if D else None, to_dev(draft) if D else None, T, seed)
+    torch.cuda.synchronize()
+    p, q, u_acc, u_res = oracle_lib.logits_to_probs(zp, zq, T, seed)
+    n_ref, t_ref, margin, _ = oracle_lib.accept_sample(p, q, draft, u_acc, u_res)
+    bad = (n.cpu().numpy() != n_ref) | (t.cpu().numpy() != t_ref)
+    assert not (bad & (margin >= MARGIN)).any(), (B, D, V, T)
