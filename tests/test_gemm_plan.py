@@ -79,10 +79,15 @@ def test_stream_k_split(M, N, K, sms):
         assert all(r[4] == -1 for r in rows if r[2] > 0)
 
 
-def test_every_sm_streams_weights_at_small_m():
+def test_weight_streaming_cuts_each_tile_in_thirds_at_small_m():
+    """M = 8, N = K = 6144: the 48 w tiles of 128 rows are cut into three
+    equal k-ranges of 32 k-blocks, one per CTA (144 of the 152 SMs stream
+    weights)."""
     seg = sv.gemm_plan(8, 6144, 6144, 152)
-    assert int(seg[:, 0].max()) + 1 == 152
+    assert int(seg[:, 0].max()) + 1 == 144
     assert (seg[:, 5] == 32).all()
+    assert ((seg[:, 3] - seg[:, 2]) == 32).all()
+    assert sorted(np.bincount(seg[:, 1]).tolist()) == [3] * 48
 
 
 def test_rejects_bad_arguments():
