@@ -10,6 +10,13 @@ import pytest
 import speculative_decoding_verification_attention_gb300 as sv
 
 
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    """The planner runs inside the library: rebuild it if a source is newer."""
+    from speculative_decoding_verification_attention_gb300 import _build
+    _build.build()
+
+
 def test_starts_at_the_largest_tier():
     c = sv.AdaptiveDraftLength((1, 3, 7), beta=0.5)
     assert c.draft_len == 7

@@ -13,6 +13,13 @@ import pytest
 
 import speculative_decoding_verification_attention_gb300 as sv
 
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    """The planner runs inside the library: rebuild it if a source is newer."""
+    from speculative_decoding_verification_attention_gb300 import _build
+    _build.build()
+
 SHAPES = [(8, 6144, 6144), (200, 6144, 6144), (256, 384, 640), (1, 128, 64), (257, 6144, 6144), (384, 128, 6144), (512, 6144, 6144), (1024, 6144, 6144),
           (2048, 6144, 6144), (4096, 6144, 6144), (3000, 6272, 1024), (512, 256, 64),
           (65536, 128, 64), (300, 384, 128)]
