@@ -134,155 +134,29 @@ __device__ __forceinline__ void st_async_peer(uint32_t addr, unsigned long long 
 
 constexpr int kGUnroll = 8;    // greedy: 128-element steps whose loads are in flight together
 
-// Greedy acceptance with register loads (rows that are not 16-byte aligned;
-// aligned rows take accept_greedy_bulk_kernel below): one thread-block
-// cluster of CS CTAs per sequence, CTA `rank` owning a contiguous slice of
-// the vocabulary.  Row by row, each CTA
-// reduces its slice to an argmax (all loads of a lane issued at once) and
-// sends the result to every CTA of the cluster with an asynchronous
-// distributed-shared-memory store that completes on the receiver's
-// mbarrier; every CTA then reduces the CS results itself and takes the same
-// decision, so no cluster-wide barrier sits on the per-row path.  Only rows
-// 0..n_accepted are read.
+// Greedy acceptance: one thread-block cluster of CS CTAs per sequence, CTA
+// `rank` owning a contiguous slice of the vocabulary.  Row by row, each CTA
+// reduces its slice to an argmax and sends the result to every CTA of the
+// cluster with an asynchronous distributed-shared-memory store that
+// completes on the receiver's mbarrier; every CTA then reduces the CS
+// results itself and takes the same decision, so no cluster-wide barrier
+// sits on the per-row path.  Only rows 0..n_accepted are read.
+// BULK (rows 16-byte aligned): each row's slice is staged in shared memory
+// in chunks of kGChunk elements, kGSlots of them in flight at once, issued
+// by one thread -- no loads held in registers, the arithmetic on a chunk
+// starting as soon as it lands; a slice longer than the ring (64 KB at
+// V = 131072 against a 48 KB ring, which keeps 4 CTAs on an SM) streams
+// through it; thread 0 issues the next row's copies as soon as it has the
+// row's decision.  Otherwise every lane loads its elements with register
+// loads, kGUnroll 128-element steps in flight.
+// The cluster barrier that orders the peers' mbarrier initialisation before
+// the first exchange is split: arrived at before row 0 is read, waited for
+// only before row 0's result is sent.
 // TREE: the 1 + D rows are the nodes of a draft tree (parent[b][k] < k,
 // node tokens tokens[b][k]); from the root the walk moves to the child whose
 // token equals the row's argmax (lowest node index among such siblings) and
 // stops when none does.  The chain is the tree parent[k] = k - 1 whose node
 // k carries draft k - 1.
-template <int CS, bool TREE>
-__global__ void __launch_bounds__(kThreads, 4) accept_greedy_kernel(
-    const float *__restrict__ p, const int32_t *__restrict__ draft, const int32_t *__restrict__ parent,
-    int D, int V, int32_t *__restrict__ n_accepted, int32_t *__restrict__ token,
-    int32_t *__restrict__ path, uint32_t *dev_status, bool vec4)
-{
-    __shared__ ArgMax s_warp[kWarps];
-    __shared__ __align__(8) unsigned long long s_res[2][CS];   // per row parity, one per CTA
-    __shared__ uint64_t s_bar[2];
-    __shared__ int32_t s_draft[kMaxDraft + 1];   // chain: drafts; tree: node tokens
-    __shared__ int32_t s_par[TREE ? kMaxDraft + 1 : 1];
-    __shared__ int s_abort, s_bad;
-    if (cluster_ctas() != static_cast<uint32_t>(CS)) {   // uniform over the grid
-        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
-        return;
-    }
-    const int rank = CS > 1 ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
-    const int b = blockIdx.x / CS;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Slice sl = warp_slice(V, CS, rank, warp);
-    volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
-    if (threadIdx.x == 0) s_bad = 0;
-    __syncthreads();
-    if constexpr (TREE) {
-        for (int k = threadIdx.x; k <= D; k += kThreads) {
-            s_draft[k] = draft[static_cast<int64_t>(b) * (D + 1) + k];
-            const int pa = parent[static_cast<int64_t>(b) * (D + 1) + k];
-            s_par[k] = pa;
-            if (k == 0 ? pa != -1 : (pa < 0 || pa >= k)) s_bad = 1;
-        }
-    } else {
-        for (int i = threadIdx.x; i < D; i += kThreads) s_draft[i] = draft[static_cast<int64_t>(b) * D + i];
-    }
-    if (threadIdx.x == 0) {
-        mbar_init(&s_bar[0], 1);
-        mbar_init(&s_bar[1], 1);
-        s_abort = 0;
-        fence_mbar_init();
-    }
-    if constexpr (CS > 1) cg::this_cluster().sync();   // peers' barriers exist before any send
-    else __syncthreads();
-
-    // a malformed tree is reported and walked as a lone root
-    if (TREE && s_bad && rank == 0 && threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_TREE);
-    int node = 0;   // tree: the node whose row this iteration reads
-    for (int i = 0; i <= D; ++i) {
-        const int par = i & 1;
-        if (CS > 1 && threadIdx.x == 0) mbar_arrive_expect_tx(&s_bar[par], CS * 8);
-        const float *row = p + (static_cast<int64_t>(b) * (D + 1) + (TREE ? node : i)) * V;
-        // Per lane, elements are visited in increasing index order; only a
-        // strictly larger value replaces the best, so ties keep the lowest
-        // index.  The index is located only when a float4's max wins.
-        ArgMax best{-FLT_MAX, INT_MAX};
-        for (int64_t base = sl.begin; base < sl.end; base += kStep * kGUnroll) {
-            float4 x[kGUnroll];
-#pragma unroll
-            for (int u = 0; u < kGUnroll; ++u) {
-                const int64_t e = base + u * kStep + lane * 4;
-                x[u] = e < sl.end ? load4(row, e, sl.end, vec4, -INFINITY)
-                                  : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            }
-#pragma unroll
-            for (int u = 0; u < kGUnroll; ++u) {
-                const int e = static_cast<int>(base) + u * kStep + lane * 4;
-                const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
-                if (e < sl.end && (m4 > best.v || (best.i == INT_MAX && m4 == m4))) {
-                    const int k = x[u].x == m4 ? 0 : x[u].y == m4 ? 1 : x[u].z == m4 ? 2 : 3;
-                    if (e + k < sl.end) best = {m4, e + k};
-                }
-            }
-        }
-        best = warp_argmax(best);
-        if (lane == 0) s_warp[warp] = best;
-        __syncthreads();
-        if (warp == 0) {
-            ArgMax c = lane < kWarps ? s_warp[lane] : ArgMax{-FLT_MAX, INT_MAX};
-            c = warp_argmax(c);
-            // this CTA's result, to every CTA of the cluster (itself included)
-            if (lane < CS) {
-                const unsigned long long w = pack_argmax(c);
-                if constexpr (CS > 1)
-                    st_async_peer(peer_smem(&s_res[par][rank], lane), w, peer_smem(&s_bar[par], lane));
-                else
-                    s_res[par][0] = w;   // a lone CTA: its own result is the row's
-            }
-        }
-        bool ok = true;
-        if constexpr (CS > 1) ok = mbar_wait_warp(&s_bar[par], (i >> 1) & 1, abort, dev_status);
-        else __syncthreads();
-        ArgMax g{-FLT_MAX, INT_MAX};
-#pragma unroll
-        for (int r = 0; r < CS; ++r) g = better(g, unpack_argmax(s_res[par][r]));
-        bool stop;
-        int next = -1;
-        if constexpr (TREE) {
-            // the lowest-index child of `node` carrying the argmax (every
-            // thread scans the same small tree, so all agree)
-            if (ok && !s_bad)
-                for (int k = node + 1; k <= D; ++k)
-                    if (s_par[k] == node && s_draft[k] == g.i) { next = k; break; }
-            stop = !ok || next < 0;
-        } else {
-            stop = !ok || i == D || s_draft[i] != g.i;
-        }
-        if (stop) {
-            if (ok && rank == 0 && threadIdx.x == 0) {
-                n_accepted[b] = i;
-                token[b] = g.i;
-            }
-            if (TREE && path && rank == 0)
-                for (int x = i + threadIdx.x; x < D; x += kThreads) path[static_cast<int64_t>(b) * D + x] = -1;
-            break;
-        }
-        if constexpr (TREE) {
-            if (path && rank == 0 && threadIdx.x == 0) path[static_cast<int64_t>(b) * D + i] = next;
-            node = next;
-        }
-        __syncthreads();   // s_warp is rewritten by the next row
-    }
-    // keep this CTA's shared memory alive until every peer is done with it
-    if constexpr (CS > 1) cg::this_cluster().sync();
-}
-
-// Greedy acceptance with the CTA's vocabulary slice staged in shared memory
-// by bulk copies (rows whose elements are 16-byte aligned).  The same walk
-// as accept_greedy_kernel, but each row's slice arrives in chunks of kGChunk
-// elements, kGSlots of them in flight at once, issued by one thread: no
-// loads held in registers, and the arithmetic on a chunk starts as soon as
-// it lands; a slice longer than the ring (64 KB at V = 131072 against a
-// 48 KB ring, which keeps 4 CTAs on an SM) streams through it.  Thread 0
-// issues the next row's copies as soon as it has the row's decision.  The
-// cluster barrier that orders the peers' mbarrier initialisation before
-// the first exchange is split: arrived at before row 0 is read, waited for
-// only before row 0's result is sent.
 constexpr int kGChunk = 4096;                                    // elements per bulk copy (16 KB)
 constexpr int kGSlots = 3;                                       // copies in flight per CTA
 constexpr uint32_t kGSmem = kGSlots * kGChunk * 4 + 128;         // ring + alignment slack
@@ -298,11 +172,11 @@ __device__ __forceinline__ void cluster_wait_acquire()
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int CS, bool TREE>
-__global__ void __launch_bounds__(kThreads, kGMinBlocks) accept_greedy_bulk_kernel(
+template <int CS, bool TREE, bool BULK>
+__global__ void __launch_bounds__(kThreads, kGMinBlocks) accept_greedy_kernel(
     const float *__restrict__ p, const int32_t *__restrict__ draft, const int32_t *__restrict__ parent,
     int D, int V, int32_t *__restrict__ n_accepted, int32_t *__restrict__ token, int32_t *__restrict__ path,
-    uint32_t *dev_status)
+    uint32_t *dev_status, bool vec4)
 {
     extern __shared__ uint8_t s_graw[];
     float *ring = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_graw) + 127) & ~uintptr_t(127));
@@ -320,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, kGMinBlocks) accept_greedy_bulk_kern
     const int rank = CS > 1 ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
     const int b = blockIdx.x / CS;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // this CTA's slice [c0, c0 + n) (a multiple of 4 elements: V % 4 == 0)
+    const Slice sl = warp_slice(V, CS, rank, warp);   // register loads: this warp's elements
+    // this CTA's slice [c0, c0 + n) (BULK: a multiple of 4 elements, V % 4 == 0)
     const int64_t cta_len = ((static_cast<int64_t>(V) + CS - 1) / CS + 3) & ~int64_t(3);
     const int64_t c0 = imin64(V, cta_len * rank);
     const int n = static_cast<int>(imin64(V, c0 + cta_len) - c0);
@@ -356,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, kGMinBlocks) accept_greedy_bulk_kern
     // its slice (row index r of sequence b) into the ring
     auto issue_row = [&](int i, int r) {
         if (CS > 1) mbar_arrive_expect_tx(&s_bar[i & 1], CS * 8);
+        if (!BULK) return;
         const float *src = p + (static_cast<int64_t>(b) * (D + 1) + r) * V + c0;
         for (int c = 0; c < nchunks && c < kGSlots; ++c) {
             const uint32_t bytes = static_cast<uint32_t>(imin64(kGChunk, n - c * kGChunk)) * 4u;
@@ -375,9 +251,30 @@ __global__ void __launch_bounds__(kThreads, kGMinBlocks) accept_greedy_bulk_kern
         // index.  The index is located only when a float4's max wins.
         ArgMax best{-FLT_MAX, INT_MAX};
         bool ok = true;
-        // every thread runs every chunk iteration (a failed wait only skips
-        // the arithmetic), so the refill barriers below always pair up
-        for (int c = 0; c < nchunks; ++c, ++used) {
+        if constexpr (!BULK) {
+            const float *grow = p + (static_cast<int64_t>(b) * (D + 1) + (TREE ? node : i)) * V;
+            for (int64_t base = sl.begin; base < sl.end; base += kStep * kGUnroll) {
+                float4 x[kGUnroll];
+#pragma unroll
+                for (int u = 0; u < kGUnroll; ++u) {
+                    const int64_t e = base + u * kStep + lane * 4;
+                    x[u] = e < sl.end ? load4(grow, e, sl.end, vec4, -INFINITY)
+                                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                }
+#pragma unroll
+                for (int u = 0; u < kGUnroll; ++u) {
+                    const int e = static_cast<int>(base) + u * kStep + lane * 4;
+                    const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+                    if (e < sl.end && (m4 > best.v || (best.i == INT_MAX && m4 == m4))) {
+                        const int k = x[u].x == m4 ? 0 : x[u].y == m4 ? 1 : x[u].z == m4 ? 2 : 3;
+                        if (e + k < sl.end) best = {m4, e + k};
+                    }
+                }
+            }
+        }
+        // BULK: every thread runs every chunk iteration (a failed wait only
+        // skips the arithmetic), so the refill barriers below always pair up
+        for (int c = 0; BULK && c < nchunks; ++c, ++used) {
             const int slot = static_cast<int>(used % kGSlots);
             if (ok) ok = mbar_wait(&s_full[slot], (used / kGSlots) & 1u, abort, dev_status);
             if (ok) {
@@ -1539,14 +1436,22 @@ int pick_cluster(int V)
     return 1;
 }
 
-template <int CS, bool TREE>
+template <int CS, bool TREE, bool BULK>
 cudaError_t launch_greedy_cs(const float *p, const int32_t *draft, const int32_t *parent, int B, int D,
                              int V, int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
                              bool vec4, cudaStream_t st)
 {
+    const uint32_t smem = BULK ? kGSmem : 0u;
+    if (BULK) {
+        const cudaError_t e = cudaFuncSetAttribute(accept_greedy_kernel<CS, TREE, BULK>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(B) * CS);
     cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1555,32 +1460,21 @@ cudaError_t launch_greedy_cs(const float *p, const int32_t *draft, const int32_t
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, accept_greedy_kernel<CS, TREE>, p, draft, parent, D, V, n_acc, token,
+    return cudaLaunchKernelEx(&cfg, accept_greedy_kernel<CS, TREE, BULK>, p, draft, parent, D, V, n_acc, token,
                               path, dev_status, vec4);
 }
 
-template <int CS, bool TREE>
-cudaError_t launch_greedy_bulk_cs(const float *p, const int32_t *draft, const int32_t *parent, int B, int D,
-                                  int V, int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
-                                  cudaStream_t st)
+template <bool TREE, bool BULK>
+cudaError_t launch_greedy_bulk(const float *p, const int32_t *draft, const int32_t *parent, int B, int D,
+                               int V, int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
+                               bool vec4, cudaStream_t st)
 {
-    cudaError_t e = cudaFuncSetAttribute(accept_greedy_bulk_kernel<CS, TREE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kGSmem));
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(B) * CS);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kGSmem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, accept_greedy_bulk_kernel<CS, TREE>, p, draft, parent, D, V, n_acc, token,
-                              path, dev_status);
+    switch (pick_cluster(V)) {
+    case 8: return launch_greedy_cs<8, TREE, BULK>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
+    case 4: return launch_greedy_cs<4, TREE, BULK>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
+    case 2: return launch_greedy_cs<2, TREE, BULK>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
+    default: return launch_greedy_cs<1, TREE, BULK>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
+    }
 }
 
 template <bool TREE>
@@ -1588,21 +1482,10 @@ cudaError_t launch_greedy(const float *p, const int32_t *draft, const int32_t *p
                           int V, int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
                           cudaStream_t st)
 {
+    // rows staged by bulk copies need 16-byte aligned rows
     const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0);
-    if (vec4) {   // rows staged by bulk copies
-        switch (pick_cluster(V)) {
-        case 8: return launch_greedy_bulk_cs<8, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, st);
-        case 4: return launch_greedy_bulk_cs<4, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, st);
-        case 2: return launch_greedy_bulk_cs<2, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, st);
-        default: return launch_greedy_bulk_cs<1, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, st);
-        }
-    }
-    switch (pick_cluster(V)) {
-    case 8: return launch_greedy_cs<8, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
-    case 4: return launch_greedy_cs<4, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
-    case 2: return launch_greedy_cs<2, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
-    default: return launch_greedy_cs<1, TREE>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
-    }
+    if (vec4) return launch_greedy_bulk<TREE, true>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
+    return launch_greedy_bulk<TREE, false>(p, draft, parent, B, D, V, n_acc, token, path, dev_status, vec4, st);
 }
 
 cudaError_t launch_accept_greedy(const float *p, const int32_t *draft, int B, int D, int V,
