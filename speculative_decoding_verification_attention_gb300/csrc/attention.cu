@@ -47,7 +47,7 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBN = kKeyTile;
 constexpr int kThreads = 384;                 // 12 warps
-constexpr int kCombineThreads = 128;
+constexpr int kCombineThreads = 512;          // 4 threads per row, a quarter of its columns each
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -69,7 +69,7 @@ struct AttnSmem {
 struct PlanShared {
     int64_t total, gbegin, gend, ub0;
     int b0, h0, groups_eff, found;
-    int64_t warp_tot[kThreads / 32];
+    int64_t warp_tot[(kThreads > kCombineThreads ? kThreads : kCombineThreads) / 32];
 };
 
 __device__ __forceinline__ float ex2(float x)
@@ -691,9 +691,14 @@ __global__ void __launch_bounds__(kCombineThreads) attention_combine_kernel(cons
     const int64_t total = ps.total;
     const int g_first = group_of(ub, total, ge);
     const int Hq = a.Hkv * a.G;
-    for (int rl = threadIdx.x; rl < kBM; rl += kCombineThreads) {
+    // four threads per row, each a quarter of its columns: short load chains
+    // and 512 contiguous bytes per row across the four
+    constexpr int kQ = kCombineThreads / kBM;   // threads per row
+    constexpr int kCols = HD / kQ;              // columns per thread
+    const int rl = threadIdx.x / kQ, c0 = (threadIdx.x % kQ) * kCols;
+    {
         const int r = mt * kBM + rl;
-        if (r >= a.R) continue;
+        if (r >= a.R) return;
         const int i = r / a.G, gg = r % a.G;
         float M = -INFINITY;
         for (int q = g_first; q <= g; ++q) {
@@ -703,9 +708,9 @@ __global__ void __launch_bounds__(kCombineThreads) attention_combine_kernel(cons
             M = fmaxf(M, a.part_ml[(static_cast<int64_t>(slot) * a.nt + mt) * kBM + rl].x);
         }
         float lsum = 0.f;
-        float acc[HD];
+        float acc[kCols];
 #pragma unroll
-        for (int c = 0; c < HD; ++c) acc[c] = 0.f;
+        for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
         for (int q = g_first; q <= g; ++q) {
             const int64_t qb = group_begin(total, ge, q), qe = group_begin(total, ge, q + 1);
             if (qb >= qe) continue;
@@ -714,21 +719,21 @@ __global__ void __launch_bounds__(kCombineThreads) attention_combine_kernel(cons
             const float2 ml = a.part_ml[row];
             const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
             lsum += w * ml.y;
-            const float4 *src = reinterpret_cast<const float4 *>(a.part_o + row * HD);
+            const float4 *src = reinterpret_cast<const float4 *>(a.part_o + row * HD + c0);
 #pragma unroll
-            for (int c = 0; c < HD / 4; ++c) {
+            for (int c = 0; c < kCols / 4; ++c) {
                 const float4 v = src[c];
                 acc[4 * c] += w * v.x; acc[4 * c + 1] += w * v.y;
                 acc[4 * c + 2] += w * v.z; acc[4 * c + 3] += w * v.w;
             }
         }
         const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-        float4 *dst = reinterpret_cast<float4 *>(a.out + ((static_cast<int64_t>(b) * (a.D + 1) + i) * Hq + h * a.G + gg) * HD);
+        const int64_t orow = (static_cast<int64_t>(b) * (a.D + 1) + i) * Hq + h * a.G + gg;
+        float4 *dst = reinterpret_cast<float4 *>(a.out + orow * HD + c0);
 #pragma unroll
-        for (int c = 0; c < HD / 4; ++c)
+        for (int c = 0; c < kCols / 4; ++c)
             dst[c] = make_float4(acc[4 * c] * inv, acc[4 * c + 1] * inv, acc[4 * c + 2] * inv, acc[4 * c + 3] * inv);
-        if (a.lse)
-            a.lse[(static_cast<int64_t>(b) * (a.D + 1) + i) * Hq + h * a.G + gg] = (M + __log2f(lsum)) * kLn2;
+        if (a.lse && c0 == 0) a.lse[orow] = (M + __log2f(lsum)) * kLn2;
     }
 }
 
