@@ -207,6 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) { tmem_alloc(tmem_slot, kCols); tmem_relinquish(); }
     plan_group(a, g, &ps);
     __syncthreads();
+    // the merge kernel may be scheduled as CTAs of this grid leave; it waits
+    // for this grid's completion before it reads a partial result
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -691,6 +694,9 @@ __global__ void __launch_bounds__(kCombineThreads) attention_combine_kernel(cons
     const int64_t total = ps.total;
     const int g_first = group_of(ub, total, ge);
     const int Hq = a.Hkv * a.G;
+    // launched as a programmatic dependent of the attention grid: its
+    // partial results are complete and visible only after this wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // four threads per row, each a quarter of its columns: short load chains
     // and 512 contiguous bytes per row across the four
     constexpr int kQ = kCombineThreads / kBM;   // threads per row
@@ -747,8 +753,16 @@ cudaError_t run(const CUtensorMap &tk, const CUtensorMap &tv, const AttnArgs &a,
     k<<<a.groups * a.nt, kThreads, L::kBytes, st>>>(tk, tv, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    attention_combine_kernel<HD><<<dim3(a.groups, a.nt), kCombineThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.groups, a.nt);
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attention_combine_kernel<HD>, a);
 }
 
 }  // namespace
