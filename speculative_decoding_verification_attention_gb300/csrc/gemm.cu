@@ -129,8 +129,20 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // at most one bulk group of this thread still reading its shared source
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-// every bulk group of this thread complete
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// every bulk group of this thread has finished reading its shared source
+// (the writes themselves complete by the end of the grid)
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Column quads of 32-column chunk cc that a cut tile's pieces publish and
+// add: swap tiles have a column per row of x, so only the quads that hold
+// rows m < M; tiled ones all 8.
+template <bool SWAP>
+__device__ __forceinline__ int live_quads(int M, int cc)
+{
+    if (!SWAP) return 8;
+    const int q = (M - cc * 32 + 3) / 4;
+    return q < 8 ? q : 8;
+}
 
 // Write 32 columns (chunk cc) of this warp's 32 tile rows as one bf16 block:
 // staged in the warp's next buffer, then one TMA store by lane 0.  Tiled:
@@ -346,11 +358,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + cc * 32, r);
                     tmem_ld_wait();
+                    const int nq = live_quads<SWAP>(M, cc);
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4)
-                        __stcg(reinterpret_cast<float4 *>(slot + partial_index(cc, q4, row)),
-                               make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
-                                           __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3])));
+                        if (q4 < nq)
+                            __stcg(reinterpret_cast<float4 *>(slot + partial_index(cc, q4, row)),
+                                   make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
+                                               __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3])));
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pub_bar);
@@ -392,15 +406,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 bool go = nred == 0 || mbar_wait(red_empty, (nred - 1) & 1, abort, dev_status);
                                 if (go) {
                                     fence_proxy_async_all();
-                                    mbar_arrive_expect_tx(red_full, (c1 - c0) * others * 32 * kBM * 4);
+                                    uint32_t bytes = 0;
+                                    for (int cc = c0; cc < c1; ++cc) bytes += live_quads<SWAP>(M, cc) * kBM * 16;
+                                    mbar_arrive_expect_tx(red_full, bytes * others);
                                     int k = 0;
                                     for (int v = f; v <= l; ++v) {
                                         if (v == me) continue;
                                         const float *src = part + static_cast<size_t>(
                                             piece_slot(v, rank, v != f || other_first(grid, f, s.t), kUnit)) * kBM * BN;
+                                        // a unit's quads are its outer index: the live ones are its first bytes
                                         for (int cc = c0; cc < c1; ++cc)
                                             bulk_load(smem + ((cc - c0) * others + k) * 32 * kBM * 4,
-                                                      src + cc * 32 * kBM, 32 * kBM * 4, red_full);
+                                                      src + cc * 32 * kBM, live_quads<SWAP>(M, cc) * kBM * 16, red_full);
                                         ++k;
                                     }
                                 }
@@ -424,17 +441,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         pv[q4] = make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
                                                              __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
                                 } else {
+                                    // columns past the live quads are rows m >= M, never stored
+                                    const int nq = live_quads<SWAP>(M, cc);
                                     if (ring_ok) {
                                         const float *u = ring + ((cc - c0) * others + k) * 32 * kBM;
 #pragma unroll
                                         for (int q4 = 0; q4 < 8; ++q4)
-                                            pv[q4] = *reinterpret_cast<const float4 *>(u + unit_index(q4, row));
+                                            pv[q4] = q4 < nq ? *reinterpret_cast<const float4 *>(u + unit_index(q4, row))
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
                                     } else {
                                         const float *src = part + static_cast<size_t>(piece_slot(
                                             v, rank, v != f || other_first(grid, f, s.t), kUnit)) * kBM * BN;
 #pragma unroll
                                         for (int q4 = 0; q4 < 8; ++q4)
-                                            pv[q4] = __ldcg(reinterpret_cast<const float4 *>(src + partial_index(cc, q4, row)));
+                                            pv[q4] = q4 < nq ? __ldcg(reinterpret_cast<const float4 *>(src + partial_index(cc, q4, row)))
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
                                     }
                                     ++k;
                                 }
@@ -466,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&acc_empty[ab]);
             ++lt;
         }
-        if (lane == 0) bulk_wait_all();   // output stores done before the CTA may exit
+        if (lane == 0) bulk_wait_read_all();   // staged output read before the CTA's shared memory goes
     }
     __syncwarp();
     __syncthreads();

@@ -58,6 +58,20 @@ def test_full_compare_small(sv, oracle_lib, M, N, K):
     check(y, oracle_lib.gemm(x, w))
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 6144, 512), (8, 6144, 640), (32, 6144, 64), (33, 6272, 640),
+                                   (64, 6144, 576), (128, 6272, 512), (17, 384, 192), (100, 19456, 640),
+                                   (5, 19584, 512), (24, 6272, 6144)])
+def test_weight_streaming_full_compare(sv, oracle_lib, M, N, K):
+    """Small-M weight streaming over the full width of the verify layer
+    (and widths around it): every output against the oracle, so every
+    128-row w tile, including the fp32 partials of tiles whose k-blocks are
+    cut between CTAs, of which only the columns that hold rows of x are
+    published and added."""
+    x, w = synth.gemm_inputs(M * 7 + N + K, M, N, K)
+    y, _ = run(sv, x, w)
+    check(y, oracle_lib.gemm(x, w))
+
+
 def sample_entries(rng, M, N, n=3000):
     m = rng.integers(0, M, n)
     c = rng.integers(0, N, n)
