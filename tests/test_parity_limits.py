@@ -1,0 +1,100 @@
+"""Parity at the edges of the supported set, against the oracle.
+
+The other parity tests stay at 1 + D <= 16 and G(1+D) <= 512 query rows per
+KV head; the entry points accept 1 + D <= 64 and G(1+D) <= 1024 (eight
+128-row MMA tiles reading the same K/V stream).  These cases sit on those
+limits: the longest draft with a single query head per KV head, the largest
+row count reached both through D and through G, and acceptance walking all
+63 draft rows.  Tolerances as in the dedicated tests (attention max-abs 2e-2
+and relative L2 1e-3; acceptance bit-exact except draws within 1e-6 of a
+CDF boundary).
+"""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+MARGIN = 1e-6
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from speculative_decoding_verification_attention_gb300 import _build
+    _build.build()
+    import speculative_decoding_verification_attention_gb300 as m
+    m.library()
+    return m
+
+
+def bits_dev(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def to_dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.mark.parametrize("B,Hkv,G,d,D,kv_len,page", [
+    (2, 2, 1, 128, 63, [64, 700], 64),      # 1 + D = 64, kv_len = 1 + D: the whole cache is drafts
+    (1, 1, 16, 128, 63, [300], 32),         # G(1+D) = 1024: eight m-tiles
+    (2, 1, 32, 64, 31, [33, 513], 16),      # G(1+D) = 1024 through the group size
+    (3, 2, 5, 128, 40, [41, 170, 999], 48), # 205 rows: two m-tiles, the second mostly padding
+])
+def test_attention_at_the_limits(sv, oracle_lib, B, Hkv, G, d, D, kv_len, page):
+    import torch
+    inp = synth.attention_inputs(B * 100 + D, B, Hkv, G, d, D, kv_len, page_size=page)
+    lse = torch.empty((B, D + 1, Hkv * G), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = sv.verify_attention(bits_dev(inp.q), bits_dev(inp.k_pages), bits_dev(inp.v_pages),
+                              to_dev(inp.block_table), to_dev(inp.kv_len), D, Hkv, G, lse=lse,
+                              dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref, lse_ref = oracle_lib.verify_attention(inp.q, inp.k_pages, inp.v_pages, inp.block_table, inp.kv_len,
+                                               D, Hkv, G, d, page)
+    o = out.cpu().numpy().astype(np.float64)
+    err = o - ref
+    assert np.isfinite(o).all()
+    assert np.abs(err).max() <= 2e-2, np.abs(err).max()
+    assert np.linalg.norm(err) <= 1e-3 * np.linalg.norm(ref)
+    assert np.abs(lse.cpu().numpy().astype(np.float64) - lse_ref).max() <= 2e-2
+
+
+def test_beyond_the_limits_is_unsupported(sv):
+    """1 + D = 65, or G(1+D) = 1040 rows: rejected on the host."""
+    import torch
+    from speculative_decoding_verification_attention_gb300 import SpecError
+    for G, D in ((1, 64), (16, 64), (40, 25)):
+        inp = synth.attention_inputs(7, 1, 1, G, 64, min(D, 63), [D + 1], page_size=16)
+        q = torch.zeros((1, D + 1, G, 64), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(SpecError):
+            sv.verify_attention(q, bits_dev(inp.k_pages), bits_dev(inp.v_pages),
+                                to_dev(inp.block_table), to_dev(np.array([D + 1], np.int32)), D, 1, G)
+
+
+@pytest.mark.parametrize("V", [1000, 40000])
+def test_acceptance_walks_63_drafts(sv, oracle_lib, V):
+    """D = 63 with drafts close to the target, so most sequences accept long
+    prefixes (some all 63): greedy and stochastic acceptance bit-exact."""
+    import torch
+    B, D = 6, 63
+    inp = synth.accept_inputs(300 + V % 97, B, D, V, target_std=2.0, draft_noise=0.02, mode="both")
+    p = inp["p"]
+    n, t = sv.accept_greedy(to_dev(p), to_dev(inp["draft_greedy"]))
+    torch.cuda.synchronize()
+    n_ref, t_ref = oracle_lib.accept_greedy(p, inp["draft_greedy"])
+    assert np.array_equal(n.cpu().numpy(), n_ref) and np.array_equal(t.cpu().numpy(), t_ref)
+    assert n_ref.max() >= 32            # long accepted prefixes are exercised
+    n, t = sv.accept_sample(to_dev(p), to_dev(inp["q"]), to_dev(inp["draft"]), to_dev(inp["u_acc"]),
+                            to_dev(inp["u_res"]))
+    torch.cuda.synchronize()
+    n_ref, t_ref, margin, _ = oracle_lib.accept_sample(p, inp["q"], inp["draft"], inp["u_acc"], inp["u_res"])
+    bad = (n.cpu().numpy() != n_ref) | (t.cpu().numpy() != t_ref)
+    assert not (bad & (margin >= MARGIN)).any()
+    assert n_ref.max() >= 32
