@@ -3,7 +3,8 @@ attention, GEMM, greedy, stochastic and tree acceptance, acceptance from
 logits), against the oracle.
 
 Each case draws its shape from a fixed seed inside the supported set --
-group size, draft length (1 + D <= 64, G(1+D) up to 512 rows), head_dim,
+group size, draft length (1 + D <= 16, G(1+D) up to 512 rows; the limits
+of the supported set have their own cases in test_parity_limits.py), head_dim,
 page size (multiples of 16), ragged lengths down to 1 + D; vocabulary sizes
 with and without 16-byte rows; GEMM shapes with ragged M -- so that
 combinations the hand-written cases do not name are still compared.  The
