@@ -4,8 +4,8 @@ The other parity tests stay at 1 + D <= 16 and G(1+D) <= 512 query rows per
 KV head; the entry points accept 1 + D <= 64 and G(1+D) <= 1024 (eight
 128-row MMA tiles reading the same K/V stream).  These cases sit on those
 limits: the longest draft with a single query head per KV head, the largest
-row count reached both through D and through G, and acceptance walking all
-63 draft rows.  Tolerances as in the dedicated tests (attention max-abs 2e-2
+row count reached both through D and through G, acceptance walking all 63
+draft rows, and draft trees of 64 nodes (full 64-bit ancestor masks).  Tolerances as in the dedicated tests (attention max-abs 2e-2
 and relative L2 1e-3; acceptance bit-exact except draws within 1e-6 of a
 CDF boundary).
 """
@@ -98,3 +98,47 @@ def test_acceptance_walks_63_drafts(sv, oracle_lib, V):
     bad = (n.cpu().numpy() != n_ref) | (t.cpu().numpy() != t_ref)
     assert not (bad & (margin >= MARGIN)).any()
     assert n_ref.max() >= 32
+
+
+@pytest.mark.parametrize("kind", ["random", "chain", "star"])
+def test_tree_attention_with_64_nodes(sv, oracle_lib, kind):
+    """Draft trees of 64 nodes (the 64-bit ancestor masks are full):
+    G(1+D) = 256 rows, ragged lengths down to 1 + D."""
+    import torch
+    B, Hkv, G, d, D, page = 3, 2, 4, 128, 63, 32
+    inp = synth.attention_inputs(40 + len(kind), B, Hkv, G, d, D, [64, 130, 900], page_size=page)
+    parent = synth.tree_parents(50 + len(kind), B, 1 + D, kind)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = sv.verify_tree_attention(bits_dev(inp.q), bits_dev(inp.k_pages), bits_dev(inp.v_pages),
+                                   to_dev(inp.block_table), to_dev(inp.kv_len), to_dev(parent), D, Hkv, G,
+                                   dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref, _ = oracle_lib.tree_attention(inp.q, inp.k_pages, inp.v_pages, inp.block_table, inp.kv_len, parent,
+                                       D, Hkv, G, d, page)
+    err = out.cpu().numpy().astype(np.float64) - ref
+    assert np.abs(err).max() <= 2e-2
+    assert np.linalg.norm(err) <= 1e-3 * np.linalg.norm(ref)
+
+
+def test_tree_greedy_with_64_nodes(sv, oracle_lib):
+    """Greedy tree acceptance over random 64-node trees whose nodes mostly
+    carry the target's choice after their parent (deep accepted paths)."""
+    import torch
+    rng = np.random.default_rng(77)
+    B, D, V = 8, 63, 4099
+    p = synth.accept_inputs(78, B, D, V, mode="greedy")["p"]
+    parent = synth.tree_parents(79, B, 1 + D, "random")
+    am = np.argmax(p, axis=2)
+    tokens = rng.integers(0, V, size=(B, 1 + D)).astype(np.int32)
+    hit = rng.random((B, 1 + D)) < 0.9
+    for b in range(B):
+        for k in range(1, 1 + D):
+            if hit[b, k]:
+                tokens[b, k] = am[b, parent[b, k]]
+    n, t, path = sv.accept_tree_greedy(to_dev(p), to_dev(tokens), to_dev(parent))
+    torch.cuda.synchronize()
+    n_ref, t_ref, path_ref = oracle_lib.accept_tree_greedy(p, tokens, parent)
+    assert np.array_equal(n.cpu().numpy(), n_ref)
+    assert np.array_equal(t.cpu().numpy(), t_ref) and np.array_equal(path.cpu().numpy(), path_ref)
+    assert n_ref.max() >= 4
