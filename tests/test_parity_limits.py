@@ -4,8 +4,9 @@ The other parity tests stay at 1 + D <= 16 and G(1+D) <= 512 query rows per
 KV head; the entry points accept 1 + D <= 64 and G(1+D) <= 1024 (eight
 128-row MMA tiles reading the same K/V stream).  These cases sit on those
 limits: the longest draft with a single query head per KV head, the largest
-row count reached both through D and through G, acceptance walking all 63
-draft rows, and draft trees of 64 nodes (full 64-bit ancestor masks).  Tolerances as in the dedicated tests (attention max-abs 2e-2
+row count reached both through D and through G, acceptance (lossless and
+AdaSD) walking 63 draft rows, and draft trees of 64 nodes (full 64-bit
+ancestor masks).  Tolerances as in the dedicated tests (attention max-abs 2e-2
 and relative L2 1e-3; acceptance bit-exact except draws within 1e-6 of a
 CDF boundary).
 """
@@ -142,3 +143,31 @@ def test_tree_greedy_with_64_nodes(sv, oracle_lib):
     assert np.array_equal(n.cpu().numpy(), n_ref)
     assert np.array_equal(t.cpu().numpy(), t_ref) and np.array_equal(path.cpu().numpy(), path_ref)
     assert n_ref.max() >= 4
+
+
+def test_adasd_over_63_drafts(sv, oracle_lib):
+    """AdaSD relaxed acceptance with D = 63: entropy stop at the 90th
+    percentile of the draft entropies (so stops fall deep in the draft),
+    Jensen-Shannon threshold at the median; statistics within their
+    tolerances, decisions bit-exact except draws within the margins the
+    dedicated AdaSD tests use (uniform 1e-6, statistic 5e-4)."""
+    import torch
+    B, D, V = 12, 63, 3000
+    inp = synth.accept_inputs(63, B, D, V, target_std=2.5, draft_noise=0.3, mode="sample")
+    p, q = inp["p"], inp["q"]
+    H_ref, JS_ref = oracle_lib.adasd_stats(p, q)
+    tau_h = float(np.quantile(H_ref, 0.9)) + 1e-3
+    tau_js = float(np.quantile(JS_ref, 0.5)) + 1e-3
+    n, t, de, H, JS = [o.cpu().numpy() for o in sv.accept_adasd(
+        to_dev(p), to_dev(q), to_dev(inp["draft"]), to_dev(inp["u_acc"]), to_dev(inp["u_res"]), tau_h, tau_js)]
+    torch.cuda.synchronize()
+    assert (np.abs(H - H_ref) <= 1e-5 * (1 + H_ref)).all()
+    jsd, jsd_ref = JS.astype(np.float64) ** 2, JS_ref ** 2
+    assert (np.abs(jsd - jsd_ref) <= 2e-6 + 1e-5 * jsd_ref).all()
+    n_ref, t_ref, de_ref, mu, ms, _ = oracle_lib.accept_adasd(p, q, inp["draft"], inp["u_acc"], inp["u_res"],
+                                                             tau_h, tau_js)
+    close = (mu < 1e-6) | (ms < 5e-4)
+    bad = (n != n_ref) | (t != t_ref) | (de != de_ref)
+    assert not (bad & ~close).any()
+    assert (n <= de).all() and (de <= D).all()
+    assert de_ref.max() >= 8
