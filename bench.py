@@ -575,6 +575,9 @@ def case_lines(args):
             attention_case(f"large-group B8 G32 L131072 D{D}", 8, 4, 32, D, 131072, 20 + D)
     if args.workload == "attention-small":
         attention_case("small B4 L32768 D7 (profiling)", 4, 8, 8, 7, 32768, 5)
+    if args.workload == "attention-small-d15":
+        # G(1+D) = 128: one full query tile per KV head, 537 MB of K/V
+        attention_case("small B4 L32768 D15 (profiling)", 4, 8, 8, 15, 32768, 6)
     if args.workload == "attention-largeg-small":
         # the large-group case at B=1: 4 KV heads x G=32, L=131072, D=15 (G(1+D) = 512,
         # four 128-row tiles per KV head), 268 MB of K/V, for profiler captures
@@ -869,7 +872,7 @@ def main():
     ap.add_argument("--workload", default="step",
                     choices=["step", "attention", "dsweep", "gemm", "accept", "all", "attention-small", "tree",
                              "attention-largeg-small",
-                             "adaptive", "logits", "adasd", "logits-small", "adasd-small",
+                             "adaptive", "logits", "adasd", "logits-small", "adasd-small", "attention-small-d15",
                              "accept-one"],
                     help="step: the headline line; others print one secondary JSON line per case")
     args = ap.parse_args()
