@@ -392,8 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok && *s_last) {
                     // other pieces' partials: through the stage ring with bulk
                     // copies when this is the unit's last segment (the ring is
-                    // idle then), else straight from L2
-                    const bool ring_ok = !wk.has_more();
+                    // idle then) and they are large, else straight from L2 (a
+                    // swap tile with one 32-column chunk holds a few KB per
+                    // piece: plain loads save the copies' barrier round trip)
+                    const bool ring_ok = !wk.has_more() && !(SWAP && nchunks == 1);
                     const float *ring = reinterpret_cast<const float *>(smem);
                     const int others = l - f;
                     const int per_pass_chunks =
