@@ -1,16 +1,15 @@
-"""Host logic of bench.py's multi-rank (replica) path, on CPU with gloo.
+"""bench.py under torchrun on CPU.
 
-The verification step shards into independent replicas, so the only
-cross-rank work is the timing reduction (max over ranks) and the reference
-arm's rank-0-only run.  No GPU is involved.
+The verification path runs on one GPU and has no multi-GPU arm: with more
+than one rank the GPU arm must print one "unavailable" line and launch
+nothing, and the reference arm (the oracle on the host cores) runs on rank 0
+alone while the other ranks exit without work.  No GPU is involved.
 """
 import json
 import os
 import socket
 import subprocess
 import sys
-
-import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -21,52 +20,44 @@ def free_port():
         return s.getsockname()[1]
 
 
-def _worker(rank, world, port, q):
-    import torch.distributed as dist
-    sys.path.insert(0, ROOT)
-    import bench
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
-    try:
-        m = bench.max_over_ranks(1.5 + rank, world)
-        q.put((rank, m, bench.aggregate_throughput(512, m, world)))
-    finally:
-        dist.destroy_process_group()
+def torchrun(*bench_args, timeout=600):
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), "bench.py", *bench_args]
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    return subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=timeout, env=env)
 
 
-def test_max_over_ranks_and_aggregate_with_gloo():
-    import torch.multiprocessing as mp
-    ctx = mp.get_context("spawn")
-    q = ctx.Queue()
-    port = free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
-    for p in procs:
-        p.start()
-    got = [q.get(timeout=120) for _ in procs]
-    for p in procs:
-        p.join(timeout=60)
-        assert p.exitcode == 0
-    for rank, m, v in got:
-        assert m == 2.5                       # the slowest rank's step time
-        assert abs(v - 512 * 2 / 2.5e-3) < 1e-6
+def json_lines(out):
+    return [json.loads(l) for l in out.splitlines() if l.startswith("{")]
 
 
-def test_single_rank_reduction_is_identity():
-    sys.path.insert(0, ROOT)
-    import bench
-    assert bench.max_over_ranks(3.25, 1) == 3.25
-    assert bench.aggregate_throughput(512, 2.0, 1) == 256000.0
+def test_gpu_arm_refuses_more_than_one_rank():
+    r = torchrun("--gpus", "2", "--steps", "1", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = json_lines(r.stdout)
+    assert len(lines) == 1
+    assert "unavailable" in lines[0] and lines[0]["n_gpus"] == 2
+    assert "value" not in lines[0]
+
+
+def test_gpu_arm_refuses_gpus_flag_without_torchrun():
+    r = subprocess.run([sys.executable, "bench.py", "--gpus", "4", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300,
+                       env=dict(os.environ, CUDA_VISIBLE_DEVICES=""))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = json_lines(r.stdout)
+    assert len(lines) == 1 and "unavailable" in lines[0]
 
 
 def test_reference_arm_under_torchrun_prints_one_line():
-    port = free_port()
-    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
-           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
-           "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--cpu-budget-s", "0.3"]
-    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    r = torchrun("--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
+                 "--cpu-budget-s", "0.3")
     assert r.returncode == 0, r.stderr[-2000:]
-    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    lines = json_lines(r.stdout)
     assert len(lines) == 1
-    d = json.loads(lines[0])
+    d = lines[0]
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # the step time is extrapolated from a bounded sample, and says so
+    assert d["ms_per_step_kind"].startswith("extrapolated")
+    assert 0 < d["sampled_s_per_step"] < d["ms_per_step"] * 1e-3
