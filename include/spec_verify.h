@@ -172,22 +172,28 @@ spec_status_t spec_verify_attention_noalloc(const void *q_bf16, const void *k_pa
  *   w_bf16   device, bf16 [N][K] row-major (nn.Linear weight layout),
  *            16-byte aligned.
  *   y_bf16   device, bf16 [M][N] row-major, 16-byte aligned.
+ *   dev_status  device uint32 or NULL: SPEC_DEV_ERR_TIMEOUT (a bounded wait
+ *            expired; y is then incomplete) or SPEC_DEV_ERR_LAUNCH.
  * Supported set: 1 <= M <= 65536, N a multiple of 128, K a multiple of 64.
- * workspace: spec_verify_gemm_workspace_size(M, N, K) bytes of device
- * memory, 256-byte aligned, owned by the caller.  It holds the arrival
- * counters of the tiles cut between CTAs (the first 4096 bytes) and the
- * fp32 partial tiles of the stream-K split: zero it once before its first
- * use (cudaMemset); every call that completes leaves the counters zero
- * again, also under CUDA-graph replay.  Calls that share a
- * workspace must not overlap in time.  A smaller workspace returns
- * SPEC_ERR_WORKSPACE.  The size depends on the current device's SM count
- * (without a device it is sized for 256 SMs).
+ * M <= 256 (weight streaming) splits the K range of each 128-row block of
+ * w between CTAs and adds the pieces through the workspace:
+ * spec_verify_gemm_workspace_size(M, N, K) bytes of device memory,
+ * 256-byte aligned, owned by the caller.  It holds the arrival counters of
+ * the tiles cut between CTAs (the first 4096 bytes) and the fp32 partial
+ * tiles: zero it once before its first use (cudaMemset); every call that
+ * completes leaves the counters zero again, also under CUDA-graph replay.
+ * A call that sets any dev_status bit may leave counters non-zero: zero the
+ * workspace again before the next call.  Calls that share a workspace must
+ * not overlap in time.  A smaller workspace returns SPEC_ERR_WORKSPACE.
+ * M > 256 (pairs of CTAs sharing each MMA, whole tiles) needs no workspace
+ * (its size is 0 and workspace may be NULL).  The size depends on the
+ * current device's SM count (without a device it is sized for 256 SMs).
  * ---------------------------------------------------------------------- */
 size_t spec_verify_gemm_workspace_size(int M, int N, int K);
 
 spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_bf16, int M,
                                int N, int K, void *workspace, size_t workspace_bytes,
-                               void *stream);
+                               uint32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
  * Greedy acceptance.
@@ -410,23 +416,48 @@ int spec_verify_attention_plan(int B, const int32_t *kv_len_host, int D, int Hkv
  * on the pages; launches nothing, needs no device).
  *
  * The work is split into units over at most num_sms SMs, one CTA per SM.
- *  - M > 256: a unit is a pair of CTAs (a thread-block cluster of 2); pair
- *    tile t covers output rows (t % tiles_mp) * 256 and columns
- *    (t / tiles_mp) * BN, tiles_mp = ceil(ceil(M / 128) / 2), 128 rows per
- *    CTA, both CTAs sharing each w tile.
+ *  - M > 256: a unit is a pair of CTAs (a thread-block cluster of 2) that
+ *    runs one MMA of 256 rows; output tile t covers rows
+ *    (t % tiles_m) * 256 .. + 255, tiles_m = ceil(M / 256), and column tile
+ *    t / tiles_m.  The N columns are cut into tiles_n column tiles, in
+ *    32-column units, whose widths differ by at most 32 (the wider ones
+ *    first); pair c takes tiles c, c + pairs, ... whole (all k-blocks).
  *  - M <= 256: a unit is one CTA; tile t covers the 128 w rows (output
  *    columns) t * 128 .. t * 128 + 127 for all M rows, which are padded to
- *    BN in {32, 64, 128, 256} on the MMA side.
- * Each unit walks a list of segments (a tile and a range [kb0, kb1) of its
- * 64-wide k-blocks).  Writes, for each segment in unit order, the row
- * (unit, tile, kb0, kb1, last, BN) into segments[6 * i ..] (int32, host
- * memory), where last is, for a segment with kb0 == 0, the last unit
- * holding a later piece of the same tile (the unit itself when the tile is
- * whole), and -1 otherwise.  Returns the number of segments (rows beyond
- * max_segments are counted, not written), or -1 for invalid arguments.
+ *    BN in {32, 64, 128, 256} on the MMA side.  Each unit walks a list of
+ *    segments (a tile and a range [kb0, kb1) of its 64-wide k-blocks).
+ * Writes, for each segment in unit order, the row (unit, tile, kb0, kb1,
+ * last, BN) into segments[6 * i ..] (int32, host memory), where last is,
+ * for a segment with kb0 == 0, the last unit holding a later piece of the
+ * same tile (the unit itself when the tile is whole), and -1 otherwise, and
+ * BN is the tile's width (M > 256) or the padded rows of x (M <= 256).
+ * Returns the number of segments (rows beyond max_segments are counted, not
+ * written), or -1 for invalid arguments.
  * ---------------------------------------------------------------------- */
 int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments,
                           int max_segments);
+
+/* ------------------------------------------------------------------------
+ * Self-test of the bounded device wait (no counterpart on the pages).
+ *
+ * Every mbarrier wait in the library's kernels is bounded: when it runs out
+ * the kernel ORs SPEC_DEV_ERR_TIMEOUT into *dev_status, stops its other
+ * roles, waits (bounded) for its own copies and MMAs in flight and returns,
+ * so the CUDA context stays usable.  This entry point runs that same wait
+ * in a one-CTA kernel so that a test can make it run out on purpose:
+ * warp 0 waits on an mbarrier, limited to wait_limit_ns; one thread of
+ * warp 1 arrives on it after arrive_after_ns, or never when
+ * arrive_after_ns is UINT64_MAX.  No copy or MMA is in flight.
+ *   result     device, uint64 [3], 8-byte aligned: [0] 1 if the wait saw the
+ *              barrier complete, 0 if it gave up; [1] the kernel's abort flag
+ *              after the wait; [2] how long the wait took, in ns.
+ *   dev_status device uint32 or NULL: SPEC_DEV_ERR_TIMEOUT when it gave up.
+ * 0 < wait_limit_ns <= 10 s and arrive_after_ns <= 10 s (or UINT64_MAX),
+ * else SPEC_ERR_INVALID_ARG; the kernel ends within about
+ * max(wait_limit_ns, arrive_after_ns).
+ * ---------------------------------------------------------------------- */
+spec_status_t spec_selftest_bounded_wait(uint64_t wait_limit_ns, uint64_t arrive_after_ns,
+                                         uint64_t *result, uint32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------
  * Adaptive draft length (host only; no counterpart kernels).

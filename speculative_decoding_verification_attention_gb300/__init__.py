@@ -22,7 +22,7 @@ __all__ = [
     "gemm_workspace_size", "gemm_plan", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
     "verify_tree_attention", "tree_attention_workspace_size", "accept_tree_greedy",
     "AdaptiveDraftLength", "accept_sample_logits", "accept_sample_logits_workspace_size",
-    "accept_adasd", "accept_adasd_workspace_size",
+    "accept_adasd", "accept_adasd_workspace_size", "selftest_bounded_wait",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -36,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "spec_verify_tree_attention_workspace_size", "spec_verify_tree_attention",
     "spec_accept_tree_greedy", "spec_adaptive_init", "spec_adaptive_update", "spec_adaptive_draft_len",
     "spec_accept_sample_logits_workspace_size", "spec_accept_sample_logits",
-    "spec_accept_adasd_workspace_size", "spec_accept_adasd",
+    "spec_accept_adasd_workspace_size", "spec_accept_adasd", "spec_selftest_bounded_wait",
 )
 
 DEV_STATUS_BITS = {
@@ -82,7 +82,7 @@ def library():
             lib.spec_verify_attention.restype = I
             lib.spec_verify_gemm_workspace_size.argtypes = [I, I, I]
             lib.spec_verify_gemm_workspace_size.restype = S
-            lib.spec_verify_gemm.argtypes = [P, P, P, I, I, I, P, S, P]
+            lib.spec_verify_gemm.argtypes = [P, P, P, I, I, I, P, S, P, P]
             lib.spec_verify_gemm.restype = I
             lib.spec_accept_greedy.argtypes = [P, P, I, I, I, P, P, P, P]
             lib.spec_accept_greedy.restype = I
@@ -119,6 +119,9 @@ def library():
             lib.spec_accept_adasd_workspace_size.restype = S
             lib.spec_accept_adasd.argtypes = [P, P, P, P, P, F, F, I, I, I, P, P, P, P, P, P, S, P, P]
             lib.spec_accept_adasd.restype = I
+            U64 = ctypes.c_uint64
+            lib.spec_selftest_bounded_wait.argtypes = [U64, U64, P, P, P]
+            lib.spec_selftest_bounded_wait.restype = I
             _lib = lib
     return _lib
 
@@ -265,12 +268,14 @@ def gemm_plan(M, N, K, num_sms):
     return seg[:n]
 
 
-def verify_gemm(x, w, y=None, workspace=None, stream=None):
+def verify_gemm(x, w, y=None, workspace=None, dev_status=None, stream=None):
     """y[M, N] (bf16) = x[M, K] @ w[N, K]^T with fp32 accumulation.
 
-    ``workspace`` (uint8, ``gemm_workspace_size(M, N, K)`` bytes) must be
-    zero-filled before its first use; every call leaves it ready for the
-    next.  Without one, a zeroed workspace is allocated for this call.
+    ``workspace`` (uint8, ``gemm_workspace_size(M, N, K)`` bytes; 0 for
+    M > 256) must be zero-filled before its first use; every call that
+    completes leaves it ready for the next (zero it again after a call that
+    set a ``dev_status`` bit).  Without one, a zeroed workspace is allocated
+    for this call.
     """
     import torch
     M, K = x.shape
@@ -285,7 +290,8 @@ def verify_gemm(x, w, y=None, workspace=None, stream=None):
     st = library().spec_verify_gemm(
         _dev(x, "x", torch.bfloat16), _dev(w, "w", torch.bfloat16), _dev(y, "y", torch.bfloat16),
         M, N, K, _dev(workspace, "workspace", allow_none=True),
-        0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream))
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
     _check(st, "spec_verify_gemm")
     return y
 
@@ -434,6 +440,22 @@ def accept_adasd(p, q, draft, u_acc, u_res, tau_entropy, tau_js, n_accepted=None
         _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
     _check(st, "spec_accept_adasd")
     return n_accepted, token, draft_len, entropy, js_distance
+
+
+# ------------------------------------------------------------ self-test
+def selftest_bounded_wait(wait_limit_ns, arrive_after_ns=None, dev_status=None, stream=None):
+    """Run the library's bounded mbarrier wait once on the device
+    (spec_selftest_bounded_wait): limited to ``wait_limit_ns``, on a barrier
+    that is arrived on after ``arrive_after_ns`` (never when None).  Returns
+    the device int64 tensor [completed, abort flag, wait duration in ns]."""
+    import torch
+    res = torch.zeros(3, dtype=torch.int64, device="cuda")
+    after = 0xFFFFFFFFFFFFFFFF if arrive_after_ns is None else int(arrive_after_ns)
+    st = library().spec_selftest_bounded_wait(int(wait_limit_ns), after, _dev(res, "result"),
+                                               _dev(dev_status, "dev_status", allow_none=True),
+                                               _stream(stream))
+    _check(st, "spec_selftest_bounded_wait")
+    return res
 
 
 # ------------------------------------------------------------ adaptive draft length

@@ -354,6 +354,24 @@ int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments, i
         return -1;
     const GemmPlan plan = plan_gemm(M, N, K, num_sms, num_sms / 2);
     int n = 0;
+    if (!plan.swap) {
+        // pairs: whole tiles, pair c taking tiles c, c + pairs, ...
+        const PairGrid &g = plan.pg;
+        for (int c = 0; c < g.pairs; ++c)
+            for (int t = c; t < g.tiles(); t += g.pairs) {
+                if (n < max_segments) {
+                    int32_t *r = segments + 6 * static_cast<size_t>(n);
+                    r[0] = c;
+                    r[1] = t;
+                    r[2] = 0;
+                    r[3] = g.kblocks;
+                    r[4] = c;
+                    r[5] = g.width(t / g.tiles_m);
+                }
+                ++n;
+            }
+        return n;
+    }
     for (int c = 0; c < plan.sk.G; ++c) {
         SegWalker wk(plan.sk, c);
         Seg s;
@@ -374,7 +392,8 @@ int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments, i
 }
 
 spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_bf16, int M, int N,
-                               int K, void *workspace, size_t workspace_bytes, void *stream)
+                               int K, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                               void *stream)
 {
     if (M < 0 || N < 0 || K < 0) return SPEC_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return SPEC_OK;
@@ -389,27 +408,11 @@ spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_b
     const GemmPlan probe = plan_gemm(M, N, K, sms, sms / 2);
     const int units = gemm_max_units(probe.bn, probe.swap);
     if (units <= 0) return SPEC_ERR_CUDA;
-    const GemmPlan plan = plan_gemm(M, N, K, probe.swap ? units : sms,
-                                    probe.swap ? sms / 2 : units);
-    if (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 256))
+    const GemmPlan plan = plan_gemm(M, N, K, probe.swap ? units : sms, probe.swap ? sms / 2 : units);
+    if (plan.workspace_bytes > 0 &&
+        (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 256)))
         return SPEC_ERR_WORKSPACE;
-    CUtensorMap tx, tw;
-    const uint64_t dx[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
-    const uint64_t dw[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
-    const uint64_t st[1] = {static_cast<uint64_t>(K) * 2};
-    // swap: x padded to bn rows, 128-row w tiles; tiled: 128-row x tiles,
-    // each CTA of a pair loading half of the w tile (multicast to both)
-    const uint32_t bx[2] = {64, static_cast<uint32_t>(plan.swap ? plan.bn : 128)};
-    const uint32_t bw[2] = {64, static_cast<uint32_t>(plan.swap ? 128 : plan.bn / 2)};
-    // y: 32 x 32 output blocks staged in shared memory, written by TMA stores
-    CUtensorMap ty;
-    const uint64_t dy[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
-    const uint64_t sy[1] = {static_cast<uint64_t>(N) * 2};
-    const uint32_t by[2] = {32, 32};
-    if (!encode_bf16_tmap(&tx, x_bf16, 2, dx, st, bx) || !encode_bf16_tmap(&tw, w_bf16, 2, dw, st, bw) ||
-        !encode_bf16_tmap_plain(&ty, y_bf16, 2, dy, sy, by))
-        return SPEC_ERR_CUDA;
-    return from_cuda(launch_gemm(plan, tx, tw, ty, y_bf16, M, N, workspace, nullptr,
+    return from_cuda(launch_gemm(plan, x_bf16, w_bf16, y_bf16, M, N, K, workspace, dev_status,
                                  static_cast<cudaStream_t>(stream)));
 }
 

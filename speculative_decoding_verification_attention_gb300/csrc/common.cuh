@@ -97,9 +97,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 
 // Wait for the phase with the given parity to complete.  Returns false if
 // *abort becomes non-zero (another role gave up) or the wait exceeds
-// kWaitTimeoutNs (then *abort is set and SPEC_DEV_ERR_TIMEOUT recorded).
+// limit_ns (then *abort is set and SPEC_DEV_ERR_TIMEOUT recorded).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          uint32_t *dev_status)
+                                          uint32_t *dev_status,
+                                          unsigned long long limit_ns = kWaitTimeoutNs)
 {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
@@ -108,7 +109,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 report(dev_status, SPEC_DEV_ERR_TIMEOUT);
                 return false;
@@ -121,9 +122,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 // tcgen05 instructions: the result is made uniform across the warp, so no
 // lane can proceed to a collective op that another lane has abandoned.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                               uint32_t *dev_status)
+                                               uint32_t *dev_status,
+                                               unsigned long long limit_ns = kWaitTimeoutNs)
 {
-    const bool ok = mbar_wait(bar, parity, abort, dev_status);
+    const bool ok = mbar_wait(bar, parity, abort, dev_status, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -156,19 +158,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-
-// Tiled 2-D load written to the same shared offset of every CTA in cta_mask
-// (this cluster); each destination's mbarrier at bar's offset receives the
-// byte count.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const void *tmap, uint64_t *bar,
-                                                      int x, int y, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
         : "memory");
 }
 
@@ -266,12 +255,85 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
         : "memory");
 }
 
-// Arrive on the mbarrier at the same shared offset in every CTA of cta_mask
-// (this cluster) once the MMAs issued so far have completed.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
+// ------------------------------------------------- CTA pairs (cta_group::2)
+// A pair of CTAs (a cluster of 2) shares one tcgen05.mma of M = 256: the
+// even CTA issues it, each CTA supplies its own 128 rows of A and half of
+// the N columns of B from its shared memory, and each CTA's tensor memory
+// receives its 128 rows of the accumulator.  Allocation is collective: one
+// warp of each CTA of the pair executes it, and both get the same address.
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory object in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_smem(const void *local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Arrive once on an mbarrier of another CTA of this cluster (cluster-window
+// address from cluster_smem).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D[tmem, both CTAs] (+)= A[smem desc, 128 rows per CTA] * B[smem desc, N/2
+// columns per CTA], kind::f16 with M = 256, issued by one thread of the even
+// CTA.
+__device__ __forceinline__ void umma_f16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at the same shared offset in each CTA of
+// cta_mask when every pair MMA issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(smem_u32(bar)), "h"(cta_mask)
         : "memory");
 }

@@ -6,25 +6,25 @@
 // representative expert GEMM is N = K = 6144.  Small M streams the weights
 // (HBM-bound); large M is a dense contraction on the tensor cores.
 //
-// One warp-specialised kernel (warp 0: TMA producer, warp 1: MMA issuer,
+// Two warp-specialised kernels (warp 0: TMA producer, warp 1: MMA issuer,
 // warps 2-5: epilogue), operands staged by TMA with the 128-byte swizzle,
-// tcgen05.mma kind::f16 (M = 128) accumulating in TMEM, two accumulators so
-// one piece's epilogue overlaps the next piece's main loop.  Two operand
-// orientations:
-//  * tiled (M > 256): A = x rows, B = w rows.  CTAs run in pairs (clusters
-//    of 2) on 256 x BN tiles, 128 rows each; each CTA loads half of the w
-//    tile and multicasts it to both, halving the L2 -> SM traffic of w.
-//  * swap (M <= 256): A = w rows (128 per tile), B = the M rows of x padded
-//    to MPAD, so the MMA is not mostly padding; the output is written
-//    transposed.
-// Both split the k-block iterations of all tiles evenly over the CTAs
-// (stream-K, see gemm_schedule.h).  Every piece of a tile cut between CTAs
-// leaves its fp32 partial in the workspace and counts itself in; the last
-// piece to arrive adds them all in k order (so results are deterministic)
-// and writes the tile.  No CTA waits for another.  Output blocks of 32 x 32
-// are staged in shared memory by each epilogue warp and written by TMA
-// tensor stores (coalesced, asynchronous; rows past M are clipped).
-#include <cooperative_groups.h>
+// tcgen05.mma kind::f16 accumulating in TMEM:
+//  * gemm_pair_kernel (M > 256): CTA pairs (clusters of 2) run one
+//    tcgen05.mma of M = 256 together.  Each CTA loads its own 128 rows of x
+//    and one half of the tile's w rows; the pair's tensor cores read both
+//    halves, so each w byte crosses from L2 into one SM only.  Tiles are
+//    whole (no split K) with ragged widths (multiples of 32 columns, chosen
+//    so the tiles spread evenly over the pairs).
+//  * gemm_swap_kernel (M <= 256): A = w rows (128 per tile), B = the M rows
+//    of x padded to MPAD, so the MMA is not mostly padding; the output is
+//    written transposed.  The k-block iterations of all tiles are split
+//    evenly over the CTAs (stream-K, see gemm_schedule.h): every piece of a
+//    tile cut between CTAs leaves its fp32 partial in the workspace and
+//    counts itself in; the last piece to arrive adds them all in k order
+//    (so results are deterministic) and writes the tile.  No CTA waits for
+//    another.
+// Output blocks of 32 x 32 are staged in shared memory by each epilogue warp and written by TMA tensor stores (coalesced, asynchronous;
+// rows past M are clipped).
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -32,8 +32,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "gemm_schedule.h"
-
-namespace cg = cooperative_groups;
+#include "tmap.h"
 
 namespace spec {
 namespace {
@@ -134,52 +133,66 @@ __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // Column quads of 32-column chunk cc that a cut tile's pieces publish and
-// add: swap tiles have a column per row of x, so only the quads that hold
-// rows m < M; tiled ones all 8.
-template <bool SWAP>
+// add: a swap tile has a column per row of x, so only the quads that hold
+// rows m < M.
 __device__ __forceinline__ int live_quads(int M, int cc)
 {
-    if (!SWAP) return 8;
     const int q = (M - cc * 32 + 3) / 4;
     return q < 8 ? q : 8;
 }
 
-// Write 32 columns (chunk cc) of this warp's 32 tile rows as one bf16 block:
-// staged in the warp's next buffer, then one TMA store by lane 0.  Tiled:
-// tile row = y row, block at (x = nt BN + 32 cc, y = 128 mt + 32 quad).
-// Swap: tile row = w row n = y column, tile column = x row m, so the block
-// is transposed while staged, at (x = 128 t + 32 quad, y = 32 cc).
-template <bool SWAP>
-__device__ __forceinline__ void store_out(const CUtensorMap *tm_y, uint8_t *obuf, uint32_t &nst, int lane,
-                                          int t, int mt, int nt, int BN, int quad, int cc, const float (&a)[32])
+// Take the warp's next 2 KB staging buffer (the store issued from it two
+// blocks ago has finished reading it).
+__device__ __forceinline__ uint8_t *next_out_buffer(uint8_t *obuf, uint32_t nst, int lane)
 {
-    uint8_t *buf = obuf + (nst & 1u) * kOutBlock;
-    if (lane == 0) bulk_wait_read_1();   // the store issued from this buffer two blocks ago has read it
+    if (lane == 0) bulk_wait_read_1();
     __syncwarp();
-    if (SWAP) {
-        __nv_bfloat16 *b = reinterpret_cast<__nv_bfloat16 *>(buf);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) b[j * 32 + lane] = __float2bfloat16_rn(a[j]);
-    } else {
-        uint4 *b = reinterpret_cast<uint4 *>(buf + lane * 64);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            uint4 o;
-            o.x = pack_bf16x2(a[8 * v + 0], a[8 * v + 1]);
-            o.y = pack_bf16x2(a[8 * v + 2], a[8 * v + 3]);
-            o.z = pack_bf16x2(a[8 * v + 4], a[8 * v + 5]);
-            o.w = pack_bf16x2(a[8 * v + 6], a[8 * v + 7]);
-            b[v] = o;
-        }
-    }
-    fence_proxy_async_smem();   // the staged block is visible to the TMA unit
+    return obuf + (nst & 1u) * kOutBlock;
+}
+
+// Make the staged block visible to the TMA unit and store it with lane 0.
+__device__ __forceinline__ void issue_out_store(const CUtensorMap *tm, const uint8_t *buf, int lane, int x, int y,
+                                                uint32_t &nst)
+{
+    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-        if (SWAP) tma_store_2d(tm_y, buf, t * kBM + quad * 32, cc * 32);
-        else tma_store_2d(tm_y, buf, nt * BN + cc * 32, mt * kBM + quad * 32);
+        tma_store_2d(tm, buf, x, y);
         bulk_commit();
     }
     ++nst;
+}
+
+// Swap orientation: tile row = w row n = y column, tile column = x row m, so
+// the warp's 32 tile rows x 32 columns (chunk cc) are transposed while
+// staged and stored at (x = 128 t + 32 quad, y = 32 cc).
+__device__ __forceinline__ void store_out_swap(const CUtensorMap *tm_y, uint8_t *obuf, uint32_t &nst, int lane,
+                                               int t, int quad, int cc, const float (&a)[32])
+{
+    uint8_t *buf = next_out_buffer(obuf, nst, lane);
+    __nv_bfloat16 *b = reinterpret_cast<__nv_bfloat16 *>(buf);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) b[j * 32 + lane] = __float2bfloat16_rn(a[j]);
+    issue_out_store(tm_y, buf, lane, t * kBM + quad * 32, cc * 32, nst);
+}
+
+// Pair tiles: 32 columns of the warp's 32 rows, row-major, at (x = column,
+// y = row) of y.
+__device__ __forceinline__ void store_out_rows(const CUtensorMap *tm_y, uint8_t *obuf, uint32_t &nst, int lane,
+                                               int x, int y, const uint32_t (&r)[32])
+{
+    uint8_t *buf = next_out_buffer(obuf, nst, lane);
+    uint4 *b = reinterpret_cast<uint4 *>(buf + lane * 64);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        uint4 o;
+        o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+        o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+        o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+        o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+        b[v] = o;
+    }
+    issue_out_store(tm_y, buf, lane, x, y, nst);
 }
 
 template <int BN, int STAGES>
@@ -192,12 +205,11 @@ struct TiledSmem {
 
 constexpr int stages_for(int bn) { return bn >= 256 ? 4 : bn >= 128 ? 6 : 8; }
 
-// SWAP = false: 256 x BN tiles on CTA pairs, A = x, B = w (shared half by
-// half through multicast).  SWAP = true: 128-row w tiles, A = w, B = x
-// padded to BN rows, single CTAs.
-template <int BN, int STAGES, bool SWAP>
+// Weight streaming: 128-row w tiles, A = w, B = x padded to BN rows, single
+// CTAs, stream-K split.
+template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+    gemm_swap_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_y, int M, int N, SkGrid grid, float *__restrict__ part,
                 uint32_t *__restrict__ flags, uint32_t *dev_status)
 {
@@ -219,19 +231,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *s_last = abort + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // tiled: CTA within its pair, and the pair index (the unit of the split)
-    const int rank = SWAP ? 0 : static_cast<int>(blockIdx.x & 1);
-    const int c = SWAP ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x >> 1);
-    constexpr int kUnit = SWAP ? 1 : 2;   // CTAs per unit of the split
-    constexpr uint16_t kPair = 0x3;
-    if (cluster_ctas() != static_cast<uint32_t>(kUnit)) {   // uniform over the grid
+    const int rank = 0;
+    const int c = static_cast<int>(blockIdx.x);
+    constexpr int kUnit = 1;   // CTAs per unit of the split
+    if (cluster_ctas() != 1u) {   // uniform over the grid
         if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
         return;
     }
 
     if (threadIdx.x == 0) {
-        // tiled: a stage is free once the MMAs of both CTAs of the pair read it
-        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], kUnit); }
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int a = 0; a < 2; ++a) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 4); }
         mbar_init(drain, 1);
         mbar_init(pub_bar, 4);
@@ -242,8 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 1) { tmem_alloc(tmem_slot, 2 * BN); tmem_relinquish(); }
-    if constexpr (SWAP) __syncthreads();
-    else cg::this_cluster().sync();   // the peer's barriers exist before anything targets them
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -255,32 +263,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         Seg s;
         uint32_t it = 0;
         while (!*abort && wk.next(s)) {
-            const int mt = 2 * (s.t % grid.tiles_m) + rank, nt = s.t / grid.tiles_m;
             for (int kb = s.kb0; kb < s.kb1; ++kb, ++it) {
                 const int st = it % STAGES;
                 if (it >= STAGES && !mbar_wait(&empty[st], ((it / STAGES) & 1) ^ 1, abort, dev_status)) break;
                 uint8_t *sa = smem + st * L::kStage;
                 mbar_arrive_expect_tx(&full[st], L::kStage);
-                if constexpr (SWAP) {
-                    tma_load_2d(sa, &tm_w, &full[st], kb * kBK, s.t * kBM);
-                    tma_load_2d(sa + kTileA, &tm_x, &full[st], kb * kBK, 0);
-                } else {
-                    // this CTA's rows of x, plus its half of the shared w
-                    // tile, which lands in both CTAs of the pair
-                    tma_load_2d(sa, &tm_x, &full[st], kb * kBK, mt * kBM);
-                    tma_load_2d_multicast(sa + kTileA + rank * (L::kTileB / 2), &tm_w, &full[st],
-                                          kb * kBK, nt * BN + rank * (BN / 2), kPair);
-                }
+                tma_load_2d(sa, &tm_w, &full[st], kb * kBK, s.t * kBM);
+                tma_load_2d(sa + kTileA, &tm_x, &full[st], kb * kBK, 0);
             }
         }
-        if (*abort) {
-            drain_copies(full, it, STAGES);
-        } else if (!SWAP) {
-            // the peer's MMAs signal this CTA's empty barriers: wait for their
-            // last arrivals before this CTA may exit
-            for (uint32_t i = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0; i < it; ++i)
-                if (!mbar_wait(&empty[i % STAGES], (i / STAGES) & 1, abort, dev_status)) break;
-        }
+        if (*abort) drain_copies(full, it, STAGES);
     } else if (warp == 1 && lane == 0) {
         SegWalker wk(grid, c);
         Seg s;
@@ -297,8 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t sa = smem_u32(smem + st * L::kStage);
                 mma_kblock<BN>(d, sa, sa + kTileA, kb > s.kb0);
-                if constexpr (SWAP) umma_commit(&empty[st]);
-                else umma_commit_multicast(&empty[st], kPair);
+                umma_commit(&empty[st]);
             }
             if (!ok) break;
             umma_commit(&acc_full[ab]);
@@ -307,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 2) {
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
-        // swap: only the 32-column chunks that hold rows of x are needed
-        const int nchunks = SWAP ? (M + 31) / 32 < BN / 32 ? (M + 31) / 32 : BN / 32 : BN / 32;
+        // only the 32-column chunks that hold rows of x are needed
+        const int nchunks = (M + 31) / 32 < BN / 32 ? (M + 31) / 32 : BN / 32;
         SegWalker wk(grid, c);
         Seg s;
         uint32_t lt = 0, npub = 0, nred = 0, ndec = 0;
@@ -319,7 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_warp(&acc_full[ab], (lt >> 1) & 1, abort, dev_status)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((quad * 32) << 16) + ab * BN;
-            const int mt = 2 * (s.t % grid.tiles_m) + rank, nt = s.t / grid.tiles_m;
             bool ok = true;
             if (s.kb0 == 0 && s.kb1 == grid.kblocks) {
                 // a whole tile
@@ -331,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float a[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(r[j]);
-                    store_out<SWAP>(&tm_y, obuf, nst, lane, s.t, mt, nt, BN, quad, cc, a);
+                    store_out_swap(&tm_y, obuf, nst, lane, s.t, quad, cc, a);
                 }
             } else {
                 // A piece of a cut tile: publish the fp32 partial, then count
@@ -358,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + cc * 32, r);
                     tmem_ld_wait();
-                    const int nq = live_quads<SWAP>(M, cc);
+                    const int nq = live_quads(M, cc);
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4)
                         if (q4 < nq)
@@ -395,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // idle then) and they are large, else straight from L2 (a
                     // swap tile with one 32-column chunk holds a few KB per
                     // piece: plain loads save the copies' barrier round trip)
-                    const bool ring_ok = !wk.has_more() && !(SWAP && nchunks == 1);
+                    const bool ring_ok = !wk.has_more() && nchunks != 1;
                     const float *ring = reinterpret_cast<const float *>(smem);
                     const int others = l - f;
                     const int per_pass_chunks =
@@ -409,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (go) {
                                     fence_proxy_async_all();
                                     uint32_t bytes = 0;
-                                    for (int cc = c0; cc < c1; ++cc) bytes += live_quads<SWAP>(M, cc) * kBM * 16;
+                                    for (int cc = c0; cc < c1; ++cc) bytes += live_quads(M, cc) * kBM * 16;
                                     mbar_arrive_expect_tx(red_full, bytes * others);
                                     int k = 0;
                                     for (int v = f; v <= l; ++v) {
@@ -419,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         // a unit's quads are its outer index: the live ones are its first bytes
                                         for (int cc = c0; cc < c1; ++cc)
                                             bulk_load(smem + ((cc - c0) * others + k) * 32 * kBM * 4,
-                                                      src + cc * 32 * kBM, live_quads<SWAP>(M, cc) * kBM * 16, red_full);
+                                                      src + cc * 32 * kBM, live_quads(M, cc) * kBM * 16, red_full);
                                         ++k;
                                     }
                                 }
@@ -444,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                              __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
                                 } else {
                                     // columns past the live quads are rows m >= M, never stored
-                                    const int nq = live_quads<SWAP>(M, cc);
+                                    const int nq = live_quads(M, cc);
                                     if (ring_ok) {
                                         const float *u = ring + ((cc - c0) * others + k) * 32 * kBM;
 #pragma unroll
@@ -473,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     }
                                 }
                             }
-                            store_out<SWAP>(&tm_y, obuf, nst, lane, s.t, mt, nt, BN, quad, cc, a);
+                            store_out_swap(&tm_y, obuf, nst, lane, s.t, quad, cc, a);
                         }
                         if (ring_ok) {
                             __syncwarp();
@@ -494,9 +484,200 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     __syncthreads();
     if (*abort && threadIdx.x == 32) drain_mmas(drain);
-    if constexpr (SWAP) __syncthreads();
-    else cg::this_cluster().sync();   // neither CTA of a pair exits while the other may signal it
+    __syncthreads();
     if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, 2 * BN); }
+}
+
+// ------------------------------------------------------------- CTA pairs
+// M > 256: one tcgen05.mma of M = 256 per 16-deep K step, shared by the two
+// CTAs of a cluster.  Per 64-wide k-block each CTA stages its own 128 rows
+// of x (16 KB) and its half of the tile's w rows (W / 2 rows, at most 16 KB;
+// W a multiple of 32, so each half is whole 16-row groups) in its shared
+// memory.  Both CTAs' copies of a stage complete on the even CTA's barrier
+// (the .cta_group::2 form of the TMA load may signal the barrier of the
+// pair's other CTA), the even CTA issues the MMAs once the stage has landed
+// in both, and the commit signals the stage free in both CTAs.  The
+// accumulator (128 rows x W fp32 per CTA) lives in each CTA's tensor memory
+// and each CTA's epilogue writes its own 128 output rows.
+// Measured with per-k-block timestamps of a diagnostic copy (N = K = 6144):
+// a stage completes every ~0.37 us whatever the tile width (128 to 256
+// columns), the bytes staged per k-block (x alone, w alone, or both) and the
+// number of stages (6 to 8); the same loads without the MMAs complete one
+// stage per 0.30 us.  Also measured and slower: x shared by two pairs
+// through cluster multicast (clusters of 4), TMA prefetches into L2 ahead
+// of the loads, and direct global stores from eight epilogue warps.
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairTileB = 128 * kBK * 2;            // up to 128 w rows per CTA
+constexpr uint32_t kPairStage = kTileA + kPairTileB;      // 32 KB
+constexpr uint32_t kPairSmem = kPairStages * kPairStage + kOutStaging + 1024 /*align*/ + 256 /*barriers*/;
+constexpr uint32_t kPairTmemCols = 256;                   // one accumulator, W <= 256
+constexpr uint16_t kPairMask = 0x3;
+
+// Tiled 2-D TMA load into this CTA's shared memory whose completion is
+// counted on `bar_cluster`, a barrier of this CTA or of its pair peer
+// (cluster-window address).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const void *tmap, uint32_t bar_cluster, int x, int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w_narrow,
+                     const __grid_constant__ CUtensorMap tm_w_wide, const __grid_constant__ CUtensorMap tm_y,
+                     int M, PairGrid g, uint32_t *dev_status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *out_stage = smem + kPairStages * kPairStage;   // 4 warps x 2 output blocks
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_stage + kOutStaging);   // (even CTA) stage landed in both
+    uint64_t *empty = full + kPairStages;        // the pair's MMAs are done with the stage
+    uint64_t *acc_full = empty + kPairStages;
+    uint64_t *acc_empty = acc_full + 1;          // (even CTA) both CTAs' epilogues read the accumulator
+    uint64_t *drain = acc_empty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (cluster_ctas() != 2u) {   // uniform over the grid
+        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
+        return;
+    }
+    const uint32_t rank = cluster_rank();
+    const int c = static_cast<int>(blockIdx.x >> 1);
+    const int pairs = static_cast<int>(gridDim.x >> 1);
+    const int tiles = g.tiles();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 8);
+        mbar_init(drain, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, kPairTmemCols);
+        tmem_relinquish_pair();
+        tc_fence_before();
+    }
+    cluster_sync_all();   // both CTAs' barriers and allocations exist before anything targets them
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // the pair's accumulators must sit at the same tensor-memory address
+    if (ld_cluster_u32(cluster_smem(tmem_slot, rank ^ 1u)) != tmem) {
+        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
+        *abort = 1;
+    }
+    __syncthreads();
+
+    if (warp == 0 && lane == 0) {
+        // producer: this CTA's x rows and half of the tile's w rows, counted
+        // on the even CTA's full barrier (which expects both CTAs' bytes)
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_w_narrow);
+        tma_prefetch_desc(&tm_w_wide);
+        tma_prefetch_desc(&tm_y);
+        const uint32_t full0 = cluster_smem(full, 0);
+        uint32_t it = 0;
+        for (int t = c; t < tiles && !*abort; t += pairs) {
+            const int mt = t % g.tiles_m, nt = t / g.tiles_m;
+            const int half = g.width(nt) / 2;
+            const CUtensorMap *tw = half == 16 * g.q ? &tm_w_narrow : &tm_w_wide;
+            const uint32_t bytes = kTileA + static_cast<uint32_t>(half) * kBK * 2;
+            const int row_x = (2 * mt + static_cast<int>(rank)) * kBM;
+            const int row_w = g.col0(nt) + static_cast<int>(rank) * half;
+            bool ok = true;
+            for (int kb = 0; kb < g.kblocks; ++kb, ++it) {
+                const int st = it % kPairStages;
+                if (it >= kPairStages &&
+                    !mbar_wait(&empty[st], ((it / kPairStages) & 1) ^ 1, abort, dev_status)) { ok = false; break; }
+                uint8_t *sa = smem + st * kPairStage;
+                if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * bytes);
+                tma_load_2d_pair(sa, &tm_x, full0 + st * 8, kb * kBK, row_x);
+                tma_load_2d_pair(sa + kTileA, tw, full0 + st * 8, kb * kBK, row_w);
+            }
+            if (!ok) break;
+        }
+        if (!*abort) {
+            // the last commits signal this CTA's empty barriers (and mean its
+            // copies were consumed): wait for them before this CTA may exit
+            const uint32_t first = it > static_cast<uint32_t>(kPairStages) ? it - kPairStages : 0;
+            for (uint32_t i = first; i < it; ++i)
+                if (!mbar_wait(&empty[i % kPairStages], (i / kPairStages) & 1, abort, dev_status)) break;
+        }
+        if (*abort) {
+            // copies in flight complete on the even CTA's full barriers: drain
+            // those (bounded), then give any straggler 0.2 ms to land
+            if (rank == 0) drain_copies(full, it, kPairStages);
+            const unsigned long long t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 200000ull) {
+            }
+        }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // MMA issuer (even CTA)
+        uint32_t it = 0, lt = 0;
+        for (int t = c; t < tiles && !*abort; t += pairs, ++lt) {
+            const int nt = t / g.tiles_m;
+            const uint32_t idesc = idesc_f16(2 * kBM, g.width(nt), /*bf16*/ 1, 0, 0);
+            if (lt >= 1 && !mbar_wait(acc_empty, (lt - 1) & 1, abort, dev_status)) break;
+            tc_fence_after();
+            bool ok = true;
+            for (int kb = 0; kb < g.kblocks; ++kb, ++it) {
+                const int st = it % kPairStages;
+                if (!mbar_wait(&full[st], (it / kPairStages) & 1, abort, dev_status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + st * kPairStage);
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                    umma_f16_ss_pair(tmem, sdesc(sa + k * 32, 16, 1024), sdesc(sa + kTileA + k * 32, 16, 1024),
+                                     idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                umma_commit_pair(&empty[st], kPairMask);
+            }
+            if (!ok) break;
+            umma_commit_pair(acc_full, kPairMask);
+        }
+    } else if (warp >= 2) {
+        // epilogue: this CTA's 128 rows of each tile, 32 rows per warp
+        const int quad = warp & 3;
+        uint8_t *obuf = out_stage + (warp - 2) * 2 * kOutBlock;
+        const uint32_t acc_empty0 = cluster_smem(acc_empty, 0);
+        uint32_t nst = 0, lt = 0;
+        for (int t = c; t < tiles && !*abort; t += pairs, ++lt) {
+            const int mt = t % g.tiles_m, nt = t / g.tiles_m;
+            const int W = g.width(nt), n0 = g.col0(nt);
+            if (!mbar_wait_warp(acc_full, lt & 1, abort, dev_status)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((quad * 32) << 16);
+            const int y0 = (2 * mt + static_cast<int>(rank)) * kBM + quad * 32;
+#pragma unroll 1
+            for (int cc = y0 < M ? 0 : W; cc < W; cc += 32) {   // rows past M: nothing to store
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + cc, r);
+                tmem_ld_wait();
+                store_out_rows(&tm_y, obuf, nst, lane, n0 + cc, y0, r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty0);
+        }
+        if (lane == 0) bulk_wait_read_all();   // staged output read before the CTA's shared memory goes
+    }
+    __syncwarp();
+    __syncthreads();
+    if (*abort && rank == 0 && threadIdx.x == 32) {
+        // let every pair MMA issued so far finish before tensor memory goes
+        umma_commit_pair(drain, 0x1);
+        mbar_wait_drain(drain, 0, 100000000ull);
+    }
+    cluster_sync_all();   // neither CTA exits while the other may still signal or read it
+    if (warp == 1) { tc_fence_after(); tmem_dealloc_pair(tmem, kPairTmemCols); }
 }
 
 template <typename Kern>
@@ -505,84 +686,81 @@ cudaError_t set_smem(Kern k, uint32_t bytes)
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
-template <int BN, bool SWAP>
-cudaLaunchConfig_t kernel_config(int grid, cudaStream_t st, cudaLaunchAttribute (&attr)[2])
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = TiledSmem<BN, stages_for(BN)>::kBytes;
-    cfg.stream = st;
-    int n = 0;
-    if (!SWAP) {
-        attr[n].id = cudaLaunchAttributeClusterDimension;   // CTA pairs share the w tile
-        attr[n].val.clusterDim.x = 2;
-        attr[n].val.clusterDim.y = 1;
-        attr[n].val.clusterDim.z = 1;
-        ++n;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = n;
-    return cfg;
-}
-
-template <int BN, bool SWAP>
-cudaError_t run(const GemmPlan &p, const CUtensorMap &tx, const CUtensorMap &tw, const CUtensorMap &ty,
-                int M, int N, void *workspace, uint32_t *dev_status, cudaStream_t st)
+template <int BN>
+cudaError_t run_swap(const GemmPlan &p, const CUtensorMap &tx, const CUtensorMap &tw, const CUtensorMap &ty,
+                     int M, int N, void *workspace, uint32_t *dev_status, cudaStream_t st)
 {
     constexpr int STAGES = stages_for(BN);
-    auto k = gemm_kernel<BN, STAGES, SWAP>;
+    auto k = gemm_swap_kernel<BN, STAGES>;
     cudaError_t e = set_smem(k, TiledSmem<BN, STAGES>::kBytes);
     if (e != cudaSuccess) return e;
     uint32_t *flags = static_cast<uint32_t *>(workspace);
     float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kFlagBytes);
-    cudaLaunchAttribute attr[2];
-    const cudaLaunchConfig_t cfg = kernel_config<BN, SWAP>(p.grid, st, attr);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = TiledSmem<BN, STAGES>::kBytes;
+    cfg.stream = st;
     return cudaLaunchKernelEx(&cfg, k, tx, tw, ty, M, N, p.sk, part, flags, dev_status);
+}
+
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t st, cudaLaunchAttribute (&attr)[1])
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kPairSmem;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeClusterDimension;   // the two CTAs of a pair MMA
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
 }
 
 // Units (CTA pairs, or single CTAs for the swap orientation) that can be
 // resident at once, from the occupancy calculator; 0 if the query fails.
-template <int BN, bool SWAP>
-int max_units_for()
+template <int BN>
+int max_swap_units()
 {
     constexpr int STAGES = stages_for(BN);
-    auto k = gemm_kernel<BN, STAGES, SWAP>;
+    auto k = gemm_swap_kernel<BN, STAGES>;
     if (set_smem(k, TiledSmem<BN, STAGES>::kBytes) != cudaSuccess) return 0;
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, TiledSmem<BN, STAGES>::kBytes) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return per_sm > 0 ? sms : 0;   // one CTA per SM
+}
+
+int max_pair_units()
+{
+    if (set_smem(gemm_pair_kernel, kPairSmem) != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
     int n = 0;
-    if (SWAP) {
-        int dev = 0, sms = 0, per_sm = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads,
-                                                          TiledSmem<BN, STAGES>::kBytes) != cudaSuccess) {
-            cudaGetLastError();
-            return 0;
-        }
-        n = per_sm > 0 ? sms : 0;   // one CTA per SM
-    } else {
-        cudaLaunchAttribute attr[2];
-        cudaLaunchConfig_t cfg = kernel_config<BN, SWAP>(2, nullptr, attr);
-        cfg.numAttrs = 1;   // the occupancy query takes the cluster shape only
-        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            return 0;
-        }
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
     }
     return n;
 }
 
 int query_max_units(int bn, bool swap)
 {
-    if (swap) {
-        switch (bn) {
-        case 32: return max_units_for<32, true>();
-        case 64: return max_units_for<64, true>();
-        case 128: return max_units_for<128, true>();
-        default: return max_units_for<256, true>();
-        }
+    if (!swap) return max_pair_units();
+    switch (bn) {
+    case 32: return max_swap_units<32>();
+    case 64: return max_swap_units<64>();
+    case 128: return max_swap_units<128>();
+    default: return max_swap_units<256>();
     }
-    return bn == 256 ? max_units_for<256, false>() : max_units_for<128, false>();
 }
 
 }  // namespace
@@ -590,10 +768,10 @@ int query_max_units(int bn, bool swap)
 int gemm_max_units(int bn, bool swap)
 {
     // per device and kernel variant; the answer never changes for a process
-    static std::atomic<int> cache[64][6];
+    static std::atomic<int> cache[64][5];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    const int v_idx = swap ? (bn == 32 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : 3) : (bn == 256 ? 5 : 4);
+    const int v_idx = swap ? (bn == 32 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : 3) : 4;
     std::atomic<int> &slot = cache[dev][v_idx];
     int v = slot.load(std::memory_order_relaxed);
     if (v <= 0) {
@@ -603,52 +781,76 @@ int gemm_max_units(int bn, bool swap)
     return v;
 }
 
-GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_tiled)
+// Pair tiles: choose the number of column tiles.  Widths are multiples of
+// 32 columns (each CTA's half of the pair MMA's N then covers whole 16-row
+// groups of w) within [32, 256]; the cost of a candidate is the number of
+// waves of tiles over the resident pairs times the widest tile plus a fixed
+// per-tile overhead of kPairOverheadCols columns (the x rows every k-block
+// stages whatever the width, the pipeline fill, the epilogue).  N = K =
+// 6144, 76 pairs: M = 512 takes 38 column tiles of 160 or 192 columns, one
+// tile per pair, where 256-column tiles would leave 28 pairs idle.
+constexpr int kPairOverheadCols = 32;
+
+PairGrid plan_pairs(int M, int N, int K, int max_pairs)
+{
+    PairGrid g{};
+    g.tiles_m = (M + 2 * kBM - 1) / (2 * kBM);
+    g.kblocks = K / kBK;
+    const int n32 = N / 32;
+    const int lo = (n32 + 7) / 8;   // widths <= 256
+    long long best = -1;
+    for (int tn = lo; tn <= n32; ++tn) {
+        const long long tiles = static_cast<long long>(g.tiles_m) * tn;
+        const long long waves = (tiles + max_pairs - 1) / max_pairs;
+        const long long cost = waves * (32LL * ((n32 + tn - 1) / tn) + kPairOverheadCols);
+        // on a tie, more (narrower) tiles: the same makespan with less work
+        // on most pairs
+        if (best < 0 || cost <= best) {
+            best = cost;
+            g.tiles_n = tn;
+        }
+    }
+    g.q = n32 / g.tiles_n;
+    g.r = n32 % g.tiles_n;
+    g.pairs = g.tiles() < max_pairs ? g.tiles() : max_pairs;
+    return g;
+}
+
+GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_pair)
 {
     GemmPlan p{};
     const int kblocks = K / kBK;
-    int tiles, min_iters, cap;
-    if (M <= 256) {
-        // Weight streaming: 128-row w tiles cut so that every SM streams,
-        // each into about three pieces (min_iters = ceil(kblocks / 3); at
-        // K = 6144, 48 tiles become 144 equal thirds).  Measured against a
-        // limit of five pieces for narrow tiles and three for wide ones:
-        // M = 8 26.2 -> 25.2 us, M = 64 28.6 -> 26.6 us, M = 256 37.0 ->
-        // 36.1 us.
-        p.swap = true;
-        p.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-        tiles = N / kBM;
-        p.sk.tiles_m = 1;
-        const int div = 3;
-        min_iters = (kblocks + div - 1) / div > 8 ? (kblocks + div - 1) / div : 8;
-        cap = max_units_swap;
-    } else {
-        // 256 x BN tiles on CTA pairs; a tile is cut into at most three
-        // pieces (min_iters = ceil(kblocks / 2)), or not at all (below).
+    if (M > 256) {
         p.swap = false;
-        p.bn = N % 256 == 0 ? 256 : 128;
-        p.sk.tiles_m = ((M + kBM - 1) / kBM + 1) / 2;
-        tiles = p.sk.tiles_m * (N / p.bn);
-        min_iters = (kblocks + 1) / 2 > 16 ? (kblocks + 1) / 2 : 16;
-        cap = max_units_tiled;
+        const int cap = max_units_pair < 1 ? 1 : max_units_pair > kMaxCtas / 2 ? kMaxCtas / 2 : max_units_pair;
+        p.pg = plan_pairs(M, N, K, cap);
+        p.bn = p.pg.width(0);
+        p.grid = 2 * p.pg.pairs;
+        p.workspace_bytes = 0;   // whole tiles: nothing to add across CTAs
+        return p;
     }
+    // Weight streaming: 128-row w tiles cut so that every SM streams, each
+    // into about three pieces (min_iters = ceil(kblocks / 3); at K = 6144,
+    // 48 tiles become 144 equal thirds).  Measured against a limit of five
+    // pieces for narrow tiles and three for wide ones: M = 8 26.2 -> 25.2
+    // us, M = 64 28.6 -> 26.6 us, M = 256 37.0 -> 36.1 us.
+    p.swap = true;
+    p.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    const int tiles = N / kBM;
+    p.sk.tiles_m = 1;
+    const int div = 3;
+    const int min_iters = (kblocks + div - 1) / div > 8 ? (kblocks + div - 1) / div : 8;
+    int cap = max_units_swap;
     // Stream-K: whole-tile waves while more than two waves remain, the rest
     // cut into equal k-block ranges, one per unit.
     const long long iters = static_cast<long long>(tiles) * kblocks;
-    const int unit_ctas = p.swap ? 1 : 2;
-    cap = cap < kMaxCtas / unit_ctas ? cap : kMaxCtas / unit_ctas;
+    cap = cap < kMaxCtas ? cap : kMaxCtas;
     cap = cap < 1 ? 1 : cap;
     long long u = iters / min_iters;
     u = u < 1 ? 1 : u > cap ? cap : u;
-    // Tiled orientation with at least half a wave of tiles but no more than
-    // one: one whole tile per CTA pair.  Cut tiles would keep every pair
-    // busy, but adding their pieces (fp32 partials through L2, at the same
-    // per-SM L2 rate that feeds the MMAs) costs more than the idle pairs:
-    // N = K = 6144, M = 512: 50.8 -> 45.1 us, M = 768: 55.1 -> 45.1 us.
-    if (!p.swap && tiles <= cap && 2 * tiles >= cap) u = tiles;
     const int units = static_cast<int>(u);
     const int waves = tiles / units;
-    p.grid = unit_ctas * units;
+    p.grid = units;
     p.sk.tiles = tiles;
     p.sk.kblocks = kblocks;
     p.sk.G = units;
@@ -658,21 +860,46 @@ GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_tiled)
     return p;
 }
 
-cudaError_t launch_gemm(const GemmPlan &p, const CUtensorMap &t_x, const CUtensorMap &t_w,
-                        const CUtensorMap &t_y, void *y, int M, int N, void *workspace,
-                        uint32_t *dev_status, cudaStream_t st)
+cudaError_t launch_gemm(const GemmPlan &p, const void *x, const void *w, void *y, int M, int N, int K,
+                        void *workspace, uint32_t *dev_status, cudaStream_t st)
 {
-    (void)y;   // written through t_y
+    const uint64_t dx[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+    const uint64_t dw[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
+    const uint64_t sk[1] = {static_cast<uint64_t>(K) * 2};
+    const uint64_t dy[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+    const uint64_t sy[1] = {static_cast<uint64_t>(N) * 2};
+    CUtensorMap tx, tw, ty;
     if (p.swap) {
+        // x padded to bn rows, 128-row w tiles; y written in 32 x 32 blocks
+        const uint32_t bx[2] = {64, static_cast<uint32_t>(p.bn)};
+        const uint32_t bw[2] = {64, static_cast<uint32_t>(kBM)};
+        const uint32_t by[2] = {32, 32};
+        if (!encode_bf16_tmap(&tx, x, 2, dx, sk, bx) || !encode_bf16_tmap(&tw, w, 2, dw, sk, bw) ||
+            !encode_bf16_tmap_plain(&ty, y, 2, dy, sy, by))
+            return cudaErrorInvalidValue;
         switch (p.bn) {
-        case 32: return run<32, true>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
-        case 64: return run<64, true>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
-        case 128: return run<128, true>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
-        default: return run<256, true>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
+        case 32: return run_swap<32>(p, tx, tw, ty, M, N, workspace, dev_status, st);
+        case 64: return run_swap<64>(p, tx, tw, ty, M, N, workspace, dev_status, st);
+        case 128: return run_swap<128>(p, tx, tw, ty, M, N, workspace, dev_status, st);
+        default: return run_swap<256>(p, tx, tw, ty, M, N, workspace, dev_status, st);
         }
     }
-    if (p.bn == 256) return run<256, false>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
-    return run<128, false>(p, t_x, t_w, t_y, M, N, workspace, dev_status, st);
+    // pairs: 128 x rows per CTA; half of a tile's w rows per CTA (16q rows
+    // for the narrow tiles, 16(q + 1) for the wide ones); y in 32 x 32 blocks
+    CUtensorMap tw2;
+    const uint32_t bx[2] = {64, static_cast<uint32_t>(kBM)};
+    const uint32_t bw_n[2] = {64, static_cast<uint32_t>(16 * p.pg.q)};
+    const uint32_t bw_w[2] = {64, static_cast<uint32_t>(16 * (p.pg.q + 1))};
+    const uint32_t by[2] = {32, 32};
+    if (!encode_bf16_tmap(&tx, x, 2, dx, sk, bx) || !encode_bf16_tmap(&tw, w, 2, dw, sk, bw_n) ||
+        !encode_bf16_tmap(&tw2, w, 2, dw, sk, bw_w) || !encode_bf16_tmap_plain(&ty, y, 2, dy, sy, by))
+        return cudaErrorInvalidValue;
+    cudaError_t e = set_smem(gemm_pair_kernel, kPairSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config(p.grid, st, attr);
+    (void)workspace;
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, tx, tw, tw2, ty, M, p.pg, dev_status);
 }
 
 }  // namespace spec

@@ -1,14 +1,21 @@
-// Stream-K work decomposition of the tiled verify GEMM, shared by the
-// kernel's three roles (TMA producer, MMA issuer, epilogue) and by the host
-// planner that the CPU tests enumerate.
+// Work decompositions of the verify GEMM, shared by the kernels' roles (TMA
+// producer, MMA issuer, epilogue) and by the host planner that the CPU tests
+// enumerate.
 //
-// Output tile t covers rows (t % tiles_m) * 128 and columns
-// (t / tiles_m) * BN.  The first dp_tiles tiles are whole-tile work (CTA c
-// takes c, c + G, c + 2G, ...); the k-block iterations of the remaining
-// tiles are cut into G equal contiguous ranges, one per CTA (stream-K), so
-// every SM gets the same number of MMAs whatever the tile count.  The
-// pieces of a tile cut between CTAs are added, in k order, by whichever
-// piece is finished last.
+// Weight streaming (M <= 256): stream-K.  Output tile t covers the 128 w
+// rows (output columns) t * 128 ...  The first dp_tiles tiles are
+// whole-tile work (CTA c takes c, c + G, c + 2G, ...); the k-block
+// iterations of the remaining tiles are cut into G equal contiguous ranges,
+// one per CTA, so every SM gets the same number of MMAs whatever the tile
+// count.  The pieces of a tile cut between CTAs are added, in k order, by
+// whichever piece is finished last.
+//
+// CTA pairs (M > 256): whole tiles of 256 rows and a ragged width.  The N
+// columns are cut, in 32-column units, into tiles_n tiles whose widths
+// differ by at most 32 (the first r tiles are 32 wider), so that
+// tiles_m * tiles_n tiles spread evenly over the pairs; pair c takes tiles
+// c, c + pairs, ...  Tile t covers rows (t % tiles_m) * 256 and the columns
+// of N-tile t / tiles_m.
 #pragma once
 
 #include <stdint.h>
@@ -57,6 +64,16 @@ struct SegWalker {
     }
     // whether a segment follows the one next() returned last
     SPEC_HD bool has_more() const { return w * g.G < g.dp_tiles || it < end; }
+};
+
+struct PairGrid {
+    int tiles_m, tiles_n;   // row tiles of 256, column tiles
+    int q, r;               // N-tile nt is 32 * (q + (nt < r)) columns wide
+    int kblocks;            // K / 64
+    int pairs;              // CTA pairs launched
+    SPEC_HD int tiles() const { return tiles_m * tiles_n; }
+    SPEC_HD int width(int nt) const { return 32 * (q + (nt < r ? 1 : 0)); }
+    SPEC_HD int col0(int nt) const { return 32 * (nt * q + (nt < r ? nt : r)); }
 };
 
 // For a segment that starts its tile (kb0 == 0) on unit c: the last unit

@@ -77,19 +77,20 @@ def test_accept_sample_rejects_bad_arguments(lib):
 
 def test_gemm_rejects_bad_arguments(lib):
     f = lib.spec_verify_gemm
-    assert f(FAKE, FAKE, FAKE, -1, 128, 64, None, 0, None) == INVALID
-    assert f(FAKE, FAKE, FAKE, 8, 100, 64, None, 0, None) == UNSUPPORTED   # N % 128
-    assert f(FAKE, FAKE, FAKE, 8, 128, 60, None, 0, None) == UNSUPPORTED   # K % 64
-    assert f(None, FAKE, FAKE, 8, 128, 64, None, 0, None) == INVALID
-    assert f(P(0x7F0000001008), FAKE, FAKE, 8, 128, 64, None, 0, None) == INVALID
-    assert f(None, None, None, 0, 128, 64, None, 0, None) == 0   # empty: no-op
-    # stream-K: 1 KB of ready flags, then one fp32 partial tile per CTA
-    ws = lib.spec_verify_gemm_workspace_size(512, 6144, 6144)
-    assert ws >= 1024 + 128 * 256 * 4 and ws % 256 == 0
-    assert lib.spec_verify_gemm_workspace_size(512, 6144 + 128, 6144) < ws   # 128-wide tiles
-    # small M: partials as wide as the padded x rows
-    assert lib.spec_verify_gemm_workspace_size(8, 6144, 6144) < lib.spec_verify_gemm_workspace_size(
-        256, 6144, 6144)
+    assert f(FAKE, FAKE, FAKE, -1, 128, 64, None, 0, None, None) == INVALID
+    assert f(FAKE, FAKE, FAKE, 8, 100, 64, None, 0, None, None) == UNSUPPORTED   # N % 128
+    assert f(FAKE, FAKE, FAKE, 8, 128, 60, None, 0, None, None) == UNSUPPORTED   # K % 64
+    assert f(None, FAKE, FAKE, 8, 128, 64, None, 0, None, None) == INVALID
+    assert f(P(0x7F0000001008), FAKE, FAKE, 8, 128, 64, None, 0, None, None) == INVALID
+    assert f(None, None, None, 0, 128, 64, None, 0, None, None) == 0   # empty: no-op
+    # weight streaming: 4 KB of arrival counters, then fp32 partial tiles as
+    # wide as the padded x rows, two per CTA
+    ws8 = lib.spec_verify_gemm_workspace_size(8, 6144, 6144)
+    assert ws8 >= 4096 + 2 * 128 * 32 * 4 and ws8 % 256 == 0
+    assert ws8 < lib.spec_verify_gemm_workspace_size(256, 6144, 6144)
+    # pairs of CTAs on whole tiles: no workspace
+    assert lib.spec_verify_gemm_workspace_size(512, 6144, 6144) == 0
+    assert lib.spec_verify_gemm_workspace_size(257, 6144, 6144) == 0
 
 
 def test_tree_entry_points_reject_bad_arguments(lib):
@@ -153,3 +154,13 @@ def test_adasd_rejects_bad_arguments(lib):
     assert f(*args(wb=need - 1)) == WORKSPACE
     assert f(*args(q=None, dr=None, ua=None, D=0, B=0)) == 0   # empty batch: no-op
     assert f(*args(th=float("inf"), tj=float("-inf"), B=0)) == 0
+
+
+def test_selftest_bounded_wait_rejects_bad_arguments(lib):
+    f = lib.spec_selftest_bounded_wait
+    never = 0xFFFFFFFFFFFFFFFF
+    assert f(0, never, FAKE, None, None) == INVALID                  # no limit
+    assert f(10_000_000_001, never, FAKE, None, None) == INVALID     # limit above 10 s
+    assert f(1_000_000, 10_000_000_001, FAKE, None, None) == INVALID  # arrival later than 10 s
+    assert f(1_000_000, never, None, None, None) == INVALID          # no result buffer
+    assert f(1_000_000, never, P(0x7F0000001004), None, None) == INVALID   # misaligned result

@@ -1,10 +1,12 @@
-"""The tiled verify GEMM's stream-K split, enumerated on the host.
+"""The verify GEMM's work split, enumerated on the host.
 
-The kernel's three roles walk the same segment list; these checks run the
-library's own walker (through spec_verify_gemm_plan) and need no GPU:
-coverage of every (tile, k-block) exactly once, balance across CTAs, one
-owner per tile whose contributor range matches the pieces, and the
-ordering that keeps the owners' waits free of cycles.
+The kernels' roles walk the same tile and segment lists; these checks run
+the library's own planner (through spec_verify_gemm_plan) and need no GPU.
+Weight streaming (M <= 256, stream-K): coverage of every (tile, k-block)
+exactly once, balance across CTAs, one owner per tile whose contributor
+range matches the pieces, and the ordering that keeps the owners' waits
+free of cycles.  CTA pairs (M > 256): whole tiles of ragged width that
+cover every output column once and spread evenly over the pairs.
 """
 from collections import defaultdict
 
@@ -20,24 +22,20 @@ def built():
     from speculative_decoding_verification_attention_gb300 import _build
     _build.build()
 
-SHAPES = [(8, 6144, 6144), (200, 6144, 6144), (256, 384, 640), (1, 128, 64), (257, 6144, 6144), (384, 128, 6144), (512, 6144, 6144), (1024, 6144, 6144),
-          (2048, 6144, 6144), (4096, 6144, 6144), (3000, 6272, 1024), (512, 256, 64),
-          (65536, 128, 64), (300, 384, 128)]
+SHAPES = [(8, 6144, 6144), (200, 6144, 6144), (256, 384, 640), (1, 128, 64), (100, 19456, 640),
+          (64, 128, 6144), (256, 256, 4096), (33, 6272, 640), (128, 65536, 64)]
+PAIR_SHAPES = [(257, 6144, 6144), (384, 128, 6144), (512, 6144, 6144), (1024, 6144, 6144),
+               (2048, 6144, 6144), (4096, 6144, 6144), (3000, 6272, 1024), (512, 256, 64),
+               (65536, 128, 64), (300, 384, 128), (600, 19584, 512)]
 
 
 @pytest.mark.parametrize("sms", [152, 148, 7, 1])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_stream_k_split(M, N, K, sms):
     seg = sv.gemm_plan(M, N, K, sms)
-    swap = M <= 256
-    if swap:        # 128-row w tiles; x rows padded to the MMA N
-        bn = 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
-        tiles = N // 128
-        max_units, max_contrib = sms, 4 if bn <= 64 else 2
-    else:           # 256-row pair tiles
-        bn = 256 if N % 256 == 0 else 128
-        tiles = -(-(-(-M // 128)) // 2) * (N // bn)
-        max_units, max_contrib = max(1, sms // 2), 2
+    bn = 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
+    tiles = N // 128
+    max_units, max_contrib = sms, 4 if bn <= 64 else 2
     kblocks = K // 64
     assert (seg[:, 5] == bn).all()
     ctas = seg[:, 0]
@@ -61,7 +59,6 @@ def test_stream_k_split(M, N, K, sms):
     by_tile = defaultdict(list)
     for i, (c, t, k0, k1, last, _) in enumerate(seg):
         by_tile[t].append((c, k0, k1, last, i))
-    first_sk = {}
     for t, pieces in by_tile.items():
         owners = [p for p in pieces if p[1] == 0]
         assert len(owners) == 1
@@ -86,6 +83,58 @@ def test_stream_k_split(M, N, K, sms):
         assert all(r[4] == -1 for r in rows if r[2] > 0)
 
 
+def pair_columns(seg, M):
+    """(tile -> (row block, first column, width)) from the plan rows of a
+    CTA-pair GEMM; tile t is row block t % tiles_m of column tile t // tiles_m."""
+    tiles_m = -(-M // 256)
+    width = {}
+    for c, t, k0, k1, last, w in seg:
+        width[int(t) // tiles_m] = int(w)
+    col0, acc = {}, 0
+    for nt in sorted(width):
+        col0[nt] = acc
+        acc += width[nt]
+    return tiles_m, width, col0, acc
+
+
+@pytest.mark.parametrize("sms", [152, 148, 7, 2])
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES)
+def test_pair_tiles(M, N, K, sms):
+    seg = sv.gemm_plan(M, N, K, sms)
+    kblocks = K // 64
+    assert ((seg[:, 2] == 0) & (seg[:, 3] == kblocks)).all()    # whole tiles
+    assert (seg[:, 4] == seg[:, 0]).all()
+    pairs = int(seg[:, 0].max()) + 1
+    assert pairs <= max(1, sms // 2)
+    tiles_m, width, col0, total = pair_columns(seg, M)
+    tiles = tiles_m * len(width)
+    # every tile exactly once; pair c takes tiles c, c + pairs, ...
+    assert sorted(seg[:, 1].tolist()) == list(range(tiles))
+    for c, t, *_ in seg:
+        assert t % pairs == c
+    per_pair = np.bincount(seg[:, 0], minlength=pairs)
+    assert per_pair.max() - per_pair.min() <= 1
+    # the column tiles cover N exactly; widths multiples of 32 within
+    # [32, 256] that differ by at most 32, the wider ones first
+    assert total == N
+    ws = [width[nt] for nt in sorted(width)]
+    assert all(w % 32 == 0 and 32 <= w <= 256 for w in ws)
+    assert max(ws) - min(ws) <= 32
+    assert ws == sorted(ws, reverse=True)
+    # every (row block, column tile) is some tile's
+    for c, t, k0, k1, last, w in seg:
+        assert w == width[int(t) // tiles_m]
+
+
+def test_verify_layer_at_512_rows_fills_every_pair():
+    """N = K = 6144, M = 512, 76 resident pairs: 38 column tiles (2 of 192
+    and 36 of 160 columns) x 2 row blocks = one whole tile per pair."""
+    seg = sv.gemm_plan(512, 6144, 6144, 152)
+    assert len(seg) == 76 and int(seg[:, 0].max()) + 1 == 76
+    assert sorted(np.unique(seg[:, 5], return_counts=True)[1].tolist()) == [4, 72]
+    assert set(seg[:, 5].tolist()) == {160, 192}
+
+
 def test_weight_streaming_cuts_each_tile_in_thirds_at_small_m():
     """M = 8, N = K = 6144: the 48 w tiles of 128 rows are cut into three
     equal k-ranges of 32 k-blocks, one per CTA (144 of the 152 SMs stream
@@ -105,22 +154,9 @@ def test_rejects_bad_arguments():
     assert lib.spec_verify_gemm_plan(512, 128, 64, 152, None, 4) == -1
 
 
-@pytest.mark.parametrize("M", [384, 512, 640, 768])
-def test_half_to_full_wave_takes_whole_tiles(M):
-    """N = K = 6144 with 76 resident CTA pairs: 48 or 72 pair tiles fill at
-    least half of the pairs, so every pair takes one whole tile and no tile
-    is cut (nothing to add up through the workspace)."""
-    N = K = 6144
-    seg = sv.gemm_plan(M, N, K, 152)
-    tiles = -(-(-(-M // 128)) // 2) * (N // 256)
-    assert len(seg) == tiles
-    assert sorted(seg[:, 1].tolist()) == list(range(tiles))
-    assert (seg[:, 2] == 0).all() and (seg[:, 3] == K // 64).all()
-    assert int(seg[:, 0].max()) + 1 == tiles
-
-
-def test_less_than_half_a_wave_is_cut():
-    """16 pair tiles for 76 pairs: the k-blocks are split so every pair works."""
-    seg = sv.gemm_plan(512, 2048, 6144, 152)
-    assert int(seg[:, 0].max()) + 1 > 16
+def test_small_m_few_tiles_are_cut():
+    """M = 200, 3 tiles of 128 w rows over K = 6144 for 152 SMs: the k-blocks
+    are split so that every CTA streams weights."""
+    seg = sv.gemm_plan(200, 384, 6144, 152)
+    assert int(seg[:, 0].max()) + 1 > 3
     assert ((seg[:, 2] > 0) | (seg[:, 3] < 96)).any()

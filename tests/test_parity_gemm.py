@@ -4,7 +4,8 @@ Bar: relative L2 error <= 5e-3 over the compared entries (bf16 output
 rounding alone gives ~1e-3), plus an elementwise bound of 2^-7 |y| + 1e-3.
 Small shapes are compared in full; the verify shapes (N = K = 6144,
 M = B(1+D) from 8 to 4096) on a seeded sample of entries that covers every
-128-row / 128-column tile edge, plus a full-tensor comparison with torch's
+128-row / 128-column tile edge and every edge of the ragged column tiles of
+the CTA-pair path, plus a full-tensor comparison with torch's
 fp32-accumulating matmul as a secondary property check.
 """
 import numpy as np
@@ -72,7 +73,21 @@ def test_weight_streaming_full_compare(sv, oracle_lib, M, N, K):
     check(y, oracle_lib.gemm(x, w))
 
 
-def sample_entries(rng, M, N, n=3000):
+def pair_column_edges(sv, M, N, K):
+    """First and last column of every column tile of the CTA-pair plan."""
+    if M <= 256:
+        return np.zeros(0, np.int64)
+    seg = sv.gemm_plan(M, N, K, 152)
+    tiles_m = -(-M // 256)
+    width = {int(t) // tiles_m: int(w) for _, t, _, _, _, w in seg}
+    edges, acc = [], 0
+    for nt in sorted(width):
+        edges += [acc, acc + width[nt] - 1]
+        acc += width[nt]
+    return np.asarray(edges, np.int64)
+
+
+def sample_entries(rng, M, N, n=3000, col_edges=()):
     m = rng.integers(0, M, n)
     c = rng.integers(0, N, n)
     edges_m = np.unique(np.clip(np.concatenate([[0, M - 1], np.arange(127, M, 128),
@@ -82,6 +97,11 @@ def sample_entries(rng, M, N, n=3000):
     em, en = np.meshgrid(edges_m[:64], edges_n[:64])
     m = np.concatenate([m, em.ravel()])
     c = np.concatenate([c, en.ravel()])
+    if len(col_edges):
+        # every ragged column-tile edge, on rows at the row-block edges
+        em, en = np.meshgrid(edges_m[:16], np.asarray(col_edges))
+        m = np.concatenate([m, em.ravel()])
+        c = np.concatenate([c, en.ravel()])
     return np.stack([m, c], axis=1).astype(np.int32)
 
 
@@ -92,7 +112,7 @@ def test_verify_shapes_sampled(sv, oracle_lib, M):
     x, w = synth.gemm_inputs(1000 + M, M, N, K)
     y, ydev = run(sv, x, w)
     rng = np.random.default_rng(M)
-    s = sample_entries(rng, M, N)
+    s = sample_entries(rng, M, N, col_edges=pair_column_edges(sv, M, N, K))
     ref = oracle_lib.gemm(x, w, samples=s)
     check(y[s[:, 0], s[:, 1]], ref)
     # whole-tensor property: agrees with an fp32-accumulating library matmul
@@ -108,38 +128,81 @@ def test_two_calls_in_a_row_agree(sv):
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("M,N,K", [(384, 128, 6144), (640, 256, 4096), (2000, 6272, 640)])
+@pytest.mark.parametrize("M,N,K", [(200, 128, 6144), (256, 256, 4096), (64, 384, 6144)])
 def test_stream_k_many_pieces(sv, oracle_lib, M, N, K):
-    """Few tiles and long K: tiles are cut into several pieces whose fp32
-    partials the last-arriving piece adds (checked against the oracle)."""
+    """Weight streaming with few tiles and long K: tiles are cut into several
+    pieces whose fp32 partials the last-arriving piece adds (checked against
+    the oracle in full)."""
     x, w = synth.gemm_inputs(7 * M + K, M, N, K)
     segs = sv.gemm_plan(M, N, K, 152)
     assert (segs[:, 2] > 0).any()          # the split really cuts tiles
-    if M * N <= 640 * 256:
-        y, _ = run(sv, x, w)
-        check(y, oracle_lib.gemm(x, w))
-    else:
-        y, _ = run(sv, x, w)
-        rng = np.random.default_rng(3)
-        s = sample_entries(rng, M, N)
-        check(y[s[:, 0], s[:, 1]], oracle_lib.gemm(x, w, samples=s))
+    y, _ = run(sv, x, w)
+    check(y, oracle_lib.gemm(x, w))
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 6144, 256), (300, 6272, 128), (384, 128, 64), (1024, 768, 512),
+                                   (257, 19584, 64), (768, 2304, 192), (2048, 6144, 64),
+                                   (812, 1792, 128), (5072, 256, 64)])
+def test_pair_tiles_full_compare(sv, oracle_lib, M, N, K):
+    """CTA-pair path (M > 256): ragged column tiles of 32-column multiples,
+    row blocks of 256 with a ragged last one, several tiles per pair; every
+    output against the oracle."""
+    x, w = synth.gemm_inputs(3 * M + N + K, M, N, K)
+    assert sv.gemm_workspace_size(M, N, K) == 0
+    y, _ = run(sv, x, w)
+    check(y, oracle_lib.gemm(x, w))
+
+
+def test_pair_status_clear_and_repeatable(sv):
+    """The pair kernel reports nothing in the status word and gives
+    bit-identical results call after call (whole tiles, fixed k order)."""
+    import torch
+    M, N, K = 512, 6144, 1024
+    x, w = synth.gemm_inputs(17, M, N, K)
+    xd, wd = bits_to_dev(x), bits_to_dev(w)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = [sv.verify_gemm(xd, wd, dev_status=st).clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
 
 
 def test_workspace_reused_and_left_zero(sv):
-    """One zeroed workspace serves many calls: each call leaves the arrival
-    counters zero again, and results are bit-identical (fixed summation
-    order, whichever piece of a cut tile arrives last)."""
+    """One zeroed workspace serves many weight-streaming calls: each call
+    leaves the arrival counters zero again, and results are bit-identical
+    (fixed summation order, whichever piece of a cut tile arrives last)."""
     import torch
-    M, N, K = 512, 6144, 6144
+    M, N, K = 64, 6144, 6144
     x, w = synth.gemm_inputs(11, M, N, K)
     xd, wd = bits_to_dev(x), bits_to_dev(w)
     ws = torch.zeros(sv.gemm_workspace_size(M, N, K), dtype=torch.uint8, device="cuda")
-    outs = [sv.verify_gemm(xd, wd, workspace=ws).clone() for _ in range(3)]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = [sv.verify_gemm(xd, wd, workspace=ws, dev_status=st).clone() for _ in range(3)]
     torch.cuda.synchronize()
+    assert int(st.item()) == 0
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
     counters = ws[:4096]                   # arrival counters of the cut tiles
     assert int(counters.count_nonzero()) == 0
+
+
+def test_workspace_zeroed_again_after_stale_counters(sv, oracle_lib):
+    """A call that stops on its bounded wait may leave arrival counters
+    non-zero; the contract is to zero the workspace again before the next
+    call.  Stale counters are planted on the host side of that contract
+    (the workspace filled with garbage), the workspace re-zeroed, and the
+    next call must be exact."""
+    import torch
+    M, N, K = 32, 768, 6144
+    x, w = synth.gemm_inputs(19, M, N, K)
+    xd, wd = bits_to_dev(x), bits_to_dev(w)
+    ws = torch.full((sv.gemm_workspace_size(M, N, K),), 7, dtype=torch.uint8, device="cuda")
+    ws.zero_()
+    y = sv.verify_gemm(xd, wd, workspace=ws)
+    torch.cuda.synchronize()
+    check(y.float().cpu().numpy().astype(np.float64), oracle_lib.gemm(x, w))
+    assert int(ws[:4096].count_nonzero()) == 0
 
 
 def test_graph_replay(sv, oracle_lib):
