@@ -46,6 +46,10 @@ UNIT = "tokens/s"
 WORKLOAD = dict(B=64, D=7, Hkv=8, G=8, head_dim=128, page_size=64, L_lo=4096, L_hi=131072,
                 V=131072, alpha=0.6, N=6144, K=6144, seed=2026)
 CASE_GROUPS = ("attention", "dsweep", "gemm", "accept", "logits", "adasd", "tree", "adaptive")
+# throughput attention: G(1+D) = 128 query rows per KV head, one full tile
+THROUGHPUT_CASE = dict(B=16, Hkv=8, G=8, D=15, L=32768)
+# large groups: the same cache verified at draft lengths around 128 / G - 1
+DSWEEP_CASE = dict(B=8, Hkv=4, G=32, L=131072, Ds=(0, 1, 3, 4, 7, 15))
 
 
 def peaks():
@@ -532,7 +536,8 @@ def run_cases(args, groups, dev, sv, flush, step=None):
 
     if "attention" in groups:
         # throughput regime: G(1+D) = 128, one full query tile per KV head
-        B, Hkv, G, D, L = 16, 8, 8, 15, 32768
+        c = THROUGHPUT_CASE
+        B, Hkv, G, D, L = c["B"], c["Hkv"], c["G"], c["D"], c["L"]
         inp = synth.attention_inputs_device(11, B, Hkv, G, 128, D, L, page_size=64, device=dev)
         out = torch.empty((B, D + 1, Hkv * G, 128), device=dev)
         lse = torch.empty((B, D + 1, Hkv * G), device=dev)
@@ -547,9 +552,10 @@ def run_cases(args, groups, dev, sv, flush, step=None):
     if "dsweep" in groups:
         # large groups: the same K/V cache (L = 131072 per sequence) verified
         # with D = 0, 1, 3, 4, 7, 15 (G(1+D) = 32 ... 512 query rows)
-        B, Hkv, G, L = 8, 4, 32, 131072
-        inp = synth.attention_inputs_device(20, B, Hkv, G, 128, 15, L, page_size=64, device=dev)
-        for D in (0, 1, 3, 4, 7, 15):
+        c = DSWEEP_CASE
+        B, Hkv, G, L = c["B"], c["Hkv"], c["G"], c["L"]
+        inp = synth.attention_inputs_device(20, B, Hkv, G, 128, max(c["Ds"]), L, page_size=64, device=dev)
+        for D in c["Ds"]:
             q = inp.q[:, :D + 1].contiguous()
             out = torch.empty((B, D + 1, Hkv * G, 128), device=dev)
             lse = torch.empty((B, D + 1, Hkv * G), device=dev)

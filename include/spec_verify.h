@@ -362,27 +362,31 @@ spec_status_t spec_accept_adasd(const float *p, const float *q, const int32_t *d
  * "Parallel random numbers: as easy as 1, 2, 3", SC'11; key = seed, word 0
  * of the output, u = (word >> 8) * 2^-24):
  *     u_acc[b][i] from counter (b, i, 0, 0),  u_res[b] from (b, 0, 1, 0).
- * The softmax is one fully specified fp32 procedure, so the decisions are
- * the same on every device: per row, m = max_v z_v, y_v = (z_v - m) *
- * fl32(1/T), e_v = exp_f32(y_v), Z = sum_v floor(e_v 2^55) (exact),
- * p_v = e_v / fl32(Z 2^-55) (IEEE division).  exp_f32(y): with log2 e =
- * hi + lo split into two fp32 values, t = y hi, n = rint(t),
- * f = (t - n) + fma(y, lo, fma(y, hi, -t)), e = P7(f) 2^n where P7 is the
- * degree-7 Taylor polynomial of 2^f (fp32 coefficients (ln 2)^k / k!,
- * Horner with fused multiply-adds), and e = 0 when n < -125.  Every step
- * rounds to nearest-even.
- * Every logit is read from HBM once for the row statistics; afterwards
- * only the gathered draft entries and the one row each sequence samples
- * from are read again.
+ * The probabilities are the fp32 roundings of the exact softmax, the rows
+ * spec_accept_sample would take:
+ *  - the row each sequence draws from (max(0, p_j - q_j) after a rejection
+ *    at j, else p_D) is evaluated to double-float accuracy and rounded once,
+ *    so each of its entries is the nearest fp32 to softmax(z / T) unless
+ *    the exact value lies within about 2^-33 (relative) of a rounding tie;
+ *  - the accept tests use a fast evaluation (hardware base-2 exponential,
+ *    fp32 row sums), relative error about 1e-7 (up to 1e-6 for logits far
+ *    below the row maximum): a decision can differ from the exact one only
+ *    when u_acc lies that close to p(x) / q(x).
+ * Every logit is read from HBM once for the row statistics; afterwards only
+ * the gathered draft entries and the one or two rows each sequence draws
+ * from are read again (twice: for their exact sums, then for the draw).
  *
  *   target_logits  device, fp32 [B][1+D][V]; finite or -inf.
  *   draft_logits   device, fp32 [B][D][V] (may be NULL if D = 0).
  *   temperature    T, finite and > 0.
  *   draft, n_accepted, token   as in spec_accept_sample.
  *   workspace  device, spec_accept_sample_logits_workspace_size(B, D, V)
- *              bytes, 256-byte aligned; scratch only (the row statistics
- *              (m, fl32(Z 2^-55)) of the B (2D + 1) rows, then the scratch
- *              of spec_accept_sample), needs no initialisation.
+ *              bytes, 256-byte aligned; scratch only (first the row
+ *              statistics (m = max_v z_v, Zf = sum_v 2^((z_v - m) log2(e) /
+ *              T) in fp32) of the B (2D + 1) rows as fp32 pairs, row
+ *              b (2D + 1) + k being target row k for k <= D and draft row
+ *              k - D - 1 otherwise; then the draw rows' exact partial sums and
+ *              the scratch of spec_accept_sample), needs no initialisation.
  * A row holding NaN or +inf, or only -inf, sets SPEC_DEV_ERR_LOGITS and
  * reads as all-zero probabilities.
  * Supported set: B <= 65535, 0 <= D <= 63, 1 <= V <= 2^26.

@@ -35,11 +35,14 @@ Parity status of each function (what pins it, in tests/test_oracle_*.py):
                     nothing stops; d_eff from rows of known entropy; the
                     first emitted token follows the draft distribution where
                     JS <= tau (chi-square) and the target elsewhere.
-  logits_to_probs   exp_f32 within 2 ulp of the exact exponential; the fp32
-                    softmax within its rounding bound of the fp64 softmax; its
-                    Philox equals the independent implementation of the
-                    published definition in synth bit for bit; temperature
-                    scaling and invariance to a constant shift of the logits.
+  logits_to_probs   the fp64 softmax rounded to fp32: exact invariance to a
+                    constant shift of the logits; a temperature of 1/2 equals
+                    doubled logits; equal maxima give fl32(1 / k); two
+                    logits give the logistic function; rows sum to 1 within
+                    their rounding; the first emitted token follows the
+                    target softmax (chi-square); its Philox equals the
+                    independent implementation of the published definition
+                    in synth bit for bit.
 """
 from __future__ import annotations
 
@@ -94,8 +97,6 @@ def _load():
             lib.oracle_adasd_stats.argtypes = [P, P, i32, i32, i32, P, P, i32]
             lib.oracle_accept_adasd.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_float, i32, i32, i32,
                                                 P, P, P, P, P, P, i32]
-            lib.oracle_exp_f32.argtypes = [P, P, i64]
-            lib.oracle_exp_f32.restype = None
             for f in ("oracle_verify_attention", "oracle_gemm", "oracle_accept_greedy",
                       "oracle_accept_sample", "oracle_max_threads", "oracle_tree_attention",
                       "oracle_accept_tree_greedy", "oracle_logits_to_probs", "oracle_logits_row_stats",
@@ -260,8 +261,8 @@ def accept_tree_greedy(p, tokens, parent, threads=0):
 
 
 def logits_to_probs(zp, zq, temperature, seed, threads=0):
-    """p, q (fp32 softmax of logits / temperature, reading R10) and the
-    Philox uniforms u_acc, u_res (reading R11)."""
+    """p, q (the fp64 softmax of logits / temperature rounded to fp32,
+    reading R10) and the Philox uniforms u_acc, u_res (reading R11)."""
     lib = _load()
     zp = _c(zp, np.float32)
     zq = _c(zq, np.float32)
@@ -279,7 +280,8 @@ def logits_to_probs(zp, zq, temperature, seed, threads=0):
 
 
 def logits_row_stats(zp, zq, temperature, threads=0):
-    """(m, zf) of reading R10 for every row: [B, 2D + 1] each, row k <= D
+    """(m, Z) of reading R10 for every row: m [B, 2D + 1] fp32 (the row
+    maximum) and Z [B, 2D + 1] fp64 (sum of exp((z - m) / T)), row k <= D
     being target row k and row k > D draft row k - D - 1; rows without a
     softmax (NaN, +inf or no finite entry) give (0, +inf)."""
     lib = _load()
@@ -288,12 +290,12 @@ def logits_row_stats(zp, zq, temperature, threads=0):
     B, T, V = zp.shape
     D = T - 1
     m = np.empty((B, 2 * D + 1), np.float32)
-    zf = np.empty((B, 2 * D + 1), np.float32)
-    rc = lib.oracle_logits_row_stats(_ptr(zp), _ptr(zq), float(temperature), B, D, V, _ptr(m), _ptr(zf),
+    Z = np.empty((B, 2 * D + 1), np.float64)
+    rc = lib.oracle_logits_row_stats(_ptr(zp), _ptr(zq), float(temperature), B, D, V, _ptr(m), _ptr(Z),
                                      int(threads))
     if rc < 0:
         raise ValueError(f"oracle_logits_row_stats failed: {rc}")
-    return m, zf
+    return m, Z
 
 
 def accept_sample_logits(zp, zq, draft, temperature, seed, threads=0):
@@ -341,11 +343,3 @@ def accept_adasd(p, q, draft, u_acc, u_res, tau_h, tau_js, threads=0):
     if rc:
         raise ValueError(f"oracle_accept_adasd failed: {rc}")
     return n, t, de, mu, ms, fb
-
-
-def exp_f32(y):
-    lib = _load()
-    y = _c(y, np.float32)
-    out = np.empty_like(y)
-    lib.oracle_exp_f32(_ptr(y), _ptr(out), y.size)
-    return out

@@ -487,18 +487,13 @@ int oracle_accept_tree_greedy(const float *p, const int32_t *tokens, const int32
  * "Mechanism") with p = softmax(target logits / T), q = softmax(draft
  * logits / T), and the uniforms drawn by Philox4x32-10 from a seed.
  *  R9  one temperature T > 0 for both models.
- *  R10 the softmax is taken in fp32 by a fully specified procedure, so that
- *      every device computes the same probabilities (the accept/reject
- *      decisions hinge on them):
- *        m = max_v z_v;  y_v = (z_v - m) * fl32(1/T);
- *        e_v = exp_f32(y_v) (below);  Z = sum_v floor(e_v * 2^55) exactly;
- *        p_v = e_v / fl32(Z * 2^-55)  (fp32 division).
- *      exp_f32(y), y <= 0: log2 e = hi + lo (fp32 parts); t = y * hi,
- *      n = rint(t), tl = fma(y, lo, fma(y, hi, -t)), f = (t - n) + tl;
- *      P(f) = the degree-7 Taylor polynomial of 2^f = e^(f ln 2) with fp32
- *      coefficients (ln 2)^k / k!, Horner with fused multiply-adds, and
- *      e = P(f) * 2^n; e = 0 when n < -125.  Every step rounds to nearest.
- *      fl32(Z * 2^-55) rounds the exact sum to nearest-even.
+ *  R10 the target "produces next-token probabilities" (llm-digest,
+ *      "Mechanism"): p_v = exp((z_v - m) / T) / sum_w exp((z_w - m) / T),
+ *      m = max_v z_v, all in fp64, then rounded to the nearest fp32 -- the
+ *      same fp32 probability rows the probability form of the acceptance
+ *      takes (the batched-acceptance workload's "fp32 target probs from
+ *      softmax").  A row holding NaN or +inf, or no finite entry, has no
+ *      softmax and reads as all-zero probabilities.
  *  R11 u_acc[b][i] = Philox4x32-10(key = seed, counter (b, i, 0, 0)) and
  *      u_res[b] = Philox4x32-10(key = seed, counter (b, 0, 1, 0)): word 0's
  *      top 24 bits times 2^-24 (Salmon et al., "Parallel random numbers: as
@@ -529,75 +524,9 @@ static float philox_u(uint64_t seed, uint32_t c0, uint32_t c1, uint32_t stream)
     return (float)((double)(c[0] >> 8) * 0x1p-24);
 }
 
-static float exp_f32(float y)
-{
-    /* log2 e = hi + lo, both fp32; y * log2 e = t + tl with the rounding
-     * error of y * hi recovered exactly by a fused multiply-add */
-    const float log2e_hi = 0x1.715476p+0f, log2e_lo = 0x1.4ae0c0p-26f;
-    const float c0 = 1.0f, c1 = 0x1.62e430p-1f, c2 = 0x1.ebfbe0p-3f, c3 = 0x1.c6b08ep-5f,
-                c4 = 0x1.3b2ab6p-7f, c5 = 0x1.5d87fep-10f, c6 = 0x1.430912p-13f,
-                c7 = 0x1.ffcbfcp-17f;
-    const float t = y * log2e_hi;
-    const float n = rintf(t);
-    if (!(n >= -125.0f)) return 0.0f;          /* also y = -inf */
-    const float tl = fmaf(y, log2e_lo, fmaf(y, log2e_hi, -t));
-    const float f = (t - n) + tl;
-    float p = c7;
-    p = fmaf(p, f, c6);
-    p = fmaf(p, f, c5);
-    p = fmaf(p, f, c4);
-    p = fmaf(p, f, c3);
-    p = fmaf(p, f, c2);
-    p = fmaf(p, f, c1);
-    p = fmaf(p, f, c0);
-    const uint32_t sb = (uint32_t)((int)n + 127) << 23;
-    float scale;
-    memcpy(&scale, &sb, sizeof scale);
-    return p * scale;
-}
-
-/* floor(x * 2^55) for 0 <= x < 2 (0 for anything else), from the bits. */
-static uint64_t fix55(float x)
-{
-    uint32_t b;
-    memcpy(&b, &x, sizeof b);
-    const uint32_t e = b >> 23;                 /* sign bit set: e >= 256 */
-    if (e > 127u || e == 0u) return 0;
-    const uint64_t m = (uint64_t)((b & 0x7FFFFFu) | 0x800000u) << 32;
-    const uint32_t sh = 127u - e;
-    return sh >= 64u ? 0 : m >> sh;
-}
-
-/* Z * 2^-55 rounded to the nearest fp32 (ties to even); Z > 0. */
-static float fix55_to_f32(unsigned __int128 Z)
-{
-    int top = 127;
-    while (!((Z >> top) & 1)) --top;
-    /* keep 24 bits: bits top..top-23 */
-    uint64_t mant;
-    int exp2 = top - 55;                        /* value = 1.xxx * 2^exp2 */
-    if (top >= 23) {
-        const int drop = top - 23;
-        mant = (uint64_t)(Z >> drop);
-        if (drop > 0) {
-            const unsigned __int128 rem = Z & ((((unsigned __int128)1) << drop) - 1);
-            const unsigned __int128 half = ((unsigned __int128)1) << (drop - 1);
-            if (rem > half || (rem == half && (mant & 1))) ++mant;
-            if (mant >> 24) { mant >>= 1; ++exp2; }
-        }
-    } else {
-        mant = (uint64_t)Z << (23 - top);
-    }
-    const uint32_t bits = ((uint32_t)(exp2 + 127) << 23) | ((uint32_t)mant & 0x7FFFFFu);
-    float f;
-    memcpy(&f, &bits, sizeof f);
-    return f;
-}
-
-/* Row statistics of reading R10: m = max_v z_v and zf = fl32(Z * 2^-55).
- * A row holding NaN or +inf, or no finite entry, has no softmax: it reads
- * as all-zero probabilities (m = 0, zf = +inf) and the call returns 1. */
-static int softmax_row_stats(const float *z, int V, float invT, float *m_out, float *zf_out)
+/* m = max_v z_v and Z = sum_v exp((z_v - m) / T) in fp64 (reading R10).
+ * Returns 1, with m = 0 and Z = +inf, for a row without a softmax. */
+static int softmax_row_stats(const float *z, int V, double T, float *m_out, double *Z_out)
 {
     int bad = 0;
     float m = -INFINITY;
@@ -607,21 +536,22 @@ static int softmax_row_stats(const float *z, int V, float invT, float *m_out, fl
     }
     if (bad || m == -INFINITY) {
         *m_out = 0.0f;
-        *zf_out = INFINITY;
+        *Z_out = INFINITY;
         return 1;
     }
-    unsigned __int128 Z = 0;
-    for (int v = 0; v < V; ++v) Z += fix55(exp_f32((z[v] - m) * invT));
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v) Z += exp(((double)z[v] - (double)m) / T);
     *m_out = m;
-    *zf_out = fix55_to_f32(Z);   /* Z >= 2^55: the maximum contributes exp_f32(0) = 1 */
+    *Z_out = Z;
     return 0;
 }
 
-static int softmax_f32(const float *z, int V, float invT, float *p)
+static int softmax_to_f32(const float *z, int V, double T, float *p)
 {
-    float m, zf;
-    const int bad = softmax_row_stats(z, V, invT, &m, &zf);
-    for (int v = 0; v < V; ++v) p[v] = bad ? 0.0f : exp_f32((z[v] - m) * invT) / zf;
+    float m;
+    double Z;
+    const int bad = softmax_row_stats(z, V, T, &m, &Z);
+    for (int v = 0; v < V; ++v) p[v] = bad ? 0.0f : (float)(exp(((double)z[v] - (double)m) / T) / Z);
     return bad;
 }
 
@@ -633,15 +563,15 @@ int oracle_logits_to_probs(const float *zp, const float *zq, float temperature, 
                            int num_threads)
 {
     if (B < 0 || D < 0 || V < 1 || !(temperature > 0.0f)) return -2;
-    const float invT = 1.0f / temperature;
+    const double T = temperature;
     set_threads(num_threads);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t r = 0; r < (int64_t)B * (2 * D + 1); ++r) {
         const int64_t b = r / (2 * D + 1), k = r % (2 * D + 1);
         if (k <= D)
-            softmax_f32(zp + (b * (1 + D) + k) * V, V, invT, p + (b * (1 + D) + k) * V);
+            softmax_to_f32(zp + (b * (1 + D) + k) * V, V, T, p + (b * (1 + D) + k) * V);
         else
-            softmax_f32(zq + (b * D + (k - D - 1)) * V, V, invT, q + (b * D + (k - D - 1)) * V);
+            softmax_to_f32(zq + (b * D + (k - D - 1)) * V, V, T, q + (b * D + (k - D - 1)) * V);
     }
     for (int b = 0; b < B; ++b) {
         for (int i = 0; i < D; ++i) u_acc[(int64_t)b * D + i] = philox_u(seed, (uint32_t)b, (uint32_t)i, 0u);
@@ -650,29 +580,23 @@ int oracle_logits_to_probs(const float *zp, const float *zq, float temperature, 
     return 0;
 }
 
-/* The row statistics (m, zf) of reading R10 for the B (2D + 1) rows, row
+/* The row statistics (m, Z) of reading R10 for the B (2D + 1) rows, row
  * b (2D + 1) + k being target row k for k <= D and draft row k - D - 1
  * otherwise.  Returns the number of rows without a softmax. */
 int oracle_logits_row_stats(const float *zp, const float *zq, float temperature, int B, int D, int V,
-                            float *m, float *zf, int num_threads)
+                            float *m, double *Z, int num_threads)
 {
     if (B < 0 || D < 0 || V < 1 || !(temperature > 0.0f)) return -2;
-    const float invT = 1.0f / temperature;
+    const double T = temperature;
     int nbad = 0;
     set_threads(num_threads);
 #pragma omp parallel for schedule(dynamic, 1) reduction(+ : nbad)
     for (int64_t r = 0; r < (int64_t)B * (2 * D + 1); ++r) {
         const int64_t b = r / (2 * D + 1), k = r % (2 * D + 1);
         const float *z = k <= D ? zp + (b * (1 + D) + k) * V : zq + (b * D + (k - D - 1)) * V;
-        nbad += softmax_row_stats(z, V, invT, m + r, zf + r);
+        nbad += softmax_row_stats(z, V, T, m + r, Z + r);
     }
     return nbad;
-}
-
-/* The exp_f32 of reading R10 on an array (for its pins). */
-void oracle_exp_f32(const float *y, float *out, int64_t n)
-{
-    for (int64_t i = 0; i < n; ++i) out[i] = exp_f32(y[i]);
 }
 
 /* ------------------------------------------------------------------------

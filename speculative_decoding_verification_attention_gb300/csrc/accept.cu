@@ -431,93 +431,127 @@ __device__ __forceinline__ unsigned long long scaled_threshold(float u, unsigned
 }
 
 // ------------------------------------------------------- from logits
-// The logits form of the stochastic acceptance takes p = softmax(zp / T)
-// and q = softmax(zq / T) through one fully specified fp32 procedure, so
-// that the accept/reject decisions do not depend on the device's own
-// exponential or summation order:
-//   m = max_v z_v;  y_v = (z_v - m) * fl32(1/T);  e_v = exp_f32(y_v);
-//   Z = sum_v floor(e_v * 2^55) (exact, 128-bit);  p_v = e_v / fl32(Z 2^-55).
-// exp_f32(y), y <= 0, is written here from the mathematics: log2 e = hi +
-// lo (fp32 parts), t = y hi, n = rint(t), f = (t - n) + fma(y, lo, fma(y,
-// hi, -t)), 2^f by its degree-7 Taylor polynomial (coefficients (ln 2)^k /
-// k! rounded to fp32, Horner with fused multiply-adds), times 2^n; 0 when
-// n < -125.  Every operation below rounds to nearest on its own (explicit
-// _rn intrinsics: no contraction).
-__device__ __forceinline__ float exp_f32(float y)
-{
-    const float log2e_hi = 0x1.715476p+0f, log2e_lo = 0x1.4ae0c0p-26f;
-    const float t = __fmul_rn(y, log2e_hi);
-    const float n = rintf(t);
-    if (!(n >= -125.0f)) return 0.0f;   // also y = -inf
-    const float tl = __fmaf_rn(y, log2e_lo, __fmaf_rn(y, log2e_hi, -t));
-    const float f = __fadd_rn(__fsub_rn(t, n), tl);
-    float p = 0x1.ffcbfcp-17f;
-    p = __fmaf_rn(p, f, 0x1.430912p-13f);
-    p = __fmaf_rn(p, f, 0x1.5d87fep-10f);
-    p = __fmaf_rn(p, f, 0x1.3b2ab6p-7f);
-    p = __fmaf_rn(p, f, 0x1.c6b08ep-5f);
-    p = __fmaf_rn(p, f, 0x1.ebfbe0p-3f);
-    p = __fmaf_rn(p, f, 0x1.62e430p-1f);
-    p = __fmaf_rn(p, f, 1.0f);
-    return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(static_cast<int>(n) + 127) << 23));
-}
+// The logits form takes p = softmax(zp / T) and q = softmax(zq / T).  Its
+// probabilities are the fp32 roundings of the exact softmax -- the fp32
+// probability rows the probability form takes -- evaluated two ways:
+//  * the accept tests and the row statistics use a fast evaluation: m =
+//    max_v z_v, Zf = sum_v 2^((z_v - m) c) with c = fl32(log2 e / T), the
+//    hardware base-2 exponential and fp32 sums in a fixed order, and
+//    p(x) = 2^((z_x - m) c) / Zf.  Its relative error (about 1e-7, up to
+//    1e-6 far below the maximum) can change a decision only when the
+//    uniform lies that close to p(x) / q(x);
+//  * the one row each sequence draws from (max(0, p_j - q_j), or p_D) is
+//    evaluated exactly up to the final rounding: (z - m) / T and exp in
+//    double-float arithmetic (unevaluated fp32 pairs hi + lo), the sum Z
+//    in double-float, and p_v = e_v / Z rounded to fp32 once.  Each p_v
+//    then is the nearest fp32 to the exact softmax unless the exact value
+//    lies within about 2^-33 (relative) of a rounding tie.
 
-// A 128-bit unsigned sum as (hi, lo).
-struct U128 {
-    unsigned long long lo, hi;
+struct DF {
+    float hi, lo;   // the unevaluated sum hi + lo
 };
 
-__device__ __forceinline__ void add128(U128 &a, unsigned long long x)
+// a + b exactly as hi + lo (Knuth's two-sum; every step rounds to nearest)
+__device__ __forceinline__ DF two_sum(float a, float b)
 {
-    a.lo += x;
-    a.hi += a.lo < x ? 1ull : 0ull;
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return {s, err};
 }
 
-__device__ __forceinline__ void add128(U128 &a, const U128 &x)
+// a + b for double-float values, renormalised
+__device__ __forceinline__ DF df_add(DF a, DF b)
 {
-    a.lo += x.lo;
-    a.hi += x.hi + (a.lo < x.lo ? 1ull : 0ull);
+    const DF s = two_sum(a.hi, b.hi);
+    const float lo = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+    const float hi = __fadd_rn(s.hi, lo);
+    return {hi, __fsub_rn(lo, __fsub_rn(hi, s.hi))};
 }
 
-__device__ __forceinline__ U128 warp_sum128(U128 a)
+// 2^(j / 256) for j = 0..255 as (hi, lo) fp32 pairs in the calling CTA's
+// shared memory: fp64 products of the constants 2^(2^i / 256), i = 0..7
+// (at most eight roundings of 2^-53 each).  Ends with __syncthreads.
+__device__ void build_exp2_table(float2 *tab)
 {
+    const double c[8] = {0x1.00b1afa5abcbfp+0, 0x1.0163da9fb3335p+0, 0x1.02c9a3e778061p+0,
+                         0x1.059b0d3158574p+0, 0x1.0b5586cf9890fp+0, 0x1.172b83c7d517bp+0,
+                         0x1.306fe0a31b715p+0, 0x1.6a09e667f3bcdp+0};
+    for (int j = threadIdx.x; j < 256; j += blockDim.x) {
+        double v = 1.0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        U128 x;
-        x.lo = __shfl_xor_sync(0xffffffffu, a.lo, o);
-        x.hi = __shfl_xor_sync(0xffffffffu, a.hi, o);
-        add128(a, x);
+        for (int i = 0; i < 8; ++i)
+            if ((j >> i) & 1) v = __dmul_rn(v, c[i]);
+        const float hi = __double2float_rn(v);
+        tab[j] = make_float2(hi, __double2float_rn(__dsub_rn(v, static_cast<double>(hi))));
     }
-    return a;
+    __syncthreads();
 }
 
-// Z * 2^-55 rounded to the nearest fp32, ties to even; Z > 0.  Z is shifted
-// left until its top bit is bit 127; the top 24 bits are the significand,
-// bit 103 the rounding bit and bits 0..102 the sticky bits.
-__device__ __forceinline__ float fix55_to_f32(U128 z)
+// exp(yh + yl) for yh + yl <= 0 as a double-float value, relative error
+// about 2^-33; 0 below -83 (e^-83 < 2^-119) and for -inf.
+//   k = rint((yh) 256 / ln 2);  r = y - k ln2 / 256, with ln2 / 256 split
+//   as C1 + C2 + C3 (C1 has 8 significant bits, so k C1 is exact for
+//   |k| < 2^15, and the first fused multiply-add is exact);  |r| <= ~ln2 /
+//   512;  e^r - 1 = r + r^2 (1/2 + r/6 + r^2/24) (Taylor, the next term
+//   is below 2^-41);  exp(y) = 2^(k >> 8) 2^((k & 255) / 256) e^r.
+__device__ __forceinline__ DF exp_df(float yh, float yl, const float2 *tab)
 {
-    const int top = z.hi ? 127 - __clzll(static_cast<long long>(z.hi)) : 63 - __clzll(static_cast<long long>(z.lo));
-    const int s = 127 - top;
-    unsigned long long h = z.hi, l = z.lo;
-    if (s >= 64) {
-        h = l << (s - 64);
-        l = 0ull;
-    } else if (s > 0) {
-        h = (h << s) | (l >> (64 - s));
-        l <<= s;
-    }
-    unsigned long long mant = h >> 40;                       // 24 bits
-    const bool round_bit = (h >> 39) & 1ull;
-    const bool sticky = (h & ((1ull << 39) - 1)) != 0ull || l != 0ull;
-    int exp2 = top - 55;
-    if (round_bit && (sticky || (mant & 1ull))) {
-        ++mant;
-        if (mant >> 24) {
-            mant >>= 1;
-            ++exp2;
-        }
-    }
-    return __uint_as_float((static_cast<uint32_t>(exp2 + 127) << 23) | (static_cast<uint32_t>(mant) & 0x7FFFFFu));
+    if (!(yh >= -83.0f)) return {0.0f, 0.0f};
+    const float kf = rintf(__fmul_rn(yh, 0x1.715476p+8f));
+    float t = __fmaf_rn(-kf, 0x1.62p-9f, yh);
+    t = __fmaf_rn(-kf, 0x1.c85fep-18f, t);
+    t = __fmaf_rn(-kf, -0x1.718432p-43f, t);
+    const float r = __fadd_rn(t, yl);
+    float s = __fmaf_rn(r, 0x1.555556p-5f, 0x1.555556p-3f);   // 1/24, 1/6
+    s = __fmaf_rn(s, r, 0.5f);
+    s = __fmul_rn(__fmul_rn(s, r), r);
+    const float em1 = __fadd_rn(r, s);                          // e^r - 1
+    const int k = static_cast<int>(kf);
+    const float2 tj = tab[k & 255];
+    const float scale = __int_as_float(((k >> 8) + 127) << 23);   // 2^(k >> 8), k >> 8 >= -121
+    return {__fmul_rn(tj.x, scale), __fmul_rn(__fmaf_rn(tj.x, em1, tj.y), scale)};
+}
+
+// Parameters of one logits row for the exact evaluation: 1/T = ih + il,
+// 1/Z = rh + rl (rh = 0: the row has no softmax, every probability is 0).
+struct SoftmaxRow {
+    float m, ih, il, rh, rl;
+};
+
+// exp((z - m) / T) as a double-float value.
+__device__ __forceinline__ DF softmax_exp(float z, const SoftmaxRow &r, const float2 *tab)
+{
+    const DF d = two_sum(z, -r.m);   // z - m exactly
+    const float yh = __fmul_rn(d.hi, r.ih);
+    const float yl = __fadd_rn(__fmaf_rn(d.hi, r.ih, -yh), __fmaf_rn(d.hi, r.il, __fmul_rn(d.lo, r.ih)));
+    return exp_df(yh, yl, tab);
+}
+
+// The fp32 rounding of softmax(z / T)_v: the double-float quotient e / Z
+// rounded once.
+__device__ __forceinline__ float softmax_prob(float z, const SoftmaxRow &r, const float2 *tab)
+{
+    if (r.rh == 0.0f) return 0.0f;
+    const DF e = softmax_exp(z, r, tab);
+    const float qh = __fmul_rn(e.hi, r.rh);
+    const float ql = __fadd_rn(__fmaf_rn(e.hi, r.rh, -qh), __fmaf_rn(e.hi, r.rl, __fmul_rn(e.lo, r.rh)));
+    return __fadd_rn(qh, ql);
+}
+
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The fast probability of the accept tests from the row statistics (m, Zf)
+// and c = fl32(log2 e / T); 0 for a row without a softmax (Zf = +inf).
+__device__ __forceinline__ float fast_prob(float z, float2 stat, float c)
+{
+    if (!(stat.y < INFINITY)) return 0.0f;
+    return __fdiv_rn(ex2_approx(__fmul_rn(__fsub_rn(z, stat.x), c)), stat.y);
 }
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
@@ -539,46 +573,62 @@ __device__ __forceinline__ float philox_u(unsigned long long seed, uint32_t c0, 
     return __fmul_rn(__uint2float_rn(x0 >> 8), 0x1p-24f);
 }
 
-// A row of logits' softmax parameters: p_v = exp_f32((z_v - m) / T) / zf.
-struct SoftmaxRow {
-    float m, zf, inv_t;
-};
-
-__device__ __forceinline__ float softmax_prob(float z, const SoftmaxRow &r)
-{
-    return __fdiv_rn(exp_f32(__fmul_rn(__fsub_rn(z, r.m), r.inv_t)), r.zf);
-}
-
 // Inputs of the stochastic acceptance.  Probability form: p, q and the
 // uniforms u_acc, u_res.  Logits form: p, q hold the target / draft logits,
-// stats the softmax parameters (m, zf) of every row -- row b (2D + 1) + k
-// is target row k for k <= D and draft row k - D - 1 otherwise -- and the
-// uniforms come from Philox with key `seed`: u_acc[b][i] from counter
-// (b, i, 0, 0), u_res[b] from (b, 0, 1, 0).
+// stats the fast statistics (m, Zf) of every row -- row b (2D + 1) + k is
+// target row k for k <= D and draft row k - D - 1 otherwise -- zparts the
+// double-float partial sums of exp((z - m) / T) over the nzchunks chunks of
+// each sequence's draw rows ([b][0]: the target row, [b][1]: the draft
+// row), and the uniforms come from Philox with key `seed`: u_acc[b][i] from
+// counter (b, i, 0, 0), u_res[b] from (b, 0, 1, 0).
 struct SampleIn {
     const float *p, *q;
     const float *u_acc, *u_res;
     const float2 *stats;
-    float inv_t;
+    const float2 *zparts;
+    int nzchunks;
+    float c_fast;          // fl32(log2 e / T)
+    float ih, il;          // 1 / T as a double-float value
     unsigned long long seed;
 };
 
+// The exact-evaluation parameters of row k (0..2D) of sequence b, which is
+// its draw row `which` (0: target, 1: draft): Z is the sum of the row's
+// partial sums in chunk order, 1 / Z refined by one Newton step.  Every
+// caller computes the same value from the same inputs.
 template <bool LOGITS>
-__device__ __forceinline__ SoftmaxRow row_params(const SampleIn &in, int b, int D, int k)
+__device__ __forceinline__ SoftmaxRow draw_row(const SampleIn &in, int b, int D, int k, int which)
 {
-    SoftmaxRow r{0.0f, 1.0f, 1.0f};
+    SoftmaxRow r{0.0f, 1.0f, 0.0f, 1.0f, 0.0f};
     if (LOGITS) {
-        const float2 s = __ldcg(in.stats + static_cast<int64_t>(b) * (2 * D + 1) + k);
-        r = {s.x, s.y, in.inv_t};
+        const float2 st = __ldcg(in.stats + static_cast<int64_t>(b) * (2 * D + 1) + k);
+        r.m = st.x;
+        r.ih = in.ih;
+        r.il = in.il;
+        if (!(st.y < INFINITY)) {
+            r.rh = 0.0f;
+            return r;
+        }
+        DF Z{0.0f, 0.0f};
+        const float2 *zp = in.zparts + (static_cast<int64_t>(b) * 2 + which) * in.nzchunks;
+        for (int c = 0; c < in.nzchunks; ++c) {
+            const float2 t = __ldcg(zp + c);
+            Z = df_add(Z, DF{t.x, t.y});
+        }
+        const float rh = __frcp_rn(Z.hi);
+        const float err = __fsub_rn(__fmaf_rn(-Z.hi, rh, 1.0f), __fmul_rn(Z.lo, rh));
+        r.rh = rh;
+        r.rl = __fmul_rn(rh, err);
     }
     return r;
 }
 
 template <bool LOGITS>
-__device__ __forceinline__ float4 to_prob4(float4 z, const SoftmaxRow &r)
+__device__ __forceinline__ float4 to_prob4(float4 z, const SoftmaxRow &r, const float2 *tab)
 {
     if (!LOGITS) return z;
-    return make_float4(softmax_prob(z.x, r), softmax_prob(z.y, r), softmax_prob(z.z, r), softmax_prob(z.w, r));
+    return make_float4(softmax_prob(z.x, r, tab), softmax_prob(z.y, r, tab), softmax_prob(z.z, r, tab),
+                       softmax_prob(z.w, r, tab));
 }
 
 // Value read for an element past the end of a row: no mass either way.
@@ -655,8 +705,9 @@ __global__ void __launch_bounds__(kThreads) accept_prep_kernel(SampleIn in, cons
                 float qv = in.q[(static_cast<int64_t>(b) * D + i) * V + x];
                 float uf;
                 if (LOGITS) {
-                    pv = softmax_prob(pv, row_params<true>(in, b, D, i));
-                    qv = softmax_prob(qv, row_params<true>(in, b, D, D + 1 + i));
+                    const float2 *st = in.stats + static_cast<int64_t>(b) * (2 * D + 1);
+                    pv = fast_prob(pv, __ldcg(st + i), in.c_fast);
+                    qv = fast_prob(qv, __ldcg(st + D + 1 + i), in.c_fast);
                     uf = philox_u(in.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
                 } else {
                     uf = in.u_acc[static_cast<int64_t>(b) * D + i];
@@ -683,7 +734,7 @@ template <bool SMEM, bool LOGITS>
 __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, const float *sq,
                                                                int residual, int w0, int n, bool vec4,
                                                                int lane, const SoftmaxRow &rp,
-                                                               const SoftmaxRow &rq)
+                                                               const SoftmaxRow &rq, const float2 *tab)
 {
     unsigned long long mine = 0;
 #pragma unroll
@@ -699,8 +750,8 @@ __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, 
                 xp = load4(sp, e, n, vec4, pad_value<LOGITS>());
                 if (residual) xq = load4(sq, e, n, vec4, pad_value<LOGITS>());
             }
-            xp = to_prob4<LOGITS>(xp, rp);
-            if (residual) xq = to_prob4<LOGITS>(xq, rq);
+            xp = to_prob4<LOGITS>(xp, rp, tab);
+            if (residual) xq = to_prob4<LOGITS>(xq, rq, tab);
             m = mass(xp.x, xq.x, residual) + mass(xp.y, xq.y, residual) + mass(xp.z, xq.z, residual) +
                 mass(xp.w, xq.w, residual);
         }
@@ -727,7 +778,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
     float *ring = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_raw) + 127) & ~uintptr_t(127));
     __shared__ uint64_t full[kRing], empty[kRing];
     __shared__ int s_j[kRing];
-    __shared__ float4 s_rows[kRing];   // LOGITS: (m, zf) of the target row, then of the draft row
+    __shared__ SoftmaxRow s_rp[kRing], s_rq[kRing];   // LOGITS: the draw rows' parameters
+    __shared__ float2 s_tab[LOGITS ? 256 : 1];
     __shared__ int s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
@@ -736,9 +788,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
         s_abort = 0;
         fence_mbar_init();
     }
+    if (LOGITS) build_exp2_table(s_tab);
     __syncthreads();
     pdl_launch_dependents();
-    pdl_wait();   // js comes from the previous kernel
+    pdl_wait();   // js (and, for logits, the draw rows' sums) come from the previous kernels
 
     if (warp == kConsumers) {
         if (lane == 0) {
@@ -753,9 +806,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
                 const DrawRow dr = decode_draw(code);
                 const int j = dr.j;
                 if (LOGITS) {
-                    const SoftmaxRow rp = row_params<true>(in, b, D, j);
-                    const SoftmaxRow rq = dr.residual ? row_params<true>(in, b, D, D + 1 + j) : rp;
-                    s_rows[slot] = make_float4(rp.m, rp.zf, rq.m, rq.zf);
+                    s_rp[slot] = draw_row<true>(in, b, D, j, 0);
+                    s_rq[slot] = dr.residual ? draw_row<true>(in, b, D, D + 1 + j, 1) : s_rp[slot];
                 }
                 if (bulk) {
                     const int64_t e0 = static_cast<int64_t>(chunk) * kChunk;
@@ -783,11 +835,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
         const DrawRow dr = decode_draw(s_j[slot]);
         const int j = dr.j;
         const int residual = dr.residual;
-        SoftmaxRow rp{0.0f, 1.0f, 1.0f}, rq{0.0f, 1.0f, 1.0f};
+        SoftmaxRow rp{0.0f, 1.0f, 0.0f, 1.0f, 0.0f}, rq = rp;
         if (LOGITS) {
-            const float4 r = s_rows[slot];
-            rp = {r.x, r.y, in.inv_t};
-            rq = {r.z, r.w, in.inv_t};
+            rp = s_rp[slot];
+            rq = s_rq[slot];
         }
         const int64_t e0 = static_cast<int64_t>(chunk) * kChunk;
         const int n = static_cast<int>(imin64(kChunk, V - e0));
@@ -800,8 +851,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
             sq = residual ? q + (static_cast<int64_t>(b) * D + j) * V + e0 : nullptr;
         }
         const unsigned long long t =
-            bulk ? warp_step_masses<true, LOGITS>(sp, sq, residual, warp * kGroup, n, true, lane, rp, rq)
-                 : warp_step_masses<false, LOGITS>(sp, sq, residual, warp * kGroup, n, false, lane, rp, rq);
+            bulk ? warp_step_masses<true, LOGITS>(sp, sq, residual, warp * kGroup, n, true, lane, rp, rq, s_tab)
+                 : warp_step_masses<false, LOGITS>(sp, sq, residual, warp * kGroup, n, false, lane, rp, rq, s_tab);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
         const int s0 = chunk * (kChunk / kStep) + warp * kGroupSteps;
@@ -810,6 +861,77 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
         const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull);
         const int gi = chunk * kConsumers + warp;
         if (lane == 0 && gi < sc.ngroups) sc.gtot[static_cast<int64_t>(b) * sc.ngroups + gi] = gt;
+    }
+}
+
+// Logits form, between stages 1 and 2: the exact row sums Z = sum_v
+// exp((z_v - m) / T) of each sequence's draw rows (the target row j and,
+// for a residual draw, the draft row j), in double-float.  One CTA per
+// (sequence, 8192-element chunk): each thread evaluates 32 elements of
+// each row (all its loads in flight first), the CTA adds the threads' sums
+// in a fixed order and writes the chunk's partial sum to zparts.
+constexpr int kZChunk = 8192;
+constexpr int kZPerThread = kZChunk / kThreads;   // 32
+
+__device__ __forceinline__ DF warp_sum_df(DF a)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const DF x{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+        a = df_add(a, x);
+    }
+    return a;
+}
+
+__global__ void __launch_bounds__(kThreads) logits_draw_sums_kernel(SampleIn in, int D, int V, SampleScratch sc,
+                                                                     bool vec4, float2 *__restrict__ zparts)
+{
+    __shared__ float2 s_tab[256];
+    __shared__ DF s_w[kWarps];
+    build_exp2_table(s_tab);
+    pdl_launch_dependents();
+    pdl_wait();   // the draw row comes from the previous kernel
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x / in.nzchunks, chunk = blockIdx.x % in.nzchunks;
+    const DrawRow dr = decode_draw(__ldcg(sc.js + b));
+    const int j = dr.j;
+    const int64_t e0 = static_cast<int64_t>(chunk) * kZChunk;
+    const int n = static_cast<int>(imin64(kZChunk, V - e0));
+    for (int which = 0; which < (dr.residual ? 2 : 1); ++which) {
+        const int k = which ? D + 1 + j : j;
+        const float2 st = __ldcg(in.stats + static_cast<int64_t>(b) * (2 * D + 1) + k);
+        const float *row = (which ? in.q + (static_cast<int64_t>(b) * D + j) * V
+                                  : in.p + (static_cast<int64_t>(b) * (D + 1) + j) * V) + e0;
+        DF acc{0.0f, 0.0f};
+        if (st.y < INFINITY) {
+            const SoftmaxRow r{st.x, in.ih, in.il, 1.0f, 0.0f};
+            float4 z[kZPerThread / 4];
+#pragma unroll
+            for (int u = 0; u < kZPerThread / 4; ++u) {
+                const int e = (u * kThreads + threadIdx.x) * 4;
+                z[u] = e < n ? load4(row, e, n, vec4, -INFINITY) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < kZPerThread / 4; ++u) {
+                const float v[4] = {z[u].x, z[u].y, z[u].z, z[u].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const DF e = softmax_exp(v[c], r, s_tab);
+                    const DF t = two_sum(acc.hi, e.hi);
+                    acc.hi = t.hi;
+                    acc.lo = __fadd_rn(acc.lo, __fadd_rn(t.lo, e.lo));
+                }
+            }
+        }
+        acc = warp_sum_df(acc);
+        if (lane == 0) s_w[warp] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            DF t = s_w[0];
+            for (int w = 1; w < kWarps; ++w) t = df_add(t, s_w[w]);
+            zparts[(static_cast<int64_t>(b) * 2 + which) * in.nzchunks + chunk] = make_float2(t.hi, t.lo);
+        }
+        __syncthreads();
     }
 }
 
@@ -824,6 +946,8 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
 {
     const float *__restrict__ p = in.p;
     const float *__restrict__ q = in.q;
+    __shared__ float2 s_tab[LOGITS ? 256 : 1];
+    if (LOGITS) build_exp2_table(s_tab);
     pdl_wait();   // step and group masses come from the previous kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * kWarps + warp;
@@ -835,8 +959,8 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
     const float *qrow = residual ? q + (static_cast<int64_t>(b) * D + j) * V : nullptr;
     unsigned long long *steps = sc.steps + static_cast<int64_t>(b) * sc.nsteps;
     unsigned long long *gtot = sc.gtot + static_cast<int64_t>(b) * sc.ngroups;
-    const SoftmaxRow rp = row_params<LOGITS>(in, b, D, j);
-    const SoftmaxRow rq = residual ? row_params<LOGITS>(in, b, D, D + 1 + j) : rp;
+    const SoftmaxRow rp = draw_row<LOGITS>(in, b, D, j, 0);
+    const SoftmaxRow rq = residual ? draw_row<LOGITS>(in, b, D, D + 1 + j, 1) : rp;
 
     float u = LOGITS ? philox_u(in.seed, static_cast<uint32_t>(b), 0u, 1u) : in.u_res[b];
     if (!(u >= 0.0f && u < 1.0f)) {
@@ -857,7 +981,7 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
             const int64_t g0 = static_cast<int64_t>(g) * kGroup;
             const int n = static_cast<int>(imin64(kGroup, V - g0));
             const unsigned long long t =
-                warp_step_masses<false, LOGITS>(prow + g0, nullptr, 0, 0, n, false, lane, rp, rq);
+                warp_step_masses<false, LOGITS>(prow + g0, nullptr, 0, 0, n, false, lane, rp, rq, s_tab);
             if (lane < kGroupSteps && g * kGroupSteps + lane < sc.nsteps) steps[g * kGroupSteps + lane] = t;
             const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull);
             if (lane == 0) gtot[g] = gt;
@@ -903,8 +1027,9 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
         // the element within the step
         const int64_t e = static_cast<int64_t>(step) * kStep + lane * 4;
         const float pad = pad_value<LOGITS>();
-        const float4 xp = to_prob4<LOGITS>(e < V ? load4(prow, e, V, vec4, pad) : make_float4(pad, pad, pad, pad), rp);
-        const float4 xq = (residual && e < V) ? to_prob4<LOGITS>(load4(qrow, e, V, vec4, pad), rq)
+        const float4 xp =
+            to_prob4<LOGITS>(e < V ? load4(prow, e, V, vec4, pad) : make_float4(pad, pad, pad, pad), rp, s_tab);
+        const float4 xq = (residual && e < V) ? to_prob4<LOGITS>(load4(qrow, e, V, vec4, pad), rq, s_tab)
                                               : make_float4(0, 0, 0, 0);
         const unsigned long long m[4] = {mass(xp.x, xq.x, residual), mass(xp.y, xq.y, residual),
                                          mass(xp.z, xq.z, residual), mass(xp.w, xq.w, residual)};
@@ -1065,7 +1190,9 @@ __global__ void __launch_bounds__(kThreads) adasd_prep_kernel(
 }
 
 // Logits row statistics: for every row of the target and draft logits,
-// m = max_v z_v and zf = fl32(2^-55 sum_v floor(exp_f32((z_v - m) / T) 2^55)).
+// m = max_v z_v and Zf = sum_v 2^((z_v - m) c), c = fl32(log2 e / T) (the
+// fast evaluation of the accept tests: hardware exponential, fp32 sums in
+// a fixed order).
 //
 // One thread-block cluster of CS CTAs works on one row at a time, CTA
 // `rank` owning the elements [rank * slice, (rank + 1) * slice); clusters
@@ -1076,30 +1203,10 @@ __global__ void __launch_bounds__(kThreads) adasd_prep_kernel(
 // L2).  Pass 1 takes the slice maximum; the CTAs exchange their maxima
 // through distributed shared memory (asynchronous stores that complete on
 // the receiver's mbarrier; no cluster-wide barrier per row).  Pass 2 sums
-// the fixed-point exponentials; the partial sums go to the row's owner
-// (rank = row iteration mod CS), which writes (m, zf).  Rows whose maximum
-// is not finite, or that hold NaN or +inf, get zf = +inf (every
-// probability 0) and set SPEC_DEV_ERR_LOGITS.
-//
-// Pass 2 evaluates exp_f32 on pairs of elements with packed fp32x2
-// instructions, each step rounding exactly like the scalar definition
-// (add/sub/mul/fma .rn on both halves).  Two rewrites keep it bit-identical:
-//  - it carries the negations t' = -t = y * (-hi) and F = -f, so that no
-//    operand needs negating: fma(y, hi, t') is fma(y, hi, -t), and the
-//    Taylor polynomial in F with coefficients (-1)^k c_k yields exactly the
-//    same Horner values as the polynomial in f (round to nearest is
-//    symmetric);
-//  - rint(t) is r - 1.5 * 2^23 with r = t + 1.5 * 2^23, exact with ties to
-//    even for |t| < 2^22, and then the bits of r are 0x4B400000 + n.
-// The fixed-point term floor(P 2^n 2^55), P = mp 2^(ep - 150) the
-// polynomial value, is mp 2^s with s = ep + n - 95 <= 32: for s >= 1 it is
-// 2 * (mp * 2^(s - 1)) (one 32 x 32 -> 64-bit multiply-add), for s <= 0 it
-// is mp >> -s; both shifts clamp at 32, so the other case contributes 0 and
-// no branch is needed.  Far below the maximum (|t| >= 2^22, y = -inf) the
-// bits of r leave 0x4B000000..0x4B400000 and both shift counts exceed 31,
-// so such elements add 0, as the definition's do: no clamp is needed.
-// (Checked on the host against the scalar definition for every negative
-// fp32 value and -inf.)
+// the exponentials; the partial sums go to the row's owner (rank = row
+// iteration mod CS), which adds them in rank order and writes (m, Zf).
+// Rows whose maximum is not finite, or that hold NaN or +inf, get Zf = +inf
+// (every probability 0) and set SPEC_DEV_ERR_LOGITS.
 __device__ __forceinline__ unsigned long long pack2(float lo, float hi)
 {
     return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
@@ -1115,96 +1222,11 @@ __device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigne
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b)
-{
-    unsigned long long d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b)
-{
-    unsigned long long d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c)
-{
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-// 2^s for s < 32, 0 for s >= 32 (s as unsigned: negatives are huge):
-// (1:0) << s, upper word, shift count clamped at 32.
-__device__ __forceinline__ uint32_t pow2_clamp(uint32_t s)
-{
-    uint32_t d;
-    asm("shf.l.clamp.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(0u), "r"(1u), "r"(s));
-    return d;
-}
-// x >> s, 0 for s >= 32: (0:x) >> s, lower word, shift count clamped at 32.
-__device__ __forceinline__ uint32_t shr_clamp(uint32_t x, uint32_t s)
-{
-    uint32_t d;
-    asm("shf.r.clamp.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(0u), "r"(s));
-    return d;
-}
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
-}
-
-// Row constants of pass 2, packed for both halves of a pair.
-struct ExpConsts {
-    unsigned long long neg_m, inv_t, neg_hi, hi, lo, magic, c[8];
-};
-
-__device__ __forceinline__ ExpConsts exp_consts(float m, float inv_t)
-{
-    ExpConsts k;
-    k.neg_m = pack2(-m, -m);
-    k.inv_t = pack2(inv_t, inv_t);
-    k.neg_hi = pack2(-0x1.715476p+0f, -0x1.715476p+0f);
-    k.hi = pack2(0x1.715476p+0f, 0x1.715476p+0f);
-    k.lo = pack2(0x1.4ae0c0p-26f, 0x1.4ae0c0p-26f);
-    k.magic = pack2(0x1.8p+23f, 0x1.8p+23f);
-    const float c[8] = {1.0f, 0x1.62e430p-1f, 0x1.ebfbe0p-3f, 0x1.c6b08ep-5f,
-                        0x1.3b2ab6p-7f, 0x1.5d87fep-10f, 0x1.430912p-13f, 0x1.ffcbfcp-17f};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) k.c[i] = (i & 1) ? pack2(-c[i], -c[i]) : pack2(c[i], c[i]);
-    return k;
-}
-
-// One element's fixed-point term from the polynomial value P (bits pb) and
-// r = t + 1.5 * 2^23 (bits rb): adds to big (terms / 2 for s >= 1) or small.
-__device__ __forceinline__ void fix_term(uint32_t pb, uint32_t rb, unsigned long long &big, uint32_t &small)
-{
-    const uint32_t mp = (pb & 0x7FFFFFu) | 0x800000u;
-    const uint32_t ep = pb >> 23;
-    // s - 1 = ep + (rb - 0x4B400000) - 96, -s = 0x4B400000 + 95 - ep - rb (mod 2^32)
-    const uint32_t s1 = ep + rb - (0x4B400000u + 96u);
-    const uint32_t ns = (0x4B400000u + 95u) - ep - rb;
-    big += static_cast<unsigned long long>(mp) * pow2_clamp(s1);
-    small += shr_clamp(mp, ns);
-}
-
-// floor(exp_f32((z - m) / T) 2^55) of the two elements of a pair, added to
-// big / small.
-__device__ __forceinline__ void pair_terms(unsigned long long z2, const ExpConsts &k, unsigned long long &big,
-                                           uint32_t &small)
-{
-    const unsigned long long y = mul2(add2(z2, k.neg_m), k.inv_t);
-    const unsigned long long tn = mul2(y, k.neg_hi);            // -t
-    const unsigned long long tl = fma2(y, k.lo, fma2(y, k.hi, tn));
-    const unsigned long long r = sub2(k.magic, tn);             // t + 1.5 * 2^23
-    const unsigned long long n = sub2(r, k.magic);              // rint(t)
-    const unsigned long long F = sub2(add2(tn, n), tl);         // -f
-    unsigned long long P = k.c[7];
-#pragma unroll
-    for (int i = 6; i >= 0; --i) P = fma2(P, F, k.c[i]);
-    fix_term(static_cast<uint32_t>(P), static_cast<uint32_t>(r), big, small);
-    fix_term(static_cast<uint32_t>(P >> 32), static_cast<uint32_t>(r >> 32), big, small);
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
@@ -1217,32 +1239,23 @@ __device__ __forceinline__ void cluster_sync_all()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void st_async_peer_v2(uint32_t addr, unsigned long long a, unsigned long long b,
-                                                 uint32_t bar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b64 [%0], {%1, %2}, [%3];" ::"r"(addr),
-                 "l"(a), "l"(b), "r"(bar)
-                 : "memory");
-}
-
 constexpr int kStatsThreads = 256;
 constexpr int kStatsWarps = kStatsThreads / 32;
 constexpr int kStatsMinBlocks = 3;                 // CTAs per SM (shared memory allows 3 slices of 64 KB)
-constexpr int kStatsChunk = 256 * kStatsThreads;   // elements per partial sum: 256 per thread
 
 template <int CS, bool BULK>
 __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) logits_rowstats_kernel(
-    const float *__restrict__ zp, const float *__restrict__ zq, int B, int D, int V, float inv_t, int slice,
+    const float *__restrict__ zp, const float *__restrict__ zq, int B, int D, int V, float c_fast, int slice,
     bool vec4, float2 *__restrict__ stats, uint32_t *dev_status)
 {
     extern __shared__ uint8_t s_raw[];
     float *buf = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_raw) + 127) & ~uintptr_t(127));
     __shared__ uint64_t full, bar_max[2], bar_sum[2];
     __shared__ unsigned long long s_xmax[2][CS];   // (bad << 32) | bits of CTA c's max, by row parity
-    __shared__ ulonglong2 s_xsum[2][CS];           // CTA c's exact partial sum (lo, hi), owned rows
+    __shared__ unsigned long long s_xsum[2][CS];   // CTA c's partial sum (bits), owned rows
     __shared__ float s_wmax[kStatsWarps];
     __shared__ int s_wbad[kStatsWarps];
-    __shared__ U128 s_wsum[kStatsWarps];
+    __shared__ float s_wsum[kStatsWarps];
     __shared__ int s_abort;
     volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1280,14 +1293,14 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) logits_rowstat
     auto finish_row = [&](int k, int r, float m, int rbad) {
         const int slot = (k / CS) & 1;
         if (CS > 1 && !mbar_wait(&bar_sum[slot], ((k / CS) >> 1) & 1, abort, dev_status)) return;
-        U128 z{0ull, 0ull};
-        for (int c = 0; c < CS; ++c) add128(z, U128{s_xsum[slot][c].x, s_xsum[slot][c].y});
+        float z = 0.0f;
+        for (int c = 0; c < CS; ++c) z = __fadd_rn(z, __uint_as_float(static_cast<uint32_t>(s_xsum[slot][c])));
         float2 st;
-        if (rbad || (z.lo == 0ull && z.hi == 0ull)) {
+        if (rbad || !(z > 0.0f)) {
             report(dev_status, SPEC_DEV_ERR_LOGITS);
             st = make_float2(0.0f, INFINITY);
         } else {
-            st = make_float2(m, fix55_to_f32(z));
+            st = make_float2(m, z);
         }
         stats[r] = st;
     };
@@ -1308,7 +1321,7 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) logits_rowstat
             }
             if (CS > 1) {
                 mbar_arrive_expect_tx(&bar_max[k & 1], CS * 8u);
-                if (owner == static_cast<int>(rank)) mbar_arrive_expect_tx(&bar_sum[(k / CS) & 1], CS * 16u);
+                if (owner == static_cast<int>(rank)) mbar_arrive_expect_tx(&bar_sum[(k / CS) & 1], CS * 8u);
             }
             // while this row's slice lands: the sums of the previous owned row
             if (pend_k >= 0) {
@@ -1364,35 +1377,31 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) logits_rowstat
             rbad |= static_cast<int>(w >> 32);
         }
         rbad |= !(m > -INFINITY) | !(m < INFINITY);
-        // pass 2: the exact fixed-point sum of the exponentials
-        U128 acc{0ull, 0ull};
+        // pass 2: the sum of the exponentials, in a fixed order
+        float acc = 0.0f;
         if (!rbad) {
-            const ExpConsts kc = exp_consts(m, inv_t);
-            for (int base = 0; base < len; base += kStatsChunk) {
-                const int end = static_cast<int>(imin64(len, static_cast<int64_t>(base) + kStatsChunk));
-                unsigned long long big = 0ull;   // at most 256 terms of at most 2^54
-                uint32_t small = 0u;             // at most 256 terms below 2^24
-                for (int i = base + tid * 4; i < end; i += kStatsThreads * 4) {
-                    const float4 v =
-                        BULK ? *reinterpret_cast<const float4 *>(src + i) : load4(src, i, end, vec4, -INFINITY);
-                    pair_terms(pack2(v.x, v.y), kc, big, small);
-                    pair_terms(pack2(v.z, v.w), kc, big, small);
-                }
-                add128(acc, (big << 1) + small);
+            for (int i = tid * 4; i < len; i += kStatsThreads * 4) {
+                const float4 v = BULK ? *reinterpret_cast<const float4 *>(src + i) : load4(src, i, len, vec4, -INFINITY);
+                const float e0 = ex2_approx(__fmul_rn(__fsub_rn(v.x, m), c_fast));
+                const float e1 = ex2_approx(__fmul_rn(__fsub_rn(v.y, m), c_fast));
+                const float e2 = ex2_approx(__fmul_rn(__fsub_rn(v.z, m), c_fast));
+                const float e3 = ex2_approx(__fmul_rn(__fsub_rn(v.w, m), c_fast));
+                acc = __fadd_rn(acc, __fadd_rn(__fadd_rn(e0, e1), __fadd_rn(e2, e3)));
             }
         }
-        acc = warp_sum128(acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
         if (lane == 0) s_wsum[warp] = acc;
         __syncthreads();   // also: every thread is done with this slice
         if (tid == 0) {
-            U128 t = s_wsum[0];
-            for (int w = 1; w < kStatsWarps; ++w) add128(t, s_wsum[w]);
+            float t = s_wsum[0];
+            for (int w = 1; w < kStatsWarps; ++w) t = __fadd_rn(t, s_wsum[w]);
             const int slot = (k / CS) & 1;
             if (CS > 1)
-                st_async_peer_v2(peer_smem(&s_xsum[slot][rank], static_cast<uint32_t>(owner)), t.lo, t.hi,
-                                 peer_smem(&bar_sum[slot], static_cast<uint32_t>(owner)));
+                st_async_peer(peer_smem(&s_xsum[slot][rank], static_cast<uint32_t>(owner)), __float_as_uint(t),
+                              peer_smem(&bar_sum[slot], static_cast<uint32_t>(owner)));
             else
-                s_xsum[slot][0] = make_ulonglong2(t.lo, t.hi);
+                s_xsum[slot][0] = __float_as_uint(t);
             if (owner == static_cast<int>(rank)) {
                 pend_k = k;
                 pend_r = r;
@@ -1551,6 +1560,10 @@ cudaError_t launch_sample_stages(const SampleIn &in, const int32_t *draft, int B
     } else if (LOGITS) {
         e = launch_pdl(accept_prep_kernel<LOGITS>, dim3(sgrid), dim3(kThreads), 0u, st, in, draft, B, D, V, sc,
                        dev_status);
+        // the exact sums of each sequence's draw rows
+        if (e == cudaSuccess)
+            e = launch_pdl(logits_draw_sums_kernel, dim3(static_cast<unsigned>(B) * in.nzchunks), dim3(kThreads), 0u,
+                           st, in, D, V, sc, bulk, const_cast<float2 *>(in.zparts));
     } else {
         accept_prep_kernel<LOGITS><<<sgrid, kThreads, 0, st>>>(in, draft, B, D, V, sc, dev_status);
         e = cudaGetLastError();
@@ -1569,7 +1582,7 @@ cudaError_t launch_sample_stages(const SampleIn &in, const int32_t *draft, int B
 constexpr uint32_t kStatsStaticSmem = 1024;   // bound on the row-statistics kernel's static shared memory
 
 template <int CS, bool BULK>
-cudaError_t launch_rowstats_cs(const float *zp, const float *zq, int B, int D, int V, float inv_t, int slice,
+cudaError_t launch_rowstats_cs(const float *zp, const float *zq, int B, int D, int V, float c_fast, int slice,
                                bool vec4, float2 *stats, uint32_t *dev_status, cudaStream_t st)
 {
     auto kernel = logits_rowstats_kernel<CS, BULK>;
@@ -1596,11 +1609,11 @@ cudaError_t launch_rowstats_cs(const float *zp, const float *zq, int B, int D, i
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     if (clusters > rows) clusters = static_cast<int>(rows);
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * CS));
-    return cudaLaunchKernelEx(&cfg, kernel, zp, zq, B, D, V, inv_t, slice, vec4, stats, dev_status);
+    return cudaLaunchKernelEx(&cfg, kernel, zp, zq, B, D, V, c_fast, slice, vec4, stats, dev_status);
 }
 
 template <int CS>
-cudaError_t launch_rowstats(const float *zp, const float *zq, int B, int D, int V, float inv_t, float2 *stats,
+cudaError_t launch_rowstats(const float *zp, const float *zq, int B, int D, int V, float c_fast, float2 *stats,
                             uint32_t *dev_status, cudaStream_t st)
 {
     const int slice = ((V + CS - 1) / CS + 3) & ~3;
@@ -1612,8 +1625,8 @@ cudaError_t launch_rowstats(const float *zp, const float *zq, int B, int D, int 
     if (e != cudaSuccess) return e;
     const bool fits = static_cast<long long>(slice) * 4 + 128 + kStatsStaticSmem <= optin;
     if (aligned && fits)
-        return launch_rowstats_cs<CS, true>(zp, zq, B, D, V, inv_t, slice, true, stats, dev_status, st);
-    return launch_rowstats_cs<CS, false>(zp, zq, B, D, V, inv_t, slice, aligned, stats, dev_status, st);
+        return launch_rowstats_cs<CS, true>(zp, zq, B, D, V, c_fast, slice, true, stats, dev_status, st);
+    return launch_rowstats_cs<CS, false>(zp, zq, B, D, V, c_fast, slice, aligned, stats, dev_status, st);
 }
 
 }  // namespace
@@ -1632,7 +1645,7 @@ cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *
                                  int32_t *n_acc, int32_t *token, void *workspace,
                                  uint32_t *dev_status, cudaStream_t st)
 {
-    const SampleIn in{p, q, u_acc, u_res, nullptr, 1.0f, 0ull};
+    const SampleIn in{p, q, u_acc, u_res, nullptr, nullptr, 0, 0.0f, 1.0f, 0.0f, 0ull};
     return launch_sample_stages<false>(in, draft, B, D, V, n_acc, token, workspace, dev_status, st);
 }
 
@@ -1679,34 +1692,55 @@ cudaError_t launch_accept_adasd(const float *p, const float *q, const int32_t *d
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const SampleIn in{p, q, u_acc, u_res, nullptr, 1.0f, 0ull};
+    const SampleIn in{p, q, u_acc, u_res, nullptr, nullptr, 0, 0.0f, 1.0f, 0.0f, 0ull};
     return launch_sample_stages<false>(in, draft, B, D, V, n_acc, token, w, dev_status, st, &ada);
 }
 
+namespace {
+
+size_t logits_stats_bytes(int B, int D)
+{
+    return align256(sizeof(float2) * static_cast<size_t>(B) * (2 * static_cast<size_t>(D) + 1));
+}
+
+int logits_zchunks(int V) { return (V + kZChunk - 1) / kZChunk; }
+
+size_t logits_zparts_bytes(int B, int V)
+{
+    return align256(sizeof(float2) * static_cast<size_t>(B) * 2 * logits_zchunks(V));
+}
+
+}  // namespace
+
 size_t accept_sample_logits_workspace_bytes(int B, int D, int V)
 {
-    return align256(sizeof(float2) * static_cast<size_t>(B) * (2 * static_cast<size_t>(D) + 1)) +
-           accept_sample_workspace_bytes(B, V);
+    return logits_stats_bytes(B, D) + logits_zparts_bytes(B, V) + accept_sample_workspace_bytes(B, V);
 }
 
 cudaError_t launch_accept_sample_logits(const float *zp, const float *zq, const int32_t *draft, float temperature,
                                         unsigned long long seed, int B, int D, int V, int32_t *n_acc,
                                         int32_t *token, void *workspace, uint32_t *dev_status, cudaStream_t st)
 {
-    float2 *stats = static_cast<float2 *>(workspace);
-    void *rest = static_cast<char *>(workspace) +
-                 align256(sizeof(float2) * static_cast<size_t>(B) * (2 * static_cast<size_t>(D) + 1));
-    const float inv_t = 1.0f / temperature;   // IEEE single-precision division
+    char *w = static_cast<char *>(workspace);
+    float2 *stats = reinterpret_cast<float2 *>(w);
+    w += logits_stats_bytes(B, D);
+    float2 *zparts = reinterpret_cast<float2 *>(w);
+    w += logits_zparts_bytes(B, V);
+    // fast evaluation: c = fl32(log2 e / T); exact one: 1 / T as hi + lo
+    const double inv = 1.0 / static_cast<double>(temperature);
+    const float c_fast = static_cast<float>(1.4426950408889634 * inv);
+    const float ih = static_cast<float>(inv);
+    const float il = static_cast<float>(inv - static_cast<double>(ih));
     cudaError_t e;
     switch (pick_cluster(V)) {
-    case 8: e = launch_rowstats<8>(zp, zq, B, D, V, inv_t, stats, dev_status, st); break;
-    case 4: e = launch_rowstats<4>(zp, zq, B, D, V, inv_t, stats, dev_status, st); break;
-    case 2: e = launch_rowstats<2>(zp, zq, B, D, V, inv_t, stats, dev_status, st); break;
-    default: e = launch_rowstats<1>(zp, zq, B, D, V, inv_t, stats, dev_status, st); break;
+    case 8: e = launch_rowstats<8>(zp, zq, B, D, V, c_fast, stats, dev_status, st); break;
+    case 4: e = launch_rowstats<4>(zp, zq, B, D, V, c_fast, stats, dev_status, st); break;
+    case 2: e = launch_rowstats<2>(zp, zq, B, D, V, c_fast, stats, dev_status, st); break;
+    default: e = launch_rowstats<1>(zp, zq, B, D, V, c_fast, stats, dev_status, st); break;
     }
     if (e != cudaSuccess) return e;
-    const SampleIn in{zp, zq, nullptr, nullptr, stats, inv_t, seed};
-    return launch_sample_stages<true>(in, draft, B, D, V, n_acc, token, rest, dev_status, st);
+    const SampleIn in{zp, zq, nullptr, nullptr, stats, zparts, logits_zchunks(V), c_fast, ih, il, seed};
+    return launch_sample_stages<true>(in, draft, B, D, V, n_acc, token, w, dev_status, st);
 }
 
 }  // namespace spec

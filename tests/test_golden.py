@@ -27,25 +27,26 @@ def test_fixture_rows_fill_one_tile():
     assert (G * (1 + D) == rows).all() and (rows == 128).all()
 
 
-def bench_source():
-    with open(os.path.join(os.path.dirname(HERE), "bench.py")) as f:
-        return f.read()
+def bench_module():
+    import sys
+    root = os.path.dirname(HERE)
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import bench
+    return bench
 
 
 def test_throughput_case_uses_guideline2_draft_length():
     g = {G: D for G, D, _ in load_guideline2()}
-    m = re.search(r'attention_case\("throughput B16 L32768 D(\d+)", 16, 8, (\d+), (\d+), 32768', bench_source())
-    assert m, "throughput attention case not found"
-    d_name, G, D = int(m.group(1)), int(m.group(2)), int(m.group(3))
-    assert d_name == D == g[G]
+    c = bench_module().THROUGHPUT_CASE
+    assert c["D"] == g[c["G"]] and c["G"] * (1 + c["D"]) == 128
 
 
 def test_large_group_sweep_straddles_the_tile_boundary():
     g = {G: D for G, D, _ in load_guideline2()}
-    m = re.search(r"for D in \(([0-9, ]+)\):\s*\n\s*attention_case\(f\"large-group B8 G32", bench_source())
-    assert m, "large-group sweep not found"
-    ds = [int(v) for v in m.group(1).split(",")]
-    D0 = g[32]
+    c = bench_module().DSWEEP_CASE
+    ds = list(c["Ds"])
+    D0 = g[c["G"]]
     assert D0 in ds and D0 + 1 in ds          # last D of one tile, first D of two
-    tiles = [-(-32 * (1 + d) // 128) for d in ds]
+    tiles = [-(-c["G"] * (1 + d) // 128) for d in ds]
     assert sorted(set(tiles)) == [1, 2, 4]    # one, two and four 128-row tiles

@@ -1,13 +1,16 @@
 """GPU parity of spec_accept_sample_logits against the oracle.
 
-The row statistics (m, fl32(Z 2^-55)) of every target and draft row are
-compared bit for bit with the oracle's (they are read back from the
-workspace, where the library documents them); n_accepted and token are
-compared element by element with the oracle's acceptance on its own fp32
-softmax and Philox uniforms (bit-exact, except a draw whose oracle margin
-is below 1e-6, at most 1e-4 of the draws).  The device Philox is checked bit
-for bit through uniform rows of 2^24 entries, where the drawn token is the
-24-bit integer of the uniform itself.
+The oracle takes the fp64 softmax of logits / T rounded to fp32 (the fp32
+probability rows of the probability form) and runs the fp64 acceptance on
+them with its own Philox uniforms.  n_accepted and token are compared
+element by element: bit-exact, except a draw whose oracle margin is below
+1e-6; such disagreements are tallied over the whole module and must stay
+at most 1e-4 of the sequences compared (the last test checks the tally).
+The row statistics the library leaves in the workspace are checked too:
+the maxima bit for bit, the fast fp32 sums Zf within their rounding bound
+of the oracle's fp64 sums.  The device Philox is checked bit for bit
+through uniform rows of 2^24 entries, where the drawn token is the 24-bit
+integer of the uniform itself.
 """
 import numpy as np
 import pytest
@@ -17,6 +20,11 @@ import synth
 pytestmark = pytest.mark.gpu
 
 MARGIN = 1e-6
+# Zf sums at most 64 hardware exponentials per thread, then 8 + 3 tree
+# levels, in fp32: relative error below (64 + 11) 2^-24 plus the
+# exponential's own ~2^-22
+ZF_REL = 1e-5
+TALLY = {"draws": 0, "disagree": 0}
 
 
 @pytest.fixture(scope="module")
@@ -50,19 +58,32 @@ def run(sv, zp, zq, draft, T, seed, dev_status=None, workspace=None):
     return n.cpu().numpy(), t.cpu().numpy(), stats
 
 
+def compare(n, t, n_ref, t_ref, margin):
+    """Bit-exact except draws within MARGIN of a decision boundary; tallied."""
+    bad = (n != n_ref) | (t != t_ref)
+    assert not (bad & (margin >= MARGIN)).any(), np.nonzero(bad & (margin >= MARGIN))
+    TALLY["draws"] += len(n)
+    TALLY["disagree"] += int(bad.sum())
+    return bad
+
+
+def check_stats(stats, m_ref, Z_ref):
+    assert np.array_equal(stats[..., 0].view(np.uint32), m_ref.view(np.uint32))
+    finite = np.isfinite(Z_ref)
+    assert np.array_equal(np.isfinite(stats[..., 1]), finite)
+    if finite.any():
+        assert np.abs(stats[..., 1][finite] / Z_ref[finite] - 1).max() <= ZF_REL
+
+
 def check(sv, oracle_lib, inp, T=None, seed=None):
     zp, zq, draft = inp["zp"], inp["zq"], inp["draft"]
     T = inp["temperature"] if T is None else T
     seed = inp["seed"] if seed is None else seed
     n, t, stats = run(sv, zp, zq, draft, T, seed)
-    m_ref, zf_ref = oracle_lib.logits_row_stats(zp, zq, T)
-    assert np.array_equal(stats[..., 0].view(np.uint32), m_ref.view(np.uint32))
-    assert np.array_equal(stats[..., 1].view(np.uint32), zf_ref.view(np.uint32))
+    check_stats(stats, *oracle_lib.logits_row_stats(zp, zq, T))
     p, q, u_acc, u_res = oracle_lib.logits_to_probs(zp, zq, T, seed)
     n_ref, t_ref, margin, _ = oracle_lib.accept_sample(p, q, draft, u_acc, u_res)
-    bad = (n != n_ref) | (t != t_ref)
-    assert not (bad & (margin >= MARGIN)).any(), np.nonzero(bad & (margin >= MARGIN))
-    assert bad.sum() <= int(1e-4 * len(n))
+    compare(n, t, n_ref, t_ref, margin)
     D = zp.shape[1] - 1
     assert n.min() >= 0 and n.max() <= D
     return n, t
@@ -158,12 +179,12 @@ def test_nonfinite_rows_are_flagged(sv, oracle_lib):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     n, t, stats = run(sv, zp, zq, inp["draft"], 1.0, 5, dev_status=st)
     assert int(st.item()) & sv.DEV_STATUS_BITS["LOGITS"]
-    m_ref, zf_ref = oracle_lib.logits_row_stats(zp, zq, 1.0)
-    assert np.array_equal(stats[..., 1], zf_ref) and np.isinf(zf_ref[1, 0]) and np.isinf(zf_ref[3, 4])
-    good = [0, 2, 4, 5]
+    m_ref, Z_ref = oracle_lib.logits_row_stats(zp, zq, 1.0)
+    check_stats(stats, m_ref, Z_ref)
+    assert np.isinf(Z_ref[1, 0]) and np.isinf(Z_ref[3, 4])
     p, q, u_acc, u_res = oracle_lib.logits_to_probs(zp, zq, 1.0, 5)
-    n_ref, t_ref, _, _ = oracle_lib.accept_sample(p, q, inp["draft"], u_acc, u_res)
-    assert np.array_equal(n[good], n_ref[good]) and np.array_equal(t[good], t_ref[good])
+    n_ref, t_ref, margin, _ = oracle_lib.accept_sample(p, q, inp["draft"], u_acc, u_res)
+    compare(n, t, n_ref, t_ref, margin)
 
 
 def test_workspace_reuse_and_graph_replay(sv, oracle_lib):
@@ -177,8 +198,7 @@ def test_workspace_reuse_and_graph_replay(sv, oracle_lib):
         n, t, _ = run(sv, inp["zp"], inp["zq"], inp["draft"], 1.0, seed, workspace=ws)
         p, q, u_acc, u_res = oracle_lib.logits_to_probs(inp["zp"], inp["zq"], 1.0, seed)
         n_ref, t_ref, margin, _ = oracle_lib.accept_sample(p, q, inp["draft"], u_acc, u_res)
-        bad = (n != n_ref) | (t != t_ref)
-        assert not (bad & (margin >= MARGIN)).any()
+        compare(n, t, n_ref, t_ref, margin)
     inp = synth.logits_inputs(74, B, 5, V)
     zp, zq, dr = to_dev(inp["zp"]), to_dev(inp["zq"]), to_dev(inp["draft"])
     n_out = torch.empty(B, dtype=torch.int32, device="cuda")
@@ -197,14 +217,22 @@ def test_workspace_reuse_and_graph_replay(sv, oracle_lib):
         t_out.fill_(-1)
         g.replay()
         torch.cuda.synchronize()
-        bad = (n_out.cpu().numpy() != n_ref) | (t_out.cpu().numpy() != t_ref)
-        assert not (bad & (margin >= MARGIN)).any()
+        compare(n_out.cpu().numpy(), t_out.cpu().numpy(), n_ref, t_ref, margin)
 
 
 def test_batched_full_size(sv, oracle_lib):
     """B = 256 sequences, D = 7, V = 131072, target logits N(0, 3^2), draft
-    logits the target's plus N(0, 1.5^2): every row statistic bit-exact and
-    every decision equal to the oracle's."""
-    inp = synth.logits_inputs(80, 256, 7, 131072, target_std=3.0, draft_noise=1.5)
-    n, _ = check(sv, oracle_lib, inp)
-    assert 0 < n.mean() < 7
+    logits the target's plus N(0, 1.5^2), two seeds: maxima bit-exact, sums
+    within their bound, decisions equal to the oracle's except at boundary
+    draws."""
+    for seed in (80, 81):
+        inp = synth.logits_inputs(seed, 256, 7, 131072, target_std=3.0, draft_noise=1.5)
+        n, _ = check(sv, oracle_lib, inp)
+        assert 0 < n.mean() < 7
+
+
+def test_zz_disagreements_stay_below_the_cap():
+    """Over every comparison of this module: at most 1e-4 of the sequences
+    disagree with the oracle (each of them at a boundary draw)."""
+    assert TALLY["draws"] > 0
+    assert TALLY["disagree"] <= 1e-4 * TALLY["draws"], TALLY
