@@ -447,6 +447,44 @@ __device__ __forceinline__ unsigned long long scaled_threshold(float u, unsigned
 //    then is the nearest fp32 to the exact softmax unless the exact value
 //    lies within about 2^-33 (relative) of a rounding tie.
 
+// Two fp32 values in one 64-bit register (element 0 in the low word) for
+// the packed fp32x2 instructions: each rounds both halves exactly like the
+// scalar instruction.
+using F32x2 = unsigned long long;
+
+__device__ __forceinline__ F32x2 pack2(float lo, float hi)
+{
+    return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo_of(F32x2 v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_of(F32x2 v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ F32x2 add2(F32x2 a, F32x2 b)
+{
+    F32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ F32x2 sub2(F32x2 a, F32x2 b)
+{
+    F32x2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ F32x2 mul2(F32x2 a, F32x2 b)
+{
+    F32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ F32x2 fma2(F32x2 a, F32x2 b, F32x2 c)
+{
+    F32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ F32x2 neg2(F32x2 a) { return a ^ 0x8000000080000000ull; }
+__device__ __forceinline__ F32x2 splat2(float x) { return pack2(x, x); }
+
 struct DF {
     float hi, lo;   // the unevaluated sum hi + lo
 };
@@ -488,6 +526,12 @@ __device__ void build_exp2_table(float2 *tab)
     __syncthreads();
 }
 
+// Parameters of one logits row for the exact evaluation: 1/T = ih + il,
+// 1/Z = rh + rl (rh = 0: the row has no softmax, every probability is 0).
+struct SoftmaxRow {
+    float m, ih, il, rh, rl;
+};
+
 // exp(yh + yl) for yh + yl <= 0 as a double-float value, relative error
 // about 2^-33; 0 below -83 (e^-83 < 2^-119) and for -inf.
 //   k = rint((yh) 256 / ln 2);  r = y - k ln2 / 256, with ln2 / 256 split
@@ -495,48 +539,80 @@ __device__ void build_exp2_table(float2 *tab)
 //   |k| < 2^15, and the first fused multiply-add is exact);  |r| <= ~ln2 /
 //   512;  e^r - 1 = r + r^2 (1/2 + r/6 + r^2/24) (Taylor, the next term
 //   is below 2^-41);  exp(y) = 2^(k >> 8) 2^((k & 255) / 256) e^r.
-__device__ __forceinline__ DF exp_df(float yh, float yl, const float2 *tab)
-{
-    if (!(yh >= -83.0f)) return {0.0f, 0.0f};
-    const float kf = rintf(__fmul_rn(yh, 0x1.715476p+8f));
-    float t = __fmaf_rn(-kf, 0x1.62p-9f, yh);
-    t = __fmaf_rn(-kf, 0x1.c85fep-18f, t);
-    t = __fmaf_rn(-kf, -0x1.718432p-43f, t);
-    const float r = __fadd_rn(t, yl);
-    float s = __fmaf_rn(r, 0x1.555556p-5f, 0x1.555556p-3f);   // 1/24, 1/6
-    s = __fmaf_rn(s, r, 0.5f);
-    s = __fmul_rn(__fmul_rn(s, r), r);
-    const float em1 = __fadd_rn(r, s);                          // e^r - 1
-    const int k = static_cast<int>(kf);
-    const float2 tj = tab[k & 255];
-    const float scale = __int_as_float(((k >> 8) + 127) << 23);   // 2^(k >> 8), k >> 8 >= -121
-    return {__fmul_rn(tj.x, scale), __fmul_rn(__fmaf_rn(tj.x, em1, tj.y), scale)};
-}
-
-// Parameters of one logits row for the exact evaluation: 1/T = ih + il,
-// 1/Z = rh + rl (rh = 0: the row has no softmax, every probability is 0).
-struct SoftmaxRow {
-    float m, ih, il, rh, rl;
+// Evaluated on a pair of elements at a time with packed fp32x2
+// instructions: k is taken with the 1.5 * 2^23 rounding trick (fma(y,
+// 256/ln2, 1.5 * 2^23) holds 1.5 * 2^23 + k in its significand, so its bits
+// are 0x4B400000 + k), and lanes below -83 are computed on a clamped
+// argument and zeroed at the end.  The probability is the double-float
+// quotient e / Z = (e_hi + e_lo)(1/Z_hi + 1/Z_lo) rounded once.
+struct DF2 {
+    F32x2 hi, lo;
 };
 
-// exp((z - m) / T) as a double-float value.
-__device__ __forceinline__ DF softmax_exp(float z, const SoftmaxRow &r, const float2 *tab)
+__device__ __forceinline__ DF2 two_sum2(F32x2 a, F32x2 b)
 {
-    const DF d = two_sum(z, -r.m);   // z - m exactly
-    const float yh = __fmul_rn(d.hi, r.ih);
-    const float yl = __fadd_rn(__fmaf_rn(d.hi, r.ih, -yh), __fmaf_rn(d.hi, r.il, __fmul_rn(d.lo, r.ih)));
-    return exp_df(yh, yl, tab);
+    const F32x2 s = add2(a, b);
+    const F32x2 bb = sub2(s, a);
+    return {s, add2(sub2(a, sub2(s, bb)), sub2(b, bb))};
 }
 
-// The fp32 rounding of softmax(z / T)_v: the double-float quotient e / Z
-// rounded once.
-__device__ __forceinline__ float softmax_prob(float z, const SoftmaxRow &r, const float2 *tab)
+// A row's exact-evaluation parameters on both lanes.
+struct SoftmaxPair {
+    F32x2 neg_m, ih, il, rh, rl;
+    bool unit_t;   // T = 1: (z - m) / T = z - m
+    bool none;     // no softmax: every probability 0
+};
+
+__device__ __forceinline__ SoftmaxPair softmax_pair(const SoftmaxRow &r)
 {
-    if (r.rh == 0.0f) return 0.0f;
-    const DF e = softmax_exp(z, r, tab);
-    const float qh = __fmul_rn(e.hi, r.rh);
-    const float ql = __fadd_rn(__fmaf_rn(e.hi, r.rh, -qh), __fmaf_rn(e.hi, r.rl, __fmul_rn(e.lo, r.rh)));
-    return __fadd_rn(qh, ql);
+    return {splat2(-r.m), splat2(r.ih), splat2(r.il), splat2(r.rh), splat2(r.rl),
+            r.ih == 1.0f && r.il == 0.0f, r.rh == 0.0f};
+}
+
+__device__ __forceinline__ DF2 softmax_exp2(F32x2 z, const SoftmaxPair &r, const float2 *tab)
+{
+    const DF2 d = two_sum2(z, r.neg_m);   // z - m exactly
+    F32x2 yh = d.hi, yl = d.lo;
+    if (!r.unit_t) {
+        yh = mul2(d.hi, r.ih);
+        yl = add2(fma2(d.hi, r.ih, neg2(yh)), fma2(d.hi, r.il, mul2(d.lo, r.ih)));
+    }
+    const float y0 = lo_of(yh), y1 = hi_of(yh);
+    const bool z0 = !(y0 >= -83.0f), z1 = !(y1 >= -83.0f);
+    const F32x2 yc = pack2(z0 ? -83.0f : y0, z1 ? -83.0f : y1);
+    const F32x2 magic = splat2(0x1.8p+23f);
+    const F32x2 rk = fma2(yc, splat2(0x1.715476p+8f), magic);   // 1.5 * 2^23 + k
+    const F32x2 nk = sub2(magic, rk);                           // -k
+    F32x2 t = fma2(nk, splat2(0x1.62p-9f), yc);
+    t = fma2(nk, splat2(0x1.c85fep-18f), t);
+    t = fma2(nk, splat2(-0x1.718432p-43f), t);
+    const F32x2 rr = add2(t, yl);
+    F32x2 sp = fma2(rr, splat2(0x1.555556p-5f), splat2(0x1.555556p-3f));
+    sp = fma2(sp, rr, splat2(0.5f));
+    sp = mul2(mul2(sp, rr), rr);
+    const F32x2 em1 = add2(rr, sp);
+    const int k0 = static_cast<int>(static_cast<uint32_t>(rk)) - 0x4B400000;
+    const int k1 = static_cast<int>(static_cast<uint32_t>(rk >> 32)) - 0x4B400000;
+    const float2 t0 = tab[k0 & 255], t1 = tab[k1 & 255];
+    const F32x2 sc = pack2(__int_as_float(((k0 >> 8) + 127) << 23), __int_as_float(((k1 >> 8) + 127) << 23));
+    const F32x2 th = pack2(t0.x, t1.x), tl = pack2(t0.y, t1.y);
+    F32x2 eh = mul2(th, sc), el = mul2(fma2(th, em1, tl), sc);
+    if (z0 | z1) {
+        const F32x2 keep = (z0 ? 0ull : 0xFFFFFFFFull) | (z1 ? 0ull : 0xFFFFFFFF00000000ull);
+        eh &= keep;
+        el &= keep;
+    }
+    return {eh, el};
+}
+
+// softmax_prob of two elements.
+__device__ __forceinline__ F32x2 softmax_prob2(F32x2 z, const SoftmaxPair &r, const float2 *tab)
+{
+    if (r.none) return 0ull;
+    const DF2 e = softmax_exp2(z, r, tab);
+    const F32x2 qh = mul2(e.hi, r.rh);
+    const F32x2 ql = add2(fma2(e.hi, r.rh, neg2(qh)), fma2(e.hi, r.rl, mul2(e.lo, r.rh)));
+    return add2(qh, ql);
 }
 
 __device__ __forceinline__ float ex2_approx(float x)
@@ -624,11 +700,11 @@ __device__ __forceinline__ SoftmaxRow draw_row(const SampleIn &in, int b, int D,
 }
 
 template <bool LOGITS>
-__device__ __forceinline__ float4 to_prob4(float4 z, const SoftmaxRow &r, const float2 *tab)
+__device__ __forceinline__ float4 to_prob4(float4 z, const SoftmaxPair &r, const float2 *tab)
 {
     if (!LOGITS) return z;
-    return make_float4(softmax_prob(z.x, r, tab), softmax_prob(z.y, r, tab), softmax_prob(z.z, r, tab),
-                       softmax_prob(z.w, r, tab));
+    const F32x2 a = softmax_prob2(pack2(z.x, z.y), r, tab), b = softmax_prob2(pack2(z.z, z.w), r, tab);
+    return make_float4(lo_of(a), hi_of(a), lo_of(b), hi_of(b));
 }
 
 // Value read for an element past the end of a row: no mass either way.
@@ -733,8 +809,8 @@ __global__ void __launch_bounds__(kThreads) accept_prep_kernel(SampleIn in, cons
 template <bool SMEM, bool LOGITS>
 __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, const float *sq,
                                                                int residual, int w0, int n, bool vec4,
-                                                               int lane, const SoftmaxRow &rp,
-                                                               const SoftmaxRow &rq, const float2 *tab)
+                                                               int lane, const SoftmaxPair &rp,
+                                                               const SoftmaxPair &rq, const float2 *tab)
 {
     unsigned long long mine = 0;
 #pragma unroll
@@ -851,8 +927,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
             sq = residual ? q + (static_cast<int64_t>(b) * D + j) * V + e0 : nullptr;
         }
         const unsigned long long t =
-            bulk ? warp_step_masses<true, LOGITS>(sp, sq, residual, warp * kGroup, n, true, lane, rp, rq, s_tab)
-                 : warp_step_masses<false, LOGITS>(sp, sq, residual, warp * kGroup, n, false, lane, rp, rq, s_tab);
+            bulk ? warp_step_masses<true, LOGITS>(sp, sq, residual, warp * kGroup, n, true, lane, softmax_pair(rp),
+                                                   softmax_pair(rq), s_tab)
+                 : warp_step_masses<false, LOGITS>(sp, sq, residual, warp * kGroup, n, false, lane, softmax_pair(rp),
+                                                   softmax_pair(rq), s_tab);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
         const int s0 = chunk * (kChunk / kStep) + warp * kGroupSteps;
@@ -904,24 +982,25 @@ __global__ void __launch_bounds__(kThreads) logits_draw_sums_kernel(SampleIn in,
                                   : in.p + (static_cast<int64_t>(b) * (D + 1) + j) * V) + e0;
         DF acc{0.0f, 0.0f};
         if (st.y < INFINITY) {
-            const SoftmaxRow r{st.x, in.ih, in.il, 1.0f, 0.0f};
+            const SoftmaxPair r = softmax_pair(SoftmaxRow{st.x, in.ih, in.il, 1.0f, 0.0f});
             float4 z[kZPerThread / 4];
 #pragma unroll
             for (int u = 0; u < kZPerThread / 4; ++u) {
                 const int e = (u * kThreads + threadIdx.x) * 4;
                 z[u] = e < n ? load4(row, e, n, vec4, -INFINITY) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             }
+            DF2 a2{0ull, 0ull};   // two running sums (even and odd elements), hi + lo each
 #pragma unroll
             for (int u = 0; u < kZPerThread / 4; ++u) {
-                const float v[4] = {z[u].x, z[u].y, z[u].z, z[u].w};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const DF e = softmax_exp(v[c], r, s_tab);
-                    const DF t = two_sum(acc.hi, e.hi);
-                    acc.hi = t.hi;
-                    acc.lo = __fadd_rn(acc.lo, __fadd_rn(t.lo, e.lo));
+                for (int h = 0; h < 2; ++h) {
+                    const DF2 e = softmax_exp2(h ? pack2(z[u].z, z[u].w) : pack2(z[u].x, z[u].y), r, s_tab);
+                    const DF2 t = two_sum2(a2.hi, e.hi);
+                    a2.hi = t.hi;
+                    a2.lo = add2(a2.lo, add2(t.lo, e.lo));
                 }
             }
+            acc = df_add(DF{lo_of(a2.hi), lo_of(a2.lo)}, DF{hi_of(a2.hi), hi_of(a2.lo)});
         }
         acc = warp_sum_df(acc);
         if (lane == 0) s_w[warp] = acc;
@@ -959,8 +1038,8 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
     const float *qrow = residual ? q + (static_cast<int64_t>(b) * D + j) * V : nullptr;
     unsigned long long *steps = sc.steps + static_cast<int64_t>(b) * sc.nsteps;
     unsigned long long *gtot = sc.gtot + static_cast<int64_t>(b) * sc.ngroups;
-    const SoftmaxRow rp = draw_row<LOGITS>(in, b, D, j, 0);
-    const SoftmaxRow rq = residual ? draw_row<LOGITS>(in, b, D, D + 1 + j, 1) : rp;
+    const SoftmaxPair rp = softmax_pair(draw_row<LOGITS>(in, b, D, j, 0));
+    const SoftmaxPair rq = residual ? softmax_pair(draw_row<LOGITS>(in, b, D, D + 1 + j, 1)) : rp;
 
     float u = LOGITS ? philox_u(in.seed, static_cast<uint32_t>(b), 0u, 1u) : in.u_res[b];
     if (!(u >= 0.0f && u < 1.0f)) {
@@ -1207,21 +1286,6 @@ __global__ void __launch_bounds__(kThreads) adasd_prep_kernel(
 // iteration mod CS), which adds them in rank order and writes (m, Zf).
 // Rows whose maximum is not finite, or that hold NaN or +inf, get Zf = +inf
 // (every probability 0) and set SPEC_DEV_ERR_LOGITS.
-__device__ __forceinline__ unsigned long long pack2(float lo, float hi)
-{
-    return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
-}
-__device__ __forceinline__ float lo_of(unsigned long long v) { return __uint_as_float(static_cast<uint32_t>(v)); }
-__device__ __forceinline__ float hi_of(unsigned long long v)
-{
-    return __uint_as_float(static_cast<uint32_t>(v >> 32));
-}
-__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b)
-{
-    unsigned long long d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
     float d;
