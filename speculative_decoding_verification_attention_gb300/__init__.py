@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = (
 
 DEV_STATUS_BITS = {
     "PAGE_ID": 0x1, "KV_LEN": 0x2, "TIMEOUT": 0x4, "TOKEN_ID": 0x8, "UNIFORM": 0x10,
-    "ZERO_MASS": 0x20, "LAUNCH": 0x40, "TREE": 0x80, "LOGITS": 0x100,
+    "ZERO_MASS": 0x20, "LAUNCH": 0x40, "TREE": 0x80, "LOGITS": 0x100, "PROB": 0x200,
     "INFO_ZERO_RESIDUAL": 0x10000,
 }
 

@@ -416,6 +416,26 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x)
     return x;
 }
 
+// The same sum; ovf is set when it wraps past 2^64 (a row whose
+// probabilities sum to 8 or more overflows the 2^-61 fixed point).
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x, bool &ovf)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long y = x + __shfl_xor_sync(0xffffffffu, x, o);
+        ovf |= y < x;
+        x = y;
+    }
+    return x;
+}
+
+// A probability the fixed point represents: 0 <= x <= 1 (false for NaN).
+__device__ __forceinline__ bool prob_ok(float4 x)
+{
+    return x.x >= 0.0f && x.x <= 1.0f && x.y >= 0.0f && x.y <= 1.0f && x.z >= 0.0f && x.z <= 1.0f &&
+           x.w >= 0.0f && x.w <= 1.0f;
+}
+
 __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long x, int lane)
 {
 #pragma unroll
@@ -816,11 +836,13 @@ __global__ void __launch_bounds__(kThreads) accept_prep_kernel(SampleIn in, cons
 // w0 of the n-element slice (sp, sq): staged in shared memory (SMEM,
 // n % 4 == 0) or read from global memory.  Lane k of the result holds step
 // k's total (k < kGroupSteps).
+// bad: set when an element is not a probability in [0, 1] or a step's sum
+// wraps (its row sums to 8 or more); the fixed point cannot represent them.
 template <bool SMEM, bool LOGITS>
 __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, const float *sq,
                                                                int residual, int w0, int n, bool vec4,
                                                                int lane, const SoftmaxPair &rp,
-                                                               const SoftmaxPair &rq, const float2 *tab)
+                                                               const SoftmaxPair &rq, const float2 *tab, bool &bad)
 {
     unsigned long long mine = 0;
 #pragma unroll
@@ -838,10 +860,11 @@ __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, 
             }
             xp = to_prob4<LOGITS>(xp, rp, tab);
             if (residual) xq = to_prob4<LOGITS>(xq, rq, tab);
+            if (!LOGITS) bad |= !prob_ok(xp) || (residual && !prob_ok(xq));
             m = mass(xp.x, xq.x, residual) + mass(xp.y, xq.y, residual) + mass(xp.z, xq.z, residual) +
                 mass(xp.w, xq.w, residual);
         }
-        const unsigned long long t = warp_sum_u64(m);
+        const unsigned long long t = warp_sum_u64(m, bad);
         if (lane == k) mine = t;
     }
     return mine;
@@ -936,17 +959,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
             sp = p + (static_cast<int64_t>(b) * (D + 1) + j) * V + e0;
             sq = residual ? q + (static_cast<int64_t>(b) * D + j) * V + e0 : nullptr;
         }
+        bool bad = false;
         const unsigned long long t =
             bulk ? warp_step_masses<true, LOGITS>(sp, sq, residual, warp * kGroup, n, true, lane, softmax_pair(rp),
-                                                   softmax_pair(rq), s_tab)
+                                                   softmax_pair(rq), s_tab, bad)
                  : warp_step_masses<false, LOGITS>(sp, sq, residual, warp * kGroup, n, false, lane, softmax_pair(rp),
-                                                   softmax_pair(rq), s_tab);
+                                                   softmax_pair(rq), s_tab, bad);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the slot
         const int s0 = chunk * (kChunk / kStep) + warp * kGroupSteps;
         if (lane < kGroupSteps && s0 + lane < sc.nsteps)
             sc.steps[static_cast<int64_t>(b) * sc.nsteps + s0 + lane] = t;
-        const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull);
+        const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull, bad);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) report(dev_status, SPEC_DEV_ERR_PROB);
         const int gi = chunk * kConsumers + warp;
         if (lane == 0 && gi < sc.ngroups) sc.gtot[static_cast<int64_t>(b) * sc.ngroups + gi] = gt;
     }
@@ -1057,10 +1082,15 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
         u = (u >= 1.0f) ? 0x1.fffffep-1f : 0.0f;
     }
     unsigned long long Z = 0;
+    bool ovf = false;
     for (int attempt = 0; attempt < 2; ++attempt) {
         unsigned long long z = 0;
-        for (int g = lane; g < sc.ngroups; g += 32) z += gtot[g];
-        Z = warp_sum_u64(z);
+        for (int g = lane; g < sc.ngroups; g += 32) {
+            const unsigned long long y = z + gtot[g];
+            ovf |= y < z;
+            z = y;
+        }
+        Z = warp_sum_u64(z, ovf);
         if (Z != 0 || !residual) break;
         // reading: max(0, p - q) has no mass -> draw from the target row
         // itself; this warp recomputes the step and group masses of p
@@ -1070,13 +1100,14 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
             const int64_t g0 = static_cast<int64_t>(g) * kGroup;
             const int n = static_cast<int>(imin64(kGroup, V - g0));
             const unsigned long long t =
-                warp_step_masses<false, LOGITS>(prow + g0, nullptr, 0, 0, n, false, lane, rp, rq, s_tab);
+                warp_step_masses<false, LOGITS>(prow + g0, nullptr, 0, 0, n, false, lane, rp, rq, s_tab, ovf);
             if (lane < kGroupSteps && g * kGroupSteps + lane < sc.nsteps) steps[g * kGroupSteps + lane] = t;
-            const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull);
+            const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull, ovf);
             if (lane == 0) gtot[g] = gt;
         }
         __syncwarp();
     }
+    if (__any_sync(0xffffffffu, ovf) && lane == 0) report(dev_status, SPEC_DEV_ERR_PROB);
     if (Z == 0) {
         if (lane == 0) {
             report(dev_status, SPEC_DEV_ERR_ZERO_MASS);

@@ -286,3 +286,66 @@ def test_residual_draw_uses_strict_cdf_crossing(oracle_lib):
         n, t, _, _ = oracle_lib.accept_sample(p, q, np.array([[0]], np.int32), u_acc,
                                               np.array([u], np.float32))
         assert n[0] == 0 and t[0] == expect, (u, t[0])
+
+
+# ---------------------------------------------------------------- margins
+# The margin decides which GPU/oracle disagreements are exempt: per sequence,
+# the smallest distance of a uniform from its decision boundary -- |u - p/q|
+# for every accept test taken, and |u_res Z - C(v)| / Z for the draw (C the
+# running sum, Z the total).  Dyadic rows and uniforms make every distance
+# exact in fp64, so the pins compare for equality.
+def _one(p_rows, q_row, x, ua, ur):
+    p = np.array([p_rows], np.float32)
+    q = np.array([[q_row]], np.float32)
+    return (p, q, np.array([[x]], np.int32), np.array([[ua]], np.float32), np.array([ur], np.float32))
+
+
+P_MARGIN = [[0.5, 0.125, 0.25, 0.125], [0.25, 0.25, 0.25, 0.25]]
+Q_MARGIN = [0.25, 0.25, 0.25, 0.25]
+
+
+def test_margin_of_a_rejecting_accept_test(oracle_lib):
+    """Draft 1 has p/q = 1/2; u = 1/2 + 2^-12 rejects it, 2^-12 from the
+    boundary.  The residual max(0, p - q) = (1/4, 0, 0, 0) has a single
+    boundary, at the end: with u_res = 1/2 the draw is 1/2 from it."""
+    n, t, m, _ = oracle_lib.accept_sample(*_one(P_MARGIN, Q_MARGIN, 1, 0.5 + 2.0 ** -12, 0.5))
+    assert n[0] == 0 and t[0] == 0
+    assert m[0] == 2.0 ** -12
+    # the test far from its boundary (u = 3/4, 1/4 away) and the draw close
+    # to the residual's end: u_res = 1 - 2^-10 is 2^-10 from it in units of
+    # Z (Z = 1/4, so 2^-12 in absolute terms)
+    n, t, m, _ = oracle_lib.accept_sample(*_one(P_MARGIN, Q_MARGIN, 1, 0.75, 1.0 - 2.0 ** -10))
+    assert n[0] == 0 and t[0] == 0
+    assert m[0] == 2.0 ** -10
+
+
+def test_margin_of_a_draw_close_to_a_step(oracle_lib):
+    """The same test accepted 2^-12 below its boundary, then the bonus draw
+    from the uniform row p_1 with u_res = 1/2 + 2^-14: the running sum steps
+    at 1/4, 1/2, 3/4 and 1, so the draw is 2^-14 from the step at 1/2."""
+    n, t, m, _ = oracle_lib.accept_sample(*_one(P_MARGIN, Q_MARGIN, 1, 0.5 - 2.0 ** -12, 0.5 + 2.0 ** -14))
+    assert n[0] == 1 and t[0] == 2
+    assert m[0] == 2.0 ** -14
+    # with the draw far from every step, the accept test sets the margin
+    n, t, m, _ = oracle_lib.accept_sample(*_one(P_MARGIN, Q_MARGIN, 1, 0.5 - 2.0 ** -12, 0.125))
+    assert n[0] == 1 and t[0] == 0 and m[0] == 2.0 ** -12
+
+
+def test_margin_ignores_a_test_with_zero_draft_mass(oracle_lib):
+    """q(x) = 0 < p(x) always accepts (no boundary to be near): the margin
+    comes from the draw alone (u_res = 3/8 is 1/8 from the step at 1/4)."""
+    q_row = [0.5, 0.0, 0.25, 0.25]
+    n, t, m, _ = oracle_lib.accept_sample(*_one(P_MARGIN, q_row, 1, 0.999, 0.375))
+    assert n[0] == 1 and t[0] == 1
+    assert m[0] == 0.125
+
+
+def test_margin_is_the_smallest_over_several_tests(oracle_lib):
+    """D = 3: three accepted tests at 2^-9, 2^-7, 2^-11 from their boundaries
+    (p/q = 1/2 each), then the bonus draw 1/8 from its nearest step."""
+    p = np.array([[[0.5, 0.125, 0.25, 0.125]] * 3 + [[0.25, 0.25, 0.25, 0.25]]], np.float32)
+    q = np.array([[[0.25, 0.25, 0.25, 0.25]] * 3], np.float32)
+    ua = np.array([[0.5 - 2.0 ** -9, 0.5 - 2.0 ** -7, 0.5 - 2.0 ** -11]], np.float32)
+    n, t, m, _ = oracle_lib.accept_sample(p, q, np.array([[1, 1, 1]], np.int32), ua, np.array([0.375], np.float32))
+    assert n[0] == 3 and t[0] == 1
+    assert m[0] == 2.0 ** -11

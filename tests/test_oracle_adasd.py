@@ -131,3 +131,52 @@ def test_first_token_law(oracle_lib, relaxed):
     counts = np.bincount(first, minlength=V)
     expect = (qd if relaxed else pt) * B
     assert stats.chisquare(counts, expect / expect.sum() * B).pvalue > 1e-3
+
+
+# ---------------------------------------------------------------- margins
+# margin_stat is the smallest distance of a decisive statistic from its
+# threshold (|H - tau_H| for the entropy tests taken, |JS - tau_JS| for the
+# distance tests taken); margin_u is the stochastic acceptance's margin over
+# the uniform decisions and the draw.  Rows of known entropy and distance
+# make the distances known in closed form.
+def test_margin_stat_is_the_entropy_distance(oracle_lib):
+    """One position whose draft row is uniform over 4 tokens (H = ln 4),
+    tau_H above it by d: the position is not a stop, and no distance test
+    is taken (the exact rule accepts: p(x) = q(x)), so margin_stat = d."""
+    V = 8
+    q = np.zeros((1, 1, V), np.float32)
+    q[0, 0, :4] = 0.25
+    p = np.concatenate([q, np.full((1, 1, V), 1.0 / V, np.float32)], axis=1)
+    for d in (2.0 ** -10, 2.0 ** -14, 0.125):
+        tau_h = np.float32(np.log(4.0) + d)
+        n, _, de, mu, ms, _ = oracle_lib.accept_adasd(p, q, np.array([[0]], np.int32), np.array([[0.5]], np.float32),
+                                                      np.array([0.0625], np.float32), float(tau_h), -1.0)
+        assert de[0] == 1 and n[0] == 1
+        assert ms[0] == pytest.approx(float(tau_h) - np.log(4.0), rel=1e-9, abs=1e-14)
+        # |u - p/q| = 1/2 for the test; the bonus draw is 1/16 from the step at 1/8
+        assert mu[0] == 0.0625
+
+
+def test_margin_stat_is_the_distance_distance(oracle_lib):
+    """Disjoint target and draft rows (JS = sqrt(ln 2)): the exact rule
+    rejects (p(x) = 0), so the distance test decides; tau_JS below JS by d
+    rejects and margin_stat = d (the entropy test, ln 2 against a far
+    tau_H, is farther)."""
+    V = 8
+    q = np.zeros((1, 1, V), np.float32)
+    q[0, 0, :2] = 0.5
+    p = np.zeros((1, 2, V), np.float32)
+    p[0, 0, 4:] = 0.25
+    p[0, 1, :] = 1.0 / V
+    js = np.sqrt(LN2)
+    for d in (2.0 ** -9, 2.0 ** -13):
+        tau_js = np.float32(js - d)
+        n, _, de, _, ms, _ = oracle_lib.accept_adasd(p, q, np.array([[0]], np.int32), np.array([[0.5]], np.float32),
+                                                     np.array([0.5], np.float32), 100.0, float(tau_js))
+        assert de[0] == 1 and n[0] == 0
+        assert ms[0] == pytest.approx(js - float(tau_js), rel=1e-9, abs=1e-14)
+    # above JS by d: relaxed, accepted
+    tau_js = np.float32(js + 2.0 ** -11)
+    n, _, _, _, ms, _ = oracle_lib.accept_adasd(p, q, np.array([[0]], np.int32), np.array([[0.5]], np.float32),
+                                                np.array([0.5], np.float32), 100.0, float(tau_js))
+    assert n[0] == 1 and ms[0] == pytest.approx(float(tau_js) - js, rel=1e-9, abs=1e-14)

@@ -6,8 +6,10 @@ oracle's fp64 values: |H - H_ref| <= 1e-5 (1 + H_ref) and
 through the square root).  Decisions (d_eff, n_accepted, token) are compared
 element by element; a difference is allowed only for a sequence whose oracle
 margin is below the bar -- a uniform within 1e-6 of its decision boundary,
-or a statistic within 5e-4 of its threshold -- and such differences must
-stay rare.
+or a statistic within those same error bounds of its threshold -- and such
+differences are tallied over the module and must stay at most 1e-4 of the
+sequences compared (the last test checks the tally).  Thresholds taken from
+the data sit half-way between two neighbouring statistics, never on one.
 """
 import numpy as np
 import pytest
@@ -17,7 +19,23 @@ import synth
 pytestmark = pytest.mark.gpu
 
 MARGIN_U = 1e-6
-MARGIN_STAT = 5e-4
+TALLY = {"draws": 0, "disagree": 0}
+
+
+def stat_bar(V, tau_js):
+    """How far from its threshold a statistic must be for the decision to be
+    exact: the entropy bound 1e-5 (1 + H) at H <= ln V, and the distance
+    bound, |JS - JS_ref| <= (2e-6 + 1e-5 JS^2) / (2 JS) near tau_JS."""
+    t = max(float(tau_js), 1e-2)
+    return max(1e-5 * (1 + np.log(V)), (2e-6 + 1e-5 * t * t) / (2 * t))
+
+
+def threshold_between(values, q):
+    """A threshold at quantile q of the data, half-way between the two
+    neighbouring values (no statistic lies on it)."""
+    v = np.unique(np.asarray(values, np.float64).ravel())
+    k = min(max(int(q * (len(v) - 1)), 0), len(v) - 2)
+    return float((v[k] + v[k + 1]) / 2)
 
 
 @pytest.fixture(scope="module")
@@ -46,10 +64,10 @@ def run(sv, inp, tau_h, tau_js, dev_status=None):
     return [o.cpu().numpy() for o in out]
 
 
-def check(sv, oracle_lib, inp, tau_h, tau_js, max_close=0.02):
+def check(sv, oracle_lib, inp, tau_h, tau_js):
     n, t, de, H, JS = run(sv, inp, tau_h, tau_js)
     p, q = inp["p"], inp["q"]
-    D = p.shape[1] - 1
+    D, V = p.shape[1] - 1, p.shape[2]
     if D:
         H_ref, JS_ref = oracle_lib.adasd_stats(p, q)
         assert (np.abs(H - H_ref) <= 1e-5 * (1 + H_ref)).all(), np.abs(H - H_ref).max()
@@ -57,10 +75,11 @@ def check(sv, oracle_lib, inp, tau_h, tau_js, max_close=0.02):
         assert (np.abs(jsd - jsd_ref) <= 2e-6 + 1e-5 * jsd_ref).all(), np.abs(jsd - jsd_ref).max()
     n_ref, t_ref, de_ref, mu, ms, _ = oracle_lib.accept_adasd(p, q, inp["draft"], inp["u_acc"], inp["u_res"],
                                                              tau_h, tau_js)
-    close = (mu < MARGIN_U) | (ms < MARGIN_STAT)
+    close = (mu < MARGIN_U) | (ms < stat_bar(V, tau_js))
     bad = (n != n_ref) | (t != t_ref) | (de != de_ref)
     assert not (bad & ~close).any(), np.nonzero(bad & ~close)
-    assert bad.sum() <= max(1, int(max_close * len(n)))
+    TALLY["draws"] += len(n)
+    TALLY["disagree"] += int(bad.sum())
     assert (n <= de).all() and (de <= D).all()
     return n, de
 
@@ -71,8 +90,8 @@ def test_shapes_and_thresholds(sv, oracle_lib, V, D):
     inp = synth.accept_inputs(V + D, 16, D, V, target_std=2.5, draft_noise=1.0, mode="sample")
     if D:
         H_ref, JS_ref = oracle_lib.adasd_stats(inp["p"], inp["q"])
-        tau_h = float(np.quantile(H_ref, 0.8)) + 1e-3
-        tau_js = float(np.quantile(JS_ref, 0.5)) + 1e-3
+        tau_h = threshold_between(H_ref, 0.8)
+        tau_js = threshold_between(JS_ref, 0.5)
     else:
         tau_h, tau_js = 1.0, 0.1
     check(sv, oracle_lib, inp, tau_h, tau_js)
@@ -134,7 +153,14 @@ def test_batched_full_size(sv, oracle_lib):
     percentile of the draft entropies and tau_JS at the median distance."""
     inp = synth.accept_inputs(90, 256, 7, 131072, target_std=3.0, draft_noise=1.2, mode="sample")
     H_ref, JS_ref = oracle_lib.adasd_stats(inp["p"], inp["q"])
-    tau_h = float(np.quantile(H_ref, 0.9))
-    tau_js = float(np.quantile(JS_ref, 0.5))
+    tau_h = threshold_between(H_ref, 0.9)
+    tau_js = threshold_between(JS_ref, 0.5)
     n, de = check(sv, oracle_lib, inp, tau_h, tau_js)
     assert (de < 7).any() and (n > 0).any()
+
+
+def test_zz_disagreements_stay_below_the_cap():
+    """Over every comparison of this module: at most 1e-4 of the sequences
+    disagree with the oracle (each of them at a boundary)."""
+    assert TALLY["draws"] > 0
+    assert TALLY["disagree"] <= 1e-4 * TALLY["draws"], TALLY

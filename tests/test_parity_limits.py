@@ -18,6 +18,14 @@ import synth
 pytestmark = pytest.mark.gpu
 
 MARGIN = 1e-6
+# boundary disagreements over the module (checked against 1e-4 of the
+# sequences compared by the last test)
+TALLY = {"draws": 0, "disagree": 0}
+
+
+def tally(bad):
+    TALLY["draws"] += len(bad)
+    TALLY["disagree"] += int(bad.sum())
 
 
 @pytest.fixture(scope="module")
@@ -98,6 +106,7 @@ def test_acceptance_walks_63_drafts(sv, oracle_lib, V):
     n_ref, t_ref, margin, _ = oracle_lib.accept_sample(p, inp["q"], inp["draft"], inp["u_acc"], inp["u_res"])
     bad = (n.cpu().numpy() != n_ref) | (t.cpu().numpy() != t_ref)
     assert not (bad & (margin >= MARGIN)).any()
+    tally(bad)
     assert n_ref.max() >= 32
 
 
@@ -150,14 +159,17 @@ def test_adasd_over_63_drafts(sv, oracle_lib):
     percentile of the draft entropies (so stops fall deep in the draft),
     Jensen-Shannon threshold at the median; statistics within their
     tolerances, decisions bit-exact except draws within the margins the
-    dedicated AdaSD tests use (uniform 1e-6, statistic 5e-4)."""
+    dedicated AdaSD tests use (uniform 1e-6; a statistic within its error
+    bound, 1e-5 (1 + ln V), of its threshold)."""
     import torch
     B, D, V = 12, 63, 3000
     inp = synth.accept_inputs(63, B, D, V, target_std=2.5, draft_noise=0.3, mode="sample")
     p, q = inp["p"], inp["q"]
     H_ref, JS_ref = oracle_lib.adasd_stats(p, q)
-    tau_h = float(np.quantile(H_ref, 0.9)) + 1e-3
-    tau_js = float(np.quantile(JS_ref, 0.5)) + 1e-3
+    # thresholds half-way between neighbouring statistics (none lies on one)
+    hs, js = np.unique(H_ref), np.unique(JS_ref)
+    k, kj = int(0.9 * (len(hs) - 1)), int(0.5 * (len(js) - 1))
+    tau_h, tau_js = float((hs[k] + hs[k + 1]) / 2), float((js[kj] + js[kj + 1]) / 2)
     n, t, de, H, JS = [o.cpu().numpy() for o in sv.accept_adasd(
         to_dev(p), to_dev(q), to_dev(inp["draft"]), to_dev(inp["u_acc"]), to_dev(inp["u_res"]), tau_h, tau_js)]
     torch.cuda.synchronize()
@@ -166,8 +178,15 @@ def test_adasd_over_63_drafts(sv, oracle_lib):
     assert (np.abs(jsd - jsd_ref) <= 2e-6 + 1e-5 * jsd_ref).all()
     n_ref, t_ref, de_ref, mu, ms, _ = oracle_lib.accept_adasd(p, q, inp["draft"], inp["u_acc"], inp["u_res"],
                                                              tau_h, tau_js)
-    close = (mu < 1e-6) | (ms < 5e-4)
+    close = (mu < 1e-6) | (ms < 1e-5 * (1 + np.log(V)))
     bad = (n != n_ref) | (t != t_ref) | (de != de_ref)
     assert not (bad & ~close).any()
+    tally(bad)
     assert (n <= de).all() and (de <= D).all()
     assert de_ref.max() >= 8
+
+
+def test_zz_boundary_disagreements_stay_below_the_cap():
+    """Over every comparison of this module: at most 1e-4 of the sequences
+    disagree with the oracle (each one at a draw within 1e-6 of a boundary)."""
+    assert TALLY["disagree"] <= 1e-4 * max(TALLY["draws"], 1), TALLY
