@@ -1,8 +1,18 @@
-"""CUDA-graph tiers of the verification step (GPU).
+"""CUDA-graph tiers of the verification step against the oracle (GPU).
 
-One graph per draft length D in {1, 3, 7}; replaying a tier's graph must
-give exactly what launching the same step eagerly gives, and a controller
-driven loop can switch tiers between rounds.
+One graph per draft length D in {1, 3, 7} (the SGLang tiers of the
+handbook's "Adaptive speculative decoding" section).  Each tier's step is
+verify attention (with its log-sum-exp), one linear layer at GEMM-M =
+B(1+D), greedy acceptance and stochastic acceptance.  After every replay
+that the accepted-length controller selects, each output is compared with
+the fp64 oracle on the same inputs under the bars of the per-kernel parity
+tests:
+  * attention: max-abs 2e-2 and relative L2 1e-3 (output and LSE);
+  * GEMM: relative L2 5e-3 and |err| <= 2^-7 |y| + 1e-3;
+  * greedy acceptance: bit-exact;
+  * stochastic acceptance: bit-exact except decisions whose uniform lies
+    within 1e-6 of a test or CDF step (none at these sizes).
+Replays must also equal an eager launch of the same step bit for bit.
 """
 import numpy as np
 import pytest
@@ -10,6 +20,11 @@ import pytest
 import synth
 
 pytestmark = pytest.mark.gpu
+
+TIERS = (1, 3, 7)
+ATT_MAX_ABS, ATT_REL_L2 = 2e-2, 1e-3
+GEMM_REL_L2 = 5e-3
+MARGIN = 1e-6
 
 
 @pytest.fixture(scope="module")
@@ -24,63 +39,103 @@ def sv():
 
 
 class Tier:
-    """Static buffers of one tier's step: verify attention, one linear
-    layer at GEMM-M = B(1+D), stochastic acceptance."""
+    """Static buffers of one tier's step."""
 
-    def __init__(self, sv, D, B=4, Hkv=2, G=4, L=2048, V=4096, N=512, seed=0):
+    def __init__(self, sv, D, B=4, Hkv=2, G=4, lens=(2048, 700, 1500, 129), V=4096, N=512, K=512,
+                 seed=0):
         import torch
         self.sv, self.D, self.B, self.Hkv, self.G = sv, D, B, Hkv, G
-        self.attn = synth.attention_inputs_device(seed + D, B, Hkv, G, 128, D, L, page_size=64)
+        self.lens = [max(int(x), D + 1) for x in lens[:B]]
+        self.attn = synth.attention_inputs_device(seed + D, B, Hkv, G, 128, D, self.lens, page_size=64)
         self.out = torch.empty((B, D + 1, Hkv * G, 128), device="cuda")
-        self.ws_a = torch.empty(sv.attention_workspace_size(B, D, Hkv, G, 128, L), dtype=torch.uint8,
-                                device="cuda")
-        x, w = synth.gemm_inputs(seed + 10 + D, B * (D + 1), N, 512)
+        self.lse = torch.empty((B, D + 1, Hkv * G), device="cuda")
+        self.ws_a = torch.empty(sv.attention_workspace_size(B, D, Hkv, G, 128, max(self.lens)),
+                                dtype=torch.uint8, device="cuda")
+        self.x_bits, self.w_bits = synth.gemm_inputs(seed + 10 + D, B * (D + 1), N, K)
         to = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
-        self.x, self.w = to(x), to(w)
+        self.x, self.w = to(self.x_bits), to(self.w_bits)
         self.y = torch.empty((B * (D + 1), N), dtype=torch.bfloat16, device="cuda")
-        self.ws_g = torch.zeros(max(256, sv.gemm_workspace_size(B * (D + 1), N, 512)), dtype=torch.uint8,
+        self.ws_g = torch.zeros(max(256, sv.gemm_workspace_size(B * (D + 1), N, K)), dtype=torch.uint8,
                                 device="cuda")
-        acc = synth.accept_inputs(seed + 20 + D, B, D, V, mode="sample")
-        self.acc = {k: torch.from_numpy(np.ascontiguousarray(acc[k])).cuda()
-                    for k in ("p", "q", "draft", "u_acc", "u_res")}
-        self.na = torch.empty(B, dtype=torch.int32, device="cuda")
-        self.tk = torch.empty(B, dtype=torch.int32, device="cuda")
+        self.acc_host = synth.accept_inputs(seed + 20 + D, B, D, V, mode="both")
+        keys = ("p", "q", "draft_sample", "draft_greedy", "u_acc", "u_res")
+        self.acc = {k: torch.from_numpy(np.ascontiguousarray(self.acc_host[k])).cuda() for k in keys}
+        self.ng = torch.empty(B, dtype=torch.int32, device="cuda")
+        self.tg = torch.empty(B, dtype=torch.int32, device="cuda")
+        self.ns = torch.empty(B, dtype=torch.int32, device="cuda")
+        self.ts = torch.empty(B, dtype=torch.int32, device="cuda")
         self.ws_s = torch.empty(sv.accept_sample_workspace_size(B, V), dtype=torch.uint8, device="cuda")
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     def step(self):
         a, c = self.attn, self.acc
         self.sv.verify_attention(a.q, a.k_pages, a.v_pages, a.block_table, a.kv_len, self.D, self.Hkv, self.G,
-                                 out=self.out, workspace=self.ws_a)
-        self.sv.verify_gemm(self.x, self.w, y=self.y, workspace=self.ws_g)
-        self.sv.accept_sample(c["p"], c["q"], c["draft"], c["u_acc"], c["u_res"], self.na, self.tk,
-                              workspace=self.ws_s)
+                                 out=self.out, lse=self.lse, workspace=self.ws_a, dev_status=self.status)
+        self.sv.verify_gemm(self.x, self.w, y=self.y, workspace=self.ws_g, dev_status=self.status)
+        self.sv.accept_greedy(c["p"], c["draft_greedy"], self.ng, self.tg, dev_status=self.status)
+        self.sv.accept_sample(c["p"], c["q"], c["draft_sample"], c["u_acc"], c["u_res"], self.ns, self.ts,
+                              workspace=self.ws_s, dev_status=self.status)
+
+    def outputs(self):
+        return [self.out, self.lse, self.y, self.ng, self.tg, self.ns, self.ts]
 
     def results(self):
-        return [t.clone() for t in (self.out, self.y, self.na, self.tk)]
+        return [t.clone() for t in self.outputs()]
+
+    def oracle(self, oracle_lib):
+        """The oracle's outputs of this tier's step (computed once)."""
+        a, h = self.attn, self.acc_host
+        att, lse = oracle_lib.verify_attention(synth.bits_from_device(a.q), synth.bits_from_device(a.k_pages),
+                                               synth.bits_from_device(a.v_pages), a.block_table_host,
+                                               a.kv_len_host, self.D, self.Hkv, self.G, 128, a.page_size)
+        y = oracle_lib.gemm(self.x_bits, self.w_bits)
+        ng, tg = oracle_lib.accept_greedy(h["p"], h["draft_greedy"])
+        ns, ts, margin, _ = oracle_lib.accept_sample(h["p"], h["q"], h["draft_sample"], h["u_acc"], h["u_res"])
+        return dict(att=att, lse=lse, y=y, ng=ng, tg=tg, ns=ns, ts=ts, margin=margin)
 
 
-def test_graph_tiers_replay_exactly(sv):
+def check_against_oracle(tier, ref):
+    out, lse, y, ng, tg, ns, ts = (x.float().cpu().numpy() if x.is_floating_point() else x.cpu().numpy()
+                                   for x in tier.outputs())
+    for got, want in ((out.astype(np.float64), ref["att"]), (lse.astype(np.float64), ref["lse"])):
+        err = got - want
+        assert np.isfinite(got).all()
+        assert np.abs(err).max() <= ATT_MAX_ABS, np.abs(err).max()
+        assert np.linalg.norm(err) / np.linalg.norm(want) <= ATT_REL_L2
+    err = y.astype(np.float64) - ref["y"]
+    assert np.linalg.norm(err) / np.linalg.norm(ref["y"]) <= GEMM_REL_L2
+    assert (np.abs(err) <= 2 ** -7 * np.abs(ref["y"]) + 1e-3).all()
+    assert np.array_equal(ng, ref["ng"]) and np.array_equal(tg, ref["tg"])
+    bad = (ns != ref["ns"]) | (ts != ref["ts"])
+    assert not (bad & (ref["margin"] >= MARGIN)).any(), np.nonzero(bad)
+    assert int(tier.status.item()) == 0
+
+
+def test_graph_tiers_match_the_oracle(sv, oracle_lib):
     import torch
     from speculative_decoding_verification_attention_gb300.graphs import TierGraphs
-    tiers = {D: Tier(sv, D) for D in (1, 3, 7)}
+    tiers = {D: Tier(sv, D) for D in TIERS}
+    refs = {D: t.oracle(oracle_lib) for D, t in tiers.items()}
     eager = {}
     for D, t in tiers.items():
         t.step()
         torch.cuda.synchronize()
+        check_against_oracle(t, refs[D])           # the eager step itself
         eager[D] = t.results()
-    graphs = TierGraphs(lambda D: tiers[D].step(), tiers=(1, 3, 7))
-    ctl = sv.AdaptiveDraftLength((1, 3, 7), beta=0.5)
-    seen = set()
+    graphs = TierGraphs(lambda D: tiers[D].step(), tiers=TIERS)
+    ctl = sv.AdaptiveDraftLength(TIERS, beta=0.5)
+    seen = []
     for r in range(9):
         D = ctl.draft_len
-        seen.add(D)
-        for x in tiers[D].results():
+        seen.append(D)
+        for x in tiers[D].outputs():
             x.zero_()
         graphs.replay(D)
         torch.cuda.synchronize()
-        for got, ref in zip(tiers[D].results(), eager[D]):
-            assert torch.equal(got, ref)
-        # drive the controller with a synthetic acceptance pattern
-        n = np.full(4, [0, D, 1, D // 2, 0, 0, D, D, 0][r], np.int32)
-        ctl.update(n)
-    assert len(seen) >= 2
+        check_against_oracle(tiers[D], refs[D])
+        for got, want in zip(tiers[D].outputs(), eager[D]):
+            assert torch.equal(got, want)
+        # drive the controller with a synthetic acceptance pattern that
+        # walks it across the tiers
+        ctl.update(np.full(4, [0, D, 1, D // 2, 0, 0, D, D, 0][r], np.int32))
+    assert len(set(seen)) >= 2, seen
