@@ -64,10 +64,10 @@ typedef enum {
 #define SPEC_DEV_ERR_TREE        0x00000080u /* draft tree not in topological order */
 #define SPEC_DEV_ERR_LOGITS      0x00000100u /* a logits row holding NaN or +inf, or no
                                                 finite entry: all its probabilities 0 */
-#define SPEC_DEV_ERR_PROB        0x00000200u /* a probability outside [0, 1] (or NaN) in a
-                                                row the stochastic acceptance draws from, or
-                                                a row summing to 8 or more: the draw is
-                                                undefined */
+#define SPEC_DEV_ERR_PROB        0x00000200u /* the row the stochastic acceptance draws
+                                                from holds a value its exact masses cannot
+                                                represent (negative, NaN, 2 or more) or sums
+                                                to about 8 or more: the draw is undefined */
 #define SPEC_DEV_INFO_ZERO_RESIDUAL 0x00010000u /* informational: max(0,p-q) summed to 0
                                                    after a rejection; drew from p instead */
 
@@ -295,9 +295,11 @@ spec_status_t spec_accept_tree_greedy(const float *p, const int32_t *tokens, con
  *
  *   p        device, fp32 [B][1+D][V], entries in [0, 1], row sums < 8.
  *   q        device, fp32 [B][D][V], same constraints (may be NULL if D=0).
- *            The row a sequence draws from is checked: an entry outside
- *            [0, 1] (or NaN), or a row sum of 8 or more (its exact masses
- *            would overflow), sets SPEC_DEV_ERR_PROB.
+ *            The values a sequence draws from are checked: a residual
+ *            max(0, p - q), or a bonus-row p, that is negative (other than
+ *            -0), NaN or 2 or more, or a row whose values sum to about 8 or
+ *            more (the 64-bit sums of its 2^-61 masses would wrap), sets
+ *            SPEC_DEV_ERR_PROB.
  *   draft    device, int32 [B][D].
  *   u_acc    device, fp32 [B][D] in [0, 1).
  *   u_res    device, fp32 [B] in [0, 1).

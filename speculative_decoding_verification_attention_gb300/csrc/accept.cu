@@ -429,11 +429,20 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x,
     return x;
 }
 
-// A probability the fixed point represents: 0 <= x <= 1 (false for NaN).
-__device__ __forceinline__ bool prob_ok(float4 x)
+// Range checks of the probability form, cheap enough for the streaming
+// loop.  A value the fixed point represents, 0 <= x < 2 (+0 included, NaN
+// not), has bits below 0x40000000: one unsigned max per element covers
+// negative values, NaN, infinities and x >= 2 at once.  A group's 512
+// masses wrap their 64-bit sums only if they add up to 8 or more; each
+// lane keeps the sum of its 4-element masses >> 40 (a 32-bit shadow, at
+// most 2 lost per step), and only when some lane's shadow reaches a
+// 32nd of the bound is the warp's total formed.
+constexpr uint32_t kFixRangeBits = 0x40000000u;        // bits of 2.0f
+constexpr uint32_t kShadowBound = (1u << 24) - 128u;   // 2^64 >> 40, less the truncation
+__device__ __forceinline__ uint32_t max_bits4(uint32_t acc, float4 r)
 {
-    return x.x >= 0.0f && x.x <= 1.0f && x.y >= 0.0f && x.y <= 1.0f && x.z >= 0.0f && x.z <= 1.0f &&
-           x.w >= 0.0f && x.w <= 1.0f;
+    return max(max(acc, max(__float_as_uint(r.x), __float_as_uint(r.y))),
+               max(__float_as_uint(r.z), __float_as_uint(r.w)));
 }
 
 __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long x, int lane)
@@ -836,8 +845,10 @@ __global__ void __launch_bounds__(kThreads) accept_prep_kernel(SampleIn in, cons
 // w0 of the n-element slice (sp, sq): staged in shared memory (SMEM,
 // n % 4 == 0) or read from global memory.  Lane k of the result holds step
 // k's total (k < kGroupSteps).
-// bad: set when an element is not a probability in [0, 1] or a step's sum
-// wraps (its row sums to 8 or more); the fixed point cannot represent them.
+// Probability form: bad is set when a value turned into mass (max(0, p -
+// q), or p for a bonus draw) is negative, NaN or 2 or more, or when the
+// group's masses sum to about 8 or more (their 64-bit sums could wrap);
+// the fixed point represents neither.
 template <bool SMEM, bool LOGITS>
 __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, const float *sq,
                                                                int residual, int w0, int n, bool vec4,
@@ -845,6 +856,7 @@ __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, 
                                                                const SoftmaxPair &rq, const float2 *tab, bool &bad)
 {
     unsigned long long mine = 0;
+    uint32_t mb = 0, shadow = 0;
 #pragma unroll
     for (int k = 0; k < kGroupSteps; ++k) {
         const int e = w0 + k * kStep + lane * 4;
@@ -860,12 +872,34 @@ __device__ __forceinline__ unsigned long long warp_step_masses(const float *sp, 
             }
             xp = to_prob4<LOGITS>(xp, rp, tab);
             if (residual) xq = to_prob4<LOGITS>(xq, rq, tab);
-            if (!LOGITS) bad |= !prob_ok(xp) || (residual && !prob_ok(xq));
-            m = mass(xp.x, xq.x, residual) + mass(xp.y, xq.y, residual) + mass(xp.z, xq.z, residual) +
-                mass(xp.w, xq.w, residual);
+            float4 r;
+            if (residual) {
+                r = make_float4(fmaxf(__fsub_rn(xp.x, xq.x), 0.0f), fmaxf(__fsub_rn(xp.y, xq.y), 0.0f),
+                                fmaxf(__fsub_rn(xp.z, xq.z), 0.0f), fmaxf(__fsub_rn(xp.w, xq.w), 0.0f));
+            } else if (!LOGITS) {
+                // x + 0 turns -0 into +0, the one sign-bit value the range check must pass
+                r = make_float4(__fadd_rn(xp.x, 0.0f), __fadd_rn(xp.y, 0.0f), __fadd_rn(xp.z, 0.0f),
+                                __fadd_rn(xp.w, 0.0f));
+            } else {
+                r = xp;
+            }
+            m = fix61(r.x) + fix61(r.y) + fix61(r.z) + fix61(r.w);
+            if (!LOGITS) {
+                mb = max_bits4(mb, r);
+                shadow += static_cast<uint32_t>(m >> 40);
+            }
         }
-        const unsigned long long t = warp_sum_u64(m, bad);
+        const unsigned long long t = warp_sum_u64(m);
         if (lane == k) mine = t;
+    }
+    if (!LOGITS) {
+        bad |= mb >= kFixRangeBits;
+        if (__any_sync(0xffffffffu, shadow >= kShadowBound / 32u)) {
+            uint32_t tot = shadow;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+            bad |= tot >= kShadowBound;
+        }
     }
     return mine;
 }
@@ -970,8 +1004,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) accept_stream_kernel(
         const int s0 = chunk * (kChunk / kStep) + warp * kGroupSteps;
         if (lane < kGroupSteps && s0 + lane < sc.nsteps)
             sc.steps[static_cast<int64_t>(b) * sc.nsteps + s0 + lane] = t;
-        const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull, bad);
-        if (__any_sync(0xffffffffu, bad) && lane == 0) report(dev_status, SPEC_DEV_ERR_PROB);
+        const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull);
+        if (!LOGITS && __any_sync(0xffffffffu, bad) && lane == 0) report(dev_status, SPEC_DEV_ERR_PROB);
         const int gi = chunk * kConsumers + warp;
         if (lane == 0 && gi < sc.ngroups) sc.gtot[static_cast<int64_t>(b) * sc.ngroups + gi] = gt;
     }
@@ -1102,7 +1136,7 @@ __global__ void __launch_bounds__(kThreads) accept_finalize_kernel(
             const unsigned long long t =
                 warp_step_masses<false, LOGITS>(prow + g0, nullptr, 0, 0, n, false, lane, rp, rq, s_tab, ovf);
             if (lane < kGroupSteps && g * kGroupSteps + lane < sc.nsteps) steps[g * kGroupSteps + lane] = t;
-            const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull, ovf);
+            const unsigned long long gt = warp_sum_u64(lane < kGroupSteps ? t : 0ull);
             if (lane == 0) gtot[g] = gt;
         }
         __syncwarp();

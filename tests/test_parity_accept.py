@@ -176,12 +176,12 @@ def test_invalid_token_and_uniform_are_flagged(sv):
 
 
 def test_rows_that_are_not_probabilities_are_flagged(sv):
-    """The row a sequence draws from must hold probabilities in [0, 1] with a
-    sum below 8 (its exact 2^-61 masses fit in 64 bits); a NaN, a negative
-    entry, an entry above 1 or a row summing past 8 sets the PROB bit, and a
-    valid row does not."""
+    """The values a sequence draws from must lie in [0, 2) and sum below 8
+    (its exact 2^-61 masses fit in 64 bits); a NaN, a negative entry, an
+    entry of 2 or more or a row summing past 8 sets the PROB bit, while a
+    valid row, -0 entries included, does not."""
     import torch
-    B, D, V = 5, 1, 3000
+    B, D, V = 6, 1, 3000
     rng = np.random.default_rng(5)
     q = rng.random((B, D, V)).astype(np.float32)
     q /= q.sum(axis=-1, keepdims=True)
@@ -190,12 +190,14 @@ def test_rows_that_are_not_probabilities_are_flagged(sv):
     p[:, D] = q[:, 0]
     p[1, D, 17] = np.nan
     p[2, D, V - 1] = -0.25
-    p[3, D, 100] = 1.5
+    p[3, D, 100] = 2.5
     p[4, D, :] = 0.9               # sums to 2700
+    p[5, D, :] = 0.01              # every 512-element group below 8, the row at 30
+    p[0, D, :40] = -0.0            # -0 is a zero probability
     draft = np.zeros((B, D), np.int32)
     u_acc = np.full((B, D), 0.5, np.float32)
     u_res = np.full(B, 0.5, np.float32)
-    for rows, flagged in (([0], False), ([0, 1], True), ([2], True), ([3, 0], True), ([4], True)):
+    for rows, flagged in (([0], False), ([0, 1], True), ([2], True), ([3, 0], True), ([4], True), ([5], True)):
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         n, t = run_sample(sv, p[rows], q[rows], draft[rows], u_acc[rows], u_res[rows], dev_status=st)
         assert bool(int(st.item()) & sv.DEV_STATUS_BITS["PROB"]) == flagged, rows
