@@ -506,9 +506,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // stage per 0.30 us.  Also measured and slower: x shared by two pairs
 // through cluster multicast (clusters of 4), TMA prefetches into L2 ahead
 // of the loads, and direct global stores from eight epilogue warps.
-constexpr int kPairStages = 6;
+// A stage carries kPairKps k-blocks: [x kb][x kb + 1][w kb][w kb + 1].
+// A ring of tensor copies completes about one stage per ~0.45 us per SM
+// whatever the stage's bytes (16 to 64 KB) and the ring depth, so each
+// stage must carry enough work: one k-block per stage left the MMAs
+// waiting (0.37 us per k-block at 256 x 160 tiles, where the MMAs need
+// 0.21 us).
+constexpr int kPairKps = 2;
+constexpr int kPairStages = 3;
 constexpr uint32_t kPairTileB = 128 * kBK * 2;            // up to 128 w rows per CTA
-constexpr uint32_t kPairStage = kTileA + kPairTileB;      // 32 KB
+constexpr uint32_t kPairStage = kPairKps * (kTileA + kPairTileB);   // 64 KB
 constexpr uint32_t kPairSmem = kPairStages * kPairStage + kOutStaging + 1024 /*align*/ + 256 /*barriers*/;
 constexpr uint32_t kPairTmemCols = 256;                   // one accumulator, W <= 256
 constexpr uint16_t kPairMask = 0x3;
@@ -594,14 +601,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row_x = (2 * mt + static_cast<int>(rank)) * kBM;
             const int row_w = g.col0(nt) + static_cast<int>(rank) * half;
             bool ok = true;
-            for (int kb = 0; kb < g.kblocks; ++kb, ++it) {
+            for (int kb0 = 0; kb0 < g.kblocks; kb0 += kPairKps, ++it) {
+                const int nk = g.kblocks - kb0 < kPairKps ? g.kblocks - kb0 : kPairKps;
                 const int st = it % kPairStages;
                 if (it >= kPairStages &&
                     !mbar_wait(&empty[st], ((it / kPairStages) & 1) ^ 1, abort, dev_status)) { ok = false; break; }
                 uint8_t *sa = smem + st * kPairStage;
-                if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * bytes);
-                tma_load_2d_pair(sa, &tm_x, full0 + st * 8, kb * kBK, row_x);
-                tma_load_2d_pair(sa + kTileA, tw, full0 + st * 8, kb * kBK, row_w);
+                if (rank == 0) mbar_arrive_expect_tx(&full[st], 2 * bytes * nk);
+                for (int q = 0; q < nk; ++q) {
+                    tma_load_2d_pair(sa + q * kTileA, &tm_x, full0 + st * 8, (kb0 + q) * kBK, row_x);
+                    tma_load_2d_pair(sa + kPairKps * kTileA + q * kPairTileB, tw, full0 + st * 8, (kb0 + q) * kBK,
+                                     row_w);
+                }
             }
             if (!ok) break;
         }
@@ -629,15 +640,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lt >= 1 && !mbar_wait(acc_empty, (lt - 1) & 1, abort, dev_status)) break;
             tc_fence_after();
             bool ok = true;
-            for (int kb = 0; kb < g.kblocks; ++kb, ++it) {
+            for (int kb0 = 0; kb0 < g.kblocks; kb0 += kPairKps, ++it) {
+                const int nk = g.kblocks - kb0 < kPairKps ? g.kblocks - kb0 : kPairKps;
                 const int st = it % kPairStages;
                 if (!mbar_wait(&full[st], (it / kPairStages) & 1, abort, dev_status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sa = smem_u32(smem + st * kPairStage);
+                for (int q = 0; q < nk; ++q) {
+                    const uint32_t a = sa + q * kTileA, b = sa + kPairKps * kTileA + q * kPairTileB;
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k)
-                    umma_f16_ss_pair(tmem, sdesc(sa + k * 32, 16, 1024), sdesc(sa + kTileA + k * 32, 16, 1024),
-                                     idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < kBK / 16; ++k)
+                        umma_f16_ss_pair(tmem, sdesc(a + k * 32, 16, 1024), sdesc(b + k * 32, 16, 1024), idesc,
+                                         (kb0 > 0 || q > 0 || k > 0) ? 1u : 0u);
+                }
                 umma_commit_pair(&empty[st], kPairMask);
             }
             if (!ok) break;
