@@ -499,19 +499,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 // in both, and the commit signals the stage free in both CTAs.  The
 // accumulator (128 rows x W fp32 per CTA) lives in each CTA's tensor memory
 // and each CTA's epilogue writes its own 128 output rows.
-// Measured with per-k-block timestamps of a diagnostic copy (N = K = 6144):
-// a stage completes every ~0.37 us whatever the tile width (128 to 256
-// columns), the bytes staged per k-block (x alone, w alone, or both) and the
-// number of stages (6 to 8); the same loads without the MMAs complete one
-// stage per 0.30 us.  Also measured and slower: x shared by two pairs
-// through cluster multicast (clusters of 4), TMA prefetches into L2 ahead
-// of the loads, and direct global stores from eight epilogue warps.
 // A stage carries kPairKps k-blocks: [x kb][x kb + 1][w kb][w kb + 1].
 // A ring of tensor copies completes about one stage per ~0.45 us per SM
-// whatever the stage's bytes (16 to 64 KB) and the ring depth, so each
-// stage must carry enough work: one k-block per stage left the MMAs
-// waiting (0.37 us per k-block at 256 x 160 tiles, where the MMAs need
-// 0.21 us).
+// whatever the stage's bytes (16 to 64 KB) and the ring depth (a copy
+// micro-benchmark on GB300), so a stage must carry enough work: with one
+// k-block per stage a stage completed every ~0.37 us whatever the tile
+// width, the bytes staged and the stage count (6 to 8), and the MMAs, which
+// need 0.21 us per k-block at 256 x 160 tiles, waited.  Measured and no
+// faster: a second producer warp filling alternate stages, each pair
+// starting at its own k-block, three k-blocks per stage in two stages
+// (slower: a stage's refill waits for its MMAs), x shared by two pairs
+// through cluster multicast (clusters of 4), TMA prefetches into L2 ahead
+// of the loads, direct global stores from eight epilogue warps.
 constexpr int kPairKps = 2;
 constexpr int kPairStages = 3;
 constexpr uint32_t kPairTileB = 128 * kBK * 2;            // up to 128 w rows per CTA
