@@ -96,8 +96,8 @@ int spec_version(void);
  *                 belongs to KV head h.  16-byte aligned.
  *   k_pages_bf16,
  *   v_pages_bf16  device, bf16 [num_pages][page_size][Hkv][head_dim].
- *                 16-byte aligned.  V entries must be finite and within
- *                 +-65504 (they are staged in fp16 for the P.V product).
+ *                 16-byte aligned.  V is used as stored (bf16 operand of
+ *                 the P.V product, P carried as a bf16 hi + lo pair).
  *   block_table   device, int32 [B][max_pages_per_seq]; key j of sequence b
  *                 is slot j % page_size of page block_table[b][j/page_size].
  *                 Entries past a sequence's last page are never read.
