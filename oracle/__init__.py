@@ -91,6 +91,7 @@ def _load():
             lib.oracle_tree_attention.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
                                                   i32, f64, i64, i32, P, P, P, i32]
             lib.oracle_accept_tree_greedy.argtypes = [P, P, P, i32, i32, i32, P, P, P, i32]
+            lib.oracle_accept_tree_sample.argtypes = [P, P, P, P, P, P, i32, i32, i32, P, P, P, P, P, i32]
             lib.oracle_logits_to_probs.argtypes = [P, P, ctypes.c_float, ctypes.c_uint64, i32, i32, i32,
                                                    P, P, P, P, i32]
             lib.oracle_logits_row_stats.argtypes = [P, P, ctypes.c_float, i32, i32, i32, P, P, i32]
@@ -99,7 +100,8 @@ def _load():
                                                 P, P, P, P, P, P, i32]
             for f in ("oracle_verify_attention", "oracle_gemm", "oracle_accept_greedy",
                       "oracle_accept_sample", "oracle_max_threads", "oracle_tree_attention",
-                      "oracle_accept_tree_greedy", "oracle_logits_to_probs", "oracle_logits_row_stats",
+                      "oracle_accept_tree_greedy", "oracle_accept_tree_sample", "oracle_logits_to_probs",
+                      "oracle_logits_row_stats",
                       "oracle_adasd_stats", "oracle_accept_adasd"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -258,6 +260,31 @@ def accept_tree_greedy(p, tokens, parent, threads=0):
     if rc:
         raise ValueError(f"oracle_accept_tree_greedy failed: {rc}")
     return n, t, path[:, :D]
+
+
+def accept_tree_sample(p, q, tokens, parent, u_acc, u_res, threads=0):
+    """Stochastic tree acceptance (reading R12): p, q float32 [B, 1+D, V]
+    (q row k = the draft distribution node k's children were drawn from),
+    tokens, parent int32 [B, 1+D], u_acc float32 [B, 1+D] (entry 0 unused),
+    u_res float32 [B].  Returns (n_accepted, token, path [B, D], margin,
+    flag)."""
+    lib = _load()
+    p, q = _c(p, np.float32), _c(q, np.float32)
+    tokens, parent = _c(tokens, np.int32), _c(parent, np.int32)
+    u_acc, u_res = _c(u_acc, np.float32), _c(u_res, np.float32)
+    B, T, V = p.shape
+    D = T - 1
+    n = np.empty(B, np.int32)
+    t = np.empty(B, np.int32)
+    path = np.empty((B, max(D, 1)), np.int32)
+    margin = np.empty(B, np.float64)
+    flag = np.empty(B, np.int32)
+    rc = lib.oracle_accept_tree_sample(_ptr(p), _ptr(q), _ptr(tokens), _ptr(parent), _ptr(u_acc), _ptr(u_res),
+                                       B, D, V, _ptr(n), _ptr(t), _ptr(path), _ptr(margin), _ptr(flag),
+                                       int(threads))
+    if rc:
+        raise ValueError(f"oracle_accept_tree_sample failed: {rc}")
+    return n, t, path[:, :D], margin, flag
 
 
 def logits_to_probs(zp, zq, temperature, seed, threads=0):

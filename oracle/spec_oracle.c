@@ -337,6 +337,7 @@ int oracle_accept_sample(const float *p, const float *q, const int32_t *draft,
  *     n_acc = the depth reached, the emitted token is the argmax at the
  *     last node, and the path lists the accepted nodes in order.  A chain
  *     whose node k carries draft k-1 is the greedy acceptance above.
+ *  R12 stochastic tree acceptance: see oracle_accept_tree_sample.
  * ---------------------------------------------------------------------- */
 
 /* Whether parent[0..T) is a valid tree in topological order. */
@@ -478,6 +479,112 @@ int oracle_accept_tree_greedy(const float *p, const int32_t *tokens, const int32
         token[b] = t;
     }
     return 0;
+}
+
+/* Stochastic tree acceptance (reading R12).  The children of node k (the
+ * nodes whose parent is k, in increasing index) carry tokens drafted from
+ * q[b][k].  From the root, at the current node v the working row r starts
+ * as p[b][v]; child c with token x is accepted iff u_acc[b][c] * q[b][v][x]
+ * < r(x) (the walk then moves to c), otherwise r becomes max(0, r -
+ * q[b][v]) divided by its sum (left unchanged, and flagged, when that sum is
+ * 0) and the next child is tried.  When no child of v is accepted, or v has
+ * none, the token is drawn from r with u_res[b]: the smallest v with
+ * sum_{w <= v} r(w) > u_res[b] * sum_w r(w).  For a chain whose node k
+ * carries draft k - 1 this is the stochastic acceptance above.
+ * p, q [B][1+D][V] (q's rows of leaves are not read), tokens, parent,
+ * u_acc [B][1+D] (entry 0 unused), u_res [B].  Outputs n_accepted (the
+ * depth reached), token, path [B][D] (accepted nodes, -1 after the last),
+ * margin (min over the tests of |u - r(x)/q(x)| and over the draw of the
+ * CDF gap / sum r) and flag (1 when an empty residual was left as it
+ * was).  Returns -4 for an invalid tree or token. */
+static int draw_row_f64(const double *r, int V, double u, double *margin)
+{
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v) Z += r[v];
+    if (!(Z > 0.0)) return -1;
+    const double T = u * Z;
+    double C = 0.0, mg = INFINITY;
+    int pick = -1;
+    for (int v = 0; v < V; ++v) {
+        C += r[v];
+        const double gap = fabs(T - C);
+        if (gap < mg) mg = gap;
+        if (pick < 0 && C > T) pick = v;
+    }
+    if (pick < 0)
+        for (int v = V - 1; v >= 0; --v)
+            if (r[v] > 0.0) { pick = v; break; }
+    if (margin) *margin = mg / Z;
+    return pick;
+}
+
+int oracle_accept_tree_sample(const float *p, const float *q, const int32_t *tokens, const int32_t *parent,
+                              const float *u_acc, const float *u_res, int B, int D, int V,
+                              int32_t *n_accepted, int32_t *token, int32_t *path, double *margin,
+                              int32_t *flag, int num_threads)
+{
+    if (B < 0 || D < 0 || D > 63 || V < 1) return -2;
+    const int T = 1 + D;
+    for (int b = 0; b < B; ++b) {
+        if (!tree_valid(parent + (int64_t)b * T, T)) return -4;
+        for (int k = 1; k < T; ++k) {
+            const int32_t x = tokens[(int64_t)b * T + k];
+            if (x < 0 || x >= V) return -4;
+        }
+    }
+    int err = 0;
+    set_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const float *pb = p + (int64_t)b * T * V, *qb = q + (int64_t)b * T * V;
+        const int32_t *par = parent + (int64_t)b * T, *tok = tokens + (int64_t)b * T;
+        double *r = (double *)malloc((size_t)V * sizeof(double));
+        if (!r) {
+#pragma omp atomic write
+            err = -3;
+            continue;
+        }
+        for (int x = 0; x < D; ++x) path[(int64_t)b * D + x] = -1;
+        int cur = 0, depth = 0, fl = 0;
+        double mg = INFINITY;
+        for (;;) {
+            const float *pv = pb + (int64_t)cur * V, *qv = qb + (int64_t)cur * V;
+            for (int v = 0; v < V; ++v) r[v] = (double)pv[v];
+            int next = -1;
+            for (int c = cur + 1; c < T && next < 0; ++c) {
+                if (par[c] != cur) continue;
+                const int x = tok[c];
+                const double u = (double)u_acc[(int64_t)b * T + c];
+                const double qx = (double)qv[x];
+                if (qx > 0.0) {
+                    const double gap = fabs(u - r[x] / qx);
+                    if (gap < mg) mg = gap;
+                }
+                if (u * qx < r[x]) { next = c; break; }
+                double Z = 0.0;
+                for (int v = 0; v < V; ++v) Z += fmax(0.0, r[v] - (double)qv[v]);
+                if (Z > 0.0) {
+                    for (int v = 0; v < V; ++v) r[v] = fmax(0.0, r[v] - (double)qv[v]) / Z;
+                } else {
+                    fl = 1;
+                }
+            }
+            if (next < 0) break;
+            path[(int64_t)b * D + depth] = next;
+            ++depth;
+            cur = next;
+        }
+        double dm = INFINITY;
+        int t = draw_row_f64(r, V, (double)u_res[b], &dm);
+        if (t < 0) t = 0;
+        if (dm < mg) mg = dm;
+        n_accepted[b] = depth;
+        token[b] = t;
+        if (margin) margin[b] = mg;
+        if (flag) flag[b] = fl;
+        free(r);
+    }
+    return err;
 }
 
 /* ------------------------------------------------------------------------

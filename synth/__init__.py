@@ -36,7 +36,7 @@ __all__ = [
     "philox4x32_10", "philox_uniform", "acceptance_uniforms",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "AttentionInputs",
     "attention_inputs", "paged_layout", "accept_inputs", "gemm_inputs",
-    "draw_from_rows", "tune_sigma_for_alpha", "STREAM_ACCEPT",
+    "draw_from_rows", "tune_sigma_for_alpha", "tree_sample_inputs", "STREAM_ACCEPT",
     "STREAM_RESAMPLE", "STREAM_DRAFT",
 ]
 
@@ -349,6 +349,32 @@ def log2_ceil(x):
 # ---------------------------------------------------------------------------
 # Draft trees.
 # ---------------------------------------------------------------------------
+def tree_sample_inputs(seed, B, D, V, kind="random", target_std=2.0, draft_noise=0.5):
+    """Inputs of the stochastic tree acceptance: p, q float32 [B, 1+D, V]
+    (fp32 softmax of fp64 logits; target logits ~ N(0, target_std^2) per
+    node, draft logits = target + N(0, draft_noise^2)), parent int32
+    [B, 1+D] (``tree_parents``), tokens int32 [B, 1+D] where node k's token
+    is drawn from q[b, parent[k]] with Philox stream 2, counter (b, k)
+    (siblings are independent draws; entry 0 is 0), u_acc float32 [B, 1+D]
+    from counter (b, k, 0, 0) and u_res float32 [B] from (b, 0, 1, 0)."""
+    rng = np.random.default_rng(seed)
+    T = 1 + D
+    t = rng.standard_normal((B, T, V)) * target_std
+    p = _softmax64(t).astype(np.float32)
+    q = _softmax64(t + rng.standard_normal((B, T, V)) * draft_noise).astype(np.float32)
+    parent = tree_parents(seed + 1, B, T, kind)
+    b = np.arange(B, dtype=np.uint64)
+    k = np.arange(T, dtype=np.uint64)
+    ud = philox_uniform(seed, b[:, None], k[None, :], STREAM_DRAFT)
+    tokens = np.zeros((B, T), np.int32)
+    for kk in range(1, T):
+        rows = q[np.arange(B), parent[:, kk]]
+        tokens[:, kk] = draw_from_rows(rows, ud[:, kk])
+    u_acc = philox_uniform(seed, b[:, None], k[None, :], STREAM_ACCEPT).astype(np.float32)
+    u_res = philox_uniform(seed, b, np.zeros_like(b), STREAM_RESAMPLE).astype(np.float32)
+    return dict(p=p, q=q, parent=parent, tokens=tokens, u_acc=u_acc, u_res=u_res)
+
+
 def tree_parents(seed, B, T, kind="random"):
     """Parent arrays int32 [B, T] of draft trees in topological order
     (parent[:, 0] = -1, 0 <= parent[b, k] < k).

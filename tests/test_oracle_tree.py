@@ -16,6 +16,7 @@ Greedy tree acceptance (reading R8) is checked against:
 import numpy as np
 import pytest
 import torch
+from scipy import stats
 
 import synth
 from test_oracle_attention import gather_contiguous
@@ -226,3 +227,143 @@ def test_emitted_tokens_are_greedy_decoding_of_a_toy_model(oracle_lib):
         for _ in range(n[0] + 1):
             s.append(int(np.argmax(model(s[-2], s[-1]))))
         assert emitted == s[len(ctx):]
+
+
+# ---------------------------------------------------------------- stochastic
+# Stochastic tree acceptance (reading R12) is checked against:
+#   * the chain special case, which must reproduce the (separately pinned)
+#     stochastic acceptance;
+#   * hand-worked small cases with siblings (a rejected child changes the
+#     row the next sibling is tested against, then the residual draw);
+#   * the law of the first emitted token: with k children drafted
+#     independently from q at the root, it must follow p at the root
+#     exactly (the rule is lossless), checked by chi-square;
+#   * the flag for an empty residual and the rejection of invalid trees.
+
+def chain_as_tree(inp):
+    """The chain acceptance's inputs laid out as a tree: node k carries draft
+    k - 1 and node k's draft row is q[:, k] (the last node has none)."""
+    p, q, draft, u_acc = inp["p"], inp["q"], inp["draft"], inp["u_acc"]
+    B, T, V = p.shape
+    D = T - 1
+    qt = np.zeros_like(p)
+    qt[:, :D] = q
+    tokens = np.zeros((B, T), np.int32)
+    tokens[:, 1:] = draft
+    parent = np.tile(np.arange(-1, D, dtype=np.int32), (B, 1))
+    ua = np.zeros((B, T), np.float32)
+    ua[:, 1:] = u_acc
+    return p, qt, tokens, parent, ua
+
+
+@pytest.mark.parametrize("B,D,V", [(200, 4, 50), (60, 7, 3000), (30, 0, 100)])
+def test_tree_sample_chain_equals_stochastic_acceptance(oracle_lib, B, D, V):
+    inp = synth.accept_inputs(B + D, B, D, V, mode="sample")
+    n, t, margin, _ = oracle_lib.accept_sample(inp["p"], inp["q"], inp["draft"], inp["u_acc"], inp["u_res"])
+    p, qt, tokens, parent, ua = chain_as_tree(inp)
+    n2, t2, path, margin2, flag = oracle_lib.accept_tree_sample(p, qt, tokens, parent, ua, inp["u_res"])
+    # the chain draws from max(0, p - q) as it is, the tree from it divided
+    # by its sum: equal except within rounding of a step
+    ok = margin > 1e-9
+    assert np.array_equal(n[ok], n2[ok]) and np.array_equal(t[ok], t2[ok])
+    assert ok.mean() > 0.99
+    for b in range(B):
+        assert list(path[b, :n2[b]]) == list(range(1, n2[b] + 1))
+        assert (path[b, n2[b]:] == -1).all()
+
+
+def one_node_tree(p_rows, q_rows, parent, tokens, u_acc, u_res):
+    p = np.asarray(p_rows, np.float32)[None]
+    q = np.asarray(q_rows, np.float32)[None]
+    return (p, q, np.asarray(tokens, np.int32)[None], np.asarray(parent, np.int32)[None],
+            np.asarray(u_acc, np.float32)[None], np.asarray([u_res], np.float32))
+
+
+def test_tree_sample_siblings_hand_worked(oracle_lib):
+    # root p = (.5, .3, .2, 0), q = uniform.  Child 1 carries token 3 (p = 0:
+    # rejected for any u); the working row becomes max(0, p - q) / .3 =
+    # (5/6, 1/6, 0, 0).  Child 2 carries token 0: 5/6 > u * 1/4 for any u,
+    # so it is accepted; child 2 is a leaf and the token is drawn from its
+    # own p row (one-hot on 2).
+    V = 4
+    p = [[.5, .3, .2, 0], [0, 0, 0, 0], [0, 0, 1, 0]]
+    q = [[.25, .25, .25, .25], [.25] * 4, [.25] * 4]
+    for u in (0.0, 0.5, 0.999):
+        args = one_node_tree(p, q, [-1, 0, 0], [0, 3, 0], [0, u, u], 0.3)
+        n, t, path, margin, flag = oracle_lib.accept_tree_sample(*args)
+        assert n[0] == 1 and path[0, 0] == 2 and t[0] == 2 and flag[0] == 0
+    # child 2 carries token 1 instead: accepted iff u * 1/4 < 1/6, i.e.
+    # u < 2/3.  Rejected, the row becomes max(0, (5/6, 1/6, 0, 0) - q) / sum
+    # = (1, 0, 0, 0): the token is 0 whatever u_res.
+    for u, acc in ((0.5, True), (0.9, False)):
+        for ur in (0.0, 0.7):
+            args = one_node_tree(p, q, [-1, 0, 0], [0, 3, 1], [0, 0.5, u], ur)
+            n, t, path, margin, flag = oracle_lib.accept_tree_sample(*args)
+            if acc:
+                assert n[0] == 1 and path[0, 0] == 2
+            else:
+                assert n[0] == 0 and t[0] == 0 and path[0, 0] == -1
+    # rejected at u = .7: the margin is the smallest of the first test's
+    # |.5 - 0|, the second's |.7 - (1/6)/(1/4)| and the draw's 1 - .3
+    args = one_node_tree(p, q, [-1, 0, 0], [0, 3, 1], [0, 0.5, 0.7], 0.3)
+    n, _, _, margin, _ = oracle_lib.accept_tree_sample(*args)
+    assert n[0] == 0 and abs(margin[0] - abs(0.7 - 2.0 / 3.0)) < 1e-6   # fp32 inputs
+
+
+def test_tree_sample_empty_residual_is_flagged(oracle_lib):
+    # a draft token of zero target mass is rejected even at u = 0 (0 < 0 is
+    # false); the residual max(0, p - q) = (0, .3, 0) then gives token 1
+    p = [[.4, .6, 0], [1, 0, 0]]
+    q = [[.4, .3, .3], [1, 0, 0]]
+    n, t, path, margin, flag = oracle_lib.accept_tree_sample(*one_node_tree(p, q, [-1, 0], [0, 2], [0, 0.0], 0.5))
+    assert n[0] == 0 and t[0] == 1 and flag[0] == 0
+    # p = q at the root and two children on a token with p = q = 0: both are
+    # rejected, max(0, p - q) has no mass each time, so the row stays p and
+    # the flag is set; the draw from p = (.5, .5, 0) at .75 gives token 1
+    p = [[.5, .5, 0], [1, 0, 0], [1, 0, 0]]
+    n, t, path, margin, flag = oracle_lib.accept_tree_sample(
+        *one_node_tree(p, p, [-1, 0, 0], [0, 2, 2], [0, 0.5, 0.5], 0.75))
+    assert n[0] == 0 and t[0] == 1 and flag[0] == 1
+
+
+@pytest.mark.parametrize("k", [1, 3])
+def test_tree_sample_first_token_follows_the_target(oracle_lib, k):
+    """Root with k children drafted independently from q_0: the first token
+    emitted (an accepted child's token, else the residual draw) follows p_0."""
+    rng = np.random.default_rng(40 + k)
+    N, V = 60000, 6
+    zt = rng.standard_normal(V) * 1.5
+    p0 = synth.softmax_rows_fp32(zt)
+    q0 = synth.softmax_rows_fp32(zt + rng.standard_normal(V) * 1.0)
+    T = 1 + k
+    p = np.broadcast_to(np.concatenate([p0[None], np.tile(p0[None], (k, 1))]), (N, T, V)).copy()
+    q = np.broadcast_to(np.concatenate([q0[None], np.tile(q0[None], (k, 1))]), (N, T, V)).copy()
+    parent = np.tile(np.array([-1] + [0] * k, np.int32), (N, 1))
+    b = np.arange(N, dtype=np.uint64)
+    kk = np.arange(T, dtype=np.uint64)
+    ud = synth.philox_uniform(91 + k, b[:, None], kk[None, :], synth.STREAM_DRAFT)
+    tokens = np.zeros((N, T), np.int32)
+    for c in range(1, T):
+        tokens[:, c] = synth.draw_from_rows(np.broadcast_to(q0, (N, V)), ud[:, c])
+    u_acc = synth.philox_uniform(92 + k, b[:, None], kk[None, :], synth.STREAM_ACCEPT).astype(np.float32)
+    u_res = synth.philox_uniform(93 + k, b, np.zeros_like(b), synth.STREAM_RESAMPLE).astype(np.float32)
+    n, t, path, _, _ = oracle_lib.accept_tree_sample(p, q, tokens, parent, u_acc, u_res)
+    first = np.where(n >= 1, tokens[np.arange(N), np.maximum(path[:, 0], 0)], t)
+    counts = np.bincount(first, minlength=V)
+    assert stats.chisquare(counts, p0.astype(np.float64) / p0.sum() * N).pvalue > 1e-3
+    # and with more than one child, later children are accepted sometimes
+    if k > 1:
+        assert (path[:, 0] > 1).any()
+
+
+def test_tree_sample_rejects_invalid_trees(oracle_lib):
+    p = np.full((1, 3, 4), 0.25, np.float32)
+    good = np.array([[-1, 0, 1]], np.int32)
+    tokens = np.array([[0, 1, 2]], np.int32)
+    ua = np.zeros((1, 3), np.float32)
+    ur = np.zeros(1, np.float32)
+    oracle_lib.accept_tree_sample(p, p, tokens, good, ua, ur)
+    with pytest.raises(ValueError):
+        oracle_lib.accept_tree_sample(p, p, tokens, np.array([[-1, 2, 0]], np.int32), ua, ur)
+    with pytest.raises(ValueError):
+        oracle_lib.accept_tree_sample(p, p, np.array([[0, 1, 4]], np.int32), good, ua, ur)
