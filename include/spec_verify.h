@@ -202,9 +202,9 @@ spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_b
 /* ------------------------------------------------------------------------
  * Greedy acceptance.
  *
- * "Accept the longest prefix the target agrees with, then emit one more
- * target token" (LLM inference handbook, "How speculative decoding works";
- * co-design blog, "What is speculative decoding").  With
+ * The target keeps the longest draft prefix it agrees with and adds one
+ * token of its own (LLM inference handbook, "How speculative decoding
+ * works"; co-design blog, "What is speculative decoding").  With
  * t_i = argmax_v p[b][i][v] (lowest index on ties):
  *     n_accepted[b] = first i < D with draft[b][i] != t_i, else D
  *     token[b]      = t_{n_accepted[b]}
@@ -225,11 +225,11 @@ spec_status_t spec_accept_greedy(const float *p, const int32_t *draft, int B, in
 /* ------------------------------------------------------------------------
  * Tree verification.
  *
- * "The candidates are combined into a tree of possible continuations; the
- * target evaluates the whole tree in one forward pass with tree attention,
- * whose mask keeps causality inside each candidate branch; the longest
- * accepted candidate prefix moves on" (LLM inference handbook, "Speculative
- * decoding", Medusa; EAGLE-2's dynamic draft tree in the same section).
+ * Multi-head and feature-level drafters propose a tree of candidate
+ * continuations; the target scores the whole tree in one pass with a mask
+ * that keeps each branch causal, and the longest accepted candidate prefix
+ * is kept (LLM inference handbook, "Speculative decoding", Medusa; EAGLE-2's
+ * dynamic draft tree in the same section).
  *
  * A draft tree of sequence b has 1 + D nodes in topological order:
  *   tree_parent  device, int32 [B][1+D]; tree_parent[b][0] = -1 (the root:
@@ -272,6 +272,41 @@ spec_status_t spec_verify_tree_attention(const void *q_bf16, const void *k_pages
  * node k carrying draft k - 1 gives exactly spec_accept_greedy.
  * ---------------------------------------------------------------------- */
 spec_status_t spec_accept_tree_greedy(const float *p, const int32_t *tokens, const int32_t *parent,
+                                      int B, int D, int V, int32_t *n_accepted, int32_t *token,
+                                      int32_t *path, uint32_t *dev_status, void *stream);
+
+/* spec_accept_tree_sample: stochastic acceptance over a draft tree (the
+ * lossless rule of the stochastic acceptance below, generalised to
+ * siblings).  The children of node k (nodes whose parent is k, in
+ * increasing index) carry tokens drafted from q[b][k].  From the root, at
+ * the current node the working row r starts as p[b][node]; a child with
+ * token x is accepted iff u_acc[b][child] * q[b][node][x] < r(x), and the
+ * walk moves to it; otherwise r becomes max(0, r - q[b][node]) divided by
+ * its sum (left as it is, with SPEC_DEV_INFO_ZERO_RESIDUAL, when that sum is
+ * 0) and the next child is tried.  When no child is accepted, or the node
+ * has none, the token is the smallest v with sum_{w <= v} r(w) > u_res[b] *
+ * sum_w r(w).  A chain whose node k carries draft k - 1 is
+ * spec_accept_sample.
+ *   p, q       device, fp32 [B][1+D][V]; q[b][k] is the draft distribution
+ *              node k's children were drawn from (rows of leaves are not
+ *              read).  Probabilities in [0, 1].
+ *   tokens     device, int32 [B][1+D]; tokens[b][0] is not read.
+ *   parent     device, int32 [B][1+D], as for tree attention.
+ *   u_acc      device, fp32 [B][1+D] in [0, 1): the uniform of node k's
+ *              test (u_acc[b][0] is not read).
+ *   u_res      device, fp32 [B] in [0, 1): the uniform of the final draw.
+ *   n_accepted, token, path  as for spec_accept_tree_greedy.
+ * Arithmetic: the row after j rejections is kept unnormalised (R_j =
+ * max(0, R_(j-1) - S_(j-1) q) with S_0 = 1 and S_j the sum of R_j), its
+ * elements in fp32 and its sums exact in 2^-61 fixed point; a test after j
+ * rejections is u q(x) S_j < R_j(x) in fp64.  One CTA per sequence; each
+ * rejection and the final draw read the node's p and q rows once.
+ * Supported: D <= 63, V <= 2^22.  A malformed tree (SPEC_DEV_ERR_TREE) or a
+ * token outside [0, V) (SPEC_DEV_ERR_TOKEN_ID) makes the walk stop at the
+ * root; uniforms outside [0, 1) are clamped (SPEC_DEV_ERR_UNIFORM).
+ * ---------------------------------------------------------------------- */
+spec_status_t spec_accept_tree_sample(const float *p, const float *q, const int32_t *tokens,
+                                      const int32_t *parent, const float *u_acc, const float *u_res,
                                       int B, int D, int V, int32_t *n_accepted, int32_t *token,
                                       int32_t *path, uint32_t *dev_status, void *stream);
 
@@ -475,11 +510,11 @@ spec_status_t spec_selftest_bounded_wait(uint64_t wait_limit_ns, uint64_t arrive
 /* ------------------------------------------------------------------------
  * Adaptive draft length (host only; no counterpart kernels).
  *
- * "After each verification round, keep an exponential moving average of
- * the accept length and switch between a small set of predefined
- * speculation lengths (default [1, 3, 7]), each with its own pre-captured
- * CUDA graph" (LLM inference handbook, "Adaptive speculative decoding",
- * SGLang).  Rule (the pages leave it open): the next round uses the
+ * SGLang's controller tracks an exponential moving average of the accept
+ * length after every round and switches among a few fixed draft lengths
+ * (by default 1, 3 and 7), each with a CUDA graph captured in advance (LLM
+ * inference handbook, "Adaptive speculative decoding").  Rule (the pages
+ * leave it open): the next round uses the
  * smallest tier D >= EMA(AL), AL = n_accepted + 1, else the largest tier;
  * EMA_1 = mean AL of the first round, EMA_r = beta * EMA_(r-1) +
  * (1 - beta) * mean AL.

@@ -317,12 +317,11 @@ int oracle_accept_sample(const float *p, const float *q, const int32_t *draft,
 /* ------------------------------------------------------------------------
  * Tree verification (Medusa / EAGLE-2 style draft trees).
  *
- * "The candidates ... are combined into a tree of possible continuations;
- * the target model evaluates the whole tree in one forward pass with tree
- * attention, whose attention mask keeps causality inside each candidate
- * branch; the longest accepted candidate prefix moves on to the next
- * decoding step" (LLM inference handbook, "Speculative decoding", section
- * on Medusa; EAGLE-2's dynamic draft tree in the same section).
+ * Candidate continuations form a tree that the target scores in one pass,
+ * with an attention mask keeping every branch causal; the longest accepted
+ * candidate prefix is carried into the next step (LLM inference handbook,
+ * "Speculative decoding", section on Medusa; EAGLE-2's dynamic draft tree
+ * in the same section).
  *
  * The tree of sequence b has T = 1 + D nodes in topological order:
  * parent[b][0] = -1 (node 0 is the last accepted token, the root) and
@@ -590,12 +589,13 @@ int oracle_accept_tree_sample(const float *p, const float *q, const int32_t *tok
 /* ------------------------------------------------------------------------
  * Acceptance from logits (the fused form of the stochastic acceptance).
  *
- * "Accept x with probability min(1, p(x)/q(x)) ..." (llm-digest,
- * "Mechanism") with p = softmax(target logits / T), q = softmax(draft
- * logits / T), and the uniforms drawn by Philox4x32-10 from a seed.
+ * The acceptance of the llm-digest page ("Mechanism": x is kept with
+ * probability min(1, p(x)/q(x))) with p = softmax(target logits / T),
+ * q = softmax(draft logits / T), and the uniforms drawn by Philox4x32-10
+ * from a seed.
  *  R9  one temperature T > 0 for both models.
- *  R10 the target "produces next-token probabilities" (llm-digest,
- *      "Mechanism"): p_v = exp((z_v - m) / T) / sum_w exp((z_w - m) / T),
+ *  R10 the target turns its logits into next-token probabilities
+ *      (llm-digest, "Mechanism"): p_v = exp((z_v - m) / T) / sum_w exp((z_w - m) / T),
  *      m = max_v z_v, all in fp64, then rounded to the nearest fp32 -- the
  *      same fp32 probability rows the probability form of the acceptance
  *      takes (the batched-acceptance workload's "fp32 target probs from

@@ -20,7 +20,7 @@ __all__ = [
     "SpecError", "library", "library_path", "verify_attention", "verify_gemm",
     "accept_greedy", "accept_sample", "accept_sample_workspace_size", "attention_workspace_size",
     "gemm_workspace_size", "gemm_plan", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
-    "verify_tree_attention", "tree_attention_workspace_size", "accept_tree_greedy",
+    "verify_tree_attention", "tree_attention_workspace_size", "accept_tree_greedy", "accept_tree_sample",
     "AdaptiveDraftLength", "accept_sample_logits", "accept_sample_logits_workspace_size",
     "accept_adasd", "accept_adasd_workspace_size", "selftest_bounded_wait",
 ]
@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "spec_accept_greedy", "spec_accept_sample", "spec_verify_attention_plan",
     "spec_verify_attention_noalloc", "spec_accept_sample_workspace_size", "spec_verify_gemm_plan",
     "spec_verify_tree_attention_workspace_size", "spec_verify_tree_attention",
-    "spec_accept_tree_greedy", "spec_adaptive_init", "spec_adaptive_update", "spec_adaptive_draft_len",
+    "spec_accept_tree_greedy", "spec_accept_tree_sample", "spec_adaptive_init", "spec_adaptive_update", "spec_adaptive_draft_len",
     "spec_accept_sample_logits_workspace_size", "spec_accept_sample_logits",
     "spec_accept_adasd_workspace_size", "spec_accept_adasd", "spec_selftest_bounded_wait",
 )
@@ -102,6 +102,8 @@ def library():
             lib.spec_verify_tree_attention.restype = I
             lib.spec_accept_tree_greedy.argtypes = [P, P, P, I, I, I, P, P, P, P, P]
             lib.spec_accept_tree_greedy.restype = I
+            lib.spec_accept_tree_sample.argtypes = [P, P, P, P, P, P, I, I, I, P, P, P, P, P]
+            lib.spec_accept_tree_sample.restype = I
             lib.spec_adaptive_init.argtypes = [P, P, I, F]
             lib.spec_adaptive_init.restype = I
             lib.spec_adaptive_update.argtypes = [P, P, I]
@@ -331,6 +333,30 @@ def accept_tree_greedy(p, tokens, tree_parent, n_accepted=None, token=None, path
         _dev(n_accepted, "n_accepted", torch.int32), _dev(token, "token", torch.int32),
         _dev(path, "path", torch.int32), _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
     _check(st, "spec_accept_tree_greedy")
+    return n_accepted, token, path[:, :D1 - 1]
+
+
+def accept_tree_sample(p, q, tokens, tree_parent, u_acc, u_res, n_accepted=None, token=None, path=None,
+                       dev_status=None, stream=None):
+    """Stochastic tree acceptance; p, q [B, 1+D, V] fp32 (q row k: the draft
+    distribution of node k's children), tokens / tree_parent int32 [B, 1+D],
+    u_acc fp32 [B, 1+D], u_res fp32 [B].  Returns (n_accepted, token,
+    path [B, D])."""
+    import torch
+    B, D1, V = p.shape
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=p.device)
+    if token is None:
+        token = torch.empty(B, dtype=torch.int32, device=p.device)
+    if path is None:
+        path = torch.empty((B, max(D1 - 1, 1)), dtype=torch.int32, device=p.device)
+    st = library().spec_accept_tree_sample(
+        _dev(p, "p", torch.float32), _dev(q, "q", torch.float32), _dev(tokens, "tokens", torch.int32),
+        _dev(tree_parent, "tree_parent", torch.int32), _dev(u_acc, "u_acc", torch.float32),
+        _dev(u_res, "u_res", torch.float32), B, D1 - 1, V,
+        _dev(n_accepted, "n_accepted", torch.int32), _dev(token, "token", torch.int32),
+        _dev(path, "path", torch.int32), _dev(dev_status, "dev_status", allow_none=True), _stream(stream))
+    _check(st, "spec_accept_tree_sample")
     return n_accepted, token, path[:, :D1 - 1]
 
 

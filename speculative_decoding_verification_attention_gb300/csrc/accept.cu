@@ -1,7 +1,7 @@
 // Batched accept/reject kernels for the verification step.
 //
-// Greedy: "accept the longest agreeing prefix, then emit one more target
-// token" (LLM inference handbook, "How speculative decoding works").
+// Greedy: keep the longest draft prefix the target agrees with and add one
+// target token (LLM inference handbook, "How speculative decoding works").
 // Stochastic: accept x with probability min(1, p(x)/q(x)); at the first
 // rejection resample from max(0, p - q) renormalised (llm-digest,
 // "Mechanism" and "Math intuition").
@@ -1558,6 +1558,226 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) logits_rowstat
     if (CS > 1) cluster_sync_all();
 }
 
+// ------------------------------------------------------- stochastic tree
+// Stochastic acceptance over a draft tree: the children of node k (nodes
+// whose parent is k, in increasing index) carry tokens drafted from
+// q[b][k].  At the current node the working row starts as p; a child with
+// token x is accepted iff u * q(x) < r(x), and after a rejection the row
+// becomes max(0, r - q) renormalised, before the next sibling is tried;
+// when no child is accepted the token is drawn from the row.  A chain is
+// the stochastic acceptance above (and the rule is lossless for siblings
+// drafted independently from q).
+// One CTA per sequence.  The row is kept unnormalised: R_0 = p and R_j =
+// max(0, R_{j-1} - s_{j-1} q) with s_0 = 1 and s_j = S_j = sum_v R_j(v), so
+// r_j = R_j / S_j; each R_j(v) is recomputed from p(v), q(v) and the s's in
+// fp32 (the same function for one element and for a whole pass), and each
+// S_j is the exact sum of the elements' 2^-61 fixed-point masses.  A test
+// after j rejections is u q(x) S_j < R_j(x) in fp64.  An empty residual
+// (S = 0) leaves the row as it was and is reported.
+constexpr int kTSThreads = 512;
+constexpr int kTSWarps = kTSThreads / 32;
+constexpr int kTSGroup = 4 * kStep;   // 512 elements: 4 steps of 128
+
+__device__ __forceinline__ float tree_row_value(float pv, float qv, const float *s, int j)
+{
+    float r = pv;
+    for (int i = 0; i < j; ++i) r = fmaxf(__fsub_rn(r, __fmul_rn(s[i], qv)), 0.0f);
+    return r;
+}
+
+// Exact sum over the row of the masses of R_j (every thread gets it).
+__device__ unsigned long long tree_row_mass(const float *prow, const float *qrow, const float *s, int j, int V,
+                                            bool vec4, unsigned long long *s_warp, unsigned long long *s_total)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned long long m = 0;
+    for (int64_t e = static_cast<int64_t>(tid) * 4; e < V; e += kTSThreads * 4) {
+        const float4 xp = load4(prow, e, V, vec4, 0.0f);
+        const float4 xq = j > 0 ? load4(qrow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        m += fix61(tree_row_value(xp.x, xq.x, s, j)) + fix61(tree_row_value(xp.y, xq.y, s, j)) +
+             fix61(tree_row_value(xp.z, xq.z, s, j)) + fix61(tree_row_value(xp.w, xq.w, s, j));
+    }
+    m = warp_sum_u64(m);
+    if (lane == 0) s_warp[warp] = m;
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long t = 0;
+        for (int w = 0; w < kTSWarps; ++w) t += s_warp[w];
+        *s_total = t;
+    }
+    __syncthreads();
+    const unsigned long long t = *s_total;
+    __syncthreads();   // s_total and s_warp may be rewritten by the next call
+    return t;
+}
+
+__global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
+    const float *__restrict__ p, const float *__restrict__ q, const int32_t *__restrict__ tokens,
+    const int32_t *__restrict__ parent, const float *__restrict__ u_acc, const float *__restrict__ u_res, int D,
+    int V, int32_t *__restrict__ n_accepted, int32_t *__restrict__ token, int32_t *__restrict__ path,
+    uint32_t *dev_status, bool vec4)
+{
+    extern __shared__ unsigned long long s_gtot[];   // one total per 512-element group
+    __shared__ int32_t s_par[kMaxDraft + 1], s_tok[kMaxDraft + 1];
+    __shared__ float s_s[kMaxDraft + 1];
+    __shared__ unsigned long long s_warp[kTSWarps], s_total;
+    __shared__ int s_bad;
+    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = 1 + D;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    for (int k = tid; k < T; k += kTSThreads) {
+        const int pa = parent[static_cast<int64_t>(b) * T + k];
+        const int tk = tokens[static_cast<int64_t>(b) * T + k];
+        s_par[k] = pa;
+        s_tok[k] = tk;
+        if (k == 0 ? pa != -1 : (pa < 0 || pa >= k)) atomicOr(&s_bad, 1);
+        if (k > 0 && (tk < 0 || tk >= V)) atomicOr(&s_bad, 2);
+    }
+    __syncthreads();
+    const int bad = s_bad;
+    // a malformed tree (or a token out of range) is walked as a lone root
+    if (bad && tid == 0) report(dev_status, (bad & 1) ? SPEC_DEV_ERR_TREE : SPEC_DEV_ERR_TOKEN_ID);
+    if (path && tid < D) path[static_cast<int64_t>(b) * D + tid] = -1;
+
+    int cur = 0, depth = 0, j = 0;
+    unsigned long long S = 0;   // S_j (j >= 1)
+    const float *prow = p, *qrow = q;
+    for (;;) {
+        prow = p + (static_cast<int64_t>(b) * T + cur) * V;
+        qrow = q + (static_cast<int64_t>(b) * T + cur) * V;
+        j = 0;
+        if (tid == 0) s_s[0] = 1.0f;
+        __syncthreads();
+        int next = -1;
+        for (int c = cur + 1; c < T && !bad; ++c) {
+            if (s_par[c] != cur) continue;
+            const int x = s_tok[c];
+            float u = u_acc[static_cast<int64_t>(b) * T + c];
+            if (!(u >= 0.0f && u < 1.0f)) {
+                if (tid == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
+                u = (u >= 1.0f) ? 0x1.fffffep-1f : 0.0f;
+            }
+            const float px = prow[x], qx = qrow[x];
+            bool acc;
+            if (j == 0) {
+                acc = static_cast<double>(u) * static_cast<double>(qx) < static_cast<double>(px);
+            } else {
+                const float rx = tree_row_value(px, qx, s_s, j);
+                acc = static_cast<double>(u) * static_cast<double>(qx) * (static_cast<double>(S) * 0x1p-61) <
+                      static_cast<double>(rx);
+            }
+            if (acc) {
+                next = c;
+                break;
+            }
+            const unsigned long long Sn = tree_row_mass(prow, qrow, s_s, j + 1, V, vec4, s_warp, &s_total);
+            if (Sn == 0) {
+                if (tid == 0) report(dev_status, SPEC_DEV_INFO_ZERO_RESIDUAL);
+            } else {
+                if (tid == 0) s_s[j + 1] = static_cast<float>(static_cast<double>(Sn) * 0x1p-61);
+                __syncthreads();
+                ++j;
+                S = Sn;
+            }
+        }
+        if (next < 0) break;
+        if (path && tid == 0) path[static_cast<int64_t>(b) * D + depth] = next;
+        ++depth;
+        cur = next;
+    }
+
+    // the token: inverse CDF of R_j over the row with u_res
+    float u = u_res[b];
+    if (!(u >= 0.0f && u < 1.0f)) {
+        if (tid == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
+        u = (u >= 1.0f) ? 0x1.fffffep-1f : 0.0f;
+    }
+    const int ngroups = (V + kTSGroup - 1) / kTSGroup;
+    for (int g = warp; g < ngroups; g += kTSWarps) {
+        unsigned long long m = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t e = static_cast<int64_t>(g) * kTSGroup + k * kStep + lane * 4;
+            if (e < V) {
+                const float4 xp = load4(prow, e, V, vec4, 0.0f);
+                const float4 xq = j > 0 ? load4(qrow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+                m += fix61(tree_row_value(xp.x, xq.x, s_s, j)) + fix61(tree_row_value(xp.y, xq.y, s_s, j)) +
+                     fix61(tree_row_value(xp.z, xq.z, s_s, j)) + fix61(tree_row_value(xp.w, xq.w, s_s, j));
+            }
+        }
+        m = warp_sum_u64(m);
+        if (lane == 0) s_gtot[g] = m;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    unsigned long long z = 0;
+    for (int g = lane; g < ngroups; g += 32) z += s_gtot[g];
+    const unsigned long long Z = warp_sum_u64(z);
+    int tok = 0;
+    if (Z == 0) {
+        if (lane == 0) report(dev_status, SPEC_DEV_ERR_ZERO_MASS);
+    } else {
+        const unsigned long long Tt = scaled_threshold(u, Z);
+        // the group: smallest g with prefix(g) <= Tt < prefix(g) + mass(g)
+        int found = -1;
+        unsigned long long run_g = 0, base = 0;
+        for (int g0 = 0; g0 < ngroups && found < 0; g0 += 32) {
+            const int g = g0 + lane;
+            const unsigned long long v = g < ngroups ? s_gtot[g] : 0ull;
+            const unsigned long long incl = warp_incl_scan_u64(v, lane);
+            const unsigned long long run = base + incl - v;
+            const unsigned hit = __ballot_sync(0xffffffffu, g < ngroups && v > 0 && run <= Tt && Tt < run + v);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                found = g0 + l;
+                run_g = __shfl_sync(0xffffffffu, run, l);
+            }
+            base += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (found >= 0) {
+            // the element: walk the group's 512 elements, 128 at a time
+            unsigned long long run = run_g;
+            for (int k = 0; k < 4 && found >= 0; ++k) {
+                const int64_t e = static_cast<int64_t>(found) * kTSGroup + k * kStep + lane * 4;
+                float4 xp = make_float4(0.f, 0.f, 0.f, 0.f), xq = xp;
+                if (e < V) {
+                    xp = load4(prow, e, V, vec4, 0.0f);
+                    if (j > 0) xq = load4(qrow, e, V, vec4, 0.0f);
+                }
+                const unsigned long long m0 = e < V ? fix61(tree_row_value(xp.x, xq.x, s_s, j)) : 0ull;
+                const unsigned long long m1 = e < V ? fix61(tree_row_value(xp.y, xq.y, s_s, j)) : 0ull;
+                const unsigned long long m2 = e < V ? fix61(tree_row_value(xp.z, xq.z, s_s, j)) : 0ull;
+                const unsigned long long m3 = e < V ? fix61(tree_row_value(xp.w, xq.w, s_s, j)) : 0ull;
+                const unsigned long long ls = m0 + m1 + m2 + m3;
+                const unsigned long long incl = warp_incl_scan_u64(ls, lane);
+                const unsigned hit = __ballot_sync(0xffffffffu, run + incl > Tt);
+                if (hit) {
+                    const int l = __ffs(hit) - 1;
+                    if (lane == l) {
+                        unsigned long long c0 = run + incl - ls;
+                        const unsigned long long mm[4] = {m0, m1, m2, m3};
+                        int k4 = 3;
+                        for (int i = 0; i < 4; ++i) {
+                            c0 += mm[i];
+                            if (c0 > Tt) { k4 = i; break; }
+                        }
+                        tok = static_cast<int>(e) + k4;
+                    }
+                    tok = __shfl_sync(0xffffffffu, tok, l);
+                    found = -1;   // done
+                } else {
+                    run += __shfl_sync(0xffffffffu, incl, 31);
+                }
+            }
+        }
+    }
+    if (lane == 0) {
+        n_accepted[b] = depth;
+        token[b] = tok;
+    }
+}
+
 }  // namespace
 
 template <typename Kernel, typename... Args>
@@ -1647,6 +1867,25 @@ cudaError_t launch_accept_tree_greedy(const float *p, const int32_t *tokens, con
                                       uint32_t *dev_status, cudaStream_t st)
 {
     return launch_greedy<true>(p, tokens, parent, B, D, V, n_acc, token, path, dev_status, st);
+}
+
+cudaError_t launch_accept_tree_sample(const float *p, const float *q, const int32_t *tokens, const int32_t *parent,
+                                      const float *u_acc, const float *u_res, int B, int D, int V,
+                                      int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
+                                      cudaStream_t st)
+{
+    const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
+                      (reinterpret_cast<uintptr_t>(q) % 16 == 0);
+    const uint32_t smem = static_cast<uint32_t>((V + kTSGroup - 1) / kTSGroup) * 8u;
+    if (smem > 48u * 1024u) {
+        const cudaError_t e = cudaFuncSetAttribute(accept_tree_sample_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    accept_tree_sample_kernel<<<B, kTSThreads, smem, st>>>(p, q, tokens, parent, u_acc, u_res, D, V, n_acc, token,
+                                                           path, dev_status, vec4);
+    return cudaGetLastError();
 }
 
 namespace {

@@ -1,11 +1,10 @@
 // Adaptive draft length: the serving-side controller of the D-sweep.
 //
-// "After each verification round, measure how many draft tokens were
-// accepted and keep an exponential moving average (EMA) of the accept
-// length; switch between a small set of predefined speculation lengths
-// (by default [1, 3, 7]); every tier has its own pre-captured CUDA graph,
-// so switching is cheap" (LLM inference handbook, "Adaptive speculative
-// decoding", SGLang's built-in mechanism).  The pages leave the switching
+// SGLang's controller keeps an exponential moving average (EMA) of the
+// accept length over verification rounds and switches among a few fixed
+// draft lengths (1, 3 and 7 by default), each with a CUDA graph captured in
+// advance, so that a switch costs next to nothing (LLM inference handbook,
+// "Adaptive speculative decoding").  The pages leave the switching
 // rule open; the reading taken here: the next round uses the smallest tier
 // whose draft length is at least the EMA of the accept length AL =
 // n_accepted + 1 (a tier D can show AL up to D + 1, so a saturated tier

@@ -75,6 +75,24 @@ spec_status_t spec_accept_tree_greedy(const float *p, const int32_t *tokens, con
                                                dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+spec_status_t spec_accept_tree_sample(const float *p, const float *q, const int32_t *tokens,
+                                      const int32_t *parent, const float *u_acc, const float *u_res, int B,
+                                      int D, int V, int32_t *n_accepted, int32_t *token, int32_t *path,
+                                      uint32_t *dev_status, void *stream)
+{
+    if (B < 0 || D < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+    if (D > kMaxDraft || V > (1 << 22)) return SPEC_ERR_UNSUPPORTED;
+    if (B == 0) return SPEC_OK;
+    if (!p || !q || !tokens || !parent || !u_acc || !u_res || !n_accepted || !token)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned(p, 4) || !aligned(q, 4) || !aligned(tokens, 4) || !aligned(parent, 4) || !aligned(u_acc, 4) ||
+        !aligned(u_res, 4) || !aligned(n_accepted, 4) || !aligned(token, 4) || (path && !aligned(path, 4)))
+        return SPEC_ERR_INVALID_ARG;
+    if (B > 0x7fffffff / 2) return SPEC_ERR_UNSUPPORTED;
+    return from_cuda(launch_accept_tree_sample(p, q, tokens, parent, u_acc, u_res, B, D, V, n_accepted, token, path,
+                                               dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 size_t spec_accept_sample_workspace_size(int B, int V)
 {
     if (B < 0 || V < 1 || V > (1 << 26)) return 0;

@@ -16,6 +16,11 @@ cudaError_t launch_accept_tree_greedy(const float *p, const int32_t *tokens, con
                                       int D, int V, int32_t *n_acc, int32_t *token, int32_t *path,
                                       uint32_t *dev_status, cudaStream_t st);
 
+cudaError_t launch_accept_tree_sample(const float *p, const float *q, const int32_t *tokens, const int32_t *parent,
+                                      const float *u_acc, const float *u_res, int B, int D, int V,
+                                      int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
+                                      cudaStream_t st);
+
 size_t accept_sample_workspace_bytes(int B, int V);
 
 cudaError_t launch_accept_sample(const float *p, const float *q, const int32_t *draft,

@@ -110,6 +110,16 @@ def test_tree_entry_points_reject_bad_arguments(lib):
     assert g(FAKE, FAKE, FAKE, 2, 64, 10, FAKE, FAKE, None, None, None) == UNSUPPORTED
     assert g(FAKE, FAKE, FAKE, 2, 3, 0, FAKE, FAKE, None, None, None) == INVALID
     assert g(None, None, None, 0, 3, 10, None, None, None, None, None) == 0
+    h = lib.spec_accept_tree_sample
+    args = lambda q=FAKE, ua=FAKE, D=3, V=10, B=2: (FAKE, q, FAKE, FAKE, ua, FAKE, B, D, V, FAKE, FAKE, None,
+                                                    None, None)
+    assert h(*args(q=None)) == INVALID                      # the draft rows are needed
+    assert h(*args(ua=None)) == INVALID
+    assert h(*args(ua=P(0x7F0000001002))) == INVALID        # misaligned uniforms
+    assert h(*args(D=64)) == UNSUPPORTED
+    assert h(*args(V=(1 << 22) + 1)) == UNSUPPORTED
+    assert h(*args(V=0)) == INVALID
+    assert h(None, None, None, None, None, None, 0, 3, 10, None, None, None, None, None) == 0
 
 
 def test_logits_acceptance_rejects_bad_arguments(lib):
