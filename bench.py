@@ -738,6 +738,45 @@ def run_cases(args, groups, dev, sv, flush, step=None):
                                   nacc, int(np.sum(nacc + 1)) * Vt * 4))
         del pt, tok, par
         torch.cuda.empty_cache()
+        # stochastic tree acceptance on the same tree shape: a target and a
+        # draft row per node (alpha ~ 0.6), each node's token drawn from the
+        # draft row of its parent
+        pt, qt = device_probs(Bt, D + 1, Vt, sigma, 78, dev)
+        pt = pt[:, :D + 1].contiguous()
+        bidx = torch.arange(Bt, device=dev)
+        par_d = torch.from_numpy(par_h).to(dev).long()
+        qsel = torch.stack([qt[bidx, par_d[:, k]] for k in range(1, D + 1)], 1)
+        ds, _ = device_drafts(qsel, 79)
+        del qsel
+        tok = torch.zeros((Bt, D + 1), dtype=torch.int32, device=dev)
+        tok[:, 1:] = ds
+        ua, ur = synth.acceptance_uniforms(80, Bt, D + 1)
+        ua, ur = torch.from_numpy(ua).to(dev), torch.from_numpy(ur).to(dev)
+        par = torch.from_numpy(par_h).to(dev)
+        ms_s = time_launches(lambda: sv.accept_tree_sample(pt, qt, tok, par, ua, ur, na, tk, path), W, S, flush)
+        nacc = na.cpu().numpy().astype(np.int64)
+        path_h = path.cpu().numpy()
+        # rows the rule reads: one pass over the node's p and q rows per
+        # rejected child, and the final draw over p (and q after a rejection)
+        kids = [[c for c in range(1, D + 1) if par_h[b, c] == v] for b in range(Bt) for v in range(D + 1)]
+        passes = np.zeros(Bt, np.int64)
+        last_rej = np.zeros(Bt, np.int64)
+        for b in range(Bt):
+            node = 0
+            for d in range(int(nacc[b]) + 1):
+                ch = kids[b * (D + 1) + node]
+                if d < nacc[b]:
+                    nxt = int(path_h[b, d])
+                    passes[b] += sum(1 for c in ch if c < nxt)
+                    node = nxt
+                else:
+                    passes[b] += len(ch)
+                    last_rej[b] = len(ch)
+        by = int(np.sum(passes * 2 + np.where(last_rej > 0, 2, 1))) * Vt * 4
+        recs.append(accept_record(f"tree accept sample B{Bt} D{D} V{Vt} wide tree alpha0.6", "accept_tree_sample",
+                                  ms_s, nacc, by, row_passes_per_sequence=float(passes.mean())))
+        del pt, qt, tok, par, ua, ur
+        torch.cuda.empty_cache()
 
     if "adaptive" in groups:
         recs.extend(adaptive_cases(args, dev, sv))

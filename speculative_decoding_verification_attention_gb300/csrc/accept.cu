@@ -1585,17 +1585,102 @@ __device__ __forceinline__ float tree_row_value(float pv, float qv, const float 
     return r;
 }
 
+// The same for a fixed count J with the s's in registers (identical
+// operations, so identical values).
+template <int J>
+__device__ __forceinline__ float tree_row_value_t(float pv, float qv, const float (&s)[4])
+{
+    float r = pv;
+#pragma unroll
+    for (int i = 0; i < J; ++i) r = fmaxf(__fsub_rn(r, __fmul_rn(s[i], qv)), 0.0f);
+    return r;
+}
+
+// This thread's part of the sum of R_J's masses over the row (J <= 3 from
+// registers, a larger J through the general form).
+template <int J>
+__device__ __forceinline__ unsigned long long tree_pass_part(const float *prow, const float *qrow, const float *s,
+                                                             int j, int V, bool vec4)
+{
+    float sr[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (i < J) sr[i] = s[i];
+    unsigned long long m = 0;
+    constexpr int kU = 4;   // float4 loads of p and q in flight per thread
+    for (int64_t e0 = static_cast<int64_t>(threadIdx.x) * 4; e0 < V; e0 += kTSThreads * 4 * kU) {
+        float4 xp[kU], xq[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int64_t e = e0 + static_cast<int64_t>(u) * kTSThreads * 4;
+            xp[u] = e < V ? load4(prow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xq[u] = (j > 0 && e < V) ? load4(qrow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (J >= 0) {
+                m += fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[u].x, xq[u].x, sr)) +
+                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[u].y, xq[u].y, sr)) +
+                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[u].z, xq[u].z, sr)) +
+                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[u].w, xq[u].w, sr));
+            } else {
+                m += fix61(tree_row_value(xp[u].x, xq[u].x, s, j)) + fix61(tree_row_value(xp[u].y, xq[u].y, s, j)) +
+                     fix61(tree_row_value(xp[u].z, xq[u].z, s, j)) + fix61(tree_row_value(xp[u].w, xq[u].w, s, j));
+            }
+        }
+    }
+    return m;
+}
+
+// Exact masses of R_J per 512-element group (warp w takes groups w, w +
+// kTSWarps, ...), into gtot.
+template <int J>
+__device__ __forceinline__ void tree_group_totals(const float *prow, const float *qrow, const float *s, int j,
+                                                  int V, bool vec4, unsigned long long *gtot, int ngroups)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float sr[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (i < J) sr[i] = s[i];
+    for (int g = warp; g < ngroups; g += kTSWarps) {
+        float4 xp[4], xq[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int64_t e = static_cast<int64_t>(g) * kTSGroup + k * kStep + lane * 4;
+            xp[k] = e < V ? load4(prow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xq[k] = (j > 0 && e < V) ? load4(qrow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        unsigned long long m = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (J >= 0) {
+                m += fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[k].x, xq[k].x, sr)) +
+                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[k].y, xq[k].y, sr)) +
+                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[k].z, xq[k].z, sr)) +
+                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[k].w, xq[k].w, sr));
+            } else {
+                m += fix61(tree_row_value(xp[k].x, xq[k].x, s, j)) + fix61(tree_row_value(xp[k].y, xq[k].y, s, j)) +
+                     fix61(tree_row_value(xp[k].z, xq[k].z, s, j)) + fix61(tree_row_value(xp[k].w, xq[k].w, s, j));
+            }
+        }
+        m = warp_sum_u64(m);
+        if (lane == 0) gtot[g] = m;
+    }
+}
+
 // Exact sum over the row of the masses of R_j (every thread gets it).
 __device__ unsigned long long tree_row_mass(const float *prow, const float *qrow, const float *s, int j, int V,
                                             bool vec4, unsigned long long *s_warp, unsigned long long *s_total)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    unsigned long long m = 0;
-    for (int64_t e = static_cast<int64_t>(tid) * 4; e < V; e += kTSThreads * 4) {
-        const float4 xp = load4(prow, e, V, vec4, 0.0f);
-        const float4 xq = j > 0 ? load4(qrow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
-        m += fix61(tree_row_value(xp.x, xq.x, s, j)) + fix61(tree_row_value(xp.y, xq.y, s, j)) +
-             fix61(tree_row_value(xp.z, xq.z, s, j)) + fix61(tree_row_value(xp.w, xq.w, s, j));
+    unsigned long long m;
+    switch (j) {   // uniform over the CTA
+    case 0: m = tree_pass_part<0>(prow, qrow, s, j, V, vec4); break;
+    case 1: m = tree_pass_part<1>(prow, qrow, s, j, V, vec4); break;
+    case 2: m = tree_pass_part<2>(prow, qrow, s, j, V, vec4); break;
+    case 3: m = tree_pass_part<3>(prow, qrow, s, j, V, vec4); break;
+    default: m = tree_pass_part<-1>(prow, qrow, s, j, V, vec4); break;
     }
     m = warp_sum_u64(m);
     if (lane == 0) s_warp[warp] = m;
@@ -1694,20 +1779,12 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
         u = (u >= 1.0f) ? 0x1.fffffep-1f : 0.0f;
     }
     const int ngroups = (V + kTSGroup - 1) / kTSGroup;
-    for (int g = warp; g < ngroups; g += kTSWarps) {
-        unsigned long long m = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int64_t e = static_cast<int64_t>(g) * kTSGroup + k * kStep + lane * 4;
-            if (e < V) {
-                const float4 xp = load4(prow, e, V, vec4, 0.0f);
-                const float4 xq = j > 0 ? load4(qrow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
-                m += fix61(tree_row_value(xp.x, xq.x, s_s, j)) + fix61(tree_row_value(xp.y, xq.y, s_s, j)) +
-                     fix61(tree_row_value(xp.z, xq.z, s_s, j)) + fix61(tree_row_value(xp.w, xq.w, s_s, j));
-            }
-        }
-        m = warp_sum_u64(m);
-        if (lane == 0) s_gtot[g] = m;
+    switch (j) {   // uniform over the CTA
+    case 0: tree_group_totals<0>(prow, qrow, s_s, j, V, vec4, s_gtot, ngroups); break;
+    case 1: tree_group_totals<1>(prow, qrow, s_s, j, V, vec4, s_gtot, ngroups); break;
+    case 2: tree_group_totals<2>(prow, qrow, s_s, j, V, vec4, s_gtot, ngroups); break;
+    case 3: tree_group_totals<3>(prow, qrow, s_s, j, V, vec4, s_gtot, ngroups); break;
+    default: tree_group_totals<-1>(prow, qrow, s_s, j, V, vec4, s_gtot, ngroups); break;
     }
     __syncthreads();
     if (warp != 0) return;
