@@ -1574,7 +1574,7 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) logits_rowstat
 // S_j is the exact sum of the elements' 2^-61 fixed-point masses.  A test
 // after j rejections is u q(x) S_j < R_j(x) in fp64.  An empty residual
 // (S = 0) leaves the row as it was and is reported.
-constexpr int kTSThreads = 512;
+constexpr int kTSThreads = 256;
 constexpr int kTSWarps = kTSThreads / 32;
 constexpr int kTSGroup = 4 * kStep;   // 512 elements: 4 steps of 128
 
@@ -1696,21 +1696,47 @@ __device__ unsigned long long tree_row_mass(const float *prow, const float *qrow
     return t;
 }
 
+// CS CTAs (a cluster) per sequence, CTA `rank` owning the vocabulary slice
+// [c0, c0 + n).  Every CTA takes the same decisions: the tests read the two
+// gathered values from global memory, and each row sum is the CTAs' exact
+// slice sums, sent to every CTA of the cluster by asynchronous shared-memory
+// stores that complete on the receiver's mbarrier and added in rank order.
+// The final draw exchanges the slice totals the same way; the CTA whose
+// prefix holds the threshold finds the token in its slice.
+template <int CS>
 __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
     const float *__restrict__ p, const float *__restrict__ q, const int32_t *__restrict__ tokens,
     const int32_t *__restrict__ parent, const float *__restrict__ u_acc, const float *__restrict__ u_res, int D,
     int V, int32_t *__restrict__ n_accepted, int32_t *__restrict__ token, int32_t *__restrict__ path,
     uint32_t *dev_status, bool vec4)
 {
-    extern __shared__ unsigned long long s_gtot[];   // one total per 512-element group
+    extern __shared__ unsigned long long s_gtot[];   // one total per 512-element group of the slice
     __shared__ int32_t s_par[kMaxDraft + 1], s_tok[kMaxDraft + 1];
     __shared__ float s_s[kMaxDraft + 1];
     __shared__ unsigned long long s_warp[kTSWarps], s_total;
-    __shared__ int s_bad;
-    const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    __shared__ __align__(8) unsigned long long s_x[2][CS];   // exchanged partials, per parity
+    __shared__ uint64_t s_xbar[2];
+    __shared__ int s_bad, s_abort;
+    if (cluster_ctas() != static_cast<uint32_t>(CS)) {   // uniform over the grid
+        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
+        return;
+    }
+    const int rank = CS > 1 ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
+    const int b = blockIdx.x / CS, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = 1 + D;
-    if (tid == 0) s_bad = 0;
+    const int64_t cta_len = ((static_cast<int64_t>(V) + CS - 1) / CS + 3) & ~int64_t(3);
+    const int64_t c0 = imin64(V, cta_len * rank);
+    const int n = static_cast<int>(imin64(V, c0 + cta_len) - c0);
+    volatile int *abort = reinterpret_cast<volatile int *>(&s_abort);
+    if (tid == 0) {
+        s_bad = 0;
+        s_abort = 0;
+        mbar_init(&s_xbar[0], 1);
+        mbar_init(&s_xbar[1], 1);
+        fence_mbar_init();
+    }
     __syncthreads();
+    if constexpr (CS > 1) cluster_arrive_release();   // waited for before the first send
     for (int k = tid; k < T; k += kTSThreads) {
         const int pa = parent[static_cast<int64_t>(b) * T + k];
         const int tk = tokens[static_cast<int64_t>(b) * T + k];
@@ -1722,8 +1748,30 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
     __syncthreads();
     const int bad = s_bad;
     // a malformed tree (or a token out of range) is walked as a lone root
-    if (bad && tid == 0) report(dev_status, (bad & 1) ? SPEC_DEV_ERR_TREE : SPEC_DEV_ERR_TOKEN_ID);
-    if (path && tid < D) path[static_cast<int64_t>(b) * D + tid] = -1;
+    if (bad && rank == 0 && tid == 0) report(dev_status, (bad & 1) ? SPEC_DEV_ERR_TREE : SPEC_DEV_ERR_TOKEN_ID);
+    if (path && rank == 0 && tid < D) path[static_cast<int64_t>(b) * D + tid] = -1;
+
+    // sum over the cluster of each CTA's value (identical in every CTA)
+    uint32_t nx = 0;    // exchanges so far
+    bool ok = true;
+    auto exchange = [&](unsigned long long mine) -> unsigned long long {
+        const int slot = static_cast<int>(nx & 1u);
+        if constexpr (CS > 1) {
+            if (tid == 0) mbar_arrive_expect_tx(&s_xbar[slot], CS * 8);
+            if (nx == 0) cluster_wait_acquire();   // every peer's barriers are initialised
+            if (tid < CS) st_async_peer(peer_smem(&s_x[slot][rank], tid), mine, peer_smem(&s_xbar[slot], tid));
+            if (ok) ok = mbar_wait(&s_xbar[slot], (nx >> 1) & 1u, abort, dev_status);
+            ok = __syncthreads_and(ok);
+        } else {
+            if (tid == 0) s_x[slot][0] = mine;
+            __syncthreads();
+        }
+        unsigned long long t = 0;
+#pragma unroll
+        for (int r = 0; r < CS; ++r) t += s_x[slot][r];
+        ++nx;
+        return t;
+    };
 
     int cur = 0, depth = 0, j = 0;
     unsigned long long S = 0;   // S_j (j >= 1)
@@ -1735,12 +1783,12 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
         if (tid == 0) s_s[0] = 1.0f;
         __syncthreads();
         int next = -1;
-        for (int c = cur + 1; c < T && !bad; ++c) {
+        for (int c = cur + 1; c < T && !bad && ok; ++c) {
             if (s_par[c] != cur) continue;
             const int x = s_tok[c];
             float u = u_acc[static_cast<int64_t>(b) * T + c];
             if (!(u >= 0.0f && u < 1.0f)) {
-                if (tid == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
+                if (rank == 0 && tid == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
                 u = (u >= 1.0f) ? 0x1.fffffep-1f : 0.0f;
             }
             const float px = prow[x], qx = qrow[x];
@@ -1756,9 +1804,10 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
                 next = c;
                 break;
             }
-            const unsigned long long Sn = tree_row_mass(prow, qrow, s_s, j + 1, V, vec4, s_warp, &s_total);
+            const unsigned long long Sn =
+                exchange(tree_row_mass(prow + c0, qrow + c0, s_s, j + 1, n, vec4, s_warp, &s_total));
             if (Sn == 0) {
-                if (tid == 0) report(dev_status, SPEC_DEV_INFO_ZERO_RESIDUAL);
+                if (rank == 0 && tid == 0) report(dev_status, SPEC_DEV_INFO_ZERO_RESIDUAL);
             } else {
                 if (tid == 0) s_s[j + 1] = static_cast<float>(static_cast<double>(Sn) * 0x1p-61);
                 __syncthreads();
@@ -1766,93 +1815,105 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
                 S = Sn;
             }
         }
-        if (next < 0) break;
-        if (path && tid == 0) path[static_cast<int64_t>(b) * D + depth] = next;
+        if (next < 0 || !ok) break;
+        if (path && rank == 0 && tid == 0) path[static_cast<int64_t>(b) * D + depth] = next;
         ++depth;
         cur = next;
     }
 
-    // the token: inverse CDF of R_j over the row with u_res
+    // the token: inverse CDF of R_j over the row with u_res; this CTA's
+    // slice holds the cumulative masses base .. base + total
     float u = u_res[b];
     if (!(u >= 0.0f && u < 1.0f)) {
-        if (tid == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
+        if (rank == 0 && tid == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
         u = (u >= 1.0f) ? 0x1.fffffep-1f : 0.0f;
     }
-    const int ngroups = (V + kTSGroup - 1) / kTSGroup;
-    switch (j) {   // uniform over the CTA
-    case 0: tree_group_totals<0>(prow, qrow, s_s, j, V, vec4, s_gtot, ngroups); break;
-    case 1: tree_group_totals<1>(prow, qrow, s_s, j, V, vec4, s_gtot, ngroups); break;
-    case 2: tree_group_totals<2>(prow, qrow, s_s, j, V, vec4, s_gtot, ngroups); break;
-    case 3: tree_group_totals<3>(prow, qrow, s_s, j, V, vec4, s_gtot, ngroups); break;
-    default: tree_group_totals<-1>(prow, qrow, s_s, j, V, vec4, s_gtot, ngroups); break;
+    const int ngroups = (n + kTSGroup - 1) / kTSGroup;
+    switch (j) {   // uniform over the cluster
+    case 0: tree_group_totals<0>(prow + c0, qrow + c0, s_s, j, n, vec4, s_gtot, ngroups); break;
+    case 1: tree_group_totals<1>(prow + c0, qrow + c0, s_s, j, n, vec4, s_gtot, ngroups); break;
+    case 2: tree_group_totals<2>(prow + c0, qrow + c0, s_s, j, n, vec4, s_gtot, ngroups); break;
+    case 3: tree_group_totals<3>(prow + c0, qrow + c0, s_s, j, n, vec4, s_gtot, ngroups); break;
+    default: tree_group_totals<-1>(prow + c0, qrow + c0, s_s, j, n, vec4, s_gtot, ngroups); break;
     }
     __syncthreads();
-    if (warp != 0) return;
-    unsigned long long z = 0;
-    for (int g = lane; g < ngroups; g += 32) z += s_gtot[g];
-    const unsigned long long Z = warp_sum_u64(z);
-    int tok = 0;
-    if (Z == 0) {
-        if (lane == 0) report(dev_status, SPEC_DEV_ERR_ZERO_MASS);
-    } else {
-        const unsigned long long Tt = scaled_threshold(u, Z);
+    if (warp == 0) {
+        unsigned long long z = 0;
+        for (int g = lane; g < ngroups; g += 32) z += s_gtot[g];
+        z = warp_sum_u64(z);
+        if (lane == 0) s_total = z;
+    }
+    __syncthreads();
+    const unsigned long long mine = s_total;
+    const unsigned long long Z = ok ? exchange(mine) : 0ull;
+    unsigned long long base = 0;
+    for (int r = 0; r < rank; ++r) base += s_x[(nx - 1) & 1u][r];
+    const unsigned long long Tt = Z ? scaled_threshold(u, Z) : 0ull;
+    const bool owner = Z != 0 && base <= Tt && Tt < base + mine;
+    if (ok && Z == 0 && rank == 0 && tid == 0) {
+        report(dev_status, SPEC_DEV_ERR_ZERO_MASS);
+        n_accepted[b] = depth;
+        token[b] = 0;
+    }
+    if (ok && owner && warp == 0) {
+        int tok = 0;
         // the group: smallest g with prefix(g) <= Tt < prefix(g) + mass(g)
         int found = -1;
-        unsigned long long run_g = 0, base = 0;
+        unsigned long long run_g = 0, gbase = base;
         for (int g0 = 0; g0 < ngroups && found < 0; g0 += 32) {
             const int g = g0 + lane;
             const unsigned long long v = g < ngroups ? s_gtot[g] : 0ull;
             const unsigned long long incl = warp_incl_scan_u64(v, lane);
-            const unsigned long long run = base + incl - v;
+            const unsigned long long run = gbase + incl - v;
             const unsigned hit = __ballot_sync(0xffffffffu, g < ngroups && v > 0 && run <= Tt && Tt < run + v);
             if (hit) {
                 const int l = __ffs(hit) - 1;
                 found = g0 + l;
                 run_g = __shfl_sync(0xffffffffu, run, l);
             }
-            base += __shfl_sync(0xffffffffu, incl, 31);
+            gbase += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (found >= 0) {
-            // the element: walk the group's 512 elements, 128 at a time
-            unsigned long long run = run_g;
-            for (int k = 0; k < 4 && found >= 0; ++k) {
-                const int64_t e = static_cast<int64_t>(found) * kTSGroup + k * kStep + lane * 4;
-                float4 xp = make_float4(0.f, 0.f, 0.f, 0.f), xq = xp;
-                if (e < V) {
-                    xp = load4(prow, e, V, vec4, 0.0f);
-                    if (j > 0) xq = load4(qrow, e, V, vec4, 0.0f);
-                }
-                const unsigned long long m0 = e < V ? fix61(tree_row_value(xp.x, xq.x, s_s, j)) : 0ull;
-                const unsigned long long m1 = e < V ? fix61(tree_row_value(xp.y, xq.y, s_s, j)) : 0ull;
-                const unsigned long long m2 = e < V ? fix61(tree_row_value(xp.z, xq.z, s_s, j)) : 0ull;
-                const unsigned long long m3 = e < V ? fix61(tree_row_value(xp.w, xq.w, s_s, j)) : 0ull;
-                const unsigned long long ls = m0 + m1 + m2 + m3;
-                const unsigned long long incl = warp_incl_scan_u64(ls, lane);
-                const unsigned hit = __ballot_sync(0xffffffffu, run + incl > Tt);
-                if (hit) {
-                    const int l = __ffs(hit) - 1;
-                    if (lane == l) {
-                        unsigned long long c0 = run + incl - ls;
-                        const unsigned long long mm[4] = {m0, m1, m2, m3};
-                        int k4 = 3;
-                        for (int i = 0; i < 4; ++i) {
-                            c0 += mm[i];
-                            if (c0 > Tt) { k4 = i; break; }
-                        }
-                        tok = static_cast<int>(e) + k4;
+        // the element: walk the group's 512 elements, 128 at a time
+        unsigned long long run = run_g;
+        for (int k = 0; k < 4 && found >= 0; ++k) {
+            const int64_t e = static_cast<int64_t>(found) * kTSGroup + k * kStep + lane * 4;
+            float4 xp = make_float4(0.f, 0.f, 0.f, 0.f), xq = xp;
+            if (e < n) {
+                xp = load4(prow + c0, e, n, vec4, 0.0f);
+                if (j > 0) xq = load4(qrow + c0, e, n, vec4, 0.0f);
+            }
+            const unsigned long long m0 = e < n ? fix61(tree_row_value(xp.x, xq.x, s_s, j)) : 0ull;
+            const unsigned long long m1 = e < n ? fix61(tree_row_value(xp.y, xq.y, s_s, j)) : 0ull;
+            const unsigned long long m2 = e < n ? fix61(tree_row_value(xp.z, xq.z, s_s, j)) : 0ull;
+            const unsigned long long m3 = e < n ? fix61(tree_row_value(xp.w, xq.w, s_s, j)) : 0ull;
+            const unsigned long long ls = m0 + m1 + m2 + m3;
+            const unsigned long long incl = warp_incl_scan_u64(ls, lane);
+            const unsigned hit = __ballot_sync(0xffffffffu, run + incl > Tt);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                if (lane == l) {
+                    unsigned long long cc = run + incl - ls;
+                    const unsigned long long mm[4] = {m0, m1, m2, m3};
+                    int k4 = 3;
+                    for (int i = 0; i < 4; ++i) {
+                        cc += mm[i];
+                        if (cc > Tt) { k4 = i; break; }
                     }
-                    tok = __shfl_sync(0xffffffffu, tok, l);
-                    found = -1;   // done
-                } else {
-                    run += __shfl_sync(0xffffffffu, incl, 31);
+                    tok = static_cast<int>(c0 + e) + k4;
                 }
+                tok = __shfl_sync(0xffffffffu, tok, l);
+                found = -1;   // done
+            } else {
+                run += __shfl_sync(0xffffffffu, incl, 31);
             }
         }
+        if (lane == 0) {
+            n_accepted[b] = depth;
+            token[b] = tok;
+        }
     }
-    if (lane == 0) {
-        n_accepted[b] = depth;
-        token[b] = tok;
-    }
+    // keep this CTA's shared memory alive until every peer is done with it
+    if constexpr (CS > 1) cg::this_cluster().sync();
 }
 
 }  // namespace
@@ -1946,23 +2007,53 @@ cudaError_t launch_accept_tree_greedy(const float *p, const int32_t *tokens, con
     return launch_greedy<true>(p, tokens, parent, B, D, V, n_acc, token, path, dev_status, st);
 }
 
+template <int CS>
+cudaError_t launch_tree_sample_cs(const float *p, const float *q, const int32_t *tokens, const int32_t *parent,
+                                  const float *u_acc, const float *u_res, int B, int D, int V, int32_t *n_acc,
+                                  int32_t *token, int32_t *path, uint32_t *dev_status, bool vec4, cudaStream_t st)
+{
+    const int64_t cta_len = ((static_cast<int64_t>(V) + CS - 1) / CS + 3) & ~int64_t(3);
+    const uint32_t smem = static_cast<uint32_t>((cta_len + kTSGroup - 1) / kTSGroup) * 8u;
+    if (smem > 48u * 1024u) {
+        const cudaError_t e = cudaFuncSetAttribute(accept_tree_sample_kernel<CS>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B) * CS);
+    cfg.blockDim = dim3(kTSThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, accept_tree_sample_kernel<CS>, p, q, tokens, parent, u_acc, u_res, D, V, n_acc,
+                              token, path, dev_status, vec4);
+}
+
 cudaError_t launch_accept_tree_sample(const float *p, const float *q, const int32_t *tokens, const int32_t *parent,
                                       const float *u_acc, const float *u_res, int B, int D, int V,
                                       int32_t *n_acc, int32_t *token, int32_t *path, uint32_t *dev_status,
                                       cudaStream_t st)
 {
+    // slices start on 16-byte boundaries when rows do (V % 4 == 0)
     const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
                       (reinterpret_cast<uintptr_t>(q) % 16 == 0);
-    const uint32_t smem = static_cast<uint32_t>((V + kTSGroup - 1) / kTSGroup) * 8u;
-    if (smem > 48u * 1024u) {
-        const cudaError_t e = cudaFuncSetAttribute(accept_tree_sample_kernel,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
+    switch (pick_cluster(V)) {
+    case 8: return launch_tree_sample_cs<8>(p, q, tokens, parent, u_acc, u_res, B, D, V, n_acc, token, path,
+                                            dev_status, vec4, st);
+    case 4: return launch_tree_sample_cs<4>(p, q, tokens, parent, u_acc, u_res, B, D, V, n_acc, token, path,
+                                            dev_status, vec4, st);
+    case 2: return launch_tree_sample_cs<2>(p, q, tokens, parent, u_acc, u_res, B, D, V, n_acc, token, path,
+                                            dev_status, vec4, st);
+    default: return launch_tree_sample_cs<1>(p, q, tokens, parent, u_acc, u_res, B, D, V, n_acc, token, path,
+                                             dev_status, vec4, st);
     }
-    accept_tree_sample_kernel<<<B, kTSThreads, smem, st>>>(p, q, tokens, parent, u_acc, u_res, D, V, n_acc, token,
-                                                           path, dev_status, vec4);
-    return cudaGetLastError();
 }
 
 namespace {

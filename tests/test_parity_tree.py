@@ -225,7 +225,8 @@ def check_tree_sample(sv, oracle_lib, inp):
 @pytest.mark.parametrize("B,D,V,kind,noise", [(64, 7, 3000, "wide", 0.5), (48, 15, 5000, "random", 0.3),
                                                (40, 9, 2048, "star", 0.8), (30, 6, 1001, "random", 0.5),
                                                (16, 0, 700, "chain", 0.5), (20, 63, 640, "random", 0.2),
-                                               (25, 5, 1, "star", 0.5)])
+                                               (25, 5, 1, "star", 0.5), (24, 7, 10000, "wide", 0.5),
+                                               (12, 5, 16383, "random", 0.4), (8, 3, 40000, "star", 0.6)])
 def test_tree_sample_small(sv, oracle_lib, B, D, V, kind, noise):
     inp = synth.tree_sample_inputs(100 + D + V, B, D, V, kind=kind, draft_noise=noise)
     n, _ = check_tree_sample(sv, oracle_lib, inp)
