@@ -757,7 +757,8 @@ def run_cases(args, groups, dev, sv, flush, step=None):
         nacc = na.cpu().numpy().astype(np.int64)
         path_h = path.cpu().numpy()
         # rows the rule reads: one pass over the node's p and q rows per
-        # rejected child, and the final draw over p (and q after a rejection)
+        # rejected child (the last one's pass also serves the draw), and a
+        # pass over p for a draw at a node without a rejection
         kids = [[c for c in range(1, D + 1) if par_h[b, c] == v] for b in range(Bt) for v in range(D + 1)]
         passes = np.zeros(Bt, np.int64)
         last_rej = np.zeros(Bt, np.int64)
@@ -772,7 +773,7 @@ def run_cases(args, groups, dev, sv, flush, step=None):
                 else:
                     passes[b] += len(ch)
                     last_rej[b] = len(ch)
-        by = int(np.sum(passes * 2 + np.where(last_rej > 0, 2, 1))) * Vt * 4
+        by = int(np.sum(passes * 2 + np.where(last_rej > 0, 0, 1))) * Vt * 4
         recs.append(accept_record(f"tree accept sample B{Bt} D{D} V{Vt} wide tree alpha0.6", "accept_tree_sample",
                                   ms_s, nacc, by, row_passes_per_sequence=float(passes.mean())))
         del pt, qt, tok, par, ua, ur

@@ -1596,42 +1596,6 @@ __device__ __forceinline__ float tree_row_value_t(float pv, float qv, const floa
     return r;
 }
 
-// This thread's part of the sum of R_J's masses over the row (J <= 3 from
-// registers, a larger J through the general form).
-template <int J>
-__device__ __forceinline__ unsigned long long tree_pass_part(const float *prow, const float *qrow, const float *s,
-                                                             int j, int V, bool vec4)
-{
-    float sr[4] = {1.0f, 1.0f, 1.0f, 1.0f};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        if (i < J) sr[i] = s[i];
-    unsigned long long m = 0;
-    constexpr int kU = 4;   // float4 loads of p and q in flight per thread
-    for (int64_t e0 = static_cast<int64_t>(threadIdx.x) * 4; e0 < V; e0 += kTSThreads * 4 * kU) {
-        float4 xp[kU], xq[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int64_t e = e0 + static_cast<int64_t>(u) * kTSThreads * 4;
-            xp[u] = e < V ? load4(prow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
-            xq[u] = (j > 0 && e < V) ? load4(qrow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            if (J >= 0) {
-                m += fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[u].x, xq[u].x, sr)) +
-                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[u].y, xq[u].y, sr)) +
-                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[u].z, xq[u].z, sr)) +
-                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[u].w, xq[u].w, sr));
-            } else {
-                m += fix61(tree_row_value(xp[u].x, xq[u].x, s, j)) + fix61(tree_row_value(xp[u].y, xq[u].y, s, j)) +
-                     fix61(tree_row_value(xp[u].z, xq[u].z, s, j)) + fix61(tree_row_value(xp[u].w, xq[u].w, s, j));
-            }
-        }
-    }
-    return m;
-}
-
 // Exact masses of R_J per 512-element group (warp w takes groups w, w +
 // kTSWarps, ...), into gtot.
 template <int J>
@@ -1669,33 +1633,6 @@ __device__ __forceinline__ void tree_group_totals(const float *prow, const float
     }
 }
 
-// Exact sum over the row of the masses of R_j (every thread gets it).
-__device__ unsigned long long tree_row_mass(const float *prow, const float *qrow, const float *s, int j, int V,
-                                            bool vec4, unsigned long long *s_warp, unsigned long long *s_total)
-{
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    unsigned long long m;
-    switch (j) {   // uniform over the CTA
-    case 0: m = tree_pass_part<0>(prow, qrow, s, j, V, vec4); break;
-    case 1: m = tree_pass_part<1>(prow, qrow, s, j, V, vec4); break;
-    case 2: m = tree_pass_part<2>(prow, qrow, s, j, V, vec4); break;
-    case 3: m = tree_pass_part<3>(prow, qrow, s, j, V, vec4); break;
-    default: m = tree_pass_part<-1>(prow, qrow, s, j, V, vec4); break;
-    }
-    m = warp_sum_u64(m);
-    if (lane == 0) s_warp[warp] = m;
-    __syncthreads();
-    if (tid == 0) {
-        unsigned long long t = 0;
-        for (int w = 0; w < kTSWarps; ++w) t += s_warp[w];
-        *s_total = t;
-    }
-    __syncthreads();
-    const unsigned long long t = *s_total;
-    __syncthreads();   // s_total and s_warp may be rewritten by the next call
-    return t;
-}
-
 // CS CTAs (a cluster) per sequence, CTA `rank` owning the vocabulary slice
 // [c0, c0 + n).  Every CTA takes the same decisions: the tests read the two
 // gathered values from global memory, and each row sum is the CTAs' exact
@@ -1713,7 +1650,7 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
     extern __shared__ unsigned long long s_gtot[];   // one total per 512-element group of the slice
     __shared__ int32_t s_par[kMaxDraft + 1], s_tok[kMaxDraft + 1];
     __shared__ float s_s[kMaxDraft + 1];
-    __shared__ unsigned long long s_warp[kTSWarps], s_total;
+    __shared__ unsigned long long s_total;
     __shared__ __align__(8) unsigned long long s_x[2][CS];   // exchanged partials, per parity
     __shared__ uint64_t s_xbar[2];
     __shared__ int s_bad, s_abort;
@@ -1776,10 +1713,34 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
     int cur = 0, depth = 0, j = 0;
     unsigned long long S = 0;   // S_j (j >= 1)
     const float *prow = p, *qrow = q;
+    const int ngroups = (n + kTSGroup - 1) / kTSGroup;
+    int gtot_j = -1;            // s_gtot holds the group totals of R_gtot_j of the current node
+    // group totals of R_jj over this CTA's slice into s_gtot; returns their sum
+    auto slice_totals = [&](int jj) -> unsigned long long {
+        switch (jj) {   // uniform over the cluster
+        case 0: tree_group_totals<0>(prow + c0, qrow + c0, s_s, jj, n, vec4, s_gtot, ngroups); break;
+        case 1: tree_group_totals<1>(prow + c0, qrow + c0, s_s, jj, n, vec4, s_gtot, ngroups); break;
+        case 2: tree_group_totals<2>(prow + c0, qrow + c0, s_s, jj, n, vec4, s_gtot, ngroups); break;
+        case 3: tree_group_totals<3>(prow + c0, qrow + c0, s_s, jj, n, vec4, s_gtot, ngroups); break;
+        default: tree_group_totals<-1>(prow + c0, qrow + c0, s_s, jj, n, vec4, s_gtot, ngroups); break;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            unsigned long long z = 0;
+            for (int g = lane; g < ngroups; g += 32) z += s_gtot[g];
+            z = warp_sum_u64(z);
+            if (lane == 0) s_total = z;
+        }
+        __syncthreads();
+        const unsigned long long t = s_total;
+        __syncthreads();   // s_total is rewritten by the next call
+        return t;
+    };
     for (;;) {
         prow = p + (static_cast<int64_t>(b) * T + cur) * V;
         qrow = q + (static_cast<int64_t>(b) * T + cur) * V;
         j = 0;
+        gtot_j = -1;
         if (tid == 0) s_s[0] = 1.0f;
         __syncthreads();
         int next = -1;
@@ -1804,14 +1765,17 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
                 next = c;
                 break;
             }
-            const unsigned long long Sn =
-                exchange(tree_row_mass(prow + c0, qrow + c0, s_s, j + 1, n, vec4, s_warp, &s_total));
+            // the residual's group totals (kept: if no later sibling is
+            // accepted, the draw uses them as they are)
+            const unsigned long long Sn = exchange(slice_totals(j + 1));
             if (Sn == 0) {
+                gtot_j = -1;   // the totals are of an empty row, not of R_j
                 if (rank == 0 && tid == 0) report(dev_status, SPEC_DEV_INFO_ZERO_RESIDUAL);
             } else {
                 if (tid == 0) s_s[j + 1] = static_cast<float>(static_cast<double>(Sn) * 0x1p-61);
                 __syncthreads();
                 ++j;
+                gtot_j = j;
                 S = Sn;
             }
         }
@@ -1828,23 +1792,20 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
         if (rank == 0 && tid == 0) report(dev_status, SPEC_DEV_ERR_UNIFORM);
         u = (u >= 1.0f) ? 0x1.fffffep-1f : 0.0f;
     }
-    const int ngroups = (n + kTSGroup - 1) / kTSGroup;
-    switch (j) {   // uniform over the cluster
-    case 0: tree_group_totals<0>(prow + c0, qrow + c0, s_s, j, n, vec4, s_gtot, ngroups); break;
-    case 1: tree_group_totals<1>(prow + c0, qrow + c0, s_s, j, n, vec4, s_gtot, ngroups); break;
-    case 2: tree_group_totals<2>(prow + c0, qrow + c0, s_s, j, n, vec4, s_gtot, ngroups); break;
-    case 3: tree_group_totals<3>(prow + c0, qrow + c0, s_s, j, n, vec4, s_gtot, ngroups); break;
-    default: tree_group_totals<-1>(prow + c0, qrow + c0, s_s, j, n, vec4, s_gtot, ngroups); break;
+    // the last rejection's pass already left R_j's group totals
+    unsigned long long mine;
+    if (gtot_j == j) {
+        if (warp == 0) {
+            unsigned long long z = 0;
+            for (int g = lane; g < ngroups; g += 32) z += s_gtot[g];
+            z = warp_sum_u64(z);
+            if (lane == 0) s_total = z;
+        }
+        __syncthreads();
+        mine = s_total;
+    } else {
+        mine = slice_totals(j);
     }
-    __syncthreads();
-    if (warp == 0) {
-        unsigned long long z = 0;
-        for (int g = lane; g < ngroups; g += 32) z += s_gtot[g];
-        z = warp_sum_u64(z);
-        if (lane == 0) s_total = z;
-    }
-    __syncthreads();
-    const unsigned long long mine = s_total;
     const unsigned long long Z = ok ? exchange(mine) : 0ull;
     unsigned long long base = 0;
     for (int r = 0; r < rank; ++r) base += s_x[(nx - 1) & 1u][r];
