@@ -171,14 +171,28 @@ constexpr int kGSlots = 3;                                       // copies in fl
 constexpr uint32_t kGSmem = kGSlots * kGChunk * 4 + 128;         // ring + alignment slack
 constexpr int kGMinBlocks = 4;                                   // CTAs per SM (4 rings of 48 KB)
 
-__device__ __forceinline__ void cluster_arrive_release()
+// Cluster barriers of the push-only exchanges (greedy and tree sampling):
+// peers only write into a CTA's shared memory with st.async, whose bytes the
+// receiver always waits for on its own mbarrier, so no arrive has to publish
+// ordinary stores.  The start arrive follows fence.mbarrier_init, which
+// already makes the barrier initialisations visible to the cluster, and the
+// exit barrier only has to keep each CTA resident until every peer has issued
+// its last send.  Relaxed arrives there take 3-4% off greedy acceptance
+// (B=256, V=131072) against release arrives and a full cluster sync.
+__device__ __forceinline__ void cluster_arrive_relaxed()
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_wait_acquire()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_exit_barrier()
+{
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
 }
 
 template <int CS, bool TREE, bool BULK>
@@ -219,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, kGMinBlocks) accept_greedy_kernel(
         fence_mbar_init();
     }
     __syncthreads();
-    if constexpr (CS > 1) cluster_arrive_release();   // waited for before the first send
+    if constexpr (CS > 1) cluster_arrive_relaxed();   // waited for before the first send
     uint32_t issued[kGSlots] = {};   // thread 0: copies issued per slot (its phase count)
     uint32_t used = 0;               // every thread: chunks consumed so far (slot c % kGSlots)
     // thread 0: arm row i's exchange barrier and copy the first chunks of
@@ -375,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, kGMinBlocks) accept_greedy_kernel(
         for (int k = 0; k < kGSlots; ++k)
             if (issued[k]) mbar_wait_drain(&s_full[k], (issued[k] - 1u) & 1u, kWaitTimeoutNs);
     // keep this CTA's shared memory alive until every peer is done with it
-    if constexpr (CS > 1) cg::this_cluster().sync();
+    if constexpr (CS > 1) cluster_exit_barrier();
 }
 
 // --------------------------------------------------------------- stochastic
@@ -1673,7 +1687,7 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
         fence_mbar_init();
     }
     __syncthreads();
-    if constexpr (CS > 1) cluster_arrive_release();   // waited for before the first send
+    if constexpr (CS > 1) cluster_arrive_relaxed();   // waited for before the first send
     for (int k = tid; k < T; k += kTSThreads) {
         const int pa = parent[static_cast<int64_t>(b) * T + k];
         const int tk = tokens[static_cast<int64_t>(b) * T + k];
@@ -1874,7 +1888,7 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
         }
     }
     // keep this CTA's shared memory alive until every peer is done with it
-    if constexpr (CS > 1) cg::this_cluster().sync();
+    if constexpr (CS > 1) cluster_exit_barrier();
 }
 
 }  // namespace
