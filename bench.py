@@ -756,26 +756,30 @@ def run_cases(args, groups, dev, sv, flush, step=None):
         ms_s = time_launches(lambda: sv.accept_tree_sample(pt, qt, tok, par, ua, ur, na, tk, path), W, S, flush)
         nacc = na.cpu().numpy().astype(np.int64)
         path_h = path.cpu().numpy()
-        # rows the rule reads: one pass over the node's p and q rows per
-        # rejected child (the last one's pass also serves the draw), and a
-        # pass over p for a draw at a node without a rejection
+        # algorithmic bytes: the distinct rows the rule must read -- a
+        # node's p and q rows when one of its children is rejected there,
+        # and p alone at the final node when none is.  Passes after the
+        # first at a node re-read rows already read (on-chip or L2 traffic,
+        # reported as passes per sequence, not counted as HBM bytes).
         kids = [[c for c in range(1, D + 1) if par_h[b, c] == v] for b in range(Bt) for v in range(D + 1)]
         passes = np.zeros(Bt, np.int64)
-        last_rej = np.zeros(Bt, np.int64)
+        rows = np.zeros(Bt, np.int64)
         for b in range(Bt):
             node = 0
             for d in range(int(nacc[b]) + 1):
                 ch = kids[b * (D + 1) + node]
                 if d < nacc[b]:
                     nxt = int(path_h[b, d])
-                    passes[b] += sum(1 for c in ch if c < nxt)
+                    rej = sum(1 for c in ch if c < nxt)
                     node = nxt
                 else:
-                    passes[b] += len(ch)
-                    last_rej[b] = len(ch)
-        by = int(np.sum(passes * 2 + np.where(last_rej > 0, 0, 1))) * Vt * 4
+                    rej = len(ch)
+                passes[b] += rej
+                rows[b] += 2 if rej > 0 else (1 if d == nacc[b] else 0)
+        by = int(rows.sum()) * Vt * 4
         recs.append(accept_record(f"tree accept sample B{Bt} D{D} V{Vt} wide tree alpha0.6", "accept_tree_sample",
-                                  ms_s, nacc, by, row_passes_per_sequence=float(passes.mean())))
+                                  ms_s, nacc, by, row_passes_per_sequence=float(passes.mean()),
+                                  rows_read_per_sequence=float(rows.mean())))
         del pt, qt, tok, par, ua, ur
         torch.cuda.empty_cache()
 

@@ -297,12 +297,15 @@ spec_status_t spec_accept_tree_greedy(const float *p, const int32_t *tokens, con
  *   u_res      device, fp32 [B] in [0, 1): the uniform of the final draw.
  *   n_accepted, token, path  as for spec_accept_tree_greedy.
  * Arithmetic: the row after j rejections is kept unnormalised (R_j =
- * max(0, R_(j-1) - S_(j-1) q) with S_0 = 1 and S_j the sum of R_j), its
- * elements in fp32 and its sums exact in 2^-61 fixed point; a test after j
- * rejections is u q(x) S_j < R_j(x) in fp64.  A cluster of CTAs per
- * sequence (vocabulary slices whose exact sums are exchanged through
- * distributed shared memory); each rejection and the final draw read the
- * node's p and q rows once.
+ * max(0, R_(j-1) - S_(j-1) q) with S_0 = 1 and S_j the sum of R_j), which
+ * unrolls to R_j = max(0, p - c_j q) with c_j = S_0 + ... + S_(j-1); each
+ * element is evaluated in that form (c_j summed in fp64 and rounded to fp32
+ * once, then one fp32 fused multiply-add), and the sums are exact in 2^-61
+ * fixed point; a test after j rejections is u q(x) S_j < R_j(x) in fp64.  A
+ * cluster of CTAs per sequence (vocabulary slices whose exact sums are
+ * exchanged through distributed shared memory); each rejection and the
+ * final draw read the node's p and q rows once (from HBM the first time,
+ * mostly from L2 after).
  * Supported: D <= 63, V <= 2^22.  A malformed tree (SPEC_DEV_ERR_TREE) or a
  * token outside [0, V) (SPEC_DEV_ERR_TOKEN_ID) makes the walk stop at the
  * root; uniforms outside [0, 1) are clamped (SPEC_DEV_ERR_UNIFORM).

@@ -1581,70 +1581,76 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsMinBlocks) logits_rowstat
 // when no child is accepted the token is drawn from the row.  A chain is
 // the stochastic acceptance above (and the rule is lossless for siblings
 // drafted independently from q).
-// One CTA per sequence.  The row is kept unnormalised: R_0 = p and R_j =
-// max(0, R_{j-1} - s_{j-1} q) with s_0 = 1 and s_j = S_j = sum_v R_j(v), so
-// r_j = R_j / S_j; each R_j(v) is recomputed from p(v), q(v) and the s's in
-// fp32 (the same function for one element and for a whole pass), and each
-// S_j is the exact sum of the elements' 2^-61 fixed-point masses.  A test
-// after j rejections is u q(x) S_j < R_j(x) in fp64.  An empty residual
-// (S = 0) leaves the row as it was and is reported.
+// One cluster per sequence.  The row is kept unnormalised: R_0 = p and
+// R_j = max(0, R_{j-1} - S_{j-1} q) with S_0 = 1 and S_j = sum_v R_j(v), so
+// r_j = R_j / S_j.  Unrolled, R_j = max(0, p - c_j q) with c_j = S_0 + ... +
+// S_{j-1} (a clipped element stays clipped as c grows), which is how each
+// R_j(v) is evaluated: one fp32 fused multiply-add from p(v), q(v) and c_j,
+// whatever the depth, by the same function for one element and for a whole
+// pass.  c_j accumulates in fp64 from the exact S's and is rounded to fp32
+// once.  Each S_j is the exact sum of the elements' 2^-61 fixed-point
+// masses, and a test after j rejections is u q(x) S_j < R_j(x) in fp64.  An
+// empty residual (S = 0) leaves the row as it was and is reported.
 constexpr int kTSThreads = 256;
 constexpr int kTSWarps = kTSThreads / 32;
 constexpr int kTSGroup = 4 * kStep;   // 512 elements: 4 steps of 128
 
-__device__ __forceinline__ float tree_row_value(float pv, float qv, const float *s, int j)
+// R_j(v) for j >= 1 (RES) or R_0(v) = p(v)
+template <bool RES>
+__device__ __forceinline__ float tree_row_value(float pv, float qv, float c)
 {
-    float r = pv;
-    for (int i = 0; i < j; ++i) r = fmaxf(__fsub_rn(r, __fmul_rn(s[i], qv)), 0.0f);
-    return r;
+    return RES ? fmaxf(__fmaf_rn(-c, qv, pv), 0.0f) : pv;
 }
 
-// The same for a fixed count J with the s's in registers (identical
-// operations, so identical values).
-template <int J>
-__device__ __forceinline__ float tree_row_value_t(float pv, float qv, const float (&s)[4])
+template <bool RES>
+__device__ __forceinline__ unsigned long long tree_masses4(const float4 &xp, const float4 &xq, float c)
 {
-    float r = pv;
-#pragma unroll
-    for (int i = 0; i < J; ++i) r = fmaxf(__fsub_rn(r, __fmul_rn(s[i], qv)), 0.0f);
-    return r;
+    return (fix61(tree_row_value<RES>(xp.x, xq.x, c)) + fix61(tree_row_value<RES>(xp.y, xq.y, c))) +
+           (fix61(tree_row_value<RES>(xp.z, xq.z, c)) + fix61(tree_row_value<RES>(xp.w, xq.w, c)));
 }
 
-// Exact masses of R_J per 512-element group (warp w takes groups w, w +
-// kTSWarps, ...), into gtot.
-template <int J>
-__device__ __forceinline__ void tree_group_totals(const float *prow, const float *qrow, const float *s, int j,
-                                                  int V, bool vec4, unsigned long long *gtot, int ngroups)
+// Exact masses of R per 512-element group of a slice of n elements (warp w
+// takes groups w, w + kTSWarps, ...), into gtot; returns the sum of the
+// warp's groups (in every lane).  With 16-byte aligned rows (vec4) every
+// group inside the slice takes four unconditional float4 loads per operand
+// (q only for a residual); the ragged last group is checked.
+template <bool RES>
+__device__ __forceinline__ unsigned long long tree_group_totals(const float *prow, const float *qrow, float c, int n,
+                                                                bool vec4, unsigned long long *gtot, int ngroups)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float sr[4] = {1.0f, 1.0f, 1.0f, 1.0f};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        if (i < J) sr[i] = s[i];
-    for (int g = warp; g < ngroups; g += kTSWarps) {
+    const int nfull = vec4 ? n / kTSGroup : 0;
+    const float4 *p4 = reinterpret_cast<const float4 *>(prow) + lane;
+    const float4 *q4 = reinterpret_cast<const float4 *>(qrow) + lane;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    unsigned long long part = 0;
+    for (int g = warp; g < nfull; g += kTSWarps) {
         float4 xp[4], xq[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int64_t e = static_cast<int64_t>(g) * kTSGroup + k * kStep + lane * 4;
-            xp[k] = e < V ? load4(prow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
-            xq[k] = (j > 0 && e < V) ? load4(qrow, e, V, vec4, 0.0f) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xp[k] = __ldg(p4 + g * (kTSGroup / 4) + k * 32);
+            xq[k] = RES ? __ldg(q4 + g * (kTSGroup / 4) + k * 32) : zero;
         }
+        const unsigned long long m0 = tree_masses4<RES>(xp[0], xq[0], c) + tree_masses4<RES>(xp[1], xq[1], c);
+        const unsigned long long m1 = tree_masses4<RES>(xp[2], xq[2], c) + tree_masses4<RES>(xp[3], xq[3], c);
+        const unsigned long long m = warp_sum_u64(m0 + m1);
+        if (lane == 0) gtot[g] = m;
+        part += m;
+    }
+    for (int g = nfull + warp; g < ngroups; g += kTSWarps) {
         unsigned long long m = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            if (J >= 0) {
-                m += fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[k].x, xq[k].x, sr)) +
-                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[k].y, xq[k].y, sr)) +
-                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[k].z, xq[k].z, sr)) +
-                     fix61(tree_row_value_t<(J < 0 ? 0 : J)>(xp[k].w, xq[k].w, sr));
-            } else {
-                m += fix61(tree_row_value(xp[k].x, xq[k].x, s, j)) + fix61(tree_row_value(xp[k].y, xq[k].y, s, j)) +
-                     fix61(tree_row_value(xp[k].z, xq[k].z, s, j)) + fix61(tree_row_value(xp[k].w, xq[k].w, s, j));
-            }
+            const int64_t e = static_cast<int64_t>(g) * kTSGroup + k * kStep + lane * 4;
+            const float4 xp = e < n ? load4(prow, e, n, vec4, 0.0f) : zero;
+            const float4 xq = (RES && e < n) ? load4(qrow, e, n, vec4, 0.0f) : zero;
+            m += tree_masses4<RES>(xp, xq, c);
         }
         m = warp_sum_u64(m);
         if (lane == 0) gtot[g] = m;
+        part += m;
     }
+    return part;
 }
 
 // CS CTAs (a cluster) per sequence, CTA `rank` owning the vocabulary slice
@@ -1663,8 +1669,7 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
 {
     extern __shared__ unsigned long long s_gtot[];   // one total per 512-element group of the slice
     __shared__ int32_t s_par[kMaxDraft + 1], s_tok[kMaxDraft + 1];
-    __shared__ float s_s[kMaxDraft + 1];
-    __shared__ unsigned long long s_total;
+    __shared__ unsigned long long s_wpart[kTSWarps];
     __shared__ __align__(8) unsigned long long s_x[2][CS];   // exchanged partials, per parity
     __shared__ uint64_t s_xbar[2];
     __shared__ int s_bad, s_abort;
@@ -1711,8 +1716,13 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
             if (tid == 0) mbar_arrive_expect_tx(&s_xbar[slot], CS * 8);
             if (nx == 0) cluster_wait_acquire();   // every peer's barriers are initialised
             if (tid < CS) st_async_peer(peer_smem(&s_x[slot][rank], tid), mine, peer_smem(&s_xbar[slot], tid));
-            if (ok) ok = mbar_wait(&s_xbar[slot], (nx >> 1) & 1u, abort, dev_status);
+            // one warp spins (spinning warps would take issue slots from the
+            // passes of the SM's other CTAs); the others block in the barrier
+            // and then take the completed phase, without waiting, to acquire
+            // the peers' stores themselves
+            if (ok && warp == 0) ok = mbar_wait(&s_xbar[slot], (nx >> 1) & 1u, abort, dev_status);
             ok = __syncthreads_and(ok);
+            if (ok && warp != 0) (void)mbar_try_wait(smem_u32(&s_xbar[slot]), (nx >> 1) & 1u);
         } else {
             if (tid == 0) s_x[slot][0] = mine;
             __syncthreads();
@@ -1724,39 +1734,38 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
         return t;
     };
 
+    // the current row R_j: j rejections so far, c_j (fp64 and rounded to
+    // fp32) and S_j (exact, and in fp64); c_0 = 0 and S_0 = 1
     int cur = 0, depth = 0, j = 0;
-    unsigned long long S = 0;   // S_j (j >= 1)
+    double Cj = 0.0, Sj = 1.0;
+    float cf = 0.0f;
     const float *prow = p, *qrow = q;
     const int ngroups = (n + kTSGroup - 1) / kTSGroup;
     int gtot_j = -1;            // s_gtot holds the group totals of R_gtot_j of the current node
-    // group totals of R_jj over this CTA's slice into s_gtot; returns their sum
-    auto slice_totals = [&](int jj) -> unsigned long long {
-        switch (jj) {   // uniform over the cluster
-        case 0: tree_group_totals<0>(prow + c0, qrow + c0, s_s, jj, n, vec4, s_gtot, ngroups); break;
-        case 1: tree_group_totals<1>(prow + c0, qrow + c0, s_s, jj, n, vec4, s_gtot, ngroups); break;
-        case 2: tree_group_totals<2>(prow + c0, qrow + c0, s_s, jj, n, vec4, s_gtot, ngroups); break;
-        case 3: tree_group_totals<3>(prow + c0, qrow + c0, s_s, jj, n, vec4, s_gtot, ngroups); break;
-        default: tree_group_totals<-1>(prow + c0, qrow + c0, s_s, jj, n, vec4, s_gtot, ngroups); break;
-        }
+    unsigned long long gtot_sum = 0;   // ... and their sum
+    // group totals of R (p, or the residual with coefficient c) over this
+    // CTA's slice into s_gtot; returns their sum.  The warps' partials are
+    // read before the exchange that follows every call, whose barrier keeps
+    // the next call from rewriting them early.
+    auto slice_totals = [&](bool res, float c) -> unsigned long long {
+        const unsigned long long part =   // res is uniform over the cluster
+            res ? tree_group_totals<true>(prow + c0, qrow + c0, c, n, vec4, s_gtot, ngroups)
+                : tree_group_totals<false>(prow + c0, qrow + c0, c, n, vec4, s_gtot, ngroups);
+        if (lane == 0) s_wpart[warp] = part;
         __syncthreads();
-        if (warp == 0) {
-            unsigned long long z = 0;
-            for (int g = lane; g < ngroups; g += 32) z += s_gtot[g];
-            z = warp_sum_u64(z);
-            if (lane == 0) s_total = z;
-        }
-        __syncthreads();
-        const unsigned long long t = s_total;
-        __syncthreads();   // s_total is rewritten by the next call
+        unsigned long long t = 0;
+#pragma unroll
+        for (int w = 0; w < kTSWarps; ++w) t += s_wpart[w];
         return t;
     };
     for (;;) {
         prow = p + (static_cast<int64_t>(b) * T + cur) * V;
         qrow = q + (static_cast<int64_t>(b) * T + cur) * V;
         j = 0;
+        Cj = 0.0;
+        Sj = 1.0;
+        cf = 0.0f;
         gtot_j = -1;
-        if (tid == 0) s_s[0] = 1.0f;
-        __syncthreads();
         int next = -1;
         for (int c = cur + 1; c < T && !bad && ok; ++c) {
             if (s_par[c] != cur) continue;
@@ -1771,26 +1780,34 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
             if (j == 0) {
                 acc = static_cast<double>(u) * static_cast<double>(qx) < static_cast<double>(px);
             } else {
-                const float rx = tree_row_value(px, qx, s_s, j);
-                acc = static_cast<double>(u) * static_cast<double>(qx) * (static_cast<double>(S) * 0x1p-61) <
-                      static_cast<double>(rx);
+                const float rx = tree_row_value<true>(px, qx, cf);
+                acc = static_cast<double>(u) * static_cast<double>(qx) * Sj < static_cast<double>(rx);
             }
             if (acc) {
                 next = c;
                 break;
             }
-            // the residual's group totals (kept: if no later sibling is
-            // accepted, the draw uses them as they are)
-            const unsigned long long Sn = exchange(slice_totals(j + 1));
+            // R_{j+1} = max(0, p - c_{j+1} q) with c_{j+1} = c_j + S_j; its
+            // group totals are kept: if no later sibling is accepted, the
+            // draw uses them as they are
+            if (j == 0 && vec4 && tid == 0 && n >= 4) {   // the node's first pass
+                prefetch_l2(prow + c0, static_cast<uint32_t>(n & ~3) * 4u);
+                prefetch_l2(qrow + c0, static_cast<uint32_t>(n & ~3) * 4u);
+            }
+            const double Cn = Cj + Sj;
+            const float cn = static_cast<float>(Cn);
+            const unsigned long long mine = slice_totals(true, cn);
+            const unsigned long long Sn = exchange(mine);
             if (Sn == 0) {
                 gtot_j = -1;   // the totals are of an empty row, not of R_j
                 if (rank == 0 && tid == 0) report(dev_status, SPEC_DEV_INFO_ZERO_RESIDUAL);
             } else {
-                if (tid == 0) s_s[j + 1] = static_cast<float>(static_cast<double>(Sn) * 0x1p-61);
-                __syncthreads();
                 ++j;
+                Cj = Cn;
+                cf = cn;
+                Sj = static_cast<double>(Sn) * 0x1p-61;
                 gtot_j = j;
-                S = Sn;
+                gtot_sum = mine;
             }
         }
         if (next < 0 || !ok) break;
@@ -1809,16 +1826,13 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
     // the last rejection's pass already left R_j's group totals
     unsigned long long mine;
     if (gtot_j == j) {
-        if (warp == 0) {
-            unsigned long long z = 0;
-            for (int g = lane; g < ngroups; g += 32) z += s_gtot[g];
-            z = warp_sum_u64(z);
-            if (lane == 0) s_total = z;
-        }
-        __syncthreads();
-        mine = s_total;
+        mine = gtot_sum;
     } else {
-        mine = slice_totals(j);
+        if (vec4 && tid == 0 && n >= 4) {
+            prefetch_l2(prow + c0, static_cast<uint32_t>(n & ~3) * 4u);
+            if (j > 0) prefetch_l2(qrow + c0, static_cast<uint32_t>(n & ~3) * 4u);
+        }
+        mine = slice_totals(j > 0, cf);
     }
     const unsigned long long Z = ok ? exchange(mine) : 0ull;
     unsigned long long base = 0;
@@ -1849,6 +1863,7 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
             gbase += __shfl_sync(0xffffffffu, incl, 31);
         }
         // the element: walk the group's 512 elements, 128 at a time
+        auto rv = [&](float pv, float qv) { return j > 0 ? tree_row_value<true>(pv, qv, cf) : pv; };
         unsigned long long run = run_g;
         for (int k = 0; k < 4 && found >= 0; ++k) {
             const int64_t e = static_cast<int64_t>(found) * kTSGroup + k * kStep + lane * 4;
@@ -1857,10 +1872,10 @@ __global__ void __launch_bounds__(kTSThreads) accept_tree_sample_kernel(
                 xp = load4(prow + c0, e, n, vec4, 0.0f);
                 if (j > 0) xq = load4(qrow + c0, e, n, vec4, 0.0f);
             }
-            const unsigned long long m0 = e < n ? fix61(tree_row_value(xp.x, xq.x, s_s, j)) : 0ull;
-            const unsigned long long m1 = e < n ? fix61(tree_row_value(xp.y, xq.y, s_s, j)) : 0ull;
-            const unsigned long long m2 = e < n ? fix61(tree_row_value(xp.z, xq.z, s_s, j)) : 0ull;
-            const unsigned long long m3 = e < n ? fix61(tree_row_value(xp.w, xq.w, s_s, j)) : 0ull;
+            const unsigned long long m0 = e < n ? fix61(rv(xp.x, xq.x)) : 0ull;
+            const unsigned long long m1 = e < n ? fix61(rv(xp.y, xq.y)) : 0ull;
+            const unsigned long long m2 = e < n ? fix61(rv(xp.z, xq.z)) : 0ull;
+            const unsigned long long m3 = e < n ? fix61(rv(xp.w, xq.w)) : 0ull;
             const unsigned long long ls = m0 + m1 + m2 + m3;
             const unsigned long long incl = warp_incl_scan_u64(ls, lane);
             const unsigned hit = __ballot_sync(0xffffffffu, run + incl > Tt);
