@@ -19,7 +19,7 @@ import threading
 __all__ = [
     "SpecError", "library", "library_path", "verify_attention", "verify_gemm",
     "accept_greedy", "accept_sample", "accept_sample_workspace_size", "attention_workspace_size",
-    "gemm_workspace_size", "gemm_plan", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
+    "gemm_workspace_size", "gemm_plan", "gemm_plan_cluster", "attention_plan", "EXPORTED_SYMBOLS", "DEV_STATUS_BITS",
     "verify_tree_attention", "tree_attention_workspace_size", "accept_tree_greedy", "accept_tree_sample",
     "AdaptiveDraftLength", "accept_sample_logits", "accept_sample_logits_workspace_size",
     "accept_adasd", "accept_adasd_workspace_size", "selftest_bounded_wait",
@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "spec_verify_attention", "spec_verify_gemm_workspace_size", "spec_verify_gemm",
     "spec_accept_greedy", "spec_accept_sample", "spec_verify_attention_plan",
     "spec_verify_attention_noalloc", "spec_accept_sample_workspace_size", "spec_verify_gemm_plan",
+    "spec_verify_gemm_plan_cluster",
     "spec_verify_tree_attention_workspace_size", "spec_verify_tree_attention",
     "spec_accept_tree_greedy", "spec_accept_tree_sample", "spec_adaptive_init", "spec_adaptive_update", "spec_adaptive_draft_len",
     "spec_accept_sample_logits_workspace_size", "spec_accept_sample_logits",
@@ -112,6 +113,8 @@ def library():
             lib.spec_adaptive_draft_len.restype = I
             lib.spec_verify_gemm_plan.argtypes = [I, I, I, I, P, I]
             lib.spec_verify_gemm_plan.restype = I
+            lib.spec_verify_gemm_plan_cluster.argtypes = [I, I, I, I]
+            lib.spec_verify_gemm_plan_cluster.restype = I
             lib.spec_accept_sample_logits_workspace_size.argtypes = [I, I, I]
             lib.spec_accept_sample_logits_workspace_size.restype = S
             lib.spec_accept_sample_logits.argtypes = [P, P, P, F, ctypes.c_uint64, I, I, I, P, P, P, S,
@@ -258,8 +261,17 @@ def gemm_workspace_size(M, N, K):
     return int(library().spec_verify_gemm_workspace_size(M, N, K))
 
 
+def gemm_plan_cluster(M, N, K, num_sms):
+    """Cluster size of the planned launch: 2 for CTA pairs (M > 256); for
+    M <= 256, 1 for stream-K and S >= 2 for split K over clusters of S."""
+    n = library().spec_verify_gemm_plan_cluster(M, N, K, num_sms)
+    if n < 0:
+        raise ValueError("spec_verify_gemm_plan_cluster rejected its arguments")
+    return n
+
+
 def gemm_plan(M, N, K, num_sms):
-    """Segments (cta, tile, kb0, kb1, last, BN) of the stream-K split."""
+    """Segments (cta, tile, kb0, kb1, last, BN) of the planned work split."""
     import numpy as np
     lib = library()
     n = lib.spec_verify_gemm_plan(M, N, K, num_sms, None, 0)

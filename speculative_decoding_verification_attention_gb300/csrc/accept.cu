@@ -115,22 +115,7 @@ __device__ __forceinline__ ArgMax unpack_argmax(unsigned long long w)
     return {__uint_as_float(static_cast<uint32_t>(w >> 32)), lo == 0xFFFFFFFFu ? INT_MAX : static_cast<int>(lo)};
 }
 
-// Address of the same shared variable in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t peer_smem(const void *local, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
-    return r;
-}
 
-// 8-byte store into a peer CTA's shared memory that completes on the peer's
-// mbarrier (both addresses in the cluster window).
-__device__ __forceinline__ void st_async_peer(uint32_t addr, unsigned long long v, uint32_t bar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(addr),
-                 "l"(v), "r"(bar)
-                 : "memory");
-}
 
 constexpr int kGUnroll = 8;    // greedy: 128-element steps whose loads are in flight together
 
@@ -171,29 +156,6 @@ constexpr int kGSlots = 3;                                       // copies in fl
 constexpr uint32_t kGSmem = kGSlots * kGChunk * 4 + 128;         // ring + alignment slack
 constexpr int kGMinBlocks = 4;                                   // CTAs per SM (4 rings of 48 KB)
 
-// Cluster barriers of the push-only exchanges (greedy and tree sampling):
-// peers only write into a CTA's shared memory with st.async, whose bytes the
-// receiver always waits for on its own mbarrier, so no arrive has to publish
-// ordinary stores.  The start arrive follows fence.mbarrier_init, which
-// already makes the barrier initialisations visible to the cluster, and the
-// exit barrier only has to keep each CTA resident until every peer has issued
-// its last send.  Relaxed arrives there take 3-4% off greedy acceptance
-// (B=256, V=131072) against release arrives and a full cluster sync.
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait_acquire()
-{
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_exit_barrier()
-{
-    cluster_arrive_relaxed();
-    cluster_wait_acquire();
-}
 
 template <int CS, bool TREE, bool BULK>
 __global__ void __launch_bounds__(kThreads, kGMinBlocks) accept_greedy_kernel(

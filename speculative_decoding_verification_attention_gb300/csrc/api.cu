@@ -362,7 +362,9 @@ size_t spec_verify_gemm_workspace_size(int M, int N, int K)
     if (M <= 0 || N <= 0 || K <= 0) return 0;
     int sms = device_sm_count();
     if (sms <= 0) sms = kSmFallback;
-    return plan_gemm(M, N, K, sms, sms / 2).workspace_bytes;   // an upper bound
+    // an upper bound: the stream-K plan (split K needs no workspace, and the
+    // device decides between the two)
+    return plan_gemm(M, N, K, sms, sms / 2, SplitCaps{}).workspace_bytes;
 }
 
 int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments, int max_segments)
@@ -370,7 +372,7 @@ int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments, i
     if (M <= 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 64 != 0 || num_sms <= 0 ||
         max_segments < 0 || (max_segments > 0 && !segments))
         return -1;
-    const GemmPlan plan = plan_gemm(M, N, K, num_sms, num_sms / 2);
+    const GemmPlan plan = plan_gemm(M, N, K, num_sms, num_sms / 2, split_caps_estimate(num_sms));
     int n = 0;
     if (!plan.swap) {
         // pairs: whole tiles, pair c taking tiles c, c + pairs, ...
@@ -388,6 +390,25 @@ int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments, i
                 }
                 ++n;
             }
+        return n;
+    }
+    if (plan.split >= 2) {
+        // split K: CTA c = t S + r takes k-blocks [r K/S, (r + 1) K/S) of
+        // tile t; rank 0's row names the last CTA of the tile's cluster
+        const int S = plan.split, kblocks = K / 64;
+        for (int c = 0; c < plan.grid; ++c) {
+            if (n < max_segments) {
+                const int t = c / S, r = c % S;
+                int32_t *row = segments + 6 * static_cast<size_t>(n);
+                row[0] = c;
+                row[1] = t;
+                row[2] = r * kblocks / S;
+                row[3] = (r + 1) * kblocks / S;
+                row[4] = r == 0 ? c + S - 1 : -1;
+                row[5] = plan.bn;
+            }
+            ++n;
+        }
         return n;
     }
     for (int c = 0; c < plan.sk.G; ++c) {
@@ -409,6 +430,13 @@ int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments, i
     return n;
 }
 
+int spec_verify_gemm_plan_cluster(int M, int N, int K, int num_sms)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 64 != 0 || num_sms <= 0) return -1;
+    const GemmPlan plan = plan_gemm(M, N, K, num_sms, num_sms / 2, split_caps_estimate(num_sms));
+    return !plan.swap ? 2 : plan.split >= 2 ? plan.split : 1;
+}
+
 spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_bf16, int M, int N,
                                int K, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
                                void *stream)
@@ -423,10 +451,11 @@ spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_b
     const int sms = device_sm_count();
     if (sms <= 0) return SPEC_ERR_CUDA;
     // only the variant this call runs is asked for its residency
-    const GemmPlan probe = plan_gemm(M, N, K, sms, sms / 2);
+    const GemmPlan probe = plan_gemm(M, N, K, sms, sms / 2, SplitCaps{});
     const int units = gemm_max_units(probe.bn, probe.swap);
     if (units <= 0) return SPEC_ERR_CUDA;
-    const GemmPlan plan = plan_gemm(M, N, K, probe.swap ? units : sms, probe.swap ? sms / 2 : units);
+    const GemmPlan plan = plan_gemm(M, N, K, probe.swap ? units : sms, probe.swap ? sms / 2 : units,
+                                    probe.swap ? split_caps_device(probe.bn) : SplitCaps{});
     if (plan.workspace_bytes > 0 &&
         (!workspace || workspace_bytes < plan.workspace_bytes || !aligned(workspace, 256)))
         return SPEC_ERR_WORKSPACE;

@@ -15,14 +15,18 @@
 //    halves, so each w byte crosses from L2 into one SM only.  Tiles are
 //    whole (no split K) with ragged widths (multiples of 32 columns, chosen
 //    so the tiles spread evenly over the pairs).
-//  * gemm_swap_kernel (M <= 256): A = w rows (128 per tile), B = the M rows
-//    of x padded to MPAD, so the MMA is not mostly padding; the output is
-//    written transposed.  The k-block iterations of all tiles are split
-//    evenly over the CTAs (stream-K, see gemm_schedule.h): every piece of a
-//    tile cut between CTAs leaves its fp32 partial in the workspace and
-//    counts itself in; the last piece to arrive adds them all in k order
-//    (so results are deterministic) and writes the tile.  No CTA waits for
-//    another.
+//  * gemm_split_kernel (M <= 256, when every tile's cluster fits at once):
+//    A = w rows (128 per tile), B = the M rows of x padded to BN, so the
+//    MMA is not mostly padding; the output is written transposed.  Each
+//    tile's k-blocks are split over the S CTAs of a thread-block cluster,
+//    whose fp32 pieces meet in their shared memory and are added in k
+//    order (see the kernel).
+//  * gemm_swap_kernel (M <= 256, otherwise): the same orientation; the
+//    k-block iterations of all tiles are split evenly over the CTAs
+//    (stream-K, see gemm_schedule.h): every piece of a tile cut between
+//    CTAs leaves its fp32 partial in the workspace and counts itself in;
+//    the last piece to arrive adds them all in k order (so results are
+//    deterministic) and writes the tile.  No CTA waits for another.
 // Output blocks of 32 x 32 are staged in shared memory by each epilogue warp and written by TMA tensor stores (coalesced, asynchronous;
 // rows past M are clipped).
 #include <cuda_bf16.h>
@@ -488,6 +492,195 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, 2 * BN); }
 }
 
+// ------------------------------------------------- weight streaming, split K
+// M <= 256 with few 128-row w tiles (N = 6144: 48): tile t's k-blocks are
+// cut into S equal ranges, one per CTA of a cluster of S (rank r takes
+// k-blocks [r K/S, (r + 1) K/S) of K/64), all of a tile's CTAs resident
+// together.  Each CTA streams its range (KPS k-blocks per stage) into its
+// own tensor-memory accumulator.  Once every CTA of the cluster has
+// finished its MMAs (a cluster barrier), their stage rings are idle and
+// receive the partial sums: 32-column chunk cc of the tile belongs to CTA
+// cc % S, and every other CTA sends its fp32 piece of the chunk into slot
+// (cc / S, rank) of the owner's ring by asynchronous shared-memory stores
+// that complete on the owner's mbarrier.  The owner adds the S pieces in
+// rank (= k) order, its own read from its tensor memory, and stores the
+// chunk as bf16.  Against stream-K this
+// removes the fp32 partials' round trip through L2 and the tile fix-up
+// that one CTA did alone after all others had finished.
+template <int BN>
+struct SplitCfg {
+    static constexpr int kKps = 2;                                      // k-blocks per stage
+    static constexpr int kStages = BN >= 256 ? 2 : BN >= 128 ? 3 : 4;
+    static constexpr uint32_t kTileB = BN * kBK * 2;
+    static constexpr uint32_t kStage = kKps * (kTileA + kTileB);
+    static constexpr uint32_t kRing = kStages * kStage;
+    static constexpr uint32_t kBytes = kRing + kOutStaging + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t kChunkBytes = 32 * kBM * 4;            // one fp32 piece of a chunk
+};
+
+// Whether a cluster of S CTAs can hold the pieces its CTAs receive (each
+// owns ceil(chunks / S) chunks of S pieces) in one CTA's stage ring.
+template <int BN>
+__host__ __device__ constexpr bool split_fits(int S)
+{
+    return S >= 2 && S <= 8 &&
+           static_cast<uint32_t>(S * ((BN / 32 + S - 1) / S)) * SplitCfg<BN>::kChunkBytes <= SplitCfg<BN>::kRing;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_split_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                      const __grid_constant__ CUtensorMap tm_y, int M, int kblocks, uint32_t *dev_status)
+{
+    using C = SplitCfg<BN>;
+    constexpr int STAGES = C::kStages, KPS = C::kKps;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *out_stage = smem + C::kRing;   // 4 warps x 2 output blocks
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_stage + kOutStaging);
+    uint64_t *empty = full + STAGES;
+    uint64_t *acc_full = empty + STAGES;
+    uint64_t *recv = acc_full + 1;    // the pieces of this CTA's chunks landed
+    uint64_t *drain = recv + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = static_cast<int>(cluster_ctas());
+    if (!split_fits<BN>(S) || kblocks < S) {   // uniform over the grid
+        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
+        return;
+    }
+    const int rank = static_cast<int>(cluster_rank());
+    const int t = static_cast<int>(blockIdx.x) / S;
+    const int kb0 = rank * kblocks / S, kb1 = (rank + 1) * kblocks / S;
+    const int nchunks = (M + 31) / 32 < BN / 32 ? (M + 31) / 32 : BN / 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(acc_full, 1);
+        mbar_init(recv, 1);
+        mbar_init(drain, 1);
+        *abort = 0;
+        // the bytes this CTA will receive: S - 1 pieces of each chunk it owns
+        uint32_t bytes = 0;
+        for (int cc = rank; cc < nchunks; cc += S)
+            bytes += static_cast<uint32_t>((S - 1) * live_quads(M, cc)) * kBM * 16;
+        mbar_arrive_expect_tx(recv, bytes);
+        fence_mbar_init();
+    }
+    if (warp == 1) { tmem_alloc(tmem_slot, BN); tmem_relinquish(); }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    bool ok = true;
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_y);
+        uint32_t it = 0;
+        for (int kb = kb0; kb < kb1 && !*abort; kb += KPS, ++it) {
+            const int nk = kb1 - kb < KPS ? kb1 - kb : KPS;
+            const int st = static_cast<int>(it % STAGES);
+            if (it >= static_cast<uint32_t>(STAGES) &&
+                !mbar_wait(&empty[st], ((it / STAGES) & 1) ^ 1, abort, dev_status)) break;
+            uint8_t *sa = smem + st * C::kStage;
+            mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(nk) * (kTileA + C::kTileB));
+            for (int q = 0; q < nk; ++q) {
+                tma_load_2d(sa + q * kTileA, &tm_w, &full[st], (kb + q) * kBK, t * kBM);
+                tma_load_2d(sa + KPS * kTileA + q * C::kTileB, &tm_x, &full[st], (kb + q) * kBK, 0);
+            }
+        }
+        if (*abort) drain_copies(full, it, STAGES);
+    } else if (warp == 1 && lane == 0) {
+        uint32_t it = 0;
+        for (int kb = kb0; kb < kb1; kb += KPS, ++it) {
+            const int nk = kb1 - kb < KPS ? kb1 - kb : KPS;
+            const int st = static_cast<int>(it % STAGES);
+            if (!mbar_wait(&full[st], (it / STAGES) & 1, abort, dev_status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + st * C::kStage);
+            for (int q = 0; q < nk; ++q)
+                mma_kblock<BN>(tmem, sa + q * kTileA, sa + KPS * kTileA + q * C::kTileB, it > 0 || q > 0);
+            umma_commit(&empty[st]);
+        }
+        if (ok) umma_commit(acc_full);
+    } else if (warp >= 2) {
+        ok = mbar_wait_warp(acc_full, 0, abort, dev_status);
+        tc_fence_after();
+    }
+    // every CTA of the cluster is done with its stage ring (its MMAs have
+    // completed: the epilogue warps arrive after the accumulator is final)
+    __syncwarp();
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    tc_fence_after();
+
+    if (warp >= 2) {
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t tbase = tmem + ((quad * 32) << 16);
+        // send: this CTA's piece of every chunk it does not own to the owner
+#pragma unroll 1
+        for (int cc = 0; cc < nchunks && ok && !*abort; ++cc) {
+            if (cc % S == rank) continue;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + cc * 32, r);
+            tmem_ld_wait();
+            const uint32_t owner = static_cast<uint32_t>(cc % S);
+            const float *slot =
+                reinterpret_cast<const float *>(smem) + static_cast<size_t>((cc / S) * S + rank) * (32 * kBM);
+            const uint32_t dst = peer_smem(slot, owner);
+            const uint32_t bar = peer_smem(recv, owner);
+            const int nq = live_quads(M, cc);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+                if (q4 < nq)
+                    st_async_peer_v4(dst + unit_index(q4, row) * 4, r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2],
+                                     r[4 * q4 + 3], bar);
+        }
+        // receive: the S pieces of each owned chunk, added in k order
+        if (ok) ok = mbar_wait_warp(recv, 0, abort, dev_status);
+        uint8_t *obuf = out_stage + (warp - 2) * 2 * kOutBlock;
+        uint32_t nst = 0;
+#pragma unroll 1
+        for (int cc = rank; cc < nchunks && ok; cc += S) {
+            const int nq = live_quads(M, cc);
+            const float *base = reinterpret_cast<const float *>(smem) + static_cast<size_t>((cc / S) * S) * (32 * kBM);
+            uint32_t own[32];
+            tmem_ld_32x32b_x32(tbase + cc * 32, own);
+            tmem_ld_wait();
+            float a[32];
+            for (int src = 0; src < S; ++src) {
+                const float *u = base + static_cast<size_t>(src) * (32 * kBM);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    float4 v = make_float4(__uint_as_float(own[4 * q4]), __uint_as_float(own[4 * q4 + 1]),
+                                           __uint_as_float(own[4 * q4 + 2]), __uint_as_float(own[4 * q4 + 3]));
+                    if (src != rank)
+                        v = q4 < nq ? *reinterpret_cast<const float4 *>(u + unit_index(q4, row))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (src == 0) {
+                        a[4 * q4] = v.x; a[4 * q4 + 1] = v.y; a[4 * q4 + 2] = v.z; a[4 * q4 + 3] = v.w;
+                    } else {
+                        a[4 * q4] += v.x; a[4 * q4 + 1] += v.y; a[4 * q4 + 2] += v.z; a[4 * q4 + 3] += v.w;
+                    }
+                }
+            }
+            store_out_swap(&tm_y, obuf, nst, lane, t, quad, cc, a);
+        }
+        if (lane == 0) bulk_wait_read_all();   // staged output read before the CTA's shared memory goes
+    }
+    // no CTA leaves while a peer may still send into it
+    __syncwarp();
+    cluster_exit_barrier();
+    __syncthreads();
+    if (*abort && threadIdx.x == 32) drain_mmas(drain);
+    __syncthreads();
+    if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, BN); }
+}
+
 // ------------------------------------------------------------- CTA pairs
 // M > 256: one tcgen05.mma of M = 256 per 16-deep K step, shared by the two
 // CTAs of a cluster.  Per 64-wide k-block each CTA stages its own 128 rows
@@ -753,6 +946,61 @@ int max_swap_units()
     return per_sm > 0 ? sms : 0;   // one CTA per SM
 }
 
+template <int BN>
+cudaLaunchConfig_t split_config(int grid, int S, cudaStream_t st, cudaLaunchAttribute (&attr)[1])
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SplitCfg<BN>::kBytes;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeClusterDimension;   // the CTAs sharing a tile's k-blocks
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int BN>
+cudaError_t run_split(const GemmPlan &p, const CUtensorMap &tx, const CUtensorMap &tw, const CUtensorMap &ty,
+                      int M, int K, uint32_t *dev_status, cudaStream_t st)
+{
+    cudaError_t e = set_smem(gemm_split_kernel<BN>, SplitCfg<BN>::kBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = split_config<BN>(p.grid, p.split, st, attr);
+    return cudaLaunchKernelEx(&cfg, gemm_split_kernel<BN>, tx, tw, ty, M, K / kBK, dev_status);
+}
+
+// Clusters of S split CTAs that can be resident at once (0 if the query
+// fails or the ring cannot hold the exchanged pieces).
+template <int BN>
+int max_split_clusters(int S)
+{
+    if (!split_fits<BN>(S)) return 0;
+    if (set_smem(gemm_split_kernel<BN>, SplitCfg<BN>::kBytes) != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = split_config<BN>(S, S, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_split_kernel<BN>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+bool split_fits_bn(int bn, int S)
+{
+    switch (bn) {
+    case 32: return split_fits<32>(S);
+    case 64: return split_fits<64>(S);
+    case 128: return split_fits<128>(S);
+    default: return split_fits<256>(S);
+    }
+}
+
 int max_pair_units()
 {
     if (set_smem(gemm_pair_kernel, kPairSmem) != cudaSuccess) return 0;
@@ -778,6 +1026,38 @@ int query_max_units(int bn, bool swap)
 }
 
 }  // namespace
+
+SplitCaps split_caps_estimate(int sms)
+{
+    SplitCaps c{};
+    for (int S = 2; S <= 8; ++S) c.max_clusters[S] = sms / S;
+    return c;
+}
+
+SplitCaps split_caps_device(int bn)
+{
+    // per device and width; the answers never change for a process
+    static std::atomic<int> cache[64][4][9];
+    SplitCaps c{};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return c;
+    const int b = bn == 32 ? 0 : bn == 64 ? 1 : bn == 128 ? 2 : 3;
+    for (int S = 2; S <= 8; ++S) {
+        std::atomic<int> &slot = cache[dev][b][S];
+        int v = slot.load(std::memory_order_relaxed);
+        if (v == 0) {
+            switch (bn) {
+            case 32: v = max_split_clusters<32>(S); break;
+            case 64: v = max_split_clusters<64>(S); break;
+            case 128: v = max_split_clusters<128>(S); break;
+            default: v = max_split_clusters<256>(S); break;
+            }
+            slot.store(v > 0 ? v : -1, std::memory_order_relaxed);
+        }
+        c.max_clusters[S] = v > 0 ? v : 0;
+    }
+    return c;
+}
 
 int gemm_max_units(int bn, bool swap)
 {
@@ -830,7 +1110,7 @@ PairGrid plan_pairs(int M, int N, int K, int max_pairs)
     return g;
 }
 
-GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_pair)
+GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_pair, const SplitCaps &caps)
 {
     GemmPlan p{};
     const int kblocks = K / kBK;
@@ -851,6 +1131,16 @@ GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_pair)
     p.swap = true;
     p.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     const int tiles = N / kBM;
+    // Split K over clusters when every tile's S CTAs can be resident at
+    // once: the largest S (up to 8, at most one k-block per CTA less than
+    // K / 64) whose clusters all fit and whose exchanged pieces fit a ring.
+    for (int S = 8; S >= 2; --S) {
+        if (S > kblocks || !split_fits_bn(p.bn, S) || caps.max_clusters[S] < tiles) continue;
+        p.split = S;
+        p.grid = tiles * S;
+        p.workspace_bytes = 0;   // the pieces meet in shared memory
+        return p;
+    }
     p.sk.tiles_m = 1;
     const int div = 3;
     const int min_iters = (kblocks + div - 1) / div > 8 ? (kblocks + div - 1) / div : 8;
@@ -891,6 +1181,14 @@ cudaError_t launch_gemm(const GemmPlan &p, const void *x, const void *w, void *y
         if (!encode_bf16_tmap(&tx, x, 2, dx, sk, bx) || !encode_bf16_tmap(&tw, w, 2, dw, sk, bw) ||
             !encode_bf16_tmap_plain(&ty, y, 2, dy, sy, by))
             return cudaErrorInvalidValue;
+        if (p.split >= 2) {
+            switch (p.bn) {
+            case 32: return run_split<32>(p, tx, tw, ty, M, K, dev_status, st);
+            case 64: return run_split<64>(p, tx, tw, ty, M, K, dev_status, st);
+            case 128: return run_split<128>(p, tx, tw, ty, M, K, dev_status, st);
+            default: return run_split<256>(p, tx, tw, ty, M, K, dev_status, st);
+            }
+        }
         switch (p.bn) {
         case 32: return run_swap<32>(p, tx, tw, ty, M, N, workspace, dev_status, st);
         case 64: return run_swap<64>(p, tx, tw, ty, M, N, workspace, dev_status, st);

@@ -21,14 +21,27 @@ struct GemmPlan {
     bool swap;     // w rows on the MMA M side (M <= 256), x rows padded to bn
     int bn;        // swap: padded rows of x (MMA N); pairs: width of the first tile
     int grid;      // CTAs (pairs: in clusters of 2), all co-resident
-    SkGrid sk;     // swap: stream-K decomposition over single CTAs
+    int split;     // swap: S >= 2 when each tile's k-blocks go to a cluster of S, else 0
+    SkGrid sk;     // swap, split 0: stream-K decomposition over single CTAs
     PairGrid pg;   // pairs: ragged whole tiles
-    size_t workspace_bytes;  // swap: ready flags + fp32 partial slots; pairs: 0
+    size_t workspace_bytes;  // stream-K: ready flags + fp32 partial slots; split, pairs: 0
 };
 
+// Resident clusters of the split-K weight-streaming kernel per cluster size
+// S (index 2..8; 0 where S cannot be used).
+struct SplitCaps {
+    int max_clusters[9];
+};
+
+// The resident clusters on the current device for x padded to bn rows, and
+// an estimate from the SM count alone (host planning without a device).
+SplitCaps split_caps_device(int bn);
+SplitCaps split_caps_estimate(int sms);
+
 // max_units_*: units (single CTAs for the swap orientation, CTA pairs for
-// M > 256) that can be resident at once.
-GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_pair);
+// M > 256) that can be resident at once; caps: where split K is possible
+// (all zero: stream-K only).
+GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_pair, const SplitCaps &caps);
 
 // Resident units of the kernel variant on the current device (0 if the
 // query fails).

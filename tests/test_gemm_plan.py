@@ -2,11 +2,13 @@
 
 The kernels' roles walk the same tile and segment lists; these checks run
 the library's own planner (through spec_verify_gemm_plan) and need no GPU.
-Weight streaming (M <= 256, stream-K): coverage of every (tile, k-block)
-exactly once, balance across CTAs, one owner per tile whose contributor
-range matches the pieces, and the ordering that keeps the owners' waits
-free of cycles.  CTA pairs (M > 256): whole tiles of ragged width that
-cover every output column once and spread evenly over the pairs.
+Weight streaming (M <= 256): with split K over clusters of S (when the
+tiles' clusters all fit), S equal k-ranges per tile in rank order, one CTA
+each; with stream-K, coverage of every (tile, k-block) exactly once,
+balance across CTAs, one owner per tile whose contributor range matches
+the pieces, and the ordering that keeps the owners' waits free of cycles.
+CTA pairs (M > 256): whole tiles of ragged width that cover every output
+column once and spread evenly over the pairs.
 """
 from collections import defaultdict
 
@@ -23,7 +25,13 @@ def built():
     _build.build()
 
 SHAPES = [(8, 6144, 6144), (200, 6144, 6144), (256, 384, 640), (1, 128, 64), (100, 19456, 640),
-          (64, 128, 6144), (256, 256, 4096), (33, 6272, 640), (128, 65536, 64)]
+          (64, 128, 6144), (256, 256, 4096), (33, 6272, 640), (128, 65536, 64), (64, 10240, 6144)]
+
+
+def split_size(M, N, K, sms):
+    """S >= 2 when the plan splits K over clusters of S, else 0."""
+    c = sv.gemm_plan_cluster(M, N, K, sms)
+    return c if M <= 256 and c >= 2 else 0
 PAIR_SHAPES = [(257, 6144, 6144), (384, 128, 6144), (512, 6144, 6144), (1024, 6144, 6144),
                (2048, 6144, 6144), (4096, 6144, 6144), (3000, 6272, 1024), (512, 256, 64),
                (65536, 128, 64), (300, 384, 128), (600, 19584, 512)]
@@ -33,6 +41,8 @@ PAIR_SHAPES = [(257, 6144, 6144), (384, 128, 6144), (512, 6144, 6144), (1024, 61
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_stream_k_split(M, N, K, sms):
     seg = sv.gemm_plan(M, N, K, sms)
+    if split_size(M, N, K, sms):
+        pytest.skip("split K over clusters (test_split_k_clusters)")
     bn = 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
     tiles = N // 128
     max_units, max_contrib = sms, 4 if bn <= 64 else 2
@@ -81,6 +91,50 @@ def test_stream_k_split(M, N, K, sms):
         # an owned cut tile is the CTA's last segment (its stage ring is idle)
         assert all(i == len(rows) - 1 for i in waits)
         assert all(r[4] == -1 for r in rows if r[2] > 0)
+
+
+@pytest.mark.parametrize("sms", [152, 148, 20])
+@pytest.mark.parametrize("M,N,K", SHAPES + [(8, 2304, 1024), (100, 2688, 1024), (256, 2560, 1024),
+                                           (64, 3712, 512), (256, 4608, 6144), (128, 9472, 640)])
+def test_split_k_clusters(M, N, K, sms):
+    """Split K: tile t's k-blocks go to CTAs t S .. t S + S - 1 of a cluster
+    of S, rank r taking [r K/S, (r + 1) K/S); S is the largest size (up to
+    8, at most K/64, the exchanged pieces fitting one stage ring) for which
+    all the tiles' clusters fit at once (num_sms / S of them), and the
+    ranks' ranges cover each tile once in k order."""
+    S = split_size(M, N, K, sms)
+    tiles, kblocks = N // 128, K // 64
+    bn = 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
+    ring_ok = lambda s: s * -(-(bn // 32) // s) * 16384 <= 196608 if bn > 32 else s * 16384 <= 163840
+    feasible = [s for s in range(2, 9) if s <= kblocks and tiles <= sms // s and ring_ok(s)]
+    if M > 256 or not feasible:
+        assert S == 0
+        return
+    assert S == max(feasible)
+    seg = sv.gemm_plan(M, N, K, sms)
+    assert len(seg) == tiles * S
+    assert (seg[:, 0] == np.arange(tiles * S)).all()
+    assert (seg[:, 5] == bn).all()
+    for c, t, k0, k1, last, _ in seg:
+        r = c % S
+        assert t == c // S
+        assert (k0, k1) == (r * kblocks // S, (r + 1) * kblocks // S) and k0 < k1
+        assert last == (c + S - 1 if r == 0 else -1)
+    cover = np.zeros((tiles, kblocks), np.int32)
+    for c, t, k0, k1, *_ in seg:
+        cover[t, k0:k1] += 1
+    assert (cover == 1).all()
+
+
+def test_verify_layer_at_small_m_splits_over_clusters_of_three():
+    """N = K = 6144, M <= 256, 152 SMs: 48 tiles, clusters of 3 (48 of them
+    fit, 38 of 4 do not), 32 k-blocks per CTA, 144 CTAs."""
+    for M in (8, 64, 128, 256):
+        assert sv.gemm_plan_cluster(M, 6144, 6144, 152) == 3
+        seg = sv.gemm_plan(M, 6144, 6144, 152)
+        assert len(seg) == 144 and ((seg[:, 3] - seg[:, 2]) == 32).all()
+    assert sv.gemm_plan_cluster(512, 6144, 6144, 152) == 2     # CTA pairs
+    assert sv.gemm_plan_cluster(64, 19456, 640, 152) == 1      # 152 tiles: stream-K
 
 
 def pair_columns(seg, M):
@@ -138,7 +192,7 @@ def test_verify_layer_at_512_rows_fills_every_pair():
 def test_weight_streaming_cuts_each_tile_in_thirds_at_small_m():
     """M = 8, N = K = 6144: the 48 w tiles of 128 rows are cut into three
     equal k-ranges of 32 k-blocks, one per CTA (144 of the 152 SMs stream
-    weights)."""
+    weights), as clusters of three."""
     seg = sv.gemm_plan(8, 6144, 6144, 152)
     assert int(seg[:, 0].max()) + 1 == 144
     assert (seg[:, 5] == 32).all()
@@ -152,6 +206,8 @@ def test_rejects_bad_arguments():
     assert lib.spec_verify_gemm_plan(512, 128, 60, 152, None, 0) == -1
     assert lib.spec_verify_gemm_plan(512, 128, 64, 0, None, 0) == -1
     assert lib.spec_verify_gemm_plan(512, 128, 64, 152, None, 4) == -1
+    assert lib.spec_verify_gemm_plan_cluster(512, 100, 64, 152) == -1
+    assert lib.spec_verify_gemm_plan_cluster(512, 128, 64, 0) == -1
 
 
 def test_small_m_few_tiles_are_cut():

@@ -121,6 +121,20 @@ def test_verify_shapes_sampled(sv, oracle_lib, M):
     assert float(rel) < REL_L2
 
 
+def test_split_k_status_clear_and_repeatable(sv):
+    """Split K over clusters of 3 (M = 128, N = K = 6144): no status bit, and
+    a second call gives the same bits (the pieces are added in k order)."""
+    import torch
+    x, w = synth.gemm_inputs(23, 128, 6144, 6144)
+    xd, wd = bits_to_dev(x), bits_to_dev(w)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = sv.verify_gemm(xd, wd, dev_status=st).clone()
+    b = sv.verify_gemm(xd, wd, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(a, b)
+
+
 def test_two_calls_in_a_row_agree(sv):
     x, w = synth.gemm_inputs(5, 64, 768, 6144)
     a, _ = run(sv, x, w)
@@ -128,14 +142,28 @@ def test_two_calls_in_a_row_agree(sv):
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("M,N,K", [(200, 128, 6144), (256, 256, 4096), (64, 384, 6144)])
-def test_stream_k_many_pieces(sv, oracle_lib, M, N, K):
-    """Weight streaming with few tiles and long K: tiles are cut into several
-    pieces whose fp32 partials the last-arriving piece adds (checked against
-    the oracle in full)."""
-    x, w = synth.gemm_inputs(7 * M + K, M, N, K)
+@pytest.mark.parametrize("M,N,K", [(200, 128, 6144), (256, 256, 4096), (64, 384, 6144), (8, 2304, 1024),
+                                   (100, 2688, 1024), (256, 2560, 1024), (64, 3712, 512), (31, 4608, 1024),
+                                   (256, 6144, 1024), (128, 9472, 640), (1, 1024, 128)])
+def test_split_k_clusters(sv, oracle_lib, M, N, K):
+    """Weight streaming with each tile's k-blocks split over a cluster
+    (sizes 2 to 8 across these shapes: few tiles and long K take 8, N = 6144
+    takes 3, N = 9472 takes 2), the pieces exchanged through distributed
+    shared memory and added in k order: every output against the oracle."""
+    x, w = synth.gemm_inputs(7 * M + K + N, M, N, K)
     segs = sv.gemm_plan(M, N, K, 152)
-    assert (segs[:, 2] > 0).any()          # the split really cuts tiles
+    assert (segs[:, 2] > 0).any()          # tiles really are cut
+    y, _ = run(sv, x, w)
+    check(y, oracle_lib.gemm(x, w))
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 10240, 6144), (200, 10240, 1024)])
+def test_stream_k_wide_layers(sv, oracle_lib, M, N, K):
+    """More 128-row tiles (80) than clusters of two can hold at once: the
+    stream-K split, whose cut tiles add their fp32 partials through the
+    workspace (checked against the oracle in full)."""
+    assert sv.gemm_plan_cluster(M, N, K, 152) == 1
+    x, w = synth.gemm_inputs(11 * M + K, M, N, K)
     y, _ = run(sv, x, w)
     check(y, oracle_lib.gemm(x, w))
 
