@@ -181,9 +181,10 @@ spec_status_t spec_verify_attention_noalloc(const void *q_bf16, const void *k_pa
  * Supported set: 1 <= M <= 65536, N a multiple of 128, K a multiple of 64.
  * M <= 256 (weight streaming) splits the K range of each 128-row block of
  * w between CTAs.  When every block's CTAs fit on the device at once (a
- * thread-block cluster of S <= 8 per block: N = 6144 takes S = 3), the
- * pieces are added in shared memory across the cluster and the workspace
- * is not touched; otherwise (stream-K) they are added through it.  Either
+ * thread-block cluster per block or, for M > 64, per pair of blocks whose
+ * MMAs CTA pairs share), the pieces are added in shared memory across the
+ * cluster and the workspace is not touched; otherwise (stream-K) they are
+ * added through it.  Either
  * way pass spec_verify_gemm_workspace_size(M, N, K) bytes of device memory,
  * 256-byte aligned, owned by the caller.  It holds the arrival counters of
  * the tiles cut between CTAs (the first 4096 bytes) and the fp32 partial
@@ -482,10 +483,12 @@ int spec_verify_attention_plan(int B, const int32_t *kv_len_host, int D, int Hkv
  *    columns) t * 128 .. t * 128 + 127 for all M rows, which are padded to
  *    BN in {32, 64, 128, 256} on the MMA side.  Each unit walks a list of
  *    segments (a tile and a range [kb0, kb1) of its 64-wide k-blocks).
- *    With split K over clusters of S (the S that
- *    spec_verify_gemm_plan_cluster returns for M <= 256, when >= 2), unit
- *    c = t S + r has the one segment [r K/S, (r + 1) K/S) of tile t, in
- *    k-blocks of 64.
+ *    With split K over clusters (spec_verify_gemm_plan_cluster returns
+ *    their size C >= 2 for M <= 256), each unit has one segment: either
+ *    S = C single CTAs per tile (unit c = t S + r takes [r K/S,
+ *    (r + 1) K/S) of tile t) or, for 64 < M <= 256, S = C / 2 CTA pairs
+ *    per 256-row pair tile T (unit c = T C + 2p + h takes [p K/S,
+ *    (p + 1) K/S) of tile 2T + h), in k-blocks of 64.
  * Writes, for each segment in unit order, the row (unit, tile, kb0, kb1,
  * last, BN) into segments[6 * i ..] (int32, host memory), where last is,
  * for a segment with kb0 == 0, the last unit holding a later piece of the
@@ -499,10 +502,11 @@ int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments,
 
 /* The cluster size of the launch that spec_verify_gemm_plan describes: 2
  * for CTA pairs when M > 256; for M <= 256, 1 for stream-K weight
- * streaming and S in [2, 8] for split K over clusters of S (unit c is CTA
- * c of the grid, rank c % S of its cluster).  Planned for num_sms SMs
- * holding num_sms / S clusters of S (a device may hold fewer and plan
- * otherwise); -1 for invalid arguments.  No device needed. */
+ * streaming and C in [2, 8] for split K over clusters of C CTAs (unit c is
+ * CTA c of the grid, rank c % C of its cluster; the CTAs of a cluster that
+ * hold the same tile split its k-blocks in rank order).  Planned for
+ * num_sms SMs holding num_sms / C clusters of C (a device may hold fewer
+ * and plan otherwise); -1 for invalid arguments.  No device needed. */
 int spec_verify_gemm_plan_cluster(int M, int N, int K, int num_sms);
 
 /* ------------------------------------------------------------------------

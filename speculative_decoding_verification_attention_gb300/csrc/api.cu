@@ -392,6 +392,26 @@ int spec_verify_gemm_plan(int M, int N, int K, int num_sms, int32_t *segments, i
             }
         return n;
     }
+    if (plan.split >= 2 && plan.split_pairs) {
+        // split K over S CTA pairs: CTA c = T 2S + 2p + h takes k-blocks
+        // [p K/S, (p + 1) K/S) of 128-row tile 2T + h; pair 0's rows name
+        // the last CTA holding the same tile (pair S - 1)
+        const int S = plan.split, CS = 2 * S, kblocks = K / 64;
+        for (int c = 0; c < plan.grid; ++c) {
+            if (n < max_segments) {
+                const int T = c / CS, pp = (c % CS) >> 1, h = c & 1;
+                int32_t *row = segments + 6 * static_cast<size_t>(n);
+                row[0] = c;
+                row[1] = 2 * T + h;
+                row[2] = pp * kblocks / S;
+                row[3] = (pp + 1) * kblocks / S;
+                row[4] = pp == 0 ? c + 2 * (S - 1) : -1;
+                row[5] = plan.bn;
+            }
+            ++n;
+        }
+        return n;
+    }
     if (plan.split >= 2) {
         // split K: CTA c = t S + r takes k-blocks [r K/S, (r + 1) K/S) of
         // tile t; rank 0's row names the last CTA of the tile's cluster
@@ -434,7 +454,9 @@ int spec_verify_gemm_plan_cluster(int M, int N, int K, int num_sms)
 {
     if (M <= 0 || N <= 0 || K <= 0 || N % 128 != 0 || K % 64 != 0 || num_sms <= 0) return -1;
     const GemmPlan plan = plan_gemm(M, N, K, num_sms, num_sms / 2, split_caps_estimate(num_sms));
-    return !plan.swap ? 2 : plan.split >= 2 ? plan.split : 1;
+    if (!plan.swap) return 2;
+    if (plan.split < 2) return 1;
+    return plan.split_pairs ? 2 * plan.split : plan.split;
 }
 
 spec_status_t spec_verify_gemm(const void *x_bf16, const void *w_bf16, void *y_bf16, int M, int N,

@@ -21,6 +21,9 @@
 //    tile's k-blocks are split over the S CTAs of a thread-block cluster,
 //    whose fp32 pieces meet in their shared memory and are added in k
 //    order (see the kernel).
+//  * gemm_split_pair_kernel (64 < M <= 256, N a multiple of 256, when its
+//    clusters fit and are not fewer CTAs): the same split with each MMA
+//    shared by a CTA pair, each CTA staging half of the x rows.
 //  * gemm_swap_kernel (M <= 256, otherwise): the same orientation; the
 //    k-block iterations of all tiles are split evenly over the CTAs
 //    (stream-K, see gemm_schedule.h): every piece of a tile cut between
@@ -887,6 +890,229 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) { tc_fence_after(); tmem_dealloc_pair(tmem, kPairTmemCols); }
 }
 
+// ------------------------------------- weight streaming, split K, CTA pairs
+// 64 < M <= 256 with N a multiple of 256: the split above with each MMA
+// shared by a CTA pair (tcgen05 cta_group::2).  A pair tile is 256 w rows
+// (128 per CTA, the MMA's M side) and the pair's MMAs read half of the
+// padded x rows from each CTA (the N side), so an SM takes in half of x per
+// k-block instead of all of it: at M = 256 the x rows of a k-block are
+// twice its w rows, and the single-CTA split streams at the SMs' L2 read
+// rate, not HBM's.  A cluster holds S pairs (2S CTAs); pair p takes
+// k-blocks [p K/S, (p + 1) K/S) of the pair tile and CTA 2p + h holds w
+// rows h * 128 .. + 127 of it.  Both CTAs' copies of a stage complete on
+// the pair's even CTA's barrier, whose MMA thread issues the pair's MMAs
+// and commits to both.  After the cluster barrier the pieces of each
+// 32-column chunk are exchanged among the S CTAs that hold the same w rows
+// (the same h) exactly as in the single-CTA split, and added in k order.
+template <int BN>
+struct SplitPairCfg {
+    static constexpr int kKps = 2;                                      // k-blocks per stage
+    static constexpr int kStages = BN >= 256 ? 3 : 4;
+    static constexpr uint32_t kTileB = (BN / 2) * kBK * 2;             // this CTA's half of the x rows
+    static constexpr uint32_t kStage = kKps * (kTileA + kTileB);
+    static constexpr uint32_t kRing = kStages * kStage;
+    static constexpr uint32_t kBytes = kRing + kOutStaging + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t kChunkBytes = 32 * kBM * 4;
+};
+
+// S pairs per cluster (2S CTAs, at most 8): each CTA receives the pieces of
+// ceil(chunks / S) chunks from S sources in its stage ring.
+template <int BN>
+__host__ __device__ constexpr bool split_pair_fits(int S)
+{
+    return (BN == 128 || BN == 256) && S >= 2 && 2 * S <= 8 &&
+           static_cast<uint32_t>(S * ((BN / 32 + S - 1) / S)) * SplitPairCfg<BN>::kChunkBytes <=
+               SplitPairCfg<BN>::kRing;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_split_pair_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                           const __grid_constant__ CUtensorMap tm_y, int M, int kblocks, uint32_t *dev_status)
+{
+    using C = SplitPairCfg<BN>;
+    constexpr int STAGES = C::kStages, KPS = C::kKps;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *out_stage = smem + C::kRing;   // 4 warps x 2 output blocks
+    uint64_t *full = reinterpret_cast<uint64_t *>(out_stage + kOutStaging);   // (even CTA) stage landed in both
+    uint64_t *empty = full + STAGES;        // the pair's MMAs are done with the stage
+    uint64_t *acc_full = empty + STAGES;
+    uint64_t *recv = acc_full + 1;          // the pieces of this CTA's chunks landed
+    uint64_t *drain = recv + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int CS = static_cast<int>(cluster_ctas());
+    const int S = CS / 2;
+    if ((CS & 1) || !split_pair_fits<BN>(S) || kblocks < S) {   // uniform over the grid
+        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
+        return;
+    }
+    const uint32_t rank = cluster_rank();
+    const int p = static_cast<int>(rank >> 1), h = static_cast<int>(rank & 1u);
+    const int T = static_cast<int>(blockIdx.x) / CS;
+    const int kb0 = p * kblocks / S, kb1 = (p + 1) * kblocks / S;
+    const int nchunks = (M + 31) / 32 < BN / 32 ? (M + 31) / 32 : BN / 32;
+    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * p));
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(acc_full, 1);
+        mbar_init(recv, 1);
+        mbar_init(drain, 1);
+        *abort = 0;
+        // the bytes this CTA will receive: S - 1 pieces of each chunk it owns
+        uint32_t bytes = 0;
+        for (int cc = p; cc < nchunks; cc += S) bytes += static_cast<uint32_t>((S - 1) * live_quads(M, cc)) * kBM * 16;
+        mbar_arrive_expect_tx(recv, bytes);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, BN);
+        tmem_relinquish_pair();
+        tc_fence_before();
+    }
+    cluster_sync_all();   // every CTA's barriers and allocation exist before anything targets them
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // the pair's accumulators must sit at the same tensor-memory address
+    if (ld_cluster_u32(cluster_smem(tmem_slot, rank ^ 1u)) != tmem) {
+        if (threadIdx.x == 0) report(dev_status, SPEC_DEV_ERR_LAUNCH);
+        *abort = 1;
+    }
+    __syncthreads();
+
+    bool ok = true;
+    if (warp == 0 && lane == 0) {
+        // producer: this CTA's 128 w rows and half of the x rows, counted on
+        // the pair's even CTA's full barrier (which expects both CTAs' bytes)
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_y);
+        const uint32_t full_even = cluster_smem(full, rank & ~1u);
+        const uint32_t bytes = kTileA + C::kTileB;
+        uint32_t it = 0;
+        for (int kb = kb0; kb < kb1 && !*abort; kb += KPS, ++it) {
+            const int nk = kb1 - kb < KPS ? kb1 - kb : KPS;
+            const int st = static_cast<int>(it % STAGES);
+            if (it >= static_cast<uint32_t>(STAGES) &&
+                !mbar_wait(&empty[st], ((it / STAGES) & 1) ^ 1, abort, dev_status)) break;
+            uint8_t *sa = smem + st * C::kStage;
+            if (h == 0) mbar_arrive_expect_tx(&full[st], 2 * bytes * static_cast<uint32_t>(nk));
+            for (int q = 0; q < nk; ++q) {
+                tma_load_2d_pair(sa + q * kTileA, &tm_w, full_even + st * 8, (kb + q) * kBK, (2 * T + h) * kBM);
+                tma_load_2d_pair(sa + KPS * kTileA + q * C::kTileB, &tm_x, full_even + st * 8, (kb + q) * kBK,
+                                 h * (BN / 2));
+            }
+        }
+        if (*abort) {
+            // copies in flight complete on the even CTA's full barriers: drain
+            // those (bounded), then give any straggler 0.2 ms to land
+            if (h == 0) drain_copies(full, it, STAGES);
+            const unsigned long long t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 200000ull) {
+            }
+        }
+    } else if (warp == 1 && lane == 0 && h == 0) {
+        // MMA issuer (the pair's even CTA)
+        constexpr uint32_t idesc = idesc_f16(2 * kBM, BN, /*bf16*/ 1, 0, 0);
+        uint32_t it = 0;
+        for (int kb = kb0; kb < kb1; kb += KPS, ++it) {
+            const int nk = kb1 - kb < KPS ? kb1 - kb : KPS;
+            const int st = static_cast<int>(it % STAGES);
+            if (!mbar_wait(&full[st], (it / STAGES) & 1, abort, dev_status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + st * C::kStage);
+            for (int q = 0; q < nk; ++q) {
+                const uint32_t a = sa + q * kTileA, b = sa + KPS * kTileA + q * C::kTileB;
+#pragma unroll
+                for (int k = 0; k < kBK / 16; ++k)
+                    umma_f16_ss_pair(tmem, sdesc(a + k * 32, 16, 1024), sdesc(b + k * 32, 16, 1024), idesc,
+                                     (it > 0 || q > 0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit_pair(&empty[st], pair_mask);
+        }
+        if (ok) umma_commit_pair(acc_full, pair_mask);
+    } else if (warp >= 2) {
+        ok = mbar_wait_warp(acc_full, 0, abort, dev_status);
+        tc_fence_after();
+    }
+    // every pair of the cluster is done with its stage rings (its MMAs have
+    // completed: the epilogue warps arrive after the accumulator is final)
+    __syncwarp();
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    tc_fence_after();
+
+    if (warp >= 2) {
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t tbase = tmem + ((quad * 32) << 16);
+        // send: this CTA's piece of every chunk it does not own to the CTA of
+        // the owning pair that holds the same w rows
+#pragma unroll 1
+        for (int cc = 0; cc < nchunks && ok && !*abort; ++cc) {
+            if (cc % S == p) continue;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + cc * 32, r);
+            tmem_ld_wait();
+            const uint32_t owner = static_cast<uint32_t>(2 * (cc % S) + h);
+            const float *slot =
+                reinterpret_cast<const float *>(smem) + static_cast<size_t>((cc / S) * S + p) * (32 * kBM);
+            const uint32_t dst = peer_smem(slot, owner);
+            const uint32_t bar = peer_smem(recv, owner);
+            const int nq = live_quads(M, cc);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+                if (q4 < nq)
+                    st_async_peer_v4(dst + unit_index(q4, row) * 4, r[4 * q4], r[4 * q4 + 1], r[4 * q4 + 2],
+                                     r[4 * q4 + 3], bar);
+        }
+        // receive: the S pieces of each owned chunk, added in k order
+        if (ok) ok = mbar_wait_warp(recv, 0, abort, dev_status);
+        uint8_t *obuf = out_stage + (warp - 2) * 2 * kOutBlock;
+        uint32_t nst = 0;
+#pragma unroll 1
+        for (int cc = p; cc < nchunks && ok; cc += S) {
+            const int nq = live_quads(M, cc);
+            const float *base = reinterpret_cast<const float *>(smem) + static_cast<size_t>((cc / S) * S) * (32 * kBM);
+            uint32_t own[32];
+            tmem_ld_32x32b_x32(tbase + cc * 32, own);
+            tmem_ld_wait();
+            float a[32];
+            for (int src = 0; src < S; ++src) {
+                const float *u = base + static_cast<size_t>(src) * (32 * kBM);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    float4 v = make_float4(__uint_as_float(own[4 * q4]), __uint_as_float(own[4 * q4 + 1]),
+                                           __uint_as_float(own[4 * q4 + 2]), __uint_as_float(own[4 * q4 + 3]));
+                    if (src != p)
+                        v = q4 < nq ? *reinterpret_cast<const float4 *>(u + unit_index(q4, row))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (src == 0) {
+                        a[4 * q4] = v.x; a[4 * q4 + 1] = v.y; a[4 * q4 + 2] = v.z; a[4 * q4 + 3] = v.w;
+                    } else {
+                        a[4 * q4] += v.x; a[4 * q4 + 1] += v.y; a[4 * q4 + 2] += v.z; a[4 * q4 + 3] += v.w;
+                    }
+                }
+            }
+            store_out_swap(&tm_y, obuf, nst, lane, 2 * T + h, quad, cc, a);
+        }
+        if (lane == 0) bulk_wait_read_all();   // staged output read before the CTA's shared memory goes
+    }
+    __syncwarp();
+    __syncthreads();
+    if (*abort && h == 0 && threadIdx.x == 32) {
+        // let every pair MMA issued so far finish before tensor memory goes
+        umma_commit_pair(drain, static_cast<uint16_t>(1u << rank));
+        mbar_wait_drain(drain, 0, 100000000ull);
+    }
+    cluster_sync_all();   // no CTA exits while another may still send into it, signal or read it
+    if (warp == 1) { tc_fence_after(); tmem_dealloc_pair(tmem, BN); }
+}
+
 template <typename Kern>
 cudaError_t set_smem(Kern k, uint32_t bytes)
 {
@@ -946,6 +1172,9 @@ int max_swap_units()
     return per_sm > 0 ? sms : 0;   // one CTA per SM
 }
 
+template <typename Kern>
+cudaError_t set_smem(Kern k, uint32_t bytes);
+
 template <int BN>
 cudaLaunchConfig_t split_config(int grid, int S, cudaStream_t st, cudaLaunchAttribute (&attr)[1])
 {
@@ -991,6 +1220,56 @@ int max_split_clusters(int S)
     return n;
 }
 
+template <int BN>
+cudaLaunchConfig_t split_pair_config(int grid, int S, cudaStream_t st, cudaLaunchAttribute (&attr)[1])
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SplitPairCfg<BN>::kBytes;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeClusterDimension;   // S CTA pairs sharing a pair tile's k-blocks
+    attr[0].val.clusterDim.x = 2 * S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int BN>
+cudaError_t run_split_pair(const GemmPlan &p, const CUtensorMap &tx, const CUtensorMap &tw, const CUtensorMap &ty,
+                           int M, int K, uint32_t *dev_status, cudaStream_t st)
+{
+    cudaError_t e = set_smem(gemm_split_pair_kernel<BN>, SplitPairCfg<BN>::kBytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = split_pair_config<BN>(p.grid, p.split, st, attr);
+    return cudaLaunchKernelEx(&cfg, gemm_split_pair_kernel<BN>, tx, tw, ty, M, K / kBK, dev_status);
+}
+
+// Clusters of S CTA pairs that can be resident at once (0 if the query
+// fails or S cannot be used).
+template <int BN>
+int max_split_pair_clusters(int S)
+{
+    if (!split_pair_fits<BN>(S)) return 0;
+    if (set_smem(gemm_split_pair_kernel<BN>, SplitPairCfg<BN>::kBytes) != cudaSuccess) return 0;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = split_pair_config<BN>(2 * S, S, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_split_pair_kernel<BN>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+bool split_pair_fits_bn(int bn, int S)
+{
+    return bn == 128 ? split_pair_fits<128>(S) : bn == 256 ? split_pair_fits<256>(S) : false;
+}
+
 bool split_fits_bn(int bn, int S)
 {
     switch (bn) {
@@ -1031,6 +1310,7 @@ SplitCaps split_caps_estimate(int sms)
 {
     SplitCaps c{};
     for (int S = 2; S <= 8; ++S) c.max_clusters[S] = sms / S;
+    for (int S = 2; S <= 4; ++S) c.pair_clusters[S] = sms / (2 * S);
     return c;
 }
 
@@ -1038,6 +1318,7 @@ SplitCaps split_caps_device(int bn)
 {
     // per device and width; the answers never change for a process
     static std::atomic<int> cache[64][4][9];
+    static std::atomic<int> pair_cache[64][4][5];
     SplitCaps c{};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return c;
@@ -1055,6 +1336,15 @@ SplitCaps split_caps_device(int bn)
             slot.store(v > 0 ? v : -1, std::memory_order_relaxed);
         }
         c.max_clusters[S] = v > 0 ? v : 0;
+    }
+    for (int S = 2; S <= 4; ++S) {
+        std::atomic<int> &slot = pair_cache[dev][b][S];
+        int v = slot.load(std::memory_order_relaxed);
+        if (v == 0) {
+            v = bn == 128 ? max_split_pair_clusters<128>(S) : bn == 256 ? max_split_pair_clusters<256>(S) : -1;
+            slot.store(v > 0 ? v : -1, std::memory_order_relaxed);
+        }
+        c.pair_clusters[S] = v > 0 ? v : 0;
     }
     return c;
 }
@@ -1131,14 +1421,29 @@ GemmPlan plan_gemm(int M, int N, int K, int max_units_swap, int max_units_pair, 
     p.swap = true;
     p.bn = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     const int tiles = N / kBM;
-    // Split K over clusters when every tile's S CTAs can be resident at
-    // once: the largest S (up to 8, at most one k-block per CTA less than
-    // K / 64) whose clusters all fit and whose exchanged pieces fit a ring.
-    for (int S = 8; S >= 2; --S) {
-        if (S > kblocks || !split_fits_bn(p.bn, S) || caps.max_clusters[S] < tiles) continue;
-        p.split = S;
-        p.grid = tiles * S;
+    // Split K over clusters when every tile's cluster can be resident at
+    // once: the largest S (at most K / 64) whose clusters all fit and whose
+    // exchanged pieces fit a stage ring; S single CTAs per 128-row tile, or
+    // (M > 64, N a multiple of 256) S CTA pairs per 256-row tile, which
+    // halve the x rows each SM takes in -- preferred unless they would use
+    // fewer CTAs.
+    int S1 = 0, S2 = 0;
+    for (int S = 8; S >= 2 && !S1; --S)
+        if (S <= kblocks && split_fits_bn(p.bn, S) && caps.max_clusters[S] >= tiles) S1 = S;
+    if (M > 64 && N % 256 == 0)
+        for (int S = 4; S >= 2 && !S2; --S)
+            if (S <= kblocks && split_pair_fits_bn(p.bn, S) && caps.pair_clusters[S] >= N / 256) S2 = S;
+    if (S2 && (N / 256) * 2 * S2 >= tiles * S1) {
+        p.split = S2;
+        p.split_pairs = true;
+        p.grid = (N / 256) * 2 * S2;
         p.workspace_bytes = 0;   // the pieces meet in shared memory
+        return p;
+    }
+    if (S1) {
+        p.split = S1;
+        p.grid = tiles * S1;
+        p.workspace_bytes = 0;
         return p;
     }
     p.sk.tiles_m = 1;
@@ -1181,6 +1486,14 @@ cudaError_t launch_gemm(const GemmPlan &p, const void *x, const void *w, void *y
         if (!encode_bf16_tmap(&tx, x, 2, dx, sk, bx) || !encode_bf16_tmap(&tw, w, 2, dw, sk, bw) ||
             !encode_bf16_tmap_plain(&ty, y, 2, dy, sy, by))
             return cudaErrorInvalidValue;
+        if (p.split >= 2 && p.split_pairs) {
+            // the pair's B operand: half of the padded x rows per CTA
+            const uint32_t bxh[2] = {64, static_cast<uint32_t>(p.bn / 2)};
+            CUtensorMap txh;
+            if (!encode_bf16_tmap(&txh, x, 2, dx, sk, bxh)) return cudaErrorInvalidValue;
+            return p.bn == 128 ? run_split_pair<128>(p, txh, tw, ty, M, K, dev_status, st)
+                               : run_split_pair<256>(p, txh, tw, ty, M, K, dev_status, st);
+        }
         if (p.split >= 2) {
             switch (p.bn) {
             case 32: return run_split<32>(p, tx, tw, ty, M, K, dev_status, st);

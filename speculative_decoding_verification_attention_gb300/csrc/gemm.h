@@ -21,16 +21,19 @@ struct GemmPlan {
     bool swap;     // w rows on the MMA M side (M <= 256), x rows padded to bn
     int bn;        // swap: padded rows of x (MMA N); pairs: width of the first tile
     int grid;      // CTAs (pairs: in clusters of 2), all co-resident
-    int split;     // swap: S >= 2 when each tile's k-blocks go to a cluster of S, else 0
+    int split;     // swap: S >= 2 when each tile's k-blocks are split S ways in a cluster, else 0
+    bool split_pairs;  // split: S CTA pairs per cluster over 256-row tiles (else S single CTAs)
     SkGrid sk;     // swap, split 0: stream-K decomposition over single CTAs
     PairGrid pg;   // pairs: ragged whole tiles
     size_t workspace_bytes;  // stream-K: ready flags + fp32 partial slots; split, pairs: 0
 };
 
-// Resident clusters of the split-K weight-streaming kernel per cluster size
-// S (index 2..8; 0 where S cannot be used).
+// Resident clusters of the split-K weight-streaming kernels: of S single
+// CTAs (index S = 2..8) and of S CTA pairs (2S CTAs, index S = 2..4); 0
+// where S cannot be used.
 struct SplitCaps {
     int max_clusters[9];
+    int pair_clusters[5];
 };
 
 // The resident clusters on the current device for x padded to bn rows, and

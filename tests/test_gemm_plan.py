@@ -29,7 +29,7 @@ SHAPES = [(8, 6144, 6144), (200, 6144, 6144), (256, 384, 640), (1, 128, 64), (10
 
 
 def split_size(M, N, K, sms):
-    """S >= 2 when the plan splits K over clusters of S, else 0."""
+    """The cluster size C >= 2 when the plan splits K over clusters, else 0."""
     c = sv.gemm_plan_cluster(M, N, K, sms)
     return c if M <= 256 and c >= 2 else 0
 PAIR_SHAPES = [(257, 6144, 6144), (384, 128, 6144), (512, 6144, 6144), (1024, 6144, 6144),
@@ -95,45 +95,56 @@ def test_stream_k_split(M, N, K, sms):
 
 @pytest.mark.parametrize("sms", [152, 148, 20])
 @pytest.mark.parametrize("M,N,K", SHAPES + [(8, 2304, 1024), (100, 2688, 1024), (256, 2560, 1024),
-                                           (64, 3712, 512), (256, 4608, 6144), (128, 9472, 640)])
+                                           (64, 3712, 512), (256, 4608, 6144), (128, 9472, 640),
+                                           (65, 6144, 6144), (200, 512, 128)])
 def test_split_k_clusters(M, N, K, sms):
-    """Split K: tile t's k-blocks go to CTAs t S .. t S + S - 1 of a cluster
-    of S, rank r taking [r K/S, (r + 1) K/S); S is the largest size (up to
-    8, at most K/64, the exchanged pieces fitting one stage ring) for which
-    all the tiles' clusters fit at once (num_sms / S of them), and the
-    ranks' ranges cover each tile once in k order."""
-    S = split_size(M, N, K, sms)
+    """Split K over clusters of C CTAs: unit c is CTA c of the grid, rank
+    c % C; within a cluster the CTAs that hold the same 128-row tile split
+    its k-blocks into equal contiguous ranges in rank order (S single CTAs
+    per tile, or S CTA pairs per 256-row pair tile, ranks 2p + h holding
+    tile 2T + h); every (tile, k-block) is covered once; the first piece's
+    row names the last CTA holding the same tile; and all clusters fit the
+    estimate of num_sms / C resident clusters."""
+    C = split_size(M, N, K, sms)
+    if not C:
+        return
     tiles, kblocks = N // 128, K // 64
     bn = 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
-    ring_ok = lambda s: s * -(-(bn // 32) // s) * 16384 <= 196608 if bn > 32 else s * 16384 <= 163840
-    feasible = [s for s in range(2, 9) if s <= kblocks and tiles <= sms // s and ring_ok(s)]
-    if M > 256 or not feasible:
-        assert S == 0
-        return
-    assert S == max(feasible)
     seg = sv.gemm_plan(M, N, K, sms)
-    assert len(seg) == tiles * S
-    assert (seg[:, 0] == np.arange(tiles * S)).all()
+    G = len(seg)
+    assert G % C == 0 and G // C <= sms // C
+    assert (seg[:, 0] == np.arange(G)).all()
     assert (seg[:, 5] == bn).all()
-    for c, t, k0, k1, last, _ in seg:
-        r = c % S
-        assert t == c // S
-        assert (k0, k1) == (r * kblocks // S, (r + 1) * kblocks // S) and k0 < k1
-        assert last == (c + S - 1 if r == 0 else -1)
     cover = np.zeros((tiles, kblocks), np.int32)
-    for c, t, k0, k1, *_ in seg:
-        cover[t, k0:k1] += 1
+    for cl in range(G // C):
+        rows = seg[cl * C:(cl + 1) * C]
+        by_tile = defaultdict(list)
+        for c, t, k0, k1, last, _ in rows:
+            by_tile[int(t)].append((int(c), int(k0), int(k1), int(last)))
+        S = len(next(iter(by_tile.values())))
+        assert S >= 2 and all(len(v) == S for v in by_tile.values())
+        assert len(by_tile) * S == C and len(by_tile) in (1, 2)
+        if len(by_tile) == 2:
+            assert M > 64 and N % 256 == 0        # CTA pairs: 256-row pair tiles
+        for t, pieces in by_tile.items():
+            pieces.sort()
+            for i, (c, k0, k1, last) in enumerate(pieces):
+                assert (k0, k1) == (i * kblocks // S, (i + 1) * kblocks // S) and k0 < k1
+                assert last == (pieces[-1][0] if i == 0 else -1)
+                cover[t, k0:k1] += 1
     assert (cover == 1).all()
 
 
-def test_verify_layer_at_small_m_splits_over_clusters_of_three():
-    """N = K = 6144, M <= 256, 152 SMs: 48 tiles, clusters of 3 (48 of them
-    fit, 38 of 4 do not), 32 k-blocks per CTA, 144 CTAs."""
-    for M in (8, 64, 128, 256):
-        assert sv.gemm_plan_cluster(M, 6144, 6144, 152) == 3
+def test_verify_layer_at_small_m_splits_over_clusters():
+    """N = K = 6144, M <= 256, planned for 152 SMs (estimate: 152 / C
+    clusters of C): 48 tiles of 128 w rows; M <= 64 in clusters of three
+    single CTAs, 64 < M in clusters of three CTA pairs (the pair's MMAs
+    share the x rows); 32 k-blocks per CTA, 144 CTAs either way."""
+    for M, C in ((8, 3), (64, 3), (65, 6), (128, 6), (256, 6)):
+        assert sv.gemm_plan_cluster(M, 6144, 6144, 152) == C
         seg = sv.gemm_plan(M, 6144, 6144, 152)
         assert len(seg) == 144 and ((seg[:, 3] - seg[:, 2]) == 32).all()
-    assert sv.gemm_plan_cluster(512, 6144, 6144, 152) == 2     # CTA pairs
+    assert sv.gemm_plan_cluster(512, 6144, 6144, 152) == 2     # CTA pairs, whole tiles
     assert sv.gemm_plan_cluster(64, 19456, 640, 152) == 1      # 152 tiles: stream-K
 
 

@@ -157,6 +157,17 @@ def test_split_k_clusters(sv, oracle_lib, M, N, K):
     check(y, oracle_lib.gemm(x, w))
 
 
+@pytest.mark.parametrize("M,N,K", [(100, 8192, 256), (129, 6144, 1024), (256, 6656, 512), (65, 6144, 640)])
+def test_split_k_cta_pairs(sv, oracle_lib, M, N, K):
+    """64 < M <= 256 with N a multiple of 256 and many tiles: split K over
+    clusters of CTA pairs whose MMAs (M = 256 w rows) each read half of the
+    padded x rows from each CTA of the pair; the pieces of the two k-halves
+    added in shared memory.  Every output against the oracle."""
+    x, w = synth.gemm_inputs(13 * M + K + N, M, N, K)
+    y, _ = run(sv, x, w)
+    check(y, oracle_lib.gemm(x, w))
+
+
 @pytest.mark.parametrize("M,N,K", [(64, 10240, 6144), (200, 10240, 1024)])
 def test_stream_k_wide_layers(sv, oracle_lib, M, N, K):
     """More 128-row tiles (80) than clusters of two can hold at once: the
