@@ -25,6 +25,9 @@ TIERS = (1, 3, 7)
 ATT_MAX_ABS, ATT_REL_L2 = 2e-2, 1e-3
 GEMM_REL_L2 = 5e-3
 MARGIN = 1e-6
+# boundary disagreements of the stochastic acceptance over the module
+# (checked against 1e-4 of the draws by the last test)
+TALLY = {"draws": 0, "disagree": 0}
 
 
 @pytest.fixture(scope="module")
@@ -108,6 +111,8 @@ def check_against_oracle(tier, ref):
     assert np.array_equal(ng, ref["ng"]) and np.array_equal(tg, ref["tg"])
     bad = (ns != ref["ns"]) | (ts != ref["ts"])
     assert not (bad & (ref["margin"] >= MARGIN)).any(), np.nonzero(bad)
+    TALLY["draws"] += bad.size
+    TALLY["disagree"] += int(bad.sum())
     assert int(tier.status.item()) == 0
 
 
@@ -139,3 +144,10 @@ def test_graph_tiers_match_the_oracle(sv, oracle_lib):
         # walks it across the tiers
         ctl.update(np.full(4, [0, D, 1, D // 2, 0, 0, D, D, 0][r], np.int32))
     assert len(set(seen)) >= 2, seen
+
+
+def test_zz_boundary_disagreements_stay_below_the_cap():
+    """Over every comparison of this module: at most 1e-4 of the sequences
+    disagree with the oracle (only where a uniform lies within 1e-6 of a
+    test or CDF step)."""
+    assert TALLY["disagree"] <= 1e-4 * max(TALLY["draws"], 1), TALLY
