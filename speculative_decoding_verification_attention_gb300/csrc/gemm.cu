@@ -674,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_out_swap(&tm_y, obuf, nst, lane, t, quad, cc, a);
         }
         if (lane == 0) bulk_wait_read_all();   // staged output read before the CTA's shared memory goes
+        tc_fence_before();                     // the tensor-memory reads, before the deallocation
     }
     // no CTA leaves while a peer may still send into it
     __syncwarp();
@@ -1101,6 +1102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_out_swap(&tm_y, obuf, nst, lane, 2 * T + h, quad, cc, a);
         }
         if (lane == 0) bulk_wait_read_all();   // staged output read before the CTA's shared memory goes
+        tc_fence_before();                     // the tensor-memory reads, before the deallocation
     }
     __syncwarp();
     __syncthreads();
